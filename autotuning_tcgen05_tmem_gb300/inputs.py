@@ -1,0 +1,97 @@
+"""Seeded synthetic inputs shaped like the workloads the pages discuss.
+
+This module holds no arithmetic of the method: it only draws random operands.
+Both sides of every parity check (the CUDA path and the CPU oracle) take their
+inputs from here, so that they see bit-identical values.
+
+Recipe (per workload; seeds 0, 1, 2 for A, B and bias unless a caller passes
+another base seed): draw in fp32 with torch's CPU generator (or a CUDA
+generator for timing-only buffers), then round once, to bf16 with torch's
+round-to-nearest-even conversion when the workload is bf16.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+BF16, FP32 = "bf16", "fp32"
+EPI_CODES = {"none": 0, "bias": 1, "relu": 2, "gelu": 3}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    dtype: str
+    epi: str
+    dist: str          # "uniform", "int", "scaled_normal", "decode"
+
+
+# hidden 4096, FFN 14336: QKV (GQA, 4096 -> 6144), out, up, fused gate+up, down, KV
+PROJECTIONS = [("qkv", 4096, 6144), ("out", 4096, 4096), ("up", 4096, 14336),
+               ("gate_up", 4096, 28672), ("down", 14336, 4096), ("kv", 4096, 1024)]
+TOKENS = (16, 128, 512, 2048, 8192)
+
+WORKLOADS = {
+    "fp32_relu_256": Workload("fp32_relu_256", 256, 256, 256, FP32, "relu", "uniform"),
+    "fp32_relu_256_int": Workload("fp32_relu_256_int", 256, 256, 256, FP32, "relu", "int"),
+    "bf16_gelu_1000x1000x8192": Workload("bf16_gelu_1000x1000x8192", 1000, 1000, 8192, BF16,
+                                         "gelu", "scaled_normal"),
+    "bf16_relu_8192": Workload("bf16_relu_8192", 8192, 8192, 8192, BF16, "relu", "scaled_normal"),
+    "bf16_decode_16x8192x28672": Workload("bf16_decode_16x8192x28672", 16, 28672, 8192, BF16,
+                                          "none", "decode"),
+}
+for _t in TOKENS:
+    for _p, _k, _n in PROJECTIONS:
+        _name = f"bf16_gelu_{_p}_t{_t}"
+        WORKLOADS[_name] = Workload(_name, _t, _n, _k, BF16, "gelu", "scaled_normal")
+
+SWEEP = [WORKLOADS[f"bf16_gelu_{p}_t{t}"] for t in TOKENS for (p, _k, _n) in PROJECTIONS]
+
+
+def torch_dtype(dtype: str):
+    return torch.bfloat16 if dtype == BF16 else torch.float32
+
+
+def _gen(seed: int, device):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def make_operands(M: int, N: int, K: int, dtype: str, dist: str, seed: int = 0,
+                  device="cpu", with_bias: bool = True):
+    """Return (A [M,K], B [K,N], bias [N] or None) in the workload dtype."""
+    dev = torch.device(device)
+    gA, gB, gb = _gen(seed, dev), _gen(seed + 1, dev), _gen(seed + 2, dev)
+    f32 = torch.float32
+    if dist == "uniform":
+        A = torch.rand(M, K, generator=gA, device=dev, dtype=f32) * 2 - 1
+        B = torch.rand(K, N, generator=gB, device=dev, dtype=f32) * 2 - 1
+        bias = torch.rand(N, generator=gb, device=dev, dtype=f32) * 2 - 1
+    elif dist == "int":
+        A = torch.randint(-2, 3, (M, K), generator=gA, device=dev).to(f32)
+        B = torch.randint(-2, 3, (K, N), generator=gB, device=dev).to(f32)
+        bias = torch.randint(-2, 3, (N,), generator=gb, device=dev).to(f32)
+    elif dist == "scaled_normal":
+        s = 1.0 / math.sqrt(max(K, 1))
+        A = torch.randn(M, K, generator=gA, device=dev, dtype=f32) * s
+        B = torch.randn(K, N, generator=gB, device=dev, dtype=f32) * s
+        bias = torch.randn(N, generator=gb, device=dev, dtype=f32) * 0.1
+    elif dist == "decode":
+        A = torch.randn(M, K, generator=gA, device=dev, dtype=f32)
+        B = torch.randn(K, N, generator=gB, device=dev, dtype=f32) * 0.02
+        bias = torch.randn(N, generator=gb, device=dev, dtype=f32) * 0.1
+    else:
+        raise ValueError(f"unknown distribution {dist!r}")
+    td = torch_dtype(dtype)
+    return A.to(td).contiguous(), B.to(td).contiguous(), (bias.to(td).contiguous() if with_bias else None)
+
+
+def make_workload(w: Workload, seed: int = 0, device="cpu"):
+    return make_operands(w.M, w.N, w.K, w.dtype, w.dist, seed=seed, device=device,
+                         with_bias=(w.epi != "none"))

@@ -1,0 +1,177 @@
+"""numpy front end of the fp64 GEMM oracle (gemm_ref.c).
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and the
+CPU-baseline leg of bench.py.  The product package never imports it.
+
+Citations (page title, section):
+  * "Tile Selection: Cost Models Against Measurement", "The structure of the
+    search space": C = AB, C is M x N, reduction depth K.
+  * "Tiling the hierarchy", fusion section: bias + activation is an elementwise
+    epilogue of the product.
+Readings where the pages are silent: bias is a length-N vector added to every
+row; GELU is the erf form 0.5·x·(1 + erf(x/√2)).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemm_ref.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle_gemm.so")
+
+EPI_NONE, EPI_BIAS, EPI_BIAS_RELU, EPI_BIAS_GELU = 0, 1, 2, 3
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile gemm_ref.c with gcc into oracle/_build/liboracle_gemm.so."""
+    if not force and os.path.exists(_LIB_PATH) and \
+            os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-D_GNU_SOURCE",
+           "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        f32p = ctypes.POINTER(ctypes.c_float)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        lib.oracle_gemm.argtypes = [f32p, f32p, f32p, ctypes.c_int, ctypes.c_int64,
+                                    ctypes.c_int64, ctypes.c_int64, f64p, ctypes.c_int]
+        lib.oracle_gemm.restype = ctypes.c_int
+        lib.oracle_gemm_entries.argtypes = [f32p, f32p, f32p, ctypes.c_int, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_int64, i64p, i64p,
+                                            ctypes.c_int64, f64p]
+        lib.oracle_gemm_entries.restype = ctypes.c_int
+        lib.oracle_round_bf16.argtypes = [f64p, ctypes.c_int64,
+                                          ctypes.POINTER(ctypes.c_uint16)]
+        lib.oracle_round_bf16.restype = None
+        _lib = lib
+    return _lib
+
+
+def _f32(x):
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def _as_f32_input(x):
+    """Inputs may arrive as float32 arrays or torch tensors of bf16/fp32 (CPU)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return x.detach().to("cpu", torch.float32).contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x, dtype=np.float32)
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def gemm(A, B, bias=None, epi: int = EPI_NONE, threads: int | None = None) -> np.ndarray:
+    """fp64 C = act(A·B + bias) for A [M,K], B [K,N], bias [N] (or None)."""
+    lib = _load()
+    A = _as_f32_input(A)
+    B = _as_f32_input(B)
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {A.shape} x {B.shape}")
+    a, ap = _f32(A)
+    b, bp = _f32(B)
+    if bias is not None:
+        bb, biasp = _f32(_as_f32_input(bias).reshape(-1))
+        if bb.shape[0] != N:
+            raise ValueError("bias must have N entries")
+    else:
+        bb, biasp = None, ctypes.POINTER(ctypes.c_float)()
+    C = np.empty((M, N), dtype=np.float64)
+    rc = lib.oracle_gemm(ap, bp, biasp, int(epi), M, N, K,
+                         C.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                         int(threads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle_gemm rejected its arguments")
+    return C
+
+
+def gemm_entries(A, B, bias, epi: int, rows, cols) -> np.ndarray:
+    """fp64 values of C at the listed (row, col) positions, one dot product each."""
+    lib = _load()
+    A = _as_f32_input(A)
+    B = _as_f32_input(B)
+    M, K = A.shape
+    N = B.shape[1]
+    a, ap = _f32(A)
+    b, bp = _f32(B)
+    if bias is not None:
+        bb, biasp = _f32(_as_f32_input(bias).reshape(-1))
+    else:
+        bb, biasp = None, ctypes.POINTER(ctypes.c_float)()
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    c = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    out = np.empty(r.shape[0], dtype=np.float64)
+    rc = lib.oracle_gemm_entries(ap, bp, biasp, int(epi), M, N, K,
+                                 r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                 c.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                 r.shape[0], out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    if rc != 0:
+        raise ValueError("oracle_gemm_entries rejected its arguments")
+    return out
+
+
+def round_bf16_bits(x) -> np.ndarray:
+    """Round-to-nearest-even of fp64 values to bf16; returns the uint16 patterns."""
+    lib = _load()
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib.oracle_round_bf16(x.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), x.size,
+                          out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)))
+    return out
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Exact value of bf16 bit patterns (the pattern is the top half of a float)."""
+    u = np.asarray(bits, dtype=np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def round_f32(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64).astype(np.float32)
+
+
+def normalised_error(C_dev, C_ref, A, B) -> float:
+    """max |C_dev - C_ref| / (||a_i||_2 · ||b_j||_2) over all (i, j).
+
+    The error scale of entry (i, j) is the product of the norms of row i of A
+    and column j of B (Cauchy–Schwarz bound of the dot product)."""
+    A = _as_f32_input(A).astype(np.float64)
+    B = _as_f32_input(B).astype(np.float64)
+    ra = np.sqrt((A * A).sum(axis=1))
+    cb = np.sqrt((B * B).sum(axis=0))
+    scale = np.outer(ra, cb)
+    scale[scale == 0] = 1.0
+    d = np.abs(np.asarray(C_dev, dtype=np.float64) - np.asarray(C_ref, dtype=np.float64))
+    return float((d / scale).max()) if d.size else 0.0
+
+
+if __name__ == "__main__":  # pragma: no cover
+    print(build(force="--force" in sys.argv))

@@ -1,0 +1,553 @@
+"""Oracle for the selection layer: candidate spaces, wave arithmetic, cost models,
+schedule order and rank agreement — plain Python, one function per idea.
+
+TEST INFRASTRUCTURE ONLY: imported by tests/ (and nothing in the product).
+
+Sources (page title, section / equation):
+  * "Tile Selection: Cost Models Against Measurement"
+      - "The structure of the search space": the candidate enumerator, the
+        48 KB shared-memory cap of 12,288 fp32 panel elements.
+      - "Analytical models and where they break": per-block traffic
+        4K(BM+BN) bytes, 2·BM·BN·K operations, intensity BM·BN/(2(BM+BN)).
+  * "Compilers and Kernel Languages" (workshop paragraph and "A different tile
+    for every shape"): waves of one tile per multiprocessor, the H100 workshop
+    model and its printed results.
+  * "Tiling the hierarchy", square-tile derivation: traffic 2N³/T with
+    T = √(C/3); the double-buffering discussion (stages hide latency).
+  * "Autotuning & cost models", §6: cost-model-guided search vs measurement;
+    rank agreement is how the model's ordering is judged against measurement.
+
+Parity status of each function is stated in its docstring.  The GB300 rules
+(`gb300_*`) restate the library's documented feasibility rules, enumeration and
+cost model independently of the library source; the pages say nothing about
+TMEM or tcgen05, so those functions are "parity unpinned" against the pages
+(they are pinned only by brute-force/invariant checks and, for the cost model,
+by its reduction to the workshop model).
+"""
+from __future__ import annotations
+
+import itertools
+import math
+from dataclasses import dataclass, field
+
+# ---------------------------------------------------------------------------
+# "Tile Selection", "The structure of the search space": the fp32 SIMT enumerator
+# ---------------------------------------------------------------------------
+
+P1_BLOCK = (32, 64, 128, 256)
+P1_KSTEP = (8, 16, 32, 64)
+P1_THREAD = (2, 4, 8)
+
+
+def p1_candidates(M, N, K, smem_bytes=48 * 1024, max_threads=1024):
+    """All (BM, BN, KS, TM, TN) the page's enumerator accepts, in its loop order.
+
+    Rules (page: "The structure of the search space"): both fp32 panels fit in
+    shared memory, 4·(BM·KS + KS·BN) <= smem; the block has between 32 and
+    max_threads threads, (BM/TM)·(BN/TN); whole warps; TM·TN <= 128 accumulators.
+    The problem extents do not enter the rules (the page's listing ignores them).
+    Pinned by: the 12,288-element cap the page prints for 48 KB, the "few hundred
+    to a few thousand" count it states, and brute-force rule checks in tests."""
+    del M, N, K
+    out = []
+    for bm, bn, ks, tm, tn in itertools.product(P1_BLOCK, P1_BLOCK, P1_KSTEP,
+                                                P1_THREAD, P1_THREAD):
+        panel_bytes = 4 * ks * (bm + bn)
+        nthreads = (bm // tm) * (bn // tn)
+        ok = (panel_bytes <= smem_bytes
+              and 32 <= nthreads <= max_threads
+              and nthreads % 32 == 0
+              and tm * tn <= 128)
+        if ok:
+            out.append((bm, bn, ks, tm, tn))
+    return out
+
+
+def p1_panel_cap_elements(smem_bytes=48 * 1024):
+    """Largest BM·KS + KS·BN that fits as fp32: smem / 4 (12,288 at 48 KB)."""
+    return smem_bytes // 4
+
+
+# ---------------------------------------------------------------------------
+# Wave arithmetic ("Compilers and Kernel Languages": tiles run in waves of one
+# per multiprocessor; 133 tiles on 132 take two waves)
+# ---------------------------------------------------------------------------
+
+def ceil_div(a, b):
+    return -(-a // b)
+
+
+def tile_count(M, N, bm, bn):
+    return ceil_div(M, bm) * ceil_div(N, bn)
+
+
+def waves(units, sms):
+    return ceil_div(units, sms)
+
+
+def wave_efficiency(units, sms):
+    """Fraction of multiprocessor-slots busy over the waves the units need."""
+    return units / (waves(units, sms) * sms)
+
+
+# ---------------------------------------------------------------------------
+# "Tile Selection", "Analytical models and where they break"
+# ---------------------------------------------------------------------------
+
+def block_traffic_bytes(bm, bn, K, elt=4):
+    """Bytes one block moves over the full depth: K·(BM+BN)·elt (4K(BM+BN) for fp32)."""
+    return K * (bm + bn) * elt
+
+
+def block_ops(bm, bn, K):
+    return 2 * bm * bn * K
+
+
+def block_intensity(bm, bn, K, elt=4):
+    """Operations per byte of one block; for fp32 it equals BM·BN/(2(BM+BN))."""
+    return block_ops(bm, bn, K) / block_traffic_bytes(bm, bn, K, elt)
+
+
+def roofline_time(M, N, K, bm, bn, peak_flops, bw, elt=4):
+    """The page's simplest model: max(ops/peak, grid traffic/bandwidth) with no
+    panel sharing between blocks."""
+    grid_bytes = tile_count(M, N, bm, bn) * block_traffic_bytes(bm, bn, K, elt)
+    return max(2 * M * N * K / peak_flops, grid_bytes / bw)
+
+
+# ---------------------------------------------------------------------------
+# "Tiling the hierarchy": square tiles at one level of capacity C (elements)
+# ---------------------------------------------------------------------------
+
+def square_tile_side(capacity_elems):
+    """Three resident T×T tiles: 3T² <= C, so T = √(C/3)."""
+    return math.sqrt(capacity_elems / 3.0)
+
+
+def square_tile_traffic_law(Nn, T):
+    """Closed form 2N³/T (elements read)."""
+    return 2 * Nn ** 3 / T
+
+
+def square_tile_traffic_count(Nn, T):
+    """Explicit count: walk the (N/T)³ tile triples, each reading one A tile and
+    one B tile of T² elements."""
+    assert Nn % T == 0
+    nt = Nn // T
+    total = 0
+    for _i in range(nt):
+        for _j in range(nt):
+            for _k in range(nt):
+                total += T * T  # A[i,k]
+                total += T * T  # B[k,j]
+    return total
+
+
+def double_buffer_load_ns(tile_bytes, bw_bytes_per_s, capacity_factor=1.0):
+    """Bandwidth time of one tile load; halving reuse capacity multiplies traffic
+    by √2 ("Tiling the hierarchy", double-buffering discussion)."""
+    return tile_bytes / bw_bytes_per_s * 1e9 * capacity_factor
+
+
+# ---------------------------------------------------------------------------
+# "Compilers and Kernel Languages": the H100 workshop model
+# ---------------------------------------------------------------------------
+
+@dataclass
+class WorkshopDevice:
+    sms: int = 132
+    smem_bytes: int = 228 * 1024
+    peak_flops: float = 989e12
+    bw: float = 3.35e12
+    elt: int = 2          # BF16 operands
+    bk: int = 64
+
+
+WORKSHOP_TILES = (32, 64, 128, 256)
+
+
+def workshop_tile_efficiency(bm, bn):
+    """Reading: the page says only that tile efficiency "falls for tiles smaller
+    than 128 × 128"; the simplest law that reproduces both printed ratios
+    (1.83× and 1.50×) is 0.5 + 0.5·min(1, bm·bn/128²)."""
+    return 0.5 + 0.5 * min(1.0, bm * bn / (128 * 128))
+
+
+def workshop_time(M, N, K, bm, bn, dev: WorkshopDevice = WorkshopDevice()):
+    """Modelled time (seconds) of one bm × bn tile shape.
+
+    compute = 2MNK / peak / wave efficiency / tile efficiency;
+    memory  = max(panel traffic / g + C bytes, compulsory bytes) / bandwidth, where
+              g = √(tiles sharing panels in one wave) = √min(tiles, SMs);
+    time    = max(compute, memory).
+    Pinned by the page's printed results (tests/golden/workshop_h100.json)."""
+    t = tile_count(M, N, bm, bn)
+    compute = 2.0 * M * N * K / dev.peak_flops / wave_efficiency(t, dev.sms) \
+        / workshop_tile_efficiency(bm, bn)
+    g = math.sqrt(min(t, dev.sms))
+    panel = t * K * (bm + bn) * dev.elt / g + M * N * dev.elt
+    floor = (M * K + K * N + M * N) * dev.elt
+    memory = max(panel, floor) / dev.bw
+    return max(compute, memory)
+
+
+def workshop_sweep(M, N, K, dev: WorkshopDevice = WorkshopDevice()):
+    """Every (bm, bn) with its time; best = first minimum in bm-outer, bn-inner
+    order (reading: the page's tie-break between equal times)."""
+    times = {}
+    for bm in WORKSHOP_TILES:
+        for bn in WORKSHOP_TILES:
+            times[(bm, bn)] = workshop_time(M, N, K, bm, bn, dev)
+    best = None
+    for key, val in times.items():
+        if best is None or val < times[best]:
+            best = key
+    worst = max(times, key=lambda k: times[k])
+    return {"times": times, "best": best, "worst": worst,
+            "best_s": times[best], "worst_s": times[worst],
+            "fixed_128": times[(128, 128)]}
+
+
+# ---------------------------------------------------------------------------
+# GB300 restatement of the library's documented rules (parity unpinned against
+# the pages, which say nothing about TMEM/tcgen05; pinned by brute force).
+# ---------------------------------------------------------------------------
+
+DT_BF16, DT_FP32 = 0, 1
+EPI_NONE, EPI_BIAS, EPI_RELU, EPI_GELU = 0, 1, 2, 3
+
+R_OK, R_CTA_GROUP, R_UMMA_M, R_UMMA_N, R_LAYOUT, R_BK, R_STAGES, R_SCHEDULE, \
+    R_SPLIT_K, R_ALIGN, R_TMEM, R_SMEM, R_REGS = range(13)
+
+THREADS_PER_CTA = 192
+TMEM_COLUMNS = 512
+AUX_SMEM = 2048            # barriers/flags (1 KB) + 1 KB alignment slack
+MAX_STAGES = 16
+SPLITS = (2, 3, 4, 6, 8, 12, 16)
+GROUPS = (1, 2, 4, 8, 16)
+
+
+@dataclass
+class Config:
+    bm: int
+    bn: int
+    bk: int
+    stages: int
+    raster: int = 0
+    group: int = 1
+    split_k: int = 1
+    cta_group: int = 1
+    swap_ab: int = 0
+
+    def astuple(self):
+        return (self.bm, self.bn, self.bk, self.stages, self.raster, self.group,
+                self.split_k, self.cta_group, self.swap_ab)
+
+
+@dataclass
+class Device:
+    """Mirror of the library's device-parameter record, field by field."""
+    sm_count: int = 152
+    model_kind: int = 0
+    smem_per_block: int = 232448
+    l2_bytes: int = 126 * 1024 * 1024
+    peak_tflops_bf16: float = 1889.6
+    peak_tflops_tf32: float = 944.8
+    hbm_gbs: float = 6675.8
+    sm_clock_mhz: float = 1920.0
+    mma_flops_per_clk_bf16: float = 8192.0
+    mma_flops_per_clk_tf32: float = 4096.0
+    smem_bytes_per_clk: float = 128.0
+    mem_latency_us: float = 0.8
+    epi_elems_per_clk: float = 64.0
+    launch_us: float = 4.0
+    kernel_regs: int = 0
+    threads_per_cta: int = THREADS_PER_CTA
+    extra: dict = field(default_factory=dict)
+
+
+def elt_bytes(dtype):
+    return 2 if dtype == DT_BF16 else 4
+
+
+def span_elems(dtype):
+    """Elements of one 128-byte swizzle span along the contiguous dimension."""
+    return 128 // elt_bytes(dtype)
+
+
+def staging_bytes(dtype, swap_ab):
+    """Epilogue staging: 4 epilogue warps × 2 buffers × one store chunk
+    (32 rows × 32 columns, or 16 token rows × 32 columns when swapped)."""
+    rows = 16 if swap_ab else 32
+    return 4 * 2 * rows * 32 * elt_bytes(dtype)
+
+
+def stage_bytes(cfg: Config, dtype):
+    return (cfg.bm + cfg.bn) * cfg.bk * elt_bytes(dtype)
+
+
+def smem_bytes(cfg: Config, dtype):
+    return cfg.stages * stage_bytes(cfg, dtype) + staging_bytes(dtype, cfg.swap_ab) + AUX_SMEM
+
+
+def max_stages(bm, bn, bk, dtype, swap_ab, smem_per_block):
+    per = (bm + bn) * bk * elt_bytes(dtype)
+    room = smem_per_block - staging_bytes(dtype, swap_ab) - AUX_SMEM
+    return max(0, min(MAX_STAGES, room // per))
+
+
+def tmem_columns(cfg: Config):
+    """Columns of one accumulator (fp32, one column per output column per 128
+    rows) and how many accumulators fit (2 = epilogue overlaps the next tile)."""
+    acc = (cfg.bm // 128) * cfg.bn
+    nbuf = 2 if 2 * acc <= TMEM_COLUMNS else 1
+    return acc, nbuf
+
+
+def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
+    """First violated rule, in the documented order, or R_OK."""
+    elt = elt_bytes(dtype)
+    span = span_elems(dtype)
+    if cfg.cta_group != 1:
+        return R_CTA_GROUP
+    if cfg.bm not in (128, 256):
+        return R_UMMA_M
+    if cfg.bn % 16 != 0 or not (16 <= cfg.bn <= 256):
+        return R_UMMA_N
+    if cfg.swap_ab not in (0, 1):
+        return R_LAYOUT
+    if cfg.swap_ab == 0 and (cfg.bn % span != 0 or cfg.bn % 32 != 0):
+        return R_LAYOUT
+    if cfg.bk % span != 0 or not (1 <= cfg.bk // span <= 4):
+        return R_BK
+    if not (2 <= cfg.stages <= MAX_STAGES):
+        return R_STAGES
+    if cfg.raster not in (0, 1) or cfg.group not in GROUPS:
+        return R_SCHEDULE
+    num_kb = ceil_div(K, cfg.bk)
+    if cfg.split_k < 1 or cfg.split_k > 16 or cfg.split_k > max(1, num_kb):
+        return R_SPLIT_K
+    if (K * elt) % 16 != 0 or (N * elt) % 16 != 0:
+        return R_ALIGN
+    acc, _nbuf = tmem_columns(cfg)
+    if acc > TMEM_COLUMNS:
+        return R_TMEM
+    if smem_bytes(cfg, dtype) > dev.smem_per_block:
+        return R_SMEM
+    if dev.kernel_regs > 0 and dev.kernel_regs * dev.threads_per_cta > 65536:
+        return R_REGS
+    return R_OK
+
+
+def gb300_candidates(M, N, K, dtype, epi, dev: Device):
+    """The documented GB300 candidate generator (nested in this order): swap_ab,
+    bm, bn, bk, stages, then the schedule/split combinations; infeasible
+    combinations are dropped."""
+    span = span_elems(dtype)
+    out = []
+    swaps = (0, 1) if M <= 256 else (0,)
+    for swap in swaps:
+        rows, cols = (N, M) if swap else (M, N)
+        for bm in (128, 256):
+            if swap:
+                bns = (16, 32, 64, 128, 256)
+            elif dtype == DT_BF16:
+                bns = (64, 128, 192, 256)
+            else:
+                bns = (32, 64, 128, 192, 256)
+            for bn in bns:
+                for bk in (span, 2 * span):
+                    st_max = max_stages(bm, bn, bk, dtype, swap, dev.smem_per_block)
+                    if st_max < 2:
+                        continue
+                    stage_list = sorted({min(4, st_max), st_max})
+                    tiles = ceil_div(rows, bm) * ceil_div(cols, bn)
+                    num_kb = ceil_div(K, bk)
+                    splits = []
+                    if tiles < 4 * dev.sm_count:
+                        splits = [s for s in SPLITS
+                                  if 2 * s <= num_kb and tiles * s <= 16 * dev.sm_count]
+                    scheds = [(0, 1)]
+                    if tiles > dev.sm_count:
+                        scheds = [(r, g) for r in (0, 1) for g in (1, 4, 8, 16)]
+                    combos = [(r, g, 1) for (r, g) in scheds] + [(0, 1, s) for s in splits]
+                    for st in stage_list:
+                        for (r, g, s) in combos:
+                            cfg = Config(bm, bn, bk, st, r, g, s, 1, swap)
+                            if gb300_check(M, N, K, dtype, epi, cfg, dev) == R_OK:
+                                out.append(cfg)
+    return out
+
+
+def gb300_fixed_config(dtype, dev: Device):
+    """The untuned default: 128 × 128 tiles, one span of K, as many stages as fit,
+    row-major tile order, no split, no swap."""
+    span = span_elems(dtype)
+    st = max_stages(128, 128, span, dtype, 0, dev.smem_per_block)
+    return Config(128, 128, span, st, 0, 1, 1, 1, 0)
+
+
+# ---------------------------------------------------------------------------
+# Persistent tile schedule (grouped raster), restated
+# ---------------------------------------------------------------------------
+
+def schedule_unit(u, tiles_m, tiles_n, split_k, raster, group, num_kb):
+    """Work unit u -> (tile_m, tile_n, split, kb_begin, kb_end).
+
+    Units are tile-major (the split index varies fastest).  raster 0 walks a band
+    of `group` tile-rows column by column; raster 1 walks a band of `group`
+    tile-columns row by row ("Compilers and Kernel Languages": the order in which
+    tiles are scheduled is one of the choices a real kernel adds)."""
+    tile, s = divmod(u, split_k)
+    if raster == 0:
+        per_band = group * tiles_n
+        band, r = divmod(tile, per_band)
+        first = band * group
+        height = min(group, tiles_m - first)
+        tm, tn = first + r % height, r // height
+    else:
+        per_band = group * tiles_m
+        band, r = divmod(tile, per_band)
+        first = band * group
+        width = min(group, tiles_n - first)
+        tn, tm = first + r % width, r // width
+    return tm, tn, s, (s * num_kb) // split_k, ((s + 1) * num_kb) // split_k
+
+
+# ---------------------------------------------------------------------------
+# GB300 cost model, restated from its documented terms (parity unpinned against
+# the pages; with model_kind = 1 it is the workshop model above)
+# ---------------------------------------------------------------------------
+
+def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
+    """Predicted time and its terms (a dict, times in microseconds)."""
+    if dev.model_kind == 1:
+        wd = WorkshopDevice(sms=dev.sm_count, peak_flops=dev.peak_tflops_bf16 * 1e12,
+                            bw=dev.hbm_gbs * 1e9, elt=elt_bytes(dtype))
+        t = tile_count(M, N, cfg.bm, cfg.bn)
+        return {"predicted_us": workshop_time(M, N, K, cfg.bm, cfg.bn, wd) * 1e6,
+                "tiles": t, "units": t, "waves": waves(t, dev.sm_count),
+                "wave_eff": wave_efficiency(t, dev.sm_count),
+                "tile_eff": workshop_tile_efficiency(cfg.bm, cfg.bn)}
+    elt = elt_bytes(dtype)
+    rows, cols = (N, M) if cfg.swap_ab else (M, N)
+    tiles_m, tiles_n = ceil_div(rows, cfg.bm), ceil_div(cols, cfg.bn)
+    tiles = tiles_m * tiles_n
+    S = cfg.split_k
+    num_kb = ceil_div(K, cfg.bk)
+    units = tiles * S
+    sms = dev.sm_count
+    ctas = min(units, sms)
+    nw = waves(units, sms)
+    weff = units / (nw * sms)
+    flops = 2.0 * M * N * K
+    peak = (dev.peak_tflops_bf16 if dtype == DT_BF16 else dev.peak_tflops_tf32) * 1e12
+    fpc = dev.mma_flops_per_clk_bf16 if dtype == DT_BF16 else dev.mma_flops_per_clk_tf32
+    kslice = 32 // elt
+    mma_clk = 2.0 * 128 * cfg.bn * kslice / fpc
+    smem_clk = (128 + cfg.bn) * 32 / dev.smem_bytes_per_clk
+    teff = mma_clk / max(mma_clk, smem_clk)
+    if K > 0:
+        peff = (rows * cols * K) / (tiles_m * cfg.bm * tiles_n * cfg.bn * num_kb * cfg.bk)
+    else:
+        peff = 1.0
+    compute_s = flops / (peak * weff * teff * peff) if flops > 0 else 0.0
+
+    in_bytes = (M * K + K * N) * elt
+    wave_tiles = min(tiles, max(1, ctas // S))
+    if cfg.raster == 0:
+        rows_w = min(cfg.group, tiles_m, wave_tiles)
+        cols_w = min(ceil_div(wave_tiles, rows_w), tiles_n)
+    else:
+        cols_w = min(cfg.group, tiles_n, wave_tiles)
+        rows_w = min(ceil_div(wave_tiles, cols_w), tiles_m)
+    wave_bytes = K * (rows_w * cfg.bm + cols_w * cfg.bn) * elt
+    panel = (tiles / wave_tiles) * wave_bytes
+    if in_bytes <= dev.l2_bytes / 2:
+        operand = in_bytes
+    else:
+        operand = max(in_bytes, panel)
+    epi_bytes = M * N * elt + (N * elt if epi != EPI_NONE else 0)
+    split_bytes = units * cfg.bm * cfg.bn * 4 if S > 1 else 0
+    hbm = operand + epi_bytes + split_bytes
+    memory_s = hbm / (dev.hbm_gbs * 1e9)
+
+    per_cta_units = ceil_div(units, ctas) if ctas > 0 else 0
+    per_cta_kb = per_cta_units * ceil_div(num_kb, S)
+    latency_s = per_cta_kb * dev.mem_latency_us * 1e-6 / cfg.stages
+    epi_unit_s = cfg.bm * cfg.bn / (dev.epi_elems_per_clk * dev.sm_clock_mhz * 1e6)
+    epilogue_s = per_cta_units * epi_unit_s
+    body = max(compute_s, memory_s, latency_s, epilogue_s)
+    fill_s = dev.mem_latency_us * 1e-6 + epi_unit_s
+    total = body + fill_s + dev.launch_us * 1e-6
+    return {"predicted_us": total * 1e6, "compute_us": compute_s * 1e6,
+            "memory_us": memory_s * 1e6, "latency_us": latency_s * 1e6,
+            "epilogue_us": epilogue_s * 1e6, "fill_us": fill_s * 1e6,
+            "wave_eff": weff, "tile_eff": teff, "pad_eff": peff,
+            "tiles": tiles, "units": units, "waves": nw, "ctas": ctas,
+            "hbm_bytes": hbm, "flops": flops}
+
+
+# ---------------------------------------------------------------------------
+# Rank agreement between predicted and measured times
+# ---------------------------------------------------------------------------
+
+def average_ranks(values):
+    """1-based ranks, ties sharing the mean of their positions."""
+    order = sorted(range(len(values)), key=lambda i: values[i])
+    ranks = [0.0] * len(values)
+    i = 0
+    while i < len(order):
+        j = i
+        while j + 1 < len(order) and values[order[j + 1]] == values[order[i]]:
+            j += 1
+        avg = (i + j) / 2.0 + 1.0
+        for t in range(i, j + 1):
+            ranks[order[t]] = avg
+        i = j + 1
+    return ranks
+
+
+def kendall_tau_b(x, y):
+    """τ_b = (concordant − discordant) / √((n0 − ties_x)(n0 − ties_y)), by
+    looking at every pair."""
+    n = len(x)
+    conc = disc = tx = ty = 0
+    for i in range(n):
+        for j in range(i + 1, n):
+            dx = (x[i] > x[j]) - (x[i] < x[j])
+            dy = (y[i] > y[j]) - (y[i] < y[j])
+            if dx == 0 and dy == 0:
+                continue
+            if dx == 0:
+                tx += 1
+            elif dy == 0:
+                ty += 1
+            elif dx == dy:
+                conc += 1
+            else:
+                disc += 1
+    denom = math.sqrt((conc + disc + tx) * (conc + disc + ty))
+    return (conc - disc) / denom if denom > 0 else float("nan")
+
+
+def spearman_rho(x, y):
+    """Pearson correlation of the average ranks."""
+    rx, ry = average_ranks(x), average_ranks(y)
+    n = len(x)
+    mx, my = sum(rx) / n, sum(ry) / n
+    sxy = sum((a - mx) * (b - my) for a, b in zip(rx, ry))
+    sxx = sum((a - mx) ** 2 for a in rx)
+    syy = sum((b - my) ** 2 for b in ry)
+    return sxy / math.sqrt(sxx * syy) if sxx > 0 and syy > 0 else float("nan")
+
+
+def rank_agreement(predicted, measured):
+    """τ_b, ρ, whether the model's first choice is the measured fastest, and the
+    regret of following the model (its pick's measured time / best − 1)."""
+    pick = min(range(len(predicted)), key=lambda i: predicted[i])
+    best = min(range(len(measured)), key=lambda i: measured[i])
+    return {"kendall_tau": kendall_tau_b(predicted, measured),
+            "spearman_rho": spearman_rho(predicted, measured),
+            "top1_hit": int(measured[pick] == measured[best]),
+            "regret": measured[pick] / measured[best] - 1.0}
