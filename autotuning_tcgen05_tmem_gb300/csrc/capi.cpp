@@ -1,0 +1,225 @@
+// extern "C" boundary of the library (declared in include/gemm_gb300.h).
+// Argument checking and marshalling only; the work is in planner.cpp,
+// runtime.cpp and gemm_kernel.cu.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <string>
+#include <vector>
+
+#include "gemm_internal.h"
+#include "schedule.h"
+
+namespace gemmgb {
+
+static thread_local std::string t_last_error;
+
+int set_error(int code, const char *fmt, ...)
+{
+    char buf[1024];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
+void clear_error() { t_last_error.clear(); }
+
+// runtime.cpp
+extern std::atomic<int64_t> g_timeout_ns;
+extern std::atomic<int32_t> g_debug_stall;
+int query_params(gemm_device_params *d);
+int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out);
+int plan_explicit(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &cfg, gemm_plan_t *out);
+int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream);
+int run_host(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream);
+int plan_status(gemm_plan_t p);
+int plan_config(gemm_plan_t p, gemm_config *out);
+void destroy_plan(gemm_plan_t p);
+int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int topk, std::vector<gemm_tune_row> &rows,
+         gemm_rank_stats &stats, gemm_config *winner);
+void cache_stats(int64_t *tunes, int64_t *hits, int64_t *entries);
+void cache_clear();
+
+}  // namespace gemmgb
+
+using namespace gemmgb;
+
+struct gemm_plan_s;  // defined in runtime.cpp
+extern "C" {
+
+const char *gemm_version(void) { return GEMM_LIB_VERSION; }
+
+const char *gemm_last_error(void) { return t_last_error.c_str(); }
+
+void gemm_device_params_default(gemm_device_params *out)
+{
+    if (out) params_default(out);
+}
+
+void gemm_device_params_workshop(gemm_device_params *out)
+{
+    if (out) params_workshop(out);
+}
+
+static bool enums_ok(int dt, int epi)
+{
+    return (dt == GEMM_BF16 || dt == GEMM_FP32_TF32) && epi >= GEMM_EPI_NONE && epi <= GEMM_EPI_BIAS_GELU;
+}
+
+int gemm_check_config(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, const gemm_config *cfg,
+                      const gemm_device_params *dev)
+{
+    clear_error();
+    if (!cfg || !dev || !enums_ok(dtype, epi) || M < 0 || N < 0 || K < 0)
+        return set_error(GEMM_ERR_INVALID_ARG, "gemm_check_config: bad argument");
+    return check_config(M, N, K, dtype, epi, *cfg, *dev);
+}
+
+int gemm_enumerate(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
+                   const gemm_device_params *dev, gemm_config *out, int32_t cap, int32_t *n)
+{
+    clear_error();
+    if (!dev || !n || !enums_ok(dtype, epi) || M < 0 || N < 0 || K < 0 || cap < 0 || (cap > 0 && !out))
+        return set_error(GEMM_ERR_INVALID_ARG, "gemm_enumerate: bad argument");
+    const std::vector<gemm_config> v = enumerate(M, N, K, dtype, epi, *dev);
+    *n = (int32_t)v.size();
+    for (int32_t i = 0; i < cap && i < (int32_t)v.size(); ++i) out[i] = v[i];
+    return GEMM_OK;
+}
+
+int gemm_fixed_config(gemm_dtype dtype, const gemm_device_params *dev, gemm_config *out)
+{
+    clear_error();
+    if (!dev || !out || !enums_ok(dtype, 0)) return set_error(GEMM_ERR_INVALID_ARG, "gemm_fixed_config: bad argument");
+    *out = fixed_config(dtype, *dev);
+    return GEMM_OK;
+}
+
+int gemm_model_predict(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, const gemm_config *cfg,
+                       const gemm_device_params *dev, gemm_model_terms *out)
+{
+    clear_error();
+    if (!cfg || !dev || !out || !enums_ok(dtype, epi) || M < 0 || N < 0 || K < 0 || cfg->bm <= 0 || cfg->bn <= 0 ||
+        cfg->bk <= 0 || cfg->stages <= 0 || cfg->split_k <= 0 || cfg->group <= 0 || dev->sm_count <= 0)
+        return set_error(GEMM_ERR_INVALID_ARG, "gemm_model_predict: bad argument");
+    *out = predict(M, N, K, dtype, epi, *cfg, *dev);
+    return GEMM_OK;
+}
+
+int gemm_rank_agreement(const double *predicted, const double *measured, int32_t n, gemm_rank_stats *out)
+{
+    clear_error();
+    if (!predicted || !measured || !out || n < 2) return set_error(GEMM_ERR_INVALID_ARG, "gemm_rank_agreement: bad argument");
+    *out = rank_agreement(predicted, measured, n);
+    return GEMM_OK;
+}
+
+int gemm_schedule_unit(int64_t unit, int32_t tiles_m, int32_t tiles_n, int32_t split_k, int32_t raster, int32_t group,
+                       int32_t num_kb, int32_t *tile_m, int32_t *tile_n, int32_t *split, int32_t *kb_begin,
+                       int32_t *kb_end)
+{
+    clear_error();
+    if (tiles_m <= 0 || tiles_n <= 0 || split_k <= 0 || group <= 0 || num_kb < 0 || (raster != 0 && raster != 1) ||
+        unit < 0 || unit >= (int64_t)tiles_m * tiles_n * split_k)
+        return set_error(GEMM_ERR_INVALID_ARG, "gemm_schedule_unit: bad argument");
+    const SchedUnit u = schedule_unit(unit, tiles_m, tiles_n, split_k, raster, group, num_kb);
+    if (tile_m) *tile_m = u.tile_m;
+    if (tile_n) *tile_n = u.tile_n;
+    if (split) *split = u.split;
+    if (kb_begin) *kb_begin = u.kb_begin;
+    if (kb_end) *kb_end = u.kb_end;
+    return GEMM_OK;
+}
+
+int gemm_device_params_query(gemm_device_params *out)
+{
+    clear_error();
+    if (!out) return set_error(GEMM_ERR_INVALID_ARG, "null output");
+    return query_params(out);
+}
+
+int gemm_plan(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, gemm_plan_t *out)
+{
+    clear_error();
+    if (!out) return set_error(GEMM_ERR_INVALID_ARG, "null output");
+    return plan_tuned(M, N, K, dtype, epi, out);
+}
+
+int gemm_plan_with_config(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
+                          const gemm_config *cfg, gemm_plan_t *out)
+{
+    clear_error();
+    if (!out || !cfg) return set_error(GEMM_ERR_INVALID_ARG, "null argument");
+    return plan_explicit(M, N, K, dtype, epi, *cfg, out);
+}
+
+int gemm_plan_config(gemm_plan_t plan, gemm_config *out)
+{
+    clear_error();
+    return plan_config(plan, out);
+}
+
+int gemm_run(gemm_plan_t plan, const void *A, const void *B, const void *bias, void *C, gemm_stream_t stream)
+{
+    return run_plan(plan, A, B, bias, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gemm_run_host(gemm_plan_t plan, const void *A, const void *B, const void *bias, void *C, gemm_stream_t stream)
+{
+    clear_error();
+    return run_host(plan, A, B, bias, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gemm_plan_status(gemm_plan_t plan)
+{
+    clear_error();
+    return plan_status(plan);
+}
+
+void gemm_plan_destroy(gemm_plan_t plan) { destroy_plan(plan); }
+
+int gemm_tune(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, int32_t topk, gemm_tune_row *rows,
+              int32_t cap, int32_t *n_rows, gemm_rank_stats *stats)
+{
+    clear_error();
+    if (!n_rows || cap < 0 || (cap > 0 && !rows)) return set_error(GEMM_ERR_INVALID_ARG, "gemm_tune: bad argument");
+    std::vector<gemm_tune_row> v;
+    gemm_rank_stats s;
+    const int rc = tune(M, N, K, dtype, epi, topk, v, s, nullptr);
+    if (rc) return rc;
+    int32_t k = 0;
+    for (; k < cap && k < (int32_t)v.size(); ++k) rows[k] = v[k];
+    *n_rows = k;
+    if (stats) *stats = s;
+    return GEMM_OK;
+}
+
+int gemm_cache_stats(int64_t *tunes, int64_t *hits, int64_t *entries)
+{
+    cache_stats(tunes, hits, entries);
+    return GEMM_OK;
+}
+
+void gemm_cache_clear(void) { cache_clear(); }
+
+int gemm_debug_set(int32_t what, int64_t value)
+{
+    clear_error();
+    if (what == 0) {
+        if (value <= 0) return set_error(GEMM_ERR_INVALID_ARG, "wait limit must be positive");
+        g_timeout_ns.store(value);
+        return GEMM_OK;
+    }
+    if (what == 1) {
+        g_debug_stall.store(value ? 1 : 0);
+        return GEMM_OK;
+    }
+    return set_error(GEMM_ERR_INVALID_ARG, "unknown debug control %d", what);
+}
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+// Internal declarations shared by the host-side translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/gemm_gb300.h"
+#include "kernel_params.h"
+
+#define GEMM_LIB_VERSION "gb300-tcgen05-gemm 0.1.0"
+
+namespace gemmgb {
+
+constexpr int kThreadsPerCta = 192;
+constexpr int kTmemColumns = 512;
+constexpr int kAuxSmem = 2048;     // barriers and flags (1 KB) + 1 KB of base-alignment slack
+constexpr int kMaxStages = 16;
+constexpr int kMaxSplitK = 16;
+
+inline int elt_bytes(int dt) { return dt == GEMM_BF16 ? 2 : 4; }
+inline int span_elems(int dt) { return 128 / elt_bytes(dt); }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Shared-memory and TMEM layout of one configuration.
+struct Layout {
+    uint32_t a_stage_bytes, b_stage_bytes, stage_bytes;
+    uint32_t staging_buf_bytes, staging_total;
+    uint32_t off_b, off_staging, off_bar;
+    uint32_t smem_total;              // bytes the kernel needs, slack included
+    uint32_t acc_cols, n_acc, tmem_cols;
+};
+Layout layout_of(const gemm_config &c, int dt);
+int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block);
+
+// Host logic (planner.cpp)
+void params_default(gemm_device_params *d);
+void params_workshop(gemm_device_params *d);
+int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &c,
+                 const gemm_device_params &d);
+std::vector<gemm_config> enumerate(int64_t M, int64_t N, int64_t K, int dt, int epi,
+                                   const gemm_device_params &d);
+gemm_config fixed_config(int dt, const gemm_device_params &d);
+gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &c,
+                         const gemm_device_params &d);
+gemm_rank_stats rank_agreement(const double *pred, const double *meas, int n);
+const char *reason_text(int reason);
+
+// Errors (capi.cpp)
+int set_error(int code, const char *fmt, ...);
+void clear_error();
+
+// Kernel launch (gemm_kernel.cu)
+cudaError_t kernel_attributes(int dt, int *num_regs, int *max_threads);
+cudaError_t set_kernel_smem_limit(int dt, int bytes);
+cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
+                        const KernelParams &p, int grid, int smem_bytes, cudaStream_t stream);
+cudaError_t launch_fill_uniform(void *dst, int64_t n, int dt, float scale, uint32_t seed,
+                                cudaStream_t stream);
+
+}  // namespace gemmgb

@@ -1,0 +1,854 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a:  C = act(A·B + bias).
+//
+// What the pages fix and how this kernel realises it on GB300:
+//   * "Tile Selection: Cost Models Against Measurement", "The structure of the
+//     search space": one output tile [BM, BN] per work unit; the reduction runs
+//     in steps of BK, each step staging a [BM, BK] panel of A and a [BK, BN]
+//     panel of B in shared memory.  Here the per-thread tile of the page is
+//     replaced by a tensor-memory (TMEM) accumulator written by tcgen05.mma.
+//   * "Tiling the hierarchy", double buffering: loads overlap compute only when
+//     they are asynchronous; a deeper ring absorbs latency.  Here TMA
+//     (cp.async.bulk.tensor) fills an S-stage ring guarded by mbarriers, and the
+//     accumulator itself is double-buffered in TMEM so the epilogue of one tile
+//     overlaps the main loop of the next.
+//   * "Tiling the hierarchy", fusion: the elementwise epilogue (bias, ReLU,
+//     GELU) is fused onto the GEMM: TMEM -> registers -> shared staging -> TMA
+//     store, so C is written once, coalesced.
+//   * "Compilers and Kernel Languages": pipeline depth, split-K and tile order
+//     are runtime choices of this kernel (stages, split_k, raster/group).
+//
+// Roles (192 threads): warp 0 lane 0 issues TMA loads; warp 1 owns TMEM and its
+// lane 0 issues tcgen05.mma; warps 2..5 (128 threads) drain the accumulator,
+// each reading the 32 TMEM lanes of its sub-partition (warp % 4).
+//
+// Every mbarrier wait is bounded: after the limit the waiting role writes a
+// code to the status word, raises a CTA-wide abort flag and returns; the other
+// roles see the flag, the CTA waits (bounded) for its own copies and MMAs in
+// flight, frees TMEM and exits.  Nothing traps.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernel_params.h"
+#include "schedule.h"
+
+namespace gemmgb {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Inline-PTX primitives
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                            int32_t x, int32_t y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src, int32_t x,
+                                             int32_t y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v)
+{
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// OR of `pred` over the `count` threads that meet at named barrier `id`.
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// --- tcgen05 -----------------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// D[tmem] (+)= A[smem] · B[smem]; kind::f16 reads bf16, kind::tf32 reads fp32 as tf32.
+template <int DT>
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                     uint32_t accumulate)
+{
+    if constexpr (DT == 0) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
+// byte offset (MN-major: distance between 128-byte-wide column blocks; unused
+// for K-major), stride byte offset 1024 (distance between 8-row groups), the
+// descriptor-version bit of the sm_100 family, swizzle mode 2 (128 B).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo)
+{
+    uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+#define GEMM_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
+                   "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+#define GEMM_P8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), \
+                   "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
+
+// 32 lanes x 32 columns of fp32 from TMEM; each thread gets its lane's row.
+__device__ __forceinline__ void tmem_ld_32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+        "%30, %31}, [%32];"
+        : GEMM_R8(0), GEMM_R8(8), GEMM_R8(16), GEMM_R8(24)
+        : "r"(taddr));
+    // The wait names the registers so no use of them is scheduled above it.
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : GEMM_P8(0), GEMM_P8(8), GEMM_P8(16), GEMM_P8(24)::"memory");
+}
+
+__device__ __forceinline__ void tmem_ld_16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15}, [%16];"
+        : GEMM_R8(0), GEMM_R8(8)
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : GEMM_P8(0), GEMM_P8(8)::"memory");
+}
+
+template <int CH>
+__device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[CH])
+{
+    if constexpr (CH == 32) {
+        uint32_t r[32];
+        tmem_ld_32(taddr, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    } else {
+        uint32_t r[16];
+        tmem_ld_16(taddr, r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Bounded waits
+// ---------------------------------------------------------------------------
+
+struct WaitCtl {
+    volatile int32_t *abort;
+    int32_t *status;
+    int64_t timeout_ns;
+};
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtl &c, int32_t site,
+                                       bool heed_abort, int64_t limit_ns)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (heed_abort && *c.abort) return false;
+            if ((int64_t)(global_timer_ns() - t0) > limit_ns) {
+                *c.abort = 1;
+                atomicCAS(c.status, 0, site);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl &c, int32_t site)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, c, site, true, c.timeout_ns);
+}
+
+// Teardown waits (copies / MMAs already issued): one second, abort flag ignored.
+__device__ __forceinline__ bool wait_teardown(uint32_t bar, uint32_t parity, const WaitCtl &c)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, c, SITE_TEARDOWN, false, 1000000000LL);
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue helpers
+// ---------------------------------------------------------------------------
+
+template <int DT>
+struct Elt;
+template <>
+struct Elt<0> {
+    static constexpr int BYTES = 2;
+};
+template <>
+struct Elt<1> {
+    static constexpr int BYTES = 4;
+};
+
+__device__ __forceinline__ float apply_act(float x, int epi)
+{
+    if (epi == 2) return fmaxf(x, 0.0f);
+    if (epi == 3) return 0.5f * x * (1.0f + erff(x * 0.70710678118654752440f));
+    return x;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16)
+{
+    return __uint_as_float(bits16 << 16);
+}
+
+// Bias of 32 consecutive output columns starting at n (same for every lane).
+template <int DT>
+__device__ __forceinline__ void load_bias32(const void *bias, int n, int cols, float (&b)[32])
+{
+    if constexpr (DT == 0) {
+        const uint16_t *bp = reinterpret_cast<const uint16_t *>(bias) + n;
+        if (n + 32 <= cols) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 q = __ldg(reinterpret_cast<const uint4 *>(bp) + i);
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    b[8 * i + 2 * t] = bf16_bits_to_float(w[t] & 0xFFFFu);
+                    b[8 * i + 2 * t + 1] = bf16_bits_to_float(w[t] >> 16);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) b[j] = (n + j < cols) ? bf16_bits_to_float(__ldg(bp + j)) : 0.0f;
+        }
+    } else {
+        const float *bp = reinterpret_cast<const float *>(bias) + n;
+        if (n + 32 <= cols) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 q = __ldg(reinterpret_cast<const float4 *>(bp) + i);
+                b[4 * i] = q.x;
+                b[4 * i + 1] = q.y;
+                b[4 * i + 2] = q.z;
+                b[4 * i + 3] = q.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) b[j] = (n + j < cols) ? __ldg(bp + j) : 0.0f;
+        }
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ float load_bias1(const void *bias, int n, int limit)
+{
+    if (n >= limit) return 0.0f;
+    if constexpr (DT == 0) return bf16_bits_to_float(__ldg(reinterpret_cast<const uint16_t *>(bias) + n));
+    else return __ldg(reinterpret_cast<const float *>(bias) + n);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Per-warp store state: two staging buffers used alternately.
+struct StoreRing {
+    uint32_t buf0;      // shared address of this warp's first staging buffer
+    uint32_t buf_bytes;
+    uint32_t count;     // chunks issued so far
+};
+
+// Unswapped store: the warp's 32 rows (one per lane) x 32 columns -> staging
+// (swizzled like the tensor map) -> one TMA store of a 32x32 box at (x, y).
+template <int DT>
+__device__ __forceinline__ void store_rows_chunk(const CUtensorMap *tmC, StoreRing &ring, const float (&v)[32],
+                                                 int lane, int x, int y, bool in_bounds)
+{
+    const uint32_t buf = ring.buf0 + (ring.count & 1u) * ring.buf_bytes;
+    if (lane == 0) bulk_wait_read_1();
+    __syncwarp();
+    if constexpr (DT == 0) {
+        // 64-byte rows, 64-byte swizzle: 16-byte chunk i of row r lands at i ^ ((r >> 1) & 3)
+        const uint32_t row = buf + (uint32_t)lane * 64u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t phys = (uint32_t)(i ^ ((lane >> 1) & 3)) * 16u;
+            st_shared_v4(row + phys, pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                         pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+        }
+    } else {
+        // 128-byte rows, 128-byte swizzle: chunk i of row r lands at i ^ (r & 7)
+        const uint32_t row = buf + (uint32_t)lane * 128u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t phys = (uint32_t)(i ^ (lane & 7)) * 16u;
+            st_shared_v4(row + phys, __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                         __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+        }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && in_bounds) {
+        tma_store_2d(tmC, buf, x, y);
+        bulk_commit();
+    }
+    ring.count++;
+}
+
+// Swapped store: lane = output column n, 16 values = 16 output rows m.
+// Staging is [16 rows][32 columns] (no swizzle); one TMA store of a 32x16 box.
+template <int DT>
+__device__ __forceinline__ void store_cols_chunk(const CUtensorMap *tmC, StoreRing &ring, const float (&v)[16],
+                                                 int lane, int x, int y, bool in_bounds)
+{
+    const uint32_t buf = ring.buf0 + (ring.count & 1u) * ring.buf_bytes;
+    if (lane == 0) bulk_wait_read_1();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if constexpr (DT == 0) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
+            st_shared_u16(buf + (uint32_t)(j * 64 + lane * 2), *reinterpret_cast<const uint16_t *>(&h));
+        } else {
+            st_shared_u32(buf + (uint32_t)(j * 128 + lane * 4), __float_as_uint(v[j]));
+        }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && in_bounds) {
+        tma_store_2d(tmC, buf, x, y);
+        bulk_commit();
+    }
+    ring.count++;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+
+template <int DT>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const KernelParams p)
+{
+    constexpr int ELT = Elt<DT>::BYTES;
+    constexpr int SPAN = 128 / ELT;                  // elements in one 128-byte swizzle span
+    constexpr uint32_t MN_KSTEP = (32u / ELT) * 128u; // bytes per MMA K-step in an MN-major tile
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const uint32_t bars = base + p.off_bar;
+    const uint32_t full0 = bars;
+    const uint32_t empty0 = bars + 8u * (uint32_t)p.stages;
+    const uint32_t tfull0 = bars + 16u * (uint32_t)p.stages;
+    const uint32_t tempty0 = tfull0 + 16u;
+    const uint32_t teardown_bar = tfull0 + 32u;
+    const uint32_t never_bar = tfull0 + 40u;
+    const uint32_t tmem_slot = tfull0 + 48u;
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(gbase + (tmem_slot - base) + 4);
+    volatile int32_t *last_flag = reinterpret_cast<volatile int32_t *>(gbase + (tmem_slot - base) + 8);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tfull0 + 8u * i, 1);
+            mbar_init(tempty0 + 8u * i, 128);
+        }
+        mbar_init(teardown_bar, 1);
+        mbar_init(never_bar, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(gbase + (tmem_slot - base));
+
+    WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------
+        // TMA producer
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            if (p.num_kb > 0) {
+                prefetch_tmap(&tmA);
+                prefetch_tmap(&tmB);
+            }
+            uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
+                const int32_t ra = w.tile_m * p.bm;
+                const int32_t rb = w.tile_n * p.bn;
+                for (int32_t kb = w.kb_begin; kb < w.kb_end; ++kb) {
+                    if (!wait_bar(empty0 + 8u * stage, phase ^ 1u, ctl, SITE_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full0 + 8u * stage;
+                    mbar_arrive_expect_tx(fb, p.tx_bytes);
+                    const uint32_t sa = base + stage * p.a_stage_bytes;
+                    const uint32_t sb = base + p.off_b + stage * p.b_stage_bytes;
+                    const int32_t k0 = kb * p.bk;
+                    if (!p.a_mn_major) {
+                        for (int32_t sp = 0; sp < p.bk / SPAN; ++sp)
+                            tma_load_2d(sa + (uint32_t)(sp * p.bm * 128), &tmA, fb, k0 + sp * SPAN, ra);
+                    } else {
+                        for (int32_t j = 0; j < p.bm / SPAN; ++j)
+                            tma_load_2d(sa + (uint32_t)(j * p.bk * 128), &tmA, fb, ra + j * SPAN, k0);
+                    }
+                    if (!p.b_mn_major) {
+                        for (int32_t sp = 0; sp < p.bk / SPAN; ++sp)
+                            tma_load_2d(sb + (uint32_t)(sp * p.bn * 128), &tmB, fb, k0 + sp * SPAN, rb);
+                    } else {
+                        for (int32_t j = 0; j < p.bn / SPAN; ++j)
+                            tma_load_2d(sb + (uint32_t)(j * p.bk * 128), &tmB, fb, rb + j * SPAN, k0);
+                    }
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == (uint32_t)p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Every armed stage's last copy must land before the CTA may exit.
+            for (int s = 0; s < p.stages; ++s)
+                if ((armed >> s) & 1u) wait_teardown(full0 + 8u * s, (armed_parity >> s) & 1u, ctl);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------
+        // MMA issuer
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool issued = false, ok = true;
+            const int32_t ksteps = p.bk * ELT / 32;
+            const int32_t halves = p.bm / 128;
+            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
+                const int32_t nk = w.kb_end - w.kb_begin;
+                if (!wait_bar(tempty0 + 8u * acc, acc_phase ^ 1u, ctl, SITE_MMA_TMEM_EMPTY)) break;
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + acc * p.acc_cols;
+                for (int32_t kb = 0; kb < nk; ++kb) {
+                    if (!wait_bar(full0 + 8u * stage, phase, ctl, SITE_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + stage * p.a_stage_bytes;
+                    const uint32_t sb = base + p.off_b + stage * p.b_stage_bytes;
+                    for (int32_t kk = 0; kk < ksteps; ++kk) {
+                        const uint32_t b_off = p.b_mn_major
+                                                   ? (uint32_t)kk * MN_KSTEP
+                                                   : (uint32_t)((kk >> 2) * p.bn * 128 + (kk & 3) * 32);
+                        const uint64_t bdesc = smem_desc(sb + b_off, p.b_lbo);
+                        for (int32_t h = 0; h < halves; ++h) {
+                            const uint32_t a_off =
+                                p.a_mn_major ? (uint32_t)kk * MN_KSTEP + (uint32_t)(h * (128 / SPAN) * p.bk * 128)
+                                             : (uint32_t)((kk >> 2) * p.bm * 128 + h * 128 * 128 + (kk & 3) * 32);
+                            umma<DT>(d0 + (uint32_t)(h * p.bn), smem_desc(sa + a_off, p.a_lbo), bdesc, p.idesc,
+                                     (kb | kk) != 0 ? 1u : 0u);
+                        }
+                    }
+                    umma_commit(empty0 + 8u * stage);  // slot is free once these MMAs have read it
+                    issued = true;
+                    if (++stage == (uint32_t)p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (nk > 0) umma_commit(tfull0 + 8u * acc);
+                else mbar_arrive(tfull0 + 8u * acc);
+                if (++acc == p.n_acc) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (issued) {
+                umma_commit(teardown_bar);
+                wait_teardown(teardown_bar, 0, ctl);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------
+        // Epilogue: TMEM -> registers -> (+bias, act) -> staging -> TMA store
+        // ------------------------------------------------------------------
+        const int q = warp & 3;  // TMEM sub-partition this warp may read
+        const int ew = warp - 2;
+        StoreRing ring{base + p.off_staging + (uint32_t)ew * 2u * p.staging_buf_bytes, p.staging_buf_bytes, 0};
+        uint32_t acc = 0, acc_phase = 0;
+        bool first = true;
+        const int32_t halves = p.bm / 128;
+        const int32_t tile_elems = p.bm * p.bn;
+        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
+            bool ok = true;
+            if (first && p.debug_stall) ok = wait_bar(never_bar, 0, ctl, SITE_EPI_STALL);
+            first = false;
+            if (ok) ok = wait_bar(tfull0 + 8u * acc, acc_phase, ctl, SITE_EPI_TMEM_FULL);
+            if (named_bar_any(1, 128, !ok)) break;
+            tc_fence_after();
+            const int32_t nk = w.kb_end - w.kb_begin;
+            const int32_t r0 = w.tile_m * p.bm;
+            const int32_t c0 = w.tile_n * p.bn;
+            const uint32_t tacc = tmem_base + acc * p.acc_cols + ((uint32_t)(q * 32) << 16);
+            float *ws = nullptr;
+            if (p.split_k > 1) ws = p.workspace + ((size_t)w.tile * p.split_k + w.split) * (size_t)tile_elems;
+
+            if (!p.swap_ab) {
+                for (int32_t h = 0; h < halves; ++h) {
+                    const int32_t r = h * 128 + q * 32 + lane;
+                    for (int32_t c = 0; c < p.bn / 32; ++c) {
+                        float v[32];
+                        if (nk > 0) tmem_load_chunk<32>(tacc + (uint32_t)(h * p.bn + c * 32), v);
+                        else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                        }
+                        if (p.split_k > 1) {
+                            float4 *dst = reinterpret_cast<float4 *>(ws);
+#pragma unroll
+                            for (int j4 = 0; j4 < 8; ++j4)
+                                dst[(size_t)(c * 8 + j4) * p.bm + r] =
+                                    make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+                        } else {
+                            const int32_t n = c0 + c * 32;
+                            if (p.epi != 0) {
+                                float b[32];
+                                load_bias32<DT>(p.bias, n, p.cols, b);
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] = apply_act(v[j] + b[j], p.epi);
+                            }
+                            const int32_t y = r0 + h * 128 + q * 32;
+                            store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < p.cols && y < p.rows);
+                        }
+                    }
+                }
+            } else {
+                for (int32_t h = 0; h < halves; ++h) {
+                    const int32_t r = h * 128 + q * 32 + lane;
+                    for (int32_t c = 0; c < p.bn / 16; ++c) {
+                        float v[16];
+                        if (nk > 0) tmem_load_chunk<16>(tacc + (uint32_t)(h * p.bn + c * 16), v);
+                        else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+                        }
+                        if (p.split_k > 1) {
+                            float4 *dst = reinterpret_cast<float4 *>(ws);
+#pragma unroll
+                            for (int j4 = 0; j4 < 4; ++j4)
+                                dst[(size_t)(c * 4 + j4) * p.bm + r] =
+                                    make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+                        } else {
+                            const int32_t xn = r0 + h * 128 + q * 32;  // output column block (user N)
+                            if (p.epi != 0) {
+                                const float b = load_bias1<DT>(p.bias, xn + lane, p.rows);
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) v[j] = apply_act(v[j] + b, p.epi);
+                            }
+                            const int32_t ym = c0 + c * 16;  // output row block (user M)
+                            store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < p.rows && ym < p.cols);
+                        }
+                    }
+                }
+            }
+            // The accumulator may be overwritten by the next unit's MMAs.
+            tc_fence_before();
+            mbar_arrive(tempty0 + 8u * acc);
+            if (++acc == p.n_acc) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+
+            if (p.split_k > 1) {
+                // The last K slice to arrive sums the partial tiles in slice
+                // order (deterministic) and applies the epilogue.
+                __threadfence();
+                named_bar_sync(1, 128);
+                if (ew == 0 && lane == 0) {
+                    const int32_t old = atomicAdd(p.counters + w.tile, 1);
+                    const int32_t last = (old == p.split_k - 1) ? 1 : 0;
+                    if (last) atomicExch(p.counters + w.tile, 0);
+                    *last_flag = last;
+                }
+                named_bar_sync(1, 128);
+                if (*last_flag) {
+                    __threadfence();
+                    const float4 *tile_ws = reinterpret_cast<const float4 *>(
+                        p.workspace + (size_t)w.tile * p.split_k * (size_t)tile_elems);
+                    const size_t slice4 = (size_t)tile_elems / 4;
+                    if (!p.swap_ab) {
+                        for (int32_t h = 0; h < halves; ++h) {
+                            const int32_t r = h * 128 + q * 32 + lane;
+                            for (int32_t c = 0; c < p.bn / 32; ++c) {
+                                float v[32];
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                                for (int32_t s = 0; s < p.split_k; ++s) {
+#pragma unroll
+                                    for (int j4 = 0; j4 < 8; ++j4) {
+                                        const float4 t = __ldcg(tile_ws + s * slice4 + (size_t)(c * 8 + j4) * p.bm + r);
+                                        v[4 * j4] += t.x;
+                                        v[4 * j4 + 1] += t.y;
+                                        v[4 * j4 + 2] += t.z;
+                                        v[4 * j4 + 3] += t.w;
+                                    }
+                                }
+                                const int32_t n = c0 + c * 32;
+                                if (p.epi != 0) {
+                                    float b[32];
+                                    load_bias32<DT>(p.bias, n, p.cols, b);
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] = apply_act(v[j] + b[j], p.epi);
+                                }
+                                const int32_t y = r0 + h * 128 + q * 32;
+                                store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < p.cols && y < p.rows);
+                            }
+                        }
+                    } else {
+                        for (int32_t h = 0; h < halves; ++h) {
+                            const int32_t r = h * 128 + q * 32 + lane;
+                            for (int32_t c = 0; c < p.bn / 16; ++c) {
+                                float v[16];
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+                                for (int32_t s = 0; s < p.split_k; ++s) {
+#pragma unroll
+                                    for (int j4 = 0; j4 < 4; ++j4) {
+                                        const float4 t = __ldcg(tile_ws + s * slice4 + (size_t)(c * 4 + j4) * p.bm + r);
+                                        v[4 * j4] += t.x;
+                                        v[4 * j4 + 1] += t.y;
+                                        v[4 * j4 + 2] += t.z;
+                                        v[4 * j4 + 3] += t.w;
+                                    }
+                                }
+                                const int32_t xn = r0 + h * 128 + q * 32;
+                                if (p.epi != 0) {
+                                    const float b = load_bias1<DT>(p.bias, xn + lane, p.rows);
+#pragma unroll
+                                    for (int j = 0; j < 16; ++j) v[j] = apply_act(v[j] + b, p.epi);
+                                }
+                                const int32_t ym = c0 + c * 16;
+                                store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < p.rows && ym < p.cols);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, p.tmem_cols);
+    }
+}
+
+// Fills a buffer with a counter-based pseudo-random uniform in [-scale, scale]
+// (tuning inputs: same value distribution as real operands, never user data).
+__global__ void fill_uniform_kernel(void *dst, int64_t n, int dt, float scale, uint32_t seed)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        uint32_t x = (uint32_t)i * 0x9E3779B9u ^ seed;
+        x ^= x >> 16;
+        x *= 0x7FEB352Du;
+        x ^= x >> 15;
+        x *= 0x846CA68Bu;
+        x ^= x >> 16;
+        const float f = ((float)(x >> 8) * (1.0f / 16777216.0f) * 2.0f - 1.0f) * scale;
+        if (dt == 0) reinterpret_cast<__nv_bfloat16 *>(dst)[i] = __float2bfloat16_rn(f);
+        else reinterpret_cast<float *>(dst)[i] = f;
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Host-side launch helpers
+// ---------------------------------------------------------------------------
+
+cudaError_t kernel_attributes(int dt, int *num_regs, int *max_threads)
+{
+    cudaFuncAttributes a;
+    cudaError_t e = dt == 0 ? cudaFuncGetAttributes(&a, gemm_tcgen05_kernel<0>)
+                            : cudaFuncGetAttributes(&a, gemm_tcgen05_kernel<1>);
+    if (e != cudaSuccess) return e;
+    if (num_regs) *num_regs = a.numRegs;
+    if (max_threads) *max_threads = a.maxThreadsPerBlock;
+    return cudaSuccess;
+}
+
+cudaError_t set_kernel_smem_limit(int dt, int bytes)
+{
+    return dt == 0 ? cudaFuncSetAttribute(gemm_tcgen05_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+                   : cudaFuncSetAttribute(gemm_tcgen05_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
+                        const KernelParams &p, int grid, int smem_bytes, cudaStream_t stream)
+{
+    if (dt == 0) gemm_tcgen05_kernel<0><<<grid, 192, smem_bytes, stream>>>(a, b, c, p);
+    else gemm_tcgen05_kernel<1><<<grid, 192, smem_bytes, stream>>>(a, b, c, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_uniform(void *dst, int64_t n, int dt, float scale, uint32_t seed, cudaStream_t stream)
+{
+    if (n <= 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    fill_uniform_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dst, n, dt, scale, seed);
+    return cudaGetLastError();
+}
+
+}  // namespace gemmgb

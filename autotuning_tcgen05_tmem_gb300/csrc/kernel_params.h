@@ -1,0 +1,40 @@
+// Launch record of the tcgen05 GEMM kernel (host and device agree on it).
+#pragma once
+#include <stdint.h>
+
+namespace gemmgb {
+
+// Status-word codes written by a kernel whose bounded wait expired.
+enum WaitSite : int32_t {
+    SITE_PRODUCER_EMPTY = 1,
+    SITE_MMA_FULL = 2,
+    SITE_MMA_TMEM_EMPTY = 3,
+    SITE_EPI_TMEM_FULL = 4,
+    SITE_EPI_STALL = 5,
+    SITE_TEARDOWN = 6,
+};
+
+struct KernelParams {
+    // Problem in MMA orientation: rows along the MMA M axis, cols along MMA N.
+    // Unswapped: rows = M, cols = N.  Swapped (Cᵀ = Bᵀ·Aᵀ): rows = N, cols = M.
+    int32_t rows, cols, K;
+    int32_t bm, bn, bk, stages;
+    int32_t raster, group, split_k;
+    int32_t tiles_m, tiles_n, num_kb, num_units;
+    int32_t swap_ab, epi;
+    int32_t a_mn_major, b_mn_major;   // operand majorness in shared memory
+    uint32_t idesc;                    // tcgen05 instruction descriptor
+    uint32_t a_stage_bytes, b_stage_bytes, tx_bytes;
+    uint32_t a_lbo, b_lbo;             // leading-byte offsets of MN-major operands
+    uint32_t acc_cols, n_acc, tmem_cols;
+    uint32_t off_b, off_staging, off_bar, staging_buf_bytes;
+    const void *bias;                  // nullable iff epi == 0
+    float *workspace;                  // split-K partial tiles
+    int32_t *counters;                 // split-K arrival counters, one per tile
+    int32_t *status;                   // device status word (0 = ok)
+    int64_t timeout_ns;                // bound of every mbarrier wait
+    int32_t debug_stall;               // epilogue waits on a barrier nothing signals
+    int32_t pad_;
+};
+
+}  // namespace gemmgb

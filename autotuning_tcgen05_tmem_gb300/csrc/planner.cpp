@@ -1,0 +1,393 @@
+// Selection-layer host logic: device parameters, the feasibility filter, the
+// candidate generator, the analytical cost model and rank agreement.
+//
+// Sources (page title, section):
+//  * "Tile Selection: Cost Models Against Measurement": hardware limits that are
+//    checkable before any code runs ("The structure of the search space");
+//    the roofline model with its pipeline-fill, occupancy and tail corrections
+//    ("Analytical models and where they break"); the hybrid filter -> rank ->
+//    measure arrangement ("Hybrid strategies"); per-device selection.
+//  * "Compilers and Kernel Languages": waves of one tile per multiprocessor,
+//    the workshop model (HBM traffic divided by g = √(tiles sharing panels in
+//    one wave), compute divided by wave and tile efficiency, time = max).
+//  * "Tiling the hierarchy": shared memory holds the reuse tile, the pipeline
+//    stages and the epilogue scratch together; stages convert load + compute
+//    into max(load, compute) once enough bytes are in flight; the threshold
+//    regime when the working set fits in a cache level.
+//  * "Autotuning & cost models" §6: the model ranks, measurement decides; rank
+//    agreement (Kendall τ, Spearman ρ) says how far the ranking can be trusted.
+#include <math.h>
+#include <stdarg.h>
+#include <string.h>
+
+#include <algorithm>
+#include <numeric>
+
+#include "gemm_internal.h"
+
+namespace gemmgb {
+
+void params_default(gemm_device_params *d)
+{
+    memset(d, 0, sizeof(*d));
+    d->sm_count = 152;
+    d->model_kind = 0;
+    d->smem_per_block = 232448;
+    d->l2_bytes = 129LL * 1024 * 1024;
+    d->peak_tflops_bf16 = 2250.0;
+    d->peak_tflops_tf32 = 1125.0;
+    d->hbm_gbs = 7900.0;
+    d->sm_clock_mhz = 2070.0;
+    d->mma_flops_per_clk_bf16 = 8192.0;
+    d->mma_flops_per_clk_tf32 = 4096.0;
+    d->smem_bytes_per_clk = 128.0;
+    d->mem_latency_us = 0.8;
+    d->epi_elems_per_clk = 64.0;
+    d->launch_us = 4.0;
+    d->kernel_regs = 0;
+    d->threads_per_cta = kThreadsPerCta;
+}
+
+void params_workshop(gemm_device_params *d)
+{
+    params_default(d);
+    d->sm_count = 132;
+    d->model_kind = 1;
+    d->smem_per_block = 228 * 1024;
+    d->peak_tflops_bf16 = 989.0;
+    d->peak_tflops_tf32 = 494.5;
+    d->hbm_gbs = 3350.0;
+}
+
+static int staging_bytes(int dt, int swap_ab)
+{
+    const int rows = swap_ab ? 16 : 32;   // store chunk: 32 rows x 32 cols, or 16 token rows x 32 cols
+    return 4 * 2 * rows * 32 * elt_bytes(dt);
+}
+
+Layout layout_of(const gemm_config &c, int dt)
+{
+    Layout L;
+    const int e = elt_bytes(dt);
+    L.a_stage_bytes = (uint32_t)(c.bm * c.bk * e);
+    L.b_stage_bytes = (uint32_t)(c.bn * c.bk * e);
+    L.stage_bytes = L.a_stage_bytes + L.b_stage_bytes;
+    L.staging_total = (uint32_t)staging_bytes(dt, c.swap_ab);
+    L.staging_buf_bytes = L.staging_total / 8;
+    L.off_b = (uint32_t)c.stages * L.a_stage_bytes;
+    L.off_staging = L.off_b + (uint32_t)c.stages * L.b_stage_bytes;
+    L.off_bar = L.off_staging + L.staging_total;
+    L.smem_total = L.off_bar + (uint32_t)kAuxSmem;
+    L.acc_cols = (uint32_t)((c.bm / 128) * c.bn);
+    L.n_acc = (2 * L.acc_cols <= (uint32_t)kTmemColumns) ? 2u : 1u;
+    uint32_t need = L.acc_cols * L.n_acc, cols = 32;
+    while (cols < need) cols <<= 1;
+    L.tmem_cols = cols;
+    return L;
+}
+
+int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block)
+{
+    const int64_t per = (int64_t)(bm + bn) * bk * elt_bytes(dt);
+    const int64_t room = smem_per_block - staging_bytes(dt, swap_ab) - kAuxSmem;
+    int64_t s = room / per;
+    if (s < 0) s = 0;
+    if (s > kMaxStages) s = kMaxStages;
+    return (int)s;
+}
+
+const char *reason_text(int r)
+{
+    switch (r) {
+    case GEMM_FEASIBLE: return "feasible";
+    case GEMM_REASON_CTA_GROUP: return "cta_group must be 1";
+    case GEMM_REASON_UMMA_M: return "bm must be 128 or 256 (tcgen05 M per CTA is 128)";
+    case GEMM_REASON_UMMA_N: return "bn must be a multiple of 16 in [16, 256]";
+    case GEMM_REASON_LAYOUT: return "bn must be a multiple of 32 and of the 128-byte span when B is MN-major";
+    case GEMM_REASON_BK: return "bk must be 1..4 spans of 128 bytes";
+    case GEMM_REASON_STAGES: return "stages must be in 2..16";
+    case GEMM_REASON_SCHEDULE: return "raster must be 0/1 and group one of 1,2,4,8,16";
+    case GEMM_REASON_SPLIT_K: return "split_k must be in 1..16 and at most ceil(K/bk)";
+    case GEMM_REASON_ALIGN: return "K*elt and N*elt must be multiples of 16 bytes (TMA row stride)";
+    case GEMM_REASON_TMEM: return "one accumulator needs more than 512 TMEM columns";
+    case GEMM_REASON_SMEM: return "ring + staging + barriers exceed the shared-memory limit";
+    case GEMM_REASON_REGS: return "kernel registers x threads exceed the register file";
+    default: return "unknown reason";
+    }
+}
+
+int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &c,
+                 const gemm_device_params &d)
+{
+    (void)M;
+    (void)epi;
+    const int e = elt_bytes(dt);
+    const int span = span_elems(dt);
+    if (c.cta_group != 1) return GEMM_REASON_CTA_GROUP;
+    if (c.bm != 128 && c.bm != 256) return GEMM_REASON_UMMA_M;
+    if (c.bn % 16 != 0 || c.bn < 16 || c.bn > 256) return GEMM_REASON_UMMA_N;
+    if (c.swap_ab != 0 && c.swap_ab != 1) return GEMM_REASON_LAYOUT;
+    if (c.swap_ab == 0 && (c.bn % span != 0 || c.bn % 32 != 0)) return GEMM_REASON_LAYOUT;
+    if (c.bk % span != 0 || c.bk / span < 1 || c.bk / span > 4) return GEMM_REASON_BK;
+    if (c.stages < 2 || c.stages > kMaxStages) return GEMM_REASON_STAGES;
+    if ((c.raster != 0 && c.raster != 1) ||
+        !(c.group == 1 || c.group == 2 || c.group == 4 || c.group == 8 || c.group == 16))
+        return GEMM_REASON_SCHEDULE;
+    const int64_t num_kb = cdiv(K, c.bk);
+    if (c.split_k < 1 || c.split_k > kMaxSplitK || c.split_k > std::max<int64_t>(1, num_kb))
+        return GEMM_REASON_SPLIT_K;
+    if ((K * e) % 16 != 0 || (N * e) % 16 != 0) return GEMM_REASON_ALIGN;
+    const Layout L = layout_of(c, dt);
+    if (L.acc_cols > (uint32_t)kTmemColumns) return GEMM_REASON_TMEM;
+    if ((int64_t)L.smem_total > d.smem_per_block) return GEMM_REASON_SMEM;
+    if (d.kernel_regs > 0 && (int64_t)d.kernel_regs * d.threads_per_cta > 65536) return GEMM_REASON_REGS;
+    return GEMM_FEASIBLE;
+}
+
+std::vector<gemm_config> enumerate(int64_t M, int64_t N, int64_t K, int dt, int epi,
+                                   const gemm_device_params &d)
+{
+    static const int kSplits[] = {2, 3, 4, 6, 8, 12, 16};
+    static const int kGroups[] = {1, 4, 8, 16};
+    std::vector<gemm_config> out;
+    const int span = span_elems(dt);
+    const int nswap = (M <= 256) ? 2 : 1;
+    for (int swap = 0; swap < nswap; ++swap) {
+        const int64_t rows = swap ? N : M, cols = swap ? M : N;
+        for (int bm : {128, 256}) {
+            std::vector<int> bns;
+            if (swap) bns = {16, 32, 64, 128, 256};
+            else if (dt == GEMM_BF16) bns = {64, 128, 192, 256};
+            else bns = {32, 64, 128, 192, 256};
+            for (int bn : bns) {
+                for (int bk : {span, 2 * span}) {
+                    const int st_max = max_stages_for(bm, bn, bk, dt, swap, d.smem_per_block);
+                    if (st_max < 2) continue;
+                    std::vector<int> stage_list = {std::min(4, st_max)};
+                    if (st_max != stage_list[0]) stage_list.push_back(st_max);
+                    const int64_t tiles = cdiv(rows, bm) * cdiv(cols, bn);
+                    const int64_t num_kb = cdiv(K, bk);
+                    std::vector<int> splits;
+                    if (tiles < 4LL * d.sm_count)
+                        for (int s : kSplits)
+                            if (2LL * s <= num_kb && tiles * s <= 16LL * d.sm_count) splits.push_back(s);
+                    std::vector<std::pair<int, int>> scheds = {{0, 1}};
+                    if (tiles > d.sm_count) {
+                        scheds.clear();
+                        for (int r = 0; r < 2; ++r)
+                            for (int g : kGroups) scheds.push_back({r, g});
+                    }
+                    struct Combo { int raster, group, split; };
+                    std::vector<Combo> combos;
+                    for (auto &s : scheds) combos.push_back({s.first, s.second, 1});
+                    for (int s : splits) combos.push_back({0, 1, s});
+                    for (int st : stage_list) {
+                        for (const Combo &cb : combos) {
+                            gemm_config c{bm, bn, bk, st, cb.raster, cb.group, cb.split, 1, swap};
+                            if (check_config(M, N, K, dt, epi, c, d) == GEMM_FEASIBLE) out.push_back(c);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    return out;
+}
+
+gemm_config fixed_config(int dt, const gemm_device_params &d)
+{
+    const int span = span_elems(dt);
+    gemm_config c{128, 128, span, max_stages_for(128, 128, span, dt, 0, d.smem_per_block), 0, 1, 1, 1, 0};
+    return c;
+}
+
+// ---------------------------------------------------------------------------
+// Cost model
+// ---------------------------------------------------------------------------
+
+static gemm_model_terms predict_workshop(int64_t M, int64_t N, int64_t K, int dt, const gemm_config &c,
+                                         const gemm_device_params &d)
+{
+    // "Compilers and Kernel Languages", workshop paragraph.  The tile-efficiency
+    // law 0.5 + 0.5·min(1, bm·bn/128²) is the reading that reproduces the page's
+    // printed ratios; g = √min(tiles, SMs).
+    gemm_model_terms t;
+    memset(&t, 0, sizeof(t));
+    const double e = elt_bytes(dt);
+    const int64_t tiles = cdiv(M, c.bm) * cdiv(N, c.bn);
+    const int64_t waves = cdiv(tiles, d.sm_count);
+    const double weff = (double)tiles / ((double)waves * d.sm_count);
+    const double teff = 0.5 + 0.5 * std::min(1.0, (double)c.bm * c.bn / (128.0 * 128.0));
+    const double flops = 2.0 * (double)M * (double)N * (double)K;
+    const double compute = flops / (d.peak_tflops_bf16 * 1e12) / weff / teff;
+    const double g = sqrt((double)std::min<int64_t>(tiles, d.sm_count));
+    const double panel = (double)tiles * K * (c.bm + c.bn) * e / g + (double)M * N * e;
+    const double floor_b = ((double)M * K + (double)K * N + (double)M * N) * e;
+    const double bytes = std::max(panel, floor_b);
+    const double memory = bytes / (d.hbm_gbs * 1e9);
+    t.compute_us = compute * 1e6;
+    t.memory_us = memory * 1e6;
+    t.predicted_us = std::max(compute, memory) * 1e6;
+    t.wave_eff = weff;
+    t.tile_eff = teff;
+    t.pad_eff = 1.0;
+    t.hbm_bytes = bytes;
+    t.flops = flops;
+    t.tiles = tiles;
+    t.units = tiles;
+    t.waves = waves;
+    t.ctas = std::min<int64_t>(tiles, d.sm_count);
+    return t;
+}
+
+gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &c,
+                         const gemm_device_params &d)
+{
+    if (d.model_kind == 1) return predict_workshop(M, N, K, dt, c, d);
+    gemm_model_terms t;
+    memset(&t, 0, sizeof(t));
+    const double e = elt_bytes(dt);
+    const int64_t rows = c.swap_ab ? N : M, cols = c.swap_ab ? M : N;
+    const int64_t tiles_m = cdiv(rows, c.bm), tiles_n = cdiv(cols, c.bn);
+    const int64_t tiles = tiles_m * tiles_n;
+    const int64_t S = c.split_k;
+    const int64_t num_kb = cdiv(K, c.bk);
+    const int64_t units = tiles * S;
+    const int64_t sms = d.sm_count;
+    const int64_t ctas = std::min(units, sms);
+    const int64_t waves = cdiv(units, sms);
+    const double weff = (double)units / ((double)waves * sms);
+
+    // Tensor pipe: one tcgen05 MMA is 128 x bn x (32 bytes of K); it needs
+    // (128 + bn) rows x 32 bytes of operands from shared memory.  The slower of
+    // the two clocks sets the tile efficiency.
+    const double flops = 2.0 * (double)M * (double)N * (double)K;
+    const double peak = (dt == GEMM_BF16 ? d.peak_tflops_bf16 : d.peak_tflops_tf32) * 1e12;
+    const double fpc = dt == GEMM_BF16 ? d.mma_flops_per_clk_bf16 : d.mma_flops_per_clk_tf32;
+    const double kslice = 32.0 / e;
+    const double mma_clk = 2.0 * 128.0 * c.bn * kslice / fpc;
+    const double smem_clk = (128.0 + c.bn) * 32.0 / d.smem_bytes_per_clk;
+    const double teff = mma_clk / std::max(mma_clk, smem_clk);
+    const double peff = K > 0 ? ((double)rows * cols * K) /
+                                    ((double)tiles_m * c.bm * (double)tiles_n * c.bn * (double)num_kb * c.bk)
+                              : 1.0;
+    const double compute = flops > 0 ? flops / (peak * weff * teff * peff) : 0.0;
+
+    // HBM: operands either fit in half of L2 (threshold regime: compulsory
+    // bytes only) or are re-read once per wave of concurrent tiles, with the
+    // wave's footprint shaped by the tile order (group-G band).
+    const double in_bytes = ((double)M * K + (double)K * N) * e;
+    const int64_t wave_tiles = std::min<int64_t>(tiles, std::max<int64_t>(1, ctas / S));
+    int64_t rows_w, cols_w;
+    if (c.raster == 0) {
+        rows_w = std::min<int64_t>(std::min<int64_t>(c.group, tiles_m), wave_tiles);
+        cols_w = std::min<int64_t>(cdiv(wave_tiles, rows_w), tiles_n);
+    } else {
+        cols_w = std::min<int64_t>(std::min<int64_t>(c.group, tiles_n), wave_tiles);
+        rows_w = std::min<int64_t>(cdiv(wave_tiles, cols_w), tiles_m);
+    }
+    const double wave_bytes = (double)K * ((double)rows_w * c.bm + (double)cols_w * c.bn) * e;
+    const double panel = ((double)tiles / (double)wave_tiles) * wave_bytes;
+    const double operand = (in_bytes <= (double)d.l2_bytes / 2.0) ? in_bytes : std::max(in_bytes, panel);
+    const double epi_bytes = (double)M * N * e + (epi != GEMM_EPI_NONE ? (double)N * e : 0.0);
+    const double split_bytes = S > 1 ? (double)units * c.bm * c.bn * 4.0 : 0.0;
+    const double hbm = operand + epi_bytes + split_bytes;
+    const double memory = hbm / (d.hbm_gbs * 1e9);
+
+    // Bytes in flight: a CTA keeps at most `stages` slots outstanding, so one
+    // memory latency covers `stages` K-steps.
+    const int64_t per_cta_units = ctas > 0 ? cdiv(units, ctas) : 0;
+    const double per_cta_kb = (double)per_cta_units * (double)cdiv(num_kb, S);
+    const double latency = per_cta_kb * d.mem_latency_us * 1e-6 / c.stages;
+    // Epilogue: drains bm·bn accumulators per unit; overlapped with the next
+    // unit's main loop, so it bounds the CTA only when it is the slower stage.
+    const double epi_unit = (double)c.bm * c.bn / (d.epi_elems_per_clk * d.sm_clock_mhz * 1e6);
+    const double epilogue = (double)per_cta_units * epi_unit;
+    const double body = std::max(std::max(compute, memory), std::max(latency, epilogue));
+    const double fill = d.mem_latency_us * 1e-6 + epi_unit;
+    const double total = body + fill + d.launch_us * 1e-6;
+
+    t.predicted_us = total * 1e6;
+    t.compute_us = compute * 1e6;
+    t.memory_us = memory * 1e6;
+    t.latency_us = latency * 1e6;
+    t.epilogue_us = epilogue * 1e6;
+    t.fill_us = fill * 1e6;
+    t.wave_eff = weff;
+    t.tile_eff = teff;
+    t.pad_eff = peff;
+    t.hbm_bytes = hbm;
+    t.flops = flops;
+    t.tiles = tiles;
+    t.units = units;
+    t.waves = waves;
+    t.ctas = ctas;
+    return t;
+}
+
+// ---------------------------------------------------------------------------
+// Rank agreement
+// ---------------------------------------------------------------------------
+
+static std::vector<double> average_ranks(const double *v, int n)
+{
+    std::vector<int> idx(n);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return v[a] < v[b]; });
+    std::vector<double> r(n);
+    for (int i = 0; i < n;) {
+        int j = i;
+        while (j + 1 < n && v[idx[j + 1]] == v[idx[i]]) ++j;
+        const double avg = 0.5 * (i + j) + 1.0;
+        for (int t = i; t <= j; ++t) r[idx[t]] = avg;
+        i = j + 1;
+    }
+    return r;
+}
+
+gemm_rank_stats rank_agreement(const double *x, const double *y, int n)
+{
+    gemm_rank_stats s;
+    memset(&s, 0, sizeof(s));
+    int64_t conc = 0, disc = 0, tx = 0, ty = 0;
+    for (int i = 0; i < n; ++i)
+        for (int j = i + 1; j < n; ++j) {
+            const int dx = (x[i] > x[j]) - (x[i] < x[j]);
+            const int dy = (y[i] > y[j]) - (y[i] < y[j]);
+            if (dx == 0 && dy == 0) continue;
+            if (dx == 0) ++tx;
+            else if (dy == 0) ++ty;
+            else if (dx == dy) ++conc;
+            else ++disc;
+        }
+    const double den = sqrt((double)(conc + disc + tx) * (double)(conc + disc + ty));
+    s.kendall_tau = den > 0 ? (double)(conc - disc) / den : NAN;
+    const std::vector<double> rx = average_ranks(x, n), ry = average_ranks(y, n);
+    double mx = 0, my = 0;
+    for (int i = 0; i < n; ++i) {
+        mx += rx[i];
+        my += ry[i];
+    }
+    mx /= n;
+    my /= n;
+    double sxy = 0, sxx = 0, syy = 0;
+    for (int i = 0; i < n; ++i) {
+        sxy += (rx[i] - mx) * (ry[i] - my);
+        sxx += (rx[i] - mx) * (rx[i] - mx);
+        syy += (ry[i] - my) * (ry[i] - my);
+    }
+    s.spearman_rho = (sxx > 0 && syy > 0) ? sxy / sqrt(sxx * syy) : NAN;
+    int pick = 0, best = 0;
+    for (int i = 1; i < n; ++i) {
+        if (x[i] < x[pick]) pick = i;
+        if (y[i] < y[best]) best = i;
+    }
+    s.top1_hit = y[pick] == y[best] ? 1 : 0;
+    s.regret = y[pick] / y[best] - 1.0;
+    s.best_us = y[best];
+    s.n_measured = n;
+    s.fixed_us = -1.0;
+    return s;
+}
+
+}  // namespace gemmgb

@@ -1,0 +1,766 @@
+// Plans, launches, the on-device tuner and the tune-once cache.
+//
+// Sources (page title, section):
+//  * "Tile Selection: Cost Models Against Measurement", "Measurement, and what it
+//    must control": interleave candidates (clock drift), realistic input values,
+//    many repetitions per timing (launch overhead); results cached by shape,
+//    dtype, device model and library version.  "Hybrid strategies": resource
+//    filter -> model rank -> measure the top handful.
+//  * "Autotuning & cost models" §4: benchmark on the first call for a key,
+//    remember the winner, reuse it for every later call with the same key.
+//  * "CuTile Autotuning": tune once, cache config and launchable object, launch
+//    directly; the search space includes the original fixed config; in-place
+//    kernels are tuned on separate buffers (here: tuning never touches user
+//    memory); DISABLE_AUTOTUNE-style switch for correctness runs.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <map>
+#include <mutex>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include "gemm_internal.h"
+#include "schedule.h"
+
+namespace gemmgb {
+
+std::atomic<int64_t> g_timeout_ns{2000000000LL};
+std::atomic<int32_t> g_debug_stall{0};
+
+// ---------------------------------------------------------------------------
+// TMA descriptor encoding through the driver entry point
+// ---------------------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+static int encoder_ready()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// Row-major [outer, inner] matrix, box [box_outer, box_inner].
+static int encode_2d(CUtensorMap *m, int dt, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                     uint32_t box_outer, CUtensorMapSwizzle sw, CUtensorMapL2promotion l2)
+{
+    if (!encoder_ready()) return set_error(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * (uint64_t)elt_bytes(dt)};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType t = dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUresult r = g_encode(m, t, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] box [%u x %u]", (int)r,
+                         (unsigned long long)outer, (unsigned long long)inner, box_outer, box_inner);
+    return GEMM_OK;
+}
+
+static int cuda_err(cudaError_t e, const char *what)
+{
+    return set_error(GEMM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------------------
+// Device parameters
+// ---------------------------------------------------------------------------
+
+static double env_double(const char *name, double dflt)
+{
+    const char *v = getenv(name);
+    if (!v || !*v) return dflt;
+    char *end = nullptr;
+    const double x = strtod(v, &end);
+    return (end && end != v && x > 0) ? x : dflt;
+}
+
+int query_params(gemm_device_params *d)
+{
+    params_default(d);
+    int dev = 0, v = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(GEMM_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+    }
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_err(e, "cudaDeviceGetAttribute(SM count)");
+    d->sm_count = v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess) d->smem_per_block = v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) == cudaSuccess) d->l2_bytes = v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrClockRate, dev) == cudaSuccess && v > 0) d->sm_clock_mhz = v / 1000.0;
+    int regs = 0;
+    if (kernel_attributes(GEMM_BF16, &regs, nullptr) == cudaSuccess) d->kernel_regs = regs;
+    d->peak_tflops_bf16 = env_double("GEMM_PEAK_BF16_TFLOPS", d->peak_tflops_bf16);
+    d->peak_tflops_tf32 = env_double("GEMM_PEAK_TF32_TFLOPS", d->peak_tflops_bf16 / 2.0);
+    d->hbm_gbs = env_double("GEMM_HBM_GBS", d->hbm_gbs);
+    return GEMM_OK;
+}
+
+static int check_device_arch(int *device_out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(GEMM_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+    }
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+        return set_error(GEMM_ERR_UNSUPPORTED, "kernels are built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+    if (device_out) *device_out = dev;
+    return GEMM_OK;
+}
+
+}  // namespace gemmgb
+
+// ---------------------------------------------------------------------------
+// Plan object
+// ---------------------------------------------------------------------------
+
+struct DescEntry {
+    const void *a = nullptr, *b = nullptr;
+    void *c = nullptr;
+    bool valid = false;
+    CUtensorMap ma, mb, mc;
+};
+
+struct gemm_plan_s {
+    int64_t M = 0, N = 0, K = 0;
+    int dt = 0, epi = 0, device = 0;
+    gemm_config cfg{};
+    gemm_device_params dev{};
+    gemmgb::Layout L{};
+    gemmgb::KernelParams kp{};
+    int grid = 0, smem_request = 0;
+    float *workspace = nullptr;
+    bool owns_workspace = false;
+    int32_t *aux = nullptr;          // [0] status word, [1..tiles] split-K counters
+    int64_t tiles = 0;
+    std::vector<DescEntry> descs = std::vector<DescEntry>(16);
+    int next_desc = 0;
+    void *hA = nullptr, *hB = nullptr, *hBias = nullptr, *hC = nullptr;  // device buffers for run_host
+};
+
+namespace gemmgb {
+
+static int configure_smem_limit(int dt, int64_t bytes)
+{
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, int64_t> done;  // (device, dtype) -> bytes set
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_pair(dev, dt);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return GEMM_OK;
+    cudaError_t e = set_kernel_smem_limit(dt, (int)bytes);
+    if (e != cudaSuccess) return cuda_err(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+    done[key] = bytes;
+    return GEMM_OK;
+}
+
+static bool valid_enums(int dt, int epi)
+{
+    return (dt == GEMM_BF16 || dt == GEMM_FP32_TF32) && epi >= GEMM_EPI_NONE && epi <= GEMM_EPI_BIAS_GELU;
+}
+
+static int check_extents(int64_t M, int64_t N, int64_t K)
+{
+    const int64_t lim = (int64_t)1 << 31;
+    if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim)
+        return set_error(GEMM_ERR_INVALID_ARG, "extents must be in [0, 2^31): M=%lld N=%lld K=%lld", (long long)M,
+                         (long long)N, (long long)K);
+    return GEMM_OK;
+}
+
+// Builds a plan; `shared_ws` (may be null) is a caller-owned split-K workspace
+// of at least the needed size (used while tuning many candidates).
+int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &cfg,
+              const gemm_device_params &dev, float *shared_ws, gemm_plan_t *out)
+{
+    *out = nullptr;
+    int rc = check_extents(M, N, K);
+    if (rc) return rc;
+    if (!valid_enums(dt, epi)) return set_error(GEMM_ERR_INVALID_ARG, "unknown dtype %d or epilogue %d", dt, epi);
+    const int reason = check_config(M, N, K, dt, epi, cfg, dev);
+    if (reason == GEMM_REASON_ALIGN)
+        return set_error(GEMM_ERR_MISALIGNED, "K=%lld / N=%lld: %s", (long long)K, (long long)N, reason_text(reason));
+    if (reason != GEMM_FEASIBLE)
+        return set_error(GEMM_ERR_INFEASIBLE, "config %dx%dx%d s%d r%d g%d k%d c%d sw%d: %s", cfg.bm, cfg.bn, cfg.bk,
+                         cfg.stages, cfg.raster, cfg.group, cfg.split_k, cfg.cta_group, cfg.swap_ab,
+                         reason_text(reason));
+    gemm_plan_s *p = new gemm_plan_s();
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->dt = dt;
+    p->epi = epi;
+    p->cfg = cfg;
+    p->dev = dev;
+    cudaGetDevice(&p->device);
+    p->L = layout_of(cfg, dt);
+    KernelParams &k = p->kp;
+    memset(&k, 0, sizeof(k));
+    k.rows = (int32_t)(cfg.swap_ab ? N : M);
+    k.cols = (int32_t)(cfg.swap_ab ? M : N);
+    k.K = (int32_t)K;
+    k.bm = cfg.bm;
+    k.bn = cfg.bn;
+    k.bk = cfg.bk;
+    k.stages = cfg.stages;
+    k.raster = cfg.raster;
+    k.group = cfg.group;
+    k.split_k = cfg.split_k;
+    k.tiles_m = (int32_t)cdiv(k.rows, cfg.bm);
+    k.tiles_n = (int32_t)cdiv(k.cols, cfg.bn);
+    k.num_kb = (int32_t)cdiv(K, cfg.bk);
+    p->tiles = (int64_t)k.tiles_m * k.tiles_n;
+    k.num_units = (int32_t)(p->tiles * cfg.split_k);
+    k.swap_ab = cfg.swap_ab;
+    k.epi = epi;
+    k.a_mn_major = cfg.swap_ab ? 1 : 0;   // MMA-A is user B (N-contiguous) when swapped
+    k.b_mn_major = cfg.swap_ab ? 0 : 1;   // MMA-B is user B (N-contiguous) when not swapped
+    const uint32_t fmt = dt == GEMM_BF16 ? 1u : 2u;  // BF16 (kind::f16) / TF32 (kind::tf32)
+    k.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)k.a_mn_major << 15) |
+              ((uint32_t)k.b_mn_major << 16) | ((uint32_t)(cfg.bn >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    k.a_stage_bytes = p->L.a_stage_bytes;
+    k.b_stage_bytes = p->L.b_stage_bytes;
+    k.tx_bytes = p->L.stage_bytes;
+    k.a_lbo = k.a_mn_major ? (uint32_t)(cfg.bk * 128) : 16u;
+    k.b_lbo = k.b_mn_major ? (uint32_t)(cfg.bk * 128) : 16u;
+    k.acc_cols = p->L.acc_cols;
+    k.n_acc = p->L.n_acc;
+    k.tmem_cols = p->L.tmem_cols;
+    k.off_b = p->L.off_b;
+    k.off_staging = p->L.off_staging;
+    k.off_bar = p->L.off_bar;
+    k.staging_buf_bytes = p->L.staging_buf_bytes;
+    p->grid = (int)std::min<int64_t>(k.num_units, dev.sm_count);
+    // Ask for more than half of the SM's shared memory so that no two CTAs of
+    // this kernel share an SM (each may hold up to 512 TMEM columns).
+    const int64_t one_per_sm = dev.smem_per_block / 2 + 1024;
+    p->smem_request = (int)std::min<int64_t>(dev.smem_per_block, std::max<int64_t>(p->L.smem_total, one_per_sm));
+
+    cudaError_t e = cudaMalloc(&p->aux, (size_t)(1 + p->tiles) * sizeof(int32_t));
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_err(e, "cudaMalloc(plan status/counters)");
+    }
+    e = cudaMemset(p->aux, 0, (size_t)(1 + p->tiles) * sizeof(int32_t));
+    if (e != cudaSuccess) {
+        cudaFree(p->aux);
+        delete p;
+        return cuda_err(e, "cudaMemset(plan status/counters)");
+    }
+    k.status = p->aux;
+    k.counters = p->aux + 1;
+    if (cfg.split_k > 1) {
+        if (shared_ws) {
+            p->workspace = shared_ws;
+        } else {
+            const size_t bytes = (size_t)p->tiles * cfg.split_k * cfg.bm * cfg.bn * sizeof(float);
+            e = cudaMalloc(&p->workspace, bytes);
+            if (e != cudaSuccess) {
+                cudaFree(p->aux);
+                delete p;
+                return cuda_err(e, "cudaMalloc(split-K workspace)");
+            }
+            p->owns_workspace = true;
+        }
+    }
+    k.workspace = p->workspace;
+    rc = configure_smem_limit(dt, dev.smem_per_block);
+    if (rc) {
+        if (p->owns_workspace) cudaFree(p->workspace);
+        cudaFree(p->aux);
+        delete p;
+        return rc;
+    }
+    *out = p;
+    return GEMM_OK;
+}
+
+static size_t split_ws_bytes(int64_t M, int64_t N, const gemm_config &c)
+{
+    if (c.split_k <= 1) return 0;
+    const int64_t rows = c.swap_ab ? N : M, cols = c.swap_ab ? M : N;
+    return (size_t)(cdiv(rows, c.bm) * cdiv(cols, c.bn)) * c.split_k * c.bm * c.bn * sizeof(float);
+}
+
+void destroy_plan(gemm_plan_t p)
+{
+    if (!p) return;
+    if (p->owns_workspace) cudaFree(p->workspace);
+    cudaFree(p->aux);
+    cudaFree(p->hA);
+    cudaFree(p->hB);
+    cudaFree(p->hBias);
+    cudaFree(p->hC);
+    delete p;
+}
+
+static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const DescEntry **out)
+{
+    for (const DescEntry &d : p->descs)
+        if (d.valid && d.a == A && d.b == B && d.c == C) {
+            *out = &d;
+            return GEMM_OK;
+        }
+    DescEntry &d = p->descs[p->next_desc];
+    p->next_desc = (p->next_desc + 1) % (int)p->descs.size();
+    d.valid = false;
+    const int dt = p->dt;
+    const int span = span_elems(dt);
+    const gemm_config &c = p->cfg;
+    int rc = GEMM_OK;
+    memset(&d.ma, 0, sizeof(d.ma));
+    memset(&d.mb, 0, sizeof(d.mb));
+    if (p->K > 0) {
+        if (!c.swap_ab) {
+            rc = encode_2d(&d.ma, dt, A, p->K, p->M, span, c.bm, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+            if (!rc)
+                rc = encode_2d(&d.mb, dt, B, p->N, p->K, span, c.bk, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        } else {
+            rc = encode_2d(&d.ma, dt, B, p->N, p->K, span, c.bk, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+            if (!rc)
+                rc = encode_2d(&d.mb, dt, A, p->K, p->M, span, c.bn, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        }
+    }
+    if (!rc) {
+        if (!c.swap_ab)
+            rc = encode_2d(&d.mc, dt, C, p->N, p->M, 32, 32,
+                           dt == GEMM_BF16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE);
+        else
+            rc = encode_2d(&d.mc, dt, C, p->N, p->M, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    }
+    if (rc) return rc;
+    d.a = A;
+    d.b = B;
+    d.c = C;
+    d.valid = true;
+    *out = &d;
+    return GEMM_OK;
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream)
+{
+    if (!p) return set_error(GEMM_ERR_INVALID_ARG, "null plan");
+    if (p->M == 0 || p->N == 0) return GEMM_OK;
+    if (!C || (p->K > 0 && (!A || !B))) return set_error(GEMM_ERR_INVALID_ARG, "null A, B or C");
+    if (p->epi != GEMM_EPI_NONE && !bias) return set_error(GEMM_ERR_INVALID_ARG, "bias is required by the epilogue");
+    if ((p->K > 0 && (!aligned16(A) || !aligned16(B))) || !aligned16(C) ||
+        (p->epi != GEMM_EPI_NONE && !aligned16(bias)))
+        return set_error(GEMM_ERR_MISALIGNED, "A, B, C and bias must be 16-byte aligned");
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev != p->device)
+        return set_error(GEMM_ERR_INVALID_ARG, "plan was made on device %d, current device is %d", p->device, dev);
+    const DescEntry *d = nullptr;
+    int rc = get_descs(p, A, B, C, &d);
+    if (rc) return rc;
+    KernelParams kp = p->kp;
+    kp.bias = p->epi != GEMM_EPI_NONE ? bias : nullptr;
+    kp.timeout_ns = g_timeout_ns.load();
+    kp.debug_stall = g_debug_stall.load();
+    cudaError_t e = launch_gemm(p->dt, d->ma, d->mb, d->mc, kp, p->grid, p->smem_request, stream);
+    if (e != cudaSuccess) return cuda_err(e, "kernel launch");
+    return GEMM_OK;
+}
+
+int plan_config(gemm_plan_t p, gemm_config *out)
+{
+    if (!p || !out) return set_error(GEMM_ERR_INVALID_ARG, "null plan or output");
+    *out = p->cfg;
+    return GEMM_OK;
+}
+
+int plan_status(gemm_plan_t p)
+{
+    if (!p) return set_error(GEMM_ERR_INVALID_ARG, "null plan");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_err(e, "cudaDeviceSynchronize");
+    int32_t st = 0;
+    e = cudaMemcpy(&st, p->aux, sizeof(st), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_err(e, "reading the status word");
+    if (st != 0) {
+        cudaMemset(p->aux, 0, (size_t)(1 + p->tiles) * sizeof(int32_t));
+        return set_error(GEMM_ERR_TIMEOUT, "a device wait expired (site %d); the kernel returned early", st);
+    }
+    return GEMM_OK;
+}
+
+int run_host(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream)
+{
+    if (!p) return set_error(GEMM_ERR_INVALID_ARG, "null plan");
+    if (p->M == 0 || p->N == 0) return GEMM_OK;
+    const size_t e = (size_t)elt_bytes(p->dt);
+    const size_t nA = (size_t)p->M * p->K * e, nB = (size_t)p->K * p->N * e, nBias = (size_t)p->N * e,
+                 nC = (size_t)p->M * p->N * e;
+    cudaError_t err;
+    if (!p->hC) {
+        if ((nA && (err = cudaMalloc(&p->hA, nA)) != cudaSuccess) ||
+            (nB && (err = cudaMalloc(&p->hB, nB)) != cudaSuccess) ||
+            (err = cudaMalloc(&p->hBias, nBias)) != cudaSuccess || (err = cudaMalloc(&p->hC, nC)) != cudaSuccess)
+            return cuda_err(err, "cudaMalloc(host-run buffers)");
+    }
+    if (nA && (err = cudaMemcpyAsync(p->hA, A, nA, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return cuda_err(err, "copy A to device");
+    if (nB && (err = cudaMemcpyAsync(p->hB, B, nB, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return cuda_err(err, "copy B to device");
+    const bool has_bias = p->epi != GEMM_EPI_NONE;
+    if (has_bias) {
+        if (!bias) return set_error(GEMM_ERR_INVALID_ARG, "bias is required by the epilogue");
+        if ((err = cudaMemcpyAsync(p->hBias, bias, nBias, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+            return cuda_err(err, "copy bias to device");
+    }
+    int rc = run_plan(p, p->hA, p->hB, has_bias ? p->hBias : nullptr, p->hC, stream);
+    if (rc) return rc;
+    if ((err = cudaMemcpyAsync(C, p->hC, nC, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+        return cuda_err(err, "copy C to host");
+    if ((err = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_err(err, "cudaStreamSynchronize");
+    return GEMM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Tuner
+// ---------------------------------------------------------------------------
+
+struct TuneBuffers {
+    std::vector<void *> A, B, bias, C;
+    float *ws = nullptr;
+    ~TuneBuffers()
+    {
+        for (auto *v : {&A, &B, &bias, &C})
+            for (void *p : *v) cudaFree(p);
+        cudaFree(ws);
+    }
+};
+
+static double median_of(std::vector<double> v)
+{
+    std::sort(v.begin(), v.end());
+    const size_t n = v.size();
+    if (n == 0) return -1.0;
+    return n % 2 ? v[n / 2] : 0.5 * (v[n / 2 - 1] + v[n / 2]);
+}
+
+static int env_int(const char *name, int dflt)
+{
+    const char *v = getenv(name);
+    if (!v || !*v) return dflt;
+    return atoi(v);
+}
+
+int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int topk, std::vector<gemm_tune_row> &rows,
+         gemm_rank_stats &stats, gemm_config *winner)
+{
+    const auto t_start = std::chrono::steady_clock::now();
+    memset(&stats, 0, sizeof(stats));
+    stats.fixed_us = -1.0;
+    rows.clear();
+    int rc = check_extents(M, N, K);
+    if (rc) return rc;
+    if (!valid_enums(dt, epi)) return set_error(GEMM_ERR_INVALID_ARG, "unknown dtype %d or epilogue %d", dt, epi);
+    if ((rc = check_device_arch(nullptr))) return rc;
+    gemm_device_params dev;
+    if ((rc = query_params(&dev))) return rc;
+    std::vector<gemm_config> cands = enumerate(M, N, K, dt, epi, dev);
+    if (cands.empty()) {
+        const int reason = check_config(M, N, K, dt, epi, fixed_config(dt, dev), dev);
+        if (reason == GEMM_REASON_ALIGN) return set_error(GEMM_ERR_MISALIGNED, "%s", reason_text(reason));
+        return set_error(GEMM_ERR_UNSUPPORTED, "no feasible configuration for M=%lld N=%lld K=%lld", (long long)M,
+                         (long long)N, (long long)K);
+    }
+    const gemm_config fixed = fixed_config(dt, dev);
+    const int n = (int)cands.size();
+    rows.resize(n);
+    std::vector<double> pred(n);
+    for (int i = 0; i < n; ++i) {
+        memset(&rows[i], 0, sizeof(gemm_tune_row));
+        rows[i].config = cands[i];
+        pred[i] = predict(M, N, K, dt, epi, cands[i], dev).predicted_us;
+        rows[i].predicted_us = pred[i];
+        rows[i].measured_us = -1.0;
+        rows[i].measured_min_us = -1.0;
+        rows[i].measured_rank = -1;
+    }
+    std::vector<int> by_model(n);
+    std::iota(by_model.begin(), by_model.end(), 0);
+    std::stable_sort(by_model.begin(), by_model.end(), [&](int a, int b) { return pred[a] < pred[b]; });
+    for (int r = 0; r < n; ++r) rows[by_model[r]].model_rank = r;
+    auto same = [](const gemm_config &a, const gemm_config &b) { return memcmp(&a, &b, sizeof(a)) == 0; };
+    int fixed_idx = -1;
+    for (int i = 0; i < n; ++i)
+        if (same(cands[i], fixed)) fixed_idx = i;
+
+    // Which candidates to time: all, or the model's top-k plus the fixed tile.
+    std::vector<int> meas;
+    if (topk <= 0 || topk >= n) {
+        meas = by_model;
+    } else {
+        meas.assign(by_model.begin(), by_model.begin() + topk);
+        if (fixed_idx >= 0 && std::find(meas.begin(), meas.end(), fixed_idx) == meas.end()) meas.push_back(fixed_idx);
+    }
+    const int nm = (int)meas.size();
+
+    // Library-owned buffers, rotated so that shapes smaller than L2 are timed
+    // from HBM like the real, larger working set.
+    const size_t e = (size_t)elt_bytes(dt);
+    const size_t bytes_a = (size_t)std::max<int64_t>(M * K, 1) * e, bytes_b = (size_t)std::max<int64_t>(K * N, 1) * e,
+                 bytes_bias = (size_t)std::max<int64_t>(N, 1) * e, bytes_c = (size_t)std::max<int64_t>(M * N, 1) * e;
+    const size_t set_bytes = bytes_a + bytes_b + bytes_bias + bytes_c;
+    int nsets = (int)std::min<int64_t>(8, std::max<int64_t>(1, cdiv(2 * dev.l2_bytes + (int64_t)set_bytes, set_bytes)));
+    TuneBuffers buf;
+    cudaStream_t stream = nullptr;
+    cudaError_t err = cudaStreamCreateWithFlags(&stream, cudaStreamNonBlocking);
+    if (err != cudaSuccess) return cuda_err(err, "cudaStreamCreate");
+    struct StreamGuard {
+        cudaStream_t s;
+        ~StreamGuard() { cudaStreamDestroy(s); }
+    } sg{stream};
+    const float scale_ab = (float)sqrt(3.0 / (double)std::max<int64_t>(K, 1));
+    for (int s = 0; s < nsets; ++s) {
+        void *a = nullptr, *b = nullptr, *bb = nullptr, *c = nullptr;
+        if ((err = cudaMalloc(&a, bytes_a)) != cudaSuccess) return cuda_err(err, "cudaMalloc(tuning A)");
+        buf.A.push_back(a);
+        if ((err = cudaMalloc(&b, bytes_b)) != cudaSuccess) return cuda_err(err, "cudaMalloc(tuning B)");
+        buf.B.push_back(b);
+        if ((err = cudaMalloc(&bb, bytes_bias)) != cudaSuccess) return cuda_err(err, "cudaMalloc(tuning bias)");
+        buf.bias.push_back(bb);
+        if ((err = cudaMalloc(&c, bytes_c)) != cudaSuccess) return cuda_err(err, "cudaMalloc(tuning C)");
+        buf.C.push_back(c);
+        launch_fill_uniform(a, (int64_t)(bytes_a / e), dt, scale_ab, 0x1234u + 17u * s, stream);
+        launch_fill_uniform(b, (int64_t)(bytes_b / e), dt, scale_ab, 0x5678u + 17u * s, stream);
+        launch_fill_uniform(bb, (int64_t)(bytes_bias / e), dt, 0.1f, 0x9ABCu + 17u * s, stream);
+    }
+    size_t ws_bytes = 0;
+    for (int i : meas) ws_bytes = std::max(ws_bytes, split_ws_bytes(M, N, cands[i]));
+    if (ws_bytes && (err = cudaMalloc(&buf.ws, ws_bytes)) != cudaSuccess) return cuda_err(err, "cudaMalloc(tuning workspace)");
+
+    std::vector<gemm_plan_t> plans(nm, nullptr);
+    struct PlanGuard {
+        std::vector<gemm_plan_t> &v;
+        ~PlanGuard()
+        {
+            for (auto p : v) destroy_plan(p);
+        }
+    } pg{plans};
+    std::vector<int> status(nm, GEMM_OK);
+    for (int j = 0; j < nm; ++j) {
+        status[j] = make_plan(M, N, K, dt, epi, cands[meas[j]], dev, buf.ws, &plans[j]);
+    }
+    auto run_one = [&](int j, int set) {
+        return run_plan(plans[j], buf.A[set], buf.B[set], epi != GEMM_EPI_NONE ? buf.bias[set] : nullptr, buf.C[set],
+                        stream);
+    };
+    // Warm-up and a first estimate of each candidate's time.
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    std::vector<int> reps(nm, 1);
+    for (int j = 0; j < nm; ++j) {
+        if (status[j]) continue;
+        for (int w = 0; w < 2 && !status[j]; ++w) status[j] = run_one(j, w % nsets);
+        if (status[j]) continue;
+        cudaEventRecord(e0, stream);
+        status[j] = run_one(j, 2 % nsets);
+        cudaEventRecord(e1, stream);
+        if ((err = cudaEventSynchronize(e1)) != cudaSuccess) {
+            cudaEventDestroy(e0);
+            cudaEventDestroy(e1);
+            return cuda_err(err, "tuning warm-up");
+        }
+        if (!status[j]) status[j] = plan_status(plans[j]);
+        float ms = 0;
+        cudaEventElapsedTime(&ms, e0, e1);
+        const double us = std::max(1.0, ms * 1000.0);
+        reps[j] = (int)std::min(200.0, std::max(1.0, ceil(300.0 / us)));
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    // Interleaved rounds: every round times every candidate once, starting at a
+    // different candidate, so clock drift is spread over all of them.
+    const int rounds = std::max(1, env_int("GEMM_TUNE_ROUNDS", 5));
+    std::vector<std::vector<double>> times(nm);
+    std::vector<cudaEvent_t> ev(2 * nm);
+    for (auto &x : ev) cudaEventCreate(&x);
+    int set = 0;
+    for (int r = 0; r < rounds; ++r) {
+        for (int t = 0; t < nm; ++t) {
+            const int j = (t + r) % nm;
+            if (status[j]) continue;
+            cudaEventRecord(ev[2 * j], stream);
+            for (int q = 0; q < reps[j] && !status[j]; ++q) {
+                status[j] = run_one(j, set);
+                set = (set + 1) % nsets;
+            }
+            cudaEventRecord(ev[2 * j + 1], stream);
+        }
+        if ((err = cudaStreamSynchronize(stream)) != cudaSuccess) {
+            for (auto &x : ev) cudaEventDestroy(x);
+            return cuda_err(err, "tuning round");
+        }
+        for (int j = 0; j < nm; ++j) {
+            if (status[j]) continue;
+            float ms = 0;
+            cudaEventElapsedTime(&ms, ev[2 * j], ev[2 * j + 1]);
+            times[j].push_back(ms * 1000.0 / reps[j]);
+        }
+    }
+    for (auto &x : ev) cudaEventDestroy(x);
+    for (int j = 0; j < nm; ++j)
+        if (!status[j]) status[j] = plan_status(plans[j]);
+
+    std::vector<int> ok_idx;
+    for (int j = 0; j < nm; ++j) {
+        gemm_tune_row &row = rows[meas[j]];
+        row.status = status[j];
+        if (status[j] || times[j].empty()) continue;
+        row.measured_us = median_of(times[j]);
+        row.measured_min_us = *std::min_element(times[j].begin(), times[j].end());
+        ok_idx.push_back(meas[j]);
+    }
+    if (ok_idx.empty()) return set_error(GEMM_ERR_CUDA, "no candidate could be timed");
+    std::stable_sort(ok_idx.begin(), ok_idx.end(), [&](int a, int b) {
+        if (rows[a].measured_us != rows[b].measured_us) return rows[a].measured_us < rows[b].measured_us;
+        return rows[a].model_rank < rows[b].model_rank;
+    });
+    for (size_t r = 0; r < ok_idx.size(); ++r) rows[ok_idx[r]].measured_rank = (int)r;
+    std::vector<double> pm, mm;
+    for (int i : ok_idx) {
+        pm.push_back(rows[i].predicted_us);
+        mm.push_back(rows[i].measured_us);
+    }
+    if (pm.size() >= 2) stats = rank_agreement(pm.data(), mm.data(), (int)pm.size());
+    stats.best_us = rows[ok_idx[0]].measured_us;
+    stats.fixed_us = (fixed_idx >= 0 && rows[fixed_idx].measured_us > 0) ? rows[fixed_idx].measured_us : -1.0;
+    stats.n_measured = (int)ok_idx.size();
+    stats.n_candidates = n;
+    if (winner) *winner = rows[ok_idx[0]].config;
+    // Rows ordered by measured time, unmeasured rows last (by model rank).
+    std::vector<gemm_tune_row> sorted;
+    for (int i : ok_idx) sorted.push_back(rows[i]);
+    std::vector<int> rest;
+    for (int i = 0; i < n; ++i)
+        if (rows[i].measured_rank < 0) rest.push_back(i);
+    std::stable_sort(rest.begin(), rest.end(), [&](int a, int b) { return rows[a].model_rank < rows[b].model_rank; });
+    for (int i : rest) sorted.push_back(rows[i]);
+    rows.swap(sorted);
+    stats.tune_seconds = std::chrono::duration<double>(std::chrono::steady_clock::now() - t_start).count();
+    return GEMM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Tune-once cache keyed by (M, N, K, dtype, epilogue, device name, SM count,
+// library version)
+// ---------------------------------------------------------------------------
+
+static std::mutex g_cache_mu;
+static std::map<std::string, gemm_config> g_cache;
+static int64_t g_tunes = 0, g_hits = 0;
+
+static std::string cache_key(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_device_params &dev)
+{
+    int d = 0;
+    cudaGetDevice(&d);
+    cudaDeviceProp prop;
+    memset(&prop, 0, sizeof(prop));
+    cudaGetDeviceProperties(&prop, d);
+    char buf[512];
+    snprintf(buf, sizeof(buf), "%lld|%lld|%lld|%d|%d|%s|%d|%s", (long long)M, (long long)N, (long long)K, dt, epi,
+             prop.name, dev.sm_count, GEMM_LIB_VERSION);
+    return buf;
+}
+
+int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out)
+{
+    *out = nullptr;
+    int rc = check_extents(M, N, K);
+    if (rc) return rc;
+    if (!valid_enums(dt, epi)) return set_error(GEMM_ERR_INVALID_ARG, "unknown dtype %d or epilogue %d", dt, epi);
+    if ((rc = check_device_arch(nullptr))) return rc;
+    gemm_device_params dev;
+    if ((rc = query_params(&dev))) return rc;
+    const char *dis = getenv("GEMM_DISABLE_AUTOTUNE");
+    if (dis && dis[0] == '1') return make_plan(M, N, K, dt, epi, fixed_config(dt, dev), dev, nullptr, out);
+    if (M == 0 || N == 0) return make_plan(M, N, K, dt, epi, fixed_config(dt, dev), dev, nullptr, out);
+    const std::string key = cache_key(M, N, K, dt, epi, dev);
+    gemm_config cfg;
+    {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        auto it = g_cache.find(key);
+        if (it != g_cache.end()) {
+            ++g_hits;
+            cfg = it->second;
+            return make_plan(M, N, K, dt, epi, cfg, dev, nullptr, out);
+        }
+    }
+    const char *mode = getenv("GEMM_TUNE_MODE");
+    const bool exhaustive = mode && strcmp(mode, "exhaustive") == 0;
+    const int topk = exhaustive ? 0 : std::max(1, env_int("GEMM_TUNE_TOPK", 12));
+    std::vector<gemm_tune_row> rows;
+    gemm_rank_stats stats;
+    rc = tune(M, N, K, dt, epi, topk, rows, stats, &cfg);
+    if (rc) return rc;
+    {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        ++g_tunes;
+        g_cache[key] = cfg;
+    }
+    return make_plan(M, N, K, dt, epi, cfg, dev, nullptr, out);
+}
+
+void cache_stats(int64_t *tunes, int64_t *hits, int64_t *entries)
+{
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    if (tunes) *tunes = g_tunes;
+    if (hits) *hits = g_hits;
+    if (entries) *entries = (int64_t)g_cache.size();
+}
+
+void cache_clear()
+{
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    g_cache.clear();
+    g_tunes = 0;
+    g_hits = 0;
+}
+
+int plan_explicit(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &cfg, gemm_plan_t *out)
+{
+    *out = nullptr;
+    int rc = check_device_arch(nullptr);
+    if (rc) return rc;
+    gemm_device_params dev;
+    if ((rc = query_params(&dev))) return rc;
+    return make_plan(M, N, K, dt, epi, cfg, dev, nullptr, out);
+}
+
+}  // namespace gemmgb

@@ -1,0 +1,302 @@
+/*
+ * gemm_gb300.h — C ABI of the autotuned tcgen05 GEMM library for GB300 (sm_103a).
+ *
+ * The library computes the fused tiled multiply
+ *
+ *     C[m,n] = act( sum_k A[m,k] · B[k,n] + bias[n] )
+ *
+ * with a tile configuration (BM, BN, BK, pipeline stages, tile order, split-K)
+ * chosen per problem shape, first by an analytical cost model and then by
+ * timing candidates on the device, and cached by shape.
+ *
+ * Sources (page title, section):
+ *   - "Tile Selection: Cost Models Against Measurement": the search space
+ *     ("The structure of the search space"), the analytical model ("Analytical
+ *     models and where they break"), measurement controls ("Measurement, and
+ *     what it must control"), the hybrid filter → rank → measure arrangement
+ *     ("Hybrid strategies"), the cache key (shape, dtype, device, library
+ *     version) and per-device selection ("Selection is per device").
+ *   - "Compilers and Kernel Languages": tiles run in waves of one per
+ *     multiprocessor; the workshop model; real kernels add pipeline depth,
+ *     split-K and tile order.
+ *   - "Autotuning & cost models": §4 tune on first call and cache by key;
+ *     §5 amortisation; §6 cost-model-guided search vs exhaustive.
+ *   - "CuTile Autotuning" (tune-once / cache / launch pattern; the search space
+ *     includes the original fixed configuration; split buffers while tuning).
+ *   - "Tiling the hierarchy": stages hide load latency; the epilogue fused onto
+ *     a GEMM is nearly free.
+ *
+ * Conventions for every entry point:
+ *   - Matrices are row-major and dense: A is [M,K], B is [K,N], C is [M,N];
+ *     bias is a length-N vector added to every row (the pages do not define
+ *     "bias"; this is the plain reading of C = act(A·B + bias)).
+ *   - GEMM_BF16: A, B, bias and C are bfloat16; products accumulate in fp32 in
+ *     tensor memory; C is rounded to nearest-even once.  GEMM_FP32_TF32: A, B,
+ *     bias and C are fp32; the tensor cores read the operands as TF32.
+ *   - GELU is the erf form 0.5·x·(1 + erf(x/√2)).
+ *   - Device pointers are caller-owned, must stay valid until the work queued
+ *     on the stream has finished, and must be 16-byte aligned; K·elt and N·elt
+ *     must be multiples of 16 bytes (TMA row-stride rule).
+ *   - Every function returns GEMM_OK (0) or a negative gemm_status; the text of
+ *     the last error of the calling thread is returned by gemm_last_error().
+ *     Nothing aborts, traps or exits the process.
+ *   - Extents are int64_t; M, N, K must be >= 0 and < 2^31.  M == 0 or
+ *     N == 0 is a no-op; K == 0 gives C = act(bias) (empty sum).
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st *gemm_stream_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = -1,  /* null pointer, negative extent, unknown enum */
+    GEMM_ERR_MISALIGNED = -2,   /* pointer not 16-byte aligned or row stride not a multiple of 16 B */
+    GEMM_ERR_UNSUPPORTED = -3,  /* no feasible configuration / not an sm_100-family GPU */
+    GEMM_ERR_INFEASIBLE = -4,   /* an explicit configuration breaks a hardware rule */
+    GEMM_ERR_CUDA = -5,         /* a CUDA runtime/driver call failed (text in gemm_last_error) */
+    GEMM_ERR_TIMEOUT = -6,      /* a device wait ran past its limit; the kernel returned early */
+    GEMM_ERR_NO_DEVICE = -7     /* no CUDA device is visible */
+} gemm_status;
+
+typedef enum { GEMM_BF16 = 0, GEMM_FP32_TF32 = 1 } gemm_dtype;
+
+typedef enum {
+    GEMM_EPI_NONE = 0,       /* C = A·B                 (bias may be NULL) */
+    GEMM_EPI_BIAS = 1,       /* C = A·B + bias          */
+    GEMM_EPI_BIAS_RELU = 2,  /* C = max(A·B + bias, 0)  */
+    GEMM_EPI_BIAS_GELU = 3   /* C = gelu(A·B + bias)    */
+} gemm_epilogue;
+
+/*
+ * One tile configuration ("Tile Selection", "The structure of the search
+ * space": block tile, reduction step; "Compilers and Kernel Languages": pipeline
+ * depth, split-K, tile order).  bm × bn is the tile of the MMA output: with
+ * swap_ab = 0 it tiles C (bm rows of M, bn columns of N); with swap_ab = 1 the
+ * kernel computes Cᵀ = Bᵀ·Aᵀ, so bm tiles N and bn tiles M (small-M decode).
+ *   bm        128 or 256 (tcgen05 M = 128 per CTA; 256 = two stacked MMAs)
+ *   bn        16..256, multiple of 16 (swap) / of 32 and of the 128-byte span
+ *             (64 bf16, 32 fp32) when B is the MN-major operand (no swap)
+ *   bk        K per pipeline stage: 1..4 spans of 128 bytes (64/128/192/256 bf16)
+ *   stages    2..16 shared-memory ring slots
+ *   raster    0: tiles walk a band of `group` tile-rows column by column;
+ *             1: a band of `group` tile-columns row by row
+ *   group     1, 2, 4, 8 or 16
+ *   split_k   1..16 slices of K; partial fp32 tiles are summed in slice order
+ *             (deterministic) by the last slice to finish
+ *   cta_group 1 (2-SM pairs are not offered yet)
+ *   swap_ab   0 or 1, as above
+ */
+typedef struct {
+    int32_t bm, bn, bk, stages, raster, group, split_k, cta_group, swap_ab;
+} gemm_config;
+
+/* Reason codes of gemm_check_config (first rule broken, in this order). */
+typedef enum {
+    GEMM_FEASIBLE = 0,
+    GEMM_REASON_CTA_GROUP = 1,  /* cta_group != 1 */
+    GEMM_REASON_UMMA_M = 2,     /* bm not 128/256 (tcgen05 M per CTA is 128) */
+    GEMM_REASON_UMMA_N = 3,     /* bn not a multiple of 16 in [16, 256] */
+    GEMM_REASON_LAYOUT = 4,     /* swap_ab not 0/1; bn not a multiple of 32 and of the span when unswapped */
+    GEMM_REASON_BK = 5,         /* bk not 1..4 spans of 128 bytes */
+    GEMM_REASON_STAGES = 6,     /* stages outside 2..16 */
+    GEMM_REASON_SCHEDULE = 7,   /* raster not 0/1 or group not in {1,2,4,8,16} */
+    GEMM_REASON_SPLIT_K = 8,    /* split_k outside 1..16 or above ceil(K/bk) */
+    GEMM_REASON_ALIGN = 9,      /* K·elt or N·elt not a multiple of 16 bytes */
+    GEMM_REASON_TMEM = 10,      /* one accumulator needs more than 512 TMEM columns */
+    GEMM_REASON_SMEM = 11,      /* ring + epilogue staging + barriers exceed the per-block limit */
+    GEMM_REASON_REGS = 12       /* kernel registers × 192 threads exceed 65,536 */
+} gemm_reason;
+
+/*
+ * Device and cost-model parameters ("Tile Selection", "Selection is per device":
+ * the SM count and the limits are properties of the device; never hard-coded).
+ * gemm_device_params_query fills it from the current device; the model
+ * coefficients start from the nominal values listed in the comments and may be
+ * overridden by the caller (e.g. with measured peaks).
+ */
+typedef struct {
+    int32_t sm_count;               /* multiprocessors */
+    int32_t model_kind;             /* 0 = tcgen05 model; 1 = the workshop model of
+                                       "Compilers and Kernel Languages" */
+    int64_t smem_per_block;         /* opt-in dynamic shared memory per block, bytes */
+    int64_t l2_bytes;
+    double  peak_tflops_bf16;       /* dense tensor peak */
+    double  peak_tflops_tf32;
+    double  hbm_gbs;                /* DRAM bandwidth, GB/s */
+    double  sm_clock_mhz;
+    double  mma_flops_per_clk_bf16; /* per SM (nominal 8192) */
+    double  mma_flops_per_clk_tf32; /* per SM (nominal 4096) */
+    double  smem_bytes_per_clk;     /* per SM operand bandwidth feeding the MMA (128) */
+    double  mem_latency_us;         /* load round trip, for the fill and bytes-in-flight terms */
+    double  epi_elems_per_clk;      /* per SM accumulators drained by the epilogue per clock */
+    double  launch_us;              /* fixed launch + teardown cost */
+    int32_t kernel_regs;            /* registers/thread of the GEMM kernel (0 = unknown) */
+    int32_t threads_per_cta;        /* 192 */
+} gemm_device_params;
+
+/* Terms of one cost-model prediction (times in microseconds). */
+typedef struct {
+    double predicted_us, compute_us, memory_us, latency_us, epilogue_us, fill_us;
+    double wave_eff, tile_eff, pad_eff;
+    double hbm_bytes, flops;
+    int64_t tiles, units, waves, ctas;
+} gemm_model_terms;
+
+/* One row of a tuning table. */
+typedef struct {
+    gemm_config config;
+    double predicted_us;     /* cost model */
+    double measured_us;      /* median over interleaved rounds (< 0: not measured) */
+    double measured_min_us;  /* fastest round */
+    int32_t model_rank;      /* 0-based rank by predicted_us */
+    int32_t measured_rank;   /* 0-based rank by measured_us (-1: not measured) */
+    int32_t status;          /* GEMM_OK, or the error the candidate returned */
+    int32_t reserved;
+} gemm_tune_row;
+
+/* How well the model's ordering agreed with measurement over the measured rows
+ * ("Autotuning & cost models", §6). */
+typedef struct {
+    double kendall_tau;      /* τ_b */
+    double spearman_rho;
+    double regret;           /* measured(model's pick) / measured(best) - 1 */
+    double tune_seconds;     /* wall time of the search */
+    double best_us;          /* measured time of the winner */
+    double fixed_us;         /* measured time of the fixed 128x128 config (< 0 if absent) */
+    int32_t top1_hit;        /* model's first choice was the measured fastest */
+    int32_t n_measured;
+    int32_t n_candidates;
+    int32_t reserved;
+} gemm_rank_stats;
+
+typedef struct gemm_plan_s *gemm_plan_t;  /* opaque, library-owned */
+
+/* ---------------------------------------------------------------------------
+ * Host logic (no GPU needed)
+ * ------------------------------------------------------------------------- */
+
+/* Library version string (part of the cache key). */
+const char *gemm_version(void);
+
+/* Text of the calling thread's last error ("" if none).  Owned by the library. */
+const char *gemm_last_error(void);
+
+/* Nominal GB300 parameters (152 SMs, 227 KB, 126 MB L2, nominal peaks).  Used
+ * on machines without a GPU and as the base that _query refines. */
+void gemm_device_params_default(gemm_device_params *out);
+
+/* The workshop device of "Compilers and Kernel Languages" (H100: 132 SMs, 228 KB,
+ * 989 TFLOP/s BF16, 3.35 TB/s) with model_kind = 1. */
+void gemm_device_params_workshop(gemm_device_params *out);
+
+/* Feasibility of `cfg` for the problem: GEMM_FEASIBLE or a gemm_reason (> 0);
+ * GEMM_ERR_INVALID_ARG (< 0) for null pointers or bad enums. */
+int gemm_check_config(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
+                      const gemm_config *cfg, const gemm_device_params *dev);
+
+/* The candidate set for the problem ("Tile Selection", "Hybrid strategies":
+ * the resource filter).  Writes up to `cap` feasible configs in generation
+ * order to out (out may be NULL when cap == 0) and the total count to *n. */
+int gemm_enumerate(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
+                   const gemm_device_params *dev, gemm_config *out, int32_t cap, int32_t *n);
+
+/* The fixed, untuned configuration (128×128 tile, one K span, as many stages as
+ * fit, row-major order, no split): the baseline tuning must never lose to. */
+int gemm_fixed_config(gemm_dtype dtype, const gemm_device_params *dev, gemm_config *out);
+
+/* Cost-model prediction for one configuration ("Tile Selection", "Analytical
+ * models and where they break"; "Compilers and Kernel Languages", workshop). */
+int gemm_model_predict(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
+                       const gemm_config *cfg, const gemm_device_params *dev,
+                       gemm_model_terms *out);
+
+/* Rank agreement of two equal-length arrays (n >= 2): τ_b, ρ, top-1, regret. */
+int gemm_rank_agreement(const double *predicted, const double *measured, int32_t n,
+                        gemm_rank_stats *out);
+
+/* The persistent schedule's map of work unit u to its tile and K slice (the
+ * same function the kernel runs).  Outputs may be NULL. */
+int gemm_schedule_unit(int64_t unit, int32_t tiles_m, int32_t tiles_n, int32_t split_k,
+                       int32_t raster, int32_t group, int32_t num_kb,
+                       int32_t *tile_m, int32_t *tile_n, int32_t *split,
+                       int32_t *kb_begin, int32_t *kb_end);
+
+/* ---------------------------------------------------------------------------
+ * Device entry points (current CUDA device)
+ * ------------------------------------------------------------------------- */
+
+/* Parameters of the current device: SM count, shared-memory limit, L2 size,
+ * clock and the GEMM kernel's register count, on top of the defaults. */
+int gemm_device_params_query(gemm_device_params *out);
+
+/* Plan a GEMM: cache lookup by (M, N, K, dtype, epilogue, device name, SM count,
+ * library version); on a miss, enumerate → rank by the model → time the top
+ * candidates on library-owned buffers → cache the winner ("Autotuning & cost
+ * models" §4; "CuTile Autotuning").  Environment: GEMM_DISABLE_AUTOTUNE=1 picks
+ * the fixed config without timing; GEMM_TUNE_MODE=exhaustive|topk (default
+ * topk); GEMM_TUNE_TOPK=k (default 12).  Synchronises; never touches user
+ * memory.  The returned handle is owned by the caller (gemm_plan_destroy) and
+ * may be used on one stream at a time. */
+int gemm_plan(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
+              gemm_plan_t *out);
+
+/* Plan with an explicit configuration (no tuning, no cache).  Returns
+ * GEMM_ERR_INFEASIBLE, with the reason in gemm_last_error, if it breaks a rule. */
+int gemm_plan_with_config(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
+                          const gemm_config *cfg, gemm_plan_t *out);
+
+/* The configuration a plan runs. */
+int gemm_plan_config(gemm_plan_t plan, gemm_config *out);
+
+/* Enqueue C = act(A·B + bias) on `stream` (asynchronous).  A, B, bias, C are
+ * device pointers as described above; bias may be NULL only with
+ * GEMM_EPI_NONE.  A split-K plan uses its own workspace, so one plan must not
+ * run on two streams at once. */
+int gemm_run(gemm_plan_t plan, const void *A, const void *B, const void *bias, void *C,
+             gemm_stream_t stream);
+
+/* Same product from HOST buffers: copies A, B, bias to plan-owned device
+ * buffers, runs, copies C back, and synchronises `stream` before returning.
+ * Host buffers should be pinned for full copy bandwidth. */
+int gemm_run_host(gemm_plan_t plan, const void *A, const void *B, const void *bias, void *C,
+                  gemm_stream_t stream);
+
+/* Synchronise and read the plan's device status word: GEMM_OK or
+ * GEMM_ERR_TIMEOUT (a bounded wait expired; the status is cleared and the
+ * split-K counters reset so the plan can run again). */
+int gemm_plan_status(gemm_plan_t plan);
+
+void gemm_plan_destroy(gemm_plan_t plan);
+
+/* Exhaustively time every feasible candidate (or the model's top `topk` when
+ * topk > 0) and fill `rows` (up to cap, ordered by measured time, unmeasured
+ * rows last) and `stats`.  *n_rows receives the number of rows written. */
+int gemm_tune(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
+              int32_t topk, gemm_tune_row *rows, int32_t cap, int32_t *n_rows,
+              gemm_rank_stats *stats);
+
+/* Tune-once cache: number of searches run, lookups served, entries held. */
+int gemm_cache_stats(int64_t *tunes, int64_t *hits, int64_t *entries);
+void gemm_cache_clear(void);
+
+/* Debug controls of the device waits.  what = 0: wait limit in nanoseconds
+ * (default 2e9; every mbarrier wait in the kernel gives up after it, sets the
+ * status word and returns); what = 1: make the epilogue wait on a barrier that
+ * nothing signals (1 = on, 0 = off) so that the timeout path can be tested.
+ * Affects launches made after the call, from any thread. */
+int gemm_debug_set(int32_t what, int64_t value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */

@@ -1,0 +1,213 @@
+"""GPU parity of the tcgen05 GEMM against the fp64 oracle, through the C ABI.
+
+Bars: bit-exact on small-integer inputs (sums exact in fp32; the output is the
+exact value rounded once, so the device result and the oracle's rounding of
+the exact value must have identical bits); normalised error
+max |C - C_ref| / (||a_i||·||b_j||) <= 2e-3 on random inputs."""
+import numpy as np
+import pytest
+import torch
+
+import autotuning_tcgen05_tmem_gb300 as g
+from autotuning_tcgen05_tmem_gb300 import inputs
+from gpu_util import (TOL, alloc_out, device_bits, normalised_error, operands, oracle_rounded_bits,
+                      run_config, sampled_error)
+
+pytestmark = pytest.mark.gpu
+
+C = g.make_config
+
+# (M, N, K) ragged against every tile size used below; configs cover both tile
+# heights, every bn class, 1-4 K spans, shallow and deep rings, both rasters,
+# grouping, split-K and the swapped (small-M) orientation.
+BF16_CASES = [
+    ((300, 320, 520), C(128, 128, 64, 4)),
+    ((300, 320, 520), C(128, 64, 64, 6)),
+    ((300, 320, 520), C(128, 192, 64, 4)),
+    ((300, 320, 520), C(128, 256, 64, 3)),
+    ((300, 320, 520), C(256, 128, 64, 3)),
+    ((300, 320, 520), C(256, 64, 128, 3)),
+    ((300, 320, 520), C(128, 128, 128, 4)),
+    ((300, 320, 520), C(128, 64, 256, 2)),
+    ((300, 320, 520), C(128, 128, 64, 2, 1, 2)),
+    ((520, 640, 264), C(128, 64, 64, 4, 0, 4)),
+    ((520, 640, 264), C(128, 128, 64, 4, 1, 16)),
+    ((300, 320, 520), C(128, 128, 64, 4, 0, 1, 3)),
+    ((300, 320, 520), C(256, 256, 64, 2, 0, 1, 4)),
+    ((20, 320, 520), C(128, 16, 64, 6, 0, 1, 1, 1, 1)),
+    ((20, 320, 520), C(128, 32, 64, 6, 0, 1, 2, 1, 1)),
+    ((40, 264, 520), C(256, 64, 128, 3, 0, 1, 3, 1, 1)),
+    ((16, 1024, 1024), C(128, 16, 64, 8, 0, 1, 8, 1, 1)),
+]
+
+FP32_CASES = [
+    ((200, 160, 136), C(128, 32, 32, 4)),
+    ((200, 160, 136), C(128, 128, 32, 4)),
+    ((200, 160, 136), C(256, 64, 64, 3)),
+    ((200, 160, 136), C(128, 96, 128, 2)),
+    ((200, 160, 136), C(128, 64, 32, 4, 0, 1, 2)),
+    ((24, 160, 136), C(128, 16, 32, 4, 0, 1, 1, 1, 1)),
+    ((24, 160, 136), C(128, 32, 64, 4, 0, 1, 3, 1, 1)),
+]
+
+
+def _cases_id(c):
+    (M, N, K), cfg = c
+    return f"{M}x{N}x{K}-{'x'.join(str(v) for v in cfg.astuple())}"
+
+
+@pytest.mark.parametrize("case", BF16_CASES, ids=_cases_id)
+@pytest.mark.parametrize("epi", ["relu", "none"])
+def test_bf16_integer_inputs_bit_exact(case, epi):
+    (M, N, K), cfg = case
+    A, B, bias = operands(M, N, K, "bf16", "int", seed=3)
+    out, guard_ok = run_config(A, B, bias, epi, cfg)
+    assert guard_ok, "write outside C"
+    want = oracle_rounded_bits(A, B, bias, epi, g.BF16)
+    got = device_bits(out)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
+
+
+@pytest.mark.parametrize("case", FP32_CASES, ids=_cases_id)
+def test_fp32_integer_inputs_bit_exact(case):
+    (M, N, K), cfg = case
+    A, B, bias = operands(M, N, K, "fp32", "int", seed=4)
+    out, guard_ok = run_config(A, B, bias, "relu", cfg)
+    assert guard_ok
+    want = oracle_rounded_bits(A, B, bias, "relu", g.FP32_TF32)
+    bad = np.argwhere(device_bits(out) != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
+
+
+@pytest.mark.parametrize("case", BF16_CASES[::2], ids=_cases_id)
+@pytest.mark.parametrize("epi", ["none", "bias", "relu", "gelu"])
+def test_bf16_random_within_tolerance(case, epi):
+    (M, N, K), cfg = case
+    A, B, bias = operands(M, N, K, "bf16", "scaled_normal", seed=5)
+    out, guard_ok = run_config(A, B, bias, epi, cfg)
+    assert guard_ok
+    assert normalised_error(out, A, B, bias, epi) <= TOL
+
+
+@pytest.mark.parametrize("case", FP32_CASES, ids=_cases_id)
+@pytest.mark.parametrize("epi", ["bias", "gelu"])
+def test_fp32_random_within_tolerance(case, epi):
+    (M, N, K), cfg = case
+    A, B, bias = operands(M, N, K, "fp32", "uniform", seed=6)
+    out, guard_ok = run_config(A, B, bias, epi, cfg)
+    assert guard_ok
+    assert normalised_error(out, A, B, bias, epi) <= TOL
+
+
+def test_every_candidate_of_the_256_cube_integer_fp32_relu():
+    """Every feasible configuration the generator offers for the 256³ fp32
+    ReLU workload is bit-exact on its integer variant."""
+    w = inputs.WORKLOADS["fp32_relu_256_int"]
+    A, B, bias = inputs.make_workload(w, seed=0)
+    dev = g.device_params_query()
+    cands = g.enumerate_configs(w.M, w.N, w.K, "fp32", "relu", dev)
+    assert len(cands) > 50
+    want = oracle_rounded_bits(A, B, bias, "relu", g.FP32_TF32)
+    Ad, Bd, bd = A.cuda(), B.cuda(), bias.cuda()
+    for cfg in cands:
+        Cd, _ = alloc_out(w.M, w.N, g.FP32_TF32)
+        with g.plan_with_config(w.M, w.N, w.K, "fp32", "relu", cfg) as p:
+            p.run(Ad, Bd, bd, Cd)
+            assert p.status() == 0, (cfg, g.last_error())
+        assert np.array_equal(device_bits(Cd.cpu()), want), cfg
+
+
+def test_split_k_is_deterministic():
+    A, B, bias = operands(257, 384, 4096, "bf16", "scaled_normal", seed=8)
+    cfg = C(128, 128, 64, 4, 0, 1, 6)
+    a, _ = run_config(A, B, bias, "gelu", cfg)
+    b, _ = run_config(A, B, bias, "gelu", cfg)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert normalised_error(a, A, B, bias, "gelu") <= TOL
+
+
+# --- full-size workloads, sampled against the oracle ------------------------------
+
+@pytest.mark.parametrize("name", ["bf16_gelu_1000x1000x8192", "bf16_decode_16x8192x28672",
+                                  "bf16_relu_8192", "fp32_relu_256"])
+def test_full_size_tuned_plan_sampled(name):
+    w = inputs.WORKLOADS[name]
+    A, B, bias = inputs.make_workload(w, seed=0)
+    with g.plan(w.M, w.N, w.K, w.dtype, w.epi) as p:
+        Cd, _ = alloc_out(w.M, w.N, g.DTYPES[w.dtype])
+        p.run(A.cuda(), B.cuda(), bias.cuda() if bias is not None else None, Cd)
+        assert p.status() == 0, g.last_error()
+    err = sampled_error(Cd.cpu(), A, B, bias, w.epi, n=4096)
+    assert err <= TOL, (p.config, err)
+
+
+def test_sweep_shapes_sampled():
+    """A slice of the 30-shape transformer sweep through tuned plans."""
+    for w in inputs.SWEEP[::7]:
+        A, B, bias = inputs.make_workload(w, seed=1)
+        with g.plan(w.M, w.N, w.K, w.dtype, w.epi) as p:
+            Cd, _ = alloc_out(w.M, w.N, g.BF16)
+            p.run(A.cuda(), B.cuda(), bias.cuda(), Cd)
+            assert p.status() == 0
+        assert sampled_error(Cd.cpu(), A, B, bias, w.epi, n=1024) <= TOL, w.name
+
+
+# --- edge cases ---------------------------------------------------------------------
+
+def test_tiny_and_degenerate_extents():
+    for (M, N, K) in [(1, 8, 8), (1, 8, 64), (129, 8, 8), (7, 24, 16)]:
+        A, B, bias = operands(M, N, K, "bf16", "int", seed=9)
+        out, ok = run_config(A, B, bias, "relu", C(128, 64, 64, 2))
+        assert ok and np.array_equal(device_bits(out), oracle_rounded_bits(A, B, bias, "relu", g.BF16))
+
+
+def test_k_zero_gives_act_of_bias():
+    M, N = 70, 96
+    bias = torch.arange(N, dtype=torch.float32).sub(48).div(8).to(torch.bfloat16)
+    A = torch.empty(M, 0, dtype=torch.bfloat16)
+    B = torch.empty(0, N, dtype=torch.bfloat16)
+    Cd, _ = alloc_out(M, N, g.BF16)
+    with g.plan_with_config(M, N, 0, "bf16", "relu", C(128, 64, 64, 2)) as p:
+        p.run(None, None, bias.cuda(), Cd)
+        assert p.status() == 0
+    want = torch.relu(bias.float()).to(torch.bfloat16).expand(M, N)
+    assert torch.equal(Cd.cpu(), want)
+
+
+def test_empty_output_is_a_no_op():
+    Cd, buf = alloc_out(0, 64, g.BF16, guard=64)
+    with g.plan_with_config(0, 64, 64, "bf16", "none", C(128, 64, 64, 2)) as p:
+        p.run(None, None, None, Cd)
+    torch.cuda.synchronize()
+    assert (buf == 12345.0).all()
+
+
+def test_error_codes():
+    cfg = C(128, 128, 64, 4)
+    rc, _ = g.plan_with_config_rc(128, 128, 72 + 3, "bf16", "none", cfg)  # K·2 not a multiple of 16
+    assert rc == g.ERR_MISALIGNED
+    rc, _ = g.plan_with_config_rc(128, 128, 128, "bf16", "none", C(64, 128, 64, 4))
+    assert rc == g.ERR_INFEASIBLE and "bm" in g.last_error()
+    rc, _ = g.plan_with_config_rc(-1, 128, 128, "bf16", "none", cfg)
+    assert rc == g.ERR_INVALID_ARG
+    A, B, bias = operands(128, 128, 128, "bf16", "int")
+    Ad, Bd = A.cuda(), B.cuda()
+    Cd, _ = alloc_out(128, 128, g.BF16)
+    with g.plan_with_config(128, 128, 128, "bf16", "relu", cfg) as p:
+        assert p.run_rc(Ad, Bd, None, Cd) == g.ERR_INVALID_ARG           # bias required
+        raw = torch.empty(128 * 128 + 8, dtype=torch.bfloat16, device="cuda")
+        assert p.run_rc(Ad, Bd, bias.cuda(), raw[1:]) == g.ERR_MISALIGNED  # C not 16-byte aligned
+        assert p.run_rc(Ad, None, bias.cuda(), Cd) == g.ERR_INVALID_ARG
+        p.run(Ad, Bd, bias.cuda(), Cd)
+        assert p.status() == 0
+
+
+def test_run_host_matches_run():
+    A, B, bias = operands(200, 192, 512, "bf16", "scaled_normal", seed=11)
+    cfg = C(128, 64, 64, 4, 0, 1, 2)
+    dev_out, _ = run_config(A, B, bias, "gelu", cfg)
+    host_out = torch.empty(200, 192, dtype=torch.bfloat16).pin_memory()
+    with g.plan_with_config(200, 192, 512, "bf16", "gelu", cfg) as p:
+        p.run_host(A.pin_memory(), B.pin_memory(), bias.pin_memory(), host_out)
+    assert torch.equal(dev_out.view(torch.int16), host_out.view(torch.int16))
