@@ -32,6 +32,7 @@ void clear_error() { t_last_error.clear(); }
 // runtime.cpp
 extern std::atomic<int64_t> g_timeout_ns;
 extern std::atomic<int32_t> g_debug_stall;
+extern std::atomic<int32_t> g_b_route;
 int query_params(gemm_device_params *d);
 int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out);
 int plan_explicit(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &cfg, gemm_plan_t *out);
@@ -217,6 +218,11 @@ int gemm_debug_set(int32_t what, int64_t value)
     }
     if (what == 1) {
         g_debug_stall.store(value ? 1 : 0);
+        return GEMM_OK;
+    }
+    if (what == 2) {
+        if (value < 0 || value > 2) return set_error(GEMM_ERR_INVALID_ARG, "B route must be 0, 1 or 2");
+        g_b_route.store((int32_t)value);
         return GEMM_OK;
     }
     return set_error(GEMM_ERR_INVALID_ARG, "unknown debug control %d", what);

@@ -57,6 +57,7 @@ cudaError_t kernel_attributes(int dt, int *num_regs, int *max_threads);
 cudaError_t set_kernel_smem_limit(int dt, int bytes);
 cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
                         const KernelParams &p, int grid, int smem_bytes, cudaStream_t stream);
+cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t cols, int elt, cudaStream_t stream);
 cudaError_t launch_fill_uniform(void *dst, int64_t n, int dt, float scale, uint32_t seed,
                                 cudaStream_t stream);
 

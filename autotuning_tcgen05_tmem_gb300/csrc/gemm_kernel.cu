@@ -811,6 +811,28 @@ __global__ void fill_uniform_kernel(void *dst, int64_t n, int dt, float scale, u
     }
 }
 
+// Row-major [rows, cols] -> row-major [cols, rows] through 32x32 shared-memory
+// tiles, so that both the reads and the writes are coalesced.  Used to give the
+// tensor cores a K-major copy of B when B must not be read MN-major.
+template <typename T>
+__global__ void transpose_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t rows, int64_t cols)
+{
+    __shared__ T tile[32][33];
+    const int64_t c0 = (int64_t)blockIdx.x * 32;
+    for (int64_t r0 = (int64_t)blockIdx.y * 32; r0 < rows; r0 += (int64_t)gridDim.y * 32) {
+        for (int i = threadIdx.y; i < 32; i += 8) {
+            const int64_t r = r0 + i, c = c0 + threadIdx.x;
+            if (r < rows && c < cols) tile[i][threadIdx.x] = src[r * cols + c];
+        }
+        __syncthreads();
+        for (int i = threadIdx.y; i < 32; i += 8) {
+            const int64_t c = c0 + i, r = r0 + threadIdx.x;
+            if (c < cols && r < rows) dst[c * rows + r] = tile[threadIdx.x][i];
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -839,6 +861,21 @@ cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, cons
 {
     if (dt == 0) gemm_tcgen05_kernel<0><<<grid, 192, smem_bytes, stream>>>(a, b, c, p);
     else gemm_tcgen05_kernel<1><<<grid, 192, smem_bytes, stream>>>(a, b, c, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t cols, int elt, cudaStream_t stream)
+{
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const int64_t gy = (rows + 31) / 32;
+    const dim3 grid((unsigned)((cols + 31) / 32), (unsigned)(gy < 65535 ? gy : 65535));
+    const dim3 block(32, 8);
+    if (elt == 2)
+        transpose_kernel<uint16_t><<<grid, block, 0, stream>>>(static_cast<const uint16_t *>(src),
+                                                               static_cast<uint16_t *>(dst), rows, cols);
+    else
+        transpose_kernel<uint32_t><<<grid, block, 0, stream>>>(static_cast<const uint32_t *>(src),
+                                                               static_cast<uint32_t *>(dst), rows, cols);
     return cudaGetLastError();
 }
 

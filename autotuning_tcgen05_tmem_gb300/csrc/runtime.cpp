@@ -33,6 +33,9 @@ namespace gemmgb {
 
 std::atomic<int64_t> g_timeout_ns{2000000000LL};
 std::atomic<int32_t> g_debug_stall{0};
+// How B reaches the tensor cores: 0 = by dtype (bf16 read MN-major in place,
+// fp32 transposed to a K-major copy), 1 = always transposed, 2 = always MN-major.
+std::atomic<int32_t> g_b_route{0};
 
 // ---------------------------------------------------------------------------
 // TMA descriptor encoding through the driver entry point
@@ -158,6 +161,8 @@ struct gemm_plan_s {
     std::vector<DescEntry> descs = std::vector<DescEntry>(16);
     int next_desc = 0;
     void *hA = nullptr, *hB = nullptr, *hBias = nullptr, *hC = nullptr;  // device buffers for run_host
+    bool b_kmajor = false;           // B is first transposed into bt ([N, K], K contiguous)
+    void *bt = nullptr;
 };
 
 namespace gemmgb {
@@ -191,6 +196,8 @@ static int check_extents(int64_t M, int64_t N, int64_t K)
                          (long long)N, (long long)K);
     return GEMM_OK;
 }
+
+void destroy_plan(gemm_plan_t p);
 
 // Builds a plan; `shared_ws` (may be null) is a caller-owned split-K workspace
 // of at least the needed size (used while tuning many candidates).
@@ -237,8 +244,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     k.num_units = (int32_t)(p->tiles * cfg.split_k);
     k.swap_ab = cfg.swap_ab;
     k.epi = epi;
-    k.a_mn_major = cfg.swap_ab ? 1 : 0;   // MMA-A is user B (N-contiguous) when swapped
-    k.b_mn_major = cfg.swap_ab ? 0 : 1;   // MMA-B is user B (N-contiguous) when not swapped
+    const int route = g_b_route.load();
+    p->b_kmajor = route == 1 || (route == 0 && dt == GEMM_FP32_TF32);
+    // User B is N-contiguous (MN-major) unless it is first transposed.  It is
+    // MMA-A when swapped and MMA-B otherwise; A is always K-major.
+    k.a_mn_major = (cfg.swap_ab && !p->b_kmajor) ? 1 : 0;
+    k.b_mn_major = (!cfg.swap_ab && !p->b_kmajor) ? 1 : 0;
     const uint32_t fmt = dt == GEMM_BF16 ? 1u : 2u;  // BF16 (kind::f16) / TF32 (kind::tf32)
     k.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)k.a_mn_major << 15) |
               ((uint32_t)k.b_mn_major << 16) | ((uint32_t)(cfg.bn >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
@@ -288,11 +299,16 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
         }
     }
     k.workspace = p->workspace;
+    if (p->b_kmajor && K > 0 && N > 0) {
+        e = cudaMalloc(&p->bt, (size_t)K * (size_t)N * elt_bytes(dt));
+        if (e != cudaSuccess) {
+            destroy_plan(p);
+            return cuda_err(e, "cudaMalloc(K-major copy of B)");
+        }
+    }
     rc = configure_smem_limit(dt, dev.smem_per_block);
     if (rc) {
-        if (p->owns_workspace) cudaFree(p->workspace);
-        cudaFree(p->aux);
-        delete p;
+        destroy_plan(p);
         return rc;
     }
     *out = p;
@@ -309,6 +325,7 @@ static size_t split_ws_bytes(int64_t M, int64_t N, const gemm_config &c)
 void destroy_plan(gemm_plan_t p)
 {
     if (!p) return;
+    cudaFree(p->bt);
     if (p->owns_workspace) cudaFree(p->workspace);
     cudaFree(p->aux);
     cudaFree(p->hA);
@@ -335,17 +352,21 @@ static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const
     memset(&d.ma, 0, sizeof(d.ma));
     memset(&d.mb, 0, sizeof(d.mb));
     if (p->K > 0) {
-        if (!c.swap_ab) {
-            rc = encode_2d(&d.ma, dt, A, p->K, p->M, span, c.bm, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-            if (!rc)
-                rc = encode_2d(&d.mb, dt, B, p->N, p->K, span, c.bk, CU_TENSOR_MAP_SWIZZLE_128B,
+        // A: [M, K] K-major, box [MMA extent x one span of K].
+        // B: [K, N] read MN-major (box [bk x one span of N]) or its transposed
+        //    copy [N, K] read K-major (box [MMA extent x one span of K]).
+        const uint32_t a_rows = c.swap_ab ? c.bn : c.bm;      // A's extent in the MMA
+        const uint32_t b_rows = c.swap_ab ? c.bm : c.bn;      // B's extent in the MMA
+        CUtensorMap *am = c.swap_ab ? &d.mb : &d.ma;
+        CUtensorMap *bm = c.swap_ab ? &d.ma : &d.mb;
+        rc = encode_2d(am, dt, A, p->K, p->M, span, a_rows, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        if (!rc) {
+            if (p->b_kmajor)
+                rc = encode_2d(bm, dt, p->bt, p->K, p->N, span, b_rows, CU_TENSOR_MAP_SWIZZLE_128B,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-        } else {
-            rc = encode_2d(&d.ma, dt, B, p->N, p->K, span, c.bk, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-            if (!rc)
-                rc = encode_2d(&d.mb, dt, A, p->K, p->M, span, c.bn, CU_TENSOR_MAP_SWIZZLE_128B,
+            else
+                rc = encode_2d(bm, dt, B, p->N, p->K, span, c.bk, CU_TENSOR_MAP_SWIZZLE_128B,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         }
     }
@@ -385,6 +406,10 @@ int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void
     const DescEntry *d = nullptr;
     int rc = get_descs(p, A, B, C, &d);
     if (rc) return rc;
+    if (p->b_kmajor && p->K > 0) {
+        cudaError_t te = launch_transpose(B, p->bt, p->K, p->N, elt_bytes(p->dt), stream);
+        if (te != cudaSuccess) return cuda_err(te, "transpose launch");
+    }
     KernelParams kp = p->kp;
     kp.bias = p->epi != GEMM_EPI_NONE ? bias : nullptr;
     kp.timeout_ns = g_timeout_ns.load();

@@ -288,11 +288,14 @@ int gemm_tune(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue e
 int gemm_cache_stats(int64_t *tunes, int64_t *hits, int64_t *entries);
 void gemm_cache_clear(void);
 
-/* Debug controls of the device waits.  what = 0: wait limit in nanoseconds
- * (default 2e9; every mbarrier wait in the kernel gives up after it, sets the
- * status word and returns); what = 1: make the epilogue wait on a barrier that
- * nothing signals (1 = on, 0 = off) so that the timeout path can be tested.
- * Affects launches made after the call, from any thread. */
+/* Debug controls.  what = 0: wait limit in nanoseconds (default 2e9; every
+ * mbarrier wait in the kernel gives up after it, sets the status word and
+ * returns); what = 1: make the epilogue wait on a barrier that nothing signals
+ * (1 = on, 0 = off) so that the timeout path can be tested; what = 2: how B
+ * reaches the tensor cores in plans made afterwards (0 = by dtype: bf16 is read
+ * MN-major in place, fp32 is first transposed into a plan-owned K-major copy;
+ * 1 = always transposed; 2 = always MN-major).  Affects launches (what 0, 1) or
+ * plans (what 2) made after the call, from any thread. */
 int gemm_debug_set(int32_t what, int64_t value);
 
 #ifdef __cplusplus

@@ -26,8 +26,8 @@ BF16_CASES = [
     ((300, 320, 520), C(128, 192, 64, 4)),
     ((300, 320, 520), C(128, 256, 64, 3)),
     ((300, 320, 520), C(256, 128, 64, 3)),
-    ((300, 320, 520), C(256, 64, 128, 3)),
-    ((300, 320, 520), C(128, 128, 128, 4)),
+    ((300, 320, 520), C(256, 64, 128, 2)),
+    ((300, 320, 520), C(128, 128, 128, 3)),
     ((300, 320, 520), C(128, 64, 256, 2)),
     ((300, 320, 520), C(128, 128, 64, 2, 1, 2)),
     ((520, 640, 264), C(128, 64, 64, 4, 0, 4)),
@@ -36,15 +36,15 @@ BF16_CASES = [
     ((300, 320, 520), C(256, 256, 64, 2, 0, 1, 4)),
     ((20, 320, 520), C(128, 16, 64, 6, 0, 1, 1, 1, 1)),
     ((20, 320, 520), C(128, 32, 64, 6, 0, 1, 2, 1, 1)),
-    ((40, 264, 520), C(256, 64, 128, 3, 0, 1, 3, 1, 1)),
+    ((40, 264, 520), C(256, 64, 128, 2, 0, 1, 3, 1, 1)),
     ((16, 1024, 1024), C(128, 16, 64, 8, 0, 1, 8, 1, 1)),
 ]
 
 FP32_CASES = [
     ((200, 160, 136), C(128, 32, 32, 4)),
     ((200, 160, 136), C(128, 128, 32, 4)),
-    ((200, 160, 136), C(256, 64, 64, 3)),
-    ((200, 160, 136), C(128, 96, 128, 2)),
+    ((200, 160, 136), C(256, 64, 64, 2)),
+    ((200, 160, 136), C(128, 96, 64, 2)),
     ((200, 160, 136), C(128, 64, 32, 4, 0, 1, 2)),
     ((24, 160, 136), C(128, 16, 32, 4, 0, 1, 1, 1, 1)),
     ((24, 160, 136), C(128, 32, 64, 4, 0, 1, 3, 1, 1)),
