@@ -1,0 +1,445 @@
+#!/usr/bin/env python3
+"""Throughput of the autotuned tcgen05 GEMM on one workload; prints one JSON line.
+
+Default workload: bf16 C = gelu(A·B + bias), M = N = 1000, K = 8192 (the
+under-filled shape of "Compilers and Kernel Languages", where a fixed 128x128
+tile leaves most SMs idle).  One step = one GEMM on each of R rotating input
+sets (R chosen so the sets together exceed twice the L2, so no step is served
+from L2); the plan is tuned on first use and cached (that is the method), and
+steps reuse it.  The timed region replays a CUDA graph of one step K times.
+
+Also reported: the roofline of the GEMM kernel against MEASURED_PEAKS.json,
+the fixed 128x128 tile on the same protocol (tuned-vs-fixed speedup), the
+tuner's rank agreement and search cost, an end-to-end number through the
+host-buffer entry point (copies inside the timed region), the CPU oracle on
+the host cores, and SM clocks sampled during the timed region.
+
+  python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no exchange step); value = work of all ranks / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (or GB/s) per shape, % of roofline; tuned vs fixed-128x128 speedup"
+DEFAULT_WORKLOAD = "bf16_gelu_1000x1000x8192"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-fixed", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch from Python instead of a CUDA graph")
+    ap.add_argument("--config", default=None,
+                    help="explicit tile config bm,bn,bk,stages,raster,group,split_k,cta_group,swap_ab "
+                         "(skips tuning; used to profile one configuration)")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def work_of(w):
+    elt = 2 if w.dtype == "bf16" else 4
+    flops = 2.0 * w.M * w.N * w.K
+    bytes_ = (w.M * w.K + w.K * w.N) * elt + (w.N * elt if w.epi != "none" else 0) + w.M * w.N * elt
+    return flops, bytes_, elt
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        threading.Thread(target=self._reader, daemon=True).start()
+        deadline = time.time() + 5
+        while not self.samples and time.time() < deadline:
+            time.sleep(0.02)
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        inside = [s for t, s in self.samples if self.t0 is not None and self.t0 <= t <= self.t1]
+        near = inside or [s for _t, s in self.samples]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in near if len(s) > 1 and num(s[1]) is not None]
+        mx = [num(s[2]) for s in near if len(s) > 2 and num(s[2]) is not None]
+        pw = [num(s[3]) for s in near if len(s) > 3 and num(s[3]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in near:
+            for i, n in enumerate(names):
+                if len(s) > 5 + i and s[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(reasons),
+                "samples_in_timed_region": len(inside),
+                "samples_total": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (rank 0, N = 1 only) — the reported CPU baseline
+# ---------------------------------------------------------------------------
+
+def cpu_oracle_run(w, seconds: float, total_budget_s: float | None = None):
+    """Time the fp64 oracle on a slab of rows of the workload; returns
+    (TFLOP/s, threads, sample text, seconds)."""
+    from autotuning_tcgen05_tmem_gb300 import inputs
+    from oracle import gemm as og
+    og.build()
+    threads = og.default_threads()
+    A, B, bias = inputs.make_workload(w, seed=0)
+    epi = {"none": 0, "bias": 1, "relu": 2, "gelu": 3}[w.epi]
+    cal = min(w.M, max(1, threads))
+    t0 = time.perf_counter()
+    og.gemm(A[:cal], B, bias, epi, threads=threads)
+    per_row = max((time.perf_counter() - t0) / cal, 1e-7)
+    rows = int(min(w.M, max(cal, seconds / per_row)))
+    passes = 0
+    t0 = time.perf_counter()
+    while True:           # whole passes over the slab until `seconds` of CPU work
+        og.gemm(A[:rows], B, bias, epi, threads=threads)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds or dt >= 30.0:
+            break
+    flops = 2.0 * rows * w.N * w.K * passes
+    sample = (f"rows 0..{rows - 1} of {w.M} (all {w.N} columns, full K={w.K}), fp64 oracle, "
+              f"{threads} threads, {passes} pass(es)")
+    return flops / dt / 1e12, threads, sample, dt
+
+
+def reference_arm(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import gemm as og
+    from autotuning_tcgen05_tmem_gb300 import inputs
+    og.build()
+    threads = og.default_threads()
+    A, B, bias = inputs.make_workload(w, seed=0)
+    epi = {"none": 0, "bias": 1, "relu": 2, "gelu": 3}[w.epi]
+    cal = min(w.M, max(1, threads))
+    t0 = time.perf_counter()
+    og.gemm(A[:cal], B, bias, epi, threads=threads)
+    per_row = max((time.perf_counter() - t0) / cal, 1e-7)
+    budget = 120.0 / max(1, args.steps + args.warmup)       # seconds of CPU work per step
+    rows = int(min(w.M, max(1, budget / per_row)))
+    for _ in range(args.warmup):
+        og.gemm(A[:rows], B, bias, epi, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        og.gemm(A[:rows], B, bias, epi, threads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K
+    value = flops * args.steps / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "epilogue": w.epi,
+                       "step": f"rows 0..{rows - 1} of the product (bounded sample)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{rows} of {w.M} rows per step, fp64, {threads} threads"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def make_sets(w, nsets, device):
+    """Rotating input sets, drawn on the device from seeded generators."""
+    import torch
+    from autotuning_tcgen05_tmem_gb300 import inputs
+    sets = []
+    for s in range(nsets):
+        A, B, bias = inputs.make_workload(w, seed=100 + 10 * s, device=device)
+        C = torch.empty(w.M, w.N, dtype=A.dtype, device=device)
+        sets.append((A, B, bias, C))
+    return sets
+
+
+def time_plan(plan, sets, steps, warmup, eager=False):
+    """Average seconds per step (one GEMM per rotating set) over `steps`
+    replays of a CUDA graph of one step; returns (sec_per_step, mode, stream)."""
+    import torch
+    stream = torch.cuda.Stream()
+
+    def one_step():
+        for (A, B, bias, C) in sets:
+            plan.run(A, B, bias, C, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one_step()
+    torch.cuda.synchronize()
+    mode = "eager"
+    graph = None
+    if not eager:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for (A, B, bias, C) in sets:
+                    plan.run(A, B, bias, C, torch.cuda.current_stream())
+            mode = "cuda_graph"
+        except Exception:
+            graph = None
+            torch.cuda.synchronize()
+    run = (lambda: graph.replay()) if graph is not None else one_step
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            run()
+    torch.cuda.synchronize()
+    return run, mode, stream
+
+
+def main():
+    args = parse_args()
+    from autotuning_tcgen05_tmem_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, w)
+
+    import torch
+    import autotuning_tcgen05_tmem_gb300 as g
+    from autotuning_tcgen05_tmem_gb300 import _build
+    rank, world, local = dist_env()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    _build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    os.environ.setdefault("GEMM_PEAK_BF16_TFLOPS", str(peaks.get("bf16_tflops", 1900.0)))
+    os.environ.setdefault("GEMM_HBM_GBS", str(peaks.get("hbm_gbs", 6800.0)))
+    flops, cbytes, elt = work_of(w)
+    devp = g.device_params_query()
+    set_bytes = (w.M * w.K + w.K * w.N + w.N + w.M * w.N) * elt
+    nsets = int(min(8, max(1, math.ceil(2 * devp.l2_bytes / set_bytes))))
+    sets = make_sets(w, nsets, dev)
+
+    # --- plan: tune once (cost model + measurement), cached by shape ---------
+    t0 = time.perf_counter()
+    if args.config:
+        plan = g.plan_with_config(w.M, w.N, w.K, w.dtype, w.epi,
+                                  g.make_config(*[int(x) for x in args.config.split(",")]))
+    else:
+        plan = g.plan(w.M, w.N, w.K, w.dtype, w.epi)
+    plan_s = time.perf_counter() - t0
+    cfg = plan.config
+    launches_per_gemm = 2 if w.dtype != "bf16" else 1
+
+    run, mode, stream = time_plan(plan, sets, args.steps, args.warmup, args.eager)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark("t0")
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    if pg:
+        pg.barrier()
+    clocks.stop()
+    assert plan.status() == 0, g.last_error()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    if pg:
+        t = torch.tensor([elapsed], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed = float(t.item())
+    sec_per_step = elapsed / args.steps
+    gemm_s = sec_per_step / nsets
+    value = flops * nsets * args.steps * world / elapsed / 1e12
+
+    # --- roofline of the GEMM kernel -----------------------------------------
+    sustained = elapsed > 1.0
+    tpeak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops", 1900.0)
+    if w.dtype != "bf16":
+        tpeak = tpeak / 2.0          # nominal tf32 : bf16 dense ratio (1.1 : 2.25 PFLOP/s)
+    bw = peaks.get("hbm_gbs", 6800.0)
+    t_compute = flops / (tpeak * 1e12)
+    t_memory = cbytes / (bw * 1e9)
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        with open(tr_path) as f:
+            tr = json.load(f)
+        ent = tr.get(w.name)
+        if ent and ent.get("source_digest") == _build._sources_digest() and \
+                ent.get("config") == list(cfg.astuple()):
+            traffic = ent.get("dram_bytes_per_launch")
+    if t_compute >= t_memory:
+        roof = {"bound": "tensor", "achieved": flops / gemm_s / 1e12, "peak": tpeak, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": cbytes / gemm_s / 1e9, "peak": bw, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic
+    roof["peak_source"] = f"{peak_src} ({'sustained' if sustained and roof['bound'] == 'tensor' else 'burst'})"
+    roof["algorithmic_per_launch"] = flops if roof["bound"] == "tensor" else cbytes
+    roof["kernel"] = "gemm_tcgen05_kernel"
+
+    out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": sec_per_step * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+           "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "epilogue": w.epi,
+                      "dtype": w.dtype, "tile_config": cfg.asdict(),
+                      "step": f"{nsets} GEMMs, one per rotating input set",
+                      "l2": f"inputs rotate over {nsets} sets ({nsets * set_bytes / 1e6:.0f} MB > 2 x L2 "
+                            f"{devp.l2_bytes / 1e6:.0f} MB)" if nsets * set_bytes > 2 * devp.l2_bytes
+                      else f"each set ({set_bytes / 1e6:.0f} MB) exceeds L2",
+                      "launch": mode, "parallelism": f"replicas x{world}"},
+           "roofline": roof,
+           "gpu_launches": args.steps * nsets * launches_per_gemm,
+           "clocks": clocks.summary(),
+           "plan_seconds": plan_s}
+
+    # --- tuned vs fixed 128x128, and the tuner's own report -------------------
+    if not args.no_fixed and rank == 0:
+        fixed = g.fixed_config(w.dtype, devp)
+        with g.plan_with_config(w.M, w.N, w.K, w.dtype, w.epi, fixed) as fp:
+            fsteps = max(20, args.steps // 4)
+            frun, _m, fstream = time_plan(fp, sets, fsteps, max(3, args.warmup // 4), args.eager)
+            torch.cuda.synchronize()
+            f0 = torch.cuda.Event(enable_timing=True)
+            f1 = torch.cuda.Event(enable_timing=True)
+            f0.record(fstream)
+            with torch.cuda.stream(fstream):
+                for _ in range(fsteps):
+                    frun()
+            f1.record(fstream)
+            torch.cuda.synchronize()
+            fixed_gemm_s = f0.elapsed_time(f1) / 1e3 / fsteps / nsets
+        out["fixed_config"] = fixed.asdict()
+        out["fixed_value"] = flops / fixed_gemm_s / 1e12
+        out["tuned_vs_fixed"] = fixed_gemm_s / gemm_s
+        tr = g.tune(w.M, w.N, w.K, w.dtype, w.epi, topk=int(os.environ.get("GEMM_TUNE_TOPK", "12")))
+        st = tr.stats
+        saved_us = max(st.fixed_us - st.best_us, 0.0) if st.fixed_us > 0 else 0.0
+        out["tune"] = {"candidates": st.n_candidates, "measured": st.n_measured,
+                       "kendall_tau": st.kendall_tau, "spearman_rho": st.spearman_rho,
+                       "top1_hit": st.top1_hit, "regret": st.regret, "search_seconds": st.tune_seconds,
+                       "best_us": st.best_us, "fixed_us": st.fixed_us,
+                       "break_even_calls": (st.tune_seconds / (saved_us * 1e-6)) if saved_us > 0 else None}
+
+    # --- end to end through the host-buffer entry point ------------------------
+    if not args.no_e2e and rank == 0:
+        A, B, bias, _C = sets[0]
+        hA, hB = A.cpu().pin_memory(), B.cpu().pin_memory()
+        hb = bias.cpu().pin_memory() if bias is not None else None
+        hC = torch.empty(w.M, w.N, dtype=A.dtype).pin_memory()
+        esteps = max(5, min(args.steps, 200))
+        hstream = torch.cuda.Stream()
+        for _ in range(3):
+            plan.run_host(hA, hB, hb, hC, hstream)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(esteps):
+            plan.run_host(hA, hB, hb, hC, hstream)
+        dt = (time.perf_counter() - t0) / esteps
+        out["e2e"] = {"value": flops / dt / 1e12, "unit": "TFLOP/s",
+                      "h2d_bytes_per_step": (w.M * w.K + w.K * w.N + (w.N if bias is not None else 0)) * elt,
+                      "d2h_bytes_per_step": w.M * w.N * elt, "steps": esteps,
+                      "path": "gemm_run_host (pinned host buffers; copies and one kernel per step)"}
+
+    # --- CPU oracle ------------------------------------------------------------
+    if not args.no_cpu and rank == 0 and world == 1:
+        v, cores, sample, secs = cpu_oracle_run(w, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                               "sample": sample, "seconds": secs}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    plan.close()
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
