@@ -115,6 +115,49 @@ def library_path() -> str:
     return _build.LIB
 
 
+def _load_library(path: str):
+    """ctypes handle of a library exporting the C ABI, with signatures set."""
+    L = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    sig = {
+        "gemm_version": (ctypes.c_char_p, []),
+        "gemm_last_error": (ctypes.c_char_p, []),
+        "gemm_device_params_default": (None, [P(DeviceParams)]),
+        "gemm_device_params_workshop": (None, [P(DeviceParams)]),
+        "gemm_check_config": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, P(Config),
+                                             P(DeviceParams)]),
+        "gemm_enumerate": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, P(DeviceParams),
+                                          P(Config), i32, P(i32)]),
+        "gemm_fixed_config": (ctypes.c_int, [ctypes.c_int, P(DeviceParams), P(Config)]),
+        "gemm_model_predict": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, P(Config),
+                                              P(DeviceParams), P(ModelTerms)]),
+        "gemm_rank_agreement": (ctypes.c_int, [P(ctypes.c_double), P(ctypes.c_double), i32,
+                                               P(RankStats)]),
+        "gemm_schedule_unit": (ctypes.c_int, [i64, i32, i32, i32, i32, i32, i32, P(i32), P(i32),
+                                              P(i32), P(i32), P(i32)]),
+        "gemm_device_params_query": (ctypes.c_int, [P(DeviceParams)]),
+        "gemm_plan": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, P(vp)]),
+        "gemm_plan_with_config": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, P(Config),
+                                                 P(vp)]),
+        "gemm_plan_config": (ctypes.c_int, [vp, P(Config)]),
+        "gemm_run": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
+        "gemm_run_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
+        "gemm_plan_status": (ctypes.c_int, [vp]),
+        "gemm_plan_destroy": (None, [vp]),
+        "gemm_tune": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, i32, P(TuneRow), i32,
+                                     P(i32), P(RankStats)]),
+        "gemm_cache_stats": (ctypes.c_int, [P(i64), P(i64), P(i64)]),
+        "gemm_cache_clear": (None, []),
+        "gemm_debug_set": (ctypes.c_int, [i32, i64]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib():
     """The loaded native library; raises if it has not been built for this machine."""
     global _LIB
@@ -123,45 +166,7 @@ def lib():
             raise RuntimeError(
                 "the native GEMM library is not built for this machine (no CPU or eager fallback "
                 "exists); run autotuning_tcgen05_tmem_gb300._build.build()")
-        L = ctypes.CDLL(_build.LIB)
-        P = ctypes.POINTER
-        i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
-        sig = {
-            "gemm_version": (ctypes.c_char_p, []),
-            "gemm_last_error": (ctypes.c_char_p, []),
-            "gemm_device_params_default": (None, [P(DeviceParams)]),
-            "gemm_device_params_workshop": (None, [P(DeviceParams)]),
-            "gemm_check_config": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, P(Config),
-                                                 P(DeviceParams)]),
-            "gemm_enumerate": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, P(DeviceParams),
-                                              P(Config), i32, P(i32)]),
-            "gemm_fixed_config": (ctypes.c_int, [ctypes.c_int, P(DeviceParams), P(Config)]),
-            "gemm_model_predict": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, P(Config),
-                                                  P(DeviceParams), P(ModelTerms)]),
-            "gemm_rank_agreement": (ctypes.c_int, [P(ctypes.c_double), P(ctypes.c_double), i32,
-                                                   P(RankStats)]),
-            "gemm_schedule_unit": (ctypes.c_int, [i64, i32, i32, i32, i32, i32, i32, P(i32), P(i32),
-                                                  P(i32), P(i32), P(i32)]),
-            "gemm_device_params_query": (ctypes.c_int, [P(DeviceParams)]),
-            "gemm_plan": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, P(vp)]),
-            "gemm_plan_with_config": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, P(Config),
-                                                     P(vp)]),
-            "gemm_plan_config": (ctypes.c_int, [vp, P(Config)]),
-            "gemm_run": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
-            "gemm_run_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
-            "gemm_plan_status": (ctypes.c_int, [vp]),
-            "gemm_plan_destroy": (None, [vp]),
-            "gemm_tune": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, i32, P(TuneRow), i32,
-                                         P(i32), P(RankStats)]),
-            "gemm_cache_stats": (ctypes.c_int, [P(i64), P(i64), P(i64)]),
-            "gemm_cache_clear": (None, []),
-            "gemm_debug_set": (ctypes.c_int, [i32, i64]),
-        }
-        for name, (res, args) in sig.items():
-            fn = getattr(L, name)
-            fn.restype = res
-            fn.argtypes = args
-        _LIB = L
+        _LIB = _load_library(_build.LIB)
     return _LIB
 
 

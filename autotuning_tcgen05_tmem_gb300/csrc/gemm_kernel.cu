@@ -45,13 +45,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -131,6 +124,19 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v)
 __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
 {
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// One lane of a converged warp (elect.sync); true in exactly that lane.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\t"
+        "elect.sync rx|px, %1;\n\t"
+        "selp.u32 %0, 1, 0, px;\n\t}"
+        : "=r"(pred)
+        : "r"(0xFFFFFFFFu));
+    return pred != 0;
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
@@ -269,15 +275,19 @@ struct WaitCtl {
     int64_t timeout_ns;
 };
 
+// Slow path of a wait: polls with a bound measured in SM clock cycles
+// (clock64 is a cheap register read; the cycle budget assumes the highest SM
+// clock, so at lower clocks the wall-clock bound only grows).
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtl &c, int32_t site,
                                        bool heed_abort, int64_t limit_ns)
 {
-    const uint64_t t0 = global_timer_ns();
+    const long long limit_cycles = (long long)((double)limit_ns * 2.2);
+    const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31u) == 0) {
+        if ((it & 63u) == 0) {
             if (heed_abort && *c.abort) return false;
-            if ((int64_t)(global_timer_ns() - t0) > limit_ns) {
+            if (clock64() - t0 > limit_cycles) {
                 *c.abort = 1;
                 atomicCAS(c.status, 0, site);
                 return false;
@@ -286,9 +296,13 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Wait
     }
 }
 
+// Fast path: a short burst of probes with no timer or flag reads, so that the
+// common case (the phase completes within microseconds) costs only try_wait.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl &c, int32_t site)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
     return wait_slow(bar, parity, c, site, true, c.timeout_ns);
 }
 
@@ -454,7 +468,7 @@ __device__ __forceinline__ void store_cols_chunk(const CUtensorMap *tmC, StoreRi
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <int DT>
+template <int DT, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(192, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const KernelParams p)
@@ -508,126 +522,144 @@ __global__ void __launch_bounds__(192, 1)
 
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 
+    // Roles run warp-converged: every lane walks the same schedule (so the
+    // loop state is warp-uniform), one elected lane issues the TMA copies and
+    // the MMAs, and the wait outcome is agreed with a warp vote.
     if (warp == 0) {
         // ------------------------------------------------------------------
         // TMA producer
         // ------------------------------------------------------------------
-        if (lane == 0) {
-            if (p.num_kb > 0) {
-                prefetch_tmap(&tmA);
-                prefetch_tmap(&tmB);
-            }
-            uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
-            bool ok = true;
-            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
-                const int32_t ra = w.tile_m * p.bm;
-                const int32_t rb = w.tile_n * p.bn;
-                for (int32_t kb = w.kb_begin; kb < w.kb_end; ++kb) {
-                    if (!wait_bar(empty0 + 8u * stage, phase ^ 1u, ctl, SITE_PRODUCER_EMPTY)) {
-                        ok = false;
-                        break;
+        const bool leader = elect_one();
+        const int32_t stages = p.stages, bm = p.bm, bn = p.bn, bk = p.bk;
+        const uint32_t a_bytes = p.a_stage_bytes, b_bytes = p.b_stage_bytes, tx = p.tx_bytes;
+        const uint32_t sb0 = base + p.off_b;
+        const int32_t a_loads = A_MN ? bm / SPAN : bk / SPAN;
+        const int32_t b_loads = B_MN ? bn / SPAN : bk / SPAN;
+        if (leader && p.num_kb > 0) {
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB);
+        }
+        uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
+            const int32_t ra = w.tile_m * bm;
+            const int32_t rb = w.tile_n * bn;
+            for (int32_t kb = w.kb_begin; kb < w.kb_end; ++kb) {
+                ok = __all_sync(0xFFFFFFFFu, wait_bar(empty0 + 8u * stage, phase ^ 1u, ctl, SITE_PRODUCER_EMPTY));
+                if (!ok) break;
+                const uint32_t fb = full0 + 8u * stage;
+                const uint32_t sa = base + stage * a_bytes;
+                const uint32_t sb = sb0 + stage * b_bytes;
+                const int32_t k0 = kb * bk;
+                if (leader) {
+                    mbar_arrive_expect_tx(fb, tx);
+                    // K-major operand: boxes of [rows x one span of K], one per span;
+                    // MN-major operand: boxes of [bk x one span of MN], one per span.
+                    for (int32_t j = 0; j < a_loads; ++j) {
+                        if constexpr (A_MN) tma_load_2d(sa + (uint32_t)(j * bk * 128), &tmA, fb, ra + j * SPAN, k0);
+                        else tma_load_2d(sa + (uint32_t)(j * bm * 128), &tmA, fb, k0 + j * SPAN, ra);
                     }
-                    const uint32_t fb = full0 + 8u * stage;
-                    mbar_arrive_expect_tx(fb, p.tx_bytes);
-                    const uint32_t sa = base + stage * p.a_stage_bytes;
-                    const uint32_t sb = base + p.off_b + stage * p.b_stage_bytes;
-                    const int32_t k0 = kb * p.bk;
-                    if (!p.a_mn_major) {
-                        for (int32_t sp = 0; sp < p.bk / SPAN; ++sp)
-                            tma_load_2d(sa + (uint32_t)(sp * p.bm * 128), &tmA, fb, k0 + sp * SPAN, ra);
-                    } else {
-                        for (int32_t j = 0; j < p.bm / SPAN; ++j)
-                            tma_load_2d(sa + (uint32_t)(j * p.bk * 128), &tmA, fb, ra + j * SPAN, k0);
-                    }
-                    if (!p.b_mn_major) {
-                        for (int32_t sp = 0; sp < p.bk / SPAN; ++sp)
-                            tma_load_2d(sb + (uint32_t)(sp * p.bn * 128), &tmB, fb, k0 + sp * SPAN, rb);
-                    } else {
-                        for (int32_t j = 0; j < p.bn / SPAN; ++j)
-                            tma_load_2d(sb + (uint32_t)(j * p.bk * 128), &tmB, fb, rb + j * SPAN, k0);
-                    }
-                    armed |= 1u << stage;
-                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == (uint32_t)p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
+                    for (int32_t j = 0; j < b_loads; ++j) {
+                        if constexpr (B_MN) tma_load_2d(sb + (uint32_t)(j * bk * 128), &tmB, fb, rb + j * SPAN, k0);
+                        else tma_load_2d(sb + (uint32_t)(j * bn * 128), &tmB, fb, k0 + j * SPAN, rb);
                     }
                 }
+                __syncwarp();
+                armed |= 1u << stage;
+                armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == (uint32_t)stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
-            // Every armed stage's last copy must land before the CTA may exit.
-            for (int s = 0; s < p.stages; ++s)
-                if ((armed >> s) & 1u) wait_teardown(full0 + 8u * s, (armed_parity >> s) & 1u, ctl);
         }
+        // Every armed stage's last copy must land before the CTA may exit.
+        for (int s = 0; s < stages; ++s)
+            if ((armed >> s) & 1u) wait_teardown(full0 + 8u * s, (armed_parity >> s) & 1u, ctl);
     } else if (warp == 1) {
         // ------------------------------------------------------------------
         // MMA issuer
         // ------------------------------------------------------------------
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-            bool issued = false, ok = true;
-            const int32_t ksteps = p.bk * ELT / 32;
-            const int32_t halves = p.bm / 128;
-            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
-                const int32_t nk = w.kb_end - w.kb_begin;
-                if (!wait_bar(tempty0 + 8u * acc, acc_phase ^ 1u, ctl, SITE_MMA_TMEM_EMPTY)) break;
+        const bool leader = elect_one();
+        const int32_t stages = p.stages, bm = p.bm, bn = p.bn, bk = p.bk;
+        const uint32_t a_bytes = p.a_stage_bytes, b_bytes = p.b_stage_bytes, idesc = p.idesc;
+        const uint32_t sb0 = base + p.off_b, acc_cols = p.acc_cols, n_acc = p.n_acc;
+        const uint32_t a_lbo = p.a_lbo, b_lbo = p.b_lbo;
+        const int32_t ksteps = bk * ELT / 32;
+        const int32_t halves = bm / 128;
+        // Descriptor increments, in the 16-byte units of the start-address field.
+        const uint32_t a_half_step = A_MN ? (uint32_t)((128 / SPAN) * bk * 128) >> 4 : (128u * 128u) >> 4;
+        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        bool issued = false, ok = true;
+        for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
+            const int32_t nk = w.kb_end - w.kb_begin;
+            ok = __all_sync(0xFFFFFFFFu, wait_bar(tempty0 + 8u * acc, acc_phase ^ 1u, ctl, SITE_MMA_TMEM_EMPTY));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d0 = tmem_base + acc * acc_cols;
+            for (int32_t kb = 0; kb < nk; ++kb) {
+                ok = __all_sync(0xFFFFFFFFu, wait_bar(full0 + 8u * stage, phase, ctl, SITE_MMA_FULL));
+                if (!ok) break;
                 tc_fence_after();
-                const uint32_t d0 = tmem_base + acc * p.acc_cols;
-                for (int32_t kb = 0; kb < nk; ++kb) {
-                    if (!wait_bar(full0 + 8u * stage, phase, ctl, SITE_MMA_FULL)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sa = base + stage * p.a_stage_bytes;
-                    const uint32_t sb = base + p.off_b + stage * p.b_stage_bytes;
+                const uint64_t adesc = smem_desc(base + stage * a_bytes, a_lbo);
+                const uint64_t bdesc = smem_desc(sb0 + stage * b_bytes, b_lbo);
+                if (leader) {
                     for (int32_t kk = 0; kk < ksteps; ++kk) {
-                        const uint32_t b_off = p.b_mn_major
-                                                   ? (uint32_t)kk * MN_KSTEP
-                                                   : (uint32_t)((kk >> 2) * p.bn * 128 + (kk & 3) * 32);
-                        const uint64_t bdesc = smem_desc(sb + b_off, p.b_lbo);
-                        for (int32_t h = 0; h < halves; ++h) {
-                            const uint32_t a_off =
-                                p.a_mn_major ? (uint32_t)kk * MN_KSTEP + (uint32_t)(h * (128 / SPAN) * p.bk * 128)
-                                             : (uint32_t)((kk >> 2) * p.bm * 128 + h * 128 * 128 + (kk & 3) * 32);
-                            umma<DT>(d0 + (uint32_t)(h * p.bn), smem_desc(sa + a_off, p.a_lbo), bdesc, p.idesc,
-                                     (kb | kk) != 0 ? 1u : 0u);
-                        }
+                        const uint32_t a_k = A_MN ? (uint32_t)kk * (MN_KSTEP >> 4)
+                                                  : (uint32_t)((kk >> 2) * bm * 8 + (kk & 3) * 2);
+                        const uint32_t b_k = B_MN ? (uint32_t)kk * (MN_KSTEP >> 4)
+                                                  : (uint32_t)((kk >> 2) * bn * 8 + (kk & 3) * 2);
+                        const uint32_t accumulate = (kb | kk) != 0 ? 1u : 0u;
+                        for (int32_t h = 0; h < halves; ++h)
+                            umma<DT>(d0 + (uint32_t)(h * bn), adesc + a_k + h * a_half_step, bdesc + b_k, idesc,
+                                     accumulate);
                     }
                     umma_commit(empty0 + 8u * stage);  // slot is free once these MMAs have read it
-                    issued = true;
-                    if (++stage == (uint32_t)p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
                 }
-                if (!ok) break;
+                __syncwarp();
+                issued = true;
+                if (++stage == (uint32_t)stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (leader) {
                 if (nk > 0) umma_commit(tfull0 + 8u * acc);
                 else mbar_arrive(tfull0 + 8u * acc);
-                if (++acc == p.n_acc) {
-                    acc = 0;
-                    acc_phase ^= 1u;
-                }
             }
-            if (issued) {
-                umma_commit(teardown_bar);
-                wait_teardown(teardown_bar, 0, ctl);
+            __syncwarp();
+            if (++acc == n_acc) {
+                acc = 0;
+                acc_phase ^= 1u;
             }
+        }
+        if (issued) {
+            if (leader) umma_commit(teardown_bar);
+            __syncwarp();
+            wait_teardown(teardown_bar, 0, ctl);
         }
     } else {
         // ------------------------------------------------------------------
         // Epilogue: TMEM -> registers -> (+bias, act) -> staging -> TMA store
         // ------------------------------------------------------------------
+        const int32_t e_bn = p.bn, e_bm = p.bm, e_epi = p.epi, e_cols = p.cols, e_rows = p.rows;
+        const int32_t e_split_k = p.split_k, e_swap_ab = p.swap_ab;
+        const uint32_t e_acc_cols = p.acc_cols, e_n_acc = p.n_acc;
+        const void *const e_bias = p.bias;
+        float *const e_workspace = p.workspace;
+        int32_t *const e_counters = p.counters;
         const int q = warp & 3;  // TMEM sub-partition this warp may read
         const int ew = warp - 2;
         StoreRing ring{base + p.off_staging + (uint32_t)ew * 2u * p.staging_buf_bytes, p.staging_buf_bytes, 0};
         uint32_t acc = 0, acc_phase = 0;
         bool first = true;
-        const int32_t halves = p.bm / 128;
-        const int32_t tile_elems = p.bm * p.bn;
+        const int32_t halves = e_bm / 128;
+        const int32_t tile_elems = e_bm * e_bn;
         for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-            const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
+            const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, e_split_k, p.raster, p.group, p.num_kb);
             bool ok = true;
             if (first && p.debug_stall) ok = wait_bar(never_bar, 0, ctl, SITE_EPI_STALL);
             first = false;
@@ -635,66 +667,66 @@ __global__ void __launch_bounds__(192, 1)
             if (named_bar_any(1, 128, !ok)) break;
             tc_fence_after();
             const int32_t nk = w.kb_end - w.kb_begin;
-            const int32_t r0 = w.tile_m * p.bm;
-            const int32_t c0 = w.tile_n * p.bn;
-            const uint32_t tacc = tmem_base + acc * p.acc_cols + ((uint32_t)(q * 32) << 16);
+            const int32_t r0 = w.tile_m * e_bm;
+            const int32_t c0 = w.tile_n * e_bn;
+            const uint32_t tacc = tmem_base + acc * e_acc_cols + ((uint32_t)(q * 32) << 16);
             float *ws = nullptr;
-            if (p.split_k > 1) ws = p.workspace + ((size_t)w.tile * p.split_k + w.split) * (size_t)tile_elems;
+            if (e_split_k > 1) ws = e_workspace + ((size_t)w.tile * e_split_k + w.split) * (size_t)tile_elems;
 
-            if (!p.swap_ab) {
+            if (!e_swap_ab) {
                 for (int32_t h = 0; h < halves; ++h) {
                     const int32_t r = h * 128 + q * 32 + lane;
-                    for (int32_t c = 0; c < p.bn / 32; ++c) {
+                    for (int32_t c = 0; c < e_bn / 32; ++c) {
                         float v[32];
-                        if (nk > 0) tmem_load_chunk<32>(tacc + (uint32_t)(h * p.bn + c * 32), v);
+                        if (nk > 0) tmem_load_chunk<32>(tacc + (uint32_t)(h * e_bn + c * 32), v);
                         else {
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] = 0.0f;
                         }
-                        if (p.split_k > 1) {
+                        if (e_split_k > 1) {
                             float4 *dst = reinterpret_cast<float4 *>(ws);
 #pragma unroll
                             for (int j4 = 0; j4 < 8; ++j4)
-                                dst[(size_t)(c * 8 + j4) * p.bm + r] =
+                                dst[(size_t)(c * 8 + j4) * e_bm + r] =
                                     make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
                         } else {
                             const int32_t n = c0 + c * 32;
-                            if (p.epi != 0) {
+                            if (e_epi != 0) {
                                 float b[32];
-                                load_bias32<DT>(p.bias, n, p.cols, b);
+                                load_bias32<DT>(e_bias, n, e_cols, b);
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] = apply_act(v[j] + b[j], p.epi);
+                                for (int j = 0; j < 32; ++j) v[j] = apply_act(v[j] + b[j], e_epi);
                             }
                             const int32_t y = r0 + h * 128 + q * 32;
-                            store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < p.cols && y < p.rows);
+                            store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                         }
                     }
                 }
             } else {
                 for (int32_t h = 0; h < halves; ++h) {
                     const int32_t r = h * 128 + q * 32 + lane;
-                    for (int32_t c = 0; c < p.bn / 16; ++c) {
+                    for (int32_t c = 0; c < e_bn / 16; ++c) {
                         float v[16];
-                        if (nk > 0) tmem_load_chunk<16>(tacc + (uint32_t)(h * p.bn + c * 16), v);
+                        if (nk > 0) tmem_load_chunk<16>(tacc + (uint32_t)(h * e_bn + c * 16), v);
                         else {
 #pragma unroll
                             for (int j = 0; j < 16; ++j) v[j] = 0.0f;
                         }
-                        if (p.split_k > 1) {
+                        if (e_split_k > 1) {
                             float4 *dst = reinterpret_cast<float4 *>(ws);
 #pragma unroll
                             for (int j4 = 0; j4 < 4; ++j4)
-                                dst[(size_t)(c * 4 + j4) * p.bm + r] =
+                                dst[(size_t)(c * 4 + j4) * e_bm + r] =
                                     make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
                         } else {
                             const int32_t xn = r0 + h * 128 + q * 32;  // output column block (user N)
-                            if (p.epi != 0) {
-                                const float b = load_bias1<DT>(p.bias, xn + lane, p.rows);
+                            if (e_epi != 0) {
+                                const float b = load_bias1<DT>(e_bias, xn + lane, e_rows);
 #pragma unroll
-                                for (int j = 0; j < 16; ++j) v[j] = apply_act(v[j] + b, p.epi);
+                                for (int j = 0; j < 16; ++j) v[j] = apply_act(v[j] + b, e_epi);
                             }
                             const int32_t ym = c0 + c * 16;  // output row block (user M)
-                            store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < p.rows && ym < p.cols);
+                            store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
                         }
                     }
                 }
@@ -702,39 +734,39 @@ __global__ void __launch_bounds__(192, 1)
             // The accumulator may be overwritten by the next unit's MMAs.
             tc_fence_before();
             mbar_arrive(tempty0 + 8u * acc);
-            if (++acc == p.n_acc) {
+            if (++acc == e_n_acc) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
 
-            if (p.split_k > 1) {
+            if (e_split_k > 1) {
                 // The last K slice to arrive sums the partial tiles in slice
                 // order (deterministic) and applies the epilogue.
                 __threadfence();
                 named_bar_sync(1, 128);
                 if (ew == 0 && lane == 0) {
-                    const int32_t old = atomicAdd(p.counters + w.tile, 1);
-                    const int32_t last = (old == p.split_k - 1) ? 1 : 0;
-                    if (last) atomicExch(p.counters + w.tile, 0);
+                    const int32_t old = atomicAdd(e_counters + w.tile, 1);
+                    const int32_t last = (old == e_split_k - 1) ? 1 : 0;
+                    if (last) atomicExch(e_counters + w.tile, 0);
                     *last_flag = last;
                 }
                 named_bar_sync(1, 128);
                 if (*last_flag) {
                     __threadfence();
                     const float4 *tile_ws = reinterpret_cast<const float4 *>(
-                        p.workspace + (size_t)w.tile * p.split_k * (size_t)tile_elems);
+                        e_workspace + (size_t)w.tile * e_split_k * (size_t)tile_elems);
                     const size_t slice4 = (size_t)tile_elems / 4;
-                    if (!p.swap_ab) {
+                    if (!e_swap_ab) {
                         for (int32_t h = 0; h < halves; ++h) {
                             const int32_t r = h * 128 + q * 32 + lane;
-                            for (int32_t c = 0; c < p.bn / 32; ++c) {
+                            for (int32_t c = 0; c < e_bn / 32; ++c) {
                                 float v[32];
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                                for (int32_t s = 0; s < p.split_k; ++s) {
+                                for (int32_t s = 0; s < e_split_k; ++s) {
 #pragma unroll
                                     for (int j4 = 0; j4 < 8; ++j4) {
-                                        const float4 t = __ldcg(tile_ws + s * slice4 + (size_t)(c * 8 + j4) * p.bm + r);
+                                        const float4 t = __ldcg(tile_ws + s * slice4 + (size_t)(c * 8 + j4) * e_bm + r);
                                         v[4 * j4] += t.x;
                                         v[4 * j4 + 1] += t.y;
                                         v[4 * j4 + 2] += t.z;
@@ -742,27 +774,27 @@ __global__ void __launch_bounds__(192, 1)
                                     }
                                 }
                                 const int32_t n = c0 + c * 32;
-                                if (p.epi != 0) {
+                                if (e_epi != 0) {
                                     float b[32];
-                                    load_bias32<DT>(p.bias, n, p.cols, b);
+                                    load_bias32<DT>(e_bias, n, e_cols, b);
 #pragma unroll
-                                    for (int j = 0; j < 32; ++j) v[j] = apply_act(v[j] + b[j], p.epi);
+                                    for (int j = 0; j < 32; ++j) v[j] = apply_act(v[j] + b[j], e_epi);
                                 }
                                 const int32_t y = r0 + h * 128 + q * 32;
-                                store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < p.cols && y < p.rows);
+                                store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                             }
                         }
                     } else {
                         for (int32_t h = 0; h < halves; ++h) {
                             const int32_t r = h * 128 + q * 32 + lane;
-                            for (int32_t c = 0; c < p.bn / 16; ++c) {
+                            for (int32_t c = 0; c < e_bn / 16; ++c) {
                                 float v[16];
 #pragma unroll
                                 for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-                                for (int32_t s = 0; s < p.split_k; ++s) {
+                                for (int32_t s = 0; s < e_split_k; ++s) {
 #pragma unroll
                                     for (int j4 = 0; j4 < 4; ++j4) {
-                                        const float4 t = __ldcg(tile_ws + s * slice4 + (size_t)(c * 4 + j4) * p.bm + r);
+                                        const float4 t = __ldcg(tile_ws + s * slice4 + (size_t)(c * 4 + j4) * e_bm + r);
                                         v[4 * j4] += t.x;
                                         v[4 * j4 + 1] += t.y;
                                         v[4 * j4 + 2] += t.z;
@@ -770,13 +802,13 @@ __global__ void __launch_bounds__(192, 1)
                                     }
                                 }
                                 const int32_t xn = r0 + h * 128 + q * 32;
-                                if (p.epi != 0) {
-                                    const float b = load_bias1<DT>(p.bias, xn + lane, p.rows);
+                                if (e_epi != 0) {
+                                    const float b = load_bias1<DT>(e_bias, xn + lane, e_rows);
 #pragma unroll
-                                    for (int j = 0; j < 16; ++j) v[j] = apply_act(v[j] + b, p.epi);
+                                    for (int j = 0; j < 16; ++j) v[j] = apply_act(v[j] + b, e_epi);
                                 }
                                 const int32_t ym = c0 + c * 16;
-                                store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < p.rows && ym < p.cols);
+                                store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
                             }
                         }
                     }
@@ -839,29 +871,65 @@ __global__ void transpose_kernel(const T *__restrict__ src, T *__restrict__ dst,
 // Host-side launch helpers
 // ---------------------------------------------------------------------------
 
+// Kernel instances: (dtype, A MN-major, B MN-major).  bf16 reads B MN-major in
+// place (unswapped: B is MMA-B; swapped: B is MMA-A); fp32 reads both operands
+// K-major from a transposed copy of B.
+template <int DT, bool AM, bool BM>
+static const void *kernel_fn()
+{
+    return reinterpret_cast<const void *>(gemm_tcgen05_kernel<DT, AM, BM>);
+}
+
+static const void *select_kernel(int dt, int a_mn, int b_mn)
+{
+    if (dt == 0) {
+        if (!a_mn && b_mn) return kernel_fn<0, false, true>();
+        if (a_mn && !b_mn) return kernel_fn<0, true, false>();
+        if (!a_mn && !b_mn) return kernel_fn<0, false, false>();
+        return nullptr;
+    }
+    if (!a_mn && !b_mn) return kernel_fn<1, false, false>();
+    return nullptr;
+}
+
 cudaError_t kernel_attributes(int dt, int *num_regs, int *max_threads)
 {
-    cudaFuncAttributes a;
-    cudaError_t e = dt == 0 ? cudaFuncGetAttributes(&a, gemm_tcgen05_kernel<0>)
-                            : cudaFuncGetAttributes(&a, gemm_tcgen05_kernel<1>);
-    if (e != cudaSuccess) return e;
-    if (num_regs) *num_regs = a.numRegs;
-    if (max_threads) *max_threads = a.maxThreadsPerBlock;
+    int regs = 0, thr = 1 << 30;
+    const int combos[3][2] = {{0, 1}, {1, 0}, {0, 0}};
+    for (const auto &c : combos) {
+        const void *f = select_kernel(dt, c[0], c[1]);
+        if (!f) continue;
+        cudaFuncAttributes a;
+        cudaError_t e = cudaFuncGetAttributes(&a, f);
+        if (e != cudaSuccess) return e;
+        if (a.numRegs > regs) regs = a.numRegs;
+        if (a.maxThreadsPerBlock < thr) thr = a.maxThreadsPerBlock;
+    }
+    if (num_regs) *num_regs = regs;
+    if (max_threads) *max_threads = thr;
     return cudaSuccess;
 }
 
 cudaError_t set_kernel_smem_limit(int dt, int bytes)
 {
-    return dt == 0 ? cudaFuncSetAttribute(gemm_tcgen05_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
-                   : cudaFuncSetAttribute(gemm_tcgen05_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const int combos[3][2] = {{0, 1}, {1, 0}, {0, 0}};
+    for (const auto &c : combos) {
+        const void *f = select_kernel(dt, c[0], c[1]);
+        if (!f) continue;
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
                         const KernelParams &p, int grid, int smem_bytes, cudaStream_t stream)
 {
-    if (dt == 0) gemm_tcgen05_kernel<0><<<grid, 192, smem_bytes, stream>>>(a, b, c, p);
-    else gemm_tcgen05_kernel<1><<<grid, 192, smem_bytes, stream>>>(a, b, c, p);
-    return cudaGetLastError();
+    const void *f = select_kernel(dt, p.a_mn_major, p.b_mn_major);
+    if (!f) return cudaErrorInvalidValue;
+    void *args[] = {const_cast<CUtensorMap *>(&a), const_cast<CUtensorMap *>(&b), const_cast<CUtensorMap *>(&c),
+                    const_cast<KernelParams *>(&p)};
+    return cudaLaunchKernel(f, dim3(grid), dim3(192), args, (size_t)smem_bytes, stream);
 }
 
 cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t cols, int elt, cudaStream_t stream)
