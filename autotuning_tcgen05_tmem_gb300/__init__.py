@@ -40,7 +40,7 @@ EXPORTS = ["gemm_version", "gemm_last_error", "gemm_device_params_default",
            "gemm_schedule_unit", "gemm_device_params_query", "gemm_plan",
            "gemm_plan_with_config", "gemm_plan_config", "gemm_run", "gemm_run_host",
            "gemm_plan_status", "gemm_plan_destroy", "gemm_tune", "gemm_cache_stats",
-           "gemm_cache_clear", "gemm_debug_set"]
+           "gemm_cache_clear", "gemm_debug_set", "gemm_run_noalloc"]
 
 
 class GemmError(RuntimeError):
@@ -150,6 +150,7 @@ def _load_library(path: str):
         "gemm_cache_stats": (ctypes.c_int, [P(i64), P(i64), P(i64)]),
         "gemm_cache_clear": (None, []),
         "gemm_debug_set": (ctypes.c_int, [i32, i64]),
+        "gemm_run_noalloc": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, P(Config), vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -367,6 +368,17 @@ def cache_clear():
 
 def debug_set(what: int, value: int):
     _check(lib().gemm_debug_set(what, value))
+
+
+def run_noalloc_rc(M, N, K, epi, cfg: Config, A, B, bias, C, stream=None) -> int:
+    """bf16 GEMM through the allocation-free entry point (for callers that
+    cannot allocate device memory); returns the status code."""
+    return lib().gemm_run_noalloc(M, N, K, _ep(epi), ctypes.byref(cfg), _ptr(A), _ptr(B), _ptr(bias), _ptr(C),
+                                  _stream_handle(stream))
+
+
+def run_noalloc(M, N, K, epi, cfg: Config, A, B, bias, C, stream=None) -> None:
+    _check(run_noalloc_rc(M, N, K, epi, cfg, A, B, bias, C, stream))
 
 
 def gemm(A, B, bias=None, epi="none", out=None, stream=None):

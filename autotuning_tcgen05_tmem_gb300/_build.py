@@ -24,7 +24,7 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libgemm_gb300.so")
 STAMP = os.path.join(LIBDIR, "build.stamp")
 
-CU_SOURCES = ["gemm_kernel.cu"]
+CU_SOURCES = ["gemm_kernel.cu", "noalloc.cu"]
 CPP_SOURCES = ["planner.cpp", "runtime.cpp", "capi.cpp"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

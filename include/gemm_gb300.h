@@ -298,6 +298,41 @@ void gemm_cache_clear(void);
  * plans (what 2) made after the call, from any thread. */
 int gemm_debug_set(int32_t what, int64_t value);
 
+/* ---------------------------------------------------------------------------
+ * Allocation-free entry point.  The pages have no counterpart: this is a
+ * deployment aid, not part of the method.
+ * ------------------------------------------------------------------------- */
+
+/* Size of the fixed scratch behind gemm_run_noalloc: split-K partial tiles
+ * (16 MiB of fp32) and one arrival counter per output tile (at most 4096 tiles). */
+#define GEMM_NOALLOC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+#define GEMM_NOALLOC_MAX_TILES 4096
+
+/* C = act(A·B + bias) for bf16 operands with the explicit configuration *cfg,
+ * for callers that cannot call cudaMalloc: code running under a framework whose
+ * caching allocator owns the device memory (a raw cudaMalloc escapes its
+ * accounting and may synchronise the device), or services that reserve all
+ * device memory up front and must not fail or stall on an allocation while
+ * serving.  It allocates nothing, host or device: its scratch (status word,
+ * split-K counters and partial tiles) is one fixed array compiled into the
+ * library, which every GPU that loads the library holds until the process exits.
+ * Arguments are those of gemm_plan_with_config + gemm_run (bf16 only); the call
+ * is asynchronous on `stream` and returns after the launch.
+ *   - The first call on a device sets that device up (looks up the scratch's
+ *     device address, reads the device's limits, sets the kernel's shared-memory
+ *     limit); make that first call before any stream capture.
+ *   - Returns GEMM_ERR_INVALID_ARG, with the limits in gemm_last_error, when the
+ *     problem needs more than GEMM_NOALLOC_MAX_TILES output tiles or, with
+ *     split_k > 1, more than GEMM_NOALLOC_WORKSPACE_BYTES of partial tiles.
+ *   - All calls share the scratch and it keeps the previous call's contents;
+ *     each call first clears, on `stream`, the status word and the counters it
+ *     uses.  Calls whose work overlaps on the GPU (other streams, other host
+ *     threads) race on the scratch and must be serialised by the caller.
+ *   - A device wait that expires is recorded in the scratch's status word but is
+ *     not reported by this call, which does not synchronise. */
+int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_epilogue epi, const gemm_config *cfg,
+                     const void *A, const void *B, const void *bias, void *C, gemm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
