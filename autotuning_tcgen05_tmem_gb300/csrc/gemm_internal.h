@@ -14,7 +14,7 @@
 
 namespace gemmgb {
 
-constexpr int kThreadsPerCta = 192;
+constexpr int kThreadsPerCta = 320;
 constexpr int kTmemColumns = 512;
 constexpr int kAuxSmem = 2048;     // barriers and flags (1 KB) + 1 KB of base-alignment slack
 constexpr int kMaxStages = 16;

@@ -17,9 +17,10 @@
 //   * "Compilers and Kernel Languages": pipeline depth, split-K and tile order
 //     are runtime choices of this kernel (stages, split_k, raster/group).
 //
-// Roles (192 threads): warp 0 lane 0 issues TMA loads; warp 1 owns TMEM and its
-// lane 0 issues tcgen05.mma; warps 2..5 (128 threads) drain the accumulator,
-// each reading the 32 TMEM lanes of its sub-partition (warp % 4).
+// Roles (320 threads): warp 0 issues TMA loads and warp 1 owns TMEM and issues
+// tcgen05.mma (one elected lane each, the warp walking the schedule converged);
+// warps 2..9 (256 threads) drain the accumulator, each reading the 32 TMEM
+// lanes of its sub-partition (warp % 4), two warps per sub-partition.
 //
 // Every mbarrier wait is bounded: after the limit the waiting role writes a
 // code to the status word, raises a CTA-wide abort flag and returns; the other
@@ -35,6 +36,10 @@
 
 namespace gemmgb {
 namespace {
+
+constexpr int kEpiWarps = 8;                    // two per TMEM sub-partition
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;      // producer warp + MMA warp + epilogue
 
 // ---------------------------------------------------------------------------
 // Inline-PTX primitives
@@ -328,55 +333,63 @@ struct Elt<1> {
     static constexpr int BYTES = 4;
 };
 
+// erf(z) for z >= 0 by Abramowitz & Stegun, "Handbook of Mathematical Functions"
+// (1964), formula 7.1.26: 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2)
+// with t = 1 / (1 + p z), absolute error at most 1.5e-7.  Branch-free, so the
+// 32 values of a chunk are computed side by side.
+__device__ __forceinline__ float gelu_erf(float x)
+{
+    const float z = fabsf(x) * 0.70710678118654752440f;
+    const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
+    const float poly =
+        t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f),
+                 0.254829592f);
+    // q = erfc(|x|/√2); 1 + erf(x/√2) is 2 - q for x >= 0 and q for x < 0
+    // (taking q directly avoids cancellation in the negative tail).
+    const float q = poly * __expf(-z * z);
+    return 0.5f * x * (x >= 0.0f ? 2.0f - q : q);
+}
+
 __device__ __forceinline__ float apply_act(float x, int epi)
 {
     if (epi == 2) return fmaxf(x, 0.0f);
-    if (epi == 3) return 0.5f * x * (1.0f + erff(x * 0.70710678118654752440f));
+    if (epi == 3) return gelu_erf(x);
     return x;
+}
+
+// Applies bias (one value per column, held by lane j for column j of the
+// chunk) and the activation to a 32-column row chunk.
+__device__ __forceinline__ void bias_act_rows(float (&v)[32], float lane_bias, int epi)
+{
+    if (epi == 0) return;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xFFFFFFFFu, lane_bias, j);
+    if (epi == 2) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j], 0.0f);
+    } else if (epi == 3) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+    }
+}
+
+__device__ __forceinline__ void bias_act_cols(float (&v)[16], float row_bias, int epi)
+{
+    if (epi == 0) return;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] += row_bias;
+    if (epi == 2) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = fmaxf(v[j], 0.0f);
+    } else if (epi == 3) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = gelu_erf(v[j]);
+    }
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16)
 {
     return __uint_as_float(bits16 << 16);
-}
-
-// Bias of 32 consecutive output columns starting at n (same for every lane).
-template <int DT>
-__device__ __forceinline__ void load_bias32(const void *bias, int n, int cols, float (&b)[32])
-{
-    if constexpr (DT == 0) {
-        const uint16_t *bp = reinterpret_cast<const uint16_t *>(bias) + n;
-        if (n + 32 <= cols) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 q = __ldg(reinterpret_cast<const uint4 *>(bp) + i);
-                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    b[8 * i + 2 * t] = bf16_bits_to_float(w[t] & 0xFFFFu);
-                    b[8 * i + 2 * t + 1] = bf16_bits_to_float(w[t] >> 16);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) b[j] = (n + j < cols) ? bf16_bits_to_float(__ldg(bp + j)) : 0.0f;
-        }
-    } else {
-        const float *bp = reinterpret_cast<const float *>(bias) + n;
-        if (n + 32 <= cols) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 q = __ldg(reinterpret_cast<const float4 *>(bp) + i);
-                b[4 * i] = q.x;
-                b[4 * i + 1] = q.y;
-                b[4 * i + 2] = q.z;
-                b[4 * i + 3] = q.w;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) b[j] = (n + j < cols) ? __ldg(bp + j) : 0.0f;
-        }
-    }
 }
 
 template <int DT>
@@ -469,7 +482,7 @@ __device__ __forceinline__ void store_cols_chunk(const CUtensorMap *tmC, StoreRi
 // ---------------------------------------------------------------------------
 
 template <int DT, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const KernelParams p)
 {
@@ -502,7 +515,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(tfull0 + 8u * i, 1);
-            mbar_init(tempty0 + 8u * i, 128);
+            mbar_init(tempty0 + 8u * i, kEpiThreads);
         }
         mbar_init(teardown_bar, 1);
         mbar_init(never_bar, 1);
@@ -643,7 +656,11 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ------------------------------------------------------------------
-        // Epilogue: TMEM -> registers -> (+bias, act) -> staging -> TMA store
+        // Epilogue: TMEM -> registers -> (+bias, act) -> staging -> TMA store.
+        // Eight warps: two per TMEM sub-partition (warp % 4), splitting the
+        // accumulator's column chunks between them (even / odd chunks).  The
+        // bias of a unit is loaded (one value per lane and chunk) before its
+        // accumulator is ready, so that load overlaps the main loop.
         // ------------------------------------------------------------------
         const int32_t e_bn = p.bn, e_bm = p.bm, e_epi = p.epi, e_cols = p.cols, e_rows = p.rows;
         const int32_t e_split_k = p.split_k, e_swap_ab = p.swap_ab;
@@ -651,32 +668,54 @@ __global__ void __launch_bounds__(192, 1)
         const void *const e_bias = p.bias;
         float *const e_workspace = p.workspace;
         int32_t *const e_counters = p.counters;
-        const int q = warp & 3;  // TMEM sub-partition this warp may read
-        const int ew = warp - 2;
+        const int q = warp & 3;             // TMEM sub-partition this warp may read
+        const int ew = warp - 2;            // 0..7
+        const int cg = ew >> 2;             // column-chunk parity handled by this warp
         StoreRing ring{base + p.off_staging + (uint32_t)ew * 2u * p.staging_buf_bytes, p.staging_buf_bytes, 0};
         uint32_t acc = 0, acc_phase = 0;
         bool first = true;
         const int32_t halves = e_bm / 128;
         const int32_t tile_elems = e_bm * e_bn;
+        const int32_t chunks = e_swap_ab ? e_bn / 16 : e_bn / 32;
         for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
             const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, e_split_k, p.raster, p.group, p.num_kb);
+            const int32_t r0 = w.tile_m * e_bm;
+            const int32_t c0 = w.tile_n * e_bn;
+            // bias: unswapped, lane j holds column c0 + c*32 + j of each of this
+            // warp's chunks; swapped, each lane holds its row's value per half.
+            float bcol[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float brow[2] = {0.0f, 0.0f};
+            if (e_epi != 0) {
+                if (!e_swap_ab) {
+#pragma unroll
+                    for (int ci = 0; ci < 4; ++ci) {
+                        const int32_t c = cg + 2 * ci;
+                        if (c < chunks) bcol[ci] = load_bias1<DT>(e_bias, c0 + c * 32 + lane, e_cols);
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        if (h < halves) brow[h] = load_bias1<DT>(e_bias, r0 + h * 128 + q * 32 + lane, e_rows);
+                }
+            }
             bool ok = true;
             if (first && p.debug_stall) ok = wait_bar(never_bar, 0, ctl, SITE_EPI_STALL);
             first = false;
             if (ok) ok = wait_bar(tfull0 + 8u * acc, acc_phase, ctl, SITE_EPI_TMEM_FULL);
-            if (named_bar_any(1, 128, !ok)) break;
+            if (named_bar_any(1, kEpiThreads, !ok)) break;
             tc_fence_after();
             const int32_t nk = w.kb_end - w.kb_begin;
-            const int32_t r0 = w.tile_m * e_bm;
-            const int32_t c0 = w.tile_n * e_bn;
             const uint32_t tacc = tmem_base + acc * e_acc_cols + ((uint32_t)(q * 32) << 16);
             float *ws = nullptr;
             if (e_split_k > 1) ws = e_workspace + ((size_t)w.tile * e_split_k + w.split) * (size_t)tile_elems;
 
-            if (!e_swap_ab) {
-                for (int32_t h = 0; h < halves; ++h) {
-                    const int32_t r = h * 128 + q * 32 + lane;
-                    for (int32_t c = 0; c < e_bn / 32; ++c) {
+            for (int32_t h = 0; h < halves; ++h) {
+                const int32_t r = h * 128 + q * 32 + lane;
+                if (!e_swap_ab) {
+#pragma unroll
+                    for (int ci = 0; ci < 4; ++ci) {
+                        const int32_t c = cg + 2 * ci;
+                        if (c >= chunks) break;
                         float v[32];
                         if (nk > 0) tmem_load_chunk<32>(tacc + (uint32_t)(h * e_bn + c * 32), v);
                         else {
@@ -690,22 +729,13 @@ __global__ void __launch_bounds__(192, 1)
                                 dst[(size_t)(c * 8 + j4) * e_bm + r] =
                                     make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
                         } else {
-                            const int32_t n = c0 + c * 32;
-                            if (e_epi != 0) {
-                                float b[32];
-                                load_bias32<DT>(e_bias, n, e_cols, b);
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] = apply_act(v[j] + b[j], e_epi);
-                            }
-                            const int32_t y = r0 + h * 128 + q * 32;
+                            bias_act_rows(v, bcol[ci], e_epi);
+                            const int32_t n = c0 + c * 32, y = r0 + h * 128 + q * 32;
                             store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                         }
                     }
-                }
-            } else {
-                for (int32_t h = 0; h < halves; ++h) {
-                    const int32_t r = h * 128 + q * 32 + lane;
-                    for (int32_t c = 0; c < e_bn / 16; ++c) {
+                } else {
+                    for (int32_t c = cg; c < chunks; c += 2) {
                         float v[16];
                         if (nk > 0) tmem_load_chunk<16>(tacc + (uint32_t)(h * e_bn + c * 16), v);
                         else {
@@ -719,13 +749,9 @@ __global__ void __launch_bounds__(192, 1)
                                 dst[(size_t)(c * 4 + j4) * e_bm + r] =
                                     make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
                         } else {
+                            bias_act_cols(v, h == 0 ? brow[0] : brow[1], e_epi);
                             const int32_t xn = r0 + h * 128 + q * 32;  // output column block (user N)
-                            if (e_epi != 0) {
-                                const float b = load_bias1<DT>(e_bias, xn + lane, e_rows);
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) v[j] = apply_act(v[j] + b, e_epi);
-                            }
-                            const int32_t ym = c0 + c * 16;  // output row block (user M)
+                            const int32_t ym = c0 + c * 16;            // output row block (user M)
                             store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
                         }
                     }
@@ -741,73 +767,81 @@ __global__ void __launch_bounds__(192, 1)
 
             if (e_split_k > 1) {
                 // The last K slice to arrive sums the partial tiles in slice
-                // order (deterministic) and applies the epilogue.
+                // order (deterministic) and applies the epilogue.  Each warp
+                // issues all loads of a slice (or of four slices, swapped)
+                // before adding them, so L2 round trips overlap.
                 __threadfence();
-                named_bar_sync(1, 128);
+                named_bar_sync(1, kEpiThreads);
                 if (ew == 0 && lane == 0) {
                     const int32_t old = atomicAdd(e_counters + w.tile, 1);
                     const int32_t last = (old == e_split_k - 1) ? 1 : 0;
                     if (last) atomicExch(e_counters + w.tile, 0);
                     *last_flag = last;
                 }
-                named_bar_sync(1, 128);
-                if (*last_flag) {
+                named_bar_sync(1, kEpiThreads);
+                const bool is_last = *last_flag != 0;
+                named_bar_sync(1, kEpiThreads);   // the flag is rewritten by the next unit
+                if (is_last) {
                     __threadfence();
                     const float4 *tile_ws = reinterpret_cast<const float4 *>(
                         e_workspace + (size_t)w.tile * e_split_k * (size_t)tile_elems);
                     const size_t slice4 = (size_t)tile_elems / 4;
-                    if (!e_swap_ab) {
-                        for (int32_t h = 0; h < halves; ++h) {
-                            const int32_t r = h * 128 + q * 32 + lane;
-                            for (int32_t c = 0; c < e_bn / 32; ++c) {
+                    for (int32_t h = 0; h < halves; ++h) {
+                        const int32_t r = h * 128 + q * 32 + lane;
+                        if (!e_swap_ab) {
+#pragma unroll
+                            for (int ci = 0; ci < 4; ++ci) {
+                                const int32_t c = cg + 2 * ci;
+                                if (c >= chunks) break;
                                 float v[32];
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                                const float4 *src = tile_ws + (size_t)(c * 8) * e_bm + r;
                                 for (int32_t s = 0; s < e_split_k; ++s) {
+                                    float4 t[8];
+#pragma unroll
+                                    for (int j4 = 0; j4 < 8; ++j4) t[j4] = __ldcg(src + s * slice4 + (size_t)j4 * e_bm);
 #pragma unroll
                                     for (int j4 = 0; j4 < 8; ++j4) {
-                                        const float4 t = __ldcg(tile_ws + s * slice4 + (size_t)(c * 8 + j4) * e_bm + r);
-                                        v[4 * j4] += t.x;
-                                        v[4 * j4 + 1] += t.y;
-                                        v[4 * j4 + 2] += t.z;
-                                        v[4 * j4 + 3] += t.w;
+                                        v[4 * j4] += t[j4].x;
+                                        v[4 * j4 + 1] += t[j4].y;
+                                        v[4 * j4 + 2] += t[j4].z;
+                                        v[4 * j4 + 3] += t[j4].w;
                                     }
                                 }
-                                const int32_t n = c0 + c * 32;
-                                if (e_epi != 0) {
-                                    float b[32];
-                                    load_bias32<DT>(e_bias, n, e_cols, b);
-#pragma unroll
-                                    for (int j = 0; j < 32; ++j) v[j] = apply_act(v[j] + b[j], e_epi);
-                                }
-                                const int32_t y = r0 + h * 128 + q * 32;
+                                bias_act_rows(v, bcol[ci], e_epi);
+                                const int32_t n = c0 + c * 32, y = r0 + h * 128 + q * 32;
                                 store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                             }
-                        }
-                    } else {
-                        for (int32_t h = 0; h < halves; ++h) {
-                            const int32_t r = h * 128 + q * 32 + lane;
-                            for (int32_t c = 0; c < e_bn / 16; ++c) {
+                        } else {
+                            for (int32_t c = cg; c < chunks; c += 2) {
                                 float v[16];
 #pragma unroll
                                 for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-                                for (int32_t s = 0; s < e_split_k; ++s) {
+                                const float4 *src = tile_ws + (size_t)(c * 4) * e_bm + r;
+                                for (int32_t s = 0; s < e_split_k; s += 4) {
+                                    float4 t[4][4];
 #pragma unroll
-                                    for (int j4 = 0; j4 < 4; ++j4) {
-                                        const float4 t = __ldcg(tile_ws + s * slice4 + (size_t)(c * 4 + j4) * e_bm + r);
-                                        v[4 * j4] += t.x;
-                                        v[4 * j4 + 1] += t.y;
-                                        v[4 * j4 + 2] += t.z;
-                                        v[4 * j4 + 3] += t.w;
-                                    }
-                                }
-                                const int32_t xn = r0 + h * 128 + q * 32;
-                                if (e_epi != 0) {
-                                    const float b = load_bias1<DT>(e_bias, xn + lane, e_rows);
+                                    for (int i = 0; i < 4; ++i)
+                                        if (s + i < e_split_k) {
 #pragma unroll
-                                    for (int j = 0; j < 16; ++j) v[j] = apply_act(v[j] + b, e_epi);
+                                            for (int j4 = 0; j4 < 4; ++j4)
+                                                t[i][j4] = __ldcg(src + (s + i) * slice4 + (size_t)j4 * e_bm);
+                                        }
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i)
+                                        if (s + i < e_split_k) {
+#pragma unroll
+                                            for (int j4 = 0; j4 < 4; ++j4) {
+                                                v[4 * j4] += t[i][j4].x;
+                                                v[4 * j4 + 1] += t[i][j4].y;
+                                                v[4 * j4 + 2] += t[i][j4].z;
+                                                v[4 * j4 + 3] += t[i][j4].w;
+                                            }
+                                        }
                                 }
-                                const int32_t ym = c0 + c * 16;
+                                bias_act_cols(v, h == 0 ? brow[0] : brow[1], e_epi);
+                                const int32_t xn = r0 + h * 128 + q * 32, ym = c0 + c * 16;
                                 store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
                             }
                         }
@@ -929,7 +963,7 @@ cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, cons
     if (!f) return cudaErrorInvalidValue;
     void *args[] = {const_cast<CUtensorMap *>(&a), const_cast<CUtensorMap *>(&b), const_cast<CUtensorMap *>(&c),
                     const_cast<KernelParams *>(&p)};
-    return cudaLaunchKernel(f, dim3(grid), dim3(192), args, (size_t)smem_bytes, stream);
+    return cudaLaunchKernel(f, dim3(grid), dim3(kThreads), args, (size_t)smem_bytes, stream);
 }
 
 cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t cols, int elt, cudaStream_t stream)

@@ -62,7 +62,7 @@ void params_workshop(gemm_device_params *d)
 static int staging_bytes(int dt, int swap_ab)
 {
     const int rows = swap_ab ? 16 : 32;   // store chunk: 32 rows x 32 cols, or 16 token rows x 32 cols
-    return 4 * 2 * rows * 32 * elt_bytes(dt);
+    return 8 * 2 * rows * 32 * elt_bytes(dt);   // 8 epilogue warps x 2 buffers
 }
 
 Layout layout_of(const gemm_config &c, int dt)
@@ -73,7 +73,7 @@ Layout layout_of(const gemm_config &c, int dt)
     L.b_stage_bytes = (uint32_t)(c.bn * c.bk * e);
     L.stage_bytes = L.a_stage_bytes + L.b_stage_bytes;
     L.staging_total = (uint32_t)staging_bytes(dt, c.swap_ab);
-    L.staging_buf_bytes = L.staging_total / 8;
+    L.staging_buf_bytes = L.staging_total / 16;
     L.off_b = (uint32_t)c.stages * L.a_stage_bytes;
     L.off_staging = L.off_b + (uint32_t)c.stages * L.b_stage_bytes;
     L.off_bar = L.off_staging + L.staging_total;

@@ -113,7 +113,7 @@ typedef enum {
     GEMM_REASON_ALIGN = 9,      /* K·elt or N·elt not a multiple of 16 bytes */
     GEMM_REASON_TMEM = 10,      /* one accumulator needs more than 512 TMEM columns */
     GEMM_REASON_SMEM = 11,      /* ring + epilogue staging + barriers exceed the per-block limit */
-    GEMM_REASON_REGS = 12       /* kernel registers × 192 threads exceed 65,536 */
+    GEMM_REASON_REGS = 12       /* kernel registers × 320 threads exceed 65,536 */
 } gemm_reason;
 
 /*
@@ -140,7 +140,7 @@ typedef struct {
     double  epi_elems_per_clk;      /* per SM accumulators drained by the epilogue per clock */
     double  launch_us;              /* fixed launch + teardown cost */
     int32_t kernel_regs;            /* registers/thread of the GEMM kernel (0 = unknown) */
-    int32_t threads_per_cta;        /* 192 */
+    int32_t threads_per_cta;        /* 320 */
 } gemm_device_params;
 
 /* Terms of one cost-model prediction (times in microseconds). */

@@ -219,7 +219,7 @@ EPI_NONE, EPI_BIAS, EPI_RELU, EPI_GELU = 0, 1, 2, 3
 R_OK, R_CTA_GROUP, R_UMMA_M, R_UMMA_N, R_LAYOUT, R_BK, R_STAGES, R_SCHEDULE, \
     R_SPLIT_K, R_ALIGN, R_TMEM, R_SMEM, R_REGS = range(13)
 
-THREADS_PER_CTA = 192
+THREADS_PER_CTA = 320
 TMEM_COLUMNS = 512
 AUX_SMEM = 2048            # barriers/flags (1 KB) + 1 KB alignment slack
 MAX_STAGES = 16
@@ -276,10 +276,10 @@ def span_elems(dtype):
 
 
 def staging_bytes(dtype, swap_ab):
-    """Epilogue staging: 4 epilogue warps × 2 buffers × one store chunk
+    """Epilogue staging: 8 epilogue warps × 2 buffers × one store chunk
     (32 rows × 32 columns, or 16 token rows × 32 columns when swapped)."""
     rows = 16 if swap_ab else 32
-    return 4 * 2 * rows * 32 * elt_bytes(dtype)
+    return 8 * 2 * rows * 32 * elt_bytes(dtype)
 
 
 def stage_bytes(cfg: Config, dtype):

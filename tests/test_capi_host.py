@@ -49,7 +49,7 @@ def test_library_exports_every_declared_symbol():
 def test_version_and_defaults():
     assert g.version().startswith("gb300-tcgen05-gemm")
     d = g.device_params_default()
-    assert d.sm_count == 152 and d.threads_per_cta == 192 and d.model_kind == 0
+    assert d.sm_count == 152 and d.threads_per_cta == 320 and d.model_kind == 0
     w = g.device_params_workshop()
     assert (w.sm_count, w.model_kind, w.peak_tflops_bf16, w.hbm_gbs) == (132, 1, 989.0, 3350.0)
 

@@ -211,3 +211,31 @@ def test_run_host_matches_run():
     with g.plan_with_config(200, 192, 512, "bf16", "gelu", cfg) as p:
         p.run_host(A.pin_memory(), B.pin_memory(), bias.pin_memory(), host_out)
     assert torch.equal(dev_out.view(torch.int16), host_out.view(torch.int16))
+
+
+def test_gelu_epilogue_pointwise_accuracy():
+    """C = gelu(x·1 + 0) over a sweep of x.  The device's erf (Abramowitz &
+    Stegun 7.1.26) has absolute error <= 1.5e-7, so |GELU_dev - GELU| <=
+    0.5·|x|·1.5e-7 before the bf16 rounding; the bf16 result may therefore
+    differ from the exactly rounded one by at most one rounding step plus that
+    bound (which is what matters far in the negative tail, where GELU ~ 0)."""
+    M, N, K = 512, 64, 64
+    xs = torch.linspace(-8, 8, M, dtype=torch.float64)
+    A = torch.zeros(M, K, dtype=torch.float32)
+    A[:, 0] = xs.float()
+    A = A.to(torch.bfloat16)
+    B = torch.zeros(K, N, dtype=torch.bfloat16)
+    B[0, :] = 1.0
+    bias = torch.zeros(N, dtype=torch.bfloat16)
+    out, ok = run_config(A, B, bias, "gelu", C(128, 64, 64, 2))
+    assert ok
+    from oracle import gemm as og
+    exact = og.gemm(A, B, bias, og.EPI_BIAS_GELU)
+    got = out.double().numpy()
+    x = A.double().numpy()[:, :1]
+    step = np.abs(exact) * 2.0 ** -8 + 1e-38           # one bf16 rounding step
+    allowed = step + 0.5 * np.abs(x) * 1.5e-7 * 1.01
+    assert np.all(np.abs(got - exact) <= allowed), np.argwhere(np.abs(got - exact) > allowed)[:5]
+    want = oracle_rounded_bits(A, B, bias, "gelu", g.BF16)
+    core = (x[:, 0] >= -1.0)                         # 1 + erf >= 0.31: the bound is relative here
+    assert (device_bits(out)[core] == want[core]).mean() > 0.98
