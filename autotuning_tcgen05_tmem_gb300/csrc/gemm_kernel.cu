@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "kernel_params.h"
 #include "schedule.h"
@@ -309,6 +310,34 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
     for (int i = 0; i < 256; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return wait_slow(bar, parity, c, site, true, c.timeout_ns);
+}
+
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *ptr)
+{
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+// Waits until *ptr >= target (other CTAs of this launch increment it), with
+// the same bound and abort protocol as the mbarrier waits.
+__device__ __noinline__ bool wait_counter(const int32_t *ptr, int32_t target, const WaitCtl &c, int32_t site)
+{
+    if (ld_acquire_gpu(ptr) >= target) return true;
+    const long long limit_cycles = (long long)((double)c.timeout_ns * 2.2);
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(32);
+        if (ld_acquire_gpu(ptr) >= target) return true;
+        if ((it & 15u) == 0) {
+            if (*c.abort) return false;
+            if (clock64() - t0 > limit_cycles) {
+                *c.abort = 1;
+                atomicCAS(c.status, 0, site);
+                return false;
+            }
+        }
+    }
 }
 
 // Teardown waits (copies / MMAs already issued): one second, abort flag ignored.
@@ -664,6 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------
         const int32_t e_bn = p.bn, e_bm = p.bm, e_epi = p.epi, e_cols = p.cols, e_rows = p.rows;
         const int32_t e_split_k = p.split_k, e_swap_ab = p.swap_ab;
+        const bool e_coop = p.coop_fixup != 0;
         const uint32_t e_acc_cols = p.acc_cols, e_n_acc = p.n_acc;
         const void *const e_bias = p.bias;
         float *const e_workspace = p.workspace;
@@ -766,84 +796,97 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             if (e_split_k > 1) {
-                // The last K slice to arrive sums the partial tiles in slice
-                // order (deterministic) and applies the epilogue.  Each warp
-                // issues all loads of a slice (or of four slices, swapped)
-                // before adding them, so L2 round trips overlap.
+                // Split-K fix-up.  Cooperative (one wave, cooperative launch):
+                // every K slice of the tile arrives, waits for the others, and
+                // finalises its share of the tile's 32-row blocks (block b goes to
+                // slice b mod S); the last slice to leave resets the counter.
+                // Otherwise the last slice to arrive finalises the whole tile.
+                // Either way the partials are summed in slice order.
                 __threadfence();
                 named_bar_sync(1, kEpiThreads);
                 if (ew == 0 && lane == 0) {
                     const int32_t old = atomicAdd(e_counters + w.tile, 1);
-                    const int32_t last = (old == e_split_k - 1) ? 1 : 0;
-                    if (last) atomicExch(e_counters + w.tile, 0);
-                    *last_flag = last;
+                    int32_t mine;
+                    if (e_coop) {
+                        mine = wait_counter(e_counters + w.tile, e_split_k, ctl, SITE_FIXUP) ? 1 : 0;
+                    } else {
+                        mine = (old == e_split_k - 1) ? 1 : 0;
+                        if (mine) atomicExch(e_counters + w.tile, 0);
+                    }
+                    *last_flag = mine;
                 }
                 named_bar_sync(1, kEpiThreads);
-                const bool is_last = *last_flag != 0;
+                const bool mine = *last_flag != 0;
                 named_bar_sync(1, kEpiThreads);   // the flag is rewritten by the next unit
-                if (is_last) {
+                if (mine) {
                     __threadfence();
                     const float4 *tile_ws = reinterpret_cast<const float4 *>(
                         e_workspace + (size_t)w.tile * e_split_k * (size_t)tile_elems);
                     const size_t slice4 = (size_t)tile_elems / 4;
-                    for (int32_t h = 0; h < halves; ++h) {
-                        const int32_t r = h * 128 + q * 32 + lane;
+                    const int32_t rgroups = e_bm / 32;
+                    const int32_t nblocks = rgroups * chunks;
+                    const int32_t first_b = e_coop ? w.split : 0, stride = e_coop ? e_split_k : 1;
+                    for (int32_t b = first_b + stride * ew; b < nblocks; b += stride * kEpiWarps) {
+                        const int32_t rg = b % rgroups, c = b / rgroups;
+                        const int32_t r = rg * 32 + lane;
                         if (!e_swap_ab) {
+                            float v[32];
 #pragma unroll
-                            for (int ci = 0; ci < 4; ++ci) {
-                                const int32_t c = cg + 2 * ci;
-                                if (c >= chunks) break;
-                                float v[32];
+                            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                            const float4 *src = tile_ws + (size_t)(c * 8) * e_bm + r;
+                            const float lb = e_epi != 0 ? load_bias1<DT>(e_bias, c0 + c * 32 + lane, e_cols) : 0.0f;
+                            for (int32_t s = 0; s < e_split_k; ++s) {
+                                float4 t[8];
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                                const float4 *src = tile_ws + (size_t)(c * 8) * e_bm + r;
-                                for (int32_t s = 0; s < e_split_k; ++s) {
-                                    float4 t[8];
+                                for (int j4 = 0; j4 < 8; ++j4) t[j4] = __ldcg(src + s * slice4 + (size_t)j4 * e_bm);
 #pragma unroll
-                                    for (int j4 = 0; j4 < 8; ++j4) t[j4] = __ldcg(src + s * slice4 + (size_t)j4 * e_bm);
-#pragma unroll
-                                    for (int j4 = 0; j4 < 8; ++j4) {
-                                        v[4 * j4] += t[j4].x;
-                                        v[4 * j4 + 1] += t[j4].y;
-                                        v[4 * j4 + 2] += t[j4].z;
-                                        v[4 * j4 + 3] += t[j4].w;
-                                    }
+                                for (int j4 = 0; j4 < 8; ++j4) {
+                                    v[4 * j4] += t[j4].x;
+                                    v[4 * j4 + 1] += t[j4].y;
+                                    v[4 * j4 + 2] += t[j4].z;
+                                    v[4 * j4 + 3] += t[j4].w;
                                 }
-                                bias_act_rows(v, bcol[ci], e_epi);
-                                const int32_t n = c0 + c * 32, y = r0 + h * 128 + q * 32;
-                                store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                             }
+                            bias_act_rows(v, lb, e_epi);
+                            const int32_t n = c0 + c * 32, y = r0 + rg * 32;
+                            store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                         } else {
-                            for (int32_t c = cg; c < chunks; c += 2) {
-                                float v[16];
+                            float v[16];
 #pragma unroll
-                                for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-                                const float4 *src = tile_ws + (size_t)(c * 4) * e_bm + r;
-                                for (int32_t s = 0; s < e_split_k; s += 4) {
-                                    float4 t[4][4];
+                            for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+                            const float4 *src = tile_ws + (size_t)(c * 4) * e_bm + r;
+                            const float rb = e_epi != 0 ? load_bias1<DT>(e_bias, r0 + r, e_rows) : 0.0f;
+                            for (int32_t s = 0; s < e_split_k; s += 4) {
+                                float4 t[4][4];
 #pragma unroll
-                                    for (int i = 0; i < 4; ++i)
-                                        if (s + i < e_split_k) {
+                                for (int i = 0; i < 4; ++i)
+                                    if (s + i < e_split_k) {
 #pragma unroll
-                                            for (int j4 = 0; j4 < 4; ++j4)
-                                                t[i][j4] = __ldcg(src + (s + i) * slice4 + (size_t)j4 * e_bm);
+                                        for (int j4 = 0; j4 < 4; ++j4)
+                                            t[i][j4] = __ldcg(src + (s + i) * slice4 + (size_t)j4 * e_bm);
+                                    }
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    if (s + i < e_split_k) {
+#pragma unroll
+                                        for (int j4 = 0; j4 < 4; ++j4) {
+                                            v[4 * j4] += t[i][j4].x;
+                                            v[4 * j4 + 1] += t[i][j4].y;
+                                            v[4 * j4 + 2] += t[i][j4].z;
+                                            v[4 * j4 + 3] += t[i][j4].w;
                                         }
-#pragma unroll
-                                    for (int i = 0; i < 4; ++i)
-                                        if (s + i < e_split_k) {
-#pragma unroll
-                                            for (int j4 = 0; j4 < 4; ++j4) {
-                                                v[4 * j4] += t[i][j4].x;
-                                                v[4 * j4 + 1] += t[i][j4].y;
-                                                v[4 * j4 + 2] += t[i][j4].z;
-                                                v[4 * j4 + 3] += t[i][j4].w;
-                                            }
-                                        }
-                                }
-                                bias_act_cols(v, h == 0 ? brow[0] : brow[1], e_epi);
-                                const int32_t xn = r0 + h * 128 + q * 32, ym = c0 + c * 16;
-                                store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
+                                    }
                             }
+                            bias_act_cols(v, rb, e_epi);
+                            const int32_t xn = r0 + rg * 32, ym = c0 + c * 16;
+                            store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
+                        }
+                    }
+                    if (e_coop) {
+                        named_bar_sync(1, kEpiThreads);
+                        if (ew == 0 && lane == 0) {
+                            const int32_t old = atomicAdd(e_counters + w.tile, 1);
+                            if (old == 2 * e_split_k - 1) atomicExch(e_counters + w.tile, 0);
                         }
                     }
                 }
@@ -963,7 +1006,21 @@ cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, cons
     if (!f) return cudaErrorInvalidValue;
     void *args[] = {const_cast<CUtensorMap *>(&a), const_cast<CUtensorMap *>(&b), const_cast<CUtensorMap *>(&c),
                     const_cast<KernelParams *>(&p)};
-    return cudaLaunchKernel(f, dim3(grid), dim3(kThreads), args, (size_t)smem_bytes, stream);
+    if (!p.coop_fixup) return cudaLaunchKernel(f, dim3(grid), dim3(kThreads), args, (size_t)smem_bytes, stream);
+    // CTAs of a cooperative fix-up wait on each other: launch them cooperatively
+    // so that all are resident at once.
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, f, args);
 }
 
 cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t cols, int elt, cudaStream_t stream)

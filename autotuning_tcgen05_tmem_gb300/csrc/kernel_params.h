@@ -12,6 +12,7 @@ enum WaitSite : int32_t {
     SITE_EPI_TMEM_FULL = 4,
     SITE_EPI_STALL = 5,
     SITE_TEARDOWN = 6,
+    SITE_FIXUP = 7,
 };
 
 struct KernelParams {
@@ -34,7 +35,8 @@ struct KernelParams {
     int32_t *status;                   // device status word (0 = ok)
     int64_t timeout_ns;                // bound of every mbarrier wait
     int32_t debug_stall;               // epilogue waits on a barrier nothing signals
-    int32_t pad_;
+    int32_t coop_fixup;                // split-K slices finalise shares of their tile together
+                                       // (launched cooperatively: every unit has its own CTA)
 };
 
 }  // namespace gemmgb

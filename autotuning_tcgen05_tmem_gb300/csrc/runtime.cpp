@@ -266,6 +266,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     k.off_bar = p->L.off_bar;
     k.staging_buf_bytes = p->L.staging_buf_bytes;
     p->grid = (int)std::min<int64_t>(k.num_units, dev.sm_count);
+    // One wave of split-K units: the slices of a tile finalise it together.
+    k.coop_fixup = (cfg.split_k > 1 && k.num_units <= dev.sm_count) ? 1 : 0;
     // Ask for more than half of the SM's shared memory so that no two CTAs of
     // this kernel share an SM (each may hold up to 512 TMEM columns).
     const int64_t one_per_sm = dev.smem_per_block / 2 + 1024;
