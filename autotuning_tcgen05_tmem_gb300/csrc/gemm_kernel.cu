@@ -506,6 +506,34 @@ __device__ __forceinline__ void store_cols_chunk(const CUtensorMap *tmC, StoreRi
     ring.count++;
 }
 
+// One pipeline stage's MMAs: KSTEPS K-steps of 32 bytes, each as HALVES
+// 128-row MMAs into consecutive accumulator column blocks.
+struct MmaStage {
+    uint32_t d0;            // TMEM address of the accumulator
+    uint64_t adesc, bdesc;  // descriptors of the stage's A and B tiles
+    uint32_t idesc;
+    uint32_t a_span_step, b_span_step, a_half_step;  // 16-byte units
+    uint32_t bn;
+    bool accumulate_first;  // false on the unit's first K-block
+};
+
+template <int DT, bool A_MN, bool B_MN, int KSTEPS, int HALVES>
+__device__ __forceinline__ void issue_stage(const MmaStage &st)
+{
+    constexpr int ELT = Elt<DT>::BYTES;
+    constexpr uint32_t MN_KSTEP16 = ((32u / ELT) * 128u) >> 4;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+        const uint32_t a_k = A_MN ? (uint32_t)kk * MN_KSTEP16 : (uint32_t)(kk >> 2) * st.a_span_step + (kk & 3) * 2u;
+        const uint32_t b_k = B_MN ? (uint32_t)kk * MN_KSTEP16 : (uint32_t)(kk >> 2) * st.b_span_step + (kk & 3) * 2u;
+        const uint32_t acc = (st.accumulate_first || kk != 0) ? 1u : 0u;
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h)
+            umma<DT>(st.d0 + (uint32_t)h * st.bn, st.adesc + a_k + (uint32_t)h * st.a_half_step, st.bdesc + b_k,
+                     st.idesc, acc);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -630,8 +658,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_lbo = p.a_lbo, b_lbo = p.b_lbo;
         const int32_t ksteps = bk * ELT / 32;
         const int32_t halves = bm / 128;
-        // Descriptor increments, in the 16-byte units of the start-address field.
+        // Descriptor increments, in the 16-byte units of the start-address field:
+        // next 128-row half of A; next 128-byte K span of a K-major operand.
         const uint32_t a_half_step = A_MN ? (uint32_t)((128 / SPAN) * bk * 128) >> 4 : (128u * 128u) >> 4;
+        const uint32_t a_span_step = (uint32_t)(bm * 128) >> 4;
+        const uint32_t b_span_step = (uint32_t)(bn * 128) >> 4;
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool issued = false, ok = true;
         for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
@@ -648,15 +679,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t adesc = smem_desc(base + stage * a_bytes, a_lbo);
                 const uint64_t bdesc = smem_desc(sb0 + stage * b_bytes, b_lbo);
                 if (leader) {
-                    for (int32_t kk = 0; kk < ksteps; ++kk) {
-                        const uint32_t a_k = A_MN ? (uint32_t)kk * (MN_KSTEP >> 4)
-                                                  : (uint32_t)((kk >> 2) * bm * 8 + (kk & 3) * 2);
-                        const uint32_t b_k = B_MN ? (uint32_t)kk * (MN_KSTEP >> 4)
-                                                  : (uint32_t)((kk >> 2) * bn * 8 + (kk & 3) * 2);
-                        const uint32_t accumulate = (kb | kk) != 0 ? 1u : 0u;
-                        for (int32_t h = 0; h < halves; ++h)
-                            umma<DT>(d0 + (uint32_t)(h * bn), adesc + a_k + h * a_half_step, bdesc + b_k, idesc,
-                                     accumulate);
+                    // The k-step loop is unrolled for every (K steps, halves) the
+                    // rules allow: with a runtime bound the loop bookkeeping costs
+                    // more than an MMA's issue and starves the tensor pipe.
+                    const MmaStage st{d0, adesc, bdesc, idesc, a_span_step, b_span_step, a_half_step,
+                                      (uint32_t)bn, kb != 0};
+                    switch (ksteps * 2 + halves - 1) {
+                    case 8: issue_stage<DT, A_MN, B_MN, 4, 1>(st); break;
+                    case 9: issue_stage<DT, A_MN, B_MN, 4, 2>(st); break;
+                    case 16: issue_stage<DT, A_MN, B_MN, 8, 1>(st); break;
+                    case 17: issue_stage<DT, A_MN, B_MN, 8, 2>(st); break;
+                    case 24: issue_stage<DT, A_MN, B_MN, 12, 1>(st); break;
+                    case 25: issue_stage<DT, A_MN, B_MN, 12, 2>(st); break;
+                    case 32: issue_stage<DT, A_MN, B_MN, 16, 1>(st); break;
+                    default: issue_stage<DT, A_MN, B_MN, 16, 2>(st); break;
                     }
                     umma_commit(empty0 + 8u * stage);  // slot is free once these MMAs have read it
                 }
