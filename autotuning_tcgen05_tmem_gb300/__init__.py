@@ -69,13 +69,12 @@ def make_config(bm, bn, bk, stages, raster=0, group=1, split_k=1, cta_group=1, s
 
 class DeviceParams(ctypes.Structure):
     _fields_ = [("sm_count", ctypes.c_int32), ("model_kind", ctypes.c_int32),
-                ("smem_per_block", ctypes.c_int64), ("l2_bytes", ctypes.c_int64),
-                ("peak_tflops_bf16", ctypes.c_double), ("peak_tflops_tf32", ctypes.c_double),
-                ("hbm_gbs", ctypes.c_double), ("sm_clock_mhz", ctypes.c_double),
-                ("mma_flops_per_clk_bf16", ctypes.c_double), ("mma_flops_per_clk_tf32", ctypes.c_double),
-                ("smem_bytes_per_clk", ctypes.c_double), ("mem_latency_us", ctypes.c_double),
-                ("epi_elems_per_clk", ctypes.c_double), ("launch_us", ctypes.c_double),
-                ("kernel_regs", ctypes.c_int32), ("threads_per_cta", ctypes.c_int32)]
+                ("smem_per_block", ctypes.c_int64), ("l2_bytes", ctypes.c_int64)] + \
+               [(n, ctypes.c_double) for n in
+                ("peak_tflops_bf16", "peak_tflops_tf32", "hbm_gbs", "sm_clock_mhz", "l2_gbs", "mma_issue_clk",
+                 "kblock_clk", "mem_latency_us", "epi_elems_per_clk", "epi_gelu_elems_per_clk", "splitk_gbs",
+                 "launch_us")] + \
+               [("kernel_regs", ctypes.c_int32), ("threads_per_cta", ctypes.c_int32)]
 
     def asdict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -83,8 +82,8 @@ class DeviceParams(ctypes.Structure):
 
 class ModelTerms(ctypes.Structure):
     _fields_ = [(n, ctypes.c_double) for n in
-                ("predicted_us", "compute_us", "memory_us", "latency_us", "epilogue_us", "fill_us",
-                 "wave_eff", "tile_eff", "pad_eff", "hbm_bytes", "flops")] + \
+                ("predicted_us", "mma_us", "l2_us", "hbm_us", "latency_us", "epilogue_us", "splitk_us",
+                 "launch_us", "wave_eff", "tile_eff", "pad_eff", "hbm_bytes", "l2_bytes", "flops")] + \
                [(n, ctypes.c_int64) for n in ("tiles", "units", "waves", "ctas")]
 
     def asdict(self):

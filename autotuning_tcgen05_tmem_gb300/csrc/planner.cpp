@@ -27,6 +27,9 @@
 
 namespace gemmgb {
 
+// GB300 values.  Peaks: a measured copy bandwidth and cuBLAS bf16 burst rate on
+// this part; model coefficients: least-squares fit (log time) to exhaustive
+// tuning tables of 34 workloads on a GB300 (gemm_tune, every candidate timed).
 void params_default(gemm_device_params *d)
 {
     memset(d, 0, sizeof(*d));
@@ -34,16 +37,18 @@ void params_default(gemm_device_params *d)
     d->model_kind = 0;
     d->smem_per_block = 232448;
     d->l2_bytes = 129LL * 1024 * 1024;
-    d->peak_tflops_bf16 = 2250.0;
-    d->peak_tflops_tf32 = 1125.0;
-    d->hbm_gbs = 7900.0;
+    d->peak_tflops_bf16 = 1889.6;
+    d->peak_tflops_tf32 = 944.8;
+    d->hbm_gbs = 6675.8;
     d->sm_clock_mhz = 2070.0;
-    d->mma_flops_per_clk_bf16 = 8192.0;
-    d->mma_flops_per_clk_tf32 = 4096.0;
-    d->smem_bytes_per_clk = 128.0;
-    d->mem_latency_us = 0.8;
-    d->epi_elems_per_clk = 64.0;
-    d->launch_us = 4.0;
+    d->l2_gbs = 15020.0;
+    d->mma_issue_clk = 40.3;
+    d->kblock_clk = 482.5;
+    d->mem_latency_us = 1.358;
+    d->epi_elems_per_clk = 3.08;
+    d->epi_gelu_elems_per_clk = 5.21;
+    d->splitk_gbs = 17.55;
+    d->launch_us = 7.68;
     d->kernel_regs = 0;
     d->threads_per_cta = kThreadsPerCta;
 }
@@ -225,8 +230,8 @@ static gemm_model_terms predict_workshop(int64_t M, int64_t N, int64_t K, int dt
     const double floor_b = ((double)M * K + (double)K * N + (double)M * N) * e;
     const double bytes = std::max(panel, floor_b);
     const double memory = bytes / (d.hbm_gbs * 1e9);
-    t.compute_us = compute * 1e6;
-    t.memory_us = memory * 1e6;
+    t.mma_us = compute * 1e6;
+    t.hbm_us = memory * 1e6;
     t.predicted_us = std::max(compute, memory) * 1e6;
     t.wave_eff = weff;
     t.tile_eff = teff;
@@ -254,28 +259,31 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
     const int64_t num_kb = cdiv(K, c.bk);
     const int64_t units = tiles * S;
     const int64_t sms = d.sm_count;
-    const int64_t ctas = std::min(units, sms);
+    const int64_t ctas = std::max<int64_t>(1, std::min(units, sms));
     const int64_t waves = cdiv(units, sms);
-    const double weff = (double)units / ((double)waves * sms);
-
-    // Tensor pipe: one tcgen05 MMA is 128 x bn x (32 bytes of K); it needs
-    // (128 + bn) rows x 32 bytes of operands from shared memory.  The slower of
-    // the two clocks sets the tile efficiency.
+    const int64_t upc = cdiv(units, ctas);           // units of the busiest CTA
+    const int64_t kbu = cdiv(num_kb, S);             // K-blocks of the longest slice
+    const double clk = d.sm_clock_mhz * 1e6;
     const double flops = 2.0 * (double)M * (double)N * (double)K;
-    const double peak = (dt == GEMM_BF16 ? d.peak_tflops_bf16 : d.peak_tflops_tf32) * 1e12;
-    const double fpc = dt == GEMM_BF16 ? d.mma_flops_per_clk_bf16 : d.mma_flops_per_clk_tf32;
-    const double kslice = 32.0 / e;
-    const double mma_clk = 2.0 * 128.0 * c.bn * kslice / fpc;
-    const double smem_clk = (128.0 + c.bn) * 32.0 / d.smem_bytes_per_clk;
-    const double teff = mma_clk / std::max(mma_clk, smem_clk);
-    const double peff = K > 0 ? ((double)rows * cols * K) /
-                                    ((double)tiles_m * c.bm * (double)tiles_n * c.bn * (double)num_kb * c.bk)
-                              : 1.0;
-    const double compute = flops > 0 ? flops / (peak * weff * teff * peff) : 0.0;
 
-    // HBM: operands either fit in half of L2 (threshold regime: compulsory
-    // bytes only) or are re-read once per wave of concurrent tiles, with the
-    // wave's footprint shaped by the tile order (group-G band).
+    // Tensor pipe, per K-block of one CTA: the MMAs execute at the per-SM share
+    // of the peak, and the issuing warp spends mma_issue_clk per MMA plus
+    // kblock_clk per stage; the slower of the two sets the pace.
+    const double peak = (dt == GEMM_BF16 ? d.peak_tflops_bf16 : d.peak_tflops_tf32) * 1e12;
+    const double halves = c.bm / 128, ksteps = (double)c.bk * e / 32.0, kslice = 32.0 / e;
+    const double mma_flop = 2.0 * 128.0 * c.bn * kslice;
+    const double t_exec = halves * ksteps * mma_flop / (peak / (double)sms);
+    const double t_issue = (halves * ksteps * d.mma_issue_clk + d.kblock_clk) / clk;
+    const double t_mma = (double)upc * (double)kbu * std::max(t_exec, t_issue);
+
+    // L2 -> shared memory: every unit streams (bm + bn)·bk·elt bytes per K-block
+    // ("Tile Selection": per-block panel traffic; reuse across blocks is in L2).
+    const double l2_bytes = (double)units * (double)kbu * (c.bm + c.bn) * (double)c.bk * e;
+    const double t_l2 = l2_bytes / (d.l2_gbs * 1e9);
+
+    // HBM: operands either fit in half of L2 (threshold regime: compulsory bytes
+    // only) or are re-read once per wave of concurrent tiles, with the wave's
+    // footprint shaped by the tile order (group-G band).
     const double in_bytes = ((double)M * K + (double)K * N) * e;
     const int64_t wave_tiles = std::min<int64_t>(tiles, std::max<int64_t>(1, ctas / S));
     int64_t rows_w, cols_w;
@@ -286,37 +294,57 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
         cols_w = std::min<int64_t>(std::min<int64_t>(c.group, tiles_n), wave_tiles);
         rows_w = std::min<int64_t>(cdiv(wave_tiles, cols_w), tiles_m);
     }
-    const double wave_bytes = (double)K * ((double)rows_w * c.bm + (double)cols_w * c.bn) * e;
-    const double panel = ((double)tiles / (double)wave_tiles) * wave_bytes;
+    const double panel = ((double)tiles / (double)wave_tiles) * (double)K *
+                         ((double)rows_w * c.bm + (double)cols_w * c.bn) * e;
     const double operand = (in_bytes <= (double)d.l2_bytes / 2.0) ? in_bytes : std::max(in_bytes, panel);
-    const double epi_bytes = (double)M * N * e + (epi != GEMM_EPI_NONE ? (double)N * e : 0.0);
-    const double split_bytes = S > 1 ? (double)units * c.bm * c.bn * 4.0 : 0.0;
-    const double hbm = operand + epi_bytes + split_bytes;
-    const double memory = hbm / (d.hbm_gbs * 1e9);
+    const double hbm = operand + (double)M * N * e + (epi != GEMM_EPI_NONE ? (double)N * e : 0.0);
+    const double t_hbm = hbm / (d.hbm_gbs * 1e9);
 
-    // Bytes in flight: a CTA keeps at most `stages` slots outstanding, so one
-    // memory latency covers `stages` K-steps.
-    const int64_t per_cta_units = ctas > 0 ? cdiv(units, ctas) : 0;
-    const double per_cta_kb = (double)per_cta_units * (double)cdiv(num_kb, S);
-    const double latency = per_cta_kb * d.mem_latency_us * 1e-6 / c.stages;
-    // Epilogue: drains bm·bn accumulators per unit; overlapped with the next
-    // unit's main loop, so it bounds the CTA only when it is the slower stage.
-    const double epi_unit = (double)c.bm * c.bn / (d.epi_elems_per_clk * d.sm_clock_mhz * 1e6);
-    const double epilogue = (double)per_cta_units * epi_unit;
-    const double body = std::max(std::max(compute, memory), std::max(latency, epilogue));
-    const double fill = d.mem_latency_us * 1e-6 + epi_unit;
-    const double total = body + fill + d.launch_us * 1e-6;
+    // Bytes in flight ("Tiling the hierarchy", double buffering): the ring
+    // covers one load latency per `stages` K-blocks.
+    const double t_lat = (double)upc * (double)kbu * d.mem_latency_us * 1e-6 / c.stages;
+    const double t_main = std::max(std::max(t_mma, t_l2), std::max(t_hbm, t_lat));
+
+    // Epilogue and split-K exchange.
+    const double rate = (epi == GEMM_EPI_BIAS_GELU ? d.epi_gelu_elems_per_clk : d.epi_elems_per_clk) * clk;
+    const double elems = (double)c.bm * c.bn;
+    const double part = elems * 4.0;
+    double exposed, t_split;
+    if (S == 1) {
+        // Double-buffered accumulators hide the epilogue behind the next unit's
+        // main loop unless it is the slower of the two.
+        const double epi_t = elems / rate;
+        const bool two_acc = 2.0 * halves * c.bn <= (double)kTmemColumns;
+        const double main_unit = t_main / (double)upc;
+        exposed = epi_t + (double)(upc - 1) * (two_acc ? std::max(0.0, epi_t - main_unit) : epi_t);
+        t_split = 0.0;
+    } else if (units <= sms) {
+        // Cooperative fix-up: write one partial tile, read one share of S.
+        exposed = elems / (double)S / rate;
+        t_split = 2.0 * part / (d.splitk_gbs * 1e9);
+    } else {
+        // Last arriver: the CTA finishing a tile reads all S partials.
+        const double fix_tiles = (double)cdiv(tiles, ctas);
+        exposed = fix_tiles * elems / rate;
+        t_split = ((double)upc + fix_tiles * (double)S) * part / (d.splitk_gbs * 1e9);
+    }
+    const double total = t_main + exposed + t_split + d.launch_us * 1e-6;
 
     t.predicted_us = total * 1e6;
-    t.compute_us = compute * 1e6;
-    t.memory_us = memory * 1e6;
-    t.latency_us = latency * 1e6;
-    t.epilogue_us = epilogue * 1e6;
-    t.fill_us = fill * 1e6;
-    t.wave_eff = weff;
-    t.tile_eff = teff;
-    t.pad_eff = peff;
+    t.mma_us = t_mma * 1e6;
+    t.l2_us = t_l2 * 1e6;
+    t.hbm_us = t_hbm * 1e6;
+    t.latency_us = t_lat * 1e6;
+    t.epilogue_us = exposed * 1e6;
+    t.splitk_us = t_split * 1e6;
+    t.launch_us = d.launch_us;
+    t.wave_eff = (double)units / ((double)waves * (double)sms);
+    t.tile_eff = t_exec / std::max(t_exec, t_issue);
+    t.pad_eff = K > 0 ? ((double)rows * cols * K) /
+                            ((double)tiles_m * c.bm * (double)tiles_n * c.bn * (double)num_kb * c.bk)
+                      : 1.0;
     t.hbm_bytes = hbm;
+    t.l2_bytes = l2_bytes;
     t.flops = flops;
     t.tiles = tiles;
     t.units = units;

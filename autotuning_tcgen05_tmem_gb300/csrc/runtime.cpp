@@ -751,7 +751,7 @@ int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *ou
     }
     const char *mode = getenv("GEMM_TUNE_MODE");
     const bool exhaustive = mode && strcmp(mode, "exhaustive") == 0;
-    const int topk = exhaustive ? 0 : std::max(1, env_int("GEMM_TUNE_TOPK", 12));
+    const int topk = exhaustive ? 0 : std::max(1, env_int("GEMM_TUNE_TOPK", 24));
     std::vector<gemm_tune_row> rows;
     gemm_rank_stats stats;
     rc = tune(M, N, K, dt, epi, topk, rows, stats, &cfg);

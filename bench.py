@@ -399,7 +399,7 @@ def main():
         out["fixed_config"] = fixed.asdict()
         out["fixed_value"] = flops / fixed_gemm_s / 1e12
         out["tuned_vs_fixed"] = fixed_gemm_s / gemm_s
-        tr = g.tune(w.M, w.N, w.K, w.dtype, w.epi, topk=int(os.environ.get("GEMM_TUNE_TOPK", "12")))
+        tr = g.tune(w.M, w.N, w.K, w.dtype, w.epi, topk=int(os.environ.get("GEMM_TUNE_TOPK", "24")))
         st = tr.stats
         saved_us = max(st.fixed_us - st.best_us, 0.0) if st.fixed_us > 0 else 0.0
         out["tune"] = {"candidates": st.n_candidates, "measured": st.n_measured,

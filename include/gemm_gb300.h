@@ -119,9 +119,10 @@ typedef enum {
 /*
  * Device and cost-model parameters ("Tile Selection", "Selection is per device":
  * the SM count and the limits are properties of the device; never hard-coded).
- * gemm_device_params_query fills it from the current device; the model
- * coefficients start from the nominal values listed in the comments and may be
- * overridden by the caller (e.g. with measured peaks).
+ * gemm_device_params_query fills the device fields from the current device;
+ * the model coefficients default to values fitted on a GB300 (least squares in
+ * log time over exhaustive tuning tables of the library's own workloads) and may
+ * be overridden by the caller.
  */
 typedef struct {
     int32_t sm_count;               /* multiprocessors */
@@ -129,25 +130,34 @@ typedef struct {
                                        "Compilers and Kernel Languages" */
     int64_t smem_per_block;         /* opt-in dynamic shared memory per block, bytes */
     int64_t l2_bytes;
-    double  peak_tflops_bf16;       /* dense tensor peak */
+    double  peak_tflops_bf16;       /* dense tensor peak (measured burst on GB300) */
     double  peak_tflops_tf32;
     double  hbm_gbs;                /* DRAM bandwidth, GB/s */
     double  sm_clock_mhz;
-    double  mma_flops_per_clk_bf16; /* per SM (nominal 8192) */
-    double  mma_flops_per_clk_tf32; /* per SM (nominal 4096) */
-    double  smem_bytes_per_clk;     /* per SM operand bandwidth feeding the MMA (128) */
-    double  mem_latency_us;         /* load round trip, for the fill and bytes-in-flight terms */
-    double  epi_elems_per_clk;      /* per SM accumulators drained by the epilogue per clock */
-    double  launch_us;              /* fixed launch + teardown cost */
+    double  l2_gbs;                 /* aggregate L2 -> shared-memory operand bandwidth, GB/s */
+    double  mma_issue_clk;          /* issue cost of one tcgen05.mma, SM clocks */
+    double  kblock_clk;             /* per pipeline stage: waits, commits, bookkeeping */
+    double  mem_latency_us;         /* load round trip seen by the shared-memory ring */
+    double  epi_elems_per_clk;      /* epilogue throughput per CTA, none/bias/ReLU */
+    double  epi_gelu_elems_per_clk; /* epilogue throughput per CTA with GELU */
+    double  splitk_gbs;             /* per-CTA bandwidth of split-K partial-tile traffic */
+    double  launch_us;              /* launch + prologue */
     int32_t kernel_regs;            /* registers/thread of the GEMM kernel (0 = unknown) */
     int32_t threads_per_cta;        /* 320 */
 } gemm_device_params;
 
 /* Terms of one cost-model prediction (times in microseconds). */
 typedef struct {
-    double predicted_us, compute_us, memory_us, latency_us, epilogue_us, fill_us;
+    double predicted_us;   /* max(mma, l2, hbm, latency) + epilogue + splitk + launch */
+    double mma_us;         /* tensor pipe: max(execute, issue) per K-block, per CTA */
+    double l2_us;          /* operand panels streamed from L2 into shared memory */
+    double hbm_us;         /* DRAM bytes (compulsory, or per-wave panels past L2) */
+    double latency_us;     /* K-blocks x load latency / stages (bytes in flight) */
+    double epilogue_us;    /* epilogue not hidden behind a main loop */
+    double splitk_us;      /* partial-tile writes and the fix-up reads */
+    double launch_us;
     double wave_eff, tile_eff, pad_eff;
-    double hbm_bytes, flops;
+    double hbm_bytes, l2_bytes, flops;
     int64_t tiles, units, waves, ctas;
 } gemm_model_terms;
 
@@ -243,7 +253,7 @@ int gemm_device_params_query(gemm_device_params *out);
  * candidates on library-owned buffers → cache the winner ("Autotuning & cost
  * models" §4; "CuTile Autotuning").  Environment: GEMM_DISABLE_AUTOTUNE=1 picks
  * the fixed config without timing; GEMM_TUNE_MODE=exhaustive|topk (default
- * topk); GEMM_TUNE_TOPK=k (default 12).  Synchronises; never touches user
+ * topk); GEMM_TUNE_TOPK=k (default 24).  Synchronises; never touches user
  * memory.  The returned handle is owned by the caller (gemm_plan_destroy) and
  * may be used on one stream at a time. */
 int gemm_plan(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,

@@ -250,17 +250,19 @@ class Device:
     sm_count: int = 152
     model_kind: int = 0
     smem_per_block: int = 232448
-    l2_bytes: int = 126 * 1024 * 1024
+    l2_bytes: int = 129 * 1024 * 1024
     peak_tflops_bf16: float = 1889.6
     peak_tflops_tf32: float = 944.8
     hbm_gbs: float = 6675.8
-    sm_clock_mhz: float = 1920.0
-    mma_flops_per_clk_bf16: float = 8192.0
-    mma_flops_per_clk_tf32: float = 4096.0
-    smem_bytes_per_clk: float = 128.0
-    mem_latency_us: float = 0.8
-    epi_elems_per_clk: float = 64.0
-    launch_us: float = 4.0
+    sm_clock_mhz: float = 2070.0
+    l2_gbs: float = 15020.0
+    mma_issue_clk: float = 40.3
+    kblock_clk: float = 482.5
+    mem_latency_us: float = 1.358
+    epi_elems_per_clk: float = 3.08
+    epi_gelu_elems_per_clk: float = 5.21
+    splitk_gbs: float = 17.55
+    launch_us: float = 7.68
     kernel_regs: int = 0
     threads_per_cta: int = THREADS_PER_CTA
     extra: dict = field(default_factory=dict)
@@ -420,7 +422,15 @@ def schedule_unit(u, tiles_m, tiles_n, split_k, raster, group, num_kb):
 # ---------------------------------------------------------------------------
 
 def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
-    """Predicted time and its terms (a dict, times in microseconds)."""
+    """Predicted time and its terms (a dict, times in microseconds).
+
+    Terms (documented model): the busiest CTA's K-blocks times the slower of MMA
+    execution (per-SM share of the peak) and MMA issue (issue clocks per MMA +
+    clocks per stage); L2 -> shared-memory panel bytes over the L2 bandwidth;
+    HBM bytes (compulsory when A+B fit in half of L2, otherwise per-wave panels)
+    over the HBM bandwidth; K-blocks × latency / stages; their maximum, plus the
+    epilogue time no main loop hides, the split-K partial-tile traffic and the
+    launch cost."""
     if dev.model_kind == 1:
         wd = WorkshopDevice(sms=dev.sm_count, peak_flops=dev.peak_tflops_bf16 * 1e12,
                             bw=dev.hbm_gbs * 1e9, elt=elt_bytes(dtype))
@@ -437,21 +447,23 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
     num_kb = ceil_div(K, cfg.bk)
     units = tiles * S
     sms = dev.sm_count
-    ctas = min(units, sms)
+    ctas = max(1, min(units, sms))
     nw = waves(units, sms)
-    weff = units / (nw * sms)
+    per_cta_units = ceil_div(units, ctas)
+    slice_kb = ceil_div(num_kb, S)
+    clock = dev.sm_clock_mhz * 1e6
     flops = 2.0 * M * N * K
+
     peak = (dev.peak_tflops_bf16 if dtype == DT_BF16 else dev.peak_tflops_tf32) * 1e12
-    fpc = dev.mma_flops_per_clk_bf16 if dtype == DT_BF16 else dev.mma_flops_per_clk_tf32
-    kslice = 32 // elt
-    mma_clk = 2.0 * 128 * cfg.bn * kslice / fpc
-    smem_clk = (128 + cfg.bn) * 32 / dev.smem_bytes_per_clk
-    teff = mma_clk / max(mma_clk, smem_clk)
-    if K > 0:
-        peff = (rows * cols * K) / (tiles_m * cfg.bm * tiles_n * cfg.bn * num_kb * cfg.bk)
-    else:
-        peff = 1.0
-    compute_s = flops / (peak * weff * teff * peff) if flops > 0 else 0.0
+    halves = cfg.bm // 128
+    ksteps = cfg.bk * elt / 32
+    one_mma = 2.0 * 128 * cfg.bn * (32 / elt)
+    execute = halves * ksteps * one_mma / (peak / sms)
+    issue = (halves * ksteps * dev.mma_issue_clk + dev.kblock_clk) / clock
+    mma_s = per_cta_units * slice_kb * max(execute, issue)
+
+    l2_bytes = units * slice_kb * (cfg.bm + cfg.bn) * cfg.bk * elt
+    l2_s = l2_bytes / (dev.l2_gbs * 1e9)
 
     in_bytes = (M * K + K * N) * elt
     wave_tiles = min(tiles, max(1, ctas // S))
@@ -461,31 +473,43 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
     else:
         cols_w = min(cfg.group, tiles_n, wave_tiles)
         rows_w = min(ceil_div(wave_tiles, cols_w), tiles_m)
-    wave_bytes = K * (rows_w * cfg.bm + cols_w * cfg.bn) * elt
-    panel = (tiles / wave_tiles) * wave_bytes
-    if in_bytes <= dev.l2_bytes / 2:
-        operand = in_bytes
-    else:
-        operand = max(in_bytes, panel)
-    epi_bytes = M * N * elt + (N * elt if epi != EPI_NONE else 0)
-    split_bytes = units * cfg.bm * cfg.bn * 4 if S > 1 else 0
-    hbm = operand + epi_bytes + split_bytes
-    memory_s = hbm / (dev.hbm_gbs * 1e9)
+    panel = (tiles / wave_tiles) * K * (rows_w * cfg.bm + cols_w * cfg.bn) * elt
+    operand = in_bytes if in_bytes <= dev.l2_bytes / 2 else max(in_bytes, panel)
+    hbm = operand + M * N * elt + (N * elt if epi != EPI_NONE else 0)
+    hbm_s = hbm / (dev.hbm_gbs * 1e9)
 
-    per_cta_units = ceil_div(units, ctas) if ctas > 0 else 0
-    per_cta_kb = per_cta_units * ceil_div(num_kb, S)
-    latency_s = per_cta_kb * dev.mem_latency_us * 1e-6 / cfg.stages
-    epi_unit_s = cfg.bm * cfg.bn / (dev.epi_elems_per_clk * dev.sm_clock_mhz * 1e6)
-    epilogue_s = per_cta_units * epi_unit_s
-    body = max(compute_s, memory_s, latency_s, epilogue_s)
-    fill_s = dev.mem_latency_us * 1e-6 + epi_unit_s
-    total = body + fill_s + dev.launch_us * 1e-6
-    return {"predicted_us": total * 1e6, "compute_us": compute_s * 1e6,
-            "memory_us": memory_s * 1e6, "latency_us": latency_s * 1e6,
-            "epilogue_us": epilogue_s * 1e6, "fill_us": fill_s * 1e6,
-            "wave_eff": weff, "tile_eff": teff, "pad_eff": peff,
-            "tiles": tiles, "units": units, "waves": nw, "ctas": ctas,
-            "hbm_bytes": hbm, "flops": flops}
+    latency_s = per_cta_units * slice_kb * dev.mem_latency_us * 1e-6 / cfg.stages
+    main = max(mma_s, l2_s, hbm_s, latency_s)
+
+    per_clock = dev.epi_gelu_elems_per_clk if epi == EPI_GELU else dev.epi_elems_per_clk
+    rate = per_clock * clock
+    elems = cfg.bm * cfg.bn
+    partial = elems * 4
+    if S == 1:
+        one = elems / rate
+        two_buffers = 2 * halves * cfg.bn <= TMEM_COLUMNS
+        unit_main = main / per_cta_units
+        hidden_excess = max(0.0, one - unit_main) if two_buffers else one
+        epi_s = one + (per_cta_units - 1) * hidden_excess
+        split_s = 0.0
+    elif units <= sms:
+        epi_s = (elems / S) / rate
+        split_s = 2 * partial / (dev.splitk_gbs * 1e9)
+    else:
+        fix = ceil_div(tiles, ctas)
+        epi_s = fix * elems / rate
+        split_s = (per_cta_units + fix * S) * partial / (dev.splitk_gbs * 1e9)
+    total = main + epi_s + split_s + dev.launch_us * 1e-6
+    if K > 0:
+        pad = (rows * cols * K) / (tiles_m * cfg.bm * tiles_n * cfg.bn * num_kb * cfg.bk)
+    else:
+        pad = 1.0
+    return {"predicted_us": total * 1e6, "mma_us": mma_s * 1e6, "l2_us": l2_s * 1e6,
+            "hbm_us": hbm_s * 1e6, "latency_us": latency_s * 1e6, "epilogue_us": epi_s * 1e6,
+            "splitk_us": split_s * 1e6, "launch_us": dev.launch_us,
+            "wave_eff": units / (nw * sms), "tile_eff": execute / max(execute, issue), "pad_eff": pad,
+            "hbm_bytes": hbm, "l2_bytes": l2_bytes, "flops": flops,
+            "tiles": tiles, "units": units, "waves": nw, "ctas": ctas}
 
 
 # ---------------------------------------------------------------------------

@@ -111,8 +111,8 @@ def test_cost_model_equals_oracle(M, N, K, dt, epi):
     for c in g.enumerate_configs(M, N, K, dt, epi, d):
         t = g.model_predict(M, N, K, dt, epi, c, d).asdict()
         o = sel.gb300_model(M, N, K, dt, epi, to_oracle_config(c), od)
-        for key in ("predicted_us", "compute_us", "memory_us", "latency_us", "epilogue_us", "fill_us",
-                    "wave_eff", "tile_eff", "pad_eff", "hbm_bytes", "flops"):
+        for key in ("predicted_us", "mma_us", "l2_us", "hbm_us", "latency_us", "epilogue_us", "splitk_us",
+                    "launch_us", "wave_eff", "tile_eff", "pad_eff", "hbm_bytes", "l2_bytes", "flops"):
             assert t[key] == pytest.approx(o[key], rel=1e-12, abs=1e-12), (key, c)
         for key in ("tiles", "units", "waves", "ctas"):
             assert t[key] == o[key]

@@ -250,11 +250,15 @@ def test_gb300_check_reasons():
 
 def test_gb300_model_terms_behave():
     dev = sel.Device()
-    # more split-K on an under-filled shape raises wave efficiency
+    # split-K on an under-filled shape raises wave efficiency and shortens the main loop
     a = sel.gb300_model(1000, 1000, 8192, 0, 3, sel.Config(128, 128, 64, 4), dev)
     b = sel.gb300_model(1000, 1000, 8192, 0, 3, sel.Config(128, 128, 64, 4, split_k=2), dev)
-    assert b["wave_eff"] > a["wave_eff"] and b["compute_us"] < a["compute_us"]
-    # the decode shape is memory-bound
-    d = sel.gb300_model(16, 28672, 8192, 0, 0, sel.Config(128, 16, 64, 8, split_k=8, swap_ab=1), dev)
-    assert d["memory_us"] > d["compute_us"]
+    assert b["wave_eff"] > a["wave_eff"] and b["mma_us"] < a["mma_us"] and b["splitk_us"] > 0
+    # the decode shape is bound by HBM, and its bytes are at least the compulsory ones
+    d = sel.gb300_model(16, 28672, 8192, 0, 0, sel.Config(256, 16, 128, 3, split_k=1, swap_ab=1), dev)
+    assert d["hbm_us"] > d["mma_us"]
     assert d["hbm_bytes"] >= (16 * 8192 + 8192 * 28672 + 16 * 28672) * 2
+    # a multi-wave split-K pays the last arriver's reads of every slice
+    e = sel.gb300_model(1000, 1000, 8192, 0, 3, sel.Config(128, 256, 64, 4, split_k=8), dev)
+    f = sel.gb300_model(1000, 1000, 8192, 0, 3, sel.Config(128, 256, 64, 4, split_k=4), dev)
+    assert e["units"] > dev.sm_count >= f["units"] and e["splitk_us"] > 4 * f["splitk_us"]
