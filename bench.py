@@ -45,7 +45,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="seconds of CPU work for the oracle baseline (our arm)")
+    ap.add_argument("--cpu-budget", type=float, default=120.0,
+                    help="total seconds of CPU work for the reference arm's steps")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-fixed", action="store_true")
@@ -196,7 +199,7 @@ def reference_arm(args, w):
     t0 = time.perf_counter()
     og.gemm(A[:cal], B, bias, epi, threads=threads)
     per_row = max((time.perf_counter() - t0) / cal, 1e-7)
-    budget = 120.0 / max(1, args.steps + args.warmup)       # seconds of CPU work per step
+    budget = args.cpu_budget / max(1, args.steps + args.warmup)   # seconds of CPU work per step
     rows = int(min(w.M, max(1, budget / per_row)))
     for _ in range(args.warmup):
         og.gemm(A[:rows], B, bias, epi, threads=threads)
@@ -270,6 +273,21 @@ def time_plan(plan, sets, steps, warmup, eager=False):
     return run, mode, stream
 
 
+def combine_ranks(elapsed: float, pg=None) -> float:
+    """Max of the ranks' timed regions (the slowest replica bounds the job)."""
+    if pg is None:
+        return elapsed
+    import torch
+    t = torch.tensor([elapsed], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(flops_per_gemm: float, gemms_per_step: int, steps: int, world: int, elapsed: float) -> float:
+    """Whole-job TFLOP/s: the work of every replica over the max rank time."""
+    return flops_per_gemm * gemms_per_step * steps * world / elapsed / 1e12
+
+
 def main():
     args = parse_args()
     from autotuning_tcgen05_tmem_gb300 import inputs
@@ -329,14 +347,10 @@ def main():
         pg.barrier()
     clocks.stop()
     assert plan.status() == 0, g.last_error()
-    elapsed = e0.elapsed_time(e1) / 1e3
-    if pg:
-        t = torch.tensor([elapsed], dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = combine_ranks(e0.elapsed_time(e1) / 1e3, pg)
     sec_per_step = elapsed / args.steps
     gemm_s = sec_per_step / nsets
-    value = flops * nsets * args.steps * world / elapsed / 1e12
+    value = job_value(flops, nsets, args.steps, world, elapsed)
 
     # --- roofline of the GEMM kernel -----------------------------------------
     sustained = elapsed > 1.0
