@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-fixed", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch from Python instead of a CUDA graph")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every workload (the four headline shapes and the 30-shape sweep): one "
+                         "JSON line per shape with tuned and fixed-tile throughput and roofline share")
     ap.add_argument("--config", default=None,
                     help="explicit tile config bm,bn,bk,stages,raster,group,split_k,cta_group,swap_ab "
                          "(skips tuning; used to profile one configuration)")
@@ -288,12 +291,73 @@ def job_value(flops_per_gemm: float, gemms_per_step: int, steps: int, world: int
     return flops_per_gemm * gemms_per_step * steps * world / elapsed / 1e12
 
 
+def time_gemm(plan, sets, steps, warmup):
+    """Seconds per GEMM of `plan` over rotating sets (graph replay, CUDA events)."""
+    import torch
+    run, mode, stream = time_plan(plan, sets, steps, warmup)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / steps / len(sets)
+
+
+def sweep(args):
+    """One JSON line per workload: tuned vs fixed throughput and roofline share."""
+    import torch
+    import autotuning_tcgen05_tmem_gb300 as g
+    from autotuning_tcgen05_tmem_gb300 import _build, inputs
+    _build.build()
+    peaks, peak_src = load_peaks()
+    os.environ.setdefault("GEMM_PEAK_BF16_TFLOPS", str(peaks.get("bf16_tflops", 1900.0)))
+    os.environ.setdefault("GEMM_HBM_GBS", str(peaks.get("hbm_gbs", 6800.0)))
+    devp = g.device_params_query()
+    names = ["fp32_relu_256", "bf16_gelu_1000x1000x8192", "bf16_relu_8192", "bf16_decode_16x8192x28672"] + \
+        [w.name for w in inputs.SWEEP]
+    for name in names:
+        w = inputs.WORKLOADS[name]
+        flops, cbytes, elt = work_of(w)
+        set_bytes = (w.M * w.K + w.K * w.N + w.N + w.M * w.N) * elt
+        nsets = int(min(8, max(1, math.ceil(2 * devp.l2_bytes / set_bytes))))
+        sets = make_sets(w, nsets, torch.device("cuda", 0))
+        t0 = time.perf_counter()
+        plan = g.plan(w.M, w.N, w.K, w.dtype, w.epi)
+        tune_s = time.perf_counter() - t0
+        steps = max(3, int(0.3 / max(1e-6, 1e-6 * 20 * nsets)))  # about 0.3 s at 20 us per GEMM
+        steps = min(steps, 2000)
+        t_tuned = time_gemm(plan, sets, steps, 5)
+        with g.plan_with_config(w.M, w.N, w.K, w.dtype, w.epi, g.fixed_config(w.dtype, devp)) as fp:
+            t_fixed = time_gemm(fp, sets, steps, 5)
+        tpeak = peaks.get("bf16_tflops", 1900.0) / (1 if w.dtype == "bf16" else 2)
+        bw = peaks.get("hbm_gbs", 6800.0)
+        roof_t = max(flops / (tpeak * 1e12), cbytes / (bw * 1e9))
+        line = {"workload": name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype, "epilogue": w.epi,
+                "tuned_config": list(plan.config.astuple()), "tuned_us": t_tuned * 1e6,
+                "tflops": flops / t_tuned / 1e12, "gbs": cbytes / t_tuned / 1e9,
+                "bound": "tensor" if flops / (tpeak * 1e12) >= cbytes / (bw * 1e9) else "hbm",
+                "roofline_frac": roof_t / t_tuned, "fixed_us": t_fixed * 1e6,
+                "tuned_vs_fixed": t_fixed / t_tuned, "plan_seconds": tune_s,
+                "peaks": f"{peak_src} bf16 burst {peaks.get('bf16_tflops')} TFLOP/s, HBM {bw} GB/s"}
+        print(json.dumps(line), flush=True)
+        plan.close()
+        del sets
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     args = parse_args()
     from autotuning_tcgen05_tmem_gb300 import inputs
     w = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         return reference_arm(args, w)
+    if args.sweep:
+        return sweep(args)
 
     import torch
     import autotuning_tcgen05_tmem_gb300 as g
