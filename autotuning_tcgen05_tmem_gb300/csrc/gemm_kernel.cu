@@ -589,6 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(gbase + (tmem_slot - base));
+    // Programmatic dependent launch: the set-up above may overlap the previous
+    // kernel on the stream; global memory is touched only once that kernel has
+    // finished and its writes are visible.  The next kernel may then begin its
+    // own set-up as soon as SMs free up.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 
@@ -1042,20 +1048,23 @@ cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, cons
     if (!f) return cudaErrorInvalidValue;
     void *args[] = {const_cast<CUtensorMap *>(&a), const_cast<CUtensorMap *>(&b), const_cast<CUtensorMap *>(&c),
                     const_cast<KernelParams *>(&p)};
-    if (!p.coop_fixup) return cudaLaunchKernel(f, dim3(grid), dim3(kThreads), args, (size_t)smem_bytes, stream);
-    // CTAs of a cooperative fix-up wait on each other: launch them cooperatively
-    // so that all are resident at once.
+    // Every launch allows programmatic overlap with the previous kernel on the
+    // stream (the kernel waits on griddepcontrol before touching memory); CTAs
+    // of a cooperative fix-up wait on each other, so those launches are also
+    // cooperative, which keeps all CTAs resident at once.
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = (size_t)smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.coop_fixup ? 2 : 1;
     return cudaLaunchKernelExC(&cfg, f, args);
 }
 
