@@ -40,7 +40,8 @@ EXPORTS = ["gemm_version", "gemm_last_error", "gemm_device_params_default",
            "gemm_schedule_unit", "gemm_device_params_query", "gemm_plan",
            "gemm_plan_with_config", "gemm_plan_config", "gemm_run", "gemm_run_host",
            "gemm_plan_status", "gemm_plan_destroy", "gemm_tune", "gemm_cache_stats",
-           "gemm_cache_clear", "gemm_debug_set", "gemm_run_noalloc"]
+           "gemm_cache_clear", "gemm_debug_set", "gemm_run_noalloc", "gemm_tune_search",
+           "gemm_cache_save", "gemm_cache_load"]
 
 
 class GemmError(RuntimeError):
@@ -147,6 +148,10 @@ def _load_library(path: str):
         "gemm_tune": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, i32, P(TuneRow), i32,
                                      P(i32), P(RankStats)]),
         "gemm_cache_stats": (ctypes.c_int, [P(i64), P(i64), P(i64)]),
+    "gemm_tune_search": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32,
+                                        ctypes.c_uint64, P(TuneRow), i32, P(i32), P(RankStats)]),
+    "gemm_cache_save": (ctypes.c_int, [ctypes.c_char_p, P(i64)]),
+    "gemm_cache_load": (ctypes.c_int, [ctypes.c_char_p, P(i64)]),
         "gemm_cache_clear": (None, []),
         "gemm_debug_set": (ctypes.c_int, [i32, i64]),
         "gemm_run_noalloc": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, P(Config), vp, vp, vp, vp, vp]),
@@ -353,6 +358,31 @@ def tune(M, N, K, dtype="bf16", epi="none", topk=0, cap=4096) -> TuneResult:
     s = RankStats()
     _check(lib().gemm_tune(M, N, K, _dt(dtype), _ep(epi), topk, rows, cap, ctypes.byref(n), ctypes.byref(s)))
     return TuneResult([rows[i] for i in range(n.value)], s)
+
+
+SEARCH_EXHAUSTIVE, SEARCH_MODEL_TOPK, SEARCH_RANDOM_K = 0, 1, 2
+
+
+def tune_search(M, N, K, dtype="bf16", epi="none", mode=SEARCH_MODEL_TOPK, k=24, seed=0, cap=4096) -> TuneResult:
+    """Time candidates chosen by `mode` (exhaustive, model top-k, random-k)."""
+    rows = (TuneRow * cap)()
+    n = ctypes.c_int32(0)
+    s = RankStats()
+    _check(lib().gemm_tune_search(M, N, K, _dt(dtype), _ep(epi), mode, k, seed, rows, cap, ctypes.byref(n),
+                                  ctypes.byref(s)))
+    return TuneResult([rows[i] for i in range(n.value)], s)
+
+
+def cache_save(path: str) -> int:
+    n = ctypes.c_int64(0)
+    _check(lib().gemm_cache_save(os.fsencode(path), ctypes.byref(n)))
+    return n.value
+
+
+def cache_load(path: str) -> int:
+    n = ctypes.c_int64(0)
+    _check(lib().gemm_cache_load(os.fsencode(path), ctypes.byref(n)))
+    return n.value
 
 
 def cache_stats():

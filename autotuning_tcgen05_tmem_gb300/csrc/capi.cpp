@@ -41,10 +41,12 @@ int run_host(gemm_plan_t p, const void *A, const void *B, const void *bias, void
 int plan_status(gemm_plan_t p);
 int plan_config(gemm_plan_t p, gemm_config *out);
 void destroy_plan(gemm_plan_t p);
-int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int topk, std::vector<gemm_tune_row> &rows,
-         gemm_rank_stats &stats, gemm_config *winner);
+int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, uint64_t seed,
+         std::vector<gemm_tune_row> &rows, gemm_rank_stats &stats, gemm_config *winner);
 void cache_stats(int64_t *tunes, int64_t *hits, int64_t *entries);
 void cache_clear();
+int cache_save(const char *path, int64_t *n);
+int cache_load(const char *path, int64_t *n);
 
 }  // namespace gemmgb
 
@@ -184,20 +186,49 @@ int gemm_plan_status(gemm_plan_t plan)
 
 void gemm_plan_destroy(gemm_plan_t plan) { destroy_plan(plan); }
 
+static int tune_into(int64_t M, int64_t N, int64_t K, int dtype, int epi, int mode, int32_t k, uint64_t seed,
+                     gemm_tune_row *rows, int32_t cap, int32_t *n_rows, gemm_rank_stats *stats)
+{
+    if (!n_rows || cap < 0 || (cap > 0 && !rows)) return set_error(GEMM_ERR_INVALID_ARG, "gemm_tune: bad argument");
+    std::vector<gemm_tune_row> v;
+    gemm_rank_stats s;
+    const int rc = tune(M, N, K, dtype, epi, mode, k, seed, v, s, nullptr);
+    if (rc) return rc;
+    int32_t i = 0;
+    for (; i < cap && i < (int32_t)v.size(); ++i) rows[i] = v[i];
+    *n_rows = i;
+    if (stats) *stats = s;
+    return GEMM_OK;
+}
+
 int gemm_tune(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, int32_t topk, gemm_tune_row *rows,
               int32_t cap, int32_t *n_rows, gemm_rank_stats *stats)
 {
     clear_error();
-    if (!n_rows || cap < 0 || (cap > 0 && !rows)) return set_error(GEMM_ERR_INVALID_ARG, "gemm_tune: bad argument");
-    std::vector<gemm_tune_row> v;
-    gemm_rank_stats s;
-    const int rc = tune(M, N, K, dtype, epi, topk, v, s, nullptr);
-    if (rc) return rc;
-    int32_t k = 0;
-    for (; k < cap && k < (int32_t)v.size(); ++k) rows[k] = v[k];
-    *n_rows = k;
-    if (stats) *stats = s;
-    return GEMM_OK;
+    return tune_into(M, N, K, dtype, epi, topk > 0 ? GEMM_SEARCH_MODEL_TOPK : GEMM_SEARCH_EXHAUSTIVE, topk, 0, rows,
+                     cap, n_rows, stats);
+}
+
+int gemm_tune_search(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, gemm_search mode,
+                     int32_t k, uint64_t seed, gemm_tune_row *rows, int32_t cap, int32_t *n_rows,
+                     gemm_rank_stats *stats)
+{
+    clear_error();
+    if (mode < GEMM_SEARCH_EXHAUSTIVE || mode > GEMM_SEARCH_RANDOM_K || (mode != GEMM_SEARCH_EXHAUSTIVE && k < 1))
+        return set_error(GEMM_ERR_INVALID_ARG, "gemm_tune_search: bad mode or budget");
+    return tune_into(M, N, K, dtype, epi, mode, k, seed, rows, cap, n_rows, stats);
+}
+
+int gemm_cache_save(const char *path, int64_t *n_written)
+{
+    clear_error();
+    return cache_save(path, n_written);
+}
+
+int gemm_cache_load(const char *path, int64_t *n_loaded)
+{
+    clear_error();
+    return cache_load(path, n_loaded);
 }
 
 int gemm_cache_stats(int64_t *tunes, int64_t *hits, int64_t *entries)

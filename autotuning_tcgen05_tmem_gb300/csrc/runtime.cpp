@@ -505,8 +505,8 @@ static int env_int(const char *name, int dflt)
     return atoi(v);
 }
 
-int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int topk, std::vector<gemm_tune_row> &rows,
-         gemm_rank_stats &stats, gemm_config *winner)
+int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, uint64_t seed,
+         std::vector<gemm_tune_row> &rows, gemm_rank_stats &stats, gemm_config *winner)
 {
     const auto t_start = std::chrono::steady_clock::now();
     memset(&stats, 0, sizeof(stats));
@@ -547,10 +547,26 @@ int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int topk, std::vector
     for (int i = 0; i < n; ++i)
         if (same(cands[i], fixed)) fixed_idx = i;
 
-    // Which candidates to time: all, or the model's top-k plus the fixed tile.
+    // Which candidates to time ("Autotuning & cost models" §6): every one
+    // (exhaustive), the model's top-k plus the fixed tile (model-guided), or k
+    // drawn uniformly at random with a seeded splitmix64 stream (random-k).
     std::vector<int> meas;
-    if (topk <= 0 || topk >= n) {
+    if (mode == GEMM_SEARCH_EXHAUSTIVE || topk <= 0 || topk >= n) {
         meas = by_model;
+    } else if (mode == GEMM_SEARCH_RANDOM_K) {
+        std::vector<int> pool(n);
+        std::iota(pool.begin(), pool.end(), 0);
+        uint64_t x = seed;
+        for (int i = 0; i < topk; ++i) {   // partial Fisher-Yates shuffle
+            x += 0x9E3779B97F4A7C15ull;
+            uint64_t z = x;
+            z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+            z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+            z ^= z >> 31;
+            const int j = i + (int)(z % (uint64_t)(n - i));
+            std::swap(pool[i], pool[j]);
+        }
+        meas.assign(pool.begin(), pool.begin() + topk);
     } else {
         meas.assign(by_model.begin(), by_model.begin() + topk);
         if (fixed_idx >= 0 && std::find(meas.begin(), meas.end(), fixed_idx) == meas.end()) meas.push_back(fixed_idx);
@@ -713,6 +729,84 @@ static std::mutex g_cache_mu;
 static std::map<std::string, gemm_config> g_cache;
 static int64_t g_tunes = 0, g_hits = 0;
 
+// Tuning database file ("Tile Selection": tuned results are "shipped with the
+// artifact or stored in a tuning database that persists across deployments";
+// "Autotuning & cost models" §5: AOT tuning log).  One text line per entry:
+//   <key> TAB bm bn bk stages raster group split_k cta_group swap_ab
+// with <key> = M|N|K|dtype|epilogue|device name|SM count|library version, so an
+// entry only ever serves the device and library version that produced it.
+static bool parse_db_line(const std::string &line, std::string &key, gemm_config &c)
+{
+    const size_t tab = line.find('\t');
+    if (tab == std::string::npos || tab == 0) return false;
+    key = line.substr(0, tab);
+    int v[9];
+    if (sscanf(line.c_str() + tab + 1, "%d %d %d %d %d %d %d %d %d", &v[0], &v[1], &v[2], &v[3], &v[4], &v[5], &v[6],
+               &v[7], &v[8]) != 9)
+        return false;
+    c = gemm_config{v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], v[8]};
+    return true;
+}
+
+static std::string db_line(const std::string &key, const gemm_config &c)
+{
+    char buf[128];
+    snprintf(buf, sizeof(buf), "\t%d %d %d %d %d %d %d %d %d\n", c.bm, c.bn, c.bk, c.stages, c.raster, c.group,
+             c.split_k, c.cta_group, c.swap_ab);
+    return key + buf;
+}
+
+// Requires g_cache_mu held.
+static int load_db_locked(const char *path, int64_t *n)
+{
+    FILE *f = fopen(path, "r");
+    if (!f) return set_error(GEMM_ERR_INVALID_ARG, "cannot open tuning database '%s'", path);
+    int64_t count = 0;
+    char buf[1024];
+    while (fgets(buf, sizeof(buf), f)) {
+        std::string line(buf), key;
+        while (!line.empty() && (line.back() == '\n' || line.back() == '\r')) line.pop_back();
+        gemm_config c;
+        if (line.empty() || line[0] == '#' || !parse_db_line(line, key, c)) continue;
+        g_cache[key] = c;
+        ++count;
+    }
+    fclose(f);
+    if (n) *n = count;
+    return GEMM_OK;
+}
+
+int cache_save(const char *path, int64_t *n)
+{
+    if (!path) return set_error(GEMM_ERR_INVALID_ARG, "null path");
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    const std::string tmp = std::string(path) + ".tmp";
+    FILE *f = fopen(tmp.c_str(), "w");
+    if (!f) return set_error(GEMM_ERR_INVALID_ARG, "cannot write tuning database '%s'", path);
+    fprintf(f, "# tuning database of %s: key TAB bm bn bk stages raster group split_k cta_group swap_ab\n",
+            GEMM_LIB_VERSION);
+    for (const auto &kv : g_cache) fputs(db_line(kv.first, kv.second).c_str(), f);
+    const bool ok = fclose(f) == 0 && rename(tmp.c_str(), path) == 0;
+    if (!ok) return set_error(GEMM_ERR_INVALID_ARG, "cannot replace tuning database '%s'", path);
+    if (n) *n = (int64_t)g_cache.size();
+    return GEMM_OK;
+}
+
+int cache_load(const char *path, int64_t *n)
+{
+    if (!path) return set_error(GEMM_ERR_INVALID_ARG, "null path");
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    return load_db_locked(path, n);
+}
+
+// GEMM_TUNING_DB=<path>: loaded on the first tuned plan, appended to on every
+// new winner (just-in-time tuning that persists).
+static const char *db_path()
+{
+    const char *p = getenv("GEMM_TUNING_DB");
+    return (p && *p) ? p : nullptr;
+}
+
 static std::string cache_key(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_device_params &dev)
 {
     int d = 0;
@@ -742,11 +836,23 @@ int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *ou
     gemm_config cfg;
     {
         std::lock_guard<std::mutex> lk(g_cache_mu);
+        static std::string loaded_db;
+        const char *dbp = db_path();
+        if (dbp && loaded_db != dbp) {
+            int64_t nl = 0;
+            load_db_locked(dbp, &nl);   // a missing file is an empty database
+            clear_error();
+            loaded_db = dbp;
+        }
         auto it = g_cache.find(key);
         if (it != g_cache.end()) {
-            ++g_hits;
             cfg = it->second;
-            return make_plan(M, N, K, dt, epi, cfg, dev, nullptr, out);
+            if (make_plan(M, N, K, dt, epi, cfg, dev, nullptr, out) == GEMM_OK) {
+                ++g_hits;
+                return GEMM_OK;
+            }
+            g_cache.erase(it);          // an entry the current limits reject is re-tuned
+            clear_error();
         }
     }
     const char *mode = getenv("GEMM_TUNE_MODE");
@@ -754,12 +860,19 @@ int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *ou
     const int topk = exhaustive ? 0 : std::max(1, env_int("GEMM_TUNE_TOPK", 24));
     std::vector<gemm_tune_row> rows;
     gemm_rank_stats stats;
-    rc = tune(M, N, K, dt, epi, topk, rows, stats, &cfg);
+    rc = tune(M, N, K, dt, epi, exhaustive ? GEMM_SEARCH_EXHAUSTIVE : GEMM_SEARCH_MODEL_TOPK, topk, 0, rows, stats,
+              &cfg);
     if (rc) return rc;
     {
         std::lock_guard<std::mutex> lk(g_cache_mu);
         ++g_tunes;
         g_cache[key] = cfg;
+        if (const char *dbp = db_path()) {
+            if (FILE *f = fopen(dbp, "a")) {
+                fputs(db_line(key, cfg).c_str(), f);
+                fclose(f);
+            }
+        }
     }
     return make_plan(M, N, K, dt, epi, cfg, dev, nullptr, out);
 }

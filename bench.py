@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload (the four headline shapes and the 30-shape sweep): one "
                          "JSON line per shape with tuned and fixed-tile throughput and roofline share")
+    ap.add_argument("--search-quality", action="store_true",
+                    help="model-guided top-k vs random-k at equal measurement budgets, from one "
+                         "exhaustive tuning table per workload (one JSON line per workload)")
     ap.add_argument("--config", default=None,
                     help="explicit tile config bm,bn,bk,stages,raster,group,split_k,cta_group,swap_ab "
                          "(skips tuning; used to profile one configuration)")
@@ -350,6 +353,43 @@ def sweep(args):
     return 0
 
 
+def expected_random_best(measured, k):
+    """E[best of k distinct uniform draws] as a fraction of the true best:
+    with values sorted ascending, P(min = v_i) = C(n-i, k-1) / C(n, k)."""
+    v = sorted(measured)
+    n = len(v)
+    if k >= n:
+        return 1.0
+    total = math.comb(n, k)
+    return sum(math.comb(n - i, k - 1) / total * v[0] / v[i - 1] for i in range(1, n - k + 2))
+
+
+def search_quality(args):
+    import autotuning_tcgen05_tmem_gb300 as g
+    from autotuning_tcgen05_tmem_gb300 import _build, inputs
+    _build.build()
+    peaks, _ = load_peaks()
+    os.environ.setdefault("GEMM_PEAK_BF16_TFLOPS", str(peaks.get("bf16_tflops", 1900.0)))
+    os.environ.setdefault("GEMM_HBM_GBS", str(peaks.get("hbm_gbs", 6800.0)))
+    budgets = [1, 2, 4, 8, 16, 24, 32]
+    names = ["bf16_gelu_1000x1000x8192", "bf16_relu_8192", "bf16_decode_16x8192x28672", "fp32_relu_256"] + \
+        [w.name for w in inputs.SWEEP]
+    for name in names:
+        w = inputs.WORKLOADS[name]
+        r = g.tune_search(w.M, w.N, w.K, w.dtype, w.epi, g.SEARCH_EXHAUSTIVE, 0)
+        rows = [row for row in r.rows if row.measured_us > 0]
+        meas = [row.measured_us for row in rows]
+        best = min(meas)
+        by_model = sorted(rows, key=lambda row: row.model_rank)
+        model_q = {k: best / min(row.measured_us for row in by_model[:k]) for k in budgets}
+        random_q = {k: expected_random_best(meas, k) for k in budgets}
+        print(json.dumps({"workload": name, "candidates": len(rows), "best_us": best,
+                          "kendall_tau": r.stats.kendall_tau, "model_quality": model_q,
+                          "random_quality_expected": random_q, "search_seconds": r.stats.tune_seconds}),
+              flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     from autotuning_tcgen05_tmem_gb300 import inputs
@@ -358,6 +398,8 @@ def main():
         return reference_arm(args, w)
     if args.sweep:
         return sweep(args)
+    if args.search_quality:
+        return search_quality(args)
 
     import torch
     import autotuning_tcgen05_tmem_gb300 as g

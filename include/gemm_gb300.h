@@ -294,9 +294,32 @@ int gemm_tune(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue e
               int32_t topk, gemm_tune_row *rows, int32_t cap, int32_t *n_rows,
               gemm_rank_stats *stats);
 
+/* Search strategies at a given measurement budget ("Autotuning & cost models"
+ * §6): time every candidate; the cost model's top k (plus the fixed tile, so
+ * tuning never loses to it — "CuTile Autotuning"); or k candidates drawn
+ * uniformly at random from the seeded splitmix64 stream `seed`. */
+typedef enum { GEMM_SEARCH_EXHAUSTIVE = 0, GEMM_SEARCH_MODEL_TOPK = 1, GEMM_SEARCH_RANDOM_K = 2 } gemm_search;
+
+/* gemm_tune with an explicit strategy and budget k (ignored for exhaustive). */
+int gemm_tune_search(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, gemm_search mode,
+                     int32_t k, uint64_t seed, gemm_tune_row *rows, int32_t cap, int32_t *n_rows,
+                     gemm_rank_stats *stats);
+
 /* Tune-once cache: number of searches run, lookups served, entries held. */
 int gemm_cache_stats(int64_t *tunes, int64_t *hits, int64_t *entries);
 void gemm_cache_clear(void);
+
+/* Tuning database ("Tile Selection", "Measurement, and what it must control":
+ * results shipped with the artifact or kept in a database that persists across
+ * deployments; "Autotuning & cost models" §5: ahead-of-time tuning log).  A text
+ * file, one entry per line: the cache key (M|N|K|dtype|epilogue|device name|SM
+ * count|library version), a tab, and the nine config fields.  Save writes the
+ * whole cache atomically (temporary file + rename); load merges entries into
+ * the cache (an entry serves only its own device and library version; one that
+ * the current limits reject is re-tuned).  With GEMM_TUNING_DB=<path>, gemm_plan
+ * loads that file on first use and appends every new winner to it. */
+int gemm_cache_save(const char *path, int64_t *n_written);
+int gemm_cache_load(const char *path, int64_t *n_loaded);
 
 /* Debug controls.  what = 0: wait limit in nanoseconds (default 2e9; every
  * mbarrier wait in the kernel gives up after it, sets the status word and

@@ -52,3 +52,14 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["steps"] == 2
+
+
+def test_expected_random_best_closed_form_against_enumeration():
+    import itertools
+    sys.path.insert(0, ROOT)
+    import bench
+    vals = [5.0, 3.0, 9.0, 4.0, 7.0, 3.5]
+    for k in range(1, 7):
+        subsets = list(itertools.combinations(vals, k))
+        brute = sum(min(vals) / min(s) for s in subsets) / len(subsets)
+        assert bench.expected_random_best(vals, k) == pytest.approx(brute, rel=1e-12)

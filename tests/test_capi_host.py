@@ -193,3 +193,24 @@ def test_device_calls_without_a_gpu_fail_loudly():
     assert e.value.code in (g.ERR_NO_DEVICE, g.ERR_UNSUPPORTED)
     with pytest.raises(g.GemmError):
         g.device_params_query()
+
+
+def test_tuning_database_round_trip(tmp_path):
+    """The database file is parsed and rewritten without a GPU: comments and
+    malformed lines are skipped, entries keep their key and nine fields."""
+    g.cache_clear()
+    src = tmp_path / "db.txt"
+    src.write_text("# comment\n"
+                   "1000|1000|8192|0|3|NVIDIA GB300|152|v\t256 128 64 4 0 1 4 1 0\n"
+                   "16|28672|8192|0|0|NVIDIA GB300|152|v\t128 16 128 5 0 8 1 1 1\n"
+                   "broken line without a tab\n")
+    assert g.cache_load(str(src)) == 2
+    assert g.cache_stats()["entries"] == 2
+    out = tmp_path / "out.txt"
+    assert g.cache_save(str(out)) == 2
+    body = [l for l in out.read_text().splitlines() if not l.startswith("#")]
+    assert sorted(body) == sorted(l for l in src.read_text().splitlines() if "\t" in l)
+    g.cache_clear()
+    assert g.cache_stats()["entries"] == 0
+    with pytest.raises(g.GemmError):
+        g.cache_load(str(tmp_path / "missing.txt"))

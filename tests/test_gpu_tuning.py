@@ -139,3 +139,41 @@ def test_zero_extents_through_the_tuned_path():
         p.run(None, None, bias, C)
         assert p.status() == 0
     assert torch.equal(C.cpu(), torch.relu(bias.float()).to(torch.bfloat16).cpu().expand(40, 64))
+
+
+def test_tuning_database_serves_a_later_process_and_persists_new_winners(tmp_path):
+    g.cache_clear()
+    w = inputs.WORKLOADS["bf16_gelu_kv_t512"]
+    with g.plan(w.M, w.N, w.K, w.dtype, w.epi) as p:
+        chosen = p.config.astuple()
+    db = tmp_path / "tuning.db"
+    assert g.cache_save(str(db)) == 1
+    g.cache_clear()
+    assert g.cache_load(str(db)) == 1
+    with g.plan(w.M, w.N, w.K, w.dtype, w.epi) as p:     # served from the loaded entry
+        assert p.config.astuple() == chosen
+    st = g.cache_stats()
+    assert st["tunes"] == 0 and st["hits"] == 1
+    # just-in-time persistence: a new winner is appended to GEMM_TUNING_DB
+    g.cache_clear()
+    jit = tmp_path / "jit.db"
+    os.environ["GEMM_TUNING_DB"] = str(jit)
+    try:
+        g.plan(384, 512, 1024, "bf16", "relu").close()
+    finally:
+        del os.environ["GEMM_TUNING_DB"]
+    lines = [l for l in jit.read_text().splitlines() if "\t" in l]
+    assert len(lines) == 1 and lines[0].startswith("384|512|1024|0|2|")
+
+
+def test_search_strategies_measure_their_budget():
+    w = inputs.WORKLOADS["bf16_gelu_out_t512"]
+    rnd = g.tune_search(w.M, w.N, w.K, w.dtype, w.epi, g.SEARCH_RANDOM_K, k=8, seed=7)
+    assert rnd.stats.n_measured == 8
+    again = g.tune_search(w.M, w.N, w.K, w.dtype, w.epi, g.SEARCH_RANDOM_K, k=8, seed=7)
+    pick = sorted(r.config.astuple() for r in rnd.rows if r.measured_us > 0)
+    assert pick == sorted(r.config.astuple() for r in again.rows if r.measured_us > 0)  # seeded
+    top = g.tune_search(w.M, w.N, w.K, w.dtype, w.epi, g.SEARCH_MODEL_TOPK, k=8)
+    assert top.stats.n_measured in (8, 9)                # + the fixed tile when it is not in the top 8
+    measured = [r for r in top.rows if r.measured_us > 0]
+    assert sorted(r.model_rank for r in measured)[:8] == list(range(8))
