@@ -41,7 +41,7 @@ EXPORTS = ["gemm_version", "gemm_last_error", "gemm_device_params_default",
            "gemm_plan_with_config", "gemm_plan_config", "gemm_run", "gemm_run_host",
            "gemm_plan_status", "gemm_plan_destroy", "gemm_tune", "gemm_cache_stats",
            "gemm_cache_clear", "gemm_debug_set", "gemm_run_noalloc", "gemm_tune_search",
-           "gemm_cache_save", "gemm_cache_load"]
+           "gemm_cache_save", "gemm_cache_load", "gemm_plan_launch_info"]
 
 
 class GemmError(RuntimeError):
@@ -97,6 +97,17 @@ class TuneRow(ctypes.Structure):
                 ("measured_rank", ctypes.c_int32), ("status", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
+class LaunchInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("grid", "block", "smem_bytes", "cluster", "splitk_route", "b_transposed", "units", "tiles")]
+
+    def asdict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+SPLITK_ROUTES = {0: "none", 1: "global_last_arriver", 2: "global_cooperative", 3: "cluster_dsmem"}
+
+
 class RankStats(ctypes.Structure):
     _fields_ = [("kendall_tau", ctypes.c_double), ("spearman_rho", ctypes.c_double),
                 ("regret", ctypes.c_double), ("tune_seconds", ctypes.c_double),
@@ -144,6 +155,7 @@ def _load_library(path: str):
         "gemm_run": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "gemm_run_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "gemm_plan_status": (ctypes.c_int, [vp]),
+        "gemm_plan_launch_info": (ctypes.c_int, [vp, P(LaunchInfo)]),
         "gemm_plan_destroy": (None, [vp]),
         "gemm_tune": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, i32, P(TuneRow), i32,
                                      P(i32), P(RankStats)]),
@@ -297,6 +309,12 @@ class Plan:
         c = Config()
         _check(lib().gemm_plan_config(self._h, ctypes.byref(c)))
         return c
+
+    @property
+    def launch_info(self) -> LaunchInfo:
+        li = LaunchInfo()
+        _check(lib().gemm_plan_launch_info(self._h, ctypes.byref(li)))
+        return li
 
     def run(self, A, B, bias, C, stream=None) -> None:
         _check(lib().gemm_run(self._h, _ptr(A), _ptr(B), _ptr(bias), _ptr(C), _stream_handle(stream)))

@@ -33,6 +33,7 @@ void clear_error() { t_last_error.clear(); }
 extern std::atomic<int64_t> g_timeout_ns;
 extern std::atomic<int32_t> g_debug_stall;
 extern std::atomic<int32_t> g_b_route;
+extern std::atomic<int32_t> g_split_route;
 int query_params(gemm_device_params *d);
 int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out);
 int plan_explicit(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &cfg, gemm_plan_t *out);
@@ -40,6 +41,7 @@ int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void
 int run_host(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream);
 int plan_status(gemm_plan_t p);
 int plan_config(gemm_plan_t p, gemm_config *out);
+int plan_launch_info(gemm_plan_t p, gemm_launch_info *out);
 void destroy_plan(gemm_plan_t p);
 int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, uint64_t seed,
          std::vector<gemm_tune_row> &rows, gemm_rank_stats &stats, gemm_config *winner);
@@ -167,6 +169,13 @@ int gemm_plan_config(gemm_plan_t plan, gemm_config *out)
     return plan_config(plan, out);
 }
 
+int gemm_plan_launch_info(gemm_plan_t plan, gemm_launch_info *out)
+{
+    clear_error();
+    if (!plan || !out) return set_error(GEMM_ERR_INVALID_ARG, "null argument");
+    return plan_launch_info(plan, out);
+}
+
 int gemm_run(gemm_plan_t plan, const void *A, const void *B, const void *bias, void *C, gemm_stream_t stream)
 {
     return run_plan(plan, A, B, bias, C, reinterpret_cast<cudaStream_t>(stream));
@@ -254,6 +263,11 @@ int gemm_debug_set(int32_t what, int64_t value)
     if (what == 2) {
         if (value < 0 || value > 2) return set_error(GEMM_ERR_INVALID_ARG, "B route must be 0, 1 or 2");
         g_b_route.store((int32_t)value);
+        return GEMM_OK;
+    }
+    if (what == 3) {
+        if (value < 0 || value > 1) return set_error(GEMM_ERR_INVALID_ARG, "split-K route must be 0 or 1");
+        g_split_route.store((int32_t)value);
         return GEMM_OK;
     }
     return set_error(GEMM_ERR_INVALID_ARG, "unknown debug control %d", what);

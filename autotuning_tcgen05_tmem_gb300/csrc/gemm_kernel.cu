@@ -22,6 +22,12 @@
 // warps 2..9 (256 threads) drain the accumulator, each reading the 32 TMEM
 // lanes of its sub-partition (warp % 4), two warps per sub-partition.
 //
+// Split-K: the K slices of a tile either exchange fp32 partial tiles through
+// global memory (a cooperative or last-arriver fix-up), or, when the slices of
+// a tile form one thread-block cluster, push them into the owning CTA's shared
+// memory with st.async (distributed shared memory) and never touch global
+// memory for the reduction.
+//
 // Every mbarrier wait is bounded: after the limit the waiting role writes a
 // code to the status word, raises a CTA-wide abort flag and returns; the other
 // roles see the flag, the CTA waits (bounded) for its own copies and MMAs in
@@ -78,6 +84,61 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
         : "r"(bar), "r"(parity)
         : "memory");
     return done != 0;
+}
+
+// The same probe with cluster-scope acquire: for barriers that CTAs of the
+// cluster arrive on remotely, or that st.async from them completes.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// 16-byte store into another CTA's shared memory; its completion is counted
+// in bytes on that CTA's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c, float d,
+                                            uint32_t cluster_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     cluster_addr),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// All threads of all CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_barrier_init()
@@ -310,6 +371,24 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
     for (int i = 0; i < 256; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return wait_slow(bar, parity, c, site, true, c.timeout_ns);
+}
+
+// Bounded wait on a barrier completed from other CTAs of the cluster.
+__device__ __noinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, const WaitCtl &c, int32_t site)
+{
+    const long long limit_cycles = (long long)((double)c.timeout_ns * 2.2);
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*c.abort) return false;
+            if (clock64() - t0 > limit_cycles) {
+                *c.abort = 1;
+                atomicCAS(c.status, 0, site);
+                return false;
+            }
+        }
+    }
 }
 
 __device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *ptr)
@@ -562,6 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t teardown_bar = tfull0 + 32u;
     const uint32_t never_bar = tfull0 + 40u;
     const uint32_t tmem_slot = tfull0 + 48u;
+    const uint32_t peer_ready_bar = tfull0 + 64u;   // cluster split-K: the other slices' rings are free
+    const uint32_t recv_bar = tfull0 + 72u;         // cluster split-K: every partial for my blocks has landed
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(gbase + (tmem_slot - base) + 4);
     volatile int32_t *last_flag = reinterpret_cast<volatile int32_t *>(gbase + (tmem_slot - base) + 8);
 
@@ -576,6 +657,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(teardown_bar, 1);
         mbar_init(never_bar, 1);
+        if (p.cluster_k > 1) {
+            mbar_init(peer_ready_bar, (uint32_t)(p.cluster_k - 1));
+            mbar_init(recv_bar, 1);
+        }
         *abort_flag = 0;
         *last_flag = 0;
         fence_barrier_init();
@@ -589,6 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(gbase + (tmem_slot - base));
+    // Peers arrive on this CTA's barriers: none may do so before every CTA of
+    // the cluster has initialised its own.
+    if (p.cluster_k > 1) cluster_sync_all();
     // Programmatic dependent launch: the set-up above may overlap the previous
     // kernel on the stream; global memory is touched only once that kernel has
     // finished and its writes are visible.  The next kernel may then begin its
@@ -736,6 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t e_bn = p.bn, e_bm = p.bm, e_epi = p.epi, e_cols = p.cols, e_rows = p.rows;
         const int32_t e_split_k = p.split_k, e_swap_ab = p.swap_ab;
         const bool e_coop = p.coop_fixup != 0;
+        const bool e_cluster = p.cluster_k > 1;
         const uint32_t e_acc_cols = p.acc_cols, e_n_acc = p.n_acc;
         const void *const e_bias = p.bias;
         float *const e_workspace = p.workspace;
@@ -778,6 +867,98 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int32_t nk = w.kb_end - w.kb_begin;
             const uint32_t tacc = tmem_base + acc * e_acc_cols + ((uint32_t)(q * 32) << 16);
+            if (e_cluster) {
+                // Split-K inside a cluster: CTA rank s of the cluster is K slice s of
+                // this tile (units are tile-major, slice fastest; one unit per CTA).
+                // The tile's 128-row x 32-column blocks are dealt out in groups of
+                // gsz: pairs (an even and an odd chunk, so that both warps of a
+                // sub-partition get work) when there are at least two per slice,
+                // else single blocks; group j belongs to slice j mod S.  Each slice pushes the
+                // blocks it does not own into their owner's pipeline ring (free once
+                // the owner's MMAs are done, which the owner announces), the owner
+                // adds the S partials in slice order and runs the epilogue.
+                const int32_t S = e_split_k, me = w.split;
+                const int32_t nblocks = halves * chunks;
+                const int32_t gsz = nblocks >= 2 * S ? 2 : 1;
+                if (ew == 0 && lane == 0) {
+                    uint32_t owned = 0;
+                    for (int32_t b = 0; b < nblocks; ++b) owned += ((b / gsz) % S == me) ? 1u : 0u;
+                    mbar_arrive_expect_tx(recv_bar, owned * (uint32_t)(S - 1) * kRedBlockBytes);
+                    for (int32_t o = 0; o < S; ++o)
+                        if (o != me) mbar_arrive_remote(mapa_u32(peer_ready_bar, (uint32_t)o));
+                }
+                bool cok = wait_bar_cluster(peer_ready_bar, 0, ctl, SITE_CLUSTER);
+                if (named_bar_any(1, kEpiThreads, !cok)) break;
+                const uint32_t row16 = (uint32_t)(q * 32 + lane) * 16u;
+                for (int32_t h = 0; h < halves; ++h) {
+#pragma unroll 1
+                    for (int ci = 0; ci < 4; ++ci) {
+                        const int32_t c = cg + 2 * ci;
+                        if (c >= chunks) break;
+                        const int32_t b = h * chunks + c, j = b / gsz, o = j % S;
+                        if (o == me) continue;
+                        const int32_t ob = (j / S) * gsz + (b - j * gsz);
+                        const uint32_t slot = (uint32_t)(ob * (S - 1) + (me < o ? me : me - 1));
+                        float v[32];
+                        tmem_load_chunk<32>(tacc + (uint32_t)(h * e_bn + c * 32), v);
+                        const uint32_t dst = mapa_u32(base + slot * kRedBlockBytes + row16, (uint32_t)o);
+                        const uint32_t rbar = mapa_u32(recv_bar, (uint32_t)o);
+#pragma unroll
+                        for (int j4 = 0; j4 < 8; ++j4)
+                            st_async_v4(dst + (uint32_t)j4 * 2048u, v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2],
+                                        v[4 * j4 + 3], rbar);
+                    }
+                }
+                cok = wait_bar_cluster(recv_bar, 0, ctl, SITE_CLUSTER);
+                if (named_bar_any(1, kEpiThreads, !cok)) break;
+                for (int32_t h = 0; h < halves; ++h) {
+#pragma unroll 1
+                    for (int ci = 0; ci < 4; ++ci) {
+                        const int32_t c = cg + 2 * ci;
+                        if (c >= chunks) break;
+                        const int32_t b = h * chunks + c, j = b / gsz;
+                        if (j % S != me) continue;
+                        const int32_t ob = (j / S) * gsz + (b - j * gsz);
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+#pragma unroll 1
+                        for (int32_t s = 0; s < S; ++s) {
+                            if (s == me) {
+                                // own partial, straight from TMEM, 16 columns at a time
+#pragma unroll
+                                for (int hh = 0; hh < 2; ++hh) {
+                                    float t[16];
+                                    tmem_load_chunk<16>(tacc + (uint32_t)(h * e_bn + c * 32 + hh * 16), t);
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) v[hh * 16 + i] += t[i];
+                                }
+                            } else {
+                                const uint32_t slot = (uint32_t)(ob * (S - 1) + (s < me ? s : s - 1));
+                                const uint32_t src = base + slot * kRedBlockBytes + row16;
+#pragma unroll
+                                for (int j4 = 0; j4 < 8; ++j4) {
+                                    const float4 t = ld_shared_v4(src + (uint32_t)j4 * 2048u);
+                                    v[4 * j4] += t.x;
+                                    v[4 * j4 + 1] += t.y;
+                                    v[4 * j4 + 2] += t.z;
+                                    v[4 * j4 + 3] += t.w;
+                                }
+                            }
+                        }
+                        bias_act_rows(v, bcol[ci], e_epi);
+                        const int32_t n = c0 + c * 32, y = r0 + h * 128 + q * 32;
+                        store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(tempty0 + 8u * acc);
+                if (++acc == e_n_acc) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+                continue;
+            }
             float *ws = nullptr;
             if (e_split_k > 1) ws = e_workspace + ((size_t)w.tile * e_split_k + w.split) * (size_t)tile_elems;
 
@@ -1061,11 +1242,42 @@ cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, cons
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeCooperative;
-    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = p.coop_fixup ? 2 : 1;
+    cfg.numAttrs = 1;
+    if (p.cluster_k > 1) {
+        // The K slices of a tile are one cluster (consecutive CTAs).
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)p.cluster_k;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    } else if (p.coop_fixup) {
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelExC(&cfg, f, args);
+}
+
+// Clusters of `cluster` CTAs of this kernel that fit on the device at once.
+cudaError_t max_active_clusters(int dt, int a_mn, int b_mn, int cluster, int smem_bytes, int *out)
+{
+    *out = 0;
+    const void *f = select_kernel(dt, a_mn, b_mn);
+    if (!f) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)cluster);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem_bytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(out, f, &cfg);
 }
 
 cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t cols, int elt, cudaStream_t stream)

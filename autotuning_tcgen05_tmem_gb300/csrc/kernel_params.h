@@ -13,7 +13,11 @@ enum WaitSite : int32_t {
     SITE_EPI_STALL = 5,
     SITE_TEARDOWN = 6,
     SITE_FIXUP = 7,
+    SITE_CLUSTER = 8,
 };
+
+// Bytes of one reduction block: 128 accumulator rows x 32 fp32 columns.
+constexpr uint32_t kRedBlockBytes = 128u * 32u * 4u;
 
 struct KernelParams {
     // Problem in MMA orientation: rows along the MMA M axis, cols along MMA N.
@@ -37,6 +41,9 @@ struct KernelParams {
     int32_t debug_stall;               // epilogue waits on a barrier nothing signals
     int32_t coop_fixup;                // split-K slices finalise shares of their tile together
                                        // (launched cooperatively: every unit has its own CTA)
+    int32_t cluster_k;                 // 0, or S: the S slices of a tile are one thread-block
+                                       // cluster and reduce through distributed shared memory
+                                       // (one unit per CTA, grid = units)
 };
 
 }  // namespace gemmgb

@@ -91,6 +91,23 @@ Layout layout_of(const gemm_config &c, int dt)
     return L;
 }
 
+// Whether split-K slices of a tile can reduce through distributed shared
+// memory: cluster of S in {2, 4, 8} CTAs, unswapped, and the partials an owner
+// receives (its blocks x (S - 1) x 16 KB) fit in its pipeline ring.  Blocks
+// (128 rows x 32 columns) are owned in groups of two when there are at least
+// 2S of them, else one by one; group j belongs to slice j mod S.
+bool cluster_reduce_fits(const gemm_config &c, int dt)
+{
+    const int S = c.split_k;
+    if (!(S == 2 || S == 4 || S == 8) || c.swap_ab) return false;
+    const int nblocks = (c.bm / 128) * (c.bn / 32);
+    const int gsz = nblocks >= 2 * S ? 2 : 1;
+    const int ngroups = (nblocks + gsz - 1) / gsz;
+    const int64_t owned = (int64_t)gsz * ((ngroups + S - 1) / S);
+    const Layout L = layout_of(c, dt);
+    return owned * (S - 1) * (int64_t)kRedBlockBytes <= (int64_t)L.off_staging;
+}
+
 int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block)
 {
     const int64_t per = (int64_t)(bm + bn) * bk * elt_bytes(dt);

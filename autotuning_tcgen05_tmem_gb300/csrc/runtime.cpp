@@ -36,6 +36,10 @@ std::atomic<int32_t> g_debug_stall{0};
 // How B reaches the tensor cores: 0 = by dtype (bf16 read MN-major in place,
 // fp32 transposed to a K-major copy), 1 = always transposed, 2 = always MN-major.
 std::atomic<int32_t> g_b_route{0};
+// How split-K slices exchange partial tiles: 0 = through distributed shared
+// memory when the slices of a tile can form a cluster, else global memory;
+// 1 = always global memory.
+std::atomic<int32_t> g_split_route{0};
 
 // ---------------------------------------------------------------------------
 // TMA descriptor encoding through the driver entry point
@@ -268,6 +272,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     p->grid = (int)std::min<int64_t>(k.num_units, dev.sm_count);
     // One wave of split-K units: the slices of a tile finalise it together.
     k.coop_fixup = (cfg.split_k > 1 && k.num_units <= dev.sm_count) ? 1 : 0;
+    // Or the slices of a tile form a cluster and reduce through distributed
+    // shared memory (decided below, once the shared-memory limit is set).  Only
+    // for one wave: past it, one CTA per unit loses the persistent schedule's
+    // overlap, which costs more than the global exchange it replaces.
+    const bool want_cluster = g_split_route.load() == 0 && k.num_units <= dev.sm_count &&
+                              cluster_reduce_fits(cfg, dt);
     // Ask for more than half of the SM's shared memory so that no two CTAs of
     // this kernel share an SM (each may hold up to 512 TMEM columns).
     const int64_t one_per_sm = dev.smem_per_block / 2 + 1024;
@@ -312,6 +322,19 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     if (rc) {
         destroy_plan(p);
         return rc;
+    }
+    if (want_cluster) {
+        int clusters = 0;
+        e = max_active_clusters(dt, k.a_mn_major, k.b_mn_major, cfg.split_k, p->smem_request, &clusters);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            clusters = 0;
+        }
+        if (clusters > 0) {
+            k.cluster_k = cfg.split_k;
+            k.coop_fixup = 0;
+            p->grid = (int)k.num_units;  // one unit per CTA
+        }
     }
     *out = p;
     return GEMM_OK;
@@ -418,6 +441,21 @@ int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void
     kp.debug_stall = g_debug_stall.load();
     cudaError_t e = launch_gemm(p->dt, d->ma, d->mb, d->mc, kp, p->grid, p->smem_request, stream);
     if (e != cudaSuccess) return cuda_err(e, "kernel launch");
+    return GEMM_OK;
+}
+
+int plan_launch_info(gemm_plan_t p, gemm_launch_info *out)
+{
+    const KernelParams &k = p->kp;
+    memset(out, 0, sizeof(*out));
+    out->grid = p->grid;
+    out->block = kThreadsPerCta;
+    out->smem_bytes = p->smem_request;
+    out->cluster = k.cluster_k > 1 ? k.cluster_k : 1;
+    out->splitk_route = p->cfg.split_k <= 1 ? 0 : k.cluster_k > 1 ? 3 : k.coop_fixup ? 2 : 1;
+    out->b_transposed = p->b_kmajor ? 1 : 0;
+    out->units = k.num_units;
+    out->tiles = (int32_t)p->tiles;
     return GEMM_OK;
 }
 

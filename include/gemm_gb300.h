@@ -267,6 +267,25 @@ int gemm_plan_with_config(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gem
 /* The configuration a plan runs. */
 int gemm_plan_config(gemm_plan_t plan, gemm_config *out);
 
+/* How a plan launches its GEMM kernel (library-specific; the pages have no
+ * counterpart).  splitk_route: 0 = no split-K; 1 = partial tiles through
+ * global memory, the last slice to arrive finalises the tile; 2 = partial
+ * tiles through global memory, all slices finalise shares of the tile together
+ * (cooperative launch, one wave); 3 = the slices of a tile form one
+ * thread-block cluster and reduce through distributed shared memory. */
+typedef struct {
+    int32_t grid;          /* CTAs launched */
+    int32_t block;         /* threads per CTA */
+    int32_t smem_bytes;    /* dynamic shared memory per CTA */
+    int32_t cluster;       /* CTAs per cluster (1 = no cluster) */
+    int32_t splitk_route;  /* see above */
+    int32_t b_transposed;  /* 1: B is first copied to a K-major layout (one extra kernel) */
+    int32_t units;         /* work units: tiles x split_k */
+    int32_t tiles;         /* output tiles */
+} gemm_launch_info;
+
+int gemm_plan_launch_info(gemm_plan_t plan, gemm_launch_info *out);
+
 /* Enqueue C = act(A·B + bias) on `stream` (asynchronous).  A, B, bias, C are
  * device pointers as described above; bias may be NULL only with
  * GEMM_EPI_NONE.  A split-K plan uses its own workspace, so one plan must not
@@ -327,8 +346,13 @@ int gemm_cache_load(const char *path, int64_t *n_loaded);
  * (1 = on, 0 = off) so that the timeout path can be tested; what = 2: how B
  * reaches the tensor cores in plans made afterwards (0 = by dtype: bf16 is read
  * MN-major in place, fp32 is first transposed into a plan-owned K-major copy;
- * 1 = always transposed; 2 = always MN-major).  Affects launches (what 0, 1) or
- * plans (what 2) made after the call, from any thread. */
+ * 1 = always transposed; 2 = always MN-major); what = 3: how split-K slices
+ * exchange partial tiles in plans made afterwards (0 = through distributed
+ * shared memory when all units fit in one wave and the slices of a tile can
+ * form a thread-block cluster, else through global memory; 1 = always through
+ * global memory).  Affects
+ * launches (what 0, 1) or plans (what 2, 3) made after the call, from any
+ * thread. */
 int gemm_debug_set(int32_t what, int64_t value);
 
 /* ---------------------------------------------------------------------------
