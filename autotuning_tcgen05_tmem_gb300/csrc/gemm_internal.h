@@ -33,7 +33,7 @@ struct Layout {
     uint32_t acc_cols, n_acc, tmem_cols;
 };
 Layout layout_of(const gemm_config &c, int dt);
-int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block);
+int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block, int cta_group);
 bool cluster_reduce_fits(const gemm_config &c, int dt);
 
 // Host logic (planner.cpp)
@@ -56,7 +56,7 @@ void clear_error();
 // Kernel launch (gemm_kernel.cu)
 cudaError_t kernel_attributes(int dt, int *num_regs, int *max_threads);
 cudaError_t set_kernel_smem_limit(int dt, int bytes);
-cudaError_t max_active_clusters(int dt, int a_mn, int b_mn, int cluster, int smem_bytes, int *out);
+cudaError_t max_active_clusters(int dt, int a_mn, int b_mn, int cg, int cluster, int smem_bytes, int *out);
 cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
                         const KernelParams &p, int grid, int smem_bytes, cudaStream_t stream);
 cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t cols, int elt, cudaStream_t stream);

@@ -86,14 +86,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
-// The same probe with cluster-scope acquire: for barriers that CTAs of the
-// cluster arrive on remotely, or that st.async from them completes.
+// Non-blocking probe with cluster-scope acquire, for barriers that CTAs of
+// the cluster arrive on remotely or that st.async from them completes (a
+// suspended try_wait is not reliably woken by those remote arrivals).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
 {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
         : "r"(bar), "r"(parity)
@@ -109,9 +110,18 @@ __device__ __forceinline__ uint32_t mapa_u32(uint32_t addr, uint32_t rank)
     return r;
 }
 
+// Arrivals on another CTA's barrier (default release.cta semantics: what they
+// order is either async-proxy traffic that completes on the barrier itself or
+// tcgen05 work fenced before the arrival).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_addr, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr), "r"(bytes)
+                 : "memory");
 }
 
 // 16-byte store into another CTA's shared memory; its completion is counted
@@ -163,6 +173,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+// Load into this CTA's shared memory, completing bytes on the barrier of the
+// pair's leader (a shared::cluster address): the second CTA of a CTA pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *m, uint32_t cluster_bar,
+                                                 int32_t x, int32_t y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(cluster_bar), "r"(x), "r"(y)
         : "memory");
 }
 
@@ -228,36 +250,88 @@ __device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool 
 
 // --- tcgen05 -----------------------------------------------------------------
 
+// TMEM management.  With a CTA pair (CG = 2) one warp of each CTA of the pair
+// executes the instruction, and the columns are allocated in both.
+template <int CG>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                 "r"(ncols)
-                 : "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                     "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                     "r"(ncols)
+                     : "memory");
 }
+template <int CG>
 __device__ __forceinline__ void tmem_relinquish()
 {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (CG == 2) asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    else asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
+template <int CG>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                     : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void umma_commit(uint32_t bar)
+__device__ __forceinline__ void umma_commit_one(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
 
+// Pair MMAs: the completion arrives on the barrier at the same offset in both
+// CTAs of the pair.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
+// Completion of this thread's prior MMAs arrives on `bar` (in both CTAs of a pair).
+template <int CG>
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    if constexpr (CG == 2) umma_commit_pair(bar);
+    else umma_commit_one(bar);
+}
+
 // D[tmem] (+)= A[smem] · B[smem]; kind::f16 reads bf16, kind::tf32 reads fp32 as tf32.
-template <int DT>
+// CG = 2: one 256-row MMA over a CTA pair, issued by the pair's leader; each CTA
+// supplies 128 rows of A and half of B's columns from its own shared memory (at
+// the descriptors' offsets) and receives its 128 rows of D in its own TMEM.
+template <int DT, int CG>
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                      uint32_t accumulate)
 {
-    if constexpr (DT == 0) {
+    if constexpr (CG == 2) {
+        if constexpr (DT == 0)
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "setp.ne.b32 p, %4, 0;\n\t"
+                "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                : "memory");
+        else
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "setp.ne.b32 p, %4, 0;\n\t"
+                "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                : "memory");
+    } else if constexpr (DT == 0) {
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
             "setp.ne.b32 p, %4, 0;\n\t"
@@ -596,7 +670,7 @@ struct MmaStage {
     bool accumulate_first;  // false on the unit's first K-block
 };
 
-template <int DT, bool A_MN, bool B_MN, int KSTEPS, int HALVES>
+template <int DT, bool A_MN, bool B_MN, int KSTEPS, int HALVES, int CG = 1>
 __device__ __forceinline__ void issue_stage(const MmaStage &st)
 {
     constexpr int ELT = Elt<DT>::BYTES;
@@ -608,8 +682,8 @@ __device__ __forceinline__ void issue_stage(const MmaStage &st)
         const uint32_t acc = (st.accumulate_first || kk != 0) ? 1u : 0u;
 #pragma unroll
         for (int h = 0; h < HALVES; ++h)
-            umma<DT>(st.d0 + (uint32_t)h * st.bn, st.adesc + a_k + (uint32_t)h * st.a_half_step, st.bdesc + b_k,
-                     st.idesc, acc);
+            umma<DT, CG>(st.d0 + (uint32_t)h * st.bn, st.adesc + a_k + (uint32_t)h * st.a_half_step,
+                         st.bdesc + b_k, st.idesc, acc);
     }
 }
 
@@ -617,7 +691,7 @@ __device__ __forceinline__ void issue_stage(const MmaStage &st)
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <int DT, bool A_MN, bool B_MN>
+template <int DT, bool A_MN, bool B_MN, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const KernelParams p)
@@ -632,6 +706,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *const gbase = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // CTA pair (cta_group::2): consecutive CTAs form a cluster of two; rank 0
+    // (the leader) issues the MMAs for both, each CTA holds 128 rows of the
+    // tile.  Both walk the same units.
+    constexpr bool pair = CG == 2;
+    const uint32_t prank = pair ? (blockIdx.x & 1u) : 0u;
+    const int64_t unit0 = pair ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
+    const int64_t unit_step = pair ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
+    const int32_t cta_rows = pair ? 128 : p.bm;        // tile rows held by this CTA
+    const int32_t cta_bcols = pair ? p.bn / 2 : p.bn;  // B columns loaded by this CTA
 
     const uint32_t bars = base + p.off_bar;
     const uint32_t full0 = bars;
@@ -648,12 +731,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
-            mbar_init(full0 + 8u * s, 1);
+            mbar_init(full0 + 8u * s, pair ? 2u : 1u);   // pair: both producers arrive on the leader's
             mbar_init(empty0 + 8u * s, 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(tfull0 + 8u * i, 1);
-            mbar_init(tempty0 + 8u * i, kEpiThreads);
+            mbar_init(tempty0 + 8u * i, pair ? 2u : (uint32_t)kEpiThreads);  // pair: one arrival per CTA
         }
         mbar_init(teardown_bar, 1);
         mbar_init(never_bar, 1);
@@ -667,8 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, p.tmem_cols);
-        tmem_relinquish();
+        tmem_alloc<CG>(tmem_slot, p.tmem_cols);
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
     __syncthreads();
@@ -676,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(gbase + (tmem_slot - base));
     // Peers arrive on this CTA's barriers: none may do so before every CTA of
     // the cluster has initialised its own.
-    if (p.cluster_k > 1) cluster_sync_all();
+    if (p.cluster_k > 1 || pair) cluster_sync_all();
     // Programmatic dependent launch: the set-up above may overlap the previous
     // kernel on the stream; global memory is touched only once that kernel has
     // finished and its writes are visible.  The next kernel may then begin its
@@ -697,18 +780,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t stages = p.stages, bm = p.bm, bn = p.bn, bk = p.bk;
         const uint32_t a_bytes = p.a_stage_bytes, b_bytes = p.b_stage_bytes, tx = p.tx_bytes;
         const uint32_t sb0 = base + p.off_b;
-        const int32_t a_loads = A_MN ? bm / SPAN : bk / SPAN;
-        const int32_t b_loads = B_MN ? bn / SPAN : bk / SPAN;
+        const int32_t a_loads = A_MN ? cta_rows / SPAN : bk / SPAN;
+        const int32_t b_loads = B_MN ? cta_bcols / SPAN : bk / SPAN;
         if (leader && p.num_kb > 0) {
             prefetch_tmap(&tmA);
             prefetch_tmap(&tmB);
         }
         uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
         bool ok = true;
-        for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        for (int64_t u = unit0; ok && u < p.num_units; u += unit_step) {
             const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
-            const int32_t ra = w.tile_m * bm;
-            const int32_t rb = w.tile_n * bn;
+            const int32_t ra = w.tile_m * bm + (int32_t)prank * 128;
+            const int32_t rb = w.tile_n * bn + (int32_t)prank * cta_bcols;
             for (int32_t kb = w.kb_begin; kb < w.kb_end; ++kb) {
                 ok = __all_sync(0xFFFFFFFFu, wait_bar(empty0 + 8u * stage, phase ^ 1u, ctl, SITE_PRODUCER_EMPTY));
                 if (!ok) break;
@@ -716,17 +799,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sa = base + stage * a_bytes;
                 const uint32_t sb = sb0 + stage * b_bytes;
                 const int32_t k0 = kb * bk;
-                if (leader) {
+                if (leader && prank == 0) {
                     mbar_arrive_expect_tx(fb, tx);
                     // K-major operand: boxes of [rows x one span of K], one per span;
                     // MN-major operand: boxes of [bk x one span of MN], one per span.
                     for (int32_t j = 0; j < a_loads; ++j) {
                         if constexpr (A_MN) tma_load_2d(sa + (uint32_t)(j * bk * 128), &tmA, fb, ra + j * SPAN, k0);
-                        else tma_load_2d(sa + (uint32_t)(j * bm * 128), &tmA, fb, k0 + j * SPAN, ra);
+                        else tma_load_2d(sa + (uint32_t)(j * cta_rows * 128), &tmA, fb, k0 + j * SPAN, ra);
                     }
                     for (int32_t j = 0; j < b_loads; ++j) {
                         if constexpr (B_MN) tma_load_2d(sb + (uint32_t)(j * bk * 128), &tmB, fb, rb + j * SPAN, k0);
-                        else tma_load_2d(sb + (uint32_t)(j * bn * 128), &tmB, fb, k0 + j * SPAN, rb);
+                        else tma_load_2d(sb + (uint32_t)(j * cta_bcols * 128), &tmB, fb, k0 + j * SPAN, rb);
+                    }
+                } else if (leader) {
+                    if constexpr (pair) {
+                        // Second CTA of a pair: its halves land in its own shared
+                        // memory and complete on the leader's barrier, where the MMAs wait.
+                        const uint32_t fbr = mapa_u32(fb, 0);
+                        mbar_arrive_expect_tx_remote(fbr, tx);
+                        for (int32_t j = 0; j < a_loads; ++j) {
+                            if constexpr (A_MN)
+                                tma_load_2d_pair(sa + (uint32_t)(j * bk * 128), &tmA, fbr, ra + j * SPAN, k0);
+                            else
+                                tma_load_2d_pair(sa + (uint32_t)(j * cta_rows * 128), &tmA, fbr, k0 + j * SPAN, ra);
+                        }
+                        for (int32_t j = 0; j < b_loads; ++j) {
+                            if constexpr (B_MN)
+                                tma_load_2d_pair(sb + (uint32_t)(j * bk * 128), &tmB, fbr, rb + j * SPAN, k0);
+                            else
+                                tma_load_2d_pair(sb + (uint32_t)(j * cta_bcols * 128), &tmB, fbr, k0 + j * SPAN,
+                                                 rb);
+                        }
                     }
                 }
                 __syncwarp();
@@ -738,31 +841,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        // Every armed stage's last copy must land before the CTA may exit.
-        for (int s = 0; s < stages; ++s)
-            if ((armed >> s) & 1u) wait_teardown(full0 + 8u * s, (armed_parity >> s) & 1u, ctl);
+        // Every armed stage's last copy must land before the CTA may exit.  The
+        // second CTA of a pair completes its copies on the leader's barriers; the
+        // leader's MMAs consume them before the pair's closing cluster barrier.
+        if (prank == 0)
+            for (int s = 0; s < stages; ++s)
+                if ((armed >> s) & 1u) wait_teardown(full0 + 8u * s, (armed_parity >> s) & 1u, ctl);
     } else if (warp == 1) {
         // ------------------------------------------------------------------
-        // MMA issuer
+        // MMA issuer (in a CTA pair, the leader's warp issues for both CTAs)
         // ------------------------------------------------------------------
+        if (prank == 0) {
         const bool leader = elect_one();
-        const int32_t stages = p.stages, bm = p.bm, bn = p.bn, bk = p.bk;
+        const int32_t stages = p.stages, bn = p.bn, bk = p.bk;
         const uint32_t a_bytes = p.a_stage_bytes, b_bytes = p.b_stage_bytes, idesc = p.idesc;
         const uint32_t sb0 = base + p.off_b, acc_cols = p.acc_cols, n_acc = p.n_acc;
         const uint32_t a_lbo = p.a_lbo, b_lbo = p.b_lbo;
         const int32_t ksteps = bk * ELT / 32;
-        const int32_t halves = bm / 128;
+        const int32_t halves = pair ? 1 : p.bm / 128;
         // Descriptor increments, in the 16-byte units of the start-address field:
         // next 128-row half of A; next 128-byte K span of a K-major operand.
         const uint32_t a_half_step = A_MN ? (uint32_t)((128 / SPAN) * bk * 128) >> 4 : (128u * 128u) >> 4;
-        const uint32_t a_span_step = (uint32_t)(bm * 128) >> 4;
-        const uint32_t b_span_step = (uint32_t)(bn * 128) >> 4;
+        const uint32_t a_span_step = (uint32_t)(cta_rows * 128) >> 4;
+        const uint32_t b_span_step = (uint32_t)(cta_bcols * 128) >> 4;
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool issued = false, ok = true;
-        for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        for (int64_t u = unit0; ok && u < p.num_units; u += unit_step) {
             const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
             const int32_t nk = w.kb_end - w.kb_begin;
-            ok = __all_sync(0xFFFFFFFFu, wait_bar(tempty0 + 8u * acc, acc_phase ^ 1u, ctl, SITE_MMA_TMEM_EMPTY));
+            // A pair's accumulator is free once both CTAs' epilogues have drained it
+            // (the second arrives remotely, hence the cluster-scope wait).
+            ok = __all_sync(0xFFFFFFFFu, pair ? wait_bar_cluster(tempty0 + 8u * acc, acc_phase ^ 1u, ctl,
+                                                                 SITE_MMA_TMEM_EMPTY)
+                                              : wait_bar(tempty0 + 8u * acc, acc_phase ^ 1u, ctl,
+                                                         SITE_MMA_TMEM_EMPTY));
             if (!ok) break;
             tc_fence_after();
             const uint32_t d0 = tmem_base + acc * acc_cols;
@@ -778,17 +890,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // more than an MMA's issue and starves the tensor pipe.
                     const MmaStage st{d0, adesc, bdesc, idesc, a_span_step, b_span_step, a_half_step,
                                       (uint32_t)bn, kb != 0};
-                    switch (ksteps * 2 + halves - 1) {
-                    case 8: issue_stage<DT, A_MN, B_MN, 4, 1>(st); break;
-                    case 9: issue_stage<DT, A_MN, B_MN, 4, 2>(st); break;
-                    case 16: issue_stage<DT, A_MN, B_MN, 8, 1>(st); break;
-                    case 17: issue_stage<DT, A_MN, B_MN, 8, 2>(st); break;
-                    case 24: issue_stage<DT, A_MN, B_MN, 12, 1>(st); break;
-                    case 25: issue_stage<DT, A_MN, B_MN, 12, 2>(st); break;
-                    case 32: issue_stage<DT, A_MN, B_MN, 16, 1>(st); break;
-                    default: issue_stage<DT, A_MN, B_MN, 16, 2>(st); break;
+                    if constexpr (pair) {
+                        switch (ksteps) {
+                        case 4: issue_stage<DT, A_MN, B_MN, 4, 1, 2>(st); break;
+                        case 8: issue_stage<DT, A_MN, B_MN, 8, 1, 2>(st); break;
+                        case 12: issue_stage<DT, A_MN, B_MN, 12, 1, 2>(st); break;
+                        default: issue_stage<DT, A_MN, B_MN, 16, 1, 2>(st); break;
+                        }
+                        umma_commit<CG>(empty0 + 8u * stage);  // both CTAs' slots are free
+                    } else {
+                        switch (ksteps * 2 + halves - 1) {
+                        case 8: issue_stage<DT, A_MN, B_MN, 4, 1>(st); break;
+                        case 9: issue_stage<DT, A_MN, B_MN, 4, 2>(st); break;
+                        case 16: issue_stage<DT, A_MN, B_MN, 8, 1>(st); break;
+                        case 17: issue_stage<DT, A_MN, B_MN, 8, 2>(st); break;
+                        case 24: issue_stage<DT, A_MN, B_MN, 12, 1>(st); break;
+                        case 25: issue_stage<DT, A_MN, B_MN, 12, 2>(st); break;
+                        case 32: issue_stage<DT, A_MN, B_MN, 16, 1>(st); break;
+                        default: issue_stage<DT, A_MN, B_MN, 16, 2>(st); break;
+                        }
+                        umma_commit<CG>(empty0 + 8u * stage);  // slot is free once these MMAs have read it
                     }
-                    umma_commit(empty0 + 8u * stage);  // slot is free once these MMAs have read it
                 }
                 __syncwarp();
                 issued = true;
@@ -799,8 +921,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             if (leader) {
-                if (nk > 0) umma_commit(tfull0 + 8u * acc);
-                else mbar_arrive(tfull0 + 8u * acc);
+                if (nk > 0) {
+                    umma_commit<CG>(tfull0 + 8u * acc);
+                } else {
+                    mbar_arrive(tfull0 + 8u * acc);
+                    if (pair) mbar_arrive_remote(mapa_u32(tfull0 + 8u * acc, 1));
+                }
             }
             __syncwarp();
             if (++acc == n_acc) {
@@ -809,9 +935,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (issued) {
-            if (leader) umma_commit(teardown_bar);
+            if (leader) umma_commit<CG>(teardown_bar);
             __syncwarp();
             wait_teardown(teardown_bar, 0, ctl);
+        }
         }
     } else {
         // ------------------------------------------------------------------
@@ -835,12 +962,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         StoreRing ring{base + p.off_staging + (uint32_t)ew * 2u * p.staging_buf_bytes, p.staging_buf_bytes, 0};
         uint32_t acc = 0, acc_phase = 0;
         bool first = true;
-        const int32_t halves = e_bm / 128;
-        const int32_t tile_elems = e_bm * e_bn;
+        // Hands the drained accumulator back to the MMA issuer: every epilogue
+        // thread arrives, or, in a CTA pair, the CTA's epilogue arrives once on
+        // the leader's barrier.
+        auto release_acc = [&](uint32_t a) {
+            tc_fence_before();
+            if (!pair) {
+                mbar_arrive(tempty0 + 8u * a);
+            } else {
+                named_bar_sync(1, kEpiThreads);
+                if (ew == 0 && lane == 0) {
+                    if (prank == 0) mbar_arrive(tempty0 + 8u * a);
+                    else mbar_arrive_remote(mapa_u32(tempty0 + 8u * a, 0));
+                }
+            }
+        };
+        const int32_t halves = pair ? 1 : e_bm / 128;
+        const int32_t tile_elems = cta_rows * e_bn;   // one CTA's share of a tile (split-K exchange)
         const int32_t chunks = e_swap_ab ? e_bn / 16 : e_bn / 32;
-        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        for (int64_t u = unit0; u < p.num_units; u += unit_step) {
             const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, e_split_k, p.raster, p.group, p.num_kb);
-            const int32_t r0 = w.tile_m * e_bm;
+            const int32_t r0 = w.tile_m * e_bm + (int32_t)prank * 128;
+            const int32_t xtile = pair ? w.tile * 2 + (int32_t)prank : w.tile;  // split-K exchange tile
             const int32_t c0 = w.tile_n * e_bn;
             // bias: unswapped, lane j holds column c0 + c*32 + j of each of this
             // warp's chunks; swapped, each lane holds its row's value per half.
@@ -951,8 +1094,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(tempty0 + 8u * acc);
+                release_acc(acc);
                 if (++acc == e_n_acc) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -960,7 +1102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             float *ws = nullptr;
-            if (e_split_k > 1) ws = e_workspace + ((size_t)w.tile * e_split_k + w.split) * (size_t)tile_elems;
+            if (e_split_k > 1) ws = e_workspace + ((size_t)xtile * e_split_k + w.split) * (size_t)tile_elems;
 
             for (int32_t h = 0; h < halves; ++h) {
                 const int32_t r = h * 128 + q * 32 + lane;
@@ -979,7 +1121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             float4 *dst = reinterpret_cast<float4 *>(ws);
 #pragma unroll
                             for (int j4 = 0; j4 < 8; ++j4)
-                                dst[(size_t)(c * 8 + j4) * e_bm + r] =
+                                dst[(size_t)(c * 8 + j4) * cta_rows + r] =
                                     make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
                         } else {
                             bias_act_rows(v, bcol[ci], e_epi);
@@ -999,7 +1141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             float4 *dst = reinterpret_cast<float4 *>(ws);
 #pragma unroll
                             for (int j4 = 0; j4 < 4; ++j4)
-                                dst[(size_t)(c * 4 + j4) * e_bm + r] =
+                                dst[(size_t)(c * 4 + j4) * cta_rows + r] =
                                     make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
                         } else {
                             bias_act_cols(v, h == 0 ? brow[0] : brow[1], e_epi);
@@ -1011,8 +1153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // The accumulator may be overwritten by the next unit's MMAs.
-            tc_fence_before();
-            mbar_arrive(tempty0 + 8u * acc);
+            release_acc(acc);
             if (++acc == e_n_acc) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -1028,13 +1169,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __threadfence();
                 named_bar_sync(1, kEpiThreads);
                 if (ew == 0 && lane == 0) {
-                    const int32_t old = atomicAdd(e_counters + w.tile, 1);
+                    const int32_t old = atomicAdd(e_counters + xtile, 1);
                     int32_t mine;
                     if (e_coop) {
-                        mine = wait_counter(e_counters + w.tile, e_split_k, ctl, SITE_FIXUP) ? 1 : 0;
+                        mine = wait_counter(e_counters + xtile, e_split_k, ctl, SITE_FIXUP) ? 1 : 0;
                     } else {
                         mine = (old == e_split_k - 1) ? 1 : 0;
-                        if (mine) atomicExch(e_counters + w.tile, 0);
+                        if (mine) atomicExch(e_counters + xtile, 0);
                     }
                     *last_flag = mine;
                 }
@@ -1044,9 +1185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (mine) {
                     __threadfence();
                     const float4 *tile_ws = reinterpret_cast<const float4 *>(
-                        e_workspace + (size_t)w.tile * e_split_k * (size_t)tile_elems);
+                        e_workspace + (size_t)xtile * e_split_k * (size_t)tile_elems);
                     const size_t slice4 = (size_t)tile_elems / 4;
-                    const int32_t rgroups = e_bm / 32;
+                    const int32_t rgroups = cta_rows / 32;
                     const int32_t nblocks = rgroups * chunks;
                     const int32_t first_b = e_coop ? w.split : 0, stride = e_coop ? e_split_k : 1;
                     for (int32_t b = first_b + stride * ew; b < nblocks; b += stride * kEpiWarps) {
@@ -1056,12 +1197,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             float v[32];
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                            const float4 *src = tile_ws + (size_t)(c * 8) * e_bm + r;
+                            const float4 *src = tile_ws + (size_t)(c * 8) * cta_rows + r;
                             const float lb = e_epi != 0 ? load_bias1<DT>(e_bias, c0 + c * 32 + lane, e_cols) : 0.0f;
                             for (int32_t s = 0; s < e_split_k; ++s) {
                                 float4 t[8];
 #pragma unroll
-                                for (int j4 = 0; j4 < 8; ++j4) t[j4] = __ldcg(src + s * slice4 + (size_t)j4 * e_bm);
+                                for (int j4 = 0; j4 < 8; ++j4) t[j4] = __ldcg(src + s * slice4 + (size_t)j4 * cta_rows);
 #pragma unroll
                                 for (int j4 = 0; j4 < 8; ++j4) {
                                     v[4 * j4] += t[j4].x;
@@ -1077,7 +1218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             float v[16];
 #pragma unroll
                             for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-                            const float4 *src = tile_ws + (size_t)(c * 4) * e_bm + r;
+                            const float4 *src = tile_ws + (size_t)(c * 4) * cta_rows + r;
                             const float rb = e_epi != 0 ? load_bias1<DT>(e_bias, r0 + r, e_rows) : 0.0f;
                             for (int32_t s = 0; s < e_split_k; s += 4) {
                                 float4 t[4][4];
@@ -1086,7 +1227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (s + i < e_split_k) {
 #pragma unroll
                                         for (int j4 = 0; j4 < 4; ++j4)
-                                            t[i][j4] = __ldcg(src + (s + i) * slice4 + (size_t)j4 * e_bm);
+                                            t[i][j4] = __ldcg(src + (s + i) * slice4 + (size_t)j4 * cta_rows);
                                     }
 #pragma unroll
                                 for (int i = 0; i < 4; ++i)
@@ -1108,8 +1249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (e_coop) {
                         named_bar_sync(1, kEpiThreads);
                         if (ew == 0 && lane == 0) {
-                            const int32_t old = atomicAdd(e_counters + w.tile, 1);
-                            if (old == 2 * e_split_k - 1) atomicExch(e_counters + w.tile, 0);
+                            const int32_t old = atomicAdd(e_counters + xtile, 1);
+                            if (old == 2 * e_split_k - 1) atomicExch(e_counters + xtile, 0);
                         }
                     }
                 }
@@ -1119,10 +1260,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     __syncthreads();
+    // A CTA pair touches each other's barriers, shared memory and TMEM until
+    // both are done: neither leaves (or frees TMEM) before the other.
+    if (pair) cluster_sync_all();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, p.tmem_cols);
+        tmem_dealloc<CG>(tmem_base, p.tmem_cols);
     }
 }
 
@@ -1171,33 +1315,42 @@ __global__ void transpose_kernel(const T *__restrict__ src, T *__restrict__ dst,
 // Host-side launch helpers
 // ---------------------------------------------------------------------------
 
-// Kernel instances: (dtype, A MN-major, B MN-major).  bf16 reads B MN-major in
-// place (unswapped: B is MMA-B; swapped: B is MMA-A); fp32 reads both operands
-// K-major from a transposed copy of B.
-template <int DT, bool AM, bool BM>
+// Kernel instances: (dtype, A MN-major, B MN-major, CTA group).  bf16 reads B
+// MN-major in place (unswapped: B is MMA-B; swapped: B is MMA-A); fp32 reads
+// both operands K-major from a transposed copy of B.  A kernel may not mix
+// single-CTA and CTA-pair tcgen05 instructions, so pairs are instances of their
+// own (unswapped only).
+template <int DT, bool AM, bool BM, int CG>
 static const void *kernel_fn()
 {
-    return reinterpret_cast<const void *>(gemm_tcgen05_kernel<DT, AM, BM>);
+    return reinterpret_cast<const void *>(gemm_tcgen05_kernel<DT, AM, BM, CG>);
 }
 
-static const void *select_kernel(int dt, int a_mn, int b_mn)
+static const void *select_kernel(int dt, int a_mn, int b_mn, int cg)
 {
+    if (cg == 2) {
+        if (a_mn) return nullptr;
+        if (dt == 0) return b_mn ? kernel_fn<0, false, true, 2>() : kernel_fn<0, false, false, 2>();
+        return b_mn ? nullptr : kernel_fn<1, false, false, 2>();
+    }
     if (dt == 0) {
-        if (!a_mn && b_mn) return kernel_fn<0, false, true>();
-        if (a_mn && !b_mn) return kernel_fn<0, true, false>();
-        if (!a_mn && !b_mn) return kernel_fn<0, false, false>();
+        if (!a_mn && b_mn) return kernel_fn<0, false, true, 1>();
+        if (a_mn && !b_mn) return kernel_fn<0, true, false, 1>();
+        if (!a_mn && !b_mn) return kernel_fn<0, false, false, 1>();
         return nullptr;
     }
-    if (!a_mn && !b_mn) return kernel_fn<1, false, false>();
+    if (!a_mn && !b_mn) return kernel_fn<1, false, false, 1>();
     return nullptr;
 }
+
+// Every instance of a dtype: (A MN-major, B MN-major, CTA group).
+static const int kInstances[5][3] = {{0, 1, 1}, {1, 0, 1}, {0, 0, 1}, {0, 1, 2}, {0, 0, 2}};
 
 cudaError_t kernel_attributes(int dt, int *num_regs, int *max_threads)
 {
     int regs = 0, thr = 1 << 30;
-    const int combos[3][2] = {{0, 1}, {1, 0}, {0, 0}};
-    for (const auto &c : combos) {
-        const void *f = select_kernel(dt, c[0], c[1]);
+    for (const auto &c : kInstances) {
+        const void *f = select_kernel(dt, c[0], c[1], c[2]);
         if (!f) continue;
         cudaFuncAttributes a;
         cudaError_t e = cudaFuncGetAttributes(&a, f);
@@ -1212,9 +1365,8 @@ cudaError_t kernel_attributes(int dt, int *num_regs, int *max_threads)
 
 cudaError_t set_kernel_smem_limit(int dt, int bytes)
 {
-    const int combos[3][2] = {{0, 1}, {1, 0}, {0, 0}};
-    for (const auto &c : combos) {
-        const void *f = select_kernel(dt, c[0], c[1]);
+    for (const auto &c : kInstances) {
+        const void *f = select_kernel(dt, c[0], c[1], c[2]);
         if (!f) continue;
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
@@ -1225,7 +1377,7 @@ cudaError_t set_kernel_smem_limit(int dt, int bytes)
 cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
                         const KernelParams &p, int grid, int smem_bytes, cudaStream_t stream)
 {
-    const void *f = select_kernel(dt, p.a_mn_major, p.b_mn_major);
+    const void *f = select_kernel(dt, p.a_mn_major, p.b_mn_major, p.pair ? 2 : 1);
     if (!f) return cudaErrorInvalidValue;
     void *args[] = {const_cast<CUtensorMap *>(&a), const_cast<CUtensorMap *>(&b), const_cast<CUtensorMap *>(&c),
                     const_cast<KernelParams *>(&p)};
@@ -1251,6 +1403,13 @@ cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, cons
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
+    } else if (p.pair) {
+        // A CTA pair is a cluster of two consecutive CTAs.
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     } else if (p.coop_fixup) {
         attr[1].id = cudaLaunchAttributeCooperative;
         attr[1].val.cooperative = 1;
@@ -1260,10 +1419,10 @@ cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, cons
 }
 
 // Clusters of `cluster` CTAs of this kernel that fit on the device at once.
-cudaError_t max_active_clusters(int dt, int a_mn, int b_mn, int cluster, int smem_bytes, int *out)
+cudaError_t max_active_clusters(int dt, int a_mn, int b_mn, int cg, int cluster, int smem_bytes, int *out)
 {
     *out = 0;
-    const void *f = select_kernel(dt, a_mn, b_mn);
+    const void *f = select_kernel(dt, a_mn, b_mn, cg);
     if (!f) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));

@@ -41,6 +41,7 @@ struct KernelParams {
     int32_t debug_stall;               // epilogue waits on a barrier nothing signals
     int32_t coop_fixup;                // split-K slices finalise shares of their tile together
                                        // (launched cooperatively: every unit has its own CTA)
+    int32_t pair;                      // 1: cta_group::2, consecutive CTAs share 256-row tiles
     int32_t cluster_k;                 // 0, or S: the S slices of a tile are one thread-block
                                        // cluster and reduce through distributed shared memory
                                        // (one unit per CTA, grid = units)

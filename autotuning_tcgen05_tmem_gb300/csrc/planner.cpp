@@ -74,8 +74,11 @@ Layout layout_of(const gemm_config &c, int dt)
 {
     Layout L;
     const int e = elt_bytes(dt);
-    L.a_stage_bytes = (uint32_t)(c.bm * c.bk * e);
-    L.b_stage_bytes = (uint32_t)(c.bn * c.bk * e);
+    // A CTA pair (cta_group 2) splits the tile: each CTA stages 128 rows of A
+    // and half of B's columns, and accumulates its 128 rows x bn.
+    const bool pair = c.cta_group == 2;
+    L.a_stage_bytes = (uint32_t)((pair ? 128 : c.bm) * c.bk * e);
+    L.b_stage_bytes = (uint32_t)((pair ? c.bn / 2 : c.bn) * c.bk * e);
     L.stage_bytes = L.a_stage_bytes + L.b_stage_bytes;
     L.staging_total = (uint32_t)staging_bytes(dt, c.swap_ab);
     L.staging_buf_bytes = L.staging_total / 16;
@@ -83,7 +86,7 @@ Layout layout_of(const gemm_config &c, int dt)
     L.off_staging = L.off_b + (uint32_t)c.stages * L.b_stage_bytes;
     L.off_bar = L.off_staging + L.staging_total;
     L.smem_total = L.off_bar + (uint32_t)kAuxSmem;
-    L.acc_cols = (uint32_t)((c.bm / 128) * c.bn);
+    L.acc_cols = (uint32_t)((pair ? 1 : c.bm / 128) * c.bn);
     L.n_acc = (2 * L.acc_cols <= (uint32_t)kTmemColumns) ? 2u : 1u;
     uint32_t need = L.acc_cols * L.n_acc, cols = 32;
     while (cols < need) cols <<= 1;
@@ -99,7 +102,7 @@ Layout layout_of(const gemm_config &c, int dt)
 bool cluster_reduce_fits(const gemm_config &c, int dt)
 {
     const int S = c.split_k;
-    if (!(S == 2 || S == 4 || S == 8) || c.swap_ab) return false;
+    if (!(S == 2 || S == 4 || S == 8) || c.swap_ab || c.cta_group != 1) return false;
     const int nblocks = (c.bm / 128) * (c.bn / 32);
     const int gsz = nblocks >= 2 * S ? 2 : 1;
     const int ngroups = (nblocks + gsz - 1) / gsz;
@@ -108,9 +111,9 @@ bool cluster_reduce_fits(const gemm_config &c, int dt)
     return owned * (S - 1) * (int64_t)kRedBlockBytes <= (int64_t)L.off_staging;
 }
 
-int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block)
+int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block, int cta_group)
 {
-    const int64_t per = (int64_t)(bm + bn) * bk * elt_bytes(dt);
+    const int64_t per = (int64_t)(cta_group == 2 ? 128 + bn / 2 : bm + bn) * bk * elt_bytes(dt);
     const int64_t room = smem_per_block - staging_bytes(dt, swap_ab) - kAuxSmem;
     int64_t s = room / per;
     if (s < 0) s = 0;
@@ -122,10 +125,12 @@ const char *reason_text(int r)
 {
     switch (r) {
     case GEMM_FEASIBLE: return "feasible";
-    case GEMM_REASON_CTA_GROUP: return "cta_group must be 1";
+    case GEMM_REASON_CTA_GROUP: return "cta_group must be 1, or 2 with bm = 256 and no swap";
     case GEMM_REASON_UMMA_M: return "bm must be 128 or 256 (tcgen05 M per CTA is 128)";
     case GEMM_REASON_UMMA_N: return "bn must be a multiple of 16 in [16, 256]";
-    case GEMM_REASON_LAYOUT: return "bn must be a multiple of 32 and of the 128-byte span when B is MN-major";
+    case GEMM_REASON_LAYOUT:
+        return "bn must be a multiple of 32 and of the 128-byte span when B is MN-major (a CTA pair: bn/2 a "
+               "multiple of the span)";
     case GEMM_REASON_BK: return "bk must be 1..4 spans of 128 bytes";
     case GEMM_REASON_STAGES: return "stages must be in 2..16";
     case GEMM_REASON_SCHEDULE: return "raster must be 0/1 and group one of 1,2,4,8,16";
@@ -145,11 +150,13 @@ int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_co
     (void)epi;
     const int e = elt_bytes(dt);
     const int span = span_elems(dt);
-    if (c.cta_group != 1) return GEMM_REASON_CTA_GROUP;
+    if (c.cta_group != 1 && c.cta_group != 2) return GEMM_REASON_CTA_GROUP;
+    if (c.cta_group == 2 && (c.bm != 256 || c.swap_ab != 0)) return GEMM_REASON_CTA_GROUP;
     if (c.bm != 128 && c.bm != 256) return GEMM_REASON_UMMA_M;
     if (c.bn % 16 != 0 || c.bn < 16 || c.bn > 256) return GEMM_REASON_UMMA_N;
     if (c.swap_ab != 0 && c.swap_ab != 1) return GEMM_REASON_LAYOUT;
     if (c.swap_ab == 0 && (c.bn % span != 0 || c.bn % 32 != 0)) return GEMM_REASON_LAYOUT;
+    if (c.cta_group == 2 && (c.bn / 2) % span != 0) return GEMM_REASON_LAYOUT;
     if (c.bk % span != 0 || c.bk / span < 1 || c.bk / span > 4) return GEMM_REASON_BK;
     if (c.stages < 2 || c.stages > kMaxStages) return GEMM_REASON_STAGES;
     if ((c.raster != 0 && c.raster != 1) ||
@@ -176,25 +183,32 @@ std::vector<gemm_config> enumerate(int64_t M, int64_t N, int64_t K, int dt, int 
     const int nswap = (M <= 256) ? 2 : 1;
     for (int swap = 0; swap < nswap; ++swap) {
         const int64_t rows = swap ? N : M, cols = swap ? M : N;
-        for (int bm : {128, 256}) {
+        // (bm, cta_group): single-CTA tiles of 128 or 256 rows, and 256-row tiles
+        // on a CTA pair (unswapped only).
+        const std::pair<int, int> shapes[] = {{128, 1}, {256, 1}, {256, 2}};
+        for (const auto &shape : shapes) {
+            const int bm = shape.first, cg = shape.second;
+            if (cg == 2 && swap) continue;
             std::vector<int> bns;
             if (swap) bns = {16, 32, 64, 128, 256};
+            else if (cg == 2) bns = dt == GEMM_BF16 ? std::vector<int>{128, 256} : std::vector<int>{64, 128, 256};
             else if (dt == GEMM_BF16) bns = {64, 128, 192, 256};
             else bns = {32, 64, 128, 192, 256};
             for (int bn : bns) {
                 for (int bk : {span, 2 * span}) {
-                    const int st_max = max_stages_for(bm, bn, bk, dt, swap, d.smem_per_block);
+                    const int st_max = max_stages_for(bm, bn, bk, dt, swap, d.smem_per_block, cg);
                     if (st_max < 2) continue;
                     std::vector<int> stage_list = {std::min(4, st_max)};
                     if (st_max != stage_list[0]) stage_list.push_back(st_max);
+                    // CTAs per tile: cg.  Split-K and raster variants are judged by CTA counts.
                     const int64_t tiles = cdiv(rows, bm) * cdiv(cols, bn);
                     const int64_t num_kb = cdiv(K, bk);
                     std::vector<int> splits;
-                    if (tiles < 4LL * d.sm_count)
+                    if (tiles * cg < 4LL * d.sm_count)
                         for (int s : kSplits)
-                            if (2LL * s <= num_kb && tiles * s <= 16LL * d.sm_count) splits.push_back(s);
+                            if (2LL * s <= num_kb && tiles * s * cg <= 16LL * d.sm_count) splits.push_back(s);
                     std::vector<std::pair<int, int>> scheds = {{0, 1}};
-                    if (tiles > d.sm_count) {
+                    if (tiles * cg > d.sm_count) {
                         scheds.clear();
                         for (int r = 0; r < 2; ++r)
                             for (int g : kGroups) scheds.push_back({r, g});
@@ -205,7 +219,7 @@ std::vector<gemm_config> enumerate(int64_t M, int64_t N, int64_t K, int dt, int 
                     for (int s : splits) combos.push_back({0, 1, s});
                     for (int st : stage_list) {
                         for (const Combo &cb : combos) {
-                            gemm_config c{bm, bn, bk, st, cb.raster, cb.group, cb.split, 1, swap};
+                            gemm_config c{bm, bn, bk, st, cb.raster, cb.group, cb.split, cg, swap};
                             if (check_config(M, N, K, dt, epi, c, d) == GEMM_FEASIBLE) out.push_back(c);
                         }
                     }
@@ -219,7 +233,7 @@ std::vector<gemm_config> enumerate(int64_t M, int64_t N, int64_t K, int dt, int 
 gemm_config fixed_config(int dt, const gemm_device_params &d)
 {
     const int span = span_elems(dt);
-    gemm_config c{128, 128, span, max_stages_for(128, 128, span, dt, 0, d.smem_per_block), 0, 1, 1, 1, 0};
+    gemm_config c{128, 128, span, max_stages_for(128, 128, span, dt, 0, d.smem_per_block, 1), 0, 1, 1, 1, 0};
     return c;
 }
 
@@ -276,9 +290,16 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
     const int64_t num_kb = cdiv(K, c.bk);
     const int64_t units = tiles * S;
     const int64_t sms = d.sm_count;
-    const int64_t ctas = std::max<int64_t>(1, std::min(units, sms));
-    const int64_t waves = cdiv(units, sms);
-    const int64_t upc = cdiv(units, ctas);           // units of the busiest CTA
+    // A CTA pair (cta_group 2) runs each unit on two CTAs, each holding 128 rows
+    // of the tile and loading half of B's columns.
+    const int64_t cg = c.cta_group == 2 ? 2 : 1;
+    const int64_t rows_cta = cg == 2 ? 128 : c.bm;
+    const int64_t bcols_cta = cg == 2 ? c.bn / 2 : c.bn;
+    const int64_t cta_units = units * cg;
+    int64_t ctas = std::max<int64_t>(cg, std::min(cta_units, sms));
+    if (cg == 2) ctas &= ~(int64_t)1;
+    const int64_t waves = cdiv(cta_units, sms);
+    const int64_t upc = cdiv(units, ctas / cg);      // units of the busiest CTA
     const int64_t kbu = cdiv(num_kb, S);             // K-blocks of the longest slice
     const double clk = d.sm_clock_mhz * 1e6;
     const double flops = 2.0 * (double)M * (double)N * (double)K;
@@ -287,7 +308,7 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
     // of the peak, and the issuing warp spends mma_issue_clk per MMA plus
     // kblock_clk per stage; the slower of the two sets the pace.
     const double peak = (dt == GEMM_BF16 ? d.peak_tflops_bf16 : d.peak_tflops_tf32) * 1e12;
-    const double halves = c.bm / 128, ksteps = (double)c.bk * e / 32.0, kslice = 32.0 / e;
+    const double halves = cg == 2 ? 1 : c.bm / 128, ksteps = (double)c.bk * e / 32.0, kslice = 32.0 / e;
     const double mma_flop = 2.0 * 128.0 * c.bn * kslice;
     const double t_exec = halves * ksteps * mma_flop / (peak / (double)sms);
     const double t_issue = (halves * ksteps * d.mma_issue_clk + d.kblock_clk) / clk;
@@ -295,14 +316,14 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
 
     // L2 -> shared memory: every unit streams (bm + bn)·bk·elt bytes per K-block
     // ("Tile Selection": per-block panel traffic; reuse across blocks is in L2).
-    const double l2_bytes = (double)units * (double)kbu * (c.bm + c.bn) * (double)c.bk * e;
+    const double l2_bytes = (double)cta_units * (double)kbu * (double)(rows_cta + bcols_cta) * (double)c.bk * e;
     const double t_l2 = l2_bytes / (d.l2_gbs * 1e9);
 
     // HBM: operands either fit in half of L2 (threshold regime: compulsory bytes
     // only) or are re-read once per wave of concurrent tiles, with the wave's
     // footprint shaped by the tile order (group-G band).
     const double in_bytes = ((double)M * K + (double)K * N) * e;
-    const int64_t wave_tiles = std::min<int64_t>(tiles, std::max<int64_t>(1, ctas / S));
+    const int64_t wave_tiles = std::min<int64_t>(tiles, std::max<int64_t>(1, ctas / cg / S));
     int64_t rows_w, cols_w;
     if (c.raster == 0) {
         rows_w = std::min<int64_t>(std::min<int64_t>(c.group, tiles_m), wave_tiles);
@@ -324,7 +345,7 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
 
     // Epilogue and split-K exchange.
     const double rate = (epi == GEMM_EPI_BIAS_GELU ? d.epi_gelu_elems_per_clk : d.epi_elems_per_clk) * clk;
-    const double elems = (double)c.bm * c.bn;
+    const double elems = (double)rows_cta * c.bn;   // one CTA's share of a tile
     const double part = elems * 4.0;
     double exposed, t_split;
     if (S == 1) {
@@ -335,13 +356,13 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
         const double main_unit = t_main / (double)upc;
         exposed = epi_t + (double)(upc - 1) * (two_acc ? std::max(0.0, epi_t - main_unit) : epi_t);
         t_split = 0.0;
-    } else if (units <= sms) {
+    } else if (cta_units <= sms) {
         // Cooperative fix-up: write one partial tile, read one share of S.
         exposed = elems / (double)S / rate;
         t_split = 2.0 * part / (d.splitk_gbs * 1e9);
     } else {
         // Last arriver: the CTA finishing a tile reads all S partials.
-        const double fix_tiles = (double)cdiv(tiles, ctas);
+        const double fix_tiles = (double)cdiv(tiles * cg, ctas);
         exposed = fix_tiles * elems / rate;
         t_split = ((double)upc + fix_tiles * (double)S) * part / (d.splitk_gbs * 1e9);
     }
@@ -355,7 +376,7 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
     t.epilogue_us = exposed * 1e6;
     t.splitk_us = t_split * 1e6;
     t.launch_us = d.launch_us;
-    t.wave_eff = (double)units / ((double)waves * (double)sms);
+    t.wave_eff = (double)cta_units / ((double)waves * (double)sms);
     t.tile_eff = t_exec / std::max(t_exec, t_issue);
     t.pad_eff = K > 0 ? ((double)rows * cols * K) /
                             ((double)tiles_m * c.bm * (double)tiles_n * c.bn * (double)num_kb * c.bk)

@@ -255,8 +255,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     k.a_mn_major = (cfg.swap_ab && !p->b_kmajor) ? 1 : 0;
     k.b_mn_major = (!cfg.swap_ab && !p->b_kmajor) ? 1 : 0;
     const uint32_t fmt = dt == GEMM_BF16 ? 1u : 2u;  // BF16 (kind::f16) / TF32 (kind::tf32)
+    k.pair = cfg.cta_group == 2 ? 1 : 0;
+    const uint32_t mma_m = k.pair ? 256u : 128u;  // a pair's MMA spans both CTAs' 128 rows
     k.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)k.a_mn_major << 15) |
-              ((uint32_t)k.b_mn_major << 16) | ((uint32_t)(cfg.bn >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+              ((uint32_t)k.b_mn_major << 16) | ((uint32_t)(cfg.bn >> 3) << 17) | ((mma_m >> 4) << 24);
     k.a_stage_bytes = p->L.a_stage_bytes;
     k.b_stage_bytes = p->L.b_stage_bytes;
     k.tx_bytes = p->L.stage_bytes;
@@ -271,24 +273,26 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     k.staging_buf_bytes = p->L.staging_buf_bytes;
     p->grid = (int)std::min<int64_t>(k.num_units, dev.sm_count);
     // One wave of split-K units: the slices of a tile finalise it together.
-    k.coop_fixup = (cfg.split_k > 1 && k.num_units <= dev.sm_count) ? 1 : 0;
+    k.coop_fixup = (cfg.split_k > 1 && k.num_units <= dev.sm_count && !k.pair) ? 1 : 0;
     // Or the slices of a tile form a cluster and reduce through distributed
     // shared memory (decided below, once the shared-memory limit is set).  Only
     // for one wave: past it, one CTA per unit loses the persistent schedule's
     // overlap, which costs more than the global exchange it replaces.
-    const bool want_cluster = g_split_route.load() == 0 && k.num_units <= dev.sm_count &&
+    const bool want_cluster = g_split_route.load() == 0 && k.num_units <= dev.sm_count && !k.pair &&
                               cluster_reduce_fits(cfg, dt);
     // Ask for more than half of the SM's shared memory so that no two CTAs of
     // this kernel share an SM (each may hold up to 512 TMEM columns).
     const int64_t one_per_sm = dev.smem_per_block / 2 + 1024;
     p->smem_request = (int)std::min<int64_t>(dev.smem_per_block, std::max<int64_t>(p->L.smem_total, one_per_sm));
 
-    cudaError_t e = cudaMalloc(&p->aux, (size_t)(1 + p->tiles) * sizeof(int32_t));
+    // Split-K counters: one per exchange tile (a pair's tile is two, one per CTA).
+    const int64_t n_counters = p->tiles * (k.pair ? 2 : 1);
+    cudaError_t e = cudaMalloc(&p->aux, (size_t)(1 + n_counters) * sizeof(int32_t));
     if (e != cudaSuccess) {
         delete p;
         return cuda_err(e, "cudaMalloc(plan status/counters)");
     }
-    e = cudaMemset(p->aux, 0, (size_t)(1 + p->tiles) * sizeof(int32_t));
+    e = cudaMemset(p->aux, 0, (size_t)(1 + n_counters) * sizeof(int32_t));
     if (e != cudaSuccess) {
         cudaFree(p->aux);
         delete p;
@@ -323,9 +327,24 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
         destroy_plan(p);
         return rc;
     }
+    if (k.pair) {
+        // Pairs that fit at once: the persistent grid, and whether all split-K
+        // units are resident together (the slices then finalise cooperatively;
+        // the capacity check stands in for a cooperative launch, which does not
+        // combine with clusters).
+        int pairs = 0;
+        e = max_active_clusters(dt, k.a_mn_major, k.b_mn_major, 2, 2, p->smem_request, &pairs);
+        if (e != cudaSuccess || pairs < 1) {
+            cudaGetLastError();
+            destroy_plan(p);
+            return set_error(GEMM_ERR_INFEASIBLE, "no CTA pair of this configuration fits on the device");
+        }
+        p->grid = 2 * (int)std::min<int64_t>(k.num_units, pairs);
+        k.coop_fixup = (cfg.split_k > 1 && k.num_units <= pairs) ? 1 : 0;
+    }
     if (want_cluster) {
         int clusters = 0;
-        e = max_active_clusters(dt, k.a_mn_major, k.b_mn_major, cfg.split_k, p->smem_request, &clusters);
+        e = max_active_clusters(dt, k.a_mn_major, k.b_mn_major, 1, cfg.split_k, p->smem_request, &clusters);
         if (e != cudaSuccess) {
             cudaGetLastError();
             clusters = 0;
@@ -380,8 +399,11 @@ static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const
         // A: [M, K] K-major, box [MMA extent x one span of K].
         // B: [K, N] read MN-major (box [bk x one span of N]) or its transposed
         //    copy [N, K] read K-major (box [MMA extent x one span of K]).
-        const uint32_t a_rows = c.swap_ab ? c.bn : c.bm;      // A's extent in the MMA
-        const uint32_t b_rows = c.swap_ab ? c.bm : c.bn;      // B's extent in the MMA
+        // A's and B's extents per CTA (a CTA pair loads 128 rows of A and half
+        // of B's columns in each CTA).
+        const bool pair = c.cta_group == 2;
+        const uint32_t a_rows = c.swap_ab ? c.bn : (pair ? 128u : (uint32_t)c.bm);
+        const uint32_t b_rows = c.swap_ab ? c.bm : (pair ? (uint32_t)c.bn / 2 : (uint32_t)c.bn);
         CUtensorMap *am = c.swap_ab ? &d.mb : &d.ma;
         CUtensorMap *bm = c.swap_ab ? &d.ma : &d.mb;
         rc = encode_2d(am, dt, A, p->K, p->M, span, a_rows, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -451,7 +473,7 @@ int plan_launch_info(gemm_plan_t p, gemm_launch_info *out)
     out->grid = p->grid;
     out->block = kThreadsPerCta;
     out->smem_bytes = p->smem_request;
-    out->cluster = k.cluster_k > 1 ? k.cluster_k : 1;
+    out->cluster = k.cluster_k > 1 ? k.cluster_k : k.pair ? 2 : 1;
     out->splitk_route = p->cfg.split_k <= 1 ? 0 : k.cluster_k > 1 ? 3 : k.coop_fixup ? 2 : 1;
     out->b_transposed = p->b_kmajor ? 1 : 0;
     out->units = k.num_units;

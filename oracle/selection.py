@@ -284,16 +284,25 @@ def staging_bytes(dtype, swap_ab):
     return 8 * 2 * rows * 32 * elt_bytes(dtype)
 
 
+def cta_share(cfg: Config):
+    """(A rows, B columns) one CTA stages: a CTA pair (cta_group 2) splits a
+    256-row tile into 128 rows of A per CTA and halves B's columns."""
+    if cfg.cta_group == 2:
+        return 128, cfg.bn // 2
+    return cfg.bm, cfg.bn
+
+
 def stage_bytes(cfg: Config, dtype):
-    return (cfg.bm + cfg.bn) * cfg.bk * elt_bytes(dtype)
+    a_rows, b_cols = cta_share(cfg)
+    return (a_rows + b_cols) * cfg.bk * elt_bytes(dtype)
 
 
 def smem_bytes(cfg: Config, dtype):
     return cfg.stages * stage_bytes(cfg, dtype) + staging_bytes(dtype, cfg.swap_ab) + AUX_SMEM
 
 
-def max_stages(bm, bn, bk, dtype, swap_ab, smem_per_block):
-    per = (bm + bn) * bk * elt_bytes(dtype)
+def max_stages(bm, bn, bk, dtype, swap_ab, smem_per_block, cta_group=1):
+    per = ((128 + bn // 2) if cta_group == 2 else (bm + bn)) * bk * elt_bytes(dtype)
     room = smem_per_block - staging_bytes(dtype, swap_ab) - AUX_SMEM
     return max(0, min(MAX_STAGES, room // per))
 
@@ -301,7 +310,7 @@ def max_stages(bm, bn, bk, dtype, swap_ab, smem_per_block):
 def tmem_columns(cfg: Config):
     """Columns of one accumulator (fp32, one column per output column per 128
     rows) and how many accumulators fit (2 = epilogue overlaps the next tile)."""
-    acc = (cfg.bm // 128) * cfg.bn
+    acc = (1 if cfg.cta_group == 2 else cfg.bm // 128) * cfg.bn
     nbuf = 2 if 2 * acc <= TMEM_COLUMNS else 1
     return acc, nbuf
 
@@ -310,7 +319,9 @@ def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
     """First violated rule, in the documented order, or R_OK."""
     elt = elt_bytes(dtype)
     span = span_elems(dtype)
-    if cfg.cta_group != 1:
+    if cfg.cta_group not in (1, 2):
+        return R_CTA_GROUP
+    if cfg.cta_group == 2 and (cfg.bm != 256 or cfg.swap_ab != 0):
         return R_CTA_GROUP
     if cfg.bm not in (128, 256):
         return R_UMMA_M
@@ -319,6 +330,8 @@ def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
     if cfg.swap_ab not in (0, 1):
         return R_LAYOUT
     if cfg.swap_ab == 0 and (cfg.bn % span != 0 or cfg.bn % 32 != 0):
+        return R_LAYOUT
+    if cfg.cta_group == 2 and (cfg.bn // 2) % span != 0:
         return R_LAYOUT
     if cfg.bk % span != 0 or not (1 <= cfg.bk // span <= 4):
         return R_BK
@@ -343,39 +356,44 @@ def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
 
 def gb300_candidates(M, N, K, dtype, epi, dev: Device):
     """The documented GB300 candidate generator (nested in this order): swap_ab,
-    bm, bn, bk, stages, then the schedule/split combinations; infeasible
-    combinations are dropped."""
+    (bm, cta_group) in (128, 1), (256, 1), (256, 2) (pairs unswapped only), bn,
+    bk, stages, then the schedule/split combinations, judged by CTA counts
+    (tiles × cta_group); infeasible combinations are dropped."""
     span = span_elems(dtype)
     out = []
     swaps = (0, 1) if M <= 256 else (0,)
     for swap in swaps:
         rows, cols = (N, M) if swap else (M, N)
-        for bm in (128, 256):
+        for bm, cg in ((128, 1), (256, 1), (256, 2)):
+            if cg == 2 and swap:
+                continue
             if swap:
                 bns = (16, 32, 64, 128, 256)
+            elif cg == 2:
+                bns = (128, 256) if dtype == DT_BF16 else (64, 128, 256)
             elif dtype == DT_BF16:
                 bns = (64, 128, 192, 256)
             else:
                 bns = (32, 64, 128, 192, 256)
             for bn in bns:
                 for bk in (span, 2 * span):
-                    st_max = max_stages(bm, bn, bk, dtype, swap, dev.smem_per_block)
+                    st_max = max_stages(bm, bn, bk, dtype, swap, dev.smem_per_block, cg)
                     if st_max < 2:
                         continue
                     stage_list = sorted({min(4, st_max), st_max})
                     tiles = ceil_div(rows, bm) * ceil_div(cols, bn)
                     num_kb = ceil_div(K, bk)
                     splits = []
-                    if tiles < 4 * dev.sm_count:
+                    if tiles * cg < 4 * dev.sm_count:
                         splits = [s for s in SPLITS
-                                  if 2 * s <= num_kb and tiles * s <= 16 * dev.sm_count]
+                                  if 2 * s <= num_kb and tiles * s * cg <= 16 * dev.sm_count]
                     scheds = [(0, 1)]
-                    if tiles > dev.sm_count:
+                    if tiles * cg > dev.sm_count:
                         scheds = [(r, g) for r in (0, 1) for g in (1, 4, 8, 16)]
                     combos = [(r, g, 1) for (r, g) in scheds] + [(0, 1, s) for s in splits]
                     for st in stage_list:
                         for (r, g, s) in combos:
-                            cfg = Config(bm, bn, bk, st, r, g, s, 1, swap)
+                            cfg = Config(bm, bn, bk, st, r, g, s, cg, swap)
                             if gb300_check(M, N, K, dtype, epi, cfg, dev) == R_OK:
                                 out.append(cfg)
     return out
@@ -447,26 +465,32 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
     num_kb = ceil_div(K, cfg.bk)
     units = tiles * S
     sms = dev.sm_count
-    ctas = max(1, min(units, sms))
-    nw = waves(units, sms)
-    per_cta_units = ceil_div(units, ctas)
+    # A CTA pair runs each unit on two CTAs (128 tile rows and half of B each).
+    cg = 2 if cfg.cta_group == 2 else 1
+    rows_cta, bcols_cta = cta_share(cfg)
+    cta_units = units * cg
+    ctas = max(cg, min(cta_units, sms))
+    if cg == 2:
+        ctas -= ctas % 2
+    nw = waves(cta_units, sms)
+    per_cta_units = ceil_div(units, ctas // cg)
     slice_kb = ceil_div(num_kb, S)
     clock = dev.sm_clock_mhz * 1e6
     flops = 2.0 * M * N * K
 
     peak = (dev.peak_tflops_bf16 if dtype == DT_BF16 else dev.peak_tflops_tf32) * 1e12
-    halves = cfg.bm // 128
+    halves = 1 if cg == 2 else cfg.bm // 128
     ksteps = cfg.bk * elt / 32
     one_mma = 2.0 * 128 * cfg.bn * (32 / elt)
     execute = halves * ksteps * one_mma / (peak / sms)
     issue = (halves * ksteps * dev.mma_issue_clk + dev.kblock_clk) / clock
     mma_s = per_cta_units * slice_kb * max(execute, issue)
 
-    l2_bytes = units * slice_kb * (cfg.bm + cfg.bn) * cfg.bk * elt
+    l2_bytes = cta_units * slice_kb * (rows_cta + bcols_cta) * cfg.bk * elt
     l2_s = l2_bytes / (dev.l2_gbs * 1e9)
 
     in_bytes = (M * K + K * N) * elt
-    wave_tiles = min(tiles, max(1, ctas // S))
+    wave_tiles = min(tiles, max(1, ctas // cg // S))
     if cfg.raster == 0:
         rows_w = min(cfg.group, tiles_m, wave_tiles)
         cols_w = min(ceil_div(wave_tiles, rows_w), tiles_n)
@@ -483,7 +507,7 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
 
     per_clock = dev.epi_gelu_elems_per_clk if epi == EPI_GELU else dev.epi_elems_per_clk
     rate = per_clock * clock
-    elems = cfg.bm * cfg.bn
+    elems = rows_cta * cfg.bn          # one CTA's share of a tile
     partial = elems * 4
     if S == 1:
         one = elems / rate
@@ -492,11 +516,11 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
         hidden_excess = max(0.0, one - unit_main) if two_buffers else one
         epi_s = one + (per_cta_units - 1) * hidden_excess
         split_s = 0.0
-    elif units <= sms:
+    elif cta_units <= sms:
         epi_s = (elems / S) / rate
         split_s = 2 * partial / (dev.splitk_gbs * 1e9)
     else:
-        fix = ceil_div(tiles, ctas)
+        fix = ceil_div(tiles * cg, ctas)
         epi_s = fix * elems / rate
         split_s = (per_cta_units + fix * S) * partial / (dev.splitk_gbs * 1e9)
     total = main + epi_s + split_s + dev.launch_us * 1e-6
@@ -507,7 +531,7 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
     return {"predicted_us": total * 1e6, "mma_us": mma_s * 1e6, "l2_us": l2_s * 1e6,
             "hbm_us": hbm_s * 1e6, "latency_us": latency_s * 1e6, "epilogue_us": epi_s * 1e6,
             "splitk_us": split_s * 1e6, "launch_us": dev.launch_us,
-            "wave_eff": units / (nw * sms), "tile_eff": execute / max(execute, issue), "pad_eff": pad,
+            "wave_eff": cta_units / (nw * sms), "tile_eff": execute / max(execute, issue), "pad_eff": pad,
             "hbm_bytes": hbm, "l2_bytes": l2_bytes, "flops": flops,
             "tiles": tiles, "units": units, "waves": nw, "ctas": ctas}
 

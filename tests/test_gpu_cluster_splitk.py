@@ -98,3 +98,31 @@ def test_other_split_plans_keep_the_global_exchange(shape, cfg):
     out, ok, info = _run("bf16", A, B, bias, "relu", cfg, route=0)
     assert info.splitk_route in (1, 2) and info.cluster == 1
     assert ok and np.array_equal(device_bits(out), oracle_rounded_bits(A, B, bias, "relu", g.BF16))
+
+
+# CTA pairs: persistent pairs walking many units (accumulator hand-back between
+# the two CTAs), and split-K on pairs through both global-memory routes.
+PAIR_CASES = [
+    ((2048, 2048, 512), C(256, 128, 64, 6, 0, 1, 1, 2), 0),     # 128 units on at most 76 pairs
+    ((1000, 1000, 2056), C(256, 256, 64, 6, 0, 1, 4, 2), 2),    # one wave: slices finalise together
+    ((2048, 2048, 1024), C(256, 256, 64, 4, 0, 1, 2, 2), 1),    # more units than pairs: last arriver
+]
+
+
+@pytest.mark.parametrize("shape,cfg,route", PAIR_CASES, ids=lambda v: str(v))
+def test_cta_pair_plans_bit_exact(shape, cfg, route):
+    M, N, K = shape
+    A, B, bias = operands(M, N, K, "bf16", "int", seed=15)
+    out, ok, info = _run("bf16", A, B, bias, "relu", cfg, route=0)
+    assert info.cluster == 2 and info.grid % 2 == 0 and info.splitk_route == route
+    assert ok and np.array_equal(device_bits(out), oracle_rounded_bits(A, B, bias, "relu", g.BF16))
+
+
+def test_cta_pair_agrees_with_single_cta_tiles_bitwise_on_integers_and_within_tolerance():
+    M, N, K = 520, 1000, 2056
+    A, B, bias = operands(M, N, K, "bf16", "scaled_normal", seed=16)
+    pair, ok1, i1 = _run("bf16", A, B, bias, "gelu", C(256, 256, 64, 6, 0, 1, 1, 2), route=0)
+    single, ok2, i2 = _run("bf16", A, B, bias, "gelu", C(256, 256, 64, 3, 0, 1, 1, 1), route=0)
+    assert i1.cluster == 2 and i2.cluster == 1 and ok1 and ok2
+    assert normalised_error(pair, A, B, bias, "gelu") <= 2e-3
+    assert normalised_error(single, A, B, bias, "gelu") <= 2e-3

@@ -38,6 +38,12 @@ BF16_CASES = [
     ((20, 320, 520), C(128, 32, 64, 6, 0, 1, 2, 1, 1)),
     ((40, 264, 520), C(256, 64, 128, 2, 0, 1, 3, 1, 1)),
     ((16, 1024, 1024), C(128, 16, 64, 8, 0, 1, 8, 1, 1)),
+    # CTA pairs (cta_group 2): 256-row tiles, each CTA 128 rows and half of B
+    ((300, 320, 520), C(256, 256, 64, 4, 0, 1, 1, 2)),
+    ((300, 320, 520), C(256, 128, 64, 6, 0, 1, 1, 2)),
+    ((300, 320, 520), C(256, 256, 128, 3, 0, 1, 1, 2)),
+    ((520, 640, 264), C(256, 128, 64, 4, 1, 4, 1, 2)),
+    ((300, 320, 1032), C(256, 256, 64, 4, 0, 1, 4, 2)),
 ]
 
 FP32_CASES = [
@@ -48,6 +54,9 @@ FP32_CASES = [
     ((200, 160, 136), C(128, 64, 32, 4, 0, 1, 2)),
     ((24, 160, 136), C(128, 16, 32, 4, 0, 1, 1, 1, 1)),
     ((24, 160, 136), C(128, 32, 64, 4, 0, 1, 3, 1, 1)),
+    ((200, 160, 136), C(256, 64, 32, 4, 0, 1, 1, 2)),
+    ((200, 160, 264), C(256, 128, 32, 4, 0, 1, 2, 2)),
+    ((264, 256, 136), C(256, 256, 64, 2, 0, 1, 1, 2)),
 ]
 
 
