@@ -135,6 +135,17 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, floa
                  : "memory");
 }
 
+// 16-byte global -> shared copy that bypasses registers (completion by group).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit_wait_all()
+{
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr)
 {
     float4 v;
@@ -463,6 +474,13 @@ __device__ __noinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, con
             }
         }
     }
+}
+
+// Publishes this CTA's earlier global writes (ordered before this thread by a
+// CTA barrier) together with the increment.
+__device__ __forceinline__ void red_release_gpu_add(int32_t *ptr, int32_t v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *ptr)
@@ -1098,6 +1116,121 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++acc == e_n_acc) {
                     acc = 0;
                     acc_phase ^= 1u;
+                }
+                continue;
+            }
+            if (e_coop && !e_swap_ab) {
+                // Cooperative split-K (all slices resident, one unit per CTA).  The
+                // tile is cut into 32-row x 32-column blocks; block (row group rg,
+                // chunk c) belongs to slice (c/2 + max(1, chunks/2)*rg) mod S, which
+                // gives every epilogue warp an even share of every slice's blocks.
+                // A slice keeps its own blocks in TMEM and writes the others to the
+                // workspace ([slice][block][4-column group][32 rows][4], 4 KB per
+                // block); after all S slices have arrived, each owner adds the S
+                // partials of its blocks in slice order and runs the epilogue.
+                const int32_t S = e_split_k, me = w.split;
+                const int32_t half_chunks = chunks >= 2 ? chunks / 2 : 1;
+                const int32_t nblocks = (cta_rows / 32) * chunks;
+                // Per-warp fetch region in the ring: R blocks of 4 KB (R >= 1).
+                const int32_t fetch_r = max(1, min(S - 1, (int32_t)(p.off_staging / (kEpiWarps * 4096u))));
+                const uint32_t fetch_base = base + (uint32_t)ew * (uint32_t)fetch_r * 4096u;
+                float4 *const xws = reinterpret_cast<float4 *>(e_workspace + (size_t)xtile * S * (size_t)tile_elems);
+                for (int32_t h = 0; h < halves; ++h) {
+                    const int32_t rg = h * 4 + q;
+#pragma unroll 1
+                    for (int ci = 0; ci < 4; ++ci) {
+                        const int32_t c = cg + 2 * ci;
+                        if (c >= chunks) break;
+                        if ((c / 2 + half_chunks * rg) % S == me) continue;
+                        float v[32];
+                        if (nk > 0) tmem_load_chunk<32>(tacc + (uint32_t)(h * e_bn + c * 32), v);
+                        else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                        }
+                        float4 *dst = xws + (size_t)(me * nblocks + rg * chunks + c) * 256 + lane;
+#pragma unroll
+                        for (int j4 = 0; j4 < 8; ++j4)
+                            dst[j4 * 32] = make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+                    }
+                }
+                named_bar_sync(1, kEpiThreads);
+                bool cok = true;
+                if (ew == 0 && lane == 0) {
+                    red_release_gpu_add(e_counters + xtile, 1);
+                    cok = wait_counter(e_counters + xtile, S, ctl, SITE_FIXUP);
+                }
+                if (named_bar_any(1, kEpiThreads, !cok)) break;
+                for (int32_t h = 0; h < halves; ++h) {
+                    const int32_t rg = h * 4 + q;
+#pragma unroll 1
+                    for (int ci = 0; ci < 4; ++ci) {
+                        const int32_t c = cg + 2 * ci;
+                        if (c >= chunks) break;
+                        if ((c / 2 + half_chunks * rg) % S != me) continue;
+                        const float4 *src = xws + (size_t)(rg * chunks + c) * 256 + lane;
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                        // The other slices' blocks are fetched R at a time with cp.async
+                        // into this warp's region of the (now idle) pipeline ring, each
+                        // thread reading back only its own 16-byte pieces; the sum runs
+                        // in slice order with this slice's partial read from TMEM.
+#pragma unroll 1
+                        for (int32_t s = 0; s < S;) {
+                            int32_t s_end = s, got = 0;
+                            while (s_end < S && (got < fetch_r || s_end == me)) {
+                                if (s_end != me) {
+                                    const uint32_t dst = fetch_base + (uint32_t)got * 4096u + (uint32_t)lane * 16u;
+                                    const float4 *g = src + (size_t)s_end * nblocks * 256;
+#pragma unroll
+                                    for (int j4 = 0; j4 < 8; ++j4) cp_async_16(dst + (uint32_t)j4 * 512u, g + j4 * 32);
+                                    ++got;
+                                }
+                                ++s_end;
+                            }
+                            cp_async_commit_wait_all();
+                            int32_t slot = 0;
+                            for (; s < s_end; ++s) {
+                                if (s == me) {
+                                    if (nk > 0) {
+#pragma unroll
+                                        for (int hh = 0; hh < 2; ++hh) {
+                                            float o[16];
+                                            tmem_load_chunk<16>(tacc + (uint32_t)(h * e_bn + c * 32 + hh * 16), o);
+#pragma unroll
+                                            for (int j = 0; j < 16; ++j) v[hh * 16 + j] += o[j];
+                                        }
+                                    }
+                                } else {
+                                    const uint32_t from = fetch_base + (uint32_t)slot * 4096u + (uint32_t)lane * 16u;
+#pragma unroll
+                                    for (int j4 = 0; j4 < 8; ++j4) {
+                                        const float4 t = ld_shared_v4(from + (uint32_t)j4 * 512u);
+                                        v[4 * j4] += t.x;
+                                        v[4 * j4 + 1] += t.y;
+                                        v[4 * j4 + 2] += t.z;
+                                        v[4 * j4 + 3] += t.w;
+                                    }
+                                    ++slot;
+                                }
+                            }
+                        }
+                        bias_act_rows(v, bcol[ci], e_epi);
+                        const int32_t n = c0 + c * 32, y = r0 + rg * 32;
+                        store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
+                    }
+                }
+                release_acc(acc);
+                if (++acc == e_n_acc) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+                // The last of the S slices to leave resets the counter for the next launch.
+                named_bar_sync(1, kEpiThreads);
+                if (ew == 0 && lane == 0) {
+                    const int32_t old = atomicAdd(e_counters + xtile, 1);
+                    if (old == 2 * S - 1) atomicExch(e_counters + xtile, 0);
                 }
                 continue;
             }

@@ -273,7 +273,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     k.staging_buf_bytes = p->L.staging_buf_bytes;
     p->grid = (int)std::min<int64_t>(k.num_units, dev.sm_count);
     // One wave of split-K units: the slices of a tile finalise it together.
-    k.coop_fixup = (cfg.split_k > 1 && k.num_units <= dev.sm_count && !k.pair) ? 1 : 0;
+    // (The cooperative fix-up stages peer partials in the idle pipeline ring: it
+    // needs 8 warps x 4 KB of it.)
+    const bool ring_room = p->L.off_staging >= 8u * 4096u;
+    k.coop_fixup = (cfg.split_k > 1 && k.num_units <= dev.sm_count && !k.pair && ring_room) ? 1 : 0;
     // Or the slices of a tile form a cluster and reduce through distributed
     // shared memory (decided below, once the shared-memory limit is set).  Only
     // for one wave: past it, one CTA per unit loses the persistent schedule's
@@ -340,7 +343,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
             return set_error(GEMM_ERR_INFEASIBLE, "no CTA pair of this configuration fits on the device");
         }
         p->grid = 2 * (int)std::min<int64_t>(k.num_units, pairs);
-        k.coop_fixup = (cfg.split_k > 1 && k.num_units <= pairs) ? 1 : 0;
+        k.coop_fixup = (cfg.split_k > 1 && k.num_units <= pairs && ring_room) ? 1 : 0;
     }
     if (want_cluster) {
         int clusters = 0;
