@@ -41,14 +41,14 @@ void params_default(gemm_device_params *d)
     d->peak_tflops_tf32 = 944.8;
     d->hbm_gbs = 6675.8;
     d->sm_clock_mhz = 2070.0;
-    d->l2_gbs = 15020.0;
-    d->mma_issue_clk = 40.3;
-    d->kblock_clk = 482.5;
-    d->mem_latency_us = 1.358;
-    d->epi_elems_per_clk = 3.08;
-    d->epi_gelu_elems_per_clk = 5.21;
-    d->splitk_gbs = 17.55;
-    d->launch_us = 7.68;
+    d->l2_gbs = 14888.0;
+    d->mma_issue_clk = 39.53;
+    d->kblock_clk = 483.2;
+    d->mem_latency_us = 1.375;
+    d->epi_elems_per_clk = 3.632;
+    d->epi_gelu_elems_per_clk = 5.109;
+    d->splitk_gbs = 15.99;
+    d->launch_us = 7.50;
     d->kernel_regs = 0;
     d->threads_per_cta = kThreadsPerCta;
 }
@@ -357,9 +357,10 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
         exposed = epi_t + (double)(upc - 1) * (two_acc ? std::max(0.0, epi_t - main_unit) : epi_t);
         t_split = 0.0;
     } else if (cta_units <= sms) {
-        // Cooperative fix-up: write one partial tile, read one share of S.
+        // Cooperative fix-up: each slice keeps its own share of the tile in TMEM,
+        // writes the other (S-1)/S and reads (S-1) partials of its share.
         exposed = elems / (double)S / rate;
-        t_split = 2.0 * part / (d.splitk_gbs * 1e9);
+        t_split = 2.0 * part * (double)(S - 1) / (double)S / (d.splitk_gbs * 1e9);
     } else {
         // Last arriver: the CTA finishing a tile reads all S partials.
         const double fix_tiles = (double)cdiv(tiles * cg, ctas);

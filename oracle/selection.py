@@ -255,14 +255,14 @@ class Device:
     peak_tflops_tf32: float = 944.8
     hbm_gbs: float = 6675.8
     sm_clock_mhz: float = 2070.0
-    l2_gbs: float = 15020.0
-    mma_issue_clk: float = 40.3
-    kblock_clk: float = 482.5
-    mem_latency_us: float = 1.358
-    epi_elems_per_clk: float = 3.08
-    epi_gelu_elems_per_clk: float = 5.21
-    splitk_gbs: float = 17.55
-    launch_us: float = 7.68
+    l2_gbs: float = 14888.0
+    mma_issue_clk: float = 39.53
+    kblock_clk: float = 483.2
+    mem_latency_us: float = 1.375
+    epi_elems_per_clk: float = 3.632
+    epi_gelu_elems_per_clk: float = 5.109
+    splitk_gbs: float = 15.99
+    launch_us: float = 7.50
     kernel_regs: int = 0
     threads_per_cta: int = THREADS_PER_CTA
     extra: dict = field(default_factory=dict)
@@ -518,7 +518,7 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
         split_s = 0.0
     elif cta_units <= sms:
         epi_s = (elems / S) / rate
-        split_s = 2 * partial / (dev.splitk_gbs * 1e9)
+        split_s = 2 * partial * (S - 1) / S / (dev.splitk_gbs * 1e9)
     else:
         fix = ceil_div(tiles * cg, ctas)
         epi_s = fix * elems / rate
