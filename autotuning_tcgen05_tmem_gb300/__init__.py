@@ -41,7 +41,8 @@ EXPORTS = ["gemm_version", "gemm_last_error", "gemm_device_params_default",
            "gemm_plan_with_config", "gemm_plan_config", "gemm_run", "gemm_run_host",
            "gemm_plan_status", "gemm_plan_destroy", "gemm_tune", "gemm_cache_stats",
            "gemm_cache_clear", "gemm_debug_set", "gemm_run_noalloc", "gemm_tune_search",
-           "gemm_cache_save", "gemm_cache_load", "gemm_plan_launch_info"]
+           "gemm_cache_save", "gemm_cache_load", "gemm_plan_launch_info", "gemm_select_config_set",
+           "gemm_plan_from_list", "gemm_tune_batch"]
 
 
 class GemmError(RuntimeError):
@@ -156,6 +157,13 @@ def _load_library(path: str):
         "gemm_run_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "gemm_plan_status": (ctypes.c_int, [vp]),
         "gemm_plan_launch_info": (ctypes.c_int, [vp, P(LaunchInfo)]),
+        "gemm_select_config_set": (ctypes.c_int, [P(ctypes.c_double), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                  P(ctypes.c_int32), P(ctypes.c_int32), P(ctypes.c_double),
+                                                  P(ctypes.c_double)]),
+        "gemm_plan_from_list": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                               ctypes.c_int, P(Config), ctypes.c_int32, P(vp)]),
+        "gemm_tune_batch": (ctypes.c_int, [P(ctypes.c_int64), ctypes.c_int32, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_char_p, P(ctypes.c_int32)]),
         "gemm_plan_destroy": (None, [vp]),
         "gemm_tune": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, i32, P(TuneRow), i32,
                                      P(i32), P(RankStats)]),
@@ -389,6 +397,40 @@ def tune_search(M, N, K, dtype="bf16", epi="none", mode=SEARCH_MODEL_TOPK, k=24,
     _check(lib().gemm_tune_search(M, N, K, _dt(dtype), _ep(epi), mode, k, seed, rows, cap, ctypes.byref(n),
                                   ctypes.byref(s)))
     return TuneResult([rows[i] for i in range(n.value)], s)
+
+
+def select_config_set(times, max_set):
+    """Greedy shipped set from a measured table (rows: shapes, columns:
+    configurations, <= 0: does not run).  Returns (chosen column indices,
+    mean slowdown, worst slowdown)."""
+    import numpy as np
+    t = np.ascontiguousarray(np.asarray(times, dtype=np.float64))
+    ns, nc = (t.shape if t.ndim == 2 else (0, 0))
+    chosen = (ctypes.c_int32 * max(1, max_set))()
+    n = ctypes.c_int32(0)
+    mean, worst = ctypes.c_double(), ctypes.c_double()
+    _check(lib().gemm_select_config_set(t.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), ns, nc, max_set, chosen,
+                                        ctypes.byref(n), ctypes.byref(mean), ctypes.byref(worst)))
+    return [chosen[i] for i in range(n.value)], mean.value, worst.value
+
+
+def plan_from_list(M, N, K, dtype, epi, configs) -> Plan:
+    """Plan by timing only the given configurations (a shipped set)."""
+    arr = (Config * max(1, len(configs)))(*configs)
+    h = ctypes.c_void_p()
+    _check(lib().gemm_plan_from_list(M, N, K, _dt(dtype), _ep(epi), arr, len(configs), ctypes.byref(h)))
+    return Plan(h.value, M, N, K, _dt(dtype), _ep(epi))
+
+
+def tune_batch(shapes, dtype="bf16", epi="none", db_path=None) -> int:
+    """Ahead-of-time tuning of (M, N, K) shapes into the cache; saves the cache
+    to db_path when given.  Returns how many shapes were newly tuned."""
+    flat = [int(v) for mnk in shapes for v in mnk]
+    arr = (ctypes.c_int64 * max(1, len(flat)))(*flat)
+    n = ctypes.c_int32(0)
+    _check(lib().gemm_tune_batch(arr, len(shapes), _dt(dtype), _ep(epi),
+                                 os.fsencode(db_path) if db_path else None, ctypes.byref(n)))
+    return n.value
 
 
 def cache_save(path: str) -> int:

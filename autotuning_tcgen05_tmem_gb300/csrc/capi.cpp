@@ -44,7 +44,11 @@ int plan_config(gemm_plan_t p, gemm_config *out);
 int plan_launch_info(gemm_plan_t p, gemm_launch_info *out);
 void destroy_plan(gemm_plan_t p);
 int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, uint64_t seed,
-         std::vector<gemm_tune_row> &rows, gemm_rank_stats &stats, gemm_config *winner);
+         std::vector<gemm_tune_row> &rows, gemm_rank_stats &stats, gemm_config *winner,
+         const gemm_config *list, int nlist);
+int plan_from_list(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config *list, int nlist,
+                   gemm_plan_t *out);
+int tune_batch(const int64_t *mnk, int n, int dt, int epi, const char *path, int32_t *n_tuned);
 void cache_stats(int64_t *tunes, int64_t *hits, int64_t *entries);
 void cache_clear();
 int cache_save(const char *path, int64_t *n);
@@ -201,7 +205,7 @@ static int tune_into(int64_t M, int64_t N, int64_t K, int dtype, int epi, int mo
     if (!n_rows || cap < 0 || (cap > 0 && !rows)) return set_error(GEMM_ERR_INVALID_ARG, "gemm_tune: bad argument");
     std::vector<gemm_tune_row> v;
     gemm_rank_stats s;
-    const int rc = tune(M, N, K, dtype, epi, mode, k, seed, v, s, nullptr);
+    const int rc = tune(M, N, K, dtype, epi, mode, k, seed, v, s, nullptr, nullptr, 0);
     if (rc) return rc;
     int32_t i = 0;
     for (; i < cap && i < (int32_t)v.size(); ++i) rows[i] = v[i];
@@ -247,6 +251,33 @@ int gemm_cache_stats(int64_t *tunes, int64_t *hits, int64_t *entries)
 }
 
 void gemm_cache_clear(void) { cache_clear(); }
+
+int gemm_select_config_set(const double *times, int32_t n_shapes, int32_t n_configs, int32_t max_set,
+                           int32_t *chosen, int32_t *n_chosen, double *mean_slowdown, double *worst_slowdown)
+{
+    clear_error();
+    if (n_shapes < 0 || n_configs < 0 || max_set < 0 || !n_chosen || (max_set > 0 && !chosen) ||
+        ((int64_t)n_shapes * n_configs > 0 && !times))
+        return set_error(GEMM_ERR_INVALID_ARG, "gemm_select_config_set: bad argument");
+    return select_config_set(times, n_shapes, n_configs, std::min(max_set, n_configs), chosen, n_chosen,
+                             mean_slowdown, worst_slowdown);
+}
+
+int gemm_plan_from_list(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
+                        const gemm_config *list, int32_t n, gemm_plan_t *out)
+{
+    clear_error();
+    if (!out || n < 0 || (n > 0 && !list)) return set_error(GEMM_ERR_INVALID_ARG, "gemm_plan_from_list: bad argument");
+    return plan_from_list(M, N, K, dtype, epi, list, n, out);
+}
+
+int gemm_tune_batch(const int64_t *mnk, int32_t n, gemm_dtype dtype, gemm_epilogue epi, const char *db_path,
+                    int32_t *n_tuned)
+{
+    clear_error();
+    if (n < 0 || (n > 0 && !mnk)) return set_error(GEMM_ERR_INVALID_ARG, "gemm_tune_batch: bad argument");
+    return tune_batch(mnk, n, dtype, epi, db_path, n_tuned);
+}
 
 int gemm_debug_set(int32_t what, int64_t value)
 {

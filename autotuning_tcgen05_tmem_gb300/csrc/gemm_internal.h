@@ -47,6 +47,8 @@ gemm_config fixed_config(int dt, const gemm_device_params &d);
 gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &c,
                          const gemm_device_params &d);
 gemm_rank_stats rank_agreement(const double *pred, const double *meas, int n);
+int select_config_set(const double *t, int ns, int nc, int max_set, int32_t *chosen, int32_t *n_chosen,
+                      double *mean_slowdown, double *worst_slowdown);
 const char *reason_text(int reason);
 
 // Errors (capi.cpp)

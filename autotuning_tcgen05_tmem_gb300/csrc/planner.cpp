@@ -393,6 +393,68 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
 }
 
 // ---------------------------------------------------------------------------
+// Shipped configuration set
+// ---------------------------------------------------------------------------
+
+// Greedy choice of a small configuration set from a measured table
+// t[shape * n_configs + config] (<= 0: the configuration does not run the
+// shape).  The set's quality is the sum over shapes of best_s / (the set's
+// fastest time on s), zero where no member runs s; each step adds the
+// configuration with the largest gain (the lowest index among equal gains)
+// until max_set members are chosen or nothing gains.  The quality is monotone
+// and submodular in the set, so the greedy set is within (1 - 1/e) of the best
+// set of its size.
+int select_config_set(const double *t, int ns, int nc, int max_set, int32_t *chosen, int32_t *n_chosen,
+                      double *mean_slowdown, double *worst_slowdown)
+{
+    std::vector<double> best(ns, 0.0), cur(ns, 0.0);
+    for (int s = 0; s < ns; ++s) {
+        double b = 0.0;
+        for (int c = 0; c < nc; ++c) {
+            const double v = t[(size_t)s * nc + c];
+            if (v > 0.0 && (b == 0.0 || v < b)) b = v;
+        }
+        best[s] = b;
+    }
+    auto quality = [&](int s, int c) {
+        const double v = t[(size_t)s * nc + c];
+        return (v > 0.0 && best[s] > 0.0) ? best[s] / v : 0.0;
+    };
+    std::vector<char> used(nc, 0);
+    int k = 0;
+    while (k < max_set) {
+        double best_gain = 0.0;
+        int pick = -1;
+        for (int c = 0; c < nc; ++c) {
+            if (used[c]) continue;
+            double gain = 0.0;
+            for (int s = 0; s < ns; ++s) gain += std::max(0.0, quality(s, c) - cur[s]);
+            if (gain > best_gain) {
+                best_gain = gain;
+                pick = c;
+            }
+        }
+        if (pick < 0) break;
+        used[pick] = 1;
+        chosen[k++] = pick;
+        for (int s = 0; s < ns; ++s) cur[s] = std::max(cur[s], quality(s, pick));
+    }
+    *n_chosen = k;
+    double sum = 0.0, worst = 0.0;
+    int counted = 0;
+    for (int s = 0; s < ns; ++s) {
+        if (best[s] <= 0.0) continue;
+        const double slow = cur[s] > 0.0 ? 1.0 / cur[s] : HUGE_VAL;
+        sum += slow;
+        worst = std::max(worst, slow);
+        ++counted;
+    }
+    if (mean_slowdown) *mean_slowdown = counted ? sum / counted : 1.0;
+    if (worst_slowdown) *worst_slowdown = counted ? worst : 1.0;
+    return GEMM_OK;
+}
+
+// ---------------------------------------------------------------------------
 // Rank agreement
 // ---------------------------------------------------------------------------
 

@@ -569,7 +569,8 @@ static int env_int(const char *name, int dflt)
 }
 
 int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, uint64_t seed,
-         std::vector<gemm_tune_row> &rows, gemm_rank_stats &stats, gemm_config *winner)
+         std::vector<gemm_tune_row> &rows, gemm_rank_stats &stats, gemm_config *winner,
+         const gemm_config *list, int nlist)
 {
     const auto t_start = std::chrono::steady_clock::now();
     memset(&stats, 0, sizeof(stats));
@@ -581,7 +582,23 @@ int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, u
     if ((rc = check_device_arch(nullptr))) return rc;
     gemm_device_params dev;
     if ((rc = query_params(&dev))) return rc;
-    std::vector<gemm_config> cands = enumerate(M, N, K, dt, epi, dev);
+    // Candidates: the generator's, or the feasible members of a given list (a
+    // shipped configuration set), every one of which is timed.
+    std::vector<gemm_config> cands;
+    if (list) {
+        for (int i = 0; i < nlist; ++i) {
+            if (check_config(M, N, K, dt, epi, list[i], dev) != GEMM_FEASIBLE) continue;
+            bool dup = false;
+            for (const gemm_config &c : cands) dup = dup || memcmp(&c, &list[i], sizeof(c)) == 0;
+            if (!dup) cands.push_back(list[i]);
+        }
+        if (cands.empty())
+            return set_error(GEMM_ERR_UNSUPPORTED, "no configuration of the list runs M=%lld N=%lld K=%lld",
+                             (long long)M, (long long)N, (long long)K);
+        mode = GEMM_SEARCH_EXHAUSTIVE;
+    } else {
+        cands = enumerate(M, N, K, dt, epi, dev);
+    }
     if (cands.empty()) {
         const int reason = check_config(M, N, K, dt, epi, fixed_config(dt, dev), dev);
         if (reason == GEMM_REASON_ALIGN) return set_error(GEMM_ERR_MISALIGNED, "%s", reason_text(reason));
@@ -924,7 +941,7 @@ int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *ou
     std::vector<gemm_tune_row> rows;
     gemm_rank_stats stats;
     rc = tune(M, N, K, dt, epi, exhaustive ? GEMM_SEARCH_EXHAUSTIVE : GEMM_SEARCH_MODEL_TOPK, topk, 0, rows, stats,
-              &cfg);
+              &cfg, nullptr, 0);
     if (rc) return rc;
     {
         std::lock_guard<std::mutex> lk(g_cache_mu);
@@ -938,6 +955,52 @@ int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *ou
         }
     }
     return make_plan(M, N, K, dt, epi, cfg, dev, nullptr, out);
+}
+
+// Plans by timing only the members of a given configuration list (no cache).
+int plan_from_list(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config *list, int nlist,
+                   gemm_plan_t *out)
+{
+    *out = nullptr;
+    int rc = check_device_arch(nullptr);
+    if (rc) return rc;
+    gemm_device_params dev;
+    if ((rc = query_params(&dev))) return rc;
+    std::vector<gemm_tune_row> rows;
+    gemm_rank_stats stats;
+    gemm_config cfg;
+    if (M == 0 || N == 0 || K == 0) {
+        // Nothing to time: the first member that the rules accept.
+        for (int i = 0; i < nlist; ++i)
+            if (check_config(M, N, K, dt, epi, list[i], dev) == GEMM_FEASIBLE)
+                return make_plan(M, N, K, dt, epi, list[i], dev, nullptr, out);
+        return set_error(GEMM_ERR_UNSUPPORTED, "no configuration of the list runs this shape");
+    }
+    rc = tune(M, N, K, dt, epi, GEMM_SEARCH_EXHAUSTIVE, 0, 0, rows, stats, &cfg, list, nlist);
+    if (rc) return rc;
+    return make_plan(M, N, K, dt, epi, cfg, dev, nullptr, out);
+}
+
+void cache_stats(int64_t *tunes, int64_t *hits, int64_t *entries);
+
+// Ahead-of-time tuning of a list of shapes into the cache (and the file).
+int tune_batch(const int64_t *mnk, int n, int dt, int epi, const char *path, int32_t *n_tuned)
+{
+    int64_t before = 0, after = 0;
+    cache_stats(&before, nullptr, nullptr);
+    for (int i = 0; i < n; ++i) {
+        gemm_plan_t p = nullptr;
+        const int rc = plan_tuned(mnk[3 * i], mnk[3 * i + 1], mnk[3 * i + 2], dt, epi, &p);
+        if (rc) return rc;
+        destroy_plan(p);
+    }
+    cache_stats(&after, nullptr, nullptr);
+    if (n_tuned) *n_tuned = (int32_t)(after - before);
+    if (path) {
+        int64_t written = 0;
+        return cache_save(path, &written);
+    }
+    return GEMM_OK;
 }
 
 void cache_stats(int64_t *tunes, int64_t *hits, int64_t *entries)

@@ -380,10 +380,13 @@ def search_quality(args):
     budgets = [1, 2, 4, 8, 16, 24, 32]
     names = ["bf16_gelu_1000x1000x8192", "bf16_relu_8192", "bf16_decode_16x8192x28672", "fp32_relu_256"] + \
         [w.name for w in inputs.SWEEP]
+    tables = {}
     for name in names:
         w = inputs.WORKLOADS[name]
         r = g.tune_search(w.M, w.N, w.K, w.dtype, w.epi, g.SEARCH_EXHAUSTIVE, 0)
         rows = [row for row in r.rows if row.measured_us > 0]
+        if w.dtype == "bf16":
+            tables[name] = {row.config.astuple(): row.measured_us for row in rows}
         meas = [row.measured_us for row in rows]
         best = min(meas)
         by_model = sorted(rows, key=lambda row: row.model_rank)
@@ -393,7 +396,38 @@ def search_quality(args):
                           "kendall_tau": r.stats.kendall_tau, "model_quality": model_q,
                           "random_quality_expected": random_q, "search_seconds": r.stats.tune_seconds}),
               flush=True)
+    print(json.dumps({"shipped_set": shipped_set_report(tables)}), flush=True)
     return 0
+
+
+def shipped_set_report(tables, sizes=(4, 8, 16, 30)):
+    """Quality of a small shipped configuration set chosen greedily from the
+    exhaustive tables (gemm_select_config_set): in sample, and leave-one-out
+    (chosen without a workload, judged on it)."""
+    import numpy as np
+    import autotuning_tcgen05_tmem_gb300 as g
+    names = sorted(tables)
+    cols = sorted({c for t in tables.values() for c in t})
+    idx = {c: j for j, c in enumerate(cols)}
+    mat = np.zeros((len(names), len(cols)))
+    for i, n in enumerate(names):
+        for c, us in tables[n].items():
+            mat[i, idx[c]] = us
+    out = {"workloads": len(names), "configurations": len(cols)}
+    for k in sizes:
+        chosen, mean, worst = g.select_config_set(mat, k)
+        loo = []
+        for i in range(len(names)):
+            rest = np.delete(mat, i, axis=0)
+            pick, _, _ = g.select_config_set(rest, k)
+            runs = [mat[i, j] for j in pick if mat[i, j] > 0]
+            best = mat[i][mat[i] > 0].min()
+            loo.append(min(runs) / best if runs else float("inf"))
+        fin = lambda v: v if math.isfinite(v) else None   # null: some workload no member runs
+        out[str(k)] = {"in_sample_mean": fin(mean), "in_sample_worst": fin(worst),
+                       "leave_one_out_mean": fin(float(np.mean(loo))), "leave_one_out_worst": fin(float(np.max(loo))),
+                       "configs": [list(cols[j]) for j in chosen]}
+    return out
 
 
 def main():

@@ -340,6 +340,34 @@ void gemm_cache_clear(void);
 int gemm_cache_save(const char *path, int64_t *n_written);
 int gemm_cache_load(const char *path, int64_t *n_loaded);
 
+/* Shipped configuration set ("Tile Selection": a kernel ships a short list of
+ * configurations; "Autotuning & cost models": tune ahead of time, not per
+ * call).  From a measured table times[s * n_configs + c] (microseconds; <= 0
+ * where configuration c does not run shape s), picks at most max_set
+ * configurations greedily: each step adds the one that most raises the sum
+ * over shapes of (shape's best time) / (fastest chosen time), the lowest
+ * index among equal gains, and stops early when nothing gains.  That sum is
+ * monotone and submodular, so the set is within (1 - 1/e) of the best set of
+ * its size.  Writes the chosen column indices in order and the mean and worst
+ * slowdown (chosen / best; +inf for a shape no chosen configuration runs).
+ * Host only. */
+int gemm_select_config_set(const double *times, int32_t n_shapes, int32_t n_configs, int32_t max_set,
+                           int32_t *chosen, int32_t *n_chosen, double *mean_slowdown, double *worst_slowdown);
+
+/* Plan by timing only the members of `list` (n configurations) that the
+ * rules accept for this shape, on library-owned buffers; the fastest wins.
+ * The cache is neither read nor written.  GEMM_ERR_UNSUPPORTED if no member
+ * runs the shape. */
+int gemm_plan_from_list(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
+                        const gemm_config *list, int32_t n, gemm_plan_t *out);
+
+/* Ahead-of-time tuning: gemm_plan for each of the n shapes mnk[3i..3i+2]
+ * (M, N, K), so that every one is in the cache; then, if db_path is not NULL,
+ * gemm_cache_save(db_path).  *n_tuned (nullable) = shapes newly tuned (the
+ * others were cached already). */
+int gemm_tune_batch(const int64_t *mnk, int32_t n, gemm_dtype dtype, gemm_epilogue epi, const char *db_path,
+                    int32_t *n_tuned);
+
 /* Debug controls.  what = 0: wait limit in nanoseconds (default 2e9; every
  * mbarrier wait in the kernel gives up after it, sets the status word and
  * returns); what = 1: make the epilogue wait on a barrier that nothing signals

@@ -599,3 +599,69 @@ def rank_agreement(predicted, measured):
             "spearman_rho": spearman_rho(predicted, measured),
             "top1_hit": int(measured[pick] == measured[best]),
             "regret": measured[pick] / measured[best] - 1.0}
+
+
+# ---------------------------------------------------------------------------
+# Shipped configuration set ("Tile Selection": a small list of configurations
+# per kernel; "Autotuning & cost models": tune ahead of time)
+# ---------------------------------------------------------------------------
+
+def shipped_set_value(times, chosen):
+    """Sum over shapes of best / (fastest chosen time); 0 for a shape that no
+    chosen configuration runs (times <= 0 mean "does not run")."""
+    total = 0.0
+    for row in times:
+        runs = [v for v in row if v > 0]
+        if not runs:
+            continue
+        best = min(runs)
+        got = [row[c] for c in chosen if row[c] > 0]
+        total += best / min(got) if got else 0.0
+    return total
+
+
+def shipped_set_greedy(times, max_set):
+    """Adds, one at a time, the configuration that most raises the value (the
+    lowest column among equal gains); stops at max_set or when nothing gains.
+    Returns (chosen, mean slowdown, worst slowdown) over shapes that some
+    configuration runs."""
+    n_shapes = len(times)
+    n_cfg = len(times[0]) if n_shapes else 0
+    best = []
+    for row in times:
+        runs = [v for v in row if v > 0]
+        best.append(min(runs) if runs else 0.0)
+    covered = [0.0] * n_shapes          # current best / fastest-chosen per shape
+    chosen = []
+    while len(chosen) < min(max_set, n_cfg):
+        pick, pick_gain = None, 0.0
+        for c in range(n_cfg):
+            if c in chosen:
+                continue
+            gain = 0.0
+            for s in range(n_shapes):
+                q = best[s] / times[s][c] if (times[s][c] > 0 and best[s] > 0) else 0.0
+                gain += max(0.0, q - covered[s])
+            if gain > pick_gain:
+                pick, pick_gain = c, gain
+        if pick is None:
+            break
+        chosen.append(pick)
+        for s in range(n_shapes):
+            q = best[s] / times[s][pick] if (times[s][pick] > 0 and best[s] > 0) else 0.0
+            covered[s] = max(covered[s], q)
+    slow = [1.0 / covered[s] if covered[s] > 0 else math.inf for s in range(n_shapes) if best[s] > 0]
+    mean = sum(slow) / len(slow) if slow else 1.0
+    worst = max(slow) if slow else 1.0
+    return chosen, mean, worst
+
+
+def shipped_set_optimal(times, size):
+    """Brute force over every set of `size` columns: the largest value."""
+    n_cfg = len(times[0]) if times else 0
+    best_v, best_set = -1.0, ()
+    for subset in itertools.combinations(range(n_cfg), min(size, n_cfg)):
+        v = shipped_set_value(times, subset)
+        if v > best_v:
+            best_v, best_set = v, subset
+    return list(best_set), best_v

@@ -63,3 +63,16 @@ def test_expected_random_best_closed_form_against_enumeration():
         subsets = list(itertools.combinations(vals, k))
         brute = sum(min(vals) / min(s) for s in subsets) / len(subsets)
         assert bench.expected_random_best(vals, k) == pytest.approx(brute, rel=1e-12)
+
+
+def test_shipped_set_report_on_a_small_table():
+    sys.path.insert(0, ROOT)
+    import bench
+    c = [(128, 128, 64, 4, 0, 1, 1, 1, 0), (256, 256, 64, 3, 0, 1, 1, 1, 0), (256, 128, 64, 4, 0, 1, 1, 2, 0)]
+    tables = {"a": {c[0]: 10.0, c[1]: 20.0}, "b": {c[0]: 30.0, c[1]: 15.0, c[2]: 14.0}, "c": {c[2]: 5.0}}
+    r = bench.shipped_set_report(tables, sizes=(1, 3))
+    assert r["workloads"] == 3 and r["configurations"] == 3
+    assert r["1"]["in_sample_worst"] is None            # one member cannot run every workload
+    assert r["3"]["in_sample_mean"] == 1.0 and r["3"]["in_sample_worst"] == 1.0
+    # c2 first (gain 2), then c0 (gain 1 on "a"); c1 then gains nothing, so the set stops at two
+    assert [tuple(x) for x in r["3"]["configs"]] == [c[2], c[0]]

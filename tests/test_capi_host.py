@@ -7,6 +7,7 @@ import os
 import random
 import re
 
+import numpy as np
 import pytest
 
 import autotuning_tcgen05_tmem_gb300 as g
@@ -214,3 +215,17 @@ def test_tuning_database_round_trip(tmp_path):
     assert g.cache_stats()["entries"] == 0
     with pytest.raises(g.GemmError):
         g.cache_load(str(tmp_path / "missing.txt"))
+
+
+def test_shipped_set_selection_equals_oracle():
+    rng = np.random.default_rng(11)
+    for trial in range(40):
+        ns, nc = int(rng.integers(1, 9)), int(rng.integers(1, 12))
+        t = rng.uniform(1, 50, size=(ns, nc))
+        t[rng.uniform(size=(ns, nc)) < 0.25] = 0.0
+        for k in (1, 2, 3, 5, 12):
+            got = g.select_config_set(t, k)
+            want = sel.shipped_set_greedy(t.tolist(), k)
+            assert got[0] == want[0]
+            assert got[1] == pytest.approx(want[1], rel=1e-12) and got[2] == pytest.approx(want[2], rel=1e-12)
+    assert g.lib().gemm_select_config_set(None, 2, 2, 1, None, None, None, None) == g.ERR_INVALID_ARG

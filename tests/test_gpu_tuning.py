@@ -177,3 +177,41 @@ def test_search_strategies_measure_their_budget():
     assert top.stats.n_measured in (8, 9)                # + the fixed tile when it is not in the top 8
     measured = [r for r in top.rows if r.measured_us > 0]
     assert sorted(r.model_rank for r in measured)[:8] == list(range(8))
+
+
+def test_plan_from_list_times_only_the_list_and_picks_its_fastest():
+    w = inputs.WORKLOADS["bf16_gelu_out_t512"]
+    C = g.make_config
+    shipped = [C(128, 128, 64, 4), C(256, 128, 128, 4, 0, 1, 1, 2), C(128, 64, 64, 6), C(256, 256, 64, 6, 0, 1, 1, 2),
+               C(256, 256, 64, 12)]                            # the last breaks the shared-memory rule
+    before = g.cache_stats()
+    with g.plan_from_list(w.M, w.N, w.K, w.dtype, w.epi, shipped) as p:
+        chosen = p.config.astuple()
+    assert g.cache_stats() == before                        # the cache is neither read nor written
+    feasible = shipped[:4]
+    assert chosen in [c.astuple() for c in feasible]
+    for attempt in range(2):
+        t = _time_configs(w, feasible)
+        mine = t[[c.astuple() for c in feasible].index(chosen)]
+        if mine <= 1.03 * min(t):
+            break
+    assert mine <= 1.03 * min(t), (chosen, t)
+    with pytest.raises(g.GemmError) as e:
+        g.plan_from_list(w.M, w.N, w.K, w.dtype, w.epi, [C(256, 256, 64, 12)])
+    assert e.value.code == g.ERR_UNSUPPORTED
+
+
+def test_tune_batch_fills_the_cache_and_the_database(tmp_path):
+    g.cache_clear()
+    db = tmp_path / "aot.db"
+    shapes = [(256, 512, 1024), (384, 512, 1024), (512, 1024, 2048)]
+    assert g.tune_batch(shapes, "bf16", "relu", str(db)) == 3
+    assert g.cache_stats()["entries"] == 3
+    assert g.tune_batch(shapes, "bf16", "relu") == 0         # all cached now
+    lines = [l for l in db.read_text().splitlines() if "\t" in l]
+    assert len(lines) == 3
+    g.cache_clear()
+    assert g.cache_load(str(db)) == 3
+    for M, N, K in shapes:
+        g.plan(M, N, K, "bf16", "relu").close()
+    assert g.cache_stats()["tunes"] == 0

@@ -5,6 +5,7 @@ import itertools
 import math
 import random
 
+import numpy as np
 import pytest
 
 from oracle import selection as sel
@@ -262,3 +263,40 @@ def test_gb300_model_terms_behave():
     e = sel.gb300_model(1000, 1000, 8192, 0, 3, sel.Config(128, 256, 64, 4, split_k=8), dev)
     f = sel.gb300_model(1000, 1000, 8192, 0, 3, sel.Config(128, 256, 64, 4, split_k=4), dev)
     assert e["units"] > dev.sm_count >= f["units"] and e["splitk_us"] > 4 * f["splitk_us"]
+
+
+def test_shipped_set_hand_example():
+    # best per shape: 10 (c0), 25 (c1), 4.5 (c2).  Step 1 gains: c0 1+25/30+4.5/5,
+    # c1 10/12+1+4.5/9, c2 25/40+1, c3 10/20+4.5/6 -> c0.  Step 2: c1 gains
+    # 1-25/30, c2 gains 1-4.5/5 -> c1.  Slowdowns 1, 1, 5/4.5.
+    t = [[10, 12, 0, 20], [30, 25, 40, 0], [5, 9, 4.5, 6]]
+    chosen, mean, worst = sel.shipped_set_greedy(t, 2)
+    assert chosen == [0, 1]
+    assert mean == pytest.approx((1 + 1 + 5 / 4.5) / 3, rel=1e-15)
+    assert worst == pytest.approx(5 / 4.5, rel=1e-15)
+    assert sel.shipped_set_greedy(t, 4)[0] == [0, 1, 2]      # c3 adds nothing
+    assert sel.shipped_set_optimal(t, 2) == ([0, 1], pytest.approx(1 + 1 + 4.5 / 5))
+
+
+def test_shipped_set_greedy_is_within_the_submodular_bound_of_the_optimum():
+    rng = np.random.default_rng(5)
+    bound = 1 - 1 / math.e
+    for trial in range(60):
+        ns, nc = rng.integers(2, 7), rng.integers(3, 8)
+        t = rng.uniform(1, 10, size=(ns, nc))
+        t[rng.uniform(size=(ns, nc)) < 0.2] = 0.0
+        for size in range(1, min(4, nc) + 1):
+            chosen, _, _ = sel.shipped_set_greedy(t.tolist(), size)
+            _, opt = sel.shipped_set_optimal(t.tolist(), size)
+            got = sel.shipped_set_value(t.tolist(), chosen)
+            assert got >= bound * opt - 1e-12
+            assert got <= opt + 1e-12
+        # enough members to hold every shape's best: slowdown 1 everywhere
+        full, mean, worst = sel.shipped_set_greedy(t.tolist(), nc)
+        if all((row > 0).any() for row in t):
+            assert mean == pytest.approx(1.0) and worst == pytest.approx(1.0)
+
+
+def test_shipped_set_single_shape_picks_its_fastest_configuration():
+    t = [[7.0, 3.0, 0.0, 5.0]]
+    assert sel.shipped_set_greedy(t, 1) == ([1], 1.0, 1.0)
