@@ -20,7 +20,10 @@ from . import _build
 
 BF16, FP32_TF32 = 0, 1
 EPI_NONE, EPI_BIAS, EPI_BIAS_RELU, EPI_BIAS_GELU = 0, 1, 2, 3
-EPILOGUES = {"none": EPI_NONE, "bias": EPI_BIAS, "relu": EPI_BIAS_RELU, "gelu": EPI_BIAS_GELU}
+EPI_BIAS_RESIDUAL, EPI_BIAS_RELU_RESIDUAL, EPI_BIAS_GELU_RESIDUAL = 4, 5, 6
+EPILOGUES = {"none": EPI_NONE, "bias": EPI_BIAS, "relu": EPI_BIAS_RELU, "gelu": EPI_BIAS_GELU,
+             "bias_residual": EPI_BIAS_RESIDUAL, "relu_residual": EPI_BIAS_RELU_RESIDUAL,
+             "gelu_residual": EPI_BIAS_GELU_RESIDUAL}
 DTYPES = {"bf16": BF16, "fp32": FP32_TF32, "tf32": FP32_TF32}
 
 OK = 0
@@ -42,7 +45,7 @@ EXPORTS = ["gemm_version", "gemm_last_error", "gemm_device_params_default",
            "gemm_plan_status", "gemm_plan_destroy", "gemm_tune", "gemm_cache_stats",
            "gemm_cache_clear", "gemm_debug_set", "gemm_run_noalloc", "gemm_tune_search",
            "gemm_cache_save", "gemm_cache_load", "gemm_plan_launch_info", "gemm_select_config_set",
-           "gemm_plan_from_list", "gemm_tune_batch"]
+           "gemm_plan_from_list", "gemm_tune_batch", "gemm_run_ex"]
 
 
 class GemmError(RuntimeError):
@@ -154,6 +157,7 @@ def _load_library(path: str):
                                                  P(vp)]),
         "gemm_plan_config": (ctypes.c_int, [vp, P(Config)]),
         "gemm_run": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
+        "gemm_run_ex": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp]),
         "gemm_run_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "gemm_plan_status": (ctypes.c_int, [vp]),
         "gemm_plan_launch_info": (ctypes.c_int, [vp, P(LaunchInfo)]),
@@ -326,6 +330,10 @@ class Plan:
 
     def run(self, A, B, bias, C, stream=None) -> None:
         _check(lib().gemm_run(self._h, _ptr(A), _ptr(B), _ptr(bias), _ptr(C), _stream_handle(stream)))
+
+    def run_ex(self, A, B, bias, R, C, stream=None) -> None:
+        """C = act(A·B + bias) + R for the residual epilogues (R may be C)."""
+        _check(lib().gemm_run_ex(self._h, _ptr(A), _ptr(B), _ptr(bias), _ptr(R), _ptr(C), _stream_handle(stream)))
 
     def run_rc(self, A, B, bias, C, stream=None) -> int:
         return lib().gemm_run(self._h, _ptr(A), _ptr(B), _ptr(bias), _ptr(C), _stream_handle(stream))

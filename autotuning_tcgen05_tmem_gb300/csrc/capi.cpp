@@ -38,6 +38,8 @@ int query_params(gemm_device_params *d);
 int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out);
 int plan_explicit(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &cfg, gemm_plan_t *out);
 int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream);
+int run_plan_ex(gemm_plan_t p, const void *A, const void *B, const void *bias, const void *R, void *C,
+                cudaStream_t stream);
 int run_host(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream);
 int plan_status(gemm_plan_t p);
 int plan_config(gemm_plan_t p, gemm_config *out);
@@ -183,6 +185,12 @@ int gemm_plan_launch_info(gemm_plan_t plan, gemm_launch_info *out)
 int gemm_run(gemm_plan_t plan, const void *A, const void *B, const void *bias, void *C, gemm_stream_t stream)
 {
     return run_plan(plan, A, B, bias, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gemm_run_ex(gemm_plan_t plan, const void *A, const void *B, const void *bias, const void *R, void *C,
+                gemm_stream_t stream)
+{
+    return run_plan_ex(plan, A, B, bias, R, C, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gemm_run_host(gemm_plan_t plan, const void *A, const void *B, const void *bias, void *C, gemm_stream_t stream)

@@ -587,6 +587,68 @@ __device__ __forceinline__ void bias_act_cols(float (&v)[16], float row_bias, in
     }
 }
 
+// Residual: R is the caller's [M, N] row-major tensor of C's type (it may be C
+// itself: each element is read once, before its own store).  Unswapped, a
+// thread holds 32 columns n0.. of row m; swapped, 16 rows m0.. of column n.
+template <int DT>
+__device__ __forceinline__ void add_residual_rows(float (&v)[32], const void *R, int64_t ld, int32_t m, int32_t n0,
+                                                  int32_t M, int32_t N)
+{
+    if (m >= M) return;
+    if constexpr (DT == 0) {
+        const uint16_t *row = static_cast<const uint16_t *>(R) + (size_t)m * (size_t)ld + n0;
+        if (n0 + 32 <= N) {
+            const uint4 *p4 = reinterpret_cast<const uint4 *>(row);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 q = p4[i];
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    v[8 * i + 2 * k] += __uint_as_float(w[k] << 16);
+                    v[8 * i + 2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (n0 + j < N) v[j] += __uint_as_float((uint32_t)row[j] << 16);
+        }
+    } else {
+        const float *row = static_cast<const float *>(R) + (size_t)m * (size_t)ld + n0;
+        if (n0 + 32 <= N) {
+            const float4 *p4 = reinterpret_cast<const float4 *>(row);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 q = p4[i];
+                v[4 * i] += q.x;
+                v[4 * i + 1] += q.y;
+                v[4 * i + 2] += q.z;
+                v[4 * i + 3] += q.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (n0 + j < N) v[j] += row[j];
+        }
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void add_residual_cols(float (&v)[16], const void *R, int64_t ld, int32_t m0, int32_t n,
+                                                  int32_t M, int32_t N)
+{
+    if (n >= N) return;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if (m0 + j < M) {
+            const size_t at = (size_t)(m0 + j) * (size_t)ld + n;
+            if constexpr (DT == 0) v[j] += __uint_as_float((uint32_t)static_cast<const uint16_t *>(R)[at] << 16);
+            else v[j] += static_cast<const float *>(R)[at];
+        }
+    }
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16)
 {
     return __uint_as_float(bits16 << 16);
@@ -967,6 +1029,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // accumulator is ready, so that load overlaps the main loop.
         // ------------------------------------------------------------------
         const int32_t e_bn = p.bn, e_bm = p.bm, e_epi = p.epi, e_cols = p.cols, e_rows = p.rows;
+        const void *const e_resid = p.residual;   // C = act(A·B + bias) + R when set
+        const bool e_res = e_resid != nullptr;
         const int32_t e_split_k = p.split_k, e_swap_ab = p.swap_ab;
         const bool e_coop = p.coop_fixup != 0;
         const bool e_cluster = p.cluster_k > 1;
@@ -1109,6 +1173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         bias_act_rows(v, bcol[ci], e_epi);
                         const int32_t n = c0 + c * 32, y = r0 + h * 128 + q * 32;
+                        if (e_res) add_residual_rows<DT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
                         store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                     }
                 }
@@ -1218,6 +1283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         bias_act_rows(v, bcol[ci], e_epi);
                         const int32_t n = c0 + c * 32, y = r0 + rg * 32;
+                        if (e_res) add_residual_rows<DT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
                         store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                     }
                 }
@@ -1259,6 +1325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else {
                             bias_act_rows(v, bcol[ci], e_epi);
                             const int32_t n = c0 + c * 32, y = r0 + h * 128 + q * 32;
+                            if (e_res) add_residual_rows<DT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
                             store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                         }
                     }
@@ -1280,6 +1347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             bias_act_cols(v, h == 0 ? brow[0] : brow[1], e_epi);
                             const int32_t xn = r0 + h * 128 + q * 32;  // output column block (user N)
                             const int32_t ym = c0 + c * 16;            // output row block (user M)
+                            if (e_res) add_residual_cols<DT>(v, e_resid, e_rows, ym, xn + lane, e_cols, e_rows);
                             store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
                         }
                     }
@@ -1346,6 +1414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             bias_act_rows(v, lb, e_epi);
                             const int32_t n = c0 + c * 32, y = r0 + rg * 32;
+                            if (e_res) add_residual_rows<DT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
                             store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                         } else {
                             float v[16];
@@ -1376,6 +1445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             bias_act_cols(v, rb, e_epi);
                             const int32_t xn = r0 + rg * 32, ym = c0 + c * 16;
+                            if (e_res) add_residual_cols<DT>(v, e_resid, e_rows, ym, xn + lane, e_cols, e_rows);
                             store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
                         }
                     }

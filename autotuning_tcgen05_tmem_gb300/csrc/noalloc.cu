@@ -144,6 +144,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_epilogue e
     if (reason == GEMM_REASON_ALIGN)
         return set_error(GEMM_ERR_MISALIGNED, "K=%lld / N=%lld: %s", (long long)K, (long long)N, reason_text(reason));
     if (reason != GEMM_FEASIBLE) return set_error(GEMM_ERR_INFEASIBLE, "config rejected: %s", reason_text(reason));
+    if (c.cta_group != 1)
+        return set_error(GEMM_ERR_UNSUPPORTED, "gemm_run_noalloc runs single-CTA tiles only (cta_group 1)");
     if (M == 0 || N == 0) return GEMM_OK;
     const int64_t rows = c.swap_ab ? N : M, cols = c.swap_ab ? M : N;
     const int64_t tiles_m = cdiv(rows, c.bm), tiles_n = cdiv(cols, c.bn), tiles = tiles_m * tiles_n;

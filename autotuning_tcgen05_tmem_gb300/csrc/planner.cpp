@@ -335,7 +335,9 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
     const double panel = ((double)tiles / (double)wave_tiles) * (double)K *
                          ((double)rows_w * c.bm + (double)cols_w * c.bn) * e;
     const double operand = (in_bytes <= (double)d.l2_bytes / 2.0) ? in_bytes : std::max(in_bytes, panel);
-    const double hbm = operand + (double)M * N * e + (epi != GEMM_EPI_NONE ? (double)N * e : 0.0);
+    // C, bias, and the residual R of the "+ R" epilogues.
+    const double hbm = operand + (double)M * N * e + (epi != GEMM_EPI_NONE ? (double)N * e : 0.0) +
+                       (epi >= GEMM_EPI_BIAS_RESIDUAL ? (double)M * N * e : 0.0);
     const double t_hbm = hbm / (d.hbm_gbs * 1e9);
 
     // Bytes in flight ("Tiling the hierarchy", double buffering): the ring
@@ -344,7 +346,8 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
     const double t_main = std::max(std::max(t_mma, t_l2), std::max(t_hbm, t_lat));
 
     // Epilogue and split-K exchange.
-    const double rate = (epi == GEMM_EPI_BIAS_GELU ? d.epi_gelu_elems_per_clk : d.epi_elems_per_clk) * clk;
+    const bool gelu = epi == GEMM_EPI_BIAS_GELU || epi == GEMM_EPI_BIAS_GELU_RESIDUAL;
+    const double rate = (gelu ? d.epi_gelu_elems_per_clk : d.epi_elems_per_clk) * clk;
     const double elems = (double)rows_cta * c.bn;   // one CTA's share of a tile
     const double part = elems * 4.0;
     double exposed, t_split;

@@ -189,8 +189,12 @@ static int configure_smem_limit(int dt, int64_t bytes)
 
 static bool valid_enums(int dt, int epi)
 {
-    return (dt == GEMM_BF16 || dt == GEMM_FP32_TF32) && epi >= GEMM_EPI_NONE && epi <= GEMM_EPI_BIAS_GELU;
+    return (dt == GEMM_BF16 || dt == GEMM_FP32_TF32) && epi >= GEMM_EPI_NONE && epi <= GEMM_EPI_BIAS_GELU_RESIDUAL;
 }
+
+// Residual epilogues are the bias / ReLU / GELU ones followed by "+ R".
+static bool has_residual(int epi) { return epi >= GEMM_EPI_BIAS_RESIDUAL; }
+static int act_code(int epi) { return has_residual(epi) ? epi - 3 : epi; }
 
 static int check_extents(int64_t M, int64_t N, int64_t K)
 {
@@ -247,7 +251,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     p->tiles = (int64_t)k.tiles_m * k.tiles_n;
     k.num_units = (int32_t)(p->tiles * cfg.split_k);
     k.swap_ab = cfg.swap_ab;
-    k.epi = epi;
+    k.epi = act_code(epi);   // the kernel's bias/activation code; the residual is a run argument
     const int route = g_b_route.load();
     p->b_kmajor = route == 1 || (route == 0 && dt == GEMM_FP32_TF32);
     // User B is N-contiguous (MN-major) unless it is first transposed.  It is
@@ -440,15 +444,20 @@ static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream)
+int run_plan_ex(gemm_plan_t p, const void *A, const void *B, const void *bias, const void *R, void *C,
+                cudaStream_t stream)
 {
     if (!p) return set_error(GEMM_ERR_INVALID_ARG, "null plan");
+    if (has_residual(p->epi) && !R)
+        return set_error(GEMM_ERR_INVALID_ARG, "the residual epilogue needs R (gemm_run_ex)");
+    if (!has_residual(p->epi) && R)
+        return set_error(GEMM_ERR_INVALID_ARG, "R given to a plan whose epilogue has no residual");
     if (p->M == 0 || p->N == 0) return GEMM_OK;
     if (!C || (p->K > 0 && (!A || !B))) return set_error(GEMM_ERR_INVALID_ARG, "null A, B or C");
     if (p->epi != GEMM_EPI_NONE && !bias) return set_error(GEMM_ERR_INVALID_ARG, "bias is required by the epilogue");
     if ((p->K > 0 && (!aligned16(A) || !aligned16(B))) || !aligned16(C) ||
-        (p->epi != GEMM_EPI_NONE && !aligned16(bias)))
-        return set_error(GEMM_ERR_MISALIGNED, "A, B, C and bias must be 16-byte aligned");
+        (p->epi != GEMM_EPI_NONE && !aligned16(bias)) || (R && !aligned16(R)))
+        return set_error(GEMM_ERR_MISALIGNED, "A, B, C, bias and R must be 16-byte aligned");
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev != p->device)
@@ -462,11 +471,17 @@ int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void
     }
     KernelParams kp = p->kp;
     kp.bias = p->epi != GEMM_EPI_NONE ? bias : nullptr;
+    kp.residual = R;
     kp.timeout_ns = g_timeout_ns.load();
     kp.debug_stall = g_debug_stall.load();
     cudaError_t e = launch_gemm(p->dt, d->ma, d->mb, d->mc, kp, p->grid, p->smem_request, stream);
     if (e != cudaSuccess) return cuda_err(e, "kernel launch");
     return GEMM_OK;
+}
+
+int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream)
+{
+    return run_plan_ex(p, A, B, bias, nullptr, C, stream);
 }
 
 int plan_launch_info(gemm_plan_t p, gemm_launch_info *out)
@@ -699,9 +714,10 @@ int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, u
     for (int j = 0; j < nm; ++j) {
         status[j] = make_plan(M, N, K, dt, epi, cands[meas[j]], dev, buf.ws, &plans[j]);
     }
+    // (A residual epilogue is timed in place: R = C.)
     auto run_one = [&](int j, int set) {
-        return run_plan(plans[j], buf.A[set], buf.B[set], epi != GEMM_EPI_NONE ? buf.bias[set] : nullptr, buf.C[set],
-                        stream);
+        return run_plan_ex(plans[j], buf.A[set], buf.B[set], epi != GEMM_EPI_NONE ? buf.bias[set] : nullptr,
+                           has_residual(epi) ? buf.C[set] : nullptr, buf.C[set], stream);
     };
     // Warm-up and a first estimate of each candidate's time.
     cudaEvent_t e0, e1;

@@ -92,6 +92,18 @@ def make_operands(M: int, N: int, K: int, dtype: str, dist: str, seed: int = 0,
     return A.to(td).contiguous(), B.to(td).contiguous(), (bias.to(td).contiguous() if with_bias else None)
 
 
+def make_residual(M: int, N: int, dtype: str, dist: str, seed: int = 0, device="cpu"):
+    """R [M, N] for the residual epilogues: small integers for the exact
+    cases, otherwise N(0, 1) (a residual stream's scale)."""
+    dev = torch.device(device)
+    g = _gen(seed + 3, dev)
+    if dist == "int":
+        R = torch.randint(-4, 5, (M, N), generator=g, device=dev).to(torch.float32)
+    else:
+        R = torch.randn(M, N, generator=g, device=dev, dtype=torch.float32)
+    return R.to(torch_dtype(dtype)).contiguous()
+
+
 def make_workload(w: Workload, seed: int = 0, device="cpu"):
     return make_operands(w.M, w.N, w.K, w.dtype, w.dist, seed=seed, device=device,
                          with_bias=(w.epi != "none"))

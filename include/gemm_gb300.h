@@ -73,7 +73,15 @@ typedef enum {
     GEMM_EPI_NONE = 0,       /* C = A·B                 (bias may be NULL) */
     GEMM_EPI_BIAS = 1,       /* C = A·B + bias          */
     GEMM_EPI_BIAS_RELU = 2,  /* C = max(A·B + bias, 0)  */
-    GEMM_EPI_BIAS_GELU = 3   /* C = gelu(A·B + bias)    */
+    GEMM_EPI_BIAS_GELU = 3,  /* C = gelu(A·B + bias)    */
+    /* Residual variants: the same, plus R, an [M, N] row-major tensor of C's
+     * type passed to gemm_run_ex (the transformer block's "x + f(x)").  The
+     * pages name a fused residual add as an epilogue beyond bias and
+     * activation; the order (activation, then + R) is the residual
+     * connection's. */
+    GEMM_EPI_BIAS_RESIDUAL = 4,       /* C = A·B + bias + R          */
+    GEMM_EPI_BIAS_RELU_RESIDUAL = 5,  /* C = max(A·B + bias, 0) + R  */
+    GEMM_EPI_BIAS_GELU_RESIDUAL = 6   /* C = gelu(A·B + bias) + R    */
 } gemm_epilogue;
 
 /*
@@ -293,7 +301,15 @@ int gemm_plan_launch_info(gemm_plan_t plan, gemm_launch_info *out);
 int gemm_run(gemm_plan_t plan, const void *A, const void *B, const void *bias, void *C,
              gemm_stream_t stream);
 
-/* Same product from HOST buffers: copies A, B, bias to plan-owned device
+/* gemm_run with a residual: R is a device pointer to [M, N] row-major of C's
+ * type, 16-byte aligned, read once per element; it may be C itself (in-place
+ * "C += f(A·B + bias)"), and may not overlap C otherwise.  Required (non-NULL)
+ * exactly for the residual epilogues, which gemm_run rejects with
+ * GEMM_ERR_INVALID_ARG.  Asynchronous on `stream`. */
+int gemm_run_ex(gemm_plan_t plan, const void *A, const void *B, const void *bias, const void *R, void *C,
+                gemm_stream_t stream);
+
+/* Same product from HOST buffers (epilogues without residual): copies A, B, bias to plan-owned device
  * buffers, runs, copies C back, and synchronises `stream` before returning.
  * Host buffers should be pinned for full copy bandwidth. */
 int gemm_run_host(gemm_plan_t plan, const void *A, const void *B, const void *bias, void *C,
@@ -401,8 +417,9 @@ int gemm_debug_set(int32_t what, int64_t value);
  * serving.  It allocates nothing, host or device: its scratch (status word,
  * split-K counters and partial tiles) is one fixed array compiled into the
  * library, which every GPU that loads the library holds until the process exits.
- * Arguments are those of gemm_plan_with_config + gemm_run (bf16 only); the call
- * is asynchronous on `stream` and returns after the launch.
+ * Arguments are those of gemm_plan_with_config + gemm_run (bf16 only; epilogues
+ * without residual; single-CTA tiles, cta_group 1, else GEMM_ERR_UNSUPPORTED);
+ * the call is asynchronous on `stream` and returns after the launch.
  *   - The first call on a device sets that device up (looks up the scratch's
  *     device address, reads the device's limits, sets the kernel's shared-memory
  *     limit); make that first call before any stream capture.

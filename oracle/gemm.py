@@ -25,6 +25,8 @@ _SRC = os.path.join(_HERE, "gemm_ref.c")
 _LIB_PATH = os.path.join(_HERE, "_build", "liboracle_gemm.so")
 
 EPI_NONE, EPI_BIAS, EPI_BIAS_RELU, EPI_BIAS_GELU = 0, 1, 2, 3
+# Residual variants: the epilogue above, then + R ([M, N], the residual connection).
+EPI_BIAS_RESIDUAL, EPI_BIAS_RELU_RESIDUAL, EPI_BIAS_GELU_RESIDUAL = 4, 5, 6
 
 _lib = None
 
@@ -87,8 +89,18 @@ def default_threads() -> int:
         return os.cpu_count() or 1
 
 
-def gemm(A, B, bias=None, epi: int = EPI_NONE, threads: int | None = None) -> np.ndarray:
-    """fp64 C = act(A·B + bias) for A [M,K], B [K,N], bias [N] (or None)."""
+def gemm(A, B, bias=None, epi: int = EPI_NONE, threads: int | None = None, residual=None) -> np.ndarray:
+    """fp64 C = act(A·B + bias) for A [M,K], B [K,N], bias [N] (or None); for
+    the residual epilogues (4, 5, 6) C = act(A·B + bias) + R with R [M, N]
+    (its values exactly, in fp64)."""
+    if epi >= EPI_BIAS_RESIDUAL:
+        if residual is None:
+            raise ValueError("the residual epilogue needs R")
+        base = gemm(A, B, bias, epi - 3, threads)
+        R = _as_f32_input(residual).astype(np.float64)
+        if R.shape != base.shape:
+            raise ValueError("R must be [M, N]")
+        return base + R
     lib = _load()
     A = _as_f32_input(A)
     B = _as_f32_input(B)
@@ -113,8 +125,15 @@ def gemm(A, B, bias=None, epi: int = EPI_NONE, threads: int | None = None) -> np
     return C
 
 
-def gemm_entries(A, B, bias, epi: int, rows, cols) -> np.ndarray:
-    """fp64 values of C at the listed (row, col) positions, one dot product each."""
+def gemm_entries(A, B, bias, epi: int, rows, cols, residual=None) -> np.ndarray:
+    """fp64 values of C at the listed (row, col) positions, one dot product each
+    (plus R at those positions for the residual epilogues)."""
+    if epi >= EPI_BIAS_RESIDUAL:
+        if residual is None:
+            raise ValueError("the residual epilogue needs R")
+        base = gemm_entries(A, B, bias, epi - 3, rows, cols)
+        R = _as_f32_input(residual)
+        return base + R[np.asarray(rows), np.asarray(cols)].astype(np.float64)
     lib = _load()
     A = _as_f32_input(A)
     B = _as_f32_input(B)

@@ -215,6 +215,7 @@ def workshop_sweep(M, N, K, dev: WorkshopDevice = WorkshopDevice()):
 
 DT_BF16, DT_FP32 = 0, 1
 EPI_NONE, EPI_BIAS, EPI_RELU, EPI_GELU = 0, 1, 2, 3
+EPI_BIAS_RES, EPI_RELU_RES, EPI_GELU_RES = 4, 5, 6   # the same plus a residual R
 
 R_OK, R_CTA_GROUP, R_UMMA_M, R_UMMA_N, R_LAYOUT, R_BK, R_STAGES, R_SCHEDULE, \
     R_SPLIT_K, R_ALIGN, R_TMEM, R_SMEM, R_REGS = range(13)
@@ -499,13 +500,14 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
         rows_w = min(ceil_div(wave_tiles, cols_w), tiles_m)
     panel = (tiles / wave_tiles) * K * (rows_w * cfg.bm + cols_w * cfg.bn) * elt
     operand = in_bytes if in_bytes <= dev.l2_bytes / 2 else max(in_bytes, panel)
-    hbm = operand + M * N * elt + (N * elt if epi != EPI_NONE else 0)
+    hbm = (operand + M * N * elt + (N * elt if epi != EPI_NONE else 0)
+           + (M * N * elt if epi >= EPI_BIAS_RES else 0))      # C, bias, residual R
     hbm_s = hbm / (dev.hbm_gbs * 1e9)
 
     latency_s = per_cta_units * slice_kb * dev.mem_latency_us * 1e-6 / cfg.stages
     main = max(mma_s, l2_s, hbm_s, latency_s)
 
-    per_clock = dev.epi_gelu_elems_per_clk if epi == EPI_GELU else dev.epi_elems_per_clk
+    per_clock = dev.epi_gelu_elems_per_clk if epi in (EPI_GELU, EPI_GELU_RES) else dev.epi_elems_per_clk
     rate = per_clock * clock
     elems = rows_cta * cfg.bn          # one CTA's share of a tile
     partial = elems * 4
