@@ -7,7 +7,9 @@ inputs from here, so that they see bit-identical values.
 Recipe (per workload; seeds 0, 1, 2 for A, B and bias unless a caller passes
 another base seed): draw in fp32 with torch's CPU generator (or a CUDA
 generator for timing-only buffers), then round once, to bf16 with torch's
-round-to-nearest-even conversion when the workload is bf16.
+round-to-nearest-even conversion when the workload is bf16, or to FP8 E4M3
+(round to nearest even; every value drawn stays inside the format's range)
+when it is fp8, whose bias and C are bf16.
 """
 from __future__ import annotations
 
@@ -16,7 +18,7 @@ from dataclasses import dataclass
 
 import torch
 
-BF16, FP32 = "bf16", "fp32"
+BF16, FP32, FP8 = "bf16", "fp32", "fp8"
 EPI_CODES = {"none": 0, "bias": 1, "relu": 2, "gelu": 3}
 
 
@@ -54,7 +56,15 @@ SWEEP = [WORKLOADS[f"bf16_gelu_{p}_t{t}"] for t in TOKENS for (p, _k, _n) in PRO
 
 
 def torch_dtype(dtype: str):
+    """Operand type: bf16, fp32, or FP8 E4M3."""
+    if dtype == FP8:
+        return torch.float8_e4m3fn
     return torch.bfloat16 if dtype == BF16 else torch.float32
+
+
+def out_torch_dtype(dtype: str):
+    """Type of C, bias and R: FP8 operands produce bf16."""
+    return torch.bfloat16 if dtype in (BF16, FP8) else torch.float32
 
 
 def _gen(seed: int, device):
@@ -89,7 +99,8 @@ def make_operands(M: int, N: int, K: int, dtype: str, dist: str, seed: int = 0,
     else:
         raise ValueError(f"unknown distribution {dist!r}")
     td = torch_dtype(dtype)
-    return A.to(td).contiguous(), B.to(td).contiguous(), (bias.to(td).contiguous() if with_bias else None)
+    tb = out_torch_dtype(dtype)
+    return A.to(td).contiguous(), B.to(td).contiguous(), (bias.to(tb).contiguous() if with_bias else None)
 
 
 def make_residual(M: int, N: int, dtype: str, dist: str, seed: int = 0, device="cpu"):
@@ -101,7 +112,7 @@ def make_residual(M: int, N: int, dtype: str, dist: str, seed: int = 0, device="
         R = torch.randint(-4, 5, (M, N), generator=g, device=dev).to(torch.float32)
     else:
         R = torch.randn(M, N, generator=g, device=dev, dtype=torch.float32)
-    return R.to(torch_dtype(dtype)).contiguous()
+    return R.to(out_torch_dtype(dtype)).contiguous()
 
 
 def make_workload(w: Workload, seed: int = 0, device="cpu"):

@@ -52,10 +52,10 @@ def _load():
         f32p = ctypes.POINTER(ctypes.c_float)
         f64p = ctypes.POINTER(ctypes.c_double)
         i64p = ctypes.POINTER(ctypes.c_int64)
-        lib.oracle_gemm.argtypes = [f32p, f32p, f32p, ctypes.c_int, ctypes.c_int64,
+        lib.oracle_gemm.argtypes = [f32p, f32p, f32p, ctypes.c_int, ctypes.c_double, ctypes.c_int64,
                                     ctypes.c_int64, ctypes.c_int64, f64p, ctypes.c_int]
         lib.oracle_gemm.restype = ctypes.c_int
-        lib.oracle_gemm_entries.argtypes = [f32p, f32p, f32p, ctypes.c_int, ctypes.c_int64,
+        lib.oracle_gemm_entries.argtypes = [f32p, f32p, f32p, ctypes.c_int, ctypes.c_double, ctypes.c_int64,
                                             ctypes.c_int64, ctypes.c_int64, i64p, i64p,
                                             ctypes.c_int64, f64p]
         lib.oracle_gemm_entries.restype = ctypes.c_int
@@ -72,10 +72,15 @@ def _f32(x):
 
 
 def _as_f32_input(x):
-    """Inputs may arrive as float32 arrays or torch tensors of bf16/fp32 (CPU)."""
+    """Inputs may arrive as float32 arrays or torch tensors of bf16/fp32 (CPU),
+    or FP8 E4M3 tensors, whose bytes are decoded here from the format's
+    definition (oracle/fp8.py)."""
     try:
         import torch
         if isinstance(x, torch.Tensor):
+            if x.dtype == getattr(torch, "float8_e4m3fn", None):
+                from . import fp8
+                return fp8.decode_codes(x.detach().cpu().contiguous().view(torch.uint8).numpy())
             return x.detach().to("cpu", torch.float32).contiguous().numpy()
     except ImportError:  # pragma: no cover
         pass
@@ -89,14 +94,15 @@ def default_threads() -> int:
         return os.cpu_count() or 1
 
 
-def gemm(A, B, bias=None, epi: int = EPI_NONE, threads: int | None = None, residual=None) -> np.ndarray:
-    """fp64 C = act(A·B + bias) for A [M,K], B [K,N], bias [N] (or None); for
-    the residual epilogues (4, 5, 6) C = act(A·B + bias) + R with R [M, N]
-    (its values exactly, in fp64)."""
+def gemm(A, B, bias=None, epi: int = EPI_NONE, threads: int | None = None, residual=None,
+         alpha: float = 1.0) -> np.ndarray:
+    """fp64 C = act(alpha·A·B + bias) for A [M,K], B [K,N], bias [N] (or None);
+    for the residual epilogues (4, 5, 6) C = act(alpha·A·B + bias) + R with R
+    [M, N] (its values exactly, in fp64)."""
     if epi >= EPI_BIAS_RESIDUAL:
         if residual is None:
             raise ValueError("the residual epilogue needs R")
-        base = gemm(A, B, bias, epi - 3, threads)
+        base = gemm(A, B, bias, epi - 3, threads, alpha=alpha)
         R = _as_f32_input(residual).astype(np.float64)
         if R.shape != base.shape:
             raise ValueError("R must be [M, N]")
@@ -117,7 +123,7 @@ def gemm(A, B, bias=None, epi: int = EPI_NONE, threads: int | None = None, resid
     else:
         bb, biasp = None, ctypes.POINTER(ctypes.c_float)()
     C = np.empty((M, N), dtype=np.float64)
-    rc = lib.oracle_gemm(ap, bp, biasp, int(epi), M, N, K,
+    rc = lib.oracle_gemm(ap, bp, biasp, int(epi), float(alpha), M, N, K,
                          C.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                          int(threads or default_threads()))
     if rc != 0:
@@ -125,13 +131,13 @@ def gemm(A, B, bias=None, epi: int = EPI_NONE, threads: int | None = None, resid
     return C
 
 
-def gemm_entries(A, B, bias, epi: int, rows, cols, residual=None) -> np.ndarray:
+def gemm_entries(A, B, bias, epi: int, rows, cols, residual=None, alpha: float = 1.0) -> np.ndarray:
     """fp64 values of C at the listed (row, col) positions, one dot product each
     (plus R at those positions for the residual epilogues)."""
     if epi >= EPI_BIAS_RESIDUAL:
         if residual is None:
             raise ValueError("the residual epilogue needs R")
-        base = gemm_entries(A, B, bias, epi - 3, rows, cols)
+        base = gemm_entries(A, B, bias, epi - 3, rows, cols, alpha=alpha)
         R = _as_f32_input(residual)
         return base + R[np.asarray(rows), np.asarray(cols)].astype(np.float64)
     lib = _load()
@@ -148,7 +154,7 @@ def gemm_entries(A, B, bias, epi: int, rows, cols, residual=None) -> np.ndarray:
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     c = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
     out = np.empty(r.shape[0], dtype=np.float64)
-    rc = lib.oracle_gemm_entries(ap, bp, biasp, int(epi), M, N, K,
+    rc = lib.oracle_gemm_entries(ap, bp, biasp, int(epi), float(alpha), M, N, K,
                                  r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                  c.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                  r.shape[0], out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))

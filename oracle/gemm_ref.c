@@ -39,6 +39,7 @@ typedef struct {
     double *C;
     int64_t M, N, K, m_begin, m_end;
     int epi;
+    double alpha;
 } oracle_rows_job;
 
 static void *oracle_rows_worker(void *arg)
@@ -53,15 +54,16 @@ static void *oracle_rows_worker(void *arg)
             for (int64_t n = 0; n < j->N; ++n) crow[n] += a * (double)brow[n];
         }
         for (int64_t n = 0; n < j->N; ++n)
-            crow[n] = oracle_epilogue(crow[n], j->bias ? (double)j->bias[n] : 0.0, j->epi);
+            crow[n] = oracle_epilogue(j->alpha * crow[n], j->bias ? (double)j->bias[n] : 0.0, j->epi);
     }
     return NULL;
 }
 
-/* Full product: C[m*N + n] = act(sum_k A[m*K+k]·B[k*N+n] + bias[n]), rows split
- * into contiguous blocks over `threads` POSIX threads (threads <= 1: caller's
- * thread only).  Returns 0, or -1 on bad arguments. */
-int oracle_gemm(const float *A, const float *B, const float *bias, int epi,
+/* Full product: C[m*N + n] = act(alpha · sum_k A[m*K+k]·B[k*N+n] + bias[n]),
+ * rows split into contiguous blocks over `threads` POSIX threads (threads <= 1:
+ * caller's thread only).  alpha is the product's scale (the tensor scales of
+ * FP8 operands; 1 otherwise).  Returns 0, or -1 on bad arguments. */
+int oracle_gemm(const float *A, const float *B, const float *bias, int epi, double alpha,
                 int64_t M, int64_t N, int64_t K, double *C, int threads)
 {
     if (M < 0 || N < 0 || K < 0 || epi < 0 || epi > 3) return -1;
@@ -74,7 +76,7 @@ int oracle_gemm(const float *A, const float *B, const float *bias, int epi,
     if (!jobs || !tids) { free(jobs); free(tids); return -1; }
     for (int t = 0; t < threads; ++t) {
         jobs[t].A = A; jobs[t].B = B; jobs[t].bias = bias; jobs[t].C = C;
-        jobs[t].M = M; jobs[t].N = N; jobs[t].K = K; jobs[t].epi = epi;
+        jobs[t].M = M; jobs[t].N = N; jobs[t].K = K; jobs[t].epi = epi; jobs[t].alpha = alpha;
         jobs[t].m_begin = (M * t) / threads;
         jobs[t].m_end = (M * (t + 1)) / threads;
     }
@@ -93,7 +95,7 @@ int oracle_gemm(const float *A, const float *B, const float *bias, int epi,
 
 /* Selected entries, one dot product each: out[i] = C[rows[i], cols[i]].  Used to
  * check full-size runs whose whole product would take too long here. */
-int oracle_gemm_entries(const float *A, const float *B, const float *bias, int epi,
+int oracle_gemm_entries(const float *A, const float *B, const float *bias, int epi, double alpha,
                         int64_t M, int64_t N, int64_t K,
                         const int64_t *rows, const int64_t *cols, int64_t count, double *out)
 {
@@ -103,7 +105,7 @@ int oracle_gemm_entries(const float *A, const float *B, const float *bias, int e
         if (m < 0 || m >= M || n < 0 || n >= N) return -1;
         double s = 0.0;
         for (int64_t k = 0; k < K; ++k) s += (double)A[m * K + k] * (double)B[k * N + n];
-        out[i] = oracle_epilogue(s, bias ? (double)bias[n] : 0.0, epi);
+        out[i] = oracle_epilogue(alpha * s, bias ? (double)bias[n] : 0.0, epi);
     }
     return 0;
 }

@@ -184,3 +184,43 @@ def test_planted_mistakes_are_caught():
     assert math.isclose(0.5 * 1.0 * (1 + math.erf(1 / math.sqrt(2))), 0.8413447460685429)
     tanh_gelu = 0.5 * (1 + math.tanh(math.sqrt(2 / math.pi) * (1 + 0.044715)))
     assert abs(tanh_gelu - 0.8413447460685429) > 1e-5
+
+
+def test_e4m3_decode_from_its_definition_matches_torch_for_every_code():
+    import torch
+    from oracle import fp8
+    table = fp8.e4m3_table()
+    # hand values of the format: 1.0, -2.0, the largest finite 448, the smallest
+    # subnormal 2^-9, the largest subnormal 7/8·2^-6, the smallest normal 2^-6
+    assert table[0x38] == 1.0 and table[0xC0] == -2.0 and table[0x7E] == 448.0
+    assert table[0x01] == 2.0 ** -9 and table[0x07] == 7 / 8 * 2.0 ** -6 and table[0x08] == 2.0 ** -6
+    assert np.isnan(table[0x7F]) and np.isnan(table[0xFF]) and table[0x80] == 0.0
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    same = (table == ref) | (np.isnan(table) & np.isnan(ref))
+    assert same.all(), np.nonzero(~same)
+    # 254 finite values, symmetric, strictly increasing over the positive codes
+    pos = table[:0x7F]
+    assert np.all(np.diff(pos) > 0) and np.array_equal(table[0x80:0xFF], -pos)
+
+
+def test_alpha_scales_the_product_before_bias_and_activation():
+    rng = np.random.default_rng(3)
+    A = rng.integers(-3, 4, size=(5, 7)).astype(np.float32)
+    B = rng.integers(-3, 4, size=(7, 6)).astype(np.float32)
+    bias = rng.integers(-2, 3, size=6).astype(np.float32)
+    exact = A.astype(np.float64) @ B.astype(np.float64)
+    for alpha in (1.0, 0.5, -0.25, 3.0):
+        got = og.gemm(A, B, bias, og.EPI_BIAS_RELU, alpha=alpha)
+        assert np.array_equal(got, np.maximum(alpha * exact + bias, 0.0))
+        ent = og.gemm_entries(A, B, bias, og.EPI_BIAS_RELU, [0, 4], [5, 0], alpha=alpha)
+        assert np.array_equal(ent, got[[0, 4], [5, 0]])
+
+
+def test_fp8_operands_reach_the_oracle_as_their_decoded_values():
+    import torch
+    from autotuning_tcgen05_tmem_gb300 import inputs
+    A, B, bias = inputs.make_operands(9, 10, 11, "fp8", "int", seed=1)
+    assert A.dtype == torch.float8_e4m3fn and bias.dtype == torch.bfloat16
+    Af = A.to(torch.float32).numpy().astype(np.float64)
+    Bf = B.to(torch.float32).numpy().astype(np.float64)
+    assert np.array_equal(og.gemm(A, B, None, og.EPI_NONE), Af @ Bf)
