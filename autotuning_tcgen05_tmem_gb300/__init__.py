@@ -18,13 +18,13 @@ from dataclasses import dataclass
 
 from . import _build
 
-BF16, FP32_TF32 = 0, 1
+BF16, FP32_TF32, FP8_E4M3 = 0, 1, 2
 EPI_NONE, EPI_BIAS, EPI_BIAS_RELU, EPI_BIAS_GELU = 0, 1, 2, 3
 EPI_BIAS_RESIDUAL, EPI_BIAS_RELU_RESIDUAL, EPI_BIAS_GELU_RESIDUAL = 4, 5, 6
 EPILOGUES = {"none": EPI_NONE, "bias": EPI_BIAS, "relu": EPI_BIAS_RELU, "gelu": EPI_BIAS_GELU,
              "bias_residual": EPI_BIAS_RESIDUAL, "relu_residual": EPI_BIAS_RELU_RESIDUAL,
              "gelu_residual": EPI_BIAS_GELU_RESIDUAL}
-DTYPES = {"bf16": BF16, "fp32": FP32_TF32, "tf32": FP32_TF32}
+DTYPES = {"bf16": BF16, "fp32": FP32_TF32, "tf32": FP32_TF32, "fp8": FP8_E4M3, "e4m3": FP8_E4M3}
 
 OK = 0
 STATUS_NAMES = {0: "GEMM_OK", -1: "GEMM_ERR_INVALID_ARG", -2: "GEMM_ERR_MISALIGNED",
@@ -45,7 +45,7 @@ EXPORTS = ["gemm_version", "gemm_last_error", "gemm_device_params_default",
            "gemm_plan_status", "gemm_plan_destroy", "gemm_tune", "gemm_cache_stats",
            "gemm_cache_clear", "gemm_debug_set", "gemm_run_noalloc", "gemm_tune_search",
            "gemm_cache_save", "gemm_cache_load", "gemm_plan_launch_info", "gemm_select_config_set",
-           "gemm_plan_from_list", "gemm_tune_batch", "gemm_run_ex"]
+           "gemm_plan_from_list", "gemm_tune_batch", "gemm_run_ex", "gemm_plan_set_scale"]
 
 
 class GemmError(RuntimeError):
@@ -76,7 +76,7 @@ class DeviceParams(ctypes.Structure):
     _fields_ = [("sm_count", ctypes.c_int32), ("model_kind", ctypes.c_int32),
                 ("smem_per_block", ctypes.c_int64), ("l2_bytes", ctypes.c_int64)] + \
                [(n, ctypes.c_double) for n in
-                ("peak_tflops_bf16", "peak_tflops_tf32", "hbm_gbs", "sm_clock_mhz", "l2_gbs", "mma_issue_clk",
+                ("peak_tflops_bf16", "peak_tflops_tf32", "peak_tflops_fp8", "hbm_gbs", "sm_clock_mhz", "l2_gbs", "mma_issue_clk",
                  "kblock_clk", "mem_latency_us", "epi_elems_per_clk", "epi_gelu_elems_per_clk", "splitk_gbs",
                  "launch_us")] + \
                [("kernel_regs", ctypes.c_int32), ("threads_per_cta", ctypes.c_int32)]
@@ -158,6 +158,7 @@ def _load_library(path: str):
         "gemm_plan_config": (ctypes.c_int, [vp, P(Config)]),
         "gemm_run": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "gemm_run_ex": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp]),
+        "gemm_plan_set_scale": (ctypes.c_int, [vp, ctypes.c_float]),
         "gemm_run_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "gemm_plan_status": (ctypes.c_int, [vp]),
         "gemm_plan_launch_info": (ctypes.c_int, [vp, P(LaunchInfo)]),
@@ -330,6 +331,10 @@ class Plan:
 
     def run(self, A, B, bias, C, stream=None) -> None:
         _check(lib().gemm_run(self._h, _ptr(A), _ptr(B), _ptr(bias), _ptr(C), _stream_handle(stream)))
+
+    def set_scale(self, alpha: float) -> None:
+        """C = act(alpha·(A·B) + bias) (+ R); for FP8 operands alpha = scale_A·scale_B."""
+        _check(lib().gemm_plan_set_scale(self._h, float(alpha)))
 
     def run_ex(self, A, B, bias, R, C, stream=None) -> None:
         """C = act(A·B + bias) + R for the residual epilogues (R may be C)."""

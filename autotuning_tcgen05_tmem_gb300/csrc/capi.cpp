@@ -44,6 +44,7 @@ int run_host(gemm_plan_t p, const void *A, const void *B, const void *bias, void
 int plan_status(gemm_plan_t p);
 int plan_config(gemm_plan_t p, gemm_config *out);
 int plan_launch_info(gemm_plan_t p, gemm_launch_info *out);
+int plan_set_scale(gemm_plan_t p, float alpha);
 void destroy_plan(gemm_plan_t p);
 int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, uint64_t seed,
          std::vector<gemm_tune_row> &rows, gemm_rank_stats &stats, gemm_config *winner,
@@ -79,7 +80,8 @@ void gemm_device_params_workshop(gemm_device_params *out)
 
 static bool enums_ok(int dt, int epi)
 {
-    return (dt == GEMM_BF16 || dt == GEMM_FP32_TF32) && epi >= GEMM_EPI_NONE && epi <= GEMM_EPI_BIAS_GELU;
+    return (dt == GEMM_BF16 || dt == GEMM_FP32_TF32 || dt == GEMM_FP8_E4M3) && epi >= GEMM_EPI_NONE &&
+           epi <= GEMM_EPI_BIAS_GELU_RESIDUAL;
 }
 
 int gemm_check_config(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, const gemm_config *cfg,
@@ -173,6 +175,12 @@ int gemm_plan_config(gemm_plan_t plan, gemm_config *out)
 {
     clear_error();
     return plan_config(plan, out);
+}
+
+int gemm_plan_set_scale(gemm_plan_t plan, float alpha)
+{
+    clear_error();
+    return plan_set_scale(plan, alpha);
 }
 
 int gemm_plan_launch_info(gemm_plan_t plan, gemm_launch_info *out)

@@ -20,8 +20,13 @@ constexpr int kAuxSmem = 2048;     // barriers and flags (1 KB) + 1 KB of base-a
 constexpr int kMaxStages = 16;
 constexpr int kMaxSplitK = 16;
 
-inline int elt_bytes(int dt) { return dt == GEMM_BF16 ? 2 : 4; }
+// Operand element size, and the size of C, bias and R (FP8 operands give bf16).
+inline int elt_bytes(int dt) { return dt == GEMM_BF16 ? 2 : dt == GEMM_FP8_E4M3 ? 1 : 4; }
+inline int out_elt_bytes(int dt) { return dt == GEMM_FP32_TF32 ? 4 : 2; }
 inline int span_elems(int dt) { return 128 / elt_bytes(dt); }
+// Whether B is read MN-major in place: bf16 always; FP8 when B's rows (N
+// bytes) meet TMA's 16-byte stride rule, else from a K-major copy, as fp32.
+inline bool b_in_place(int dt, int64_t N) { return dt == GEMM_BF16 || (dt == GEMM_FP8_E4M3 && N % 16 == 0); }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Shared-memory and TMEM layout of one configuration.

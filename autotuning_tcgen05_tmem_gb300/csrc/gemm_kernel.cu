@@ -34,6 +34,7 @@
 // flight, frees TMEM and exits.  Nothing traps.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -319,7 +320,9 @@ __device__ __forceinline__ void umma_commit(uint32_t bar)
     else umma_commit_one(bar);
 }
 
-// D[tmem] (+)= A[smem] · B[smem]; kind::f16 reads bf16, kind::tf32 reads fp32 as tf32.
+// D[tmem] (+)= A[smem] · B[smem]; kind::f16 reads bf16, kind::tf32 reads fp32 as
+// tf32, kind::f8f6f4 reads FP8 E4M3 (DT = 2).  Every kind consumes 32 bytes of K
+// per MMA.
 // CG = 2: one 256-row MMA over a CTA pair, issued by the pair's leader; each CTA
 // supplies 128 rows of A and half of B's columns from its own shared memory (at
 // the descriptors' offsets) and receives its 128 rows of D in its own TMEM.
@@ -335,6 +338,13 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t b
                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
                 : "memory");
+        else if constexpr (DT == 2)
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "setp.ne.b32 p, %4, 0;\n\t"
+                "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                : "memory");
         else
             asm volatile(
                 "{\n\t.reg .pred p;\n\t"
@@ -347,6 +357,13 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t b
             "{\n\t.reg .pred p;\n\t"
             "setp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else if constexpr (DT == 2) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
             "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
             : "memory");
     } else {
@@ -532,6 +549,10 @@ template <>
 struct Elt<1> {
     static constexpr int BYTES = 4;
 };
+template <>
+struct Elt<2> {   // FP8 E4M3
+    static constexpr int BYTES = 1;
+};
 
 // erf(z) for z >= 0 by Abramowitz & Stegun, "Handbook of Mathematical Functions"
 // (1964), formula 7.1.26: 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2)
@@ -550,17 +571,14 @@ __device__ __forceinline__ float gelu_erf(float x)
     return 0.5f * x * (x >= 0.0f ? 2.0f - q : q);
 }
 
-__device__ __forceinline__ float apply_act(float x, int epi)
-{
-    if (epi == 2) return fmaxf(x, 0.0f);
-    if (epi == 3) return gelu_erf(x);
-    return x;
-}
-
 // Applies bias (one value per column, held by lane j for column j of the
 // chunk) and the activation to a 32-column row chunk.
-__device__ __forceinline__ void bias_act_rows(float (&v)[32], float lane_bias, int epi)
+__device__ __forceinline__ void bias_act_rows(float (&v)[32], float lane_bias, int epi, float alpha)
 {
+    if (alpha != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= alpha;
+    }
     if (epi == 0) return;
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xFFFFFFFFu, lane_bias, j);
@@ -573,8 +591,12 @@ __device__ __forceinline__ void bias_act_rows(float (&v)[32], float lane_bias, i
     }
 }
 
-__device__ __forceinline__ void bias_act_cols(float (&v)[16], float row_bias, int epi)
+__device__ __forceinline__ void bias_act_cols(float (&v)[16], float row_bias, int epi, float alpha)
 {
+    if (alpha != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] *= alpha;
+    }
     if (epi == 0) return;
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] += row_bias;
@@ -777,8 +799,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmC, const KernelParams p)
 {
     constexpr int ELT = Elt<DT>::BYTES;
+    constexpr int ODT = DT == 2 ? 0 : DT;            // type of C, bias and R (FP8 operands give bf16)
     constexpr int SPAN = 128 / ELT;                  // elements in one 128-byte swizzle span
-    constexpr uint32_t MN_KSTEP = (32u / ELT) * 128u; // bytes per MMA K-step in an MN-major tile
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -1030,6 +1052,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------
         const int32_t e_bn = p.bn, e_bm = p.bm, e_epi = p.epi, e_cols = p.cols, e_rows = p.rows;
         const void *const e_resid = p.residual;   // C = act(A·B + bias) + R when set
+        const float e_alpha = p.alpha;          // C = act(alpha·(A·B) + bias) (+ R)
         const bool e_res = e_resid != nullptr;
         const int32_t e_split_k = p.split_k, e_swap_ab = p.swap_ab;
         const bool e_coop = p.coop_fixup != 0;
@@ -1076,12 +1099,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int ci = 0; ci < 4; ++ci) {
                         const int32_t c = cg + 2 * ci;
-                        if (c < chunks) bcol[ci] = load_bias1<DT>(e_bias, c0 + c * 32 + lane, e_cols);
+                        if (c < chunks) bcol[ci] = load_bias1<ODT>(e_bias, c0 + c * 32 + lane, e_cols);
                     }
                 } else {
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
-                        if (h < halves) brow[h] = load_bias1<DT>(e_bias, r0 + h * 128 + q * 32 + lane, e_rows);
+                        if (h < halves) brow[h] = load_bias1<ODT>(e_bias, r0 + h * 128 + q * 32 + lane, e_rows);
                 }
             }
             bool ok = true;
@@ -1171,10 +1194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                             }
                         }
-                        bias_act_rows(v, bcol[ci], e_epi);
+                        bias_act_rows(v, bcol[ci], e_epi, e_alpha);
                         const int32_t n = c0 + c * 32, y = r0 + h * 128 + q * 32;
-                        if (e_res) add_residual_rows<DT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
-                        store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
+                        if (e_res) add_residual_rows<ODT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
+                        store_rows_chunk<ODT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                     }
                 }
                 release_acc(acc);
@@ -1281,10 +1304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                             }
                         }
-                        bias_act_rows(v, bcol[ci], e_epi);
+                        bias_act_rows(v, bcol[ci], e_epi, e_alpha);
                         const int32_t n = c0 + c * 32, y = r0 + rg * 32;
-                        if (e_res) add_residual_rows<DT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
-                        store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
+                        if (e_res) add_residual_rows<ODT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
+                        store_rows_chunk<ODT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                     }
                 }
                 release_acc(acc);
@@ -1323,10 +1346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 dst[(size_t)(c * 8 + j4) * cta_rows + r] =
                                     make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
                         } else {
-                            bias_act_rows(v, bcol[ci], e_epi);
+                            bias_act_rows(v, bcol[ci], e_epi, e_alpha);
                             const int32_t n = c0 + c * 32, y = r0 + h * 128 + q * 32;
-                            if (e_res) add_residual_rows<DT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
-                            store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
+                            if (e_res) add_residual_rows<ODT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
+                            store_rows_chunk<ODT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                         }
                     }
                 } else {
@@ -1344,11 +1367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 dst[(size_t)(c * 4 + j4) * cta_rows + r] =
                                     make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
                         } else {
-                            bias_act_cols(v, h == 0 ? brow[0] : brow[1], e_epi);
+                            bias_act_cols(v, h == 0 ? brow[0] : brow[1], e_epi, e_alpha);
                             const int32_t xn = r0 + h * 128 + q * 32;  // output column block (user N)
                             const int32_t ym = c0 + c * 16;            // output row block (user M)
-                            if (e_res) add_residual_cols<DT>(v, e_resid, e_rows, ym, xn + lane, e_cols, e_rows);
-                            store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
+                            if (e_res) add_residual_cols<ODT>(v, e_resid, e_rows, ym, xn + lane, e_cols, e_rows);
+                            store_cols_chunk<ODT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
                         }
                     }
                 }
@@ -1399,7 +1422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] = 0.0f;
                             const float4 *src = tile_ws + (size_t)(c * 8) * cta_rows + r;
-                            const float lb = e_epi != 0 ? load_bias1<DT>(e_bias, c0 + c * 32 + lane, e_cols) : 0.0f;
+                            const float lb = e_epi != 0 ? load_bias1<ODT>(e_bias, c0 + c * 32 + lane, e_cols) : 0.0f;
                             for (int32_t s = 0; s < e_split_k; ++s) {
                                 float4 t[8];
 #pragma unroll
@@ -1412,16 +1435,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     v[4 * j4 + 3] += t[j4].w;
                                 }
                             }
-                            bias_act_rows(v, lb, e_epi);
+                            bias_act_rows(v, lb, e_epi, e_alpha);
                             const int32_t n = c0 + c * 32, y = r0 + rg * 32;
-                            if (e_res) add_residual_rows<DT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
-                            store_rows_chunk<DT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
+                            if (e_res) add_residual_rows<ODT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
+                            store_rows_chunk<ODT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                         } else {
                             float v[16];
 #pragma unroll
                             for (int j = 0; j < 16; ++j) v[j] = 0.0f;
                             const float4 *src = tile_ws + (size_t)(c * 4) * cta_rows + r;
-                            const float rb = e_epi != 0 ? load_bias1<DT>(e_bias, r0 + r, e_rows) : 0.0f;
+                            const float rb = e_epi != 0 ? load_bias1<ODT>(e_bias, r0 + r, e_rows) : 0.0f;
                             for (int32_t s = 0; s < e_split_k; s += 4) {
                                 float4 t[4][4];
 #pragma unroll
@@ -1443,10 +1466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         }
                                     }
                             }
-                            bias_act_cols(v, rb, e_epi);
+                            bias_act_cols(v, rb, e_epi, e_alpha);
                             const int32_t xn = r0 + rg * 32, ym = c0 + c * 16;
-                            if (e_res) add_residual_cols<DT>(v, e_resid, e_rows, ym, xn + lane, e_cols, e_rows);
-                            store_cols_chunk<DT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
+                            if (e_res) add_residual_cols<ODT>(v, e_resid, e_rows, ym, xn + lane, e_cols, e_rows);
+                            store_cols_chunk<ODT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
                         }
                     }
                     if (e_coop) {
@@ -1486,6 +1509,7 @@ __global__ void fill_uniform_kernel(void *dst, int64_t n, int dt, float scale, u
         x ^= x >> 16;
         const float f = ((float)(x >> 8) * (1.0f / 16777216.0f) * 2.0f - 1.0f) * scale;
         if (dt == 0) reinterpret_cast<__nv_bfloat16 *>(dst)[i] = __float2bfloat16_rn(f);
+        else if (dt == 2) reinterpret_cast<__nv_fp8_storage_t *>(dst)[i] = __nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3);
         else reinterpret_cast<float *>(dst)[i] = f;
     }
 }
@@ -1534,7 +1558,14 @@ static const void *select_kernel(int dt, int a_mn, int b_mn, int cg)
     if (cg == 2) {
         if (a_mn) return nullptr;
         if (dt == 0) return b_mn ? kernel_fn<0, false, true, 2>() : kernel_fn<0, false, false, 2>();
+        if (dt == 2) return b_mn ? kernel_fn<2, false, true, 2>() : kernel_fn<2, false, false, 2>();
         return b_mn ? nullptr : kernel_fn<1, false, false, 2>();
+    }
+    if (dt == 2) {   // FP8, like bf16: B MN-major in place (unswapped: MMA-B; swapped: MMA-A), or K-major copy
+        if (!a_mn && b_mn) return kernel_fn<2, false, true, 1>();
+        if (a_mn && !b_mn) return kernel_fn<2, true, false, 1>();
+        if (!a_mn && !b_mn) return kernel_fn<2, false, false, 1>();
+        return nullptr;
     }
     if (dt == 0) {
         if (!a_mn && b_mn) return kernel_fn<0, false, true, 1>();
@@ -1648,7 +1679,10 @@ cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t c
     const int64_t gy = (rows + 31) / 32;
     const dim3 grid((unsigned)((cols + 31) / 32), (unsigned)(gy < 65535 ? gy : 65535));
     const dim3 block(32, 8);
-    if (elt == 2)
+    if (elt == 1)
+        transpose_kernel<uint8_t><<<grid, block, 0, stream>>>(static_cast<const uint8_t *>(src),
+                                                              static_cast<uint8_t *>(dst), rows, cols);
+    else if (elt == 2)
         transpose_kernel<uint16_t><<<grid, block, 0, stream>>>(static_cast<const uint16_t *>(src),
                                                                static_cast<uint16_t *>(dst), rows, cols);
     else

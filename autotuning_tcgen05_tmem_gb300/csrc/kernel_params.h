@@ -35,6 +35,7 @@ struct KernelParams {
     uint32_t off_b, off_staging, off_bar, staging_buf_bytes;
     const void *bias;                  // nullable iff epi == 0
     const void *residual;              // nullable: C = act(A·B + bias) + residual when set
+    float alpha;                       // C = act(alpha·(A·B) + bias): the product's scale
     float *workspace;                  // split-K partial tiles
     int32_t *counters;                 // split-K arrival counters, one per tile
     int32_t *status;                   // device status word (0 = ok)

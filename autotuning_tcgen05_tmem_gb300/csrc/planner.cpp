@@ -39,6 +39,7 @@ void params_default(gemm_device_params *d)
     d->l2_bytes = 129LL * 1024 * 1024;
     d->peak_tflops_bf16 = 1889.6;
     d->peak_tflops_tf32 = 944.8;
+    d->peak_tflops_fp8 = 3779.2;     // the nominal 2x of bf16
     d->hbm_gbs = 6675.8;
     d->sm_clock_mhz = 2070.0;
     d->l2_gbs = 14888.0;
@@ -61,13 +62,14 @@ void params_workshop(gemm_device_params *d)
     d->smem_per_block = 228 * 1024;
     d->peak_tflops_bf16 = 989.0;
     d->peak_tflops_tf32 = 494.5;
+    d->peak_tflops_fp8 = 1978.0;
     d->hbm_gbs = 3350.0;
 }
 
 static int staging_bytes(int dt, int swap_ab)
 {
     const int rows = swap_ab ? 16 : 32;   // store chunk: 32 rows x 32 cols, or 16 token rows x 32 cols
-    return 8 * 2 * rows * 32 * elt_bytes(dt);   // 8 epilogue warps x 2 buffers
+    return 8 * 2 * rows * 32 * out_elt_bytes(dt);   // 8 epilogue warps x 2 buffers of C
 }
 
 Layout layout_of(const gemm_config &c, int dt)
@@ -155,8 +157,11 @@ int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_co
     if (c.bm != 128 && c.bm != 256) return GEMM_REASON_UMMA_M;
     if (c.bn % 16 != 0 || c.bn < 16 || c.bn > 256) return GEMM_REASON_UMMA_N;
     if (c.swap_ab != 0 && c.swap_ab != 1) return GEMM_REASON_LAYOUT;
-    if (c.swap_ab == 0 && (c.bn % span != 0 || c.bn % 32 != 0)) return GEMM_REASON_LAYOUT;
-    if (c.cta_group == 2 && (c.bn / 2) % span != 0) return GEMM_REASON_LAYOUT;
+    // B columns come in units of the MN-major swizzle span when B is read in
+    // place; a K-major copy of B needs only the epilogue's 32-column chunks.
+    const int b_unit = b_in_place(dt, N) ? span : 32;
+    if (c.swap_ab == 0 && (c.bn % b_unit != 0 || c.bn % 32 != 0)) return GEMM_REASON_LAYOUT;
+    if (c.cta_group == 2 && (c.bn / 2) % b_unit != 0) return GEMM_REASON_LAYOUT;
     if (c.bk % span != 0 || c.bk / span < 1 || c.bk / span > 4) return GEMM_REASON_BK;
     if (c.stages < 2 || c.stages > kMaxStages) return GEMM_REASON_STAGES;
     if ((c.raster != 0 && c.raster != 1) ||
@@ -165,7 +170,8 @@ int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_co
     const int64_t num_kb = cdiv(K, c.bk);
     if (c.split_k < 1 || c.split_k > kMaxSplitK || c.split_k > std::max<int64_t>(1, num_kb))
         return GEMM_REASON_SPLIT_K;
-    if ((K * e) % 16 != 0 || (N * e) % 16 != 0) return GEMM_REASON_ALIGN;
+    if ((K * e) % 16 != 0 || (N * out_elt_bytes(dt)) % 16 != 0 || (b_in_place(dt, N) && (N * e) % 16 != 0))
+        return GEMM_REASON_ALIGN;
     const Layout L = layout_of(c, dt);
     if (L.acc_cols > (uint32_t)kTmemColumns) return GEMM_REASON_TMEM;
     if ((int64_t)L.smem_total > d.smem_per_block) return GEMM_REASON_SMEM;
@@ -191,8 +197,12 @@ std::vector<gemm_config> enumerate(int64_t M, int64_t N, int64_t K, int dt, int 
             if (cg == 2 && swap) continue;
             std::vector<int> bns;
             if (swap) bns = {16, 32, 64, 128, 256};
-            else if (cg == 2) bns = dt == GEMM_BF16 ? std::vector<int>{128, 256} : std::vector<int>{64, 128, 256};
+            else if (cg == 2) bns = dt == GEMM_BF16                          ? std::vector<int>{128, 256}
+                                    : (dt == GEMM_FP8_E4M3 && b_in_place(dt, N)) ? std::vector<int>{256}
+                                                                            : std::vector<int>{64, 128, 256};
             else if (dt == GEMM_BF16) bns = {64, 128, 192, 256};
+            else if (dt == GEMM_FP8_E4M3) bns = b_in_place(dt, N) ? std::vector<int>{128, 256}
+                                                                  : std::vector<int>{64, 128, 192, 256};
             else bns = {32, 64, 128, 192, 256};
             for (int bn : bns) {
                 for (int bk : {span, 2 * span}) {
@@ -307,7 +317,8 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
     // Tensor pipe, per K-block of one CTA: the MMAs execute at the per-SM share
     // of the peak, and the issuing warp spends mma_issue_clk per MMA plus
     // kblock_clk per stage; the slower of the two sets the pace.
-    const double peak = (dt == GEMM_BF16 ? d.peak_tflops_bf16 : d.peak_tflops_tf32) * 1e12;
+    const double peak =
+        (dt == GEMM_BF16 ? d.peak_tflops_bf16 : dt == GEMM_FP8_E4M3 ? d.peak_tflops_fp8 : d.peak_tflops_tf32) * 1e12;
     const double halves = cg == 2 ? 1 : c.bm / 128, ksteps = (double)c.bk * e / 32.0, kslice = 32.0 / e;
     const double mma_flop = 2.0 * 128.0 * c.bn * kslice;
     const double t_exec = halves * ksteps * mma_flop / (peak / (double)sms);
@@ -336,8 +347,9 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
                          ((double)rows_w * c.bm + (double)cols_w * c.bn) * e;
     const double operand = (in_bytes <= (double)d.l2_bytes / 2.0) ? in_bytes : std::max(in_bytes, panel);
     // C, bias, and the residual R of the "+ R" epilogues.
-    const double hbm = operand + (double)M * N * e + (epi != GEMM_EPI_NONE ? (double)N * e : 0.0) +
-                       (epi >= GEMM_EPI_BIAS_RESIDUAL ? (double)M * N * e : 0.0);
+    const double eo = out_elt_bytes(dt);
+    const double hbm = operand + (double)M * N * eo + (epi != GEMM_EPI_NONE ? (double)N * eo : 0.0) +
+                       (epi >= GEMM_EPI_BIAS_RESIDUAL ? (double)M * N * eo : 0.0);
     const double t_hbm = hbm / (d.hbm_gbs * 1e9);
 
     // Bytes in flight ("Tiling the hierarchy", double buffering): the ring

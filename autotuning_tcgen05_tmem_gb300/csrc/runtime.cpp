@@ -70,7 +70,9 @@ static int encode_2d(CUtensorMap *m, int dt, const void *ptr, uint64_t inner, ui
     const cuuint64_t strides[1] = {inner * (uint64_t)elt_bytes(dt)};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapDataType t = dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUtensorMapDataType t = dt == GEMM_BF16       ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                  : dt == GEMM_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     CUresult r = g_encode(m, t, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -116,6 +118,7 @@ int query_params(gemm_device_params *d)
     if (kernel_attributes(GEMM_BF16, &regs, nullptr) == cudaSuccess) d->kernel_regs = regs;
     d->peak_tflops_bf16 = env_double("GEMM_PEAK_BF16_TFLOPS", d->peak_tflops_bf16);
     d->peak_tflops_tf32 = env_double("GEMM_PEAK_TF32_TFLOPS", d->peak_tflops_bf16 / 2.0);
+    d->peak_tflops_fp8 = env_double("GEMM_PEAK_FP8_TFLOPS", d->peak_tflops_bf16 * 2.0);
     d->hbm_gbs = env_double("GEMM_HBM_GBS", d->hbm_gbs);
     return GEMM_OK;
 }
@@ -189,7 +192,8 @@ static int configure_smem_limit(int dt, int64_t bytes)
 
 static bool valid_enums(int dt, int epi)
 {
-    return (dt == GEMM_BF16 || dt == GEMM_FP32_TF32) && epi >= GEMM_EPI_NONE && epi <= GEMM_EPI_BIAS_GELU_RESIDUAL;
+    return (dt == GEMM_BF16 || dt == GEMM_FP32_TF32 || dt == GEMM_FP8_E4M3) && epi >= GEMM_EPI_NONE &&
+           epi <= GEMM_EPI_BIAS_GELU_RESIDUAL;
 }
 
 // Residual epilogues are the bias / ReLU / GELU ones followed by "+ R".
@@ -253,13 +257,15 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     k.swap_ab = cfg.swap_ab;
     k.epi = act_code(epi);   // the kernel's bias/activation code; the residual is a run argument
     const int route = g_b_route.load();
-    p->b_kmajor = route == 1 || (route == 0 && dt == GEMM_FP32_TF32);
+    p->b_kmajor = route == 1 || (route == 0 && !b_in_place(dt, N));
     // User B is N-contiguous (MN-major) unless it is first transposed.  It is
     // MMA-A when swapped and MMA-B otherwise; A is always K-major.
     k.a_mn_major = (cfg.swap_ab && !p->b_kmajor) ? 1 : 0;
     k.b_mn_major = (!cfg.swap_ab && !p->b_kmajor) ? 1 : 0;
-    const uint32_t fmt = dt == GEMM_BF16 ? 1u : 2u;  // BF16 (kind::f16) / TF32 (kind::tf32)
+    // Operand formats: BF16 = 1 of kind::f16, TF32 = 2 of kind::tf32, E4M3 = 0 of kind::f8f6f4.
+    const uint32_t fmt = dt == GEMM_BF16 ? 1u : dt == GEMM_FP32_TF32 ? 2u : 0u;
     k.pair = cfg.cta_group == 2 ? 1 : 0;
+    k.alpha = 1.0f;
     const uint32_t mma_m = k.pair ? 256u : 128u;  // a pair's MMA spans both CTAs' 128 rows
     k.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)k.a_mn_major << 15) |
               ((uint32_t)k.b_mn_major << 16) | ((uint32_t)(cfg.bn >> 3) << 17) | ((mma_m >> 4) << 24);
@@ -425,12 +431,13 @@ static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const
         }
     }
     if (!rc) {
+        const int odt = dt == GEMM_FP8_E4M3 ? GEMM_BF16 : dt;   // C's type
         if (!c.swap_ab)
-            rc = encode_2d(&d.mc, dt, C, p->N, p->M, 32, 32,
-                           dt == GEMM_BF16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+            rc = encode_2d(&d.mc, odt, C, p->N, p->M, 32, 32,
+                           odt == GEMM_BF16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE);
         else
-            rc = encode_2d(&d.mc, dt, C, p->N, p->M, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE,
+            rc = encode_2d(&d.mc, odt, C, p->N, p->M, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE);
     }
     if (rc) return rc;
@@ -484,6 +491,14 @@ int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void
     return run_plan_ex(p, A, B, bias, nullptr, C, stream);
 }
 
+int plan_set_scale(gemm_plan_t p, float alpha)
+{
+    if (!p) return set_error(GEMM_ERR_INVALID_ARG, "null plan");
+    if (!(fabsf(alpha) <= 3.402823466e38f)) return set_error(GEMM_ERR_INVALID_ARG, "the scale must be finite");
+    p->kp.alpha = alpha;
+    return GEMM_OK;
+}
+
 int plan_launch_info(gemm_plan_t p, gemm_launch_info *out)
 {
     const KernelParams &k = p->kp;
@@ -525,9 +540,9 @@ int run_host(gemm_plan_t p, const void *A, const void *B, const void *bias, void
 {
     if (!p) return set_error(GEMM_ERR_INVALID_ARG, "null plan");
     if (p->M == 0 || p->N == 0) return GEMM_OK;
-    const size_t e = (size_t)elt_bytes(p->dt);
-    const size_t nA = (size_t)p->M * p->K * e, nB = (size_t)p->K * p->N * e, nBias = (size_t)p->N * e,
-                 nC = (size_t)p->M * p->N * e;
+    const size_t e = (size_t)elt_bytes(p->dt), eo = (size_t)out_elt_bytes(p->dt);
+    const size_t nA = (size_t)p->M * p->K * e, nB = (size_t)p->K * p->N * e, nBias = (size_t)p->N * eo,
+                 nC = (size_t)p->M * p->N * eo;
     cudaError_t err;
     if (!p->hC) {
         if ((nA && (err = cudaMalloc(&p->hA, nA)) != cudaSuccess) ||
@@ -670,9 +685,10 @@ int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, u
 
     // Library-owned buffers, rotated so that shapes smaller than L2 are timed
     // from HBM like the real, larger working set.
-    const size_t e = (size_t)elt_bytes(dt);
+    const size_t e = (size_t)elt_bytes(dt), eo = (size_t)out_elt_bytes(dt);
+    const int odt = dt == GEMM_FP8_E4M3 ? GEMM_BF16 : dt;   // type of bias and C
     const size_t bytes_a = (size_t)std::max<int64_t>(M * K, 1) * e, bytes_b = (size_t)std::max<int64_t>(K * N, 1) * e,
-                 bytes_bias = (size_t)std::max<int64_t>(N, 1) * e, bytes_c = (size_t)std::max<int64_t>(M * N, 1) * e;
+                 bytes_bias = (size_t)std::max<int64_t>(N, 1) * eo, bytes_c = (size_t)std::max<int64_t>(M * N, 1) * eo;
     const size_t set_bytes = bytes_a + bytes_b + bytes_bias + bytes_c;
     int nsets = (int)std::min<int64_t>(8, std::max<int64_t>(1, cdiv(2 * dev.l2_bytes + (int64_t)set_bytes, set_bytes)));
     TuneBuffers buf;
@@ -696,7 +712,7 @@ int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, u
         buf.C.push_back(c);
         launch_fill_uniform(a, (int64_t)(bytes_a / e), dt, scale_ab, 0x1234u + 17u * s, stream);
         launch_fill_uniform(b, (int64_t)(bytes_b / e), dt, scale_ab, 0x5678u + 17u * s, stream);
-        launch_fill_uniform(bb, (int64_t)(bytes_bias / e), dt, 0.1f, 0x9ABCu + 17u * s, stream);
+        launch_fill_uniform(bb, (int64_t)(bytes_bias / eo), odt, 0.1f, 0x9ABCu + 17u * s, stream);
     }
     size_t ws_bytes = 0;
     for (int i : meas) ws_bytes = std::max(ws_bytes, split_ws_bytes(M, N, cands[i]));

@@ -54,6 +54,13 @@ for _t in TOKENS:
 
 SWEEP = [WORKLOADS[f"bf16_gelu_{p}_t{t}"] for t in TOKENS for (p, _k, _n) in PROJECTIONS]
 
+# FP8 E4M3 operands (bf16 C) on the square, under-filled and decode shapes.
+WORKLOADS["fp8_relu_8192"] = Workload("fp8_relu_8192", 8192, 8192, 8192, FP8, "relu", "scaled_normal")
+WORKLOADS["fp8_gelu_1000x1000x8192"] = Workload("fp8_gelu_1000x1000x8192", 1000, 1000, 8192, FP8, "gelu",
+                                                "scaled_normal")
+WORKLOADS["fp8_decode_16x8192x28672"] = Workload("fp8_decode_16x8192x28672", 16, 28672, 8192, FP8, "none",
+                                                 "decode")
+
 
 def torch_dtype(dtype: str):
     """Operand type: bf16, fp32, or FP8 E4M3."""

@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload (the four headline shapes and the 30-shape sweep): one "
                          "JSON line per shape with tuned and fixed-tile throughput and roofline share")
+    ap.add_argument("--workloads", default=None,
+                    help="with --sweep: comma-separated workload names instead of the full list")
     ap.add_argument("--search-quality", action="store_true",
                     help="model-guided top-k vs random-k at equal measurement budgets, from one "
                          "exhaustive tuning table per workload (one JSON line per workload)")
@@ -79,11 +81,27 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def elt_sizes(dtype):
+    """(operand bytes, bytes of C and bias): FP8 operands give a bf16 C."""
+    return {"bf16": (2, 2), "fp8": (1, 2)}.get(dtype, (4, 4))
+
+
+def peak_ratio(dtype):
+    """Dense tensor peak of `dtype` relative to bf16 (the nominal ratios:
+    tf32 1.1, bf16 2.25, fp8 4.5 PFLOP/s)."""
+    return {"bf16": 1.0, "fp8": 2.0}.get(dtype, 0.5)
+
+
 def work_of(w):
-    elt = 2 if w.dtype == "bf16" else 4
+    elt, eo = elt_sizes(w.dtype)
     flops = 2.0 * w.M * w.N * w.K
-    bytes_ = (w.M * w.K + w.K * w.N) * elt + (w.N * elt if w.epi != "none" else 0) + w.M * w.N * elt
+    bytes_ = (w.M * w.K + w.K * w.N) * elt + (w.N * eo if w.epi != "none" else 0) + w.M * w.N * eo
     return flops, bytes_, elt
+
+
+def set_bytes_of(w):
+    elt, eo = elt_sizes(w.dtype)
+    return (w.M * w.K + w.K * w.N) * elt + (w.N + w.M * w.N) * eo
 
 
 # ---------------------------------------------------------------------------
@@ -240,7 +258,7 @@ def make_sets(w, nsets, device):
     sets = []
     for s in range(nsets):
         A, B, bias = inputs.make_workload(w, seed=100 + 10 * s, device=device)
-        C = torch.empty(w.M, w.N, dtype=A.dtype, device=device)
+        C = torch.empty(w.M, w.N, dtype=inputs.out_torch_dtype(w.dtype), device=device)
         sets.append((A, B, bias, C))
     return sets
 
@@ -321,11 +339,13 @@ def sweep(args):
     os.environ.setdefault("GEMM_HBM_GBS", str(peaks.get("hbm_gbs", 6800.0)))
     devp = g.device_params_query()
     names = ["fp32_relu_256", "bf16_gelu_1000x1000x8192", "bf16_relu_8192", "bf16_decode_16x8192x28672"] + \
-        [w.name for w in inputs.SWEEP]
+        [w.name for w in inputs.SWEEP] + ["fp8_gelu_1000x1000x8192", "fp8_relu_8192", "fp8_decode_16x8192x28672"]
+    if args.workloads:
+        names = [n for n in args.workloads.split(",")]
     for name in names:
         w = inputs.WORKLOADS[name]
         flops, cbytes, elt = work_of(w)
-        set_bytes = (w.M * w.K + w.K * w.N + w.N + w.M * w.N) * elt
+        set_bytes = set_bytes_of(w)
         nsets = int(min(8, max(1, math.ceil(2 * devp.l2_bytes / set_bytes))))
         sets = make_sets(w, nsets, torch.device("cuda", 0))
         t0 = time.perf_counter()
@@ -341,7 +361,7 @@ def sweep(args):
         region_s = t_tuned * steps * nsets
         sustained = region_s > 1.0
         bf16_peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops", 1900.0)
-        tpeak = bf16_peak / (1 if w.dtype == "bf16" else 2)
+        tpeak = bf16_peak * peak_ratio(w.dtype)
         bw = peaks.get("hbm_gbs", 6800.0)
         roof_t = max(flops / (tpeak * 1e12), cbytes / (bw * 1e9))
         line = {"workload": name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype, "epilogue": w.epi,
@@ -458,7 +478,7 @@ def main():
     os.environ.setdefault("GEMM_HBM_GBS", str(peaks.get("hbm_gbs", 6800.0)))
     flops, cbytes, elt = work_of(w)
     devp = g.device_params_query()
-    set_bytes = (w.M * w.K + w.K * w.N + w.N + w.M * w.N) * elt
+    set_bytes = set_bytes_of(w)
     nsets = int(min(8, max(1, math.ceil(2 * devp.l2_bytes / set_bytes))))
     sets = make_sets(w, nsets, dev)
 
@@ -500,9 +520,8 @@ def main():
 
     # --- roofline of the GEMM kernel -----------------------------------------
     sustained = elapsed > 1.0
-    tpeak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops", 1900.0)
-    if w.dtype != "bf16":
-        tpeak = tpeak / 2.0          # nominal tf32 : bf16 dense ratio (1.1 : 2.25 PFLOP/s)
+    # another dtype's peak: the measured bf16 peak x the nominal dense ratio
+    tpeak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops", 1900.0) * peak_ratio(w.dtype)
     bw = peaks.get("hbm_gbs", 6800.0)
     t_compute = flops / (tpeak * 1e12)
     t_memory = cbytes / (bw * 1e9)
@@ -573,7 +592,7 @@ def main():
         A, B, bias, _C = sets[0]
         hA, hB = A.cpu().pin_memory(), B.cpu().pin_memory()
         hb = bias.cpu().pin_memory() if bias is not None else None
-        hC = torch.empty(w.M, w.N, dtype=A.dtype).pin_memory()
+        hC = torch.empty(w.M, w.N, dtype=inputs.out_torch_dtype(w.dtype)).pin_memory()
         esteps = max(5, min(args.steps, 200))
         hstream = torch.cuda.Stream()
         for _ in range(3):
@@ -584,8 +603,9 @@ def main():
             plan.run_host(hA, hB, hb, hC, hstream)
         dt = (time.perf_counter() - t0) / esteps
         out["e2e"] = {"value": flops / dt / 1e12, "unit": "TFLOP/s",
-                      "h2d_bytes_per_step": (w.M * w.K + w.K * w.N + (w.N if bias is not None else 0)) * elt,
-                      "d2h_bytes_per_step": w.M * w.N * elt, "steps": esteps,
+                      "h2d_bytes_per_step": (w.M * w.K + w.K * w.N) * elt
+                                            + (w.N * elt_sizes(w.dtype)[1] if bias is not None else 0),
+                      "d2h_bytes_per_step": w.M * w.N * elt_sizes(w.dtype)[1], "steps": esteps,
                       "path": "gemm_run_host (pinned host buffers; copies and one kernel per step)"}
 
     # --- CPU oracle ------------------------------------------------------------

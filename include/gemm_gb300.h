@@ -33,10 +33,16 @@
  *   - GEMM_BF16: A, B, bias and C are bfloat16; products accumulate in fp32 in
  *     tensor memory; C is rounded to nearest-even once.  GEMM_FP32_TF32: A, B,
  *     bias and C are fp32; the tensor cores read the operands as TF32.
+ *     GEMM_FP8_E4M3: A and B are FP8 E4M3 bytes (OCP "E4M3FN": no infinities;
+ *     448 is the largest finite value), read by tcgen05.mma kind::f8f6f4; bias,
+ *     R and C are bfloat16; the product's scale (the operands' tensor scales)
+ *     is gemm_plan_set_scale's alpha.  B is read MN-major in place (as bf16)
+ *     when N is a multiple of 16, else from a K-major copy (as fp32).
  *   - GELU is the erf form 0.5·x·(1 + erf(x/√2)).
  *   - Device pointers are caller-owned, must stay valid until the work queued
  *     on the stream has finished, and must be 16-byte aligned; K·elt and N·elt
- *     must be multiples of 16 bytes (TMA row-stride rule).
+ *     must be multiples of 16 bytes (TMA row-stride rule; FP8: K a multiple of
+ *     16 and N of 8, the rows of A and of C).
  *   - Every function returns GEMM_OK (0) or a negative gemm_status; the text of
  *     the last error of the calling thread is returned by gemm_last_error().
  *     Nothing aborts, traps or exits the process.
@@ -67,7 +73,7 @@ typedef enum {
     GEMM_ERR_NO_DEVICE = -7     /* no CUDA device is visible */
 } gemm_status;
 
-typedef enum { GEMM_BF16 = 0, GEMM_FP32_TF32 = 1 } gemm_dtype;
+typedef enum { GEMM_BF16 = 0, GEMM_FP32_TF32 = 1, GEMM_FP8_E4M3 = 2 } gemm_dtype;
 
 typedef enum {
     GEMM_EPI_NONE = 0,       /* C = A·B                 (bias may be NULL) */
@@ -140,6 +146,7 @@ typedef struct {
     int64_t l2_bytes;
     double  peak_tflops_bf16;       /* dense tensor peak (measured burst on GB300) */
     double  peak_tflops_tf32;
+    double  peak_tflops_fp8;        /* FP8 dense peak (measured bf16 x the nominal 2x ratio) */
     double  hbm_gbs;                /* DRAM bandwidth, GB/s */
     double  sm_clock_mhz;
     double  l2_gbs;                 /* aggregate L2 -> shared-memory operand bandwidth, GB/s */
@@ -271,6 +278,11 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue e
  * GEMM_ERR_INFEASIBLE, with the reason in gemm_last_error, if it breaks a rule. */
 int gemm_plan_with_config(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
                           const gemm_config *cfg, gemm_plan_t *out);
+
+/* Scale of the product: C = act(alpha·(A·B) + bias) (+ R).  Default 1; for
+ * FP8 operands alpha is scale_A·scale_B.  Applies to launches queued after the
+ * call. */
+int gemm_plan_set_scale(gemm_plan_t plan, float alpha);
 
 /* The configuration a plan runs. */
 int gemm_plan_config(gemm_plan_t plan, gemm_config *out);

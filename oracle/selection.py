@@ -213,7 +213,7 @@ def workshop_sweep(M, N, K, dev: WorkshopDevice = WorkshopDevice()):
 # the pages, which say nothing about TMEM/tcgen05; pinned by brute force).
 # ---------------------------------------------------------------------------
 
-DT_BF16, DT_FP32 = 0, 1
+DT_BF16, DT_FP32, DT_FP8 = 0, 1, 2
 EPI_NONE, EPI_BIAS, EPI_RELU, EPI_GELU = 0, 1, 2, 3
 EPI_BIAS_RES, EPI_RELU_RES, EPI_GELU_RES = 4, 5, 6   # the same plus a residual R
 
@@ -254,6 +254,7 @@ class Device:
     l2_bytes: int = 129 * 1024 * 1024
     peak_tflops_bf16: float = 1889.6
     peak_tflops_tf32: float = 944.8
+    peak_tflops_fp8: float = 3779.2
     hbm_gbs: float = 6675.8
     sm_clock_mhz: float = 2070.0
     l2_gbs: float = 14888.0
@@ -270,7 +271,19 @@ class Device:
 
 
 def elt_bytes(dtype):
-    return 2 if dtype == DT_BF16 else 4
+    """Operand element size: bf16 2, FP8 E4M3 1, fp32 4."""
+    return 2 if dtype == DT_BF16 else 1 if dtype == DT_FP8 else 4
+
+
+def b_in_place(dtype, N):
+    """B read MN-major in place: bf16 always, FP8 when its rows (N bytes) meet
+    the 16-byte stride rule; otherwise from a K-major copy (fp32 always)."""
+    return dtype == DT_BF16 or (dtype == DT_FP8 and N % 16 == 0)
+
+
+def out_elt_bytes(dtype):
+    """Size of C, bias and R: FP8 operands produce bf16."""
+    return 4 if dtype == DT_FP32 else 2
 
 
 def span_elems(dtype):
@@ -282,7 +295,7 @@ def staging_bytes(dtype, swap_ab):
     """Epilogue staging: 8 epilogue warps × 2 buffers × one store chunk
     (32 rows × 32 columns, or 16 token rows × 32 columns when swapped)."""
     rows = 16 if swap_ab else 32
-    return 8 * 2 * rows * 32 * elt_bytes(dtype)
+    return 8 * 2 * rows * 32 * out_elt_bytes(dtype)
 
 
 def cta_share(cfg: Config):
@@ -330,9 +343,12 @@ def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
         return R_UMMA_N
     if cfg.swap_ab not in (0, 1):
         return R_LAYOUT
-    if cfg.swap_ab == 0 and (cfg.bn % span != 0 or cfg.bn % 32 != 0):
+    # B in place comes in MN-major swizzle spans; a K-major copy of B only
+    # needs the epilogue's 32-column chunks.
+    b_unit = span if b_in_place(dtype, N) else 32
+    if cfg.swap_ab == 0 and (cfg.bn % b_unit != 0 or cfg.bn % 32 != 0):
         return R_LAYOUT
-    if cfg.cta_group == 2 and (cfg.bn // 2) % span != 0:
+    if cfg.cta_group == 2 and (cfg.bn // 2) % b_unit != 0:
         return R_LAYOUT
     if cfg.bk % span != 0 or not (1 <= cfg.bk // span <= 4):
         return R_BK
@@ -343,7 +359,8 @@ def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
     num_kb = ceil_div(K, cfg.bk)
     if cfg.split_k < 1 or cfg.split_k > 16 or cfg.split_k > max(1, num_kb):
         return R_SPLIT_K
-    if (K * elt) % 16 != 0 or (N * elt) % 16 != 0:
+    if (K * elt) % 16 != 0 or (N * out_elt_bytes(dtype)) % 16 != 0 or \
+            (b_in_place(dtype, N) and (N * elt) % 16 != 0):
         return R_ALIGN
     acc, _nbuf = tmem_columns(cfg)
     if acc > TMEM_COLUMNS:
@@ -371,9 +388,12 @@ def gb300_candidates(M, N, K, dtype, epi, dev: Device):
             if swap:
                 bns = (16, 32, 64, 128, 256)
             elif cg == 2:
-                bns = (128, 256) if dtype == DT_BF16 else (64, 128, 256)
+                bns = (128, 256) if dtype == DT_BF16 else \
+                    (256,) if (dtype == DT_FP8 and b_in_place(dtype, N)) else (64, 128, 256)
             elif dtype == DT_BF16:
                 bns = (64, 128, 192, 256)
+            elif dtype == DT_FP8:
+                bns = (128, 256) if b_in_place(dtype, N) else (64, 128, 192, 256)
             else:
                 bns = (32, 64, 128, 192, 256)
             for bn in bns:
@@ -479,7 +499,8 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
     clock = dev.sm_clock_mhz * 1e6
     flops = 2.0 * M * N * K
 
-    peak = (dev.peak_tflops_bf16 if dtype == DT_BF16 else dev.peak_tflops_tf32) * 1e12
+    peak = (dev.peak_tflops_bf16 if dtype == DT_BF16 else
+            dev.peak_tflops_fp8 if dtype == DT_FP8 else dev.peak_tflops_tf32) * 1e12
     halves = 1 if cg == 2 else cfg.bm // 128
     ksteps = cfg.bk * elt / 32
     one_mma = 2.0 * 128 * cfg.bn * (32 / elt)
@@ -500,8 +521,9 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
         rows_w = min(ceil_div(wave_tiles, cols_w), tiles_m)
     panel = (tiles / wave_tiles) * K * (rows_w * cfg.bm + cols_w * cfg.bn) * elt
     operand = in_bytes if in_bytes <= dev.l2_bytes / 2 else max(in_bytes, panel)
-    hbm = (operand + M * N * elt + (N * elt if epi != EPI_NONE else 0)
-           + (M * N * elt if epi >= EPI_BIAS_RES else 0))      # C, bias, residual R
+    eo = out_elt_bytes(dtype)
+    hbm = (operand + M * N * eo + (N * eo if epi != EPI_NONE else 0)
+           + (M * N * eo if epi >= EPI_BIAS_RES else 0))      # C, bias, residual R
     hbm_s = hbm / (dev.hbm_gbs * 1e9)
 
     latency_s = per_cta_units * slice_kb * dev.mem_latency_us * 1e-6 / cfg.stages

@@ -33,7 +33,10 @@ def to_oracle_config(c) -> sel.Config:
 SHAPES = [(256, 256, 256, 1, 2), (1000, 1000, 8192, 0, 3), (8192, 8192, 8192, 0, 2),
           (16, 28672, 8192, 0, 0), (128, 4096, 14336, 0, 3), (512, 1024, 4096, 0, 3),
           (2048, 28672, 4096, 0, 3), (8192, 4096, 14336, 0, 3), (17, 96, 40, 1, 1),
-          (1, 8, 8, 0, 0), (300, 200, 72, 0, 2), (64, 64, 0, 0, 1)]
+          (1, 8, 8, 0, 0), (300, 200, 72, 0, 2), (64, 64, 0, 0, 1),
+          # FP8 E4M3 operands (bf16 C): K-major copy of B, 128-byte spans of 128 elements
+          (1000, 1000, 8192, 2, 3), (8192, 8192, 8192, 2, 2), (16, 28672, 8192, 2, 0), (300, 200, 128, 2, 2),
+          (512, 1024, 4096, 2, 6), (100, 104, 48, 2, 1)]
 
 
 def test_library_exports_every_declared_symbol():
