@@ -201,6 +201,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_epilogue e
     k.num_units = (int32_t)(tiles * c.split_k);
     k.swap_ab = c.swap_ab;
     k.epi = epi;
+    k.alpha = 1.0f;                 // C = act(1·(A·B) + bias); residual stays null
     k.a_mn_major = c.swap_ab ? 1 : 0;
     k.b_mn_major = c.swap_ab ? 0 : 1;
     k.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)k.a_mn_major << 15) | ((uint32_t)k.b_mn_major << 16) |

@@ -27,8 +27,11 @@ GEMM_HD SchedUnit schedule_unit(int64_t unit, int32_t tiles_m, int32_t tiles_n, 
                                 int32_t raster, int32_t group, int32_t num_kb)
 {
     SchedUnit r;
-    const int32_t tile = (int32_t)(unit / split_k);
-    const int32_t s = (int32_t)(unit - (int64_t)tile * split_k);
+    // Units number fewer than 2^31 (tiles x split_k is an int32 of the
+    // launch), so 32-bit arithmetic suffices.
+    const int32_t u = (int32_t)unit;
+    const int32_t tile = u / split_k;
+    const int32_t s = u - tile * split_k;
     if (raster == 0) {
         const int32_t per_band = group * tiles_n;
         const int32_t band = tile / per_band;
@@ -47,8 +50,9 @@ GEMM_HD SchedUnit schedule_unit(int64_t unit, int32_t tiles_m, int32_t tiles_n, 
         r.tile_m = within / width;
     }
     r.split = s;
-    r.kb_begin = (int32_t)(((int64_t)s * num_kb) / split_k);
-    r.kb_end = (int32_t)(((int64_t)(s + 1) * num_kb) / split_k);
+    // s <= 16 and num_kb <= 2^31 / 32 (K < 2^31, bk >= 32), so s * num_kb < 2^31.
+    r.kb_begin = (s * num_kb) / split_k;
+    r.kb_end = ((s + 1) * num_kb) / split_k;
     r.tile = r.tile_m * tiles_n + r.tile_n;
     return r;
 }
