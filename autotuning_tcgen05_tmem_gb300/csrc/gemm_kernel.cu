@@ -509,10 +509,19 @@ __device__ __noinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, con
 }
 
 // Publishes this CTA's earlier global writes (ordered before this thread by a
-// CTA barrier) together with the increment.
-__device__ __forceinline__ void red_release_gpu_add(int32_t *ptr, int32_t v)
+// CTA barrier) together with the increment; returns the count before it.
+__device__ __forceinline__ uint64_t atom_release_gpu_add_u64(uint64_t *ptr, uint64_t v)
 {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+    uint64_t old;
+    asm volatile("atom.release.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(ptr), "l"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *ptr)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *ptr)
@@ -532,6 +541,26 @@ __device__ __noinline__ bool wait_counter(const int32_t *ptr, int32_t target, co
     for (uint32_t it = 1;; ++it) {
         __nanosleep(32);
         if (ld_acquire_gpu(ptr) >= target) return true;
+        if ((it & 15u) == 0) {
+            if (*c.abort) return false;
+            if (clock64() - t0 > limit_cycles) {
+                *c.abort = 1;
+                atomicCAS(c.status, 0, site);
+                return false;
+            }
+        }
+    }
+}
+
+// Waits until *ptr >= target (64-bit arrival counts), bounded like the others.
+__device__ __noinline__ bool wait_epoch(const uint64_t *ptr, uint64_t target, const WaitCtl &c, int32_t site)
+{
+    if (ld_acquire_gpu_u64(ptr) >= target) return true;
+    const long long limit_cycles = (long long)((double)c.timeout_ns * 2.2);
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(32);
+        if (ld_acquire_gpu_u64(ptr) >= target) return true;
         if ((it & 15u) == 0) {
             if (*c.abort) return false;
             if (clock64() - t0 > limit_cycles) {
@@ -1087,6 +1116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const void *const e_bias = p.bias;
         float *const e_workspace = p.workspace;
         int32_t *const e_counters = p.counters;
+        uint64_t *const e_epochs = p.epochs;
         const int q = warp & 3;             // TMEM sub-partition this warp may read
         const int ew = warp - 2;            // 0..7
         const int cg = ew >> 2;             // column-chunk parity handled by this warp
@@ -1268,11 +1298,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dst[j4 * 32] = make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
                     }
                 }
+                // Each launch adds exactly S arrivals per tile and the counts never
+                // reset: this slice's own arrival names its launch's base.
                 named_bar_sync(1, kEpiThreads);
                 bool cok = true;
                 if (ew == 0 && lane == 0) {
-                    red_release_gpu_add(e_counters + xtile, 1);
-                    cok = wait_counter(e_counters + xtile, S, ctl, SITE_FIXUP);
+                    const uint64_t before = atom_release_gpu_add_u64(e_epochs + xtile, 1);
+                    const uint64_t target = before - before % (uint64_t)S + (uint64_t)S;
+                    cok = wait_epoch(e_epochs + xtile, target, ctl, SITE_FIXUP);
                 }
                 if (named_bar_any(1, kEpiThreads, !cok)) break;
                 for (int32_t h = 0; h < halves; ++h) {
@@ -1340,12 +1373,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++acc == e_n_acc) {
                     acc = 0;
                     acc_phase ^= 1u;
-                }
-                // The last of the S slices to leave resets the counter for the next launch.
-                named_bar_sync(1, kEpiThreads);
-                if (ew == 0 && lane == 0) {
-                    const int32_t old = atomicAdd(e_counters + xtile, 1);
-                    if (old == 2 * S - 1) atomicExch(e_counters + xtile, 0);
                 }
                 continue;
             }

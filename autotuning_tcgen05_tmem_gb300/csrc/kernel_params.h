@@ -37,7 +37,8 @@ struct KernelParams {
     const void *residual;              // nullable: C = act(A·B + bias) + residual when set
     float alpha;                       // C = act(alpha·(A·B) + bias): the product's scale
     float *workspace;                  // split-K partial tiles
-    int32_t *counters;                 // split-K arrival counters, one per tile
+    int32_t *counters;                 // split-K arrival counters, one per tile (last arriver)
+    uint64_t *epochs;                  // cooperative split-K: arrivals per tile, never reset
     int32_t *status;                   // device status word (0 = ok)
     int64_t timeout_ns;                // bound of every mbarrier wait
     int32_t debug_stall;               // epilogue waits on a barrier nothing signals

@@ -163,7 +163,9 @@ struct gemm_plan_s {
     int grid = 0, smem_request = 0;
     float *workspace = nullptr;
     bool owns_workspace = false;
-    int32_t *aux = nullptr;          // [0] status word, [1..tiles] split-K counters
+    int32_t *aux = nullptr;          // [0] status word, [1..n_counters] split-K counters
+    uint64_t *epochs = nullptr;      // cooperative split-K arrival counts (only ever grow)
+    int64_t n_counters = 0;
     int64_t tiles = 0;
     std::vector<DescEntry> descs = std::vector<DescEntry>(16);
     int next_desc = 0;
@@ -313,6 +315,18 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     }
     k.status = p->aux;
     k.counters = p->aux + 1;
+    p->n_counters = n_counters;
+    if (cfg.split_k > 1) {
+        e = cudaMalloc(&p->epochs, (size_t)n_counters * sizeof(uint64_t));
+        if (e == cudaSuccess) e = cudaMemset(p->epochs, 0, (size_t)n_counters * sizeof(uint64_t));
+        if (e != cudaSuccess) {
+            cudaFree(p->epochs);
+            cudaFree(p->aux);
+            delete p;
+            return cuda_err(e, "cudaMalloc(split-K epochs)");
+        }
+    }
+    k.epochs = p->epochs;
     if (cfg.split_k > 1) {
         if (shared_ws) {
             p->workspace = shared_ws;
@@ -321,6 +335,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
             e = cudaMalloc(&p->workspace, bytes);
             if (e != cudaSuccess) {
                 cudaFree(p->aux);
+                cudaFree(p->epochs);
                 delete p;
                 return cuda_err(e, "cudaMalloc(split-K workspace)");
             }
@@ -385,6 +400,7 @@ void destroy_plan(gemm_plan_t p)
     cudaFree(p->bt);
     if (p->owns_workspace) cudaFree(p->workspace);
     cudaFree(p->aux);
+    cudaFree(p->epochs);
     cudaFree(p->hA);
     cudaFree(p->hB);
     cudaFree(p->hBias);
@@ -530,7 +546,9 @@ int plan_status(gemm_plan_t p)
     e = cudaMemcpy(&st, p->aux, sizeof(st), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_err(e, "reading the status word");
     if (st != 0) {
-        cudaMemset(p->aux, 0, (size_t)(1 + p->tiles) * sizeof(int32_t));
+        // An early return may leave counts part-way: start them afresh.
+        cudaMemset(p->aux, 0, (size_t)(1 + p->n_counters) * sizeof(int32_t));
+        if (p->epochs) cudaMemset(p->epochs, 0, (size_t)p->n_counters * sizeof(uint64_t));
         return set_error(GEMM_ERR_TIMEOUT, "a device wait expired (site %d); the kernel returned early", st);
     }
     return GEMM_OK;
