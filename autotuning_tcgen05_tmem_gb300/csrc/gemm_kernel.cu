@@ -1,4 +1,6 @@
-// Persistent, warp-specialised tcgen05 GEMM for sm_103a:  C = act(A·B + bias).
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a:
+//   C = act(alpha·(A·B) + bias) (+ R),  operands bf16, fp32 (read as tf32) or
+//   FP8 E4M3 (C, bias and R then bf16).
 //
 // What the pages fix and how this kernel realises it on GB300:
 //   * "Tile Selection: Cost Models Against Measurement", "The structure of the
@@ -20,13 +22,16 @@
 // Roles (320 threads): warp 0 issues TMA loads and warp 1 owns TMEM and issues
 // tcgen05.mma (one elected lane each, the warp walking the schedule converged);
 // warps 2..9 (256 threads) drain the accumulator, each reading the 32 TMEM
-// lanes of its sub-partition (warp % 4), two warps per sub-partition.
+// lanes of its sub-partition (warp % 4), two warps per sub-partition.  With
+// CG = 2 two consecutive CTAs share a 256-row tile (cta_group::2): each holds
+// 128 rows and half of B, and the first CTA's MMA warp issues for both.
 //
 // Split-K: the K slices of a tile either exchange fp32 partial tiles through
-// global memory (a cooperative or last-arriver fix-up), or, when the slices of
-// a tile form one thread-block cluster, push them into the owning CTA's shared
-// memory with st.async (distributed shared memory) and never touch global
-// memory for the reduction.
+// global memory (a cooperative fix-up when all slices are resident, each slice
+// finalising its share; else the last slice to arrive finalises the tile), or,
+// when the slices of a tile form one thread-block cluster, push them into the
+// owning CTA's shared memory with st.async (distributed shared memory).  Every
+// route adds the partials in slice order, so all give the same bits.
 //
 // Every mbarrier wait is bounded: after the limit the waiting role writes a
 // code to the status word, raises a CTA-wide abort flag and returns; the other

@@ -33,12 +33,13 @@ namespace gemmgb {
 
 std::atomic<int64_t> g_timeout_ns{2000000000LL};
 std::atomic<int32_t> g_debug_stall{0};
-// How B reaches the tensor cores: 0 = by dtype (bf16 read MN-major in place,
-// fp32 transposed to a K-major copy), 1 = always transposed, 2 = always MN-major.
+// How B reaches the tensor cores: 0 = by dtype (bf16 read MN-major in place;
+// FP8 too when N % 16 == 0; fp32 transposed to a K-major copy), 1 = always
+// transposed, 2 = always MN-major.
 std::atomic<int32_t> g_b_route{0};
 // How split-K slices exchange partial tiles: 0 = through distributed shared
-// memory when the slices of a tile can form a cluster, else global memory;
-// 1 = always global memory.
+// memory when all units fit in one wave and the slices of a tile can form a
+// cluster, else global memory; 1 = always global memory.
 std::atomic<int32_t> g_split_route{0};
 
 // ---------------------------------------------------------------------------

@@ -3,11 +3,12 @@
  *
  * The library computes the fused tiled multiply
  *
- *     C[m,n] = act( sum_k A[m,k] · B[k,n] + bias[n] )
+ *     C[m,n] = act( alpha · sum_k A[m,k] · B[k,n] + bias[n] )  ( + R[m,n] )
  *
- * with a tile configuration (BM, BN, BK, pipeline stages, tile order, split-K)
- * chosen per problem shape, first by an analytical cost model and then by
- * timing candidates on the device, and cached by shape.
+ * (alpha = 1 and no R unless asked for) with a tile configuration (BM, BN, BK,
+ * pipeline stages, tile order, split-K, CTA pair, operand swap) chosen per
+ * problem shape, first by an analytical cost model and then by timing
+ * candidates on the device, and cached by shape (and, optionally, in a file).
  *
  * Sources (page title, section):
  *   - "Tile Selection: Cost Models Against Measurement": the search space
@@ -401,14 +402,13 @@ int gemm_tune_batch(const int64_t *mnk, int32_t n, gemm_dtype dtype, gemm_epilog
  * returns); what = 1: make the epilogue wait on a barrier that nothing signals
  * (1 = on, 0 = off) so that the timeout path can be tested; what = 2: how B
  * reaches the tensor cores in plans made afterwards (0 = by dtype: bf16 is read
- * MN-major in place, fp32 is first transposed into a plan-owned K-major copy;
- * 1 = always transposed; 2 = always MN-major); what = 3: how split-K slices
- * exchange partial tiles in plans made afterwards (0 = through distributed
- * shared memory when all units fit in one wave and the slices of a tile can
- * form a thread-block cluster, else through global memory; 1 = always through
- * global memory).  Affects
- * launches (what 0, 1) or plans (what 2, 3) made after the call, from any
- * thread. */
+ * MN-major in place, FP8 too when N is a multiple of 16, fp32 is first
+ * transposed into a plan-owned K-major copy; 1 = always transposed; 2 = always
+ * MN-major); what = 3: how split-K slices exchange partial tiles in plans made
+ * afterwards (0 = through distributed shared memory when all units fit in one
+ * wave and the slices of a tile can form a thread-block cluster, else through
+ * global memory; 1 = always through global memory).  Affects launches (what 0,
+ * 1) or plans (what 2, 3) made after the call, from any thread. */
 int gemm_debug_set(int32_t what, int64_t value);
 
 /* ---------------------------------------------------------------------------
