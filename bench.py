@@ -348,6 +348,13 @@ def sweep(args):
         set_bytes = set_bytes_of(w)
         nsets = int(min(8, max(1, math.ceil(2 * devp.l2_bytes / set_bytes))))
         sets = make_sets(w, nsets, torch.device("cuda", 0))
+        # Host side of the selection alone: enumerate and rank by the model
+        # (microseconds; "Autotuning & cost models" §5 weighs it against the
+        # on-device search below).
+        t0 = time.perf_counter()
+        cands = g.enumerate_configs(w.M, w.N, w.K, w.dtype, w.epi, devp)
+        preds = [g.model_predict(w.M, w.N, w.K, w.dtype, w.epi, c_, devp).predicted_us for c_ in cands]
+        host_rank_us = (time.perf_counter() - t0) * 1e6
         t0 = time.perf_counter()
         plan = g.plan(w.M, w.N, w.K, w.dtype, w.epi)
         tune_s = time.perf_counter() - t0
@@ -370,6 +377,8 @@ def sweep(args):
                 "bound": "tensor" if flops / (tpeak * 1e12) >= cbytes / (bw * 1e9) else "hbm",
                 "roofline_frac": roof_t / t_tuned, "fixed_us": t_fixed * 1e6,
                 "tuned_vs_fixed": t_fixed / t_tuned, "plan_seconds": tune_s, "timed_region_s": region_s,
+                "candidates": len(cands), "host_rank_us": host_rank_us,
+                "model_best_us": min(preds) if preds else None,
                 "peaks": f"{peak_src} bf16 {'sustained' if sustained else 'burst'} {bf16_peak} TFLOP/s, "
                          f"HBM {bw} GB/s"}
         print(json.dumps(line), flush=True)
