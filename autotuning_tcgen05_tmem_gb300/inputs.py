@@ -10,6 +10,14 @@ generator for timing-only buffers), then round once, to bf16 with torch's
 round-to-nearest-even conversion when the workload is bf16, or to FP8 E4M3
 (round to nearest even; every value drawn stays inside the format's range)
 when it is fp8, whose bias and C are bf16.
+
+Block-scaled FP8 (mxfp8) workloads draw E4M3 elements of order one and E8M0
+scale bytes separately (seeds +3 and +4 for A's and B's scales): for
+"scaled_normal" the elements are N(0, 1) and each 32-element block's scale is
+2^(e0 + u) with e0 = -round(log2(K) / 4) (so that C is of order one) and u
+uniform in {-1, 0, 1}; for "decode", A's scales are 2^u and B's 2^(u - 6) (the
+0.02 weight scale); for "int", elements are integers in [-2, 2] and scales
+2^u, so every product and sum is exact in fp32.
 """
 from __future__ import annotations
 
@@ -18,7 +26,7 @@ from dataclasses import dataclass
 
 import torch
 
-BF16, FP32, FP8 = "bf16", "fp32", "fp8"
+BF16, FP32, FP8, MXFP8 = "bf16", "fp32", "fp8", "mxfp8"
 EPI_CODES = {"none": 0, "bias": 1, "relu": 2, "gelu": 3}
 
 
@@ -60,18 +68,24 @@ WORKLOADS["fp8_gelu_1000x1000x8192"] = Workload("fp8_gelu_1000x1000x8192", 1000,
                                                 "scaled_normal")
 WORKLOADS["fp8_decode_16x8192x28672"] = Workload("fp8_decode_16x8192x28672", 16, 28672, 8192, FP8, "none",
                                                  "decode")
+# Block-scaled FP8 (MX: E8M0 scale per 32 elements of K) on the same shapes.
+WORKLOADS["mxfp8_relu_8192"] = Workload("mxfp8_relu_8192", 8192, 8192, 8192, MXFP8, "relu", "scaled_normal")
+WORKLOADS["mxfp8_gelu_1000x1000x8192"] = Workload("mxfp8_gelu_1000x1000x8192", 1000, 1000, 8192, MXFP8, "gelu",
+                                                  "scaled_normal")
+WORKLOADS["mxfp8_decode_16x8192x28672"] = Workload("mxfp8_decode_16x8192x28672", 16, 28672, 8192, MXFP8, "none",
+                                                   "decode")
 
 
 def torch_dtype(dtype: str):
-    """Operand type: bf16, fp32, or FP8 E4M3."""
-    if dtype == FP8:
+    """Operand type: bf16, fp32, or FP8 E4M3 (plain or block-scaled)."""
+    if dtype in (FP8, MXFP8):
         return torch.float8_e4m3fn
     return torch.bfloat16 if dtype == BF16 else torch.float32
 
 
 def out_torch_dtype(dtype: str):
     """Type of C, bias and R: FP8 operands produce bf16."""
-    return torch.bfloat16 if dtype in (BF16, FP8) else torch.float32
+    return torch.bfloat16 if dtype in (BF16, FP8, MXFP8) else torch.float32
 
 
 def _gen(seed: int, device):
@@ -122,6 +136,48 @@ def make_residual(M: int, N: int, dtype: str, dist: str, seed: int = 0, device="
     return R.to(out_torch_dtype(dtype)).contiguous()
 
 
+def make_mx_operands(M: int, N: int, K: int, dist: str, seed: int = 0, device="cpu", with_bias: bool = True):
+    """Block-scaled FP8: (A [M,K] E4M3, SA [M, ceil(K/32)] uint8 E8M0,
+    B [K,N] E4M3, SB [ceil(K/32), N] uint8 E8M0, bias [N] bf16 or None)."""
+    dev = torch.device(device)
+    gA, gB, gb, gsa, gsb = (_gen(seed + i, dev) for i in range(5))
+    f32 = torch.float32
+    kb = (K + 31) // 32
+
+    def u(shape, g):
+        return torch.randint(-1, 2, shape, generator=g, device=dev)
+
+    if dist == "int":
+        A = torch.randint(-2, 3, (M, K), generator=gA, device=dev).to(f32)
+        B = torch.randint(-2, 3, (K, N), generator=gB, device=dev).to(f32)
+        bias = torch.randint(-2, 3, (N,), generator=gb, device=dev).to(f32)
+        ea, eb = u((M, kb), gsa), u((kb, N), gsb)
+    elif dist in ("scaled_normal", "decode"):
+        A = torch.randn(M, K, generator=gA, device=dev, dtype=f32)
+        B = torch.randn(K, N, generator=gB, device=dev, dtype=f32)
+        bias = torch.randn(N, generator=gb, device=dev, dtype=f32) * 0.1
+        if dist == "scaled_normal":
+            e0 = -round(math.log2(max(K, 1)) / 4)
+            ea, eb = e0 + u((M, kb), gsa), e0 + u((kb, N), gsb)
+        else:
+            ea, eb = u((M, kb), gsa), u((kb, N), gsb) - 6
+    else:
+        raise ValueError(f"unknown distribution {dist!r}")
+    SA = (127 + ea).to(torch.uint8).contiguous()
+    SB = (127 + eb).to(torch.uint8).contiguous()
+    e4 = torch.float8_e4m3fn
+    return (A.to(e4).contiguous(), SA, B.to(e4).contiguous(), SB,
+            bias.to(torch.bfloat16).contiguous() if with_bias else None)
+
+
 def make_workload(w: Workload, seed: int = 0, device="cpu"):
+    """(A, B, bias) of a workload; for mxfp8 workloads use make_mx_workload."""
+    if w.dtype == MXFP8:
+        raise ValueError("block-scaled workloads have scales: use make_mx_workload")
     return make_operands(w.M, w.N, w.K, w.dtype, w.dist, seed=seed, device=device,
                          with_bias=(w.epi != "none"))
+
+
+def make_mx_workload(w: Workload, seed: int = 0, device="cpu"):
+    """(A, SA, B, SB, bias) of a block-scaled workload."""
+    return make_mx_operands(w.M, w.N, w.K, w.dist, seed=seed, device=device, with_bias=(w.epi != "none"))
