@@ -18,13 +18,14 @@ from dataclasses import dataclass
 
 from . import _build
 
-BF16, FP32_TF32, FP8_E4M3 = 0, 1, 2
+BF16, FP32_TF32, FP8_E4M3, MXFP8_E4M3 = 0, 1, 2, 3
 EPI_NONE, EPI_BIAS, EPI_BIAS_RELU, EPI_BIAS_GELU = 0, 1, 2, 3
 EPI_BIAS_RESIDUAL, EPI_BIAS_RELU_RESIDUAL, EPI_BIAS_GELU_RESIDUAL = 4, 5, 6
 EPILOGUES = {"none": EPI_NONE, "bias": EPI_BIAS, "relu": EPI_BIAS_RELU, "gelu": EPI_BIAS_GELU,
              "bias_residual": EPI_BIAS_RESIDUAL, "relu_residual": EPI_BIAS_RELU_RESIDUAL,
              "gelu_residual": EPI_BIAS_GELU_RESIDUAL}
-DTYPES = {"bf16": BF16, "fp32": FP32_TF32, "tf32": FP32_TF32, "fp8": FP8_E4M3, "e4m3": FP8_E4M3}
+DTYPES = {"bf16": BF16, "fp32": FP32_TF32, "tf32": FP32_TF32, "fp8": FP8_E4M3, "e4m3": FP8_E4M3,
+          "mxfp8": MXFP8_E4M3}
 
 OK = 0
 STATUS_NAMES = {0: "GEMM_OK", -1: "GEMM_ERR_INVALID_ARG", -2: "GEMM_ERR_MISALIGNED",
@@ -45,7 +46,8 @@ EXPORTS = ["gemm_version", "gemm_last_error", "gemm_device_params_default",
            "gemm_plan_status", "gemm_plan_destroy", "gemm_tune", "gemm_cache_stats",
            "gemm_cache_clear", "gemm_debug_set", "gemm_run_noalloc", "gemm_tune_search",
            "gemm_cache_save", "gemm_cache_load", "gemm_plan_launch_info", "gemm_select_config_set",
-           "gemm_plan_from_list", "gemm_tune_batch", "gemm_run_ex", "gemm_plan_set_scale"]
+           "gemm_plan_from_list", "gemm_tune_batch", "gemm_run_ex", "gemm_plan_set_scale",
+           "gemm_run_mx", "gemm_mx_scales_bytes", "gemm_mx_pack_scales"]
 
 
 class GemmError(RuntimeError):
@@ -159,6 +161,9 @@ def _load_library(path: str):
         "gemm_run": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "gemm_run_ex": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp]),
         "gemm_plan_set_scale": (ctypes.c_int, [vp, ctypes.c_float]),
+        "gemm_run_mx": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+        "gemm_mx_scales_bytes": (i64, [i64, i64]),
+        "gemm_mx_pack_scales": (ctypes.c_int, [vp, i64, i64, i32, vp, vp]),
         "gemm_run_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "gemm_plan_status": (ctypes.c_int, [vp]),
         "gemm_plan_launch_info": (ctypes.c_int, [vp, P(LaunchInfo)]),
@@ -340,6 +345,12 @@ class Plan:
         """C = act(A·B + bias) + R for the residual epilogues (R may be C)."""
         _check(lib().gemm_run_ex(self._h, _ptr(A), _ptr(B), _ptr(bias), _ptr(R), _ptr(C), _stream_handle(stream)))
 
+    def run_mx(self, A, SA, B, SB, bias, C, R=None, stream=None) -> None:
+        """Block-scaled FP8: SA and SB are A's and B's E8M0 scales packed by
+        mx_pack_scales (R as in run_ex)."""
+        _check(lib().gemm_run_mx(self._h, _ptr(A), _ptr(SA), _ptr(B), _ptr(SB), _ptr(bias), _ptr(R), _ptr(C),
+                                 _stream_handle(stream)))
+
     def run_rc(self, A, B, bias, C, stream=None) -> int:
         return lib().gemm_run(self._h, _ptr(A), _ptr(B), _ptr(bias), _ptr(C), _stream_handle(stream))
 
@@ -481,6 +492,24 @@ def run_noalloc_rc(M, N, K, epi, cfg: Config, A, B, bias, C, stream=None) -> int
 
 def run_noalloc(M, N, K, epi, cfg: Config, A, B, bias, C, stream=None) -> None:
     _check(run_noalloc_rc(M, N, K, epi, cfg, A, B, bias, C, stream))
+
+
+def mx_scales_bytes(rows: int, K: int) -> int:
+    """Bytes of one operand's packed MX scales (rows = M for A, N for B)."""
+    return int(lib().gemm_mx_scales_bytes(int(rows), int(K)))
+
+
+def mx_pack_scales(scales, rows: int, K: int, b_side: bool, out=None, stream=None):
+    """Pack E8M0 scales (a uint8 CUDA tensor: [rows, ceil(K/32)] for A, or
+    [ceil(K/32), rows] for B) into the layout gemm_run_mx reads; returns the
+    packed uint8 tensor (allocated when `out` is None)."""
+    import torch
+    n = mx_scales_bytes(rows, K)
+    if out is None:
+        out = torch.empty(max(n, 16), dtype=torch.uint8, device=scales.device)
+    _check(lib().gemm_mx_pack_scales(_ptr(scales), int(rows), int(K), 1 if b_side else 0, _ptr(out),
+                                     _stream_handle(stream)))
+    return out
 
 
 def gemm(A, B, bias=None, epi="none", out=None, stream=None):

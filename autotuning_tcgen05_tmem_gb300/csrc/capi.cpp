@@ -40,6 +40,9 @@ int plan_explicit(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_c
 int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream);
 int run_plan_ex(gemm_plan_t p, const void *A, const void *B, const void *bias, const void *R, void *C,
                 cudaStream_t stream);
+int run_plan_mx(gemm_plan_t p, const void *A, const void *SA, const void *B, const void *SB, const void *bias,
+                const void *R, void *C, cudaStream_t stream);
+int mx_pack_scales(const void *scales, int64_t rows, int64_t K, int b_side, void *packed, cudaStream_t stream);
 int run_host(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream);
 int plan_status(gemm_plan_t p);
 int plan_config(gemm_plan_t p, gemm_config *out);
@@ -80,8 +83,7 @@ void gemm_device_params_workshop(gemm_device_params *out)
 
 static bool enums_ok(int dt, int epi)
 {
-    return (dt == GEMM_BF16 || dt == GEMM_FP32_TF32 || dt == GEMM_FP8_E4M3) && epi >= GEMM_EPI_NONE &&
-           epi <= GEMM_EPI_BIAS_GELU_RESIDUAL;
+    return dt >= GEMM_BF16 && dt <= GEMM_MXFP8_E4M3 && epi >= GEMM_EPI_NONE && epi <= GEMM_EPI_BIAS_GELU_RESIDUAL;
 }
 
 int gemm_check_config(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, const gemm_config *cfg,
@@ -199,6 +201,25 @@ int gemm_run_ex(gemm_plan_t plan, const void *A, const void *B, const void *bias
                 gemm_stream_t stream)
 {
     return run_plan_ex(plan, A, B, bias, R, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gemm_run_mx(gemm_plan_t plan, const void *A, const void *SA, const void *B, const void *SB, const void *bias,
+                const void *R, void *C, gemm_stream_t stream)
+{
+    return run_plan_mx(plan, A, SA, B, SB, bias, R, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int64_t gemm_mx_scales_bytes(int64_t rows, int64_t K)
+{
+    if (rows < 0 || K < 0) return 0;
+    return mx_row_atoms(rows) * mx_k_atoms(K) * kMxAtomBytes;
+}
+
+int gemm_mx_pack_scales(const void *scales, int64_t rows, int64_t K, int32_t b_side, void *packed,
+                        gemm_stream_t stream)
+{
+    clear_error();
+    return mx_pack_scales(scales, rows, K, b_side, packed, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gemm_run_host(gemm_plan_t plan, const void *A, const void *B, const void *bias, void *C, gemm_stream_t stream)

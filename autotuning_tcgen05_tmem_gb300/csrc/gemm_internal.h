@@ -20,13 +20,20 @@ constexpr int kAuxSmem = 2048;     // barriers and flags (1 KB) + 1 KB of base-a
 constexpr int kMaxStages = 16;
 constexpr int kMaxSplitK = 16;
 
+// FP8 operands, plain (one tensor scale) or block-scaled (MX).
+inline bool is_fp8(int dt) { return dt == GEMM_FP8_E4M3 || dt == GEMM_MXFP8_E4M3; }
 // Operand element size, and the size of C, bias and R (FP8 operands give bf16).
-inline int elt_bytes(int dt) { return dt == GEMM_BF16 ? 2 : dt == GEMM_FP8_E4M3 ? 1 : 4; }
+inline int elt_bytes(int dt) { return dt == GEMM_BF16 ? 2 : is_fp8(dt) ? 1 : 4; }
 inline int out_elt_bytes(int dt) { return dt == GEMM_FP32_TF32 ? 4 : 2; }
 inline int span_elems(int dt) { return 128 / elt_bytes(dt); }
 // Whether B is read MN-major in place: bf16 always; FP8 when B's rows (N
 // bytes) meet TMA's 16-byte stride rule, else from a K-major copy, as fp32.
-inline bool b_in_place(int dt, int64_t N) { return dt == GEMM_BF16 || (dt == GEMM_FP8_E4M3 && N % 16 == 0); }
+inline bool b_in_place(int dt, int64_t N) { return dt == GEMM_BF16 || (is_fp8(dt) && N % 16 == 0); }
+// MX scales: one atom holds 128 rows x 128 K (four 32-element blocks a row) in
+// 512 bytes; the packed arrays pad rows and K to multiples of 256 (two atoms).
+constexpr int kMxAtomBytes = 512;
+inline int64_t mx_row_atoms(int64_t rows) { return 2 * ((rows + 255) / 256); }
+inline int64_t mx_k_atoms(int64_t K) { return 2 * ((K + 255) / 256); }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Shared-memory and TMEM layout of one configuration.
@@ -36,6 +43,9 @@ struct Layout {
     uint32_t off_b, off_staging, off_bar;
     uint32_t smem_total;              // bytes the kernel needs, slack included
     uint32_t acc_cols, n_acc, tmem_cols;
+    // MX scales: bytes a stage stages (A's atoms, then B's) at off_sf, and the
+    // TMEM columns a stage's scales occupy, one slot per stage from sc_col0.
+    uint32_t sf_stage_bytes, off_sf, sc_stage_cols, sc_col0;
 };
 Layout layout_of(const gemm_config &c, int dt);
 int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block, int cta_group);
@@ -69,5 +79,7 @@ cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, cons
 cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t cols, int elt, cudaStream_t stream);
 cudaError_t launch_fill_uniform(void *dst, int64_t n, int dt, float scale, uint32_t seed,
                                 cudaStream_t stream);
+cudaError_t launch_mx_pack(const uint8_t *src, int64_t rows, int64_t K, int b_side, uint8_t *dst,
+                           cudaStream_t stream);
 
 }  // namespace gemmgb

@@ -1,6 +1,7 @@
 // Persistent, warp-specialised tcgen05 GEMM for sm_103a:
-//   C = act(alpha·(A·B) + bias) (+ R),  operands bf16, fp32 (read as tf32) or
-//   FP8 E4M3 (C, bias and R then bf16).
+//   C = act(alpha·(A·B) + bias) (+ R),  operands bf16, fp32 (read as tf32),
+//   FP8 E4M3, or block-scaled FP8 (MX: E4M3 with an E8M0 scale per 32 elements
+//   of K); with FP8 operands C, bias and R are bf16.
 //
 // What the pages fix and how this kernel realises it on GB300:
 //   * "Tile Selection: Cost Models Against Measurement", "The structure of the
@@ -207,6 +208,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
+// Plain (untensored) bulk copy global -> shared memory, completing `bytes` on
+// `bar`; both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // Load into this CTA's shared memory, completing bytes on the barrier of the
 // pair's leader (a shared::cluster address): the second CTA of a CTA pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *m, uint32_t cluster_bar,
@@ -393,6 +403,43 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t b
             "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
             : "memory");
     }
+}
+
+// Block-scaled FP8 (kind::mxf8f6f4, one E8M0 scale per 32 elements of K):
+// D[tmem] (+)= (A·2^sa)·(B·2^sb).  The scales live in TMEM: row m of A reads
+// lane m, column sfa + m/32; column n of B reads lane n%32 of every lane
+// quarter, column sfb + n/32; the byte within the 32-bit word is the scale-ID
+// field of idesc (A: bits 29-30, B: bits 4-5), which names the 32-element block
+// of K that this MMA covers among the four a word holds.
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copy 32 rows x 16 bytes of shared memory into TMEM, the same 32 rows into
+// each of the four lane quarters (row r -> lane 32q + r, 4 columns); issued
+// by the MMA thread, in order with its MMAs.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Descriptor of a 32-row x 16-byte block in shared memory, no swizzle: four
+// 8-row core matrices of 128 contiguous bytes, 128 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t addr)
+{
+    uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
@@ -600,6 +647,10 @@ struct Elt<1> {
 };
 template <>
 struct Elt<2> {   // FP8 E4M3
+    static constexpr int BYTES = 1;
+};
+template <>
+struct Elt<3> {   // block-scaled FP8 E4M3 (MX)
     static constexpr int BYTES = 1;
 };
 
@@ -838,6 +889,41 @@ __device__ __forceinline__ void issue_stage(const MmaStage &st)
     }
 }
 
+// One block-scaled (MX) stage: first the stage's scale atoms go from shared
+// memory to its TMEM slot (A's atoms [half][K atom] at columns (h·KA + a)·4,
+// then B's at (HALVES·KA + a·bn_atoms + j)·4 so that a K atom's B columns are
+// contiguous, n/32 apart), then the MMAs, each naming its 32-element block of
+// K by the scale ID (kk mod 4) and its atom by the slot column (kk / 4).
+template <bool A_MN, bool B_MN, int KSTEPS, int HALVES>
+__device__ __forceinline__ void issue_stage_mx(const MmaStage &st, uint32_t slot, uint32_t sf_smem, int bn_atoms)
+{
+    constexpr int KA = KSTEPS / 4;
+    constexpr uint32_t MN_KSTEP16 = (32u * 128u) >> 4;
+#pragma unroll
+    for (int h = 0; h < HALVES; ++h)
+#pragma unroll
+        for (int a = 0; a < KA; ++a)
+            tmem_cp_32x128b_x4(slot + (uint32_t)(h * KA + a) * 4u,
+                               smem_desc_rows16(sf_smem + (uint32_t)(h * KA + a) * 512u));
+    for (int j = 0; j < bn_atoms; ++j)
+#pragma unroll
+        for (int a = 0; a < KA; ++a)
+            tmem_cp_32x128b_x4(slot + (uint32_t)(HALVES * KA + a * bn_atoms + j) * 4u,
+                               smem_desc_rows16(sf_smem + (uint32_t)(HALVES * KA + j * KA + a) * 512u));
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+        const uint32_t a_k = A_MN ? (uint32_t)kk * MN_KSTEP16 : (uint32_t)(kk >> 2) * st.a_span_step + (kk & 3) * 2u;
+        const uint32_t b_k = B_MN ? (uint32_t)kk * MN_KSTEP16 : (uint32_t)(kk >> 2) * st.b_span_step + (kk & 3) * 2u;
+        const uint32_t acc = (st.accumulate_first || kk != 0) ? 1u : 0u;
+        const uint32_t id = st.idesc | ((uint32_t)(kk & 3) << 29) | ((uint32_t)(kk & 3) << 4);
+        const uint32_t sfb = slot + (uint32_t)(HALVES * KA + (kk >> 2) * bn_atoms) * 4u;
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h)
+            umma_mx(st.d0 + (uint32_t)h * st.bn, st.adesc + a_k + (uint32_t)h * st.a_half_step, st.bdesc + b_k, id,
+                    slot + (uint32_t)(h * KA + (kk >> 2)) * 4u, sfb, acc);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -848,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmC, const KernelParams p)
 {
     constexpr int ELT = Elt<DT>::BYTES;
-    constexpr int ODT = DT == 2 ? 0 : DT;            // type of C, bias and R (FP8 operands give bf16)
+    constexpr int ODT = DT >= 2 ? 0 : DT;            // type of C, bias and R (FP8 operands give bf16)
     constexpr int SPAN = 128 / ELT;                  // elements in one 128-byte swizzle span
 
     extern __shared__ uint8_t smem_raw[];
@@ -973,6 +1059,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if constexpr (B_MN) tma_load_2d(sb + (uint32_t)(j * bk * 128), &tmB, fb, rb + j * SPAN, k0);
                         else tma_load_2d(sb + (uint32_t)(j * cta_bcols * 128), &tmB, fb, k0 + j * SPAN, rb);
                     }
+                    if constexpr (DT == 3) {
+                        // The stage's scale atoms: for each 128 rows of A, then
+                        // each 128 columns of B, its bk/128 consecutive K atoms.
+                        const uint32_t ka = (uint32_t)bk / 128u, run = ka * 512u;
+                        const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
+                        const int64_t k_atom = (int64_t)kb * ka;
+                        for (int32_t h = 0; h < bm / 128; ++h)
+                            bulk_load(sf + (uint32_t)h * run,
+                                      p.sfa + (((int64_t)w.tile_m * (bm / 128) + h) * p.sf_kt + k_atom) * 512, run, fb);
+                        for (int32_t j = 0; j < bn / 128; ++j)
+                            bulk_load(sf + (uint32_t)(bm / 128 + j) * run,
+                                      p.sfb + (((int64_t)w.tile_n * (bn / 128) + j) * p.sf_kt + k_atom) * 512, run, fb);
+                    }
                 } else if (leader) {
                     if constexpr (pair) {
                         // Second CTA of a pair: its halves land in its own shared
@@ -1052,7 +1151,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // more than an MMA's issue and starves the tensor pipe.
                     const MmaStage st{d0, adesc, bdesc, idesc, a_span_step, b_span_step, a_half_step,
                                       (uint32_t)bn, kb != 0};
-                    if constexpr (pair) {
+                    if constexpr (DT == 3) {
+                        const uint32_t slot = tmem_base + p.sc_col0 + stage * p.sc_stage_cols;
+                        const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
+                        const int bn_atoms = bn / 128;
+                        switch (ksteps * 2 + halves - 1) {
+                        case 8: issue_stage_mx<A_MN, B_MN, 4, 1>(st, slot, sf, bn_atoms); break;
+                        case 9: issue_stage_mx<A_MN, B_MN, 4, 2>(st, slot, sf, bn_atoms); break;
+                        case 16: issue_stage_mx<A_MN, B_MN, 8, 1>(st, slot, sf, bn_atoms); break;
+                        default: issue_stage_mx<A_MN, B_MN, 8, 2>(st, slot, sf, bn_atoms); break;
+                        }
+                        umma_commit<CG>(empty0 + 8u * stage);  // slot is free once these MMAs have read it
+                    } else if constexpr (pair) {
                         switch (ksteps) {
                         case 4: issue_stage<DT, A_MN, B_MN, 4, 1, 2>(st); break;
                         case 8: issue_stage<DT, A_MN, B_MN, 8, 1, 2>(st); break;
@@ -1567,7 +1677,7 @@ __global__ void fill_uniform_kernel(void *dst, int64_t n, int dt, float scale, u
         x ^= x >> 16;
         const float f = ((float)(x >> 8) * (1.0f / 16777216.0f) * 2.0f - 1.0f) * scale;
         if (dt == 0) reinterpret_cast<__nv_bfloat16 *>(dst)[i] = __float2bfloat16_rn(f);
-        else if (dt == 2) reinterpret_cast<__nv_fp8_storage_t *>(dst)[i] = __nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3);
+        else if (dt == 2 || dt == 3) reinterpret_cast<__nv_fp8_storage_t *>(dst)[i] = __nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3);
         else reinterpret_cast<float *>(dst)[i] = f;
     }
 }
@@ -1613,6 +1723,10 @@ static const void *kernel_fn()
 
 static const void *select_kernel(int dt, int a_mn, int b_mn, int cg)
 {
+    if (dt == 3) {   // block-scaled FP8: single CTA, unswapped; B in place or from a K-major copy
+        if (cg != 1 || a_mn) return nullptr;
+        return b_mn ? kernel_fn<3, false, true, 1>() : kernel_fn<3, false, false, 1>();
+    }
     if (cg == 2) {
         if (a_mn) return nullptr;
         if (dt == 0) return b_mn ? kernel_fn<0, false, true, 2>() : kernel_fn<0, false, false, 2>();
@@ -1746,6 +1860,37 @@ cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t c
     else
         transpose_kernel<uint32_t><<<grid, block, 0, stream>>>(static_cast<const uint32_t *>(src),
                                                                static_cast<uint32_t *>(dst), rows, cols);
+    return cudaGetLastError();
+}
+
+// MX scale packing: one thread per packed byte.  Packed byte o lies in atom
+// o/512 = (row atom rt, K atom kt) of the KT K atoms per row atom; within the
+// atom, byte (r%32)·16 + ((r%128)/32)·4 + j%4 holds the scale of row r, block
+// j (32 elements of K).  Rows or blocks past the operand read as 0.
+__global__ void mx_pack_kernel(const uint8_t *__restrict__ src, int64_t rows, int64_t kblocks, int64_t kt_atoms,
+                               int64_t total, int b_side, uint8_t *__restrict__ dst)
+{
+    for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < total; o += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t atom = o >> 9;
+        const int32_t within = (int32_t)(o & 511);
+        const int64_t rt = atom / kt_atoms, kt = atom % kt_atoms;
+        const int64_t r = rt * 128 + (within & 15) / 4 * 32 + within / 16;
+        const int64_t j = kt * 4 + (within & 3);
+        uint8_t v = 0;
+        if (r < rows && j < kblocks) v = b_side ? src[j * rows + r] : src[r * kblocks + j];
+        dst[o] = v;
+    }
+}
+
+cudaError_t launch_mx_pack(const uint8_t *src, int64_t rows, int64_t K, int b_side, uint8_t *dst,
+                           cudaStream_t stream)
+{
+    const int64_t rt = 2 * ((rows + 255) / 256), kt = 2 * ((K + 255) / 256);
+    const int64_t total = rt * kt * 512;
+    if (total <= 0) return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 8192) blocks = 8192;
+    mx_pack_kernel<<<(unsigned)blocks, 256, 0, stream>>>(src, rows, (K + 31) / 32, kt, total, b_side, dst);
     return cudaGetLastError();
 }
 

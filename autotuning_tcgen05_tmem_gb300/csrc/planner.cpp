@@ -84,13 +84,22 @@ Layout layout_of(const gemm_config &c, int dt)
     L.stage_bytes = L.a_stage_bytes + L.b_stage_bytes;
     L.staging_total = (uint32_t)staging_bytes(dt, c.swap_ab);
     L.staging_buf_bytes = L.staging_total / 16;
+    // MX: each stage also stages the scale atoms of its A rows (bm/128) and B
+    // columns (bn/128), bk/128 atoms along K each, and gives them a TMEM slot
+    // of 4 columns per atom (tcgen05.cp 32x128b.warpx4 fills 4 columns).
+    const int mx_atoms = dt == GEMM_MXFP8_E4M3 ? (c.bm / 128 + c.bn / 128) * (c.bk / 128) : 0;
+    L.sf_stage_bytes = (uint32_t)(mx_atoms * kMxAtomBytes);
+    L.sc_stage_cols = (uint32_t)(mx_atoms * 4);
     L.off_b = (uint32_t)c.stages * L.a_stage_bytes;
-    L.off_staging = L.off_b + (uint32_t)c.stages * L.b_stage_bytes;
+    L.off_sf = L.off_b + (uint32_t)c.stages * L.b_stage_bytes;
+    L.off_staging = L.off_sf + (((uint32_t)c.stages * L.sf_stage_bytes + 1023u) & ~1023u);
     L.off_bar = L.off_staging + L.staging_total;
     L.smem_total = L.off_bar + (uint32_t)kAuxSmem;
     L.acc_cols = (uint32_t)((pair ? 1 : c.bm / 128) * c.bn);
-    L.n_acc = (2 * L.acc_cols <= (uint32_t)kTmemColumns) ? 2u : 1u;
-    uint32_t need = L.acc_cols * L.n_acc, cols = 32;
+    const uint32_t sc_total = (uint32_t)c.stages * L.sc_stage_cols;
+    L.n_acc = (2 * L.acc_cols + sc_total <= (uint32_t)kTmemColumns) ? 2u : 1u;
+    L.sc_col0 = L.acc_cols * L.n_acc;
+    uint32_t need = L.sc_col0 + sc_total, cols = 32;
     while (cols < need) cols <<= 1;
     L.tmem_cols = cols;
     return L;
@@ -115,8 +124,9 @@ bool cluster_reduce_fits(const gemm_config &c, int dt)
 
 int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block, int cta_group)
 {
-    const int64_t per = (int64_t)(cta_group == 2 ? 128 + bn / 2 : bm + bn) * bk * elt_bytes(dt);
-    const int64_t room = smem_per_block - staging_bytes(dt, swap_ab) - kAuxSmem;
+    const int64_t mx = dt == GEMM_MXFP8_E4M3 ? (int64_t)(bm / 128 + bn / 128) * (bk / 128) * kMxAtomBytes : 0;
+    const int64_t per = (int64_t)(cta_group == 2 ? 128 + bn / 2 : bm + bn) * bk * elt_bytes(dt) + mx;
+    const int64_t room = smem_per_block - staging_bytes(dt, swap_ab) - kAuxSmem - (mx ? 1024 : 0);
     int64_t s = room / per;
     if (s < 0) s = 0;
     if (s > kMaxStages) s = kMaxStages;
@@ -127,18 +137,18 @@ const char *reason_text(int r)
 {
     switch (r) {
     case GEMM_FEASIBLE: return "feasible";
-    case GEMM_REASON_CTA_GROUP: return "cta_group must be 1, or 2 with bm = 256 and no swap";
+    case GEMM_REASON_CTA_GROUP: return "cta_group must be 1, or 2 with bm = 256 and no swap (block-scaled FP8: 1)";
     case GEMM_REASON_UMMA_M: return "bm must be 128 or 256 (tcgen05 M per CTA is 128)";
     case GEMM_REASON_UMMA_N: return "bn must be a multiple of 16 in [16, 256]";
     case GEMM_REASON_LAYOUT:
         return "bn must be a multiple of 32 and of the 128-byte span when B is MN-major (a CTA pair: bn/2 a "
-               "multiple of the span)";
-    case GEMM_REASON_BK: return "bk must be 1..4 spans of 128 bytes";
+               "multiple of the span; block-scaled FP8: no swap, bn 128 or 256)";
+    case GEMM_REASON_BK: return "bk must be 1..4 spans of 128 bytes (block-scaled FP8: 128 or 256)";
     case GEMM_REASON_STAGES: return "stages must be in 2..16";
     case GEMM_REASON_SCHEDULE: return "raster must be 0/1 and group one of 1,2,4,8,16";
     case GEMM_REASON_SPLIT_K: return "split_k must be in 1..16 and at most ceil(K/bk)";
     case GEMM_REASON_ALIGN: return "K*elt and N*elt must be multiples of 16 bytes (TMA row stride)";
-    case GEMM_REASON_TMEM: return "one accumulator needs more than 512 TMEM columns";
+    case GEMM_REASON_TMEM: return "one accumulator (block-scaled FP8: plus the scale slots) needs more than 512 TMEM columns";
     case GEMM_REASON_SMEM: return "ring + staging + barriers exceed the shared-memory limit";
     case GEMM_REASON_REGS: return "kernel registers x threads exceed the register file";
     default: return "unknown reason";
@@ -153,7 +163,7 @@ int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_co
     const int e = elt_bytes(dt);
     const int span = span_elems(dt);
     if (c.cta_group != 1 && c.cta_group != 2) return GEMM_REASON_CTA_GROUP;
-    if (c.cta_group == 2 && (c.bm != 256 || c.swap_ab != 0)) return GEMM_REASON_CTA_GROUP;
+    if (c.cta_group == 2 && (c.bm != 256 || c.swap_ab != 0 || dt == GEMM_MXFP8_E4M3)) return GEMM_REASON_CTA_GROUP;
     if (c.bm != 128 && c.bm != 256) return GEMM_REASON_UMMA_M;
     if (c.bn % 16 != 0 || c.bn < 16 || c.bn > 256) return GEMM_REASON_UMMA_N;
     if (c.swap_ab != 0 && c.swap_ab != 1) return GEMM_REASON_LAYOUT;
@@ -162,7 +172,10 @@ int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_co
     const int b_unit = b_in_place(dt, N) ? span : 32;
     if (c.swap_ab == 0 && (c.bn % b_unit != 0 || c.bn % 32 != 0)) return GEMM_REASON_LAYOUT;
     if (c.cta_group == 2 && (c.bn / 2) % b_unit != 0) return GEMM_REASON_LAYOUT;
+    // MX: a tile's B scales are whole 128-column atoms, and the MMA reads them unswapped.
+    if (dt == GEMM_MXFP8_E4M3 && (c.swap_ab != 0 || (c.bn != 128 && c.bn != 256))) return GEMM_REASON_LAYOUT;
     if (c.bk % span != 0 || c.bk / span < 1 || c.bk / span > 4) return GEMM_REASON_BK;
+    if (dt == GEMM_MXFP8_E4M3 && c.bk != 128 && c.bk != 256) return GEMM_REASON_BK;
     if (c.stages < 2 || c.stages > kMaxStages) return GEMM_REASON_STAGES;
     if ((c.raster != 0 && c.raster != 1) ||
         !(c.group == 1 || c.group == 2 || c.group == 4 || c.group == 8 || c.group == 16))
@@ -173,7 +186,7 @@ int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_co
     if ((K * e) % 16 != 0 || (N * out_elt_bytes(dt)) % 16 != 0 || (b_in_place(dt, N) && (N * e) % 16 != 0))
         return GEMM_REASON_ALIGN;
     const Layout L = layout_of(c, dt);
-    if (L.acc_cols > (uint32_t)kTmemColumns) return GEMM_REASON_TMEM;
+    if (L.sc_col0 + (uint32_t)c.stages * L.sc_stage_cols > (uint32_t)kTmemColumns) return GEMM_REASON_TMEM;
     if ((int64_t)L.smem_total > d.smem_per_block) return GEMM_REASON_SMEM;
     if (d.kernel_regs > 0 && (int64_t)d.kernel_regs * d.threads_per_cta > 65536) return GEMM_REASON_REGS;
     return GEMM_FEASIBLE;
@@ -194,7 +207,8 @@ std::vector<gemm_config> enumerate(int64_t M, int64_t N, int64_t K, int dt, int 
         const std::pair<int, int> shapes[] = {{128, 1}, {256, 1}, {256, 2}};
         for (const auto &shape : shapes) {
             const int bm = shape.first, cg = shape.second;
-            if (cg == 2 && swap) continue;
+            if (cg == 2 && (swap || dt == GEMM_MXFP8_E4M3)) continue;
+            if (swap && dt == GEMM_MXFP8_E4M3) continue;
             std::vector<int> bns;
             if (swap) bns = {16, 32, 64, 128, 256};
             else if (cg == 2) bns = dt == GEMM_BF16                          ? std::vector<int>{128, 256}
@@ -203,6 +217,7 @@ std::vector<gemm_config> enumerate(int64_t M, int64_t N, int64_t K, int dt, int 
             else if (dt == GEMM_BF16) bns = {64, 128, 192, 256};
             else if (dt == GEMM_FP8_E4M3) bns = b_in_place(dt, N) ? std::vector<int>{128, 256}
                                                                   : std::vector<int>{64, 128, 192, 256};
+            else if (dt == GEMM_MXFP8_E4M3) bns = {128, 256};
             else bns = {32, 64, 128, 192, 256};
             for (int bn : bns) {
                 for (int bk : {span, 2 * span}) {
@@ -318,7 +333,7 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
     // of the peak, and the issuing warp spends mma_issue_clk per MMA plus
     // kblock_clk per stage; the slower of the two sets the pace.
     const double peak =
-        (dt == GEMM_BF16 ? d.peak_tflops_bf16 : dt == GEMM_FP8_E4M3 ? d.peak_tflops_fp8 : d.peak_tflops_tf32) * 1e12;
+        (dt == GEMM_BF16 ? d.peak_tflops_bf16 : is_fp8(dt) ? d.peak_tflops_fp8 : d.peak_tflops_tf32) * 1e12;
     const double halves = cg == 2 ? 1 : c.bm / 128, ksteps = (double)c.bk * e / 32.0, kslice = 32.0 / e;
     const double mma_flop = 2.0 * 128.0 * c.bn * kslice;
     const double t_exec = halves * ksteps * mma_flop / (peak / (double)sms);
@@ -327,13 +342,16 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
 
     // L2 -> shared memory: every unit streams (bm + bn)·bk·elt bytes per K-block
     // ("Tile Selection": per-block panel traffic; reuse across blocks is in L2).
-    const double l2_bytes = (double)cta_units * (double)kbu * (double)(rows_cta + bcols_cta) * (double)c.bk * e;
+    // (MX: plus 4 scale bytes per row and column per 128 K.)
+    const double sf_per_k = dt == GEMM_MXFP8_E4M3 ? 4.0 / 128.0 : 0.0;
+    const double l2_bytes =
+        (double)cta_units * (double)kbu * (double)(rows_cta + bcols_cta) * (double)c.bk * (e + sf_per_k);
     const double t_l2 = l2_bytes / (d.l2_gbs * 1e9);
 
     // HBM: operands either fit in half of L2 (threshold regime: compulsory bytes
     // only) or are re-read once per wave of concurrent tiles, with the wave's
     // footprint shaped by the tile order (group-G band).
-    const double in_bytes = ((double)M * K + (double)K * N) * e;
+    const double in_bytes = ((double)M * K + (double)K * N) * (e + sf_per_k);
     const int64_t wave_tiles = std::min<int64_t>(tiles, std::max<int64_t>(1, ctas / cg / S));
     int64_t rows_w, cols_w;
     if (c.raster == 0) {
@@ -344,7 +362,7 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
         rows_w = std::min<int64_t>(cdiv(wave_tiles, cols_w), tiles_m);
     }
     const double panel = ((double)tiles / (double)wave_tiles) * (double)K *
-                         ((double)rows_w * c.bm + (double)cols_w * c.bn) * e;
+                         ((double)rows_w * c.bm + (double)cols_w * c.bn) * (e + sf_per_k);
     const double operand = (in_bytes <= (double)d.l2_bytes / 2.0) ? in_bytes : std::max(in_bytes, panel);
     // C, bias, and the residual R of the "+ R" epilogues.
     const double eo = out_elt_bytes(dt);
@@ -367,7 +385,7 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
         // Double-buffered accumulators hide the epilogue behind the next unit's
         // main loop unless it is the slower of the two.
         const double epi_t = elems / rate;
-        const bool two_acc = 2.0 * halves * c.bn <= (double)kTmemColumns;
+        const bool two_acc = layout_of(c, dt).n_acc == 2;
         const double main_unit = t_main / (double)upc;
         exposed = epi_t + (double)(upc - 1) * (two_acc ? std::max(0.0, epi_t - main_unit) : epi_t);
         t_split = 0.0;

@@ -72,7 +72,7 @@ static int encode_2d(CUtensorMap *m, int dt, const void *ptr, uint64_t inner, ui
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType t = dt == GEMM_BF16       ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                  : dt == GEMM_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                  : is_fp8(dt)          ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     CUresult r = g_encode(m, t, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -195,8 +195,7 @@ static int configure_smem_limit(int dt, int64_t bytes)
 
 static bool valid_enums(int dt, int epi)
 {
-    return (dt == GEMM_BF16 || dt == GEMM_FP32_TF32 || dt == GEMM_FP8_E4M3) && epi >= GEMM_EPI_NONE &&
-           epi <= GEMM_EPI_BIAS_GELU_RESIDUAL;
+    return dt >= GEMM_BF16 && dt <= GEMM_MXFP8_E4M3 && epi >= GEMM_EPI_NONE && epi <= GEMM_EPI_BIAS_GELU_RESIDUAL;
 }
 
 // Residual epilogues are the bias / ReLU / GELU ones followed by "+ R".
@@ -265,16 +264,28 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     // MMA-A when swapped and MMA-B otherwise; A is always K-major.
     k.a_mn_major = (cfg.swap_ab && !p->b_kmajor) ? 1 : 0;
     k.b_mn_major = (!cfg.swap_ab && !p->b_kmajor) ? 1 : 0;
-    // Operand formats: BF16 = 1 of kind::f16, TF32 = 2 of kind::tf32, E4M3 = 0 of kind::f8f6f4.
+    // Operand formats: BF16 = 1 of kind::f16, TF32 = 2 of kind::tf32, E4M3 = 0 of kind::f8f6f4
+    // and of kind::mxf8f6f4.
     const uint32_t fmt = dt == GEMM_BF16 ? 1u : dt == GEMM_FP32_TF32 ? 2u : 0u;
     k.pair = cfg.cta_group == 2 ? 1 : 0;
     k.alpha = 1.0f;
     const uint32_t mma_m = k.pair ? 256u : 128u;  // a pair's MMA spans both CTAs' 128 rows
-    k.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)k.a_mn_major << 15) |
+    // Instruction descriptor: bits 4-5 the accumulator format (fp32 = 1), 7-9 and
+    // 10-12 A's and B's formats, 15 and 16 their majorness, 17-22 N/8, 24-28 M/16.
+    // The block-scaled kind has an fp32 accumulator implied and uses bits 4-5
+    // (and 29-30) for B's (A's) scale ID, set per MMA; bit 23 = 1 names the
+    // scales E8M0.
+    const bool mx = dt == GEMM_MXFP8_E4M3;
+    k.idesc = (mx ? (1u << 23) : (1u << 4)) | (fmt << 7) | (fmt << 10) | ((uint32_t)k.a_mn_major << 15) |
               ((uint32_t)k.b_mn_major << 16) | ((uint32_t)(cfg.bn >> 3) << 17) | ((mma_m >> 4) << 24);
     k.a_stage_bytes = p->L.a_stage_bytes;
     k.b_stage_bytes = p->L.b_stage_bytes;
-    k.tx_bytes = p->L.stage_bytes;
+    k.tx_bytes = p->L.stage_bytes + p->L.sf_stage_bytes;
+    k.sf_kt = mx ? (int32_t)mx_k_atoms(K) : 0;
+    k.sf_stage_bytes = p->L.sf_stage_bytes;
+    k.off_sf = p->L.off_sf;
+    k.sc_stage_cols = p->L.sc_stage_cols;
+    k.sc_col0 = p->L.sc_col0;
     k.a_lbo = k.a_mn_major ? (uint32_t)(cfg.bk * 128) : 16u;
     k.b_lbo = k.b_mn_major ? (uint32_t)(cfg.bk * 128) : 16u;
     k.acc_cols = p->L.acc_cols;
@@ -448,7 +459,7 @@ static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const
         }
     }
     if (!rc) {
-        const int odt = dt == GEMM_FP8_E4M3 ? GEMM_BF16 : dt;   // C's type
+        const int odt = is_fp8(dt) ? GEMM_BF16 : dt;   // C's type
         if (!c.swap_ab)
             rc = encode_2d(&d.mc, odt, C, p->N, p->M, 32, 32,
                            odt == GEMM_BF16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
@@ -468,10 +479,16 @@ static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-int run_plan_ex(gemm_plan_t p, const void *A, const void *B, const void *bias, const void *R, void *C,
-                cudaStream_t stream)
+int run_plan_mx(gemm_plan_t p, const void *A, const void *SA, const void *B, const void *SB, const void *bias,
+                const void *R, void *C, cudaStream_t stream)
 {
     if (!p) return set_error(GEMM_ERR_INVALID_ARG, "null plan");
+    const bool mx = p->dt == GEMM_MXFP8_E4M3;
+    if (mx && p->K > 0 && (!SA || !SB))
+        return set_error(GEMM_ERR_INVALID_ARG, "a block-scaled FP8 plan runs through gemm_run_mx, with both scales");
+    if (!mx && (SA || SB)) return set_error(GEMM_ERR_INVALID_ARG, "scales given to a plan that is not block-scaled");
+    if (mx && p->K > 0 && (!aligned16(SA) || !aligned16(SB)))
+        return set_error(GEMM_ERR_MISALIGNED, "SA and SB must be 16-byte aligned");
     if (has_residual(p->epi) && !R)
         return set_error(GEMM_ERR_INVALID_ARG, "the residual epilogue needs R (gemm_run_ex)");
     if (!has_residual(p->epi) && R)
@@ -496,6 +513,8 @@ int run_plan_ex(gemm_plan_t p, const void *A, const void *B, const void *bias, c
     KernelParams kp = p->kp;
     kp.bias = p->epi != GEMM_EPI_NONE ? bias : nullptr;
     kp.residual = R;
+    kp.sfa = static_cast<const uint8_t *>(SA);
+    kp.sfb = static_cast<const uint8_t *>(SB);
     kp.timeout_ns = g_timeout_ns.load();
     kp.debug_stall = g_debug_stall.load();
     cudaError_t e = launch_gemm(p->dt, d->ma, d->mb, d->mc, kp, p->grid, p->smem_request, stream);
@@ -503,9 +522,27 @@ int run_plan_ex(gemm_plan_t p, const void *A, const void *B, const void *bias, c
     return GEMM_OK;
 }
 
+int run_plan_ex(gemm_plan_t p, const void *A, const void *B, const void *bias, const void *R, void *C,
+                cudaStream_t stream)
+{
+    return run_plan_mx(p, A, nullptr, B, nullptr, bias, R, C, stream);
+}
+
 int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream)
 {
     return run_plan_ex(p, A, B, bias, nullptr, C, stream);
+}
+
+int mx_pack_scales(const void *scales, int64_t rows, int64_t K, int b_side, void *packed, cudaStream_t stream)
+{
+    if (rows < 0 || K < 0) return set_error(GEMM_ERR_INVALID_ARG, "negative extent");
+    if (b_side != 0 && b_side != 1) return set_error(GEMM_ERR_INVALID_ARG, "b_side must be 0 (A) or 1 (B)");
+    if (rows == 0 || K == 0) return GEMM_OK;
+    if (!scales || !packed) return set_error(GEMM_ERR_INVALID_ARG, "null scales or packed buffer");
+    cudaError_t e = launch_mx_pack(static_cast<const uint8_t *>(scales), rows, K, b_side,
+                                   static_cast<uint8_t *>(packed), stream);
+    if (e != cudaSuccess) return cuda_err(e, "MX scale packing launch");
+    return GEMM_OK;
 }
 
 int plan_set_scale(gemm_plan_t p, float alpha)
@@ -592,11 +629,11 @@ int run_host(gemm_plan_t p, const void *A, const void *B, const void *bias, void
 // ---------------------------------------------------------------------------
 
 struct TuneBuffers {
-    std::vector<void *> A, B, bias, C;
+    std::vector<void *> A, B, bias, C, SA, SB;   // SA, SB: packed MX scales (block-scaled FP8 only)
     float *ws = nullptr;
     ~TuneBuffers()
     {
-        for (auto *v : {&A, &B, &bias, &C})
+        for (auto *v : {&A, &B, &bias, &C, &SA, &SB})
             for (void *p : *v) cudaFree(p);
         cudaFree(ws);
     }
@@ -705,10 +742,13 @@ int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, u
     // Library-owned buffers, rotated so that shapes smaller than L2 are timed
     // from HBM like the real, larger working set.
     const size_t e = (size_t)elt_bytes(dt), eo = (size_t)out_elt_bytes(dt);
-    const int odt = dt == GEMM_FP8_E4M3 ? GEMM_BF16 : dt;   // type of bias and C
+    const int odt = is_fp8(dt) ? GEMM_BF16 : dt;   // type of bias and C
+    const bool mx = dt == GEMM_MXFP8_E4M3;
+    const size_t bytes_sa = mx ? (size_t)std::max<int64_t>(mx_row_atoms(M) * mx_k_atoms(K) * kMxAtomBytes, 16) : 0,
+                 bytes_sb = mx ? (size_t)std::max<int64_t>(mx_row_atoms(N) * mx_k_atoms(K) * kMxAtomBytes, 16) : 0;
     const size_t bytes_a = (size_t)std::max<int64_t>(M * K, 1) * e, bytes_b = (size_t)std::max<int64_t>(K * N, 1) * e,
                  bytes_bias = (size_t)std::max<int64_t>(N, 1) * eo, bytes_c = (size_t)std::max<int64_t>(M * N, 1) * eo;
-    const size_t set_bytes = bytes_a + bytes_b + bytes_bias + bytes_c;
+    const size_t set_bytes = bytes_a + bytes_b + bytes_bias + bytes_c + bytes_sa + bytes_sb;
     int nsets = (int)std::min<int64_t>(8, std::max<int64_t>(1, cdiv(2 * dev.l2_bytes + (int64_t)set_bytes, set_bytes)));
     TuneBuffers buf;
     cudaStream_t stream = nullptr;
@@ -732,6 +772,16 @@ int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, u
         launch_fill_uniform(a, (int64_t)(bytes_a / e), dt, scale_ab, 0x1234u + 17u * s, stream);
         launch_fill_uniform(b, (int64_t)(bytes_b / e), dt, scale_ab, 0x5678u + 17u * s, stream);
         launch_fill_uniform(bb, (int64_t)(bytes_bias / eo), odt, 0.1f, 0x9ABCu + 17u * s, stream);
+        if (mx) {
+            // Packed scales of 2^0 (E8M0 127): the timing does not depend on their values.
+            void *sa = nullptr, *sb = nullptr;
+            if ((err = cudaMalloc(&sa, bytes_sa)) != cudaSuccess) return cuda_err(err, "cudaMalloc(tuning SA)");
+            buf.SA.push_back(sa);
+            if ((err = cudaMalloc(&sb, bytes_sb)) != cudaSuccess) return cuda_err(err, "cudaMalloc(tuning SB)");
+            buf.SB.push_back(sb);
+            cudaMemsetAsync(sa, 127, bytes_sa, stream);
+            cudaMemsetAsync(sb, 127, bytes_sb, stream);
+        }
     }
     size_t ws_bytes = 0;
     for (int i : meas) ws_bytes = std::max(ws_bytes, split_ws_bytes(M, N, cands[i]));
@@ -751,8 +801,9 @@ int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, u
     }
     // (A residual epilogue is timed in place: R = C.)
     auto run_one = [&](int j, int set) {
-        return run_plan_ex(plans[j], buf.A[set], buf.B[set], epi != GEMM_EPI_NONE ? buf.bias[set] : nullptr,
-                           has_residual(epi) ? buf.C[set] : nullptr, buf.C[set], stream);
+        return run_plan_mx(plans[j], buf.A[set], mx ? buf.SA[set] : nullptr, buf.B[set], mx ? buf.SB[set] : nullptr,
+                           epi != GEMM_EPI_NONE ? buf.bias[set] : nullptr, has_residual(epi) ? buf.C[set] : nullptr,
+                           buf.C[set], stream);
     };
     // Warm-up and a first estimate of each candidate's time.
     cudaEvent_t e0, e1;

@@ -39,6 +39,15 @@
  *     R and C are bfloat16; the product's scale (the operands' tensor scales)
  *     is gemm_plan_set_scale's alpha.  B is read MN-major in place (as bf16)
  *     when N is a multiple of 16, else from a K-major copy (as fp32).
+ *     GEMM_MXFP8_E4M3: block-scaled FP8 in the OCP Microscaling (MX) format
+ *     (OCP "Microscaling Formats (MX) Specification" v1.0, MXFP8 E4M3): A and B
+ *     are E4M3 bytes as above, and every run of 32 consecutive elements along K
+ *     shares one power-of-two scale, an E8M0 byte s meaning 2^(s-127) (255 is
+ *     NaN).  C[m,n] = act(alpha·sum_k (A[m,k]·2^(SA[m,k/32]-127))·
+ *     (B[k,n]·2^(SB[k/32,n]-127)) + bias[n]) (+ R), read by tcgen05.mma
+ *     kind::mxf8f6f4.block_scale with the scales in tensor memory.  The
+ *     scales reach the kernel packed by gemm_mx_pack_scales (below); runs go
+ *     through gemm_run_mx.  bias, R and C are bfloat16.
  *   - GELU is the erf form 0.5·x·(1 + erf(x/√2)).
  *   - Device pointers are caller-owned, must stay valid until the work queued
  *     on the stream has finished, and must be 16-byte aligned; K·elt and N·elt
@@ -74,7 +83,7 @@ typedef enum {
     GEMM_ERR_NO_DEVICE = -7     /* no CUDA device is visible */
 } gemm_status;
 
-typedef enum { GEMM_BF16 = 0, GEMM_FP32_TF32 = 1, GEMM_FP8_E4M3 = 2 } gemm_dtype;
+typedef enum { GEMM_BF16 = 0, GEMM_FP32_TF32 = 1, GEMM_FP8_E4M3 = 2, GEMM_MXFP8_E4M3 = 3 } gemm_dtype;
 
 typedef enum {
     GEMM_EPI_NONE = 0,       /* C = A·B                 (bias may be NULL) */
@@ -106,9 +115,13 @@ typedef enum {
  *             1: a band of `group` tile-columns row by row
  *   group     1, 2, 4, 8 or 16
  *   split_k   1..16 slices of K; partial fp32 tiles are summed in slice order
- *             (deterministic) by the last slice to finish
- *   cta_group 1 (2-SM pairs are not offered yet)
+ *             (deterministic: every exchange route gives the same bits)
+ *   cta_group 1, or 2: a 256-row tile on a CTA pair (tcgen05 cta_group::2;
+ *             bm = 256, no swap; each CTA holds 128 rows and half of B)
  *   swap_ab   0 or 1, as above
+ * Block-scaled FP8 (GEMM_MXFP8_E4M3) adds: cta_group 1, swap_ab 0, bn 128 or
+ * 256, bk 128 or 256, and the accumulators plus one TMEM slot of scales per
+ * stage within 512 columns.
  */
 typedef struct {
     int32_t bm, bn, bk, stages, raster, group, split_k, cta_group, swap_ab;
@@ -117,16 +130,17 @@ typedef struct {
 /* Reason codes of gemm_check_config (first rule broken, in this order). */
 typedef enum {
     GEMM_FEASIBLE = 0,
-    GEMM_REASON_CTA_GROUP = 1,  /* cta_group != 1 */
+    GEMM_REASON_CTA_GROUP = 1,  /* cta_group not 1, or 2 with bm = 256 and no swap (MX: 1) */
     GEMM_REASON_UMMA_M = 2,     /* bm not 128/256 (tcgen05 M per CTA is 128) */
     GEMM_REASON_UMMA_N = 3,     /* bn not a multiple of 16 in [16, 256] */
-    GEMM_REASON_LAYOUT = 4,     /* swap_ab not 0/1; bn not a multiple of 32 and of the span when unswapped */
-    GEMM_REASON_BK = 5,         /* bk not 1..4 spans of 128 bytes */
+    GEMM_REASON_LAYOUT = 4,     /* swap_ab not 0/1; bn not a multiple of 32 and of the span when unswapped
+                                   (MX: swap_ab 1, or bn not 128/256) */
+    GEMM_REASON_BK = 5,         /* bk not 1..4 spans of 128 bytes (MX: not 128/256) */
     GEMM_REASON_STAGES = 6,     /* stages outside 2..16 */
     GEMM_REASON_SCHEDULE = 7,   /* raster not 0/1 or group not in {1,2,4,8,16} */
     GEMM_REASON_SPLIT_K = 8,    /* split_k outside 1..16 or above ceil(K/bk) */
     GEMM_REASON_ALIGN = 9,      /* K·elt or N·elt not a multiple of 16 bytes */
-    GEMM_REASON_TMEM = 10,      /* one accumulator needs more than 512 TMEM columns */
+    GEMM_REASON_TMEM = 10,      /* one accumulator (MX: plus the scale slots) needs more than 512 TMEM columns */
     GEMM_REASON_SMEM = 11,      /* ring + epilogue staging + barriers exceed the per-block limit */
     GEMM_REASON_REGS = 12       /* kernel registers × 320 threads exceed 65,536 */
 } gemm_reason;
@@ -321,6 +335,34 @@ int gemm_run(gemm_plan_t plan, const void *A, const void *B, const void *bias, v
  * GEMM_ERR_INVALID_ARG.  Asynchronous on `stream`. */
 int gemm_run_ex(gemm_plan_t plan, const void *A, const void *B, const void *bias, const void *R, void *C,
                 gemm_stream_t stream);
+
+/* Block-scaled FP8 (GEMM_MXFP8_E4M3 plans, which gemm_run and gemm_run_ex
+ * reject): as gemm_run_ex, plus SA and SB, the device pointers of A's and B's
+ * scales in the packed layout that gemm_mx_pack_scales writes
+ * (gemm_mx_scales_bytes(M, K) and gemm_mx_scales_bytes(N, K) bytes, 16-byte
+ * aligned).  R is required exactly for the residual epilogues.  Asynchronous
+ * on `stream`. */
+int gemm_run_mx(gemm_plan_t plan, const void *A, const void *SA, const void *B, const void *SB, const void *bias,
+                const void *R, void *C, gemm_stream_t stream);
+
+/* Bytes of one operand's packed MX scales: the operand's `rows` (M for A, N
+ * for B) padded to a multiple of 256 and K padded to a multiple of 256, in
+ * atoms of 128 rows x 128 K (512 bytes, four 32-element blocks per row).
+ * Returns 0 for a negative extent. */
+int64_t gemm_mx_scales_bytes(int64_t rows, int64_t K);
+
+/* Pack one operand's E8M0 scales for gemm_run_mx (asynchronous on `stream`).
+ * `scales` is a device pointer to the natural layout: for A (b_side = 0)
+ * [rows, ceil(K/32)] row-major (SA[m, j] scales A[m, 32j .. 32j+31]); for B
+ * (b_side = 1) [ceil(K/32), rows] row-major (SB[j, n] scales B[32j .. 32j+31,
+ * n]).  `packed` receives gemm_mx_scales_bytes(rows, K) bytes: for row r and
+ * block j, atom (r/128, j/4) at byte offset ((r/128)·KT + j/4)·512 (KT the
+ * padded K over 128), and within it byte (r%32)·16 + ((r%128)/32)·4 + j%4, the
+ * order in which tcgen05.cp 32x128b.warpx4 hands a 128-row block's scales to
+ * the block-scaled MMA.  Padding bytes are 0 (2^-127; they meet only the zero
+ * fill of out-of-range operand elements). */
+int gemm_mx_pack_scales(const void *scales, int64_t rows, int64_t K, int32_t b_side, void *packed,
+                        gemm_stream_t stream);
 
 /* Same product from HOST buffers (epilogues without residual): copies A, B, bias to plan-owned device
  * buffers, runs, copies C back, and synchronises `stream` before returning.

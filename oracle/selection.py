@@ -213,7 +213,7 @@ def workshop_sweep(M, N, K, dev: WorkshopDevice = WorkshopDevice()):
 # the pages, which say nothing about TMEM/tcgen05; pinned by brute force).
 # ---------------------------------------------------------------------------
 
-DT_BF16, DT_FP32, DT_FP8 = 0, 1, 2
+DT_BF16, DT_FP32, DT_FP8, DT_MXFP8 = 0, 1, 2, 3
 EPI_NONE, EPI_BIAS, EPI_RELU, EPI_GELU = 0, 1, 2, 3
 EPI_BIAS_RES, EPI_RELU_RES, EPI_GELU_RES = 4, 5, 6   # the same plus a residual R
 
@@ -270,15 +270,31 @@ class Device:
     extra: dict = field(default_factory=dict)
 
 
+def is_fp8(dtype):
+    """FP8 E4M3 operands, with one tensor scale or block-scaled (MX)."""
+    return dtype in (DT_FP8, DT_MXFP8)
+
+
 def elt_bytes(dtype):
-    """Operand element size: bf16 2, FP8 E4M3 1, fp32 4."""
-    return 2 if dtype == DT_BF16 else 1 if dtype == DT_FP8 else 4
+    """Operand element size: bf16 2, FP8 E4M3 (plain or MX) 1, fp32 4."""
+    return 2 if dtype == DT_BF16 else 1 if is_fp8(dtype) else 4
 
 
 def b_in_place(dtype, N):
     """B read MN-major in place: bf16 always, FP8 when its rows (N bytes) meet
     the 16-byte stride rule; otherwise from a K-major copy (fp32 always)."""
-    return dtype == DT_BF16 or (dtype == DT_FP8 and N % 16 == 0)
+    return dtype == DT_BF16 or (is_fp8(dtype) and N % 16 == 0)
+
+
+MX_ATOM_BYTES = 512     # 128 rows x four 32-element scale blocks
+
+
+def mx_atoms(cfg: Config, dtype):
+    """Scale atoms one MX stage stages: A's bm/128 row atoms and B's bn/128
+    column atoms, bk/128 of each along K (zero for other dtypes)."""
+    if dtype != DT_MXFP8:
+        return 0
+    return (cfg.bm // 128 + cfg.bn // 128) * (cfg.bk // 128)
 
 
 def out_elt_bytes(dtype):
@@ -312,21 +328,28 @@ def stage_bytes(cfg: Config, dtype):
 
 
 def smem_bytes(cfg: Config, dtype):
-    return cfg.stages * stage_bytes(cfg, dtype) + staging_bytes(dtype, cfg.swap_ab) + AUX_SMEM
+    """Ring (operands, then the MX scale atoms rounded up to 1 KB) + epilogue
+    staging + barriers."""
+    scales = cfg.stages * mx_atoms(cfg, dtype) * MX_ATOM_BYTES
+    scales = -(-scales // 1024) * 1024
+    return cfg.stages * stage_bytes(cfg, dtype) + scales + staging_bytes(dtype, cfg.swap_ab) + AUX_SMEM
 
 
 def max_stages(bm, bn, bk, dtype, swap_ab, smem_per_block, cta_group=1):
-    per = ((128 + bn // 2) if cta_group == 2 else (bm + bn)) * bk * elt_bytes(dtype)
-    room = smem_per_block - staging_bytes(dtype, swap_ab) - AUX_SMEM
+    mx = (bm // 128 + bn // 128) * (bk // 128) * MX_ATOM_BYTES if dtype == DT_MXFP8 else 0
+    per = ((128 + bn // 2) if cta_group == 2 else (bm + bn)) * bk * elt_bytes(dtype) + mx
+    room = smem_per_block - staging_bytes(dtype, swap_ab) - AUX_SMEM - (1024 if mx else 0)
     return max(0, min(MAX_STAGES, room // per))
 
 
-def tmem_columns(cfg: Config):
+def tmem_columns(cfg: Config, dtype=None):
     """Columns of one accumulator (fp32, one column per output column per 128
-    rows) and how many accumulators fit (2 = epilogue overlaps the next tile)."""
+    rows), how many accumulators fit (2 = epilogue overlaps the next tile), and
+    the MX scale columns (4 per atom, one slot per stage) that share the 512."""
     acc = (1 if cfg.cta_group == 2 else cfg.bm // 128) * cfg.bn
-    nbuf = 2 if 2 * acc <= TMEM_COLUMNS else 1
-    return acc, nbuf
+    scales = cfg.stages * 4 * mx_atoms(cfg, dtype)
+    nbuf = 2 if 2 * acc + scales <= TMEM_COLUMNS else 1
+    return acc, nbuf, scales
 
 
 def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
@@ -335,7 +358,7 @@ def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
     span = span_elems(dtype)
     if cfg.cta_group not in (1, 2):
         return R_CTA_GROUP
-    if cfg.cta_group == 2 and (cfg.bm != 256 or cfg.swap_ab != 0):
+    if cfg.cta_group == 2 and (cfg.bm != 256 or cfg.swap_ab != 0 or dtype == DT_MXFP8):
         return R_CTA_GROUP
     if cfg.bm not in (128, 256):
         return R_UMMA_M
@@ -350,7 +373,11 @@ def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
         return R_LAYOUT
     if cfg.cta_group == 2 and (cfg.bn // 2) % b_unit != 0:
         return R_LAYOUT
+    if dtype == DT_MXFP8 and (cfg.swap_ab != 0 or cfg.bn not in (128, 256)):
+        return R_LAYOUT
     if cfg.bk % span != 0 or not (1 <= cfg.bk // span <= 4):
+        return R_BK
+    if dtype == DT_MXFP8 and cfg.bk not in (128, 256):
         return R_BK
     if not (2 <= cfg.stages <= MAX_STAGES):
         return R_STAGES
@@ -362,8 +389,8 @@ def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
     if (K * elt) % 16 != 0 or (N * out_elt_bytes(dtype)) % 16 != 0 or \
             (b_in_place(dtype, N) and (N * elt) % 16 != 0):
         return R_ALIGN
-    acc, _nbuf = tmem_columns(cfg)
-    if acc > TMEM_COLUMNS:
+    acc, nbuf, scales = tmem_columns(cfg, dtype)
+    if acc * nbuf + scales > TMEM_COLUMNS:
         return R_TMEM
     if smem_bytes(cfg, dtype) > dev.smem_per_block:
         return R_SMEM
@@ -383,7 +410,9 @@ def gb300_candidates(M, N, K, dtype, epi, dev: Device):
     for swap in swaps:
         rows, cols = (N, M) if swap else (M, N)
         for bm, cg in ((128, 1), (256, 1), (256, 2)):
-            if cg == 2 and swap:
+            if cg == 2 and (swap or dtype == DT_MXFP8):
+                continue
+            if swap and dtype == DT_MXFP8:
                 continue
             if swap:
                 bns = (16, 32, 64, 128, 256)
@@ -394,6 +423,8 @@ def gb300_candidates(M, N, K, dtype, epi, dev: Device):
                 bns = (64, 128, 192, 256)
             elif dtype == DT_FP8:
                 bns = (128, 256) if b_in_place(dtype, N) else (64, 128, 192, 256)
+            elif dtype == DT_MXFP8:
+                bns = (128, 256)
             else:
                 bns = (32, 64, 128, 192, 256)
             for bn in bns:
@@ -500,7 +531,7 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
     flops = 2.0 * M * N * K
 
     peak = (dev.peak_tflops_bf16 if dtype == DT_BF16 else
-            dev.peak_tflops_fp8 if dtype == DT_FP8 else dev.peak_tflops_tf32) * 1e12
+            dev.peak_tflops_fp8 if is_fp8(dtype) else dev.peak_tflops_tf32) * 1e12
     halves = 1 if cg == 2 else cfg.bm // 128
     ksteps = cfg.bk * elt / 32
     one_mma = 2.0 * 128 * cfg.bn * (32 / elt)
@@ -508,10 +539,12 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
     issue = (halves * ksteps * dev.mma_issue_clk + dev.kblock_clk) / clock
     mma_s = per_cta_units * slice_kb * max(execute, issue)
 
-    l2_bytes = cta_units * slice_kb * (rows_cta + bcols_cta) * cfg.bk * elt
+    # MX scales add 4 bytes per row (and per column) for every 128 of K.
+    per_k = elt + (4 / 128 if dtype == DT_MXFP8 else 0.0)
+    l2_bytes = cta_units * slice_kb * (rows_cta + bcols_cta) * cfg.bk * per_k
     l2_s = l2_bytes / (dev.l2_gbs * 1e9)
 
-    in_bytes = (M * K + K * N) * elt
+    in_bytes = (M * K + K * N) * per_k
     wave_tiles = min(tiles, max(1, ctas // cg // S))
     if cfg.raster == 0:
         rows_w = min(cfg.group, tiles_m, wave_tiles)
@@ -519,7 +552,7 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
     else:
         cols_w = min(cfg.group, tiles_n, wave_tiles)
         rows_w = min(ceil_div(wave_tiles, cols_w), tiles_m)
-    panel = (tiles / wave_tiles) * K * (rows_w * cfg.bm + cols_w * cfg.bn) * elt
+    panel = (tiles / wave_tiles) * K * (rows_w * cfg.bm + cols_w * cfg.bn) * per_k
     operand = in_bytes if in_bytes <= dev.l2_bytes / 2 else max(in_bytes, panel)
     eo = out_elt_bytes(dtype)
     hbm = (operand + M * N * eo + (N * eo if epi != EPI_NONE else 0)
@@ -535,7 +568,7 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
     partial = elems * 4
     if S == 1:
         one = elems / rate
-        two_buffers = 2 * halves * cfg.bn <= TMEM_COLUMNS
+        two_buffers = tmem_columns(cfg, dtype)[1] == 2
         unit_main = main / per_cta_units
         hidden_excess = max(0.0, one - unit_main) if two_buffers else one
         epi_s = one + (per_cta_units - 1) * hidden_excess

@@ -36,13 +36,16 @@ SHAPES = [(256, 256, 256, 1, 2), (1000, 1000, 8192, 0, 3), (8192, 8192, 8192, 0,
           (1, 8, 8, 0, 0), (300, 200, 72, 0, 2), (64, 64, 0, 0, 1),
           # FP8 E4M3 operands (bf16 C): K-major copy of B, 128-byte spans of 128 elements
           (1000, 1000, 8192, 2, 3), (8192, 8192, 8192, 2, 2), (16, 28672, 8192, 2, 0), (300, 200, 128, 2, 2),
-          (512, 1024, 4096, 2, 6), (100, 104, 48, 2, 1)]
+          (512, 1024, 4096, 2, 6), (100, 104, 48, 2, 1),
+          # block-scaled FP8 (MX): no swap, no pairs, bn 128/256, bk 128/256, scale slots in TMEM
+          (1000, 1000, 8192, 3, 3), (8192, 8192, 8192, 3, 2), (16, 28672, 8192, 3, 0), (300, 200, 128, 3, 2),
+          (512, 1024, 4096, 3, 6), (100, 104, 48, 3, 1)]
 
 
 def test_library_exports_every_declared_symbol():
     with open(os.path.join(ROOT, "include", "gemm_gb300.h")) as f:
         header = f.read()
-    declared = set(re.findall(r"^(?:const\s+)?(?:int|void|char)\s*\*?\s*(gemm_[a-z_]+)\s*\(",
+    declared = set(re.findall(r"^(?:const\s+)?(?:int64_t|int|void|char)\s*\*?\s*(gemm_[a-z_]+)\s*\(",
                               header, flags=re.M))
     assert declared == set(g.EXPORTS)
     L = g.lib()
@@ -85,7 +88,8 @@ def test_check_config_equals_oracle_on_a_grid():
         (1, 2, 3, 8, 16, 17), (0, 1, 2), (1, 3, 4, 16), (1, 2, 16, 17), (1, 2), (0, 1, 2)))
     sample = rng.sample(grid, 6000)
     for (M, N, K, dt) in [(1000, 1000, 8192, 0), (256, 256, 256, 1), (16, 28672, 8192, 0), (100, 36, 12, 0),
-                          (100, 36, 12, 1), (5, 5, 5, 1)]:
+                          (100, 36, 12, 1), (5, 5, 5, 1), (1000, 1008, 8192, 3), (16, 28672, 8192, 3),
+                          (100, 104, 48, 3)]:
         for t in sample:
             c = g.make_config(*t)
             assert g.check_config(M, N, K, dt, 2, c, d) == sel.gb300_check(M, N, K, dt, 2, sel.Config(*t), od), (M, N, K, dt, t)
