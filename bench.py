@@ -83,25 +83,34 @@ def load_peaks():
 
 def elt_sizes(dtype):
     """(operand bytes, bytes of C and bias): FP8 operands give a bf16 C."""
-    return {"bf16": (2, 2), "fp8": (1, 2)}.get(dtype, (4, 4))
+    return {"bf16": (2, 2), "fp8": (1, 2), "mxfp8": (1, 2)}.get(dtype, (4, 4))
 
 
 def peak_ratio(dtype):
     """Dense tensor peak of `dtype` relative to bf16 (the nominal ratios:
-    tf32 1.1, bf16 2.25, fp8 4.5 PFLOP/s)."""
-    return {"bf16": 1.0, "fp8": 2.0}.get(dtype, 0.5)
+    tf32 1.1, bf16 2.25, fp8 4.5 PFLOP/s; block-scaled FP8 runs at the FP8 rate)."""
+    return {"bf16": 1.0, "fp8": 2.0, "mxfp8": 2.0}.get(dtype, 0.5)
+
+
+def scale_bytes_of(w):
+    """Block-scaled FP8: one E8M0 byte per 32 elements of K, for A and for B."""
+    if w.dtype != "mxfp8":
+        return 0
+    kb = (w.K + 31) // 32
+    return (w.M + w.N) * kb
 
 
 def work_of(w):
     elt, eo = elt_sizes(w.dtype)
     flops = 2.0 * w.M * w.N * w.K
-    bytes_ = (w.M * w.K + w.K * w.N) * elt + (w.N * eo if w.epi != "none" else 0) + w.M * w.N * eo
+    bytes_ = (w.M * w.K + w.K * w.N) * elt + scale_bytes_of(w) + (w.N * eo if w.epi != "none" else 0) + \
+        w.M * w.N * eo
     return flops, bytes_, elt
 
 
 def set_bytes_of(w):
     elt, eo = elt_sizes(w.dtype)
-    return (w.M * w.K + w.K * w.N) * elt + (w.N + w.M * w.N) * eo
+    return (w.M * w.K + w.K * w.N) * elt + scale_bytes_of(w) + (w.N + w.M * w.N) * eo
 
 
 # ---------------------------------------------------------------------------
@@ -181,24 +190,36 @@ class ClockSampler:
 # CPU oracle (rank 0, N = 1 only) — the reported CPU baseline
 # ---------------------------------------------------------------------------
 
+def oracle_slab(w, threads):
+    """The oracle of workload w as a function of a row count (the first rows of
+    the product), and the thread count it uses."""
+    from autotuning_tcgen05_tmem_gb300 import inputs
+    from oracle import gemm as og
+    epi = {"none": 0, "bias": 1, "relu": 2, "gelu": 3}[w.epi]
+    if w.dtype == "mxfp8":
+        from oracle import mx
+        A, SA, B, SB, bias = inputs.make_mx_workload(w, seed=0)
+        # (numpy's fp64 matrix product: its BLAS threads, one per core by default)
+        return (lambda rows: mx.mx_gemm(A[:rows], SA[:rows], B, SB, bias, epi)), threads
+    og.build()
+    A, B, bias = inputs.make_workload(w, seed=0)
+    return (lambda rows: og.gemm(A[:rows], B, bias, epi, threads=threads)), threads
+
+
 def cpu_oracle_run(w, seconds: float, total_budget_s: float | None = None):
     """Time the fp64 oracle on a slab of rows of the workload; returns
     (TFLOP/s, threads, sample text, seconds)."""
-    from autotuning_tcgen05_tmem_gb300 import inputs
     from oracle import gemm as og
-    og.build()
-    threads = og.default_threads()
-    A, B, bias = inputs.make_workload(w, seed=0)
-    epi = {"none": 0, "bias": 1, "relu": 2, "gelu": 3}[w.epi]
+    run, threads = oracle_slab(w, og.default_threads())
     cal = min(w.M, max(1, threads))
     t0 = time.perf_counter()
-    og.gemm(A[:cal], B, bias, epi, threads=threads)
+    run(cal)
     per_row = max((time.perf_counter() - t0) / cal, 1e-7)
     rows = int(min(w.M, max(cal, seconds / per_row)))
     passes = 0
     t0 = time.perf_counter()
     while True:           # whole passes over the slab until `seconds` of CPU work
-        og.gemm(A[:rows], B, bias, epi, threads=threads)
+        run(rows)
         passes += 1
         dt = time.perf_counter() - t0
         if dt >= seconds or dt >= 30.0:
@@ -214,22 +235,18 @@ def reference_arm(args, w):
     if rank != 0:
         return 0
     from oracle import gemm as og
-    from autotuning_tcgen05_tmem_gb300 import inputs
-    og.build()
-    threads = og.default_threads()
-    A, B, bias = inputs.make_workload(w, seed=0)
-    epi = {"none": 0, "bias": 1, "relu": 2, "gelu": 3}[w.epi]
+    run, threads = oracle_slab(w, og.default_threads())
     cal = min(w.M, max(1, threads))
     t0 = time.perf_counter()
-    og.gemm(A[:cal], B, bias, epi, threads=threads)
+    run(cal)
     per_row = max((time.perf_counter() - t0) / cal, 1e-7)
     budget = args.cpu_budget / max(1, args.steps + args.warmup)   # seconds of CPU work per step
     rows = int(min(w.M, max(1, budget / per_row)))
     for _ in range(args.warmup):
-        og.gemm(A[:rows], B, bias, epi, threads=threads)
+        run(rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        og.gemm(A[:rows], B, bias, epi, threads=threads)
+        run(rows)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * w.N * w.K
     value = flops * args.steps / dt / 1e12
@@ -252,15 +269,33 @@ def reference_arm(args, w):
 # ---------------------------------------------------------------------------
 
 def make_sets(w, nsets, device):
-    """Rotating input sets, drawn on the device from seeded generators."""
+    """Rotating input sets, drawn on the device from seeded generators:
+    (A, B, bias, C), or for block-scaled FP8 (A, SA, B, SB, bias, C) with the
+    scales packed once, outside any timed region, as a weight's would be."""
     import torch
+    import autotuning_tcgen05_tmem_gb300 as g
     from autotuning_tcgen05_tmem_gb300 import inputs
     sets = []
     for s in range(nsets):
-        A, B, bias = inputs.make_workload(w, seed=100 + 10 * s, device=device)
         C = torch.empty(w.M, w.N, dtype=inputs.out_torch_dtype(w.dtype), device=device)
-        sets.append((A, B, bias, C))
+        if w.dtype == "mxfp8":
+            A, SA, B, SB, bias = inputs.make_mx_workload(w, seed=100 + 10 * s, device=device)
+            sets.append((A, g.mx_pack_scales(SA, w.M, w.K, False), B, g.mx_pack_scales(SB, w.N, w.K, True),
+                         bias, C))
+        else:
+            A, B, bias = inputs.make_workload(w, seed=100 + 10 * s, device=device)
+            sets.append((A, B, bias, C))
     return sets
+
+
+def run_set(plan, s, stream):
+    """One GEMM of `plan` on input set `s` (see make_sets)."""
+    if len(s) == 6:
+        A, SA, B, SB, bias, C = s
+        plan.run_mx(A, SA, B, SB, bias, C, None, stream)
+    else:
+        A, B, bias, C = s
+        plan.run(A, B, bias, C, stream)
 
 
 def time_plan(plan, sets, steps, warmup, eager=False):
@@ -270,8 +305,8 @@ def time_plan(plan, sets, steps, warmup, eager=False):
     stream = torch.cuda.Stream()
 
     def one_step():
-        for (A, B, bias, C) in sets:
-            plan.run(A, B, bias, C, stream)
+        for s in sets:
+            run_set(plan, s, stream)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -283,8 +318,8 @@ def time_plan(plan, sets, steps, warmup, eager=False):
         try:
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
-                for (A, B, bias, C) in sets:
-                    plan.run(A, B, bias, C, torch.cuda.current_stream())
+                for s in sets:
+                    run_set(plan, s, torch.cuda.current_stream())
             mode = "cuda_graph"
         except Exception:
             graph = None
@@ -339,7 +374,9 @@ def sweep(args):
     os.environ.setdefault("GEMM_HBM_GBS", str(peaks.get("hbm_gbs", 6800.0)))
     devp = g.device_params_query()
     names = ["fp32_relu_256", "bf16_gelu_1000x1000x8192", "bf16_relu_8192", "bf16_decode_16x8192x28672"] + \
-        [w.name for w in inputs.SWEEP] + ["fp8_gelu_1000x1000x8192", "fp8_relu_8192", "fp8_decode_16x8192x28672"]
+        [w.name for w in inputs.SWEEP] + ["fp8_gelu_1000x1000x8192", "fp8_relu_8192", "fp8_decode_16x8192x28672",
+                                          "mxfp8_gelu_1000x1000x8192", "mxfp8_relu_8192",
+                                          "mxfp8_decode_16x8192x28672"]
     if args.workloads:
         names = [n for n in args.workloads.split(",")]
     for name in names:
@@ -500,7 +537,7 @@ def main():
         plan = g.plan(w.M, w.N, w.K, w.dtype, w.epi)
     plan_s = time.perf_counter() - t0
     cfg = plan.config
-    launches_per_gemm = 2 if w.dtype != "bf16" else 1
+    launches_per_gemm = 1 + plan.launch_info.b_transposed   # (+ the transpose into a K-major B)
 
     run, mode, stream = time_plan(plan, sets, args.steps, args.warmup, args.eager)
     clocks = ClockSampler(local)
@@ -597,7 +634,10 @@ def main():
                        "break_even_calls": (st.tune_seconds / (saved_us * 1e-6)) if saved_us > 0 else None}
 
     # --- end to end through the host-buffer entry point ------------------------
-    if not args.no_e2e and rank == 0:
+    if not args.no_e2e and rank == 0 and w.dtype == "mxfp8":
+        out["e2e"] = None
+        out["e2e_note"] = "the host-buffer entry point takes no scales; block-scaled FP8 runs from device buffers"
+    elif not args.no_e2e and rank == 0:
         A, B, bias, _C = sets[0]
         hA, hB = A.cpu().pin_memory(), B.cpu().pin_memory()
         hb = bias.cpu().pin_memory() if bias is not None else None
