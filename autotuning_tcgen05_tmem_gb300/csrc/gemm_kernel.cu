@@ -1685,6 +1685,52 @@ __global__ void fill_uniform_kernel(void *dst, int64_t n, int dt, float scale, u
 // Row-major [rows, cols] -> row-major [cols, rows] through 32x32 shared-memory
 // tiles, so that both the reads and the writes are coalesced.  Used to give the
 // tensor cores a K-major copy of B when B must not be read MN-major.
+// Byte matrix transpose (an FP8 operand's K-major copy), rows and cols
+// multiples of 4: each thread reads a 4 x 4 block of bytes as four 32-bit words
+// (one per row; a warp covers 4 rows x 32 columns), transposes it in registers
+// with byte permutes, and the resulting words (4 consecutive rows of one
+// column each) are transposed as 32-bit elements through shared memory, so
+// that both the reads and the writes are whole 32-bit words along rows.  A
+// block moves 128 rows x 32 columns per step.
+__global__ void __launch_bounds__(256) transpose_bytes_kernel(const uint8_t *__restrict__ src,
+                                                              uint8_t *__restrict__ dst, int64_t rows, int64_t cols)
+{
+    __shared__ uint32_t tile[32][33];    // [row quad][column]
+    const int t = threadIdx.x;
+    const int g = t & 7, q = t >> 3;     // column group of 4, row quad
+    const int64_t c0 = (int64_t)blockIdx.x * 32;
+    const uint32_t *s32 = reinterpret_cast<const uint32_t *>(src);
+    uint32_t *d32 = reinterpret_cast<uint32_t *>(dst);
+    const int64_t cw = cols / 4, rw = rows / 4;   // row lengths in words
+    for (int64_t r0 = (int64_t)blockIdx.y * 128; r0 < rows; r0 += (int64_t)gridDim.y * 128) {
+        const int64_t r = r0 + 4 * q, c = c0 + 4 * g;
+        uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
+        if (r < rows && c < cols) {
+            const int64_t i = r * cw + c / 4;
+            w0 = __ldg(s32 + i);
+            w1 = __ldg(s32 + i + cw);
+            w2 = __ldg(s32 + i + 2 * cw);
+            w3 = __ldg(s32 + i + 3 * cw);
+        }
+        // Word j of the result holds column c + j of rows r .. r + 3 (byte k = row r + k).
+        const uint32_t lo01 = __byte_perm(w0, w1, 0x5140), hi01 = __byte_perm(w0, w1, 0x7362);
+        const uint32_t lo23 = __byte_perm(w2, w3, 0x5140), hi23 = __byte_perm(w2, w3, 0x7362);
+        tile[q][4 * g + 0] = __byte_perm(lo01, lo23, 0x5410);
+        tile[q][4 * g + 1] = __byte_perm(lo01, lo23, 0x7632);
+        tile[q][4 * g + 2] = __byte_perm(hi01, hi23, 0x5410);
+        tile[q][4 * g + 3] = __byte_perm(hi01, hi23, 0x7632);
+        __syncthreads();
+        // Column c0 + n of the source is row c0 + n of the destination; its
+        // words r0/4 + 0 .. 31 are tile[0 .. 31][n].
+        const int lq = t & 31;
+        for (int n = t >> 5; n < 32; n += 8) {
+            const int64_t dr = c0 + n, dq = r0 / 4 + lq;
+            if (dr < cols && dq < rw) d32[dr * rw + dq] = tile[lq][n];
+        }
+        __syncthreads();
+    }
+}
+
 template <typename T>
 __global__ void transpose_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t rows, int64_t cols)
 {
@@ -1848,6 +1894,13 @@ cudaError_t max_active_clusters(int dt, int a_mn, int b_mn, int cg, int cluster,
 cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t cols, int elt, cudaStream_t stream)
 {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
+    if (elt == 1 && rows % 4 == 0 && cols % 4 == 0 && ((uintptr_t)src & 3) == 0 && ((uintptr_t)dst & 3) == 0) {
+        const int64_t gy = (rows + 127) / 128;
+        const dim3 grid((unsigned)((cols + 31) / 32), (unsigned)(gy < 65535 ? gy : 65535));
+        transpose_bytes_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(src),
+                                                         static_cast<uint8_t *>(dst), rows, cols);
+        return cudaGetLastError();
+    }
     const int64_t gy = (rows + 31) / 32;
     const dim3 grid((unsigned)((cols + 31) / 32), (unsigned)(gy < 65535 ? gy : 65535));
     const dim3 block(32, 8);
