@@ -75,7 +75,8 @@ cudaError_t kernel_attributes(int dt, int *num_regs, int *max_threads);
 cudaError_t set_kernel_smem_limit(int dt, int bytes);
 cudaError_t max_active_clusters(int dt, int a_mn, int b_mn, int cg, int cluster, int smem_bytes, int *out);
 cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
-                        const KernelParams &p, int grid, int smem_bytes, cudaStream_t stream);
+                        const CUtensorMap *sa, const CUtensorMap *sb, const KernelParams &p, int grid, int smem_bytes,
+                        cudaStream_t stream);
 cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t cols, int elt, cudaStream_t stream);
 cudaError_t launch_fill_uniform(void *dst, int64_t n, int dt, float scale, uint32_t seed,
                                 cudaStream_t stream);

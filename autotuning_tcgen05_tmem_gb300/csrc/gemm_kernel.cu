@@ -208,15 +208,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
-// Plain (untensored) bulk copy global -> shared memory, completing `bytes` on
-// `bar`; both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 // Load into this CTA's shared memory, completing bytes on the barrier of the
 // pair's leader (a shared::cluster address): the second CTA of a CTA pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *m, uint32_t cluster_bar,
@@ -931,7 +922,8 @@ __device__ __forceinline__ void issue_stage_mx(const MmaStage &st, uint32_t slot
 template <int DT, bool A_MN, bool B_MN, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC, const KernelParams p)
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSA,
+                        const __grid_constant__ CUtensorMap tmSB, const KernelParams p)
 {
     constexpr int ELT = Elt<DT>::BYTES;
     constexpr int ODT = DT >= 2 ? 0 : DT;            // type of C, bias and R (FP8 operands give bf16)
@@ -976,6 +968,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.num_kb > 0) {
             prefetch_tmap(&tmA);
             prefetch_tmap(&tmB);
+            if constexpr (DT == 3) {
+                prefetch_tmap(&tmSA);
+                prefetch_tmap(&tmSB);
+            }
         }
         prefetch_tmap(&tmC);
         asm volatile("" ::"r"(p.rows), "r"(p.num_units), "r"(p.tiles_m), "r"(p.staging_buf_bytes), "l"(p.bias),
@@ -1061,16 +1057,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if constexpr (DT == 3) {
                         // The stage's scale atoms: for each 128 rows of A, then
-                        // each 128 columns of B, its bk/128 consecutive K atoms.
+                        // each 128 columns of B, its bk/128 consecutive K atoms,
+                        // one tensor copy each (the packed array seen as rows of
+                        // one 512-byte atom, 128 words wide).
                         const uint32_t ka = (uint32_t)bk / 128u, run = ka * 512u;
                         const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
-                        const int64_t k_atom = (int64_t)kb * ka;
+                        const int32_t k_atom = kb * (int32_t)ka;
                         for (int32_t h = 0; h < bm / 128; ++h)
-                            bulk_load(sf + (uint32_t)h * run,
-                                      p.sfa + (((int64_t)w.tile_m * (bm / 128) + h) * p.sf_kt + k_atom) * 512, run, fb);
+                            tma_load_2d(sf + (uint32_t)h * run, &tmSA, fb, 0,
+                                        (w.tile_m * (bm / 128) + h) * p.sf_kt + k_atom);
                         for (int32_t j = 0; j < bn / 128; ++j)
-                            bulk_load(sf + (uint32_t)(bm / 128 + j) * run,
-                                      p.sfb + (((int64_t)w.tile_n * (bn / 128) + j) * p.sf_kt + k_atom) * 512, run, fb);
+                            tma_load_2d(sf + (uint32_t)(bm / 128 + j) * run, &tmSB, fb, 0,
+                                        (w.tile_n * (bn / 128) + j) * p.sf_kt + k_atom);
                     }
                 } else if (leader) {
                     if constexpr (pair) {
@@ -1827,12 +1825,16 @@ cudaError_t set_kernel_smem_limit(int dt, int bytes)
 }
 
 cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
-                        const KernelParams &p, int grid, int smem_bytes, cudaStream_t stream)
+                        const CUtensorMap *sa, const CUtensorMap *sb, const KernelParams &p, int grid, int smem_bytes,
+                        cudaStream_t stream)
 {
     const void *f = select_kernel(dt, p.a_mn_major, p.b_mn_major, p.pair ? 2 : 1);
     if (!f) return cudaErrorInvalidValue;
-    void *args[] = {const_cast<CUtensorMap *>(&a), const_cast<CUtensorMap *>(&b), const_cast<CUtensorMap *>(&c),
-                    const_cast<KernelParams *>(&p)};
+    // The MX scale maps are read only by block-scaled instances; others get zeros.
+    static const CUtensorMap none{};
+    void *args[] = {const_cast<CUtensorMap *>(&a),  const_cast<CUtensorMap *>(&b),
+                    const_cast<CUtensorMap *>(&c),  const_cast<CUtensorMap *>(sa ? sa : &none),
+                    const_cast<CUtensorMap *>(sb ? sb : &none), const_cast<KernelParams *>(&p)};
     // Every launch allows programmatic overlap with the previous kernel on the
     // stream (the kernel waits on griddepcontrol before touching memory); CTAs
     // of a cooperative fix-up wait on each other, so those launches are also

@@ -45,10 +45,9 @@ struct KernelParams {
     int32_t coop_fixup;                // split-K slices finalise shares of their tile together
                                        // (launched cooperatively: every unit has its own CTA)
     int32_t pair;                      // 1: cta_group::2, consecutive CTAs share 256-row tiles
-    // Block-scaled FP8 (MX): packed scale atoms of A and B (row atoms x
-    // sf_kt K atoms, 512 bytes each), their per-stage shared-memory copy and
-    // TMEM slot (the block-scaled MMA reads scales from tensor memory).
-    const uint8_t *sfa, *sfb;
+    // Block-scaled FP8 (MX): the packed scale arrays (tensor maps tmSA, tmSB:
+    // row atoms x sf_kt K atoms of 512 bytes), their per-stage shared-memory
+    // copy and TMEM slot (the block-scaled MMA reads scales from tensor memory).
     int32_t sf_kt;
     uint32_t sf_stage_bytes, off_sf, sc_stage_cols, sc_col0;
     int32_t cluster_k;                 // 0, or S: the S slices of a tile are one thread-block

@@ -232,7 +232,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_epilogue e
     const int grid = (int)std::min<int64_t>(k.num_units, ds->params.sm_count);
     const int64_t one_per_sm = ds->params.smem_per_block / 2 + 1024;
     const int smem = (int)std::min<int64_t>(ds->params.smem_per_block, std::max<int64_t>(L.smem_total, one_per_sm));
-    e = launch_gemm(GEMM_BF16, ma, mb, mc, k, grid, smem, s);
+    e = launch_gemm(GEMM_BF16, ma, mb, mc, nullptr, nullptr, k, grid, smem, s);
     if (e != cudaSuccess) return set_error(GEMM_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return GEMM_OK;
 }

@@ -148,10 +148,10 @@ static int check_device_arch(int *device_out)
 // ---------------------------------------------------------------------------
 
 struct DescEntry {
-    const void *a = nullptr, *b = nullptr;
+    const void *a = nullptr, *b = nullptr, *sa = nullptr, *sb = nullptr;
     void *c = nullptr;
     bool valid = false;
-    CUtensorMap ma, mb, mc;
+    CUtensorMap ma, mb, mc, msa, msb;   // msa, msb: MX scales (block-scaled plans only)
 };
 
 struct gemm_plan_s {
@@ -222,6 +222,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     int rc = check_extents(M, N, K);
     if (rc) return rc;
     if (!valid_enums(dt, epi)) return set_error(GEMM_ERR_INVALID_ARG, "unknown dtype %d or epilogue %d", dt, epi);
+    if (dt == GEMM_MXFP8_E4M3 && std::max(mx_row_atoms(M), mx_row_atoms(N)) * mx_k_atoms(K) >= ((int64_t)1 << 31))
+        return set_error(GEMM_ERR_UNSUPPORTED, "block-scaled FP8: the packed scales exceed 2^31 atoms");
     const int reason = check_config(M, N, K, dt, epi, cfg, dev);
     if (reason == GEMM_REASON_ALIGN)
         return set_error(GEMM_ERR_MISALIGNED, "K=%lld / N=%lld: %s", (long long)K, (long long)N, reason_text(reason));
@@ -420,10 +422,29 @@ void destroy_plan(gemm_plan_t p)
     delete p;
 }
 
-static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const DescEntry **out)
+// A packed MX scale array as a tensor of 32-bit words: one row per 512-byte
+// atom (row atoms x K atoms rows, 128 words each), box [bk/128 atoms x 128].
+static int encode_scales(CUtensorMap *m, const void *ptr, int64_t rows, uint32_t box_rows)
+{
+    if (!encoder_ready()) return set_error(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {512};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for the MX scales [%lld atoms]", (int)r,
+                         (long long)rows);
+    return GEMM_OK;
+}
+
+static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const void *SA, const void *SB,
+                     const DescEntry **out)
 {
     for (const DescEntry &d : p->descs)
-        if (d.valid && d.a == A && d.b == B && d.c == C) {
+        if (d.valid && d.a == A && d.b == B && d.c == C && d.sa == SA && d.sb == SB) {
             *out = &d;
             return GEMM_OK;
         }
@@ -468,10 +489,19 @@ static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const
             rc = encode_2d(&d.mc, odt, C, p->N, p->M, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE);
     }
+    memset(&d.msa, 0, sizeof(d.msa));
+    memset(&d.msb, 0, sizeof(d.msb));
+    if (!rc && dt == GEMM_MXFP8_E4M3 && p->K > 0) {
+        const uint32_t ka = (uint32_t)c.bk / 128u;
+        rc = encode_scales(&d.msa, SA, mx_row_atoms(p->M) * mx_k_atoms(p->K), ka);
+        if (!rc) rc = encode_scales(&d.msb, SB, mx_row_atoms(p->N) * mx_k_atoms(p->K), ka);
+    }
     if (rc) return rc;
     d.a = A;
     d.b = B;
     d.c = C;
+    d.sa = SA;
+    d.sb = SB;
     d.valid = true;
     *out = &d;
     return GEMM_OK;
@@ -504,7 +534,7 @@ int run_plan_mx(gemm_plan_t p, const void *A, const void *SA, const void *B, con
     if (dev != p->device)
         return set_error(GEMM_ERR_INVALID_ARG, "plan was made on device %d, current device is %d", p->device, dev);
     const DescEntry *d = nullptr;
-    int rc = get_descs(p, A, B, C, &d);
+    int rc = get_descs(p, A, B, C, SA, SB, &d);
     if (rc) return rc;
     if (p->b_kmajor && p->K > 0) {
         cudaError_t te = launch_transpose(B, p->bt, p->K, p->N, elt_bytes(p->dt), stream);
@@ -513,11 +543,10 @@ int run_plan_mx(gemm_plan_t p, const void *A, const void *SA, const void *B, con
     KernelParams kp = p->kp;
     kp.bias = p->epi != GEMM_EPI_NONE ? bias : nullptr;
     kp.residual = R;
-    kp.sfa = static_cast<const uint8_t *>(SA);
-    kp.sfb = static_cast<const uint8_t *>(SB);
     kp.timeout_ns = g_timeout_ns.load();
     kp.debug_stall = g_debug_stall.load();
-    cudaError_t e = launch_gemm(p->dt, d->ma, d->mb, d->mc, kp, p->grid, p->smem_request, stream);
+    cudaError_t e = launch_gemm(p->dt, d->ma, d->mb, d->mc, mx ? &d->msa : nullptr, mx ? &d->msb : nullptr, kp, p->grid,
+                                p->smem_request, stream);
     if (e != cudaSuccess) return cuda_err(e, "kernel launch");
     return GEMM_OK;
 }
