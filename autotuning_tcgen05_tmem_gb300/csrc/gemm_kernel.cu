@@ -1056,19 +1056,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         else tma_load_2d(sb + (uint32_t)(j * cta_bcols * 128), &tmB, fb, k0 + j * SPAN, rb);
                     }
                     if constexpr (DT == 3) {
-                        // The stage's scale atoms: for each 128 rows of A, then
-                        // each 128 columns of B, its bk/128 consecutive K atoms,
-                        // one tensor copy each (the packed array seen as rows of
-                        // one 512-byte atom, 128 words wide).
+                        // The stage's scale atoms: for each 128 rows of MMA-A,
+                        // then each 128 columns of MMA-B (one atom when bn < 128:
+                        // such a tile starts on an atom), its bk/128 consecutive
+                        // K atoms, one tensor copy each (the packed array seen as
+                        // rows of one 512-byte atom, 128 words wide).  Swapped,
+                        // MMA-A is B (rows along N) and MMA-B is A.
                         const uint32_t ka = (uint32_t)bk / 128u, run = ka * 512u;
                         const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
                         const int32_t k_atom = kb * (int32_t)ka;
-                        for (int32_t h = 0; h < bm / 128; ++h)
-                            tma_load_2d(sf + (uint32_t)h * run, &tmSA, fb, 0,
-                                        (w.tile_m * (bm / 128) + h) * p.sf_kt + k_atom);
-                        for (int32_t j = 0; j < bn / 128; ++j)
-                            tma_load_2d(sf + (uint32_t)(bm / 128 + j) * run, &tmSB, fb, 0,
-                                        (w.tile_n * (bn / 128) + j) * p.sf_kt + k_atom);
+                        const CUtensorMap *sm_a = A_MN || p.swap_ab ? &tmSB : &tmSA;
+                        const CUtensorMap *sm_b = A_MN || p.swap_ab ? &tmSA : &tmSB;
+                        const int32_t na = bm / 128, nb = max(1, bn / 128);
+                        for (int32_t h = 0; h < na; ++h)
+                            tma_load_2d(sf + (uint32_t)h * run, sm_a, fb, 0, (w.tile_m * na + h) * p.sf_kt + k_atom);
+                        for (int32_t j = 0; j < nb; ++j)
+                            tma_load_2d(sf + (uint32_t)(na + j) * run, sm_b, fb, 0,
+                                        (w.tile_n * bn / 128 + j) * p.sf_kt + k_atom);
                     }
                 } else if (leader) {
                     if constexpr (pair) {
@@ -1152,7 +1156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (DT == 3) {
                         const uint32_t slot = tmem_base + p.sc_col0 + stage * p.sc_stage_cols;
                         const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
-                        const int bn_atoms = bn / 128;
+                        const int bn_atoms = max(1, bn / 128);
                         switch (ksteps * 2 + halves - 1) {
                         case 8: issue_stage_mx<A_MN, B_MN, 4, 1>(st, slot, sf, bn_atoms); break;
                         case 9: issue_stage_mx<A_MN, B_MN, 4, 2>(st, slot, sf, bn_atoms); break;
@@ -1767,9 +1771,12 @@ static const void *kernel_fn()
 
 static const void *select_kernel(int dt, int a_mn, int b_mn, int cg)
 {
-    if (dt == 3) {   // block-scaled FP8: single CTA, unswapped; B in place or from a K-major copy
-        if (cg != 1 || a_mn) return nullptr;
-        return b_mn ? kernel_fn<3, false, true, 1>() : kernel_fn<3, false, false, 1>();
+    if (dt == 3) {   // block-scaled FP8: single CTA; B in place (unswapped: MMA-B; swapped: MMA-A) or K-major
+        if (cg != 1) return nullptr;
+        if (!a_mn && b_mn) return kernel_fn<3, false, true, 1>();
+        if (a_mn && !b_mn) return kernel_fn<3, true, false, 1>();
+        if (!a_mn && !b_mn) return kernel_fn<3, false, false, 1>();
+        return nullptr;
     }
     if (cg == 2) {
         if (a_mn) return nullptr;

@@ -87,7 +87,7 @@ Layout layout_of(const gemm_config &c, int dt)
     // MX: each stage also stages the scale atoms of its A rows (bm/128) and B
     // columns (bn/128), bk/128 atoms along K each, and gives them a TMEM slot
     // of 4 columns per atom (tcgen05.cp 32x128b.warpx4 fills 4 columns).
-    const int mx_atoms = dt == GEMM_MXFP8_E4M3 ? (c.bm / 128 + c.bn / 128) * (c.bk / 128) : 0;
+    const int mx_atoms = dt == GEMM_MXFP8_E4M3 ? (c.bm / 128 + std::max(1, c.bn / 128)) * (c.bk / 128) : 0;
     L.sf_stage_bytes = (uint32_t)(mx_atoms * kMxAtomBytes);
     L.sc_stage_cols = (uint32_t)(mx_atoms * 4);
     L.off_b = (uint32_t)c.stages * L.a_stage_bytes;
@@ -124,7 +124,7 @@ bool cluster_reduce_fits(const gemm_config &c, int dt)
 
 int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block, int cta_group)
 {
-    const int64_t mx = dt == GEMM_MXFP8_E4M3 ? (int64_t)(bm / 128 + bn / 128) * (bk / 128) * kMxAtomBytes : 0;
+    const int64_t mx = dt == GEMM_MXFP8_E4M3 ? (int64_t)(bm / 128 + std::max(1, bn / 128)) * (bk / 128) * kMxAtomBytes : 0;
     const int64_t per = (int64_t)(cta_group == 2 ? 128 + bn / 2 : bm + bn) * bk * elt_bytes(dt) + mx;
     const int64_t room = smem_per_block - staging_bytes(dt, swap_ab) - kAuxSmem - (mx ? 1024 : 0);
     int64_t s = room / per;
@@ -142,7 +142,7 @@ const char *reason_text(int r)
     case GEMM_REASON_UMMA_N: return "bn must be a multiple of 16 in [16, 256]";
     case GEMM_REASON_LAYOUT:
         return "bn must be a multiple of 32 and of the 128-byte span when B is MN-major (a CTA pair: bn/2 a "
-               "multiple of the span; block-scaled FP8: no swap, bn 128 or 256)";
+               "multiple of the span; block-scaled FP8: bn 128 or 256, or swapped a multiple of 128 or >= M)";
     case GEMM_REASON_BK: return "bk must be 1..4 spans of 128 bytes (block-scaled FP8: 128 or 256)";
     case GEMM_REASON_STAGES: return "stages must be in 2..16";
     case GEMM_REASON_SCHEDULE: return "raster must be 0/1 and group one of 1,2,4,8,16";
@@ -158,7 +158,6 @@ const char *reason_text(int r)
 int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &c,
                  const gemm_device_params &d)
 {
-    (void)M;
     (void)epi;
     const int e = elt_bytes(dt);
     const int span = span_elems(dt);
@@ -172,8 +171,11 @@ int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_co
     const int b_unit = b_in_place(dt, N) ? span : 32;
     if (c.swap_ab == 0 && (c.bn % b_unit != 0 || c.bn % 32 != 0)) return GEMM_REASON_LAYOUT;
     if (c.cta_group == 2 && (c.bn / 2) % b_unit != 0) return GEMM_REASON_LAYOUT;
-    // MX: a tile's B scales are whole 128-column atoms, and the MMA reads them unswapped.
-    if (dt == GEMM_MXFP8_E4M3 && (c.swap_ab != 0 || (c.bn != 128 && c.bn != 256))) return GEMM_REASON_LAYOUT;
+    // MX: the scales of a tile's MMA-N columns come in whole 128-column atoms, so
+    // an unswapped tile has bn 128 or 256, and a swapped one (tokens along N)
+    // starts every tile on an atom: bn a multiple of 128, or all of M in one tile.
+    if (dt == GEMM_MXFP8_E4M3 && c.swap_ab == 0 && c.bn != 128 && c.bn != 256) return GEMM_REASON_LAYOUT;
+    if (dt == GEMM_MXFP8_E4M3 && c.swap_ab == 1 && c.bn % 128 != 0 && M > c.bn) return GEMM_REASON_LAYOUT;
     if (c.bk % span != 0 || c.bk / span < 1 || c.bk / span > 4) return GEMM_REASON_BK;
     if (dt == GEMM_MXFP8_E4M3 && c.bk != 128 && c.bk != 256) return GEMM_REASON_BK;
     if (c.stages < 2 || c.stages > kMaxStages) return GEMM_REASON_STAGES;
@@ -208,7 +210,6 @@ std::vector<gemm_config> enumerate(int64_t M, int64_t N, int64_t K, int dt, int 
         for (const auto &shape : shapes) {
             const int bm = shape.first, cg = shape.second;
             if (cg == 2 && (swap || dt == GEMM_MXFP8_E4M3)) continue;
-            if (swap && dt == GEMM_MXFP8_E4M3) continue;
             std::vector<int> bns;
             if (swap) bns = {16, 32, 64, 128, 256};
             else if (cg == 2) bns = dt == GEMM_BF16                          ? std::vector<int>{128, 256}

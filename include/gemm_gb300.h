@@ -119,9 +119,10 @@ typedef enum {
  *   cta_group 1, or 2: a 256-row tile on a CTA pair (tcgen05 cta_group::2;
  *             bm = 256, no swap; each CTA holds 128 rows and half of B)
  *   swap_ab   0 or 1, as above
- * Block-scaled FP8 (GEMM_MXFP8_E4M3) adds: cta_group 1, swap_ab 0, bn 128 or
- * 256, bk 128 or 256, and the accumulators plus one TMEM slot of scales per
- * stage within 512 columns.
+ * Block-scaled FP8 (GEMM_MXFP8_E4M3) adds: cta_group 1; unswapped bn 128 or
+ * 256; swapped (tokens along the MMA's N) bn a multiple of 128 or at least M,
+ * so that every tile starts on a 128-column scale atom; bk 128 or 256; and the
+ * accumulators plus one TMEM slot of scales per stage within 512 columns.
  */
 typedef struct {
     int32_t bm, bn, bk, stages, raster, group, split_k, cta_group, swap_ab;
@@ -134,7 +135,7 @@ typedef enum {
     GEMM_REASON_UMMA_M = 2,     /* bm not 128/256 (tcgen05 M per CTA is 128) */
     GEMM_REASON_UMMA_N = 3,     /* bn not a multiple of 16 in [16, 256] */
     GEMM_REASON_LAYOUT = 4,     /* swap_ab not 0/1; bn not a multiple of 32 and of the span when unswapped
-                                   (MX: swap_ab 1, or bn not 128/256) */
+                                   (MX: bn not 128/256 unswapped; swapped, bn neither a multiple of 128 nor >= M) */
     GEMM_REASON_BK = 5,         /* bk not 1..4 spans of 128 bytes (MX: not 128/256) */
     GEMM_REASON_STAGES = 6,     /* stages outside 2..16 */
     GEMM_REASON_SCHEDULE = 7,   /* raster not 0/1 or group not in {1,2,4,8,16} */

@@ -294,7 +294,7 @@ def mx_atoms(cfg: Config, dtype):
     column atoms, bk/128 of each along K (zero for other dtypes)."""
     if dtype != DT_MXFP8:
         return 0
-    return (cfg.bm // 128 + cfg.bn // 128) * (cfg.bk // 128)
+    return (cfg.bm // 128 + max(1, cfg.bn // 128)) * (cfg.bk // 128)
 
 
 def out_elt_bytes(dtype):
@@ -336,7 +336,7 @@ def smem_bytes(cfg: Config, dtype):
 
 
 def max_stages(bm, bn, bk, dtype, swap_ab, smem_per_block, cta_group=1):
-    mx = (bm // 128 + bn // 128) * (bk // 128) * MX_ATOM_BYTES if dtype == DT_MXFP8 else 0
+    mx = (bm // 128 + max(1, bn // 128)) * (bk // 128) * MX_ATOM_BYTES if dtype == DT_MXFP8 else 0
     per = ((128 + bn // 2) if cta_group == 2 else (bm + bn)) * bk * elt_bytes(dtype) + mx
     room = smem_per_block - staging_bytes(dtype, swap_ab) - AUX_SMEM - (1024 if mx else 0)
     return max(0, min(MAX_STAGES, room // per))
@@ -373,7 +373,11 @@ def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
         return R_LAYOUT
     if cfg.cta_group == 2 and (cfg.bn // 2) % b_unit != 0:
         return R_LAYOUT
-    if dtype == DT_MXFP8 and (cfg.swap_ab != 0 or cfg.bn not in (128, 256)):
+    # MX: scales of the MMA-N columns come in 128-column atoms; a swapped tile
+    # (tokens along N) must start on one: bn a multiple of 128 or M in one tile.
+    if dtype == DT_MXFP8 and cfg.swap_ab == 0 and cfg.bn not in (128, 256):
+        return R_LAYOUT
+    if dtype == DT_MXFP8 and cfg.swap_ab == 1 and cfg.bn % 128 != 0 and M > cfg.bn:
         return R_LAYOUT
     if cfg.bk % span != 0 or not (1 <= cfg.bk // span <= 4):
         return R_BK
@@ -411,8 +415,6 @@ def gb300_candidates(M, N, K, dtype, epi, dev: Device):
         rows, cols = (N, M) if swap else (M, N)
         for bm, cg in ((128, 1), (256, 1), (256, 2)):
             if cg == 2 and (swap or dtype == DT_MXFP8):
-                continue
-            if swap and dtype == DT_MXFP8:
                 continue
             if swap:
                 bns = (16, 32, 64, 128, 256)

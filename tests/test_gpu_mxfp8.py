@@ -2,7 +2,7 @@
 tcgen05.mma kind::mxf8f6f4.block_scale, scales staged through TMEM) against the
 oracle, which dequantizes the same bytes from the format's definition:
 bit-exact on small-integer inputs, within the stated tolerance on random ones,
-on every tile shape, K step, tile order and split-K route the rules allow; the
+on every tile shape, K step, tile order, operand swap and split-K route the rules allow; the
 scale packing against the documented layout; argument checks."""
 import numpy as np
 import pytest
@@ -29,6 +29,9 @@ CASES = [
     ((300, 320, 2048), C(128, 128, 128, 4, 0, 1, 4), 1),       # split-K, cooperative route
     ((200, 136, 512), C(128, 128, 128, 4), 0),                 # N % 16 != 0: B from a K-major copy
     ((1000, 1000, 4096), C(128, 128, 128, 4, 0, 1, 3), 0),     # split-K over several waves (last arriver)
+    ((20, 320, 1024), C(128, 32, 128, 6, 0, 1, 1, 1, 1), 0),   # swapped: tokens along N, one token tile
+    ((40, 264, 1024), C(256, 64, 128, 2, 0, 1, 3, 1, 1), 0),   # swapped, split-K, B from a K-major copy
+    ((200, 256, 512), C(128, 128, 128, 4, 0, 1, 1, 1, 1), 0),  # swapped, two token tiles of one atom each
 ]
 
 
