@@ -402,24 +402,42 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t b
 // quarter, column sfb + n/32; the byte within the 32-bit word is the scale-ID
 // field of idesc (A: bits 29-30, B: bits 4-5), which names the 32-element block
 // of K that this MMA covers among the four a word holds.
+// CG = 2 (a CTA pair, issued by the leader): each CTA's rows read their A
+// scales, and every column its B scale, from that CTA's own TMEM in the same
+// layout, so both CTAs hold all of the tile's B scales.
+template <int CG>
 __device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
+    if constexpr (CG == 2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
 }
 
 // Copy 32 rows x 16 bytes of shared memory into TMEM, the same 32 rows into
 // each of the four lane quarters (row r -> lane 32q + r, 4 columns); issued
-// by the MMA thread, in order with its MMAs.
+// by the MMA thread, in order with its MMAs.  CG = 2: issued by the pair's
+// leader, each CTA's block goes into that CTA's own TMEM.
+template <int CG>
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
 {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Descriptor of a 32-row x 16-byte block in shared memory, no swizzle: four
@@ -885,7 +903,7 @@ __device__ __forceinline__ void issue_stage(const MmaStage &st)
 // then B's at (HALVES·KA + a·bn_atoms + j)·4 so that a K atom's B columns are
 // contiguous, n/32 apart), then the MMAs, each naming its 32-element block of
 // K by the scale ID (kk mod 4) and its atom by the slot column (kk / 4).
-template <bool A_MN, bool B_MN, int KSTEPS, int HALVES>
+template <bool A_MN, bool B_MN, int KSTEPS, int HALVES, int CG = 1>
 __device__ __forceinline__ void issue_stage_mx(const MmaStage &st, uint32_t slot, uint32_t sf_smem, int bn_atoms)
 {
     constexpr int KA = KSTEPS / 4;
@@ -894,12 +912,12 @@ __device__ __forceinline__ void issue_stage_mx(const MmaStage &st, uint32_t slot
     for (int h = 0; h < HALVES; ++h)
 #pragma unroll
         for (int a = 0; a < KA; ++a)
-            tmem_cp_32x128b_x4(slot + (uint32_t)(h * KA + a) * 4u,
+            tmem_cp_32x128b_x4<CG>(slot + (uint32_t)(h * KA + a) * 4u,
                                smem_desc_rows16(sf_smem + (uint32_t)(h * KA + a) * 512u));
     for (int j = 0; j < bn_atoms; ++j)
 #pragma unroll
         for (int a = 0; a < KA; ++a)
-            tmem_cp_32x128b_x4(slot + (uint32_t)(HALVES * KA + a * bn_atoms + j) * 4u,
+            tmem_cp_32x128b_x4<CG>(slot + (uint32_t)(HALVES * KA + a * bn_atoms + j) * 4u,
                                smem_desc_rows16(sf_smem + (uint32_t)(HALVES * KA + j * KA + a) * 512u));
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
@@ -910,7 +928,7 @@ __device__ __forceinline__ void issue_stage_mx(const MmaStage &st, uint32_t slot
         const uint32_t sfb = slot + (uint32_t)(HALVES * KA + (kk >> 2) * bn_atoms) * 4u;
 #pragma unroll
         for (int h = 0; h < HALVES; ++h)
-            umma_mx(st.d0 + (uint32_t)h * st.bn, st.adesc + a_k + (uint32_t)h * st.a_half_step, st.bdesc + b_k, id,
+            umma_mx<CG>(st.d0 + (uint32_t)h * st.bn, st.adesc + a_k + (uint32_t)h * st.a_half_step, st.bdesc + b_k, id,
                     slot + (uint32_t)(h * KA + (kk >> 2)) * 4u, sfb, acc);
     }
 }
@@ -1067,9 +1085,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int32_t k_atom = kb * (int32_t)ka;
                         const CUtensorMap *sm_a = A_MN || p.swap_ab ? &tmSB : &tmSA;
                         const CUtensorMap *sm_b = A_MN || p.swap_ab ? &tmSA : &tmSB;
-                        const int32_t na = bm / 128, nb = max(1, bn / 128);
+                        const int32_t na = pair ? 1 : bm / 128, nb = max(1, bn / 128);
                         for (int32_t h = 0; h < na; ++h)
-                            tma_load_2d(sf + (uint32_t)h * run, sm_a, fb, 0, (w.tile_m * na + h) * p.sf_kt + k_atom);
+                            tma_load_2d(sf + (uint32_t)h * run, sm_a, fb, 0,
+                                        (w.tile_m * (bm / 128) + h) * p.sf_kt + k_atom);
                         for (int32_t j = 0; j < nb; ++j)
                             tma_load_2d(sf + (uint32_t)(na + j) * run, sm_b, fb, 0,
                                         (w.tile_n * bn / 128 + j) * p.sf_kt + k_atom);
@@ -1092,6 +1111,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             else
                                 tma_load_2d_pair(sb + (uint32_t)(j * cta_bcols * 128), &tmB, fbr, k0 + j * SPAN,
                                                  rb);
+                        }
+                        if constexpr (DT == 3) {
+                            // MX: this CTA's 128 rows of A scales and all of the
+                            // tile's B scales (the pair MMA reads each CTA's own).
+                            const uint32_t ka = (uint32_t)bk / 128u, run = ka * 512u;
+                            const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
+                            const int32_t k_atom = kb * (int32_t)ka;
+                            tma_load_2d_pair(sf, &tmSA, fbr, 0, (w.tile_m * 2 + 1) * p.sf_kt + k_atom);
+                            for (int32_t j = 0; j < bn / 128; ++j)
+                                tma_load_2d_pair(sf + (uint32_t)(1 + j) * run, &tmSB, fbr, 0,
+                                                 (w.tile_n * bn / 128 + j) * p.sf_kt + k_atom);
                         }
                     }
                 }
@@ -1157,11 +1187,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t slot = tmem_base + p.sc_col0 + stage * p.sc_stage_cols;
                         const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
                         const int bn_atoms = max(1, bn / 128);
-                        switch (ksteps * 2 + halves - 1) {
-                        case 8: issue_stage_mx<A_MN, B_MN, 4, 1>(st, slot, sf, bn_atoms); break;
-                        case 9: issue_stage_mx<A_MN, B_MN, 4, 2>(st, slot, sf, bn_atoms); break;
-                        case 16: issue_stage_mx<A_MN, B_MN, 8, 1>(st, slot, sf, bn_atoms); break;
-                        default: issue_stage_mx<A_MN, B_MN, 8, 2>(st, slot, sf, bn_atoms); break;
+                        if constexpr (pair) {   // one 256-row MMA per K step over both CTAs
+                            if (ksteps == 4) issue_stage_mx<A_MN, B_MN, 4, 1, 2>(st, slot, sf, bn_atoms);
+                            else issue_stage_mx<A_MN, B_MN, 8, 1, 2>(st, slot, sf, bn_atoms);
+                        } else {
+                            switch (ksteps * 2 + halves - 1) {
+                            case 8: issue_stage_mx<A_MN, B_MN, 4, 1>(st, slot, sf, bn_atoms); break;
+                            case 9: issue_stage_mx<A_MN, B_MN, 4, 2>(st, slot, sf, bn_atoms); break;
+                            case 16: issue_stage_mx<A_MN, B_MN, 8, 1>(st, slot, sf, bn_atoms); break;
+                            default: issue_stage_mx<A_MN, B_MN, 8, 2>(st, slot, sf, bn_atoms); break;
+                            }
                         }
                         umma_commit<CG>(empty0 + 8u * stage);  // slot is free once these MMAs have read it
                     } else if constexpr (pair) {
@@ -1771,8 +1806,11 @@ static const void *kernel_fn()
 
 static const void *select_kernel(int dt, int a_mn, int b_mn, int cg)
 {
-    if (dt == 3) {   // block-scaled FP8: single CTA; B in place (unswapped: MMA-B; swapped: MMA-A) or K-major
-        if (cg != 1) return nullptr;
+    if (dt == 3) {   // block-scaled FP8: B in place (unswapped: MMA-B; swapped: MMA-A) or K-major; pairs unswapped
+        if (cg == 2) {
+            if (a_mn) return nullptr;
+            return b_mn ? kernel_fn<3, false, true, 2>() : kernel_fn<3, false, false, 2>();
+        }
         if (!a_mn && b_mn) return kernel_fn<3, false, true, 1>();
         if (a_mn && !b_mn) return kernel_fn<3, true, false, 1>();
         if (!a_mn && !b_mn) return kernel_fn<3, false, false, 1>();

@@ -87,7 +87,8 @@ Layout layout_of(const gemm_config &c, int dt)
     // MX: each stage also stages the scale atoms of its A rows (bm/128) and B
     // columns (bn/128), bk/128 atoms along K each, and gives them a TMEM slot
     // of 4 columns per atom (tcgen05.cp 32x128b.warpx4 fills 4 columns).
-    const int mx_atoms = dt == GEMM_MXFP8_E4M3 ? (c.bm / 128 + std::max(1, c.bn / 128)) * (c.bk / 128) : 0;
+    const int mx_atoms =
+        dt == GEMM_MXFP8_E4M3 ? ((pair ? 1 : c.bm / 128) + std::max(1, c.bn / 128)) * (c.bk / 128) : 0;
     L.sf_stage_bytes = (uint32_t)(mx_atoms * kMxAtomBytes);
     L.sc_stage_cols = (uint32_t)(mx_atoms * 4);
     L.off_b = (uint32_t)c.stages * L.a_stage_bytes;
@@ -124,7 +125,9 @@ bool cluster_reduce_fits(const gemm_config &c, int dt)
 
 int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block, int cta_group)
 {
-    const int64_t mx = dt == GEMM_MXFP8_E4M3 ? (int64_t)(bm / 128 + std::max(1, bn / 128)) * (bk / 128) * kMxAtomBytes : 0;
+    const int64_t mx = dt == GEMM_MXFP8_E4M3
+                           ? (int64_t)((cta_group == 2 ? 1 : bm / 128) + std::max(1, bn / 128)) * (bk / 128) * kMxAtomBytes
+                           : 0;
     const int64_t per = (int64_t)(cta_group == 2 ? 128 + bn / 2 : bm + bn) * bk * elt_bytes(dt) + mx;
     const int64_t room = smem_per_block - staging_bytes(dt, swap_ab) - kAuxSmem - (mx ? 1024 : 0);
     int64_t s = room / per;
@@ -137,7 +140,7 @@ const char *reason_text(int r)
 {
     switch (r) {
     case GEMM_FEASIBLE: return "feasible";
-    case GEMM_REASON_CTA_GROUP: return "cta_group must be 1, or 2 with bm = 256 and no swap (block-scaled FP8: 1)";
+    case GEMM_REASON_CTA_GROUP: return "cta_group must be 1, or 2 with bm = 256 and no swap";
     case GEMM_REASON_UMMA_M: return "bm must be 128 or 256 (tcgen05 M per CTA is 128)";
     case GEMM_REASON_UMMA_N: return "bn must be a multiple of 16 in [16, 256]";
     case GEMM_REASON_LAYOUT:
@@ -162,7 +165,7 @@ int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_co
     const int e = elt_bytes(dt);
     const int span = span_elems(dt);
     if (c.cta_group != 1 && c.cta_group != 2) return GEMM_REASON_CTA_GROUP;
-    if (c.cta_group == 2 && (c.bm != 256 || c.swap_ab != 0 || dt == GEMM_MXFP8_E4M3)) return GEMM_REASON_CTA_GROUP;
+    if (c.cta_group == 2 && (c.bm != 256 || c.swap_ab != 0)) return GEMM_REASON_CTA_GROUP;
     if (c.bm != 128 && c.bm != 256) return GEMM_REASON_UMMA_M;
     if (c.bn % 16 != 0 || c.bn < 16 || c.bn > 256) return GEMM_REASON_UMMA_N;
     if (c.swap_ab != 0 && c.swap_ab != 1) return GEMM_REASON_LAYOUT;
@@ -209,12 +212,13 @@ std::vector<gemm_config> enumerate(int64_t M, int64_t N, int64_t K, int dt, int 
         const std::pair<int, int> shapes[] = {{128, 1}, {256, 1}, {256, 2}};
         for (const auto &shape : shapes) {
             const int bm = shape.first, cg = shape.second;
-            if (cg == 2 && (swap || dt == GEMM_MXFP8_E4M3)) continue;
+            if (cg == 2 && swap) continue;
             std::vector<int> bns;
             if (swap) bns = {16, 32, 64, 128, 256};
-            else if (cg == 2) bns = dt == GEMM_BF16                          ? std::vector<int>{128, 256}
-                                    : (dt == GEMM_FP8_E4M3 && b_in_place(dt, N)) ? std::vector<int>{256}
-                                                                            : std::vector<int>{64, 128, 256};
+            else if (cg == 2) bns = dt == GEMM_BF16                  ? std::vector<int>{128, 256}
+                                    : (is_fp8(dt) && b_in_place(dt, N)) ? std::vector<int>{256}
+                                    : dt == GEMM_MXFP8_E4M3             ? std::vector<int>{128, 256}
+                                                                        : std::vector<int>{64, 128, 256};
             else if (dt == GEMM_BF16) bns = {64, 128, 192, 256};
             else if (dt == GEMM_FP8_E4M3) bns = b_in_place(dt, N) ? std::vector<int>{128, 256}
                                                                   : std::vector<int>{64, 128, 192, 256};

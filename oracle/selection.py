@@ -294,7 +294,8 @@ def mx_atoms(cfg: Config, dtype):
     column atoms, bk/128 of each along K (zero for other dtypes)."""
     if dtype != DT_MXFP8:
         return 0
-    return (cfg.bm // 128 + max(1, cfg.bn // 128)) * (cfg.bk // 128)
+    a_atoms = 1 if cfg.cta_group == 2 else cfg.bm // 128     # a pair: each CTA holds 128 rows
+    return (a_atoms + max(1, cfg.bn // 128)) * (cfg.bk // 128)
 
 
 def out_elt_bytes(dtype):
@@ -336,7 +337,8 @@ def smem_bytes(cfg: Config, dtype):
 
 
 def max_stages(bm, bn, bk, dtype, swap_ab, smem_per_block, cta_group=1):
-    mx = (bm // 128 + max(1, bn // 128)) * (bk // 128) * MX_ATOM_BYTES if dtype == DT_MXFP8 else 0
+    a_atoms = 1 if cta_group == 2 else bm // 128
+    mx = (a_atoms + max(1, bn // 128)) * (bk // 128) * MX_ATOM_BYTES if dtype == DT_MXFP8 else 0
     per = ((128 + bn // 2) if cta_group == 2 else (bm + bn)) * bk * elt_bytes(dtype) + mx
     room = smem_per_block - staging_bytes(dtype, swap_ab) - AUX_SMEM - (1024 if mx else 0)
     return max(0, min(MAX_STAGES, room // per))
@@ -358,7 +360,7 @@ def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
     span = span_elems(dtype)
     if cfg.cta_group not in (1, 2):
         return R_CTA_GROUP
-    if cfg.cta_group == 2 and (cfg.bm != 256 or cfg.swap_ab != 0 or dtype == DT_MXFP8):
+    if cfg.cta_group == 2 and (cfg.bm != 256 or cfg.swap_ab != 0):
         return R_CTA_GROUP
     if cfg.bm not in (128, 256):
         return R_UMMA_M
@@ -414,13 +416,14 @@ def gb300_candidates(M, N, K, dtype, epi, dev: Device):
     for swap in swaps:
         rows, cols = (N, M) if swap else (M, N)
         for bm, cg in ((128, 1), (256, 1), (256, 2)):
-            if cg == 2 and (swap or dtype == DT_MXFP8):
+            if cg == 2 and swap:
                 continue
             if swap:
                 bns = (16, 32, 64, 128, 256)
             elif cg == 2:
                 bns = (128, 256) if dtype == DT_BF16 else \
-                    (256,) if (dtype == DT_FP8 and b_in_place(dtype, N)) else (64, 128, 256)
+                    (256,) if (is_fp8(dtype) and b_in_place(dtype, N)) else \
+                    (128, 256) if dtype == DT_MXFP8 else (64, 128, 256)
             elif dtype == DT_BF16:
                 bns = (64, 128, 192, 256)
             elif dtype == DT_FP8:

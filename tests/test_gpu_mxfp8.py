@@ -2,7 +2,7 @@
 tcgen05.mma kind::mxf8f6f4.block_scale, scales staged through TMEM) against the
 oracle, which dequantizes the same bytes from the format's definition:
 bit-exact on small-integer inputs, within the stated tolerance on random ones,
-on every tile shape, K step, tile order, operand swap and split-K route the rules allow; the
+on every tile shape, K step, tile order, operand swap, CTA pair and split-K route the rules allow; the
 scale packing against the documented layout; argument checks."""
 import numpy as np
 import pytest
@@ -32,6 +32,9 @@ CASES = [
     ((20, 320, 1024), C(128, 32, 128, 6, 0, 1, 1, 1, 1), 0),   # swapped: tokens along N, one token tile
     ((40, 264, 1024), C(256, 64, 128, 2, 0, 1, 3, 1, 1), 0),   # swapped, split-K, B from a K-major copy
     ((200, 256, 512), C(128, 128, 128, 4, 0, 1, 1, 1, 1), 0),  # swapped, two token tiles of one atom each
+    ((300, 320, 1024), C(256, 256, 128, 3, 0, 1, 1, 2), 0),    # CTA pair (each CTA holds all B scales)
+    ((1000, 1000, 4096), C(256, 256, 128, 3, 0, 1, 4, 2), 0),  # CTA pair, split-K, B from a K-major copy
+    ((200, 136, 512), C(256, 128, 128, 4, 0, 1, 1, 2), 0),     # CTA pair, bn 128, two accumulators
 ]
 
 
@@ -177,6 +180,6 @@ def test_mx_plan_rejects_the_unscaled_entry_points_and_vice_versa():
         with pytest.raises(g.GemmError) as e:
             p.run_mx(A.cuda(), sa, B.cuda(), sb, bias.cuda(), Cd)
         assert e.value.code == g.ERR_INVALID_ARG
-    with pytest.raises(g.GemmError) as e:
-        g.plan_with_config(M, N, K, "mxfp8", "relu", C(256, 256, 128, 3, 0, 1, 1, 2))
+    with pytest.raises(g.GemmError) as e:       # B's scales come in 128-column atoms: bn 192 is refused
+        g.plan_with_config(M, N, K, "mxfp8", "relu", C(128, 192, 128, 3))
     assert e.value.code == g.ERR_INFEASIBLE
