@@ -206,11 +206,11 @@ def oracle_slab(w, threads):
     return (lambda rows: og.gemm(A[:rows], B, bias, epi, threads=threads)), threads
 
 
-def cpu_oracle_run(w, seconds: float, total_budget_s: float | None = None):
-    """Time the fp64 oracle on a slab of rows of the workload; returns
-    (TFLOP/s, threads, sample text, seconds)."""
+def cpu_oracle_run(w, seconds: float, total_budget_s: float | None = None, threads: int | None = None):
+    """Time the fp64 oracle on a slab of rows of the workload (on every host
+    core, or on `threads`); returns (TFLOP/s, threads, sample text, seconds)."""
     from oracle import gemm as og
-    run, threads = oracle_slab(w, og.default_threads())
+    run, threads = oracle_slab(w, threads or og.default_threads())
     cal = min(w.M, max(1, threads))
     t0 = time.perf_counter()
     run(cal)
@@ -379,6 +379,8 @@ def sweep(args):
                                           "mxfp8_decode_16x8192x28672"]
     if args.workloads:
         names = [n for n in args.workloads.split(",")]
+    clocks = ClockSampler(0)      # sampled through the sweep; each line summarises its tuned timing
+    clocks.start()
     for name in names:
         w = inputs.WORKLOADS[name]
         flops, cbytes, elt = work_of(w)
@@ -397,7 +399,10 @@ def sweep(args):
         tune_s = time.perf_counter() - t0
         steps = max(3, int(0.3 / max(1e-6, 1e-6 * 20 * nsets)))  # about 0.3 s at 20 us per GEMM
         steps = min(steps, 2000)
+        clocks.mark("t0")
         t_tuned = time_gemm(plan, sets, steps, 5)
+        clocks.mark("t1")
+        shape_clocks = clocks.summary()
         with g.plan_with_config(w.M, w.N, w.K, w.dtype, w.epi, g.fixed_config(w.dtype, devp)) as fp:
             t_fixed = time_gemm(fp, sets, steps, 5)
         # A timed region longer than a second runs under the power cap: the
@@ -415,13 +420,14 @@ def sweep(args):
                 "roofline_frac": roof_t / t_tuned, "fixed_us": t_fixed * 1e6,
                 "tuned_vs_fixed": t_fixed / t_tuned, "plan_seconds": tune_s, "timed_region_s": region_s,
                 "candidates": len(cands), "host_rank_us": host_rank_us,
-                "model_best_us": min(preds) if preds else None,
+                "model_best_us": min(preds) if preds else None, "clocks": shape_clocks,
                 "peaks": f"{peak_src} bf16 {'sustained' if sustained else 'burst'} {bf16_peak} TFLOP/s, "
                          f"HBM {bw} GB/s"}
         print(json.dumps(line), flush=True)
         plan.close()
         del sets
         torch.cuda.empty_cache()
+    clocks.stop()
     return 0
 
 
@@ -662,6 +668,10 @@ def main():
         v, cores, sample, secs = cpu_oracle_run(w, args.cpu_seconds)
         out["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                                "sample": sample, "seconds": secs}
+        if w.dtype != "mxfp8":      # (the block-scaled oracle's matrix product picks its own threads)
+            v1, _c1, sample1, secs1 = cpu_oracle_run(w, min(3.0, args.cpu_seconds), threads=1)
+            out["cpu_baseline"]["one_core"] = {"value": v1, "unit": "TFLOP/s", "cores": 1, "sample": sample1,
+                                               "seconds": secs1}
     if rank == 0:
         print(json.dumps(out), flush=True)
     plan.close()
