@@ -34,6 +34,7 @@ extern std::atomic<int64_t> g_timeout_ns;
 extern std::atomic<int32_t> g_debug_stall;
 extern std::atomic<int32_t> g_b_route;
 extern std::atomic<int32_t> g_split_route;
+extern std::atomic<int32_t> g_check;
 int query_params(gemm_device_params *d);
 int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out);
 int plan_explicit(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &cfg, gemm_plan_t *out);
@@ -336,6 +337,10 @@ int gemm_debug_set(int32_t what, int64_t value)
     if (what == 3) {
         if (value < 0 || value > 1) return set_error(GEMM_ERR_INVALID_ARG, "split-K route must be 0 or 1");
         g_split_route.store((int32_t)value);
+        return GEMM_OK;
+    }
+    if (what == 4) {
+        g_check.store(value ? 1 : 0);
         return GEMM_OK;
     }
     return set_error(GEMM_ERR_INVALID_ARG, "unknown debug control %d", what);

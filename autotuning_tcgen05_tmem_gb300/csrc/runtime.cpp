@@ -41,6 +41,15 @@ std::atomic<int32_t> g_b_route{0};
 // memory when all units fit in one wave and the slices of a tile can form a
 // cluster, else global memory; 1 = always global memory.
 std::atomic<int32_t> g_split_route{0};
+// Checked runs (GEMM_CHECK set to anything but 0 in the environment, or
+// gemm_debug_set(4, 1)): every run synchronises its stream and reports a
+// device-side timeout itself instead of leaving it to gemm_plan_status.
+static int32_t check_from_env()
+{
+    const char *v = getenv("GEMM_CHECK");
+    return (v && *v && strcmp(v, "0") != 0) ? 1 : 0;
+}
+std::atomic<int32_t> g_check{check_from_env()};
 
 // ---------------------------------------------------------------------------
 // TMA descriptor encoding through the driver entry point
@@ -508,6 +517,7 @@ static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const
 }
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+static int read_status(gemm_plan_t p);
 
 int run_plan_mx(gemm_plan_t p, const void *A, const void *SA, const void *B, const void *SB, const void *bias,
                 const void *R, void *C, cudaStream_t stream)
@@ -548,6 +558,11 @@ int run_plan_mx(gemm_plan_t p, const void *A, const void *SA, const void *B, con
     cudaError_t e = launch_gemm(p->dt, d->ma, d->mb, d->mc, mx ? &d->msa : nullptr, mx ? &d->msb : nullptr, kp, p->grid,
                                 p->smem_request, stream);
     if (e != cudaSuccess) return cuda_err(e, "kernel launch");
+    if (g_check.load()) {
+        e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return cuda_err(e, "cudaStreamSynchronize (checked run)");
+        return read_status(p);
+    }
     return GEMM_OK;
 }
 
@@ -609,8 +624,15 @@ int plan_status(gemm_plan_t p)
     if (!p) return set_error(GEMM_ERR_INVALID_ARG, "null plan");
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_err(e, "cudaDeviceSynchronize");
+    return read_status(p);
+}
+
+// The plan's device status word, after its work has finished: GEMM_OK, or
+// GEMM_ERR_TIMEOUT with the word and the split-K counters reset.
+static int read_status(gemm_plan_t p)
+{
     int32_t st = 0;
-    e = cudaMemcpy(&st, p->aux, sizeof(st), cudaMemcpyDeviceToHost);
+    cudaError_t e = cudaMemcpy(&st, p->aux, sizeof(st), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_err(e, "reading the status word");
     if (st != 0) {
         // An early return may leave counts part-way: start them afresh.

@@ -325,7 +325,11 @@ int gemm_plan_launch_info(gemm_plan_t plan, gemm_launch_info *out);
 /* Enqueue C = act(A·B + bias) on `stream` (asynchronous).  A, B, bias, C are
  * device pointers as described above; bias may be NULL only with
  * GEMM_EPI_NONE.  A split-K plan uses its own workspace, so one plan must not
- * run on two streams at once. */
+ * run on two streams at once.  Checked runs (GEMM_CHECK set to anything but 0
+ * in the environment when the library loads, or gemm_debug_set(4, 1)): every
+ * gemm_run, gemm_run_ex and gemm_run_mx synchronises `stream` and returns
+ * GEMM_ERR_TIMEOUT itself when a device wait expired (as gemm_plan_status
+ * would). */
 int gemm_run(gemm_plan_t plan, const void *A, const void *B, const void *bias, void *C,
              gemm_stream_t stream);
 
@@ -450,8 +454,10 @@ int gemm_tune_batch(const int64_t *mnk, int32_t n, gemm_dtype dtype, gemm_epilog
  * MN-major); what = 3: how split-K slices exchange partial tiles in plans made
  * afterwards (0 = through distributed shared memory when all units fit in one
  * wave and the slices of a tile can form a thread-block cluster, else through
- * global memory; 1 = always through global memory).  Affects launches (what 0,
- * 1) or plans (what 2, 3) made after the call, from any thread. */
+ * global memory; 1 = always through global memory); what = 4: checked runs
+ * (1 = every run synchronises and reports a device timeout, 0 = off; the
+ * initial value comes from GEMM_CHECK).  Affects launches (what 0, 1, 4) or
+ * plans (what 2, 3) made after the call, from any thread. */
 int gemm_debug_set(int32_t what, int64_t value);
 
 /* ---------------------------------------------------------------------------

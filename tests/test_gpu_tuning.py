@@ -215,3 +215,27 @@ def test_tune_batch_fills_the_cache_and_the_database(tmp_path):
     for M, N, K in shapes:
         g.plan(M, N, K, "bf16", "relu").close()
     assert g.cache_stats()["tunes"] == 0
+
+
+def test_checked_runs_report_a_device_timeout_from_the_run_itself():
+    A, B, bias = operands(256, 256, 512, "bf16", "int", seed=6)
+    Ad, Bd, bd = A.cuda(), B.cuda(), bias.cuda()
+    C, _ = alloc_out(256, 256, g.BF16)
+    cfg = g.make_config(128, 128, 64, 4, 0, 1, 2)
+    with g.plan_with_config(256, 256, 512, "bf16", "relu", cfg) as p:
+        g.debug_set(4, 1)                    # checked runs: every run synchronises and reads the status
+        try:
+            p.run(Ad, Bd, bd, C)             # a normal run returns OK
+            g.debug_set(0, 50_000_000)
+            g.debug_set(1, 1)                # the epilogue waits on a barrier nothing signals
+            with pytest.raises(g.GemmError) as e:
+                p.run(Ad, Bd, bd, C)
+            assert e.value.code == g.ERR_TIMEOUT
+        finally:
+            g.debug_set(1, 0)
+            g.debug_set(0, 2_000_000_000)
+            g.debug_set(4, 0)
+        p.run(Ad, Bd, bd, C)
+        assert p.status() == 0
+    from gpu_util import device_bits, oracle_rounded_bits
+    assert np.array_equal(device_bits(C.cpu()), oracle_rounded_bits(A, B, bias, "relu", g.BF16))
