@@ -119,8 +119,8 @@ typedef enum {
  *   cta_group 1, or 2: a 256-row tile on a CTA pair (tcgen05 cta_group::2;
  *             bm = 256, no swap; each CTA holds 128 rows and half of B)
  *   swap_ab   0 or 1, as above
- * Block-scaled FP8 (GEMM_MXFP8_E4M3) adds: cta_group 1; unswapped bn 128 or
- * 256; swapped (tokens along the MMA's N) bn a multiple of 128 or at least M,
+ * Block-scaled FP8 (GEMM_MXFP8_E4M3) adds: unswapped bn 128 or 256 (a CTA pair
+ * too); swapped (tokens along the MMA's N) bn a multiple of 128 or at least M,
  * so that every tile starts on a 128-column scale atom; bk 128 or 256; and the
  * accumulators plus one TMEM slot of scales per stage within 512 columns.
  */
