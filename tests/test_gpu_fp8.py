@@ -9,7 +9,7 @@ import torch
 
 import autotuning_tcgen05_tmem_gb300 as g
 from autotuning_tcgen05_tmem_gb300 import inputs
-from gpu_util import alloc_out, device_bits, guard_intact
+from gpu_util import alloc_out, device_bits, guard_intact, sampled_error
 from oracle import gemm as og
 
 pytestmark = pytest.mark.gpu
@@ -109,3 +109,17 @@ def test_fp8_residual_bit_exact_and_tuned_plan():
         tuned = p.config.astuple()
     want = og.round_bf16_bits(og.gemm(A, B, bias, og.EPI_BIAS_RELU_RESIDUAL, residual=R))
     assert np.array_equal(device_bits(Cd.cpu()), want), tuned
+
+
+@pytest.mark.parametrize("name", ["fp8_relu_8192", "fp8_decode_16x8192x28672", "fp8_gelu_1000x1000x8192"])
+def test_fp8_full_size_tuned_plan_sampled(name):
+    """The FP8 workloads at full size through tuned plans (the configurations
+    the sweep times), checked on sampled entries."""
+    w = inputs.WORKLOADS[name]
+    A, B, bias = inputs.make_workload(w, seed=0)
+    with g.plan(w.M, w.N, w.K, w.dtype, w.epi) as p:
+        Cd = torch.empty(w.M, w.N, dtype=torch.bfloat16, device="cuda")
+        p.run(A.cuda(), B.cuda(), bias.cuda() if bias is not None else None, Cd)
+        assert p.status() == 0, g.last_error()
+        cfg = p.config.astuple()
+    assert sampled_error(Cd.cpu(), A, B, bias, w.epi, n=2048) <= 2e-3, cfg

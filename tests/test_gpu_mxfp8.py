@@ -129,7 +129,7 @@ def test_mxfp8_residual_in_place_and_tuned_plan():
     assert np.array_equal(device_bits(Cd.cpu()), want), tuned.astuple()
 
 
-@pytest.mark.parametrize("name", ["mxfp8_gelu_1000x1000x8192", "mxfp8_decode_16x8192x28672"])
+@pytest.mark.parametrize("name", ["mxfp8_gelu_1000x1000x8192", "mxfp8_decode_16x8192x28672", "mxfp8_relu_8192"])
 def test_mxfp8_full_size_sampled_entries(name):
     w = inputs.WORKLOADS[name]
     A, SA, B, SB, bias = inputs.make_mx_workload(w, seed=0)
