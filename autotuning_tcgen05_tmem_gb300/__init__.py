@@ -47,7 +47,7 @@ EXPORTS = ["gemm_version", "gemm_last_error", "gemm_device_params_default",
            "gemm_cache_clear", "gemm_debug_set", "gemm_run_noalloc", "gemm_tune_search",
            "gemm_cache_save", "gemm_cache_load", "gemm_plan_launch_info", "gemm_select_config_set",
            "gemm_plan_from_list", "gemm_tune_batch", "gemm_run_ex", "gemm_plan_set_scale",
-           "gemm_run_mx", "gemm_mx_scales_bytes", "gemm_mx_pack_scales"]
+           "gemm_run_mx", "gemm_mx_scales_bytes", "gemm_mx_pack_scales", "gemm_model_params_load"]
 
 
 class GemmError(RuntimeError):
@@ -164,6 +164,7 @@ def _load_library(path: str):
         "gemm_run_mx": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "gemm_mx_scales_bytes": (i64, [i64, i64]),
         "gemm_mx_pack_scales": (ctypes.c_int, [vp, i64, i64, i32, vp, vp]),
+        "gemm_model_params_load": (ctypes.c_int, [ctypes.c_char_p, P(DeviceParams)]),
         "gemm_run_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "gemm_plan_status": (ctypes.c_int, [vp]),
         "gemm_plan_launch_info": (ctypes.c_int, [vp, P(LaunchInfo)]),
@@ -245,6 +246,14 @@ def device_params_query() -> DeviceParams:
     d = DeviceParams()
     _check(lib().gemm_device_params_query(ctypes.byref(d)))
     return d
+
+
+def model_params_load(path: str, dev: DeviceParams) -> DeviceParams:
+    """dev with the cost-model coefficients of a "name value" file applied."""
+    out = DeviceParams()
+    ctypes.memmove(ctypes.byref(out), ctypes.byref(dev), ctypes.sizeof(DeviceParams))
+    _check(lib().gemm_model_params_load(str(path).encode(), ctypes.byref(out)))
+    return out
 
 
 def check_config(M, N, K, dtype, epi, cfg: Config, dev: DeviceParams) -> int:

@@ -36,6 +36,7 @@ extern std::atomic<int32_t> g_b_route;
 extern std::atomic<int32_t> g_split_route;
 extern std::atomic<int32_t> g_check;
 int query_params(gemm_device_params *d);
+int model_params_load(const char *path, gemm_device_params *out);
 int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out);
 int plan_explicit(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &cfg, gemm_plan_t *out);
 int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream);
@@ -202,6 +203,12 @@ int gemm_run_ex(gemm_plan_t plan, const void *A, const void *B, const void *bias
                 gemm_stream_t stream)
 {
     return run_plan_ex(plan, A, B, bias, R, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gemm_model_params_load(const char *path, gemm_device_params *dev)
+{
+    clear_error();
+    return model_params_load(path, dev);
 }
 
 int gemm_run_mx(gemm_plan_t plan, const void *A, const void *SA, const void *B, const void *SB, const void *bias,

@@ -14,6 +14,7 @@
 //    memory); DISABLE_AUTOTUNE-style switch for correctness runs.
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -109,6 +110,48 @@ static double env_double(const char *name, double dflt)
     return (end && end != v && x > 0) ? x : dflt;
 }
 
+int model_params_load(const char *path, gemm_device_params *out)
+{
+    if (!path || !out) return set_error(GEMM_ERR_INVALID_ARG, "null path or parameters");
+    FILE *f = fopen(path, "r");
+    if (!f) return set_error(GEMM_ERR_INVALID_ARG, "cannot read model parameters from %s", path);
+    gemm_device_params d = *out;
+    struct Field { const char *name; double *dst; };
+    const Field fields[] = {{"peak_tflops_bf16", &d.peak_tflops_bf16}, {"peak_tflops_tf32", &d.peak_tflops_tf32},
+                            {"peak_tflops_fp8", &d.peak_tflops_fp8},   {"hbm_gbs", &d.hbm_gbs},
+                            {"sm_clock_mhz", &d.sm_clock_mhz},         {"l2_gbs", &d.l2_gbs},
+                            {"mma_issue_clk", &d.mma_issue_clk},       {"kblock_clk", &d.kblock_clk},
+                            {"mem_latency_us", &d.mem_latency_us},     {"epi_elems_per_clk", &d.epi_elems_per_clk},
+                            {"epi_gelu_elems_per_clk", &d.epi_gelu_elems_per_clk},
+                            {"splitk_gbs", &d.splitk_gbs},             {"launch_us", &d.launch_us}};
+    char line[512];
+    int lineno = 0, rc = GEMM_OK;
+    while (rc == GEMM_OK && fgets(line, sizeof line, f)) {
+        ++lineno;
+        char *hash = strchr(line, '#');
+        if (hash) *hash = 0;
+        char name[128];
+        double value = 0.0;
+        char extra[8];
+        const int got = sscanf(line, "%127s %lf %7s", name, &value, extra);
+        if (got <= 0) continue;                      // blank or comment
+        if (got != 2 || !(value > 0.0) || !isfinite(value)) {
+            rc = set_error(GEMM_ERR_INVALID_ARG, "%s:%d: expected \"name positive-value\"", path, lineno);
+            break;
+        }
+        bool known = false;
+        for (const Field &fd : fields)
+            if (strcmp(fd.name, name) == 0) {
+                *fd.dst = value;
+                known = true;
+            }
+        if (!known) rc = set_error(GEMM_ERR_INVALID_ARG, "%s:%d: unknown model parameter %s", path, lineno, name);
+    }
+    fclose(f);
+    if (rc == GEMM_OK) *out = d;
+    return rc;
+}
+
 int query_params(gemm_device_params *d)
 {
     params_default(d);
@@ -130,6 +173,8 @@ int query_params(gemm_device_params *d)
     d->peak_tflops_tf32 = env_double("GEMM_PEAK_TF32_TFLOPS", d->peak_tflops_bf16 / 2.0);
     d->peak_tflops_fp8 = env_double("GEMM_PEAK_FP8_TFLOPS", d->peak_tflops_bf16 * 2.0);
     d->hbm_gbs = env_double("GEMM_HBM_GBS", d->hbm_gbs);
+    const char *mp = getenv("GEMM_MODEL_PARAMS");
+    if (mp && *mp) return model_params_load(mp, d);
     return GEMM_OK;
 }
 

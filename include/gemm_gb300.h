@@ -131,7 +131,7 @@ typedef struct {
 /* Reason codes of gemm_check_config (first rule broken, in this order). */
 typedef enum {
     GEMM_FEASIBLE = 0,
-    GEMM_REASON_CTA_GROUP = 1,  /* cta_group not 1, or 2 with bm = 256 and no swap (MX: 1) */
+    GEMM_REASON_CTA_GROUP = 1,  /* cta_group not 1, or 2 with bm = 256 and no swap */
     GEMM_REASON_UMMA_M = 2,     /* bm not 128/256 (tcgen05 M per CTA is 128) */
     GEMM_REASON_UMMA_N = 3,     /* bn not a multiple of 16 in [16, 256] */
     GEMM_REASON_LAYOUT = 4,     /* swap_ab not 0/1; bn not a multiple of 32 and of the span when unswapped
@@ -278,6 +278,18 @@ int gemm_schedule_unit(int64_t unit, int32_t tiles_m, int32_t tiles_n, int32_t s
 /* Parameters of the current device: SM count, shared-memory limit, L2 size,
  * clock and the GEMM kernel's register count, on top of the defaults. */
 int gemm_device_params_query(gemm_device_params *out);
+
+/* Apply a text file of cost-model coefficients to *dev: one "name value" pair
+ * per line ('#' starts a comment), names being the double fields of
+ * gemm_device_params (l2_gbs, mma_issue_clk, kblock_clk, mem_latency_us,
+ * epi_elems_per_clk, epi_gelu_elems_per_clk, splitk_gbs, launch_us, peaks,
+ * hbm_gbs, sm_clock_mhz), values positive.  A file fitted to one device's
+ * timings recalibrates the model for it ("Tile Selection", "Selection is per
+ * device").  gemm_device_params_query applies the file named by
+ * GEMM_MODEL_PARAMS when that variable is set.  Returns GEMM_ERR_INVALID_ARG
+ * (and leaves *dev unchanged) for an unreadable file, an unknown name or a bad
+ * value. */
+int gemm_model_params_load(const char *path, gemm_device_params *dev);
 
 /* Plan a GEMM: cache lookup by (M, N, K, dtype, epilogue, device name, SM count,
  * library version); on a miss, enumerate → rank by the model → time the top
