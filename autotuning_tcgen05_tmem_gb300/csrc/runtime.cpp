@@ -276,6 +276,11 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     int rc = check_extents(M, N, K);
     if (rc) return rc;
     if (!valid_enums(dt, epi)) return set_error(GEMM_ERR_INVALID_ARG, "unknown dtype %d or epilogue %d", dt, epi);
+    // The kernel's schedule arithmetic is 32-bit: work units (tiles x slices)
+    // must number fewer than 2^31.
+    if (cfg.bm > 0 && cfg.bn > 0 && cfg.split_k > 0 &&
+        cdiv(cfg.swap_ab ? N : M, cfg.bm) * cdiv(cfg.swap_ab ? M : N, cfg.bn) * cfg.split_k >= ((int64_t)1 << 31))
+        return set_error(GEMM_ERR_UNSUPPORTED, "the problem needs 2^31 or more work units with this configuration");
     if (dt == GEMM_MXFP8_E4M3 && std::max(mx_row_atoms(M), mx_row_atoms(N)) * mx_k_atoms(K) >= ((int64_t)1 << 31))
         return set_error(GEMM_ERR_UNSUPPORTED, "block-scaled FP8: the packed scales exceed 2^31 atoms");
     const int reason = check_config(M, N, K, dt, epi, cfg, dev);
