@@ -647,8 +647,48 @@ def main():
         A, B, bias, _C = sets[0]
         hA, hB = A.cpu().pin_memory(), B.cpu().pin_memory()
         hb = bias.cpu().pin_memory() if bias is not None else None
-        hC = torch.empty(w.M, w.N, dtype=inputs.out_torch_dtype(w.dtype)).pin_memory()
+        h2d = (w.M * w.K + w.K * w.N) * elt + (w.N * elt_sizes(w.dtype)[1] if bias is not None else 0)
+        d2h = w.M * w.N * elt_sizes(w.dtype)[1]
         esteps = max(5, min(args.steps, 200))
+        # (1) Pipelined through the public device API: steps alternate over two
+        # streams, each with its own plan (a split-K plan runs on one stream at
+        # a time) and device buffers; a step copies its inputs in, runs, and
+        # reads its result back, and the copies of one step overlap the kernel
+        # of the other.
+        pl2 = [plan, g.plan_with_config(w.M, w.N, w.K, w.dtype, w.epi, cfg)]
+        st2 = [torch.cuda.Stream(), torch.cuda.Stream()]
+        dA = [torch.empty_like(A) for _ in range(2)]
+        dB = [torch.empty_like(B) for _ in range(2)]
+        db = [torch.empty_like(bias) if bias is not None else None for _ in range(2)]
+        dC = [torch.empty(w.M, w.N, dtype=inputs.out_torch_dtype(w.dtype), device=dev) for _ in range(2)]
+        hC2 = [torch.empty(w.M, w.N, dtype=inputs.out_torch_dtype(w.dtype)).pin_memory() for _ in range(2)]
+
+        def e2e_step(i):
+            s = i % 2
+            with torch.cuda.stream(st2[s]):
+                dA[s].copy_(hA, non_blocking=True)
+                dB[s].copy_(hB, non_blocking=True)
+                if hb is not None:
+                    db[s].copy_(hb, non_blocking=True)
+                pl2[s].run(dA[s], dB[s], db[s], dC[s], st2[s])
+                hC2[s].copy_(dC[s], non_blocking=True)
+
+        for i in range(4):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(esteps):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        dt = (time.perf_counter() - t0) / esteps
+        assert pl2[1].status() == 0, g.last_error()
+        pl2[1].close()
+        out["e2e"] = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h, "steps": esteps,
+                      "path": "pinned host buffers -> two streams (copy in, gemm_run, copy out per step; one "
+                              "step's copies overlap the other's kernel)"}
+        # (2) The synchronous host-buffer entry point, one call per step.
+        hC = torch.empty(w.M, w.N, dtype=inputs.out_torch_dtype(w.dtype)).pin_memory()
         hstream = torch.cuda.Stream()
         for _ in range(3):
             plan.run_host(hA, hB, hb, hC, hstream)
@@ -657,11 +697,9 @@ def main():
         for _ in range(esteps):
             plan.run_host(hA, hB, hb, hC, hstream)
         dt = (time.perf_counter() - t0) / esteps
-        out["e2e"] = {"value": flops / dt / 1e12, "unit": "TFLOP/s",
-                      "h2d_bytes_per_step": (w.M * w.K + w.K * w.N) * elt
-                                            + (w.N * elt_sizes(w.dtype)[1] if bias is not None else 0),
-                      "d2h_bytes_per_step": w.M * w.N * elt_sizes(w.dtype)[1], "steps": esteps,
-                      "path": "gemm_run_host (pinned host buffers; copies and one kernel per step)"}
+        out["e2e_sync"] = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                           "d2h_bytes_per_step": d2h, "steps": esteps,
+                           "path": "gemm_run_host (copies, one kernel, copy back, synchronise; per step)"}
 
     # --- CPU oracle ------------------------------------------------------------
     if not args.no_cpu and rank == 0 and world == 1:
