@@ -47,7 +47,8 @@ EXPORTS = ["gemm_version", "gemm_last_error", "gemm_device_params_default",
            "gemm_cache_clear", "gemm_debug_set", "gemm_run_noalloc", "gemm_tune_search",
            "gemm_cache_save", "gemm_cache_load", "gemm_plan_launch_info", "gemm_select_config_set",
            "gemm_plan_from_list", "gemm_tune_batch", "gemm_run_ex", "gemm_plan_set_scale",
-           "gemm_run_mx", "gemm_mx_scales_bytes", "gemm_mx_pack_scales", "gemm_model_params_load"]
+           "gemm_run_mx", "gemm_mx_scales_bytes", "gemm_mx_pack_scales", "gemm_model_params_load",
+           "gemm_plan_set_independent_inputs"]
 
 
 class GemmError(RuntimeError):
@@ -161,6 +162,7 @@ def _load_library(path: str):
         "gemm_run": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "gemm_run_ex": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp]),
         "gemm_plan_set_scale": (ctypes.c_int, [vp, ctypes.c_float]),
+        "gemm_plan_set_independent_inputs": (ctypes.c_int, [vp, i32]),
         "gemm_run_mx": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "gemm_mx_scales_bytes": (i64, [i64, i64]),
         "gemm_mx_pack_scales": (ctypes.c_int, [vp, i64, i64, i32, vp, vp]),
@@ -349,6 +351,12 @@ class Plan:
     def set_scale(self, alpha: float) -> None:
         """C = act(alpha·(A·B) + bias) (+ R); for FP8 operands alpha = scale_A·scale_B."""
         _check(lib().gemm_plan_set_scale(self._h, float(alpha)))
+
+    def set_independent_inputs(self, on: bool = True) -> None:
+        """Declare that this plan's operands are never written by the work
+        queued before a launch (independent GEMMs): loads then start while the
+        previous kernel drains."""
+        _check(lib().gemm_plan_set_independent_inputs(self._h, 1 if on else 0))
 
     def run_ex(self, A, B, bias, R, C, stream=None) -> None:
         """C = act(A·B + bias) + R for the residual epilogues (R may be C)."""

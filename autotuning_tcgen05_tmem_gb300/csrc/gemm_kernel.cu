@@ -1030,7 +1030,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // kernel on the stream; global memory is touched only once that kernel has
     // finished and its writes are visible.  The next kernel may then begin its
     // own set-up as soon as SMs free up.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // With independent operands (early_loads) the producer and the MMA warp go
+    // ahead: they read only A, B (and MX scales) and shared/tensor memory, and
+    // the epilogue warps, which write C, the split-K workspace, the counters and
+    // the status word, still wait here.
+    if (!p.early_loads || warp >= 2) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};

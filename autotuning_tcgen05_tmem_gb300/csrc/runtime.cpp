@@ -226,6 +226,7 @@ struct gemm_plan_s {
     int next_desc = 0;
     void *hA = nullptr, *hB = nullptr, *hBias = nullptr, *hC = nullptr;  // device buffers for run_host
     bool b_kmajor = false;           // B is first transposed into bt ([N, K], K contiguous)
+    bool independent_inputs = false; // operands never written by the preceding work on the stream
     void *bt = nullptr;
 };
 
@@ -605,6 +606,8 @@ int run_plan_mx(gemm_plan_t p, const void *A, const void *SA, const void *B, con
     kp.residual = R;
     kp.timeout_ns = g_timeout_ns.load();
     kp.debug_stall = g_debug_stall.load();
+    // (A K-major copy of B is written by the kernel just before: wait for it.)
+    kp.early_loads = (p->independent_inputs && !p->b_kmajor) ? 1 : 0;
     cudaError_t e = launch_gemm(p->dt, d->ma, d->mb, d->mc, mx ? &d->msa : nullptr, mx ? &d->msb : nullptr, kp, p->grid,
                                 p->smem_request, stream);
     if (e != cudaSuccess) return cuda_err(e, "kernel launch");
@@ -636,6 +639,13 @@ int mx_pack_scales(const void *scales, int64_t rows, int64_t K, int b_side, void
     cudaError_t e = launch_mx_pack(static_cast<const uint8_t *>(scales), rows, K, b_side,
                                    static_cast<uint8_t *>(packed), stream);
     if (e != cudaSuccess) return cuda_err(e, "MX scale packing launch");
+    return GEMM_OK;
+}
+
+int plan_set_independent_inputs(gemm_plan_t p, int32_t on)
+{
+    if (!p) return set_error(GEMM_ERR_INVALID_ARG, "null plan");
+    p->independent_inputs = on != 0;
     return GEMM_OK;
 }
 

@@ -312,6 +312,20 @@ int gemm_plan_with_config(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gem
  * call. */
 int gemm_plan_set_scale(gemm_plan_t plan, float alpha);
 
+/* Declare (on != 0) or withdraw (0) that the operands of this plan's launches
+ * (A, B, bias, R, MX scales) are never written by the work queued before a
+ * launch on its stream, e.g. independent GEMMs back to back.  Every launch
+ * allows programmatic overlap with the previous kernel on the stream; with this
+ * declaration the operand loads and MMAs start before that kernel has finished,
+ * and only the stores of C, the split-K exchange and the status word wait for
+ * it.  Without it (the default) the whole launch waits.  Ignored for plans that
+ * first copy B K-major (that copy is the previous kernel).  Applies to launches
+ * queued after the call.  A caller that breaks the declaration reads operands
+ * that may still be being written.  The producer's bounded waits (the device
+ * timeout) then also span what remains of the previous kernel: one that runs
+ * longer than the timeout makes the launch report GEMM_ERR_TIMEOUT. */
+int gemm_plan_set_independent_inputs(gemm_plan_t plan, int32_t on);
+
 /* The configuration a plan runs. */
 int gemm_plan_config(gemm_plan_t plan, gemm_config *out);
 
