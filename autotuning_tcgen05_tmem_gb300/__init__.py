@@ -19,6 +19,7 @@ from dataclasses import dataclass
 from . import _build
 
 BF16, FP32_TF32, FP8_E4M3, MXFP8_E4M3 = 0, 1, 2, 3
+OPERAND_A, OPERAND_B = 1, 2            # gemm_plan_set_independent_operands
 EPI_NONE, EPI_BIAS, EPI_BIAS_RELU, EPI_BIAS_GELU = 0, 1, 2, 3
 EPI_BIAS_RESIDUAL, EPI_BIAS_RELU_RESIDUAL, EPI_BIAS_GELU_RESIDUAL = 4, 5, 6
 EPILOGUES = {"none": EPI_NONE, "bias": EPI_BIAS, "relu": EPI_BIAS_RELU, "gelu": EPI_BIAS_GELU,
@@ -48,7 +49,7 @@ EXPORTS = ["gemm_version", "gemm_last_error", "gemm_device_params_default",
            "gemm_cache_save", "gemm_cache_load", "gemm_plan_launch_info", "gemm_select_config_set",
            "gemm_plan_from_list", "gemm_tune_batch", "gemm_run_ex", "gemm_plan_set_scale",
            "gemm_run_mx", "gemm_mx_scales_bytes", "gemm_mx_pack_scales", "gemm_model_params_load",
-           "gemm_plan_set_independent_inputs"]
+           "gemm_plan_set_independent_operands"]
 
 
 class GemmError(RuntimeError):
@@ -162,7 +163,7 @@ def _load_library(path: str):
         "gemm_run": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "gemm_run_ex": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp]),
         "gemm_plan_set_scale": (ctypes.c_int, [vp, ctypes.c_float]),
-        "gemm_plan_set_independent_inputs": (ctypes.c_int, [vp, i32]),
+        "gemm_plan_set_independent_operands": (ctypes.c_int, [vp, i32]),
         "gemm_run_mx": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "gemm_mx_scales_bytes": (i64, [i64, i64]),
         "gemm_mx_pack_scales": (ctypes.c_int, [vp, i64, i64, i32, vp, vp]),
@@ -352,11 +353,15 @@ class Plan:
         """C = act(alpha·(A·B) + bias) (+ R); for FP8 operands alpha = scale_A·scale_B."""
         _check(lib().gemm_plan_set_scale(self._h, float(alpha)))
 
-    def set_independent_inputs(self, on: bool = True) -> None:
-        """Declare that this plan's operands are never written by the work
-        queued before a launch (independent GEMMs): loads then start while the
-        previous kernel drains."""
-        _check(lib().gemm_plan_set_independent_inputs(self._h, 1 if on else 0))
+    def set_independent_operands(self, operands: str = "AB") -> None:
+        """Declare which operands ("A", "B", "AB" or "") the work queued before
+        a launch never writes: their copies start while the previous kernel
+        drains ("B" for a layer chain's weights, "AB" for independent GEMMs)."""
+        bad = set(operands) - {"A", "B"}
+        if bad:
+            raise ValueError(f"unknown operands {sorted(bad)}")
+        mask = (OPERAND_A if "A" in operands else 0) | (OPERAND_B if "B" in operands else 0)
+        _check(lib().gemm_plan_set_independent_operands(self._h, mask))
 
     def run_ex(self, A, B, bias, R, C, stream=None) -> None:
         """C = act(A·B + bias) + R for the residual epilogues (R may be C)."""

@@ -50,7 +50,7 @@ int plan_status(gemm_plan_t p);
 int plan_config(gemm_plan_t p, gemm_config *out);
 int plan_launch_info(gemm_plan_t p, gemm_launch_info *out);
 int plan_set_scale(gemm_plan_t p, float alpha);
-int plan_set_independent_inputs(gemm_plan_t p, int32_t on);
+int plan_set_independent_operands(gemm_plan_t p, int32_t mask);
 void destroy_plan(gemm_plan_t p);
 int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, uint64_t seed,
          std::vector<gemm_tune_row> &rows, gemm_rank_stats &stats, gemm_config *winner,
@@ -206,10 +206,10 @@ int gemm_run_ex(gemm_plan_t plan, const void *A, const void *B, const void *bias
     return run_plan_ex(plan, A, B, bias, R, C, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int gemm_plan_set_independent_inputs(gemm_plan_t plan, int32_t on)
+int gemm_plan_set_independent_operands(gemm_plan_t plan, int32_t mask)
 {
     clear_error();
-    return plan_set_independent_inputs(plan, on);
+    return plan_set_independent_operands(plan, mask);
 }
 
 int gemm_model_params_load(const char *path, gemm_device_params *dev)

@@ -1030,11 +1030,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // kernel on the stream; global memory is touched only once that kernel has
     // finished and its writes are visible.  The next kernel may then begin its
     // own set-up as soon as SMs free up.
-    // With independent operands (early_loads) the producer and the MMA warp go
-    // ahead: they read only A, B (and MX scales) and shared/tensor memory, and
-    // the epilogue warps, which write C, the split-K workspace, the counters and
-    // the status word, still wait here.
-    if (!p.early_loads || warp >= 2) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Operands declared independent of the previous kernel (early mask: bit 0
+    // MMA-A, bit 1 MMA-B) let the producer go ahead: with both, it skips the
+    // wait; with one, it copies that operand's first stages and then waits
+    // (below).  The MMA warp touches only shared and tensor memory.  The
+    // epilogue warps, which read bias and R and write C, the split-K workspace,
+    // the counters and the status word, always wait here.
+    const uint32_t early_mask = (uint32_t)p.early_mask & 3u;
+    if (early_mask == 0u || warp >= 2) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
@@ -1052,63 +1055,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sb0 = base + p.off_b;
         const int32_t a_loads = A_MN ? cta_rows / SPAN : bk / SPAN;
         const int32_t b_loads = B_MN ? cta_bcols / SPAN : bk / SPAN;
-        uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
-        bool ok = true;
-        for (int64_t u = unit0; ok && u < p.num_units; u += unit_step) {
-            const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
+        // One stage's copies, split by operand: bit 0 of `what` issues MMA-A's
+        // panel (with its MX scale atoms), bit 1 MMA-B's; `arm` first posts the
+        // stage's full byte count on its barrier.
+        auto fill = [&](uint32_t stage, const SchedUnit &w, int32_t kb, uint32_t what, bool arm) {
             const int32_t ra = w.tile_m * bm + (int32_t)prank * 128;
             const int32_t rb = w.tile_n * bn + (int32_t)prank * cta_bcols;
-            for (int32_t kb = w.kb_begin; kb < w.kb_end; ++kb) {
-                ok = __all_sync(0xFFFFFFFFu, wait_bar(empty0 + 8u * stage, phase ^ 1u, ctl, SITE_PRODUCER_EMPTY));
-                if (!ok) break;
-                const uint32_t fb = full0 + 8u * stage;
-                const uint32_t sa = base + stage * a_bytes;
-                const uint32_t sb = sb0 + stage * b_bytes;
-                const int32_t k0 = kb * bk;
-                if (leader && prank == 0) {
-                    mbar_arrive_expect_tx(fb, tx);
-                    // K-major operand: boxes of [rows x one span of K], one per span;
-                    // MN-major operand: boxes of [bk x one span of MN], one per span.
+            const uint32_t fb = full0 + 8u * stage;
+            const uint32_t sa = base + stage * a_bytes;
+            const uint32_t sb = sb0 + stage * b_bytes;
+            const int32_t k0 = kb * bk;
+            if (leader && prank == 0) {
+                if (arm) mbar_arrive_expect_tx(fb, tx);
+                // K-major operand: boxes of [rows x one span of K], one per span;
+                // MN-major operand: boxes of [bk x one span of MN], one per span.
+                if (what & 1u)
                     for (int32_t j = 0; j < a_loads; ++j) {
                         if constexpr (A_MN) tma_load_2d(sa + (uint32_t)(j * bk * 128), &tmA, fb, ra + j * SPAN, k0);
                         else tma_load_2d(sa + (uint32_t)(j * cta_rows * 128), &tmA, fb, k0 + j * SPAN, ra);
                     }
+                if (what & 2u)
                     for (int32_t j = 0; j < b_loads; ++j) {
                         if constexpr (B_MN) tma_load_2d(sb + (uint32_t)(j * bk * 128), &tmB, fb, rb + j * SPAN, k0);
                         else tma_load_2d(sb + (uint32_t)(j * cta_bcols * 128), &tmB, fb, k0 + j * SPAN, rb);
                     }
-                    if constexpr (DT == 3) {
-                        // The stage's scale atoms: for each 128 rows of MMA-A,
-                        // then each 128 columns of MMA-B (one atom when bn < 128:
-                        // such a tile starts on an atom), its bk/128 consecutive
-                        // K atoms, one tensor copy each (the packed array seen as
-                        // rows of one 512-byte atom, 128 words wide).  Swapped,
-                        // MMA-A is B (rows along N) and MMA-B is A.
-                        const uint32_t ka = (uint32_t)bk / 128u, run = ka * 512u;
-                        const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
-                        const int32_t k_atom = kb * (int32_t)ka;
-                        const CUtensorMap *sm_a = A_MN || p.swap_ab ? &tmSB : &tmSA;
-                        const CUtensorMap *sm_b = A_MN || p.swap_ab ? &tmSA : &tmSB;
-                        const int32_t na = pair ? 1 : bm / 128, nb = max(1, bn / 128);
+                if constexpr (DT == 3) {
+                    // The stage's scale atoms: for each 128 rows of MMA-A,
+                    // then each 128 columns of MMA-B (one atom when bn < 128:
+                    // such a tile starts on an atom), its bk/128 consecutive
+                    // K atoms, one tensor copy each (the packed array seen as
+                    // rows of one 512-byte atom, 128 words wide).  Swapped,
+                    // MMA-A is B (rows along N) and MMA-B is A.
+                    const uint32_t ka = (uint32_t)bk / 128u, run = ka * 512u;
+                    const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
+                    const int32_t k_atom = kb * (int32_t)ka;
+                    const CUtensorMap *sm_a = A_MN || p.swap_ab ? &tmSB : &tmSA;
+                    const CUtensorMap *sm_b = A_MN || p.swap_ab ? &tmSA : &tmSB;
+                    const int32_t na = pair ? 1 : bm / 128, nb = max(1, bn / 128);
+                    if (what & 1u)
                         for (int32_t h = 0; h < na; ++h)
                             tma_load_2d(sf + (uint32_t)h * run, sm_a, fb, 0,
                                         (w.tile_m * (bm / 128) + h) * p.sf_kt + k_atom);
+                    if (what & 2u)
                         for (int32_t j = 0; j < nb; ++j)
                             tma_load_2d(sf + (uint32_t)(na + j) * run, sm_b, fb, 0,
                                         (w.tile_n * bn / 128 + j) * p.sf_kt + k_atom);
-                    }
-                } else if (leader) {
-                    if constexpr (pair) {
-                        // Second CTA of a pair: its halves land in its own shared
-                        // memory and complete on the leader's barrier, where the MMAs wait.
-                        const uint32_t fbr = mapa_u32(fb, 0);
-                        mbar_arrive_expect_tx_remote(fbr, tx);
+                }
+            } else if (leader) {
+                if constexpr (pair) {
+                    // Second CTA of a pair: its halves land in its own shared
+                    // memory and complete on the leader's barrier, where the MMAs wait.
+                    const uint32_t fbr = mapa_u32(fb, 0);
+                    if (arm) mbar_arrive_expect_tx_remote(fbr, tx);
+                    if (what & 1u)
                         for (int32_t j = 0; j < a_loads; ++j) {
                             if constexpr (A_MN)
                                 tma_load_2d_pair(sa + (uint32_t)(j * bk * 128), &tmA, fbr, ra + j * SPAN, k0);
                             else
                                 tma_load_2d_pair(sa + (uint32_t)(j * cta_rows * 128), &tmA, fbr, k0 + j * SPAN, ra);
                         }
+                    if (what & 2u)
                         for (int32_t j = 0; j < b_loads; ++j) {
                             if constexpr (B_MN)
                                 tma_load_2d_pair(sb + (uint32_t)(j * bk * 128), &tmB, fbr, rb + j * SPAN, k0);
@@ -1116,20 +1122,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tma_load_2d_pair(sb + (uint32_t)(j * cta_bcols * 128), &tmB, fbr, k0 + j * SPAN,
                                                  rb);
                         }
-                        if constexpr (DT == 3) {
-                            // MX: this CTA's 128 rows of A scales and all of the
-                            // tile's B scales (the pair MMA reads each CTA's own).
-                            const uint32_t ka = (uint32_t)bk / 128u, run = ka * 512u;
-                            const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
-                            const int32_t k_atom = kb * (int32_t)ka;
-                            tma_load_2d_pair(sf, &tmSA, fbr, 0, (w.tile_m * 2 + 1) * p.sf_kt + k_atom);
+                    if constexpr (DT == 3) {
+                        // MX: this CTA's 128 rows of A scales and all of the
+                        // tile's B scales (the pair MMA reads each CTA's own).
+                        const uint32_t ka = (uint32_t)bk / 128u, run = ka * 512u;
+                        const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
+                        const int32_t k_atom = kb * (int32_t)ka;
+                        if (what & 1u) tma_load_2d_pair(sf, &tmSA, fbr, 0, (w.tile_m * 2 + 1) * p.sf_kt + k_atom);
+                        if (what & 2u)
                             for (int32_t j = 0; j < bn / 128; ++j)
                                 tma_load_2d_pair(sf + (uint32_t)(1 + j) * run, &tmSB, fbr, 0,
                                                  (w.tile_n * bn / 128 + j) * p.sf_kt + k_atom);
-                        }
                     }
                 }
-                __syncwarp();
+            }
+            __syncwarp();
+        };
+
+        uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
+        // One operand declared independent of the previous kernel (early mask
+        // 1 or 2): its copies for the first pass over the ring go out before
+        // the dependency wait (the ring is fresh, so no slot needs waiting
+        // for), and the other operand's follow once the previous kernel's
+        // writes are visible.
+        int32_t pre = 0;
+        if (early_mask == 1u || early_mask == 2u) {
+            for (int64_t u = unit0; pre < stages && u < p.num_units; u += unit_step) {
+                const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
+                for (int32_t kb = w.kb_begin; pre < stages && kb < w.kb_end; ++kb, ++pre)
+                    fill((uint32_t)pre, w, kb, early_mask, true);
+            }
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+        }
+        bool ok = true;
+        int32_t filled = 0;
+        for (int64_t u = unit0; ok && u < p.num_units; u += unit_step) {
+            const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
+            for (int32_t kb = w.kb_begin; kb < w.kb_end; ++kb) {
+                if (filled < pre) {
+                    fill(stage, w, kb, 3u & ~early_mask, false);    // the deferred operand
+                } else {
+                    ok = __all_sync(0xFFFFFFFFu, wait_bar(empty0 + 8u * stage, phase ^ 1u, ctl, SITE_PRODUCER_EMPTY));
+                    if (!ok) break;
+                    fill(stage, w, kb, 3u, true);
+                }
+                ++filled;
                 armed |= 1u << stage;
                 armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == (uint32_t)stages) {

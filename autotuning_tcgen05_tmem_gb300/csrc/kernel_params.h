@@ -42,9 +42,10 @@ struct KernelParams {
     int32_t *status;                   // device status word (0 = ok)
     int64_t timeout_ns;                // bound of every mbarrier wait
     int32_t debug_stall;               // epilogue waits on a barrier nothing signals
-    int32_t early_loads;               // 1: the operands are not written by the work before this
-                                       // launch, so the producer loads them before the previous
-                                       // kernel has finished (epilogue warps still wait for it)
+    int32_t early_mask;                // operands not written by the work before this launch
+                                       // (bit 0 MMA-A, bit 1 MMA-B): the producer copies them
+                                       // before the previous kernel has finished (epilogue
+                                       // warps still wait for it)
     int32_t coop_fixup;                // split-K slices finalise shares of their tile together
                                        // (launched cooperatively: every unit has its own CTA)
     int32_t pair;                      // 1: cta_group::2, consecutive CTAs share 256-row tiles

@@ -226,7 +226,8 @@ struct gemm_plan_s {
     int next_desc = 0;
     void *hA = nullptr, *hB = nullptr, *hBias = nullptr, *hC = nullptr;  // device buffers for run_host
     bool b_kmajor = false;           // B is first transposed into bt ([N, K], K contiguous)
-    bool independent_inputs = false; // operands never written by the preceding work on the stream
+    int32_t independent = 0;         // GEMM_OPERAND_A | GEMM_OPERAND_B: operands that the work
+                                     // queued before a launch never writes
     void *bt = nullptr;
 };
 
@@ -606,8 +607,15 @@ int run_plan_mx(gemm_plan_t p, const void *A, const void *SA, const void *B, con
     kp.residual = R;
     kp.timeout_ns = g_timeout_ns.load();
     kp.debug_stall = g_debug_stall.load();
-    // (A K-major copy of B is written by the kernel just before: wait for it.)
-    kp.early_loads = (p->independent_inputs && !p->b_kmajor) ? 1 : 0;
+    // Declared operands map to the kernel's MMA-A (bit 0) and MMA-B (bit 1);
+    // swapped, MMA-A is B.  A K-major copy of B is written by the kernel just
+    // before, so B then always waits.
+    {
+        const int32_t ua = p->independent & GEMM_OPERAND_A;
+        const int32_t ub = p->b_kmajor ? 0 : (p->independent & GEMM_OPERAND_B);
+        const int32_t ka = p->cfg.swap_ab ? ub : ua, kb = p->cfg.swap_ab ? ua : ub;
+        kp.early_mask = (ka ? 1 : 0) | (kb ? 2 : 0);
+    }
     cudaError_t e = launch_gemm(p->dt, d->ma, d->mb, d->mc, mx ? &d->msa : nullptr, mx ? &d->msb : nullptr, kp, p->grid,
                                 p->smem_request, stream);
     if (e != cudaSuccess) return cuda_err(e, "kernel launch");
@@ -642,10 +650,11 @@ int mx_pack_scales(const void *scales, int64_t rows, int64_t K, int b_side, void
     return GEMM_OK;
 }
 
-int plan_set_independent_inputs(gemm_plan_t p, int32_t on)
+int plan_set_independent_operands(gemm_plan_t p, int32_t mask)
 {
     if (!p) return set_error(GEMM_ERR_INVALID_ARG, "null plan");
-    p->independent_inputs = on != 0;
+    if (mask & ~(GEMM_OPERAND_A | GEMM_OPERAND_B)) return set_error(GEMM_ERR_INVALID_ARG, "unknown operand bits");
+    p->independent = mask;
     return GEMM_OK;
 }
 

@@ -61,9 +61,10 @@ def parse_args():
     ap.add_argument("--search-quality", action="store_true",
                     help="model-guided top-k vs random-k at equal measurement budgets, from one "
                          "exhaustive tuning table per workload (one JSON line per workload)")
-    ap.add_argument("--independent", action="store_true",
-                    help="headline with the GEMMs declared independent (operand loads overlap the previous "
-                         "kernel); by default every launch waits for the previous kernel, as in a chain")
+    ap.add_argument("--operands", choices=["none", "B", "AB"], default="none",
+                    help="operands declared independent of the previous GEMM: none (the default) makes every "
+                         "launch wait for the previous kernel; B as the weights of a layer chain, whose A is "
+                         "the previous layer's output; AB for independent GEMMs")
     ap.add_argument("--config", default=None,
                     help="explicit tile config bm,bn,bk,stages,raster,group,split_k,cta_group,swap_ab "
                          "(skips tuning; used to profile one configuration)")
@@ -335,6 +336,20 @@ def time_plan(plan, sets, steps, warmup, eager=False):
     return run, mode, stream
 
 
+OPERAND_NOTES = {
+    "none": "every launch waits for the previous kernel before touching memory",
+    "B": "B declared independent (the weights of a layer chain): each launch copies its first stages of B "
+         "while the previous GEMM drains, and A after it has finished",
+    "AB": "A and B declared independent (independent GEMMs): operand copies and MMAs run ahead of the previous "
+          "GEMM's drain, and tiles that leave SMs idle fill them with the next GEMM; C stores still wait",
+}
+
+
+def declared(operands: str) -> str:
+    """The operand string a plan takes for a --operands choice."""
+    return "" if operands == "none" else operands
+
+
 def region_gemm_seconds(plan, sets, steps, warmup, eager=False) -> float:
     """Seconds per GEMM over `steps` steps of `plan` (CUDA events on its stream)."""
     import torch
@@ -422,10 +437,14 @@ def sweep(args):
         clocks.mark("t1")
         shape_clocks = clocks.summary()
         with g.plan_with_config(w.M, w.N, w.K, w.dtype, w.epi, g.fixed_config(w.dtype, devp)) as fp:
+            fp.set_independent_operands(declared(args.operands))
             t_fixed = time_gemm(fp, sets, steps, 5)
-        plan.set_independent_inputs(True)     # the rotating sets are independent GEMMs
-        t_indep = time_gemm(plan, sets, max(3, steps // 2), 5)
-        plan.set_independent_inputs(False)
+        t_decl = {}
+        for decl in ("none", "B", "AB"):
+            if decl != args.operands:
+                plan.set_independent_operands("" if decl == "none" else decl)
+                t_decl[decl] = time_gemm(plan, sets, max(3, steps // 2), 5) * 1e6
+        plan.set_independent_operands(declared(args.operands))
         # A timed region longer than a second runs under the power cap: the
         # sustained tensor peak is the denominator there (as in the main line).
         region_s = t_tuned * steps * nsets
@@ -439,7 +458,8 @@ def sweep(args):
                 "tflops": flops / t_tuned / 1e12, "gbs": cbytes / t_tuned / 1e9,
                 "bound": "tensor" if flops / (tpeak * 1e12) >= cbytes / (bw * 1e9) else "hbm",
                 "roofline_frac": roof_t / t_tuned, "fixed_us": t_fixed * 1e6,
-                "tuned_vs_fixed": t_fixed / t_tuned, "independent_us": t_indep * 1e6, "plan_seconds": tune_s, "timed_region_s": region_s,
+                "tuned_vs_fixed": t_fixed / t_tuned, "operands": args.operands, "tuned_us_other_operands": t_decl,
+                "plan_seconds": tune_s, "timed_region_s": region_s,
                 "candidates": len(cands), "host_rank_us": host_rank_us,
                 "model_best_us": min(preds) if preds else None, "clocks": shape_clocks,
                 "peaks": f"{peak_src} bf16 {'sustained' if sustained else 'burst'} {bf16_peak} TFLOP/s, "
@@ -564,9 +584,9 @@ def main():
         plan = g.plan(w.M, w.N, w.K, w.dtype, w.epi)
     plan_s = time.perf_counter() - t0
     cfg = plan.config
-    # By default every launch waits for the previous kernel, as in a chain of
-    # GEMMs; --independent declares the rotating sets independent (they are).
-    plan.set_independent_inputs(args.independent)
+    # By default nothing is declared independent: every launch waits for the
+    # previous kernel, as in any chain of GEMMs (--operands picks others).
+    plan.set_independent_operands(declared(args.operands))
     launches_per_gemm = 1 + plan.launch_info.b_transposed   # (+ the transpose into a K-major B)
 
     run, mode, stream = time_plan(plan, sets, args.steps, args.warmup, args.eager)
@@ -630,9 +650,7 @@ def main():
                             f"{devp.l2_bytes / 1e6:.0f} MB)" if nsets * set_bytes > 2 * devp.l2_bytes
                       else f"each set ({set_bytes / 1e6:.0f} MB) exceeds L2",
                       "launch": mode, "parallelism": f"replicas x{world}",
-                      "operands": ("declared independent: operand loads start while the previous GEMM drains; "
-                                   "its C stores still wait for it" if args.independent else
-                                   "every launch waits for the previous kernel (as in a chain of GEMMs)")},
+                      "operands": OPERAND_NOTES[args.operands]},
            "roofline": roof,
            "gpu_launches": args.steps * nsets * launches_per_gemm,
            "clocks": clocks.summary(),
@@ -642,7 +660,7 @@ def main():
     if not args.no_fixed and rank == 0:
         fixed = g.fixed_config(w.dtype, devp)
         with g.plan_with_config(w.M, w.N, w.K, w.dtype, w.epi, fixed) as fp:
-            fp.set_independent_inputs(args.independent)
+            fp.set_independent_operands(declared(args.operands))
             fixed_gemm_s = region_gemm_seconds(fp, sets, max(20, args.steps // 4), args.warmup, args.eager)
         out["fixed_config"] = fixed.asdict()
         out["fixed_value"] = flops / fixed_gemm_s / 1e12
@@ -656,23 +674,21 @@ def main():
                        "best_us": st.best_us, "fixed_us": st.fixed_us,
                        "break_even_calls": (st.tune_seconds / (saved_us * 1e-6)) if saved_us > 0 else None}
 
-    # --- the other operand declaration, tuned and fixed tile -----------------
+    # --- the other operand declarations, tuned and fixed tile ----------------
     if not args.no_fixed and rank == 0:
-        other = not args.independent
-        alt = {"declared_independent": other}
-        plan.set_independent_inputs(other)
-        alt["value"] = flops / region_gemm_seconds(plan, sets, max(20, args.steps // 4), args.warmup, args.eager)
-        alt["value"] /= 1e12
-        plan.set_independent_inputs(args.independent)
-        with g.plan_with_config(w.M, w.N, w.K, w.dtype, w.epi, g.fixed_config(w.dtype, devp)) as fp:
-            fp.set_independent_inputs(other)
-            alt["fixed_value"] = flops / region_gemm_seconds(fp, sets, max(20, args.steps // 4), args.warmup,
-                                                             args.eager) / 1e12
-        alt["tuned_vs_fixed"] = alt["value"] / alt["fixed_value"]
-        alt["note"] = ("independent GEMMs: the next GEMM's operand loads and MMAs overlap the previous one's "
-                       "drain, so tiles that leave SMs idle (the fixed tile here) fill them with the next GEMM"
-                       if other else "every launch waits for the previous kernel")
-        out["other_operand_declaration"] = alt
+        alt = {}
+        for decl in ("none", "B", "AB"):
+            if decl == args.operands:
+                continue
+            plan.set_independent_operands(declared(decl))
+            v = flops / region_gemm_seconds(plan, sets, max(20, args.steps // 4), args.warmup, args.eager) / 1e12
+            with g.plan_with_config(w.M, w.N, w.K, w.dtype, w.epi, g.fixed_config(w.dtype, devp)) as fp:
+                fp.set_independent_operands(declared(decl))
+                fv = flops / region_gemm_seconds(fp, sets, max(20, args.steps // 4), args.warmup,
+                                                 args.eager) / 1e12
+            alt[decl] = {"value": v, "fixed_value": fv, "tuned_vs_fixed": v / fv, "note": OPERAND_NOTES[decl]}
+        plan.set_independent_operands(declared(args.operands))
+        out["other_operand_declarations"] = alt
 
     # --- end to end through the host-buffer entry point ------------------------
     if not args.no_e2e and rank == 0 and w.dtype == "mxfp8":

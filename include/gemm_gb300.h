@@ -312,19 +312,28 @@ int gemm_plan_with_config(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gem
  * call. */
 int gemm_plan_set_scale(gemm_plan_t plan, float alpha);
 
-/* Declare (on != 0) or withdraw (0) that the operands of this plan's launches
- * (A, B, bias, R, MX scales) are never written by the work queued before a
- * launch on its stream, e.g. independent GEMMs back to back.  Every launch
- * allows programmatic overlap with the previous kernel on the stream; with this
- * declaration the operand loads and MMAs start before that kernel has finished,
- * and only the stores of C, the split-K exchange and the status word wait for
- * it.  Without it (the default) the whole launch waits.  Ignored for plans that
- * first copy B K-major (that copy is the previous kernel).  Applies to launches
- * queued after the call.  A caller that breaks the declaration reads operands
- * that may still be being written.  The producer's bounded waits (the device
- * timeout) then also span what remains of the previous kernel: one that runs
- * longer than the timeout makes the launch report GEMM_ERR_TIMEOUT. */
-int gemm_plan_set_independent_inputs(gemm_plan_t plan, int32_t on);
+/* Operands named in gemm_plan_set_independent_operands. */
+enum { GEMM_OPERAND_A = 1, GEMM_OPERAND_B = 2 };
+
+/* Declare which operands of this plan's launches are never written by the
+ * work queued before a launch on its stream: a mask of GEMM_OPERAND_A (A, and
+ * SA for block-scaled FP8) and GEMM_OPERAND_B (B, and SB); 0, the default,
+ * withdraws the declaration.  Every launch allows programmatic overlap with the
+ * previous kernel on the stream, and by default it touches no global memory
+ * before that kernel has finished.  In a chain of layers B (the weights) is
+ * independent and A (the previous layer's output) is not: declaring B lets
+ * the launch copy the first pipeline stages of B while the previous kernel
+ * drains, and copy A once it has finished.  Declaring both (independent GEMMs
+ * back to back) lets all operand copies and MMAs run ahead; then the
+ * producer's bounded waits (the device timeout) also span what remains of the
+ * previous kernel, and one that runs longer than the timeout makes the launch
+ * report GEMM_ERR_TIMEOUT.  bias and R are always read after the wait, and C,
+ * the split-K exchange and the status word are written after it.  B is
+ * treated as dependent in plans that first copy it K-major (that copy is the
+ * previous kernel).  Applies to launches queued after the call; a caller that
+ * breaks the declaration reads operands that may still be being written.
+ * GEMM_ERR_INVALID_ARG for a null plan or other bits in the mask. */
+int gemm_plan_set_independent_operands(gemm_plan_t plan, int32_t mask);
 
 /* The configuration a plan runs. */
 int gemm_plan_config(gemm_plan_t plan, gemm_config *out);
