@@ -578,6 +578,14 @@ __device__ __forceinline__ uint64_t atom_release_gpu_add_u64(uint64_t *ptr, uint
     return old;
 }
 
+// Adds with acquire-release semantics at GPU scope; returns the count before.
+__device__ __forceinline__ int32_t atom_acq_rel_gpu_add(int32_t *ptr, int32_t v)
+{
+    int32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *ptr)
 {
     uint64_t v;
@@ -585,35 +593,8 @@ __device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *ptr)
     return v;
 }
 
-__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *ptr)
-{
-    int32_t v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
-    return v;
-}
-
-// Waits until *ptr >= target (other CTAs of this launch increment it), with
-// the same bound and abort protocol as the mbarrier waits.
-__device__ __noinline__ bool wait_counter(const int32_t *ptr, int32_t target, const WaitCtl &c, int32_t site)
-{
-    if (ld_acquire_gpu(ptr) >= target) return true;
-    const long long limit_cycles = (long long)((double)c.timeout_ns * 2.2);
-    const long long t0 = clock64();
-    for (uint32_t it = 1;; ++it) {
-        __nanosleep(32);
-        if (ld_acquire_gpu(ptr) >= target) return true;
-        if ((it & 15u) == 0) {
-            if (*c.abort) return false;
-            if (clock64() - t0 > limit_cycles) {
-                *c.abort = 1;
-                atomicCAS(c.status, 0, site);
-                return false;
-            }
-        }
-    }
-}
-
-// Waits until *ptr >= target (64-bit arrival counts), bounded like the others.
+// Waits until *ptr >= target (64-bit arrival counts that other CTAs of this
+// launch increment), with the same bound and abort protocol as the mbarrier waits.
 __device__ __noinline__ bool wait_epoch(const uint64_t *ptr, uint64_t target, const WaitCtl &c, int32_t site)
 {
     if (ld_acquire_gpu_u64(ptr) >= target) return true;
@@ -1030,14 +1011,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // kernel on the stream; global memory is touched only once that kernel has
     // finished and its writes are visible.  The next kernel may then begin its
     // own set-up as soon as SMs free up.
-    // Operands declared independent of the previous kernel (early mask: bit 0
-    // MMA-A, bit 1 MMA-B) let the producer go ahead: with both, it skips the
-    // wait; with one, it copies that operand's first stages and then waits
-    // (below).  The MMA warp touches only shared and tensor memory.  The
-    // epilogue warps, which read bias and R and write C, the split-K workspace,
-    // the counters and the status word, always wait here.
+    // The epilogue warps, which read bias and R and write C, the split-K
+    // workspace, the counters and the status word, wait here, and so does the
+    // MMA warp, so that its bounded waits start only once the previous kernel
+    // has finished.  The producer waits right before its first copy: its
+    // schedule and barrier work before that (whose first pass fetches cold
+    // code and parameters, measured at about 0.9 us) overlaps the previous
+    // kernel's drain.  Operands declared independent of the previous kernel
+    // (early mask: bit 0 MMA-A, bit 1 MMA-B) let the producer go further: with
+    // one it copies that operand's first stages before waiting; with both
+    // neither it nor the MMA warp waits.
     const uint32_t early_mask = (uint32_t)p.early_mask & 3u;
-    if (early_mask == 0u || warp >= 2) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (warp >= 2 || (warp == 1 && early_mask != 3u)) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
@@ -1146,6 +1131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // for), and the other operand's follow once the previous kernel's
         // writes are visible.
         int32_t pre = 0;
+        bool waited = early_mask == 3u;
         if (early_mask == 1u || early_mask == 2u) {
             for (int64_t u = unit0; pre < stages && u < p.num_units; u += unit_step) {
                 const SchedUnit w = schedule_unit(u, p.tiles_m, p.tiles_n, p.split_k, p.raster, p.group, p.num_kb);
@@ -1153,6 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fill((uint32_t)pre, w, kb, early_mask, true);
             }
             asm volatile("griddepcontrol.wait;" ::: "memory");
+            waited = true;
         }
         bool ok = true;
         int32_t filled = 0;
@@ -1164,6 +1151,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     ok = __all_sync(0xFFFFFFFFu, wait_bar(empty0 + 8u * stage, phase ^ 1u, ctl, SITE_PRODUCER_EMPTY));
                     if (!ok) break;
+                    if (!waited) {
+                        asm volatile("griddepcontrol.wait;" ::: "memory");
+                        waited = true;
+                    }
                     fill(stage, w, kb, 3u, true);
                 }
                 ++filled;
@@ -1633,17 +1624,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Split-K fix-up.  Cooperative (one wave, cooperative launch):
                 // every K slice of the tile arrives, waits for the others, and
                 // finalises its share of the tile's 32-row blocks (block b goes to
-                // slice b mod S); the last slice to leave resets the counter.
-                // Otherwise the last slice to arrive finalises the whole tile.
-                // Either way the partials are summed in slice order.
-                __threadfence();
+                // slice b mod S); the arrival counts only grow, and this slice's
+                // own arrival names its launch's base.  Otherwise the last slice
+                // to arrive finalises the whole tile and resets the count.  Either
+                // way the partials are summed in slice order.  One thread's
+                // release (after the CTA barrier that orders every epilogue
+                // thread's partial stores before it) publishes the CTA's partial;
+                // its acquire, passed on by the next CTA barrier, makes the other
+                // slices' partials visible to every epilogue thread.
                 named_bar_sync(1, kEpiThreads);
                 if (ew == 0 && lane == 0) {
-                    const int32_t old = atomicAdd(e_counters + xtile, 1);
                     int32_t mine;
                     if (e_coop) {
-                        mine = wait_counter(e_counters + xtile, e_split_k, ctl, SITE_FIXUP) ? 1 : 0;
+                        const uint64_t before = atom_release_gpu_add_u64(e_epochs + xtile, 1);
+                        const uint64_t target = before - before % (uint64_t)e_split_k + (uint64_t)e_split_k;
+                        mine = wait_epoch(e_epochs + xtile, target, ctl, SITE_FIXUP) ? 1 : 0;
                     } else {
+                        const int32_t old = atom_acq_rel_gpu_add(e_counters + xtile, 1);
                         mine = (old == e_split_k - 1) ? 1 : 0;
                         if (mine) atomicExch(e_counters + xtile, 0);
                     }
@@ -1653,7 +1650,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool mine = *last_flag != 0;
                 named_bar_sync(1, kEpiThreads);   // the flag is rewritten by the next unit
                 if (mine) {
-                    __threadfence();
                     const float4 *tile_ws = reinterpret_cast<const float4 *>(
                         e_workspace + (size_t)xtile * e_split_k * (size_t)tile_elems);
                     const size_t slice4 = (size_t)tile_elems / 4;
@@ -1716,13 +1712,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int32_t xn = r0 + rg * 32, ym = c0 + c * 16;
                             if (e_res) add_residual_cols<ODT>(v, e_resid, e_rows, ym, xn + lane, e_cols, e_rows);
                             store_cols_chunk<ODT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
-                        }
-                    }
-                    if (e_coop) {
-                        named_bar_sync(1, kEpiThreads);
-                        if (ew == 0 && lane == 0) {
-                            const int32_t old = atomicAdd(e_counters + xtile, 1);
-                            if (old == 2 * e_split_k - 1) atomicExch(e_counters + xtile, 0);
                         }
                     }
                 }
