@@ -1365,19 +1365,90 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // blocks it does not own into their owner's pipeline ring (free once
                 // the owner's MMAs are done, which the owner announces), the owner
                 // adds the S partials in slice order and runs the epilogue.
+                // Swapped, a block is 128 rows x 16 columns (8 KB, half a slot).
                 const int32_t S = e_split_k, me = w.split;
                 const int32_t nblocks = halves * chunks;
                 const int32_t gsz = nblocks >= 2 * S ? 2 : 1;
+                const uint32_t blk_bytes = e_swap_ab ? kRedBlockBytes / 2u : kRedBlockBytes;
                 if (ew == 0 && lane == 0) {
                     uint32_t owned = 0;
                     for (int32_t b = 0; b < nblocks; ++b) owned += ((b / gsz) % S == me) ? 1u : 0u;
-                    mbar_arrive_expect_tx(recv_bar, owned * (uint32_t)(S - 1) * kRedBlockBytes);
+                    mbar_arrive_expect_tx(recv_bar, owned * (uint32_t)(S - 1) * blk_bytes);
                     for (int32_t o = 0; o < S; ++o)
                         if (o != me) mbar_arrive_remote(mapa_u32(peer_ready_bar, (uint32_t)o));
                 }
                 bool cok = wait_bar_cluster(peer_ready_bar, 0, ctl, SITE_CLUSTER);
                 if (named_bar_any(1, kEpiThreads, !cok)) break;
                 const uint32_t row16 = (uint32_t)(q * 32 + lane) * 16u;
+                if (e_swap_ab) {
+                    // Same protocol; each lane holds one output column (its TMEM
+                    // row) and 16 output rows per chunk.
+                    for (int32_t h = 0; h < halves; ++h) {
+#pragma unroll 1
+                        for (int ci = 0; ci < 4; ++ci) {
+                            const int32_t c = cg + 2 * ci;
+                            if (c >= chunks) break;
+                            const int32_t b = h * chunks + c, j = b / gsz, o = j % S;
+                            if (o == me) continue;
+                            const int32_t ob = (j / S) * gsz + (b - j * gsz);
+                            const uint32_t slot = (uint32_t)(ob * (S - 1) + (me < o ? me : me - 1));
+                            float v[16];
+                            tmem_load_chunk<16>(tacc + (uint32_t)(h * e_bn + c * 16), v);
+                            const uint32_t dst = mapa_u32(base + slot * kRedBlockBytes + row16, (uint32_t)o);
+                            const uint32_t rbar = mapa_u32(recv_bar, (uint32_t)o);
+#pragma unroll
+                            for (int j4 = 0; j4 < 4; ++j4)
+                                st_async_v4(dst + (uint32_t)j4 * 2048u, v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2],
+                                            v[4 * j4 + 3], rbar);
+                        }
+                    }
+                    cok = wait_bar_cluster(recv_bar, 0, ctl, SITE_CLUSTER);
+                    if (named_bar_any(1, kEpiThreads, !cok)) break;
+                    for (int32_t h = 0; h < halves; ++h) {
+#pragma unroll 1
+                        for (int ci = 0; ci < 4; ++ci) {
+                            const int32_t c = cg + 2 * ci;
+                            if (c >= chunks) break;
+                            const int32_t b = h * chunks + c, j = b / gsz;
+                            if (j % S != me) continue;
+                            const int32_t ob = (j / S) * gsz + (b - j * gsz);
+                            float v[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+#pragma unroll 1
+                            for (int32_t s = 0; s < S; ++s) {
+                                if (s == me) {
+                                    float t[16];
+                                    tmem_load_chunk<16>(tacc + (uint32_t)(h * e_bn + c * 16), t);
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) v[i] += t[i];
+                                } else {
+                                    const uint32_t slot = (uint32_t)(ob * (S - 1) + (s < me ? s : s - 1));
+                                    const uint32_t src = base + slot * kRedBlockBytes + row16;
+#pragma unroll
+                                    for (int j4 = 0; j4 < 4; ++j4) {
+                                        const float4 t = ld_shared_v4(src + (uint32_t)j4 * 2048u);
+                                        v[4 * j4] += t.x;
+                                        v[4 * j4 + 1] += t.y;
+                                        v[4 * j4 + 2] += t.z;
+                                        v[4 * j4 + 3] += t.w;
+                                    }
+                                }
+                            }
+                            bias_act_cols(v, h == 0 ? brow[0] : brow[1], e_epi, e_alpha);
+                            const int32_t xn = r0 + h * 128 + q * 32;  // output column block (user N)
+                            const int32_t ym = c0 + c * 16;            // output row block (user M)
+                            if (e_res) add_residual_cols<ODT>(v, e_resid, e_rows, ym, xn + lane, e_cols, e_rows);
+                            store_cols_chunk<ODT>(&tmC, ring, v, lane, xn, ym, xn < e_rows && ym < e_cols);
+                        }
+                    }
+                    release_acc(acc);
+                    if (++acc == e_n_acc) {
+                        acc = 0;
+                        acc_phase ^= 1u;
+                    }
+                    continue;
+                }
                 for (int32_t h = 0; h < halves; ++h) {
 #pragma unroll 1
                     for (int ci = 0; ci < 4; ++ci) {

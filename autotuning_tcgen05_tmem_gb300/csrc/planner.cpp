@@ -114,8 +114,10 @@ Layout layout_of(const gemm_config &c, int dt)
 bool cluster_reduce_fits(const gemm_config &c, int dt)
 {
     const int S = c.split_k;
-    if (!(S == 2 || S == 4 || S == 8) || c.swap_ab || c.cta_group != 1) return false;
-    const int nblocks = (c.bm / 128) * (c.bn / 32);
+    if (!(S == 2 || S == 4 || S == 8) || c.cta_group != 1) return false;
+    // Blocks of 128 rows x 32 columns, or x 16 when swapped (up to 8 per half).
+    if (c.swap_ab && c.bn > 128) return false;
+    const int nblocks = (c.bm / 128) * (c.swap_ab ? c.bn / 16 : c.bn / 32);
     const int gsz = nblocks >= 2 * S ? 2 : 1;
     const int ngroups = (nblocks + gsz - 1) / gsz;
     const int64_t owned = (int64_t)gsz * ((ngroups + S - 1) / S);

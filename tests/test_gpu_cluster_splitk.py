@@ -16,8 +16,8 @@ C = g.make_config
 ROUTE_CLUSTER = 3
 
 # Ragged M/N/K; cluster sizes 2, 4 and 8, both tile heights, bn 64..256, blocks
-# owned in pairs and one by one, a grouped raster; every launch fits one wave
-# (the route is taken only then).
+# owned in pairs and one by one, a grouped raster, swapped tiles; every launch
+# fits one wave (the route is taken only then).
 CASES = [
     ("bf16", (300, 320, 1032), C(256, 128, 64, 4, 0, 1, 4)),
     ("bf16", (300, 320, 1032), C(128, 256, 64, 4, 0, 1, 2)),
@@ -29,6 +29,13 @@ CASES = [
     ("bf16", (264, 136, 4096), C(128, 64, 64, 6, 0, 1, 8)),
     ("fp32", (200, 160, 264), C(128, 64, 32, 4, 0, 1, 2)),
     ("fp32", (200, 160, 264), C(128, 128, 32, 4, 0, 1, 4)),
+    # Swapped (tokens along the MMA's N): blocks of 128 rows x 16 columns.
+    ("bf16", (16, 4096, 1024), C(128, 16, 128, 4, 0, 1, 4, 1, 1)),   # one block per tile, one owner
+    ("bf16", (20, 320, 1032), C(128, 32, 64, 4, 0, 1, 2, 1, 1)),     # ragged tokens, rows and K
+    ("bf16", (40, 264, 2056), C(256, 64, 64, 3, 0, 1, 4, 1, 1)),     # two halves, blocks owned in pairs
+    ("bf16", (16, 1024, 4096), C(128, 16, 128, 4, 0, 1, 8, 1, 1)),   # cluster of 8
+    ("fp32", (24, 200, 264), C(128, 32, 32, 4, 0, 1, 2, 1, 1)),
+    ("bf16", (100, 264, 1032), C(128, 128, 64, 4, 0, 1, 2, 1, 1)),   # eight chunks per half
 ]
 
 

@@ -20,6 +20,7 @@ CASES = [
     ("bf16", (300, 320, 520), C(256, 256, 64, 2), 0),                    # two 128-row halves, one accumulator
     ("bf16", (20, 320, 520), C(128, 16, 64, 6, 0, 1, 1, 1, 1), 0),       # swapped (small M)
     ("bf16", (40, 264, 520), C(256, 64, 128, 2, 0, 1, 3, 1, 1), 0),      # swapped split-K
+    ("bf16", (40, 264, 520), C(128, 64, 64, 4, 0, 1, 2, 1, 1), 0),       # swapped split-K, cluster route
     ("bf16", (300, 320, 1032), C(256, 128, 64, 4, 0, 1, 4), 0),          # split-K, cluster route
     ("bf16", (300, 320, 1032), C(256, 128, 64, 4, 0, 1, 4), 1),          # split-K, cooperative route
     ("bf16", (2048, 2048, 512), C(128, 128, 64, 4, 0, 1, 2), 0),         # split-K, last arriver
