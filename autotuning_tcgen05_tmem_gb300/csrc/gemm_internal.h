@@ -50,6 +50,8 @@ struct Layout {
 Layout layout_of(const gemm_config &c, int dt);
 int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block, int cta_group);
 bool cluster_reduce_fits(const gemm_config &c, int dt);
+// Bytes of partials the busiest owner of a cluster split-K receives (16 KB slots).
+uint32_t cluster_recv_bytes(const gemm_config &c);
 
 // Host logic (planner.cpp)
 void params_default(gemm_device_params *d);

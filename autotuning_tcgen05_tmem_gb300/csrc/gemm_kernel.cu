@@ -1366,18 +1366,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the owner's MMAs are done, which the owner announces), the owner
                 // adds the S partials in slice order and runs the epilogue.
                 // Swapped, a block is 128 rows x 16 columns (8 KB, half a slot).
+                // With an area of its own (off_recv) the partials need no ring,
+                // so no slice waits for another: a push may even land before
+                // its owner has posted the expected bytes (the transaction count
+                // goes negative for a while; the phase still needs the owner's
+                // arrival).
                 const int32_t S = e_split_k, me = w.split;
                 const int32_t nblocks = halves * chunks;
                 const int32_t gsz = nblocks >= 2 * S ? 2 : 1;
                 const uint32_t blk_bytes = e_swap_ab ? kRedBlockBytes / 2u : kRedBlockBytes;
+                const bool own_area = p.off_recv != 0u;
+                const uint32_t rbase = own_area ? base + p.off_recv : base;
                 if (ew == 0 && lane == 0) {
                     uint32_t owned = 0;
                     for (int32_t b = 0; b < nblocks; ++b) owned += ((b / gsz) % S == me) ? 1u : 0u;
                     mbar_arrive_expect_tx(recv_bar, owned * (uint32_t)(S - 1) * blk_bytes);
-                    for (int32_t o = 0; o < S; ++o)
-                        if (o != me) mbar_arrive_remote(mapa_u32(peer_ready_bar, (uint32_t)o));
+                    if (!own_area)
+                        for (int32_t o = 0; o < S; ++o)
+                            if (o != me) mbar_arrive_remote(mapa_u32(peer_ready_bar, (uint32_t)o));
                 }
-                bool cok = wait_bar_cluster(peer_ready_bar, 0, ctl, SITE_CLUSTER);
+                bool cok = own_area || wait_bar_cluster(peer_ready_bar, 0, ctl, SITE_CLUSTER);
                 if (named_bar_any(1, kEpiThreads, !cok)) break;
                 const uint32_t row16 = (uint32_t)(q * 32 + lane) * 16u;
                 if (e_swap_ab) {
@@ -1394,7 +1402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t slot = (uint32_t)(ob * (S - 1) + (me < o ? me : me - 1));
                             float v[16];
                             tmem_load_chunk<16>(tacc + (uint32_t)(h * e_bn + c * 16), v);
-                            const uint32_t dst = mapa_u32(base + slot * kRedBlockBytes + row16, (uint32_t)o);
+                            const uint32_t dst = mapa_u32(rbase + slot * kRedBlockBytes + row16, (uint32_t)o);
                             const uint32_t rbar = mapa_u32(recv_bar, (uint32_t)o);
 #pragma unroll
                             for (int j4 = 0; j4 < 4; ++j4)
@@ -1424,7 +1432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     for (int i = 0; i < 16; ++i) v[i] += t[i];
                                 } else {
                                     const uint32_t slot = (uint32_t)(ob * (S - 1) + (s < me ? s : s - 1));
-                                    const uint32_t src = base + slot * kRedBlockBytes + row16;
+                                    const uint32_t src = rbase + slot * kRedBlockBytes + row16;
 #pragma unroll
                                     for (int j4 = 0; j4 < 4; ++j4) {
                                         const float4 t = ld_shared_v4(src + (uint32_t)j4 * 2048u);
@@ -1460,7 +1468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t slot = (uint32_t)(ob * (S - 1) + (me < o ? me : me - 1));
                         float v[32];
                         tmem_load_chunk<32>(tacc + (uint32_t)(h * e_bn + c * 32), v);
-                        const uint32_t dst = mapa_u32(base + slot * kRedBlockBytes + row16, (uint32_t)o);
+                        const uint32_t dst = mapa_u32(rbase + slot * kRedBlockBytes + row16, (uint32_t)o);
                         const uint32_t rbar = mapa_u32(recv_bar, (uint32_t)o);
 #pragma unroll
                         for (int j4 = 0; j4 < 8; ++j4)
@@ -1494,7 +1502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                             } else {
                                 const uint32_t slot = (uint32_t)(ob * (S - 1) + (s < me ? s : s - 1));
-                                const uint32_t src = base + slot * kRedBlockBytes + row16;
+                                const uint32_t src = rbase + slot * kRedBlockBytes + row16;
 #pragma unroll
                                 for (int j4 = 0; j4 < 8; ++j4) {
                                     const float4 t = ld_shared_v4(src + (uint32_t)j4 * 2048u);

@@ -57,6 +57,9 @@ struct KernelParams {
     int32_t cluster_k;                 // 0, or S: the S slices of a tile are one thread-block
                                        // cluster and reduce through distributed shared memory
                                        // (one unit per CTA, grid = units)
+    uint32_t off_recv;                 // cluster split-K: partials land in an area of their own
+                                       // at this offset; 0: in the owner's pipeline ring, once
+                                       // the owner has announced that its MMAs are done
 };
 
 }  // namespace gemmgb

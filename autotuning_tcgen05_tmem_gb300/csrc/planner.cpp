@@ -111,18 +111,24 @@ Layout layout_of(const gemm_config &c, int dt)
 // receives (its blocks x (S - 1) x 16 KB) fit in its pipeline ring.  Blocks
 // (128 rows x 32 columns) are owned in groups of two when there are at least
 // 2S of them, else one by one; group j belongs to slice j mod S.
-bool cluster_reduce_fits(const gemm_config &c, int dt)
+uint32_t cluster_recv_bytes(const gemm_config &c)
 {
     const int S = c.split_k;
-    if (!(S == 2 || S == 4 || S == 8) || c.cta_group != 1) return false;
-    // Blocks of 128 rows x 32 columns, or x 16 when swapped (up to 8 per half).
-    if (c.swap_ab && c.bn > 128) return false;
+    // Blocks of 128 rows x 32 columns, or x 16 when swapped, each in a 16 KB slot.
     const int nblocks = (c.bm / 128) * (c.swap_ab ? c.bn / 16 : c.bn / 32);
     const int gsz = nblocks >= 2 * S ? 2 : 1;
     const int ngroups = (nblocks + gsz - 1) / gsz;
     const int64_t owned = (int64_t)gsz * ((ngroups + S - 1) / S);
+    return (uint32_t)(owned * (S - 1) * (int64_t)kRedBlockBytes);
+}
+
+bool cluster_reduce_fits(const gemm_config &c, int dt)
+{
+    const int S = c.split_k;
+    if (!(S == 2 || S == 4 || S == 8) || c.cta_group != 1) return false;
+    if (c.swap_ab && c.bn > 128) return false;   // up to 8 chunks per half
     const Layout L = layout_of(c, dt);
-    return owned * (S - 1) * (int64_t)kRedBlockBytes <= (int64_t)L.off_staging;
+    return cluster_recv_bytes(c) <= L.off_staging;
 }
 
 int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block, int cta_group)

@@ -446,8 +446,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
         k.coop_fixup = (cfg.split_k > 1 && k.num_units <= pairs && ring_room) ? 1 : 0;
     }
     if (want_cluster) {
+        // Where shared memory allows, the partials get an area of their own past
+        // the barriers (base + off_bar + 1 KB; the request's 1 KB alignment slack
+        // stays), so the slices push without waiting for the owner's ring.
+        const int64_t with_recv = (int64_t)p->L.smem_total + cluster_recv_bytes(cfg);
+        const bool own_area = with_recv <= dev.smem_per_block;
+        const int request = own_area ? (int)std::max<int64_t>(p->smem_request, with_recv) : p->smem_request;
         int clusters = 0;
-        e = max_active_clusters(dt, k.a_mn_major, k.b_mn_major, 1, cfg.split_k, p->smem_request, &clusters);
+        e = max_active_clusters(dt, k.a_mn_major, k.b_mn_major, 1, cfg.split_k, request, &clusters);
         if (e != cudaSuccess) {
             cudaGetLastError();
             clusters = 0;
@@ -456,6 +462,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
             k.cluster_k = cfg.split_k;
             k.coop_fixup = 0;
             p->grid = (int)k.num_units;  // one unit per CTA
+            if (own_area) {
+                k.off_recv = p->L.off_bar + 1024u;
+                p->smem_request = request;
+            }
         }
     }
     *out = p;
