@@ -430,6 +430,7 @@ def sweep(args):
         t0 = time.perf_counter()
         plan = g.plan(w.M, w.N, w.K, w.dtype, w.epi)
         tune_s = time.perf_counter() - t0
+        plan.set_independent_operands(declared(args.operands))
         steps = max(3, int(0.3 / max(1e-6, 1e-6 * 20 * nsets)))  # about 0.3 s at 20 us per GEMM
         steps = min(steps, 2000)
         clocks.mark("t0")
@@ -442,7 +443,7 @@ def sweep(args):
         t_decl = {}
         for decl in ("none", "B", "AB"):
             if decl != args.operands:
-                plan.set_independent_operands("" if decl == "none" else decl)
+                plan.set_independent_operands(declared(decl))
                 t_decl[decl] = time_gemm(plan, sets, max(3, steps // 2), 5) * 1e6
         plan.set_independent_operands(declared(args.operands))
         # A timed region longer than a second runs under the power cap: the
