@@ -163,6 +163,13 @@ __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
 // All threads of all CTAs of the cluster.
 __device__ __forceinline__ void cluster_sync_all()
 {
@@ -322,21 +329,22 @@ __device__ __forceinline__ void umma_commit_one(uint32_t bar)
 }
 
 // Pair MMAs: the completion arrives on the barrier at the same offset in both
-// CTAs of the pair.
-__device__ __forceinline__ void umma_commit_pair(uint32_t bar)
+// CTAs of the pair (`mask`: the pair's two bits of the cluster).
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t mask)
 {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
             bar),
-        "h"((uint16_t)3)
+        "h"(mask)
         : "memory");
 }
 
-// Completion of this thread's prior MMAs arrives on `bar` (in both CTAs of a pair).
+// Completion of this thread's prior MMAs arrives on `bar` (in both CTAs of a
+// pair, whose cluster bits are `pair_mask`).
 template <int CG>
-__device__ __forceinline__ void umma_commit(uint32_t bar)
+__device__ __forceinline__ void umma_commit(uint32_t bar, uint16_t pair_mask)
 {
-    if constexpr (CG == 2) umma_commit_pair(bar);
+    if constexpr (CG == 2) umma_commit_pair(bar, pair_mask);
     else umma_commit_one(bar);
 }
 
@@ -939,6 +947,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile.  Both walk the same units.
     constexpr bool pair = CG == 2;
     const uint32_t prank = pair ? (blockIdx.x & 1u) : 0u;
+    // A pair is two consecutive ranks of its cluster: of two CTAs, or, when the
+    // K slices of a pair tile also form one cluster, of 2 x S.
+    const uint32_t crank = (pair || p.cluster_k > 1) ? cluster_ctarank() : 0u;
+    const uint32_t lead_rank = crank & ~1u;
+    const uint16_t pair_mask = (uint16_t)(3u << lead_rank);
     const int64_t unit0 = pair ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
     const int64_t unit_step = pair ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
     const int32_t cta_rows = pair ? 128 : p.bm;        // tile rows held by this CTA
@@ -1090,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (pair) {
                     // Second CTA of a pair: its halves land in its own shared
                     // memory and complete on the leader's barrier, where the MMAs wait.
-                    const uint32_t fbr = mapa_u32(fb, 0);
+                    const uint32_t fbr = mapa_u32(fb, lead_rank);
                     if (arm) mbar_arrive_expect_tx_remote(fbr, tx);
                     if (what & 1u)
                         for (int32_t j = 0; j < a_loads; ++j) {
@@ -1230,7 +1243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             default: issue_stage_mx<A_MN, B_MN, 8, 2>(st, slot, sf, bn_atoms); break;
                             }
                         }
-                        umma_commit<CG>(empty0 + 8u * stage);  // slot is free once these MMAs have read it
+                        umma_commit<CG>(empty0 + 8u * stage, pair_mask);  // slot is free once these MMAs have read it
                     } else if constexpr (pair) {
                         switch (ksteps) {
                         case 4: issue_stage<DT, A_MN, B_MN, 4, 1, 2>(st); break;
@@ -1238,7 +1251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         case 12: issue_stage<DT, A_MN, B_MN, 12, 1, 2>(st); break;
                         default: issue_stage<DT, A_MN, B_MN, 16, 1, 2>(st); break;
                         }
-                        umma_commit<CG>(empty0 + 8u * stage);  // both CTAs' slots are free
+                        umma_commit<CG>(empty0 + 8u * stage, pair_mask);  // both CTAs' slots are free
                     } else {
                         switch (ksteps * 2 + halves - 1) {
                         case 8: issue_stage<DT, A_MN, B_MN, 4, 1>(st); break;
@@ -1250,7 +1263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         case 32: issue_stage<DT, A_MN, B_MN, 16, 1>(st); break;
                         default: issue_stage<DT, A_MN, B_MN, 16, 2>(st); break;
                         }
-                        umma_commit<CG>(empty0 + 8u * stage);  // slot is free once these MMAs have read it
+                        umma_commit<CG>(empty0 + 8u * stage, pair_mask);  // slot is free once these MMAs have read it
                     }
                 }
                 __syncwarp();
@@ -1263,10 +1276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             if (leader) {
                 if (nk > 0) {
-                    umma_commit<CG>(tfull0 + 8u * acc);
+                    umma_commit<CG>(tfull0 + 8u * acc, pair_mask);
                 } else {
                     mbar_arrive(tfull0 + 8u * acc);
-                    if (pair) mbar_arrive_remote(mapa_u32(tfull0 + 8u * acc, 1));
+                    if (pair) mbar_arrive_remote(mapa_u32(tfull0 + 8u * acc, lead_rank | 1u));
                 }
             }
             __syncwarp();
@@ -1276,7 +1289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (issued) {
-            if (leader) umma_commit<CG>(teardown_bar);
+            if (leader) umma_commit<CG>(teardown_bar, pair_mask);
             __syncwarp();
             wait_teardown(teardown_bar, 0, ctl);
         }
@@ -1318,7 +1331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(1, kEpiThreads);
                 if (ew == 0 && lane == 0) {
                     if (prank == 0) mbar_arrive(tempty0 + 8u * a);
-                    else mbar_arrive_remote(mapa_u32(tempty0 + 8u * a, 0));
+                    else mbar_arrive_remote(mapa_u32(tempty0 + 8u * a, lead_rank));
                 }
             }
         };
@@ -1377,13 +1390,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t blk_bytes = e_swap_ab ? kRedBlockBytes / 2u : kRedBlockBytes;
                 const bool own_area = p.off_recv != 0u;
                 const uint32_t rbase = own_area ? base + p.off_recv : base;
+                // Slice o's CTA holding the same rows as this one (a pair tile's
+                // slices are pairs 0..S-1 of the cluster).
+                auto slice_rank = [&](int32_t o) { return pair ? 2u * (uint32_t)o + prank : (uint32_t)o; };
                 if (ew == 0 && lane == 0) {
                     uint32_t owned = 0;
                     for (int32_t b = 0; b < nblocks; ++b) owned += ((b / gsz) % S == me) ? 1u : 0u;
                     mbar_arrive_expect_tx(recv_bar, owned * (uint32_t)(S - 1) * blk_bytes);
                     if (!own_area)
                         for (int32_t o = 0; o < S; ++o)
-                            if (o != me) mbar_arrive_remote(mapa_u32(peer_ready_bar, (uint32_t)o));
+                            if (o != me) mbar_arrive_remote(mapa_u32(peer_ready_bar, slice_rank(o)));
                 }
                 bool cok = own_area || wait_bar_cluster(peer_ready_bar, 0, ctl, SITE_CLUSTER);
                 if (named_bar_any(1, kEpiThreads, !cok)) break;
@@ -1402,8 +1418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t slot = (uint32_t)(ob * (S - 1) + (me < o ? me : me - 1));
                             float v[16];
                             tmem_load_chunk<16>(tacc + (uint32_t)(h * e_bn + c * 16), v);
-                            const uint32_t dst = mapa_u32(rbase + slot * kRedBlockBytes + row16, (uint32_t)o);
-                            const uint32_t rbar = mapa_u32(recv_bar, (uint32_t)o);
+                            const uint32_t dst = mapa_u32(rbase + slot * kRedBlockBytes + row16, slice_rank(o));
+                            const uint32_t rbar = mapa_u32(recv_bar, slice_rank(o));
 #pragma unroll
                             for (int j4 = 0; j4 < 4; ++j4)
                                 st_async_v4(dst + (uint32_t)j4 * 2048u, v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2],
@@ -1468,8 +1484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t slot = (uint32_t)(ob * (S - 1) + (me < o ? me : me - 1));
                         float v[32];
                         tmem_load_chunk<32>(tacc + (uint32_t)(h * e_bn + c * 32), v);
-                        const uint32_t dst = mapa_u32(rbase + slot * kRedBlockBytes + row16, (uint32_t)o);
-                        const uint32_t rbar = mapa_u32(recv_bar, (uint32_t)o);
+                        const uint32_t dst = mapa_u32(rbase + slot * kRedBlockBytes + row16, slice_rank(o));
+                        const uint32_t rbar = mapa_u32(recv_bar, slice_rank(o));
 #pragma unroll
                         for (int j4 = 0; j4 < 8; ++j4)
                             st_async_v4(dst + (uint32_t)j4 * 2048u, v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2],
@@ -2005,9 +2021,10 @@ cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, cons
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (p.cluster_k > 1) {
-        // The K slices of a tile are one cluster (consecutive CTAs).
+        // The K slices of a tile are one cluster (consecutive CTAs, or
+        // consecutive pairs of a pair tile).
         attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = (unsigned)p.cluster_k;
+        attr[1].val.clusterDim.x = (unsigned)p.cluster_k * (p.pair ? 2u : 1u);
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;

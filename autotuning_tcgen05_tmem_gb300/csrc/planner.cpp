@@ -114,8 +114,10 @@ Layout layout_of(const gemm_config &c, int dt)
 uint32_t cluster_recv_bytes(const gemm_config &c)
 {
     const int S = c.split_k;
-    // Blocks of 128 rows x 32 columns, or x 16 when swapped, each in a 16 KB slot.
-    const int nblocks = (c.bm / 128) * (c.swap_ab ? c.bn / 16 : c.bn / 32);
+    // Blocks of 128 rows x 32 columns, or x 16 when swapped, each in a 16 KB
+    // slot; a CTA of a pair holds 128 rows of the tile.
+    const int halves = c.cta_group == 2 ? 1 : c.bm / 128;
+    const int nblocks = halves * (c.swap_ab ? c.bn / 16 : c.bn / 32);
     const int gsz = nblocks >= 2 * S ? 2 : 1;
     const int ngroups = (nblocks + gsz - 1) / gsz;
     const int64_t owned = (int64_t)gsz * ((ngroups + S - 1) / S);
@@ -125,7 +127,8 @@ uint32_t cluster_recv_bytes(const gemm_config &c)
 bool cluster_reduce_fits(const gemm_config &c, int dt)
 {
     const int S = c.split_k;
-    if (!(S == 2 || S == 4 || S == 8) || c.cta_group != 1) return false;
+    // A cluster holds S CTAs, or S pairs: at most 8 CTAs (the portable size).
+    if (!(S == 2 || S == 4 || S == 8) || S * c.cta_group > 8) return false;
     if (c.swap_ab && c.bn > 128) return false;   // up to 8 chunks per half
     const Layout L = layout_of(c, dt);
     return cluster_recv_bytes(c) <= L.off_staging;

@@ -368,7 +368,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     // shared memory (decided below, once the shared-memory limit is set).  Only
     // for one wave: past it, one CTA per unit loses the persistent schedule's
     // overlap, which costs more than the global exchange it replaces.
-    const bool want_cluster = g_split_route.load() == 0 && k.num_units <= dev.sm_count && !k.pair &&
+    const bool want_cluster = g_split_route.load() == 0 && k.num_units * (k.pair ? 2 : 1) <= dev.sm_count &&
                               cluster_reduce_fits(cfg, dt);
     // Ask for more than half of the SM's shared memory so that no two CTAs of
     // this kernel share an SM (each may hold up to 512 TMEM columns).
@@ -452,16 +452,21 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
         const int64_t with_recv = (int64_t)p->L.smem_total + cluster_recv_bytes(cfg);
         const bool own_area = with_recv <= dev.smem_per_block;
         const int request = own_area ? (int)std::max<int64_t>(p->smem_request, with_recv) : p->smem_request;
+        const int cg = k.pair ? 2 : 1;
         int clusters = 0;
-        e = max_active_clusters(dt, k.a_mn_major, k.b_mn_major, 1, cfg.split_k, request, &clusters);
+        e = max_active_clusters(dt, k.a_mn_major, k.b_mn_major, cg, cfg.split_k * cg, request, &clusters);
         if (e != cudaSuccess) {
             cudaGetLastError();
             clusters = 0;
         }
-        if (clusters > 0) {
+        // Every cluster (one tile's S slices) resident at once: a cluster must
+        // fit in one GPC, so large ones pack fewer than the SM count suggests
+        // (8-CTA clusters of CTA pairs on 1000x1000x8192 ran in two waves, 45
+        // against 24 us on the cooperative route).
+        if (clusters > 0 && (int64_t)clusters * cfg.split_k >= k.num_units) {
             k.cluster_k = cfg.split_k;
             k.coop_fixup = 0;
-            p->grid = (int)k.num_units;  // one unit per CTA
+            p->grid = (int)k.num_units * cg;  // one unit per CTA (per pair)
             if (own_area) {
                 k.off_recv = p->L.off_bar + 1024u;
                 p->smem_request = request;
@@ -683,7 +688,7 @@ int plan_launch_info(gemm_plan_t p, gemm_launch_info *out)
     out->grid = p->grid;
     out->block = kThreadsPerCta;
     out->smem_bytes = p->smem_request;
-    out->cluster = k.cluster_k > 1 ? k.cluster_k : k.pair ? 2 : 1;
+    out->cluster = k.cluster_k > 1 ? k.cluster_k * (k.pair ? 2 : 1) : k.pair ? 2 : 1;
     out->splitk_route = p->cfg.split_k <= 1 ? 0 : k.cluster_k > 1 ? 3 : k.coop_fixup ? 2 : 1;
     out->b_transposed = p->b_kmajor ? 1 : 0;
     out->units = k.num_units;

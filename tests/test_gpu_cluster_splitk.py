@@ -108,21 +108,40 @@ def test_other_split_plans_keep_the_global_exchange(shape, cfg):
 
 
 # CTA pairs: persistent pairs walking many units (accumulator hand-back between
-# the two CTAs), and split-K on pairs through both global-memory routes.
+# the two CTAs), and split-K on pairs through every route: the S pairs of a
+# tile as one cluster of 2S CTAs (distributed shared memory), and, forced, the
+# global-memory routes.
 PAIR_CASES = [
-    ((2048, 2048, 512), C(256, 128, 64, 6, 0, 1, 1, 2), 0),     # 128 units on at most 76 pairs
-    ((1000, 1000, 2056), C(256, 256, 64, 6, 0, 1, 4, 2), 2),    # one wave: slices finalise together
-    ((2048, 2048, 1024), C(256, 256, 64, 4, 0, 1, 2, 2), 1),    # more units than pairs: last arriver
+    # (shape, config, forced route, expected route, expected cluster size)
+    ((2048, 2048, 512), C(256, 128, 64, 6, 0, 1, 1, 2), 0, 0, 2),     # 128 units on at most 76 pairs
+    ((300, 320, 2056), C(256, 256, 64, 6, 0, 1, 4, 2), 0, 3, 8),      # 4 pairs per cluster, few clusters
+    ((1000, 1000, 2056), C(256, 256, 64, 6, 0, 1, 4, 2), 0, 2, 2),    # 16 clusters of 8 would not all fit: cooperative
+    ((300, 320, 2056), C(256, 256, 64, 6, 0, 1, 4, 2), 1, 2, 2),      # forced global: cooperative
+    ((520, 640, 1032), C(256, 128, 64, 4, 0, 1, 2, 2), 0, 3, 4),      # bn 128, 2 pairs per cluster
+    ((2048, 2048, 1024), C(256, 256, 64, 4, 0, 1, 2, 2), 0, 1, 2),    # more units than pairs: last arriver
 ]
 
 
-@pytest.mark.parametrize("shape,cfg,route", PAIR_CASES, ids=lambda v: str(v))
-def test_cta_pair_plans_bit_exact(shape, cfg, route):
+@pytest.mark.parametrize("shape,cfg,force,route,cluster", PAIR_CASES, ids=lambda v: str(v))
+def test_cta_pair_plans_bit_exact(shape, cfg, force, route, cluster):
     M, N, K = shape
     A, B, bias = operands(M, N, K, "bf16", "int", seed=15)
-    out, ok, info = _run("bf16", A, B, bias, "relu", cfg, route=0)
-    assert info.cluster == 2 and info.grid % 2 == 0 and info.splitk_route == route
+    out, ok, info = _run("bf16", A, B, bias, "relu", cfg, route=force)
+    assert info.cluster == cluster and info.grid % 2 == 0 and info.splitk_route == route
     assert ok and np.array_equal(device_bits(out), oracle_rounded_bits(A, B, bias, "relu", g.BF16))
+
+
+@pytest.mark.parametrize("shape,cfg", [((300, 320, 2056), C(256, 256, 64, 6, 0, 1, 4, 2)),
+                                       ((520, 640, 1032), C(256, 128, 64, 4, 0, 1, 2, 2))])
+def test_pair_cluster_and_global_exchange_agree_bitwise(shape, cfg):
+    M, N, K = shape
+    A, B, bias = operands(M, N, K, "bf16", "scaled_normal", seed=17)
+    c_cluster, ok1, i1 = _run("bf16", A, B, bias, "gelu", cfg, route=0)
+    c_global, ok2, i2 = _run("bf16", A, B, bias, "gelu", cfg, route=1)
+    assert i1.splitk_route == ROUTE_CLUSTER and i1.cluster == 2 * cfg.split_k and i2.splitk_route in (1, 2)
+    assert ok1 and ok2
+    assert np.array_equal(device_bits(c_cluster), device_bits(c_global))
+    assert normalised_error(c_cluster, A, B, bias, "gelu") <= 2e-3
 
 
 def test_cta_pair_agrees_with_single_cta_tiles_bitwise_on_integers_and_within_tolerance():

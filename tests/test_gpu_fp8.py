@@ -26,7 +26,8 @@ CASES = [
     ((300, 320, 2048), C(256, 128, 128, 4, 0, 1, 4), 0),          # split-K, cluster route
     ((300, 320, 2048), C(256, 128, 128, 4, 0, 1, 4), 1),          # split-K, cooperative route
     ((300, 320, 1024), C(256, 256, 128, 4, 0, 1, 1, 2), 0),       # CTA pair
-    ((1000, 1000, 4096), C(256, 256, 128, 3, 0, 1, 4, 2), 0),     # CTA pair, split-K
+    ((1000, 1000, 4096), C(256, 256, 128, 3, 0, 1, 4, 2), 0),     # CTA pair, split-K (cluster of 4 pairs)
+    ((1000, 1000, 4096), C(256, 256, 128, 3, 0, 1, 4, 2), 1),     # CTA pair, split-K, cooperative route
 ]
 
 

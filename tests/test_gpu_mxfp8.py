@@ -33,7 +33,8 @@ CASES = [
     ((40, 264, 1024), C(256, 64, 128, 2, 0, 1, 3, 1, 1), 0),   # swapped, split-K, B from a K-major copy
     ((200, 256, 512), C(128, 128, 128, 4, 0, 1, 1, 1, 1), 0),  # swapped, two token tiles of one atom each
     ((300, 320, 1024), C(256, 256, 128, 3, 0, 1, 1, 2), 0),    # CTA pair (each CTA holds all B scales)
-    ((1000, 1000, 4096), C(256, 256, 128, 3, 0, 1, 4, 2), 0),  # CTA pair, split-K, B from a K-major copy
+    ((1000, 1000, 4096), C(256, 256, 128, 3, 0, 1, 4, 2), 0),  # CTA pair, split-K (cluster of 4 pairs), B K-major
+    ((1000, 1000, 4096), C(256, 256, 128, 3, 0, 1, 4, 2), 1),  # the same on the cooperative route
     ((200, 136, 512), C(256, 128, 128, 4, 0, 1, 1, 2), 0),     # CTA pair, bn 128, two accumulators
 ]
 

@@ -25,7 +25,8 @@ CASES = [
     ("bf16", (300, 320, 1032), C(256, 128, 64, 4, 0, 1, 4), 1),          # split-K, cooperative route
     ("bf16", (2048, 2048, 512), C(128, 128, 64, 4, 0, 1, 2), 0),         # split-K, last arriver
     ("bf16", (300, 320, 520), C(256, 256, 64, 4, 0, 1, 1, 2), 0),        # CTA pair
-    ("bf16", (1000, 1000, 2056), C(256, 256, 64, 6, 0, 1, 4, 2), 0),     # CTA pair, cooperative split-K
+    ("bf16", (1000, 1000, 2056), C(256, 256, 64, 6, 0, 1, 4, 2), 0),     # CTA pair, split-K, cluster route
+    ("bf16", (1000, 1000, 2056), C(256, 256, 64, 6, 0, 1, 4, 2), 1),     # CTA pair, cooperative split-K
     ("fp32", (200, 160, 136), C(128, 64, 32, 4)),
 ]
 CASES = [c if len(c) == 4 else c + (0,) for c in CASES]
