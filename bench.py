@@ -627,10 +627,10 @@ def main():
     if os.path.exists(tr_path):
         with open(tr_path) as f:
             tr = json.load(f)
-        ent = tr.get(w.name)
-        if ent and ent.get("source_digest") == _build._sources_digest() and \
-                ent.get("config") == list(cfg.astuple()):
-            traffic = ent.get("dram_bytes_per_launch")
+        ents = tr.get(w.name) or []
+        for ent in ents if isinstance(ents, list) else [ents]:
+            if ent.get("source_digest") == _build._sources_digest() and ent.get("config") == list(cfg.astuple()):
+                traffic = ent.get("dram_bytes_per_launch")
     if t_compute >= t_memory:
         roof = {"bound": "tensor", "achieved": flops / gemm_s / 1e12, "peak": tpeak, "unit": "TFLOP/s"}
     else:
