@@ -124,3 +124,18 @@ def test_fp8_full_size_tuned_plan_sampled(name):
         assert p.status() == 0, g.last_error()
         cfg = p.config.astuple()
     assert sampled_error(Cd.cpu(), A, B, bias, w.epi, n=2048) <= 2e-3, cfg
+
+
+@pytest.mark.parametrize("shape,cfg,cluster", [((300, 320, 2048), C(256, 256, 128, 4, 0, 1, 4, 2), 8),
+                                               ((300, 320, 2064), C(256, 256, 128, 4, 0, 1, 2, 2), 4)])
+def test_fp8_pair_tiles_reduce_inside_a_cluster(shape, cfg, cluster):
+    # A pair tile's K slices as one cluster of 2S CTAs (split-K through
+    # distributed shared memory), bit-exact and equal to the cooperative route.
+    M, N, K = shape
+    A, B, bias = inputs.make_operands(M, N, K, "fp8", "int", seed=35)
+    out, ok, info = _run(A, B, bias, "relu", cfg, 0, 0.5)
+    assert ok and info.splitk_route == 3 and info.cluster == cluster
+    want = og.round_bf16_bits(og.gemm(A, B, bias, g.EPILOGUES["relu"], alpha=0.5))
+    assert np.array_equal(device_bits(out), want)
+    coop, ok2, info2 = _run(A, B, bias, "relu", cfg, 1, 0.5)
+    assert ok2 and info2.splitk_route == 2 and np.array_equal(device_bits(coop), device_bits(out))

@@ -184,3 +184,18 @@ def test_mx_plan_rejects_the_unscaled_entry_points_and_vice_versa():
     with pytest.raises(g.GemmError) as e:       # B's scales come in 128-column atoms: bn 192 is refused
         g.plan_with_config(M, N, K, "mxfp8", "relu", C(128, 192, 128, 3))
     assert e.value.code == g.ERR_INFEASIBLE
+
+
+@pytest.mark.parametrize("shape,cfg,cluster", [((300, 320, 2048), C(256, 256, 128, 3, 0, 1, 4, 2), 8),
+                                               ((300, 320, 2048), C(256, 256, 128, 3, 0, 1, 2, 2), 4)])
+def test_mxfp8_pair_tiles_reduce_inside_a_cluster(shape, cfg, cluster):
+    # Block-scaled pair tiles whose K slices form one cluster of 2S CTAs: the
+    # partials land in the ring that also held the scale atoms.
+    M, N, K = shape
+    A, SA, B, SB, bias = inputs.make_mx_operands(M, N, K, "int", seed=46)
+    out, ok, info = _run(A, SA, B, SB, bias, "relu", cfg, 0, 0.5)
+    assert ok and info.splitk_route == 3 and info.cluster == cluster
+    want = og.round_bf16_bits(mx.mx_gemm(A, SA, B, SB, bias, g.EPILOGUES["relu"], alpha=0.5))
+    assert np.array_equal(device_bits(out), want)
+    coop, ok2, info2 = _run(A, SA, B, SB, bias, "relu", cfg, 1, 0.5)
+    assert ok2 and info2.splitk_route == 2 and np.array_equal(device_bits(coop), device_bits(out))
