@@ -236,3 +236,15 @@ def test_shipped_set_selection_equals_oracle():
             assert got[0] == want[0]
             assert got[1] == pytest.approx(want[1], rel=1e-12) and got[2] == pytest.approx(want[2], rel=1e-12)
     assert g.lib().gemm_select_config_set(None, 2, 2, 1, None, None, None, None) == g.ERR_INVALID_ARG
+
+
+def test_operand_declaration_argument_checks():
+    # A null plan is refused without a device; unknown operand letters never
+    # reach the library.
+    assert g.lib().gemm_plan_set_independent_operands(None, g.OPERAND_B) == g.ERR_INVALID_ARG
+
+    class NoPlan:
+        _h = None
+
+    with pytest.raises(ValueError):
+        g.Plan.set_independent_operands(NoPlan(), "AC")
