@@ -134,17 +134,15 @@ bool cluster_reduce_fits(const gemm_config &c, int dt)
     return cluster_recv_bytes(c) <= L.off_staging;
 }
 
+// The most stages (at most kMaxStages) whose layout fits in shared memory, by
+// the same count as the feasibility rule (the MX scale area rounded up to 1 KB).
 int max_stages_for(int bm, int bn, int bk, int dt, int swap_ab, int64_t smem_per_block, int cta_group)
 {
-    const int64_t mx = dt == GEMM_MXFP8_E4M3
-                           ? (int64_t)((cta_group == 2 ? 1 : bm / 128) + std::max(1, bn / 128)) * (bk / 128) * kMxAtomBytes
-                           : 0;
-    const int64_t per = (int64_t)(cta_group == 2 ? 128 + bn / 2 : bm + bn) * bk * elt_bytes(dt) + mx;
-    const int64_t room = smem_per_block - staging_bytes(dt, swap_ab) - kAuxSmem - (mx ? 1024 : 0);
-    int64_t s = room / per;
-    if (s < 0) s = 0;
-    if (s > kMaxStages) s = kMaxStages;
-    return (int)s;
+    for (int s = kMaxStages; s >= 1; --s) {
+        const gemm_config c{bm, bn, bk, s, 0, 1, 1, cta_group, swap_ab};
+        if ((int64_t)layout_of(c, dt).smem_total <= smem_per_block) return s;
+    }
+    return 0;
 }
 
 const char *reason_text(int r)

@@ -21,8 +21,17 @@ Parity pins (tests/test_oracle_*.py):
   traffic law     explicit tile-loop count = 2N³/T; √(C/3).
   waves           133 tiles on 132 SMs → 2 waves; 64 tiles < half a wave.
   rank agreement  hand cases, and scipy.stats on random data.
-  gb300_*         "parity unpinned" against the pages (they say nothing about
-                  TMEM or tcgen05): brute-force and invariant checks only.
+  gb300_model     panel bytes = the per-block traffic law summed over tiles;
+                  waves and wave efficiency = a round-by-round dispatch of the
+                  CTAs; never below the roofline floor; HBM bytes = compulsory
+                  bytes when A and B fit in half of L2 (each pin with a planted
+                  mistake it catches).  Fitted coefficients: "parity unpinned".
+  gb300_candidates  = a brute-force filter of the documented grid; holds the
+                  fixed tile.  gb300_check (TMEM/tcgen05 rules): "parity
+                  unpinned" against the pages, which say nothing about them;
+                  brute force and set-equality with the library only.
+  mx, fp8         the OCP format tables, reduction to the plain GEMM oracle,
+                  power-of-two invariances, NaN propagation.
 """
 from . import gemm, selection  # noqa: F401
 

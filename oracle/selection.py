@@ -19,10 +19,19 @@ Sources (page title, section / equation):
 
 Parity status of each function is stated in its docstring.  The GB300 rules
 (`gb300_*`) restate the library's documented feasibility rules, enumeration and
-cost model independently of the library source; the pages say nothing about
-TMEM or tcgen05, so those functions are "parity unpinned" against the pages
-(they are pinned only by brute-force/invariant checks and, for the cost model,
-by its reduction to the workshop model).
+cost model independently of the library source.  What the pages fix in them is
+pinned (tests/test_oracle_gb300_pins.py, each pin with a planted mistake it
+catches): gb300_model's panel bytes equal the per-block traffic law of "Tile
+Selection" ("Analytical models and where they break") summed over tiles; its
+waves and wave efficiency equal the wave arithmetic of "Compilers and Kernel
+Languages" on CTAs (tiles x slices x CTAs per tile); no prediction beats the
+roofline floor; its HBM bytes are the compulsory bytes when A and B fit in half
+of L2; gb300_candidates equals a brute-force filter of its documented grid and
+holds the fixed tile ("CuTile Autotuning").  The rest is "parity unpinned"
+against the pages, which say nothing about TMEM or tcgen05: the feasibility
+rules themselves (pinned only by brute force and by set-equality with the
+library) and the fitted coefficients of the GB300 cost model (judged by rank
+agreement with measurement; the model also reduces to the workshop model).
 """
 from __future__ import annotations
 
@@ -209,8 +218,9 @@ def workshop_sweep(M, N, K, dev: WorkshopDevice = WorkshopDevice()):
 
 
 # ---------------------------------------------------------------------------
-# GB300 restatement of the library's documented rules (parity unpinned against
-# the pages, which say nothing about TMEM/tcgen05; pinned by brute force).
+# GB300 restatement of the library's documented rules.  The generator is pinned
+# by a brute-force filter of its grid; the TMEM/tcgen05 rules themselves are
+# parity unpinned against the pages, which say nothing about them.
 # ---------------------------------------------------------------------------
 
 DT_BF16, DT_FP32, DT_FP8, DT_MXFP8 = 0, 1, 2, 3
@@ -337,11 +347,12 @@ def smem_bytes(cfg: Config, dtype):
 
 
 def max_stages(bm, bn, bk, dtype, swap_ab, smem_per_block, cta_group=1):
-    a_atoms = 1 if cta_group == 2 else bm // 128
-    mx = (a_atoms + max(1, bn // 128)) * (bk // 128) * MX_ATOM_BYTES if dtype == DT_MXFP8 else 0
-    per = ((128 + bn // 2) if cta_group == 2 else (bm + bn)) * bk * elt_bytes(dtype) + mx
-    room = smem_per_block - staging_bytes(dtype, swap_ab) - AUX_SMEM - (1024 if mx else 0)
-    return max(0, min(MAX_STAGES, room // per))
+    """The most stages (at most MAX_STAGES) whose shared-memory footprint, as
+    smem_bytes counts it, fits; 0 when not even one does."""
+    for st in range(MAX_STAGES, 0, -1):
+        if smem_bytes(Config(bm, bn, bk, st, cta_group=cta_group, swap_ab=swap_ab), dtype) <= smem_per_block:
+            return st
+    return 0
 
 
 def tmem_columns(cfg: Config, dtype=None):
@@ -492,8 +503,10 @@ def schedule_unit(u, tiles_m, tiles_n, split_k, raster, group, num_kb):
 
 
 # ---------------------------------------------------------------------------
-# GB300 cost model, restated from its documented terms (parity unpinned against
-# the pages; with model_kind = 1 it is the workshop model above)
+# GB300 cost model, restated from its documented terms.  Its panel traffic,
+# waves, roofline floor and compulsory bytes are pinned against the pages; its
+# fitted coefficients are parity unpinned.  With model_kind = 1 it is the
+# workshop model above.
 # ---------------------------------------------------------------------------
 
 def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
