@@ -49,7 +49,7 @@ EXPORTS = ["gemm_version", "gemm_last_error", "gemm_device_params_default",
            "gemm_cache_save", "gemm_cache_load", "gemm_plan_launch_info", "gemm_select_config_set",
            "gemm_plan_from_list", "gemm_tune_batch", "gemm_run_ex", "gemm_plan_set_scale",
            "gemm_run_mx", "gemm_mx_scales_bytes", "gemm_mx_pack_scales", "gemm_model_params_load",
-           "gemm_plan_set_independent_operands"]
+           "gemm_plan_set_independent_operands", "gemm_run_host_many"]
 
 
 class GemmError(RuntimeError):
@@ -113,7 +113,7 @@ class LaunchInfo(ctypes.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
-SPLITK_ROUTES = {0: "none", 1: "global_last_arriver", 2: "global_cooperative", 3: "cluster_dsmem"}
+SPLITK_ROUTES = {0: "none", 1: "global_last_arriver", 2: "global_shares", 3: "cluster_dsmem"}
 
 
 class RankStats(ctypes.Structure):
@@ -189,6 +189,7 @@ def _load_library(path: str):
         "gemm_cache_clear": (None, []),
         "gemm_debug_set": (ctypes.c_int, [i32, i64]),
         "gemm_run_noalloc": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, P(Config), vp, vp, vp, vp, vp]),
+        "gemm_run_host_many": (ctypes.c_int, [vp, i32, P(vp), P(vp), P(vp), P(vp), vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -378,6 +379,15 @@ class Plan:
 
     def run_host(self, A, B, bias, C, stream=None) -> None:
         _check(lib().gemm_run_host(self._h, _ptr(A), _ptr(B), _ptr(bias), _ptr(C), _stream_handle(stream)))
+
+    def run_host_many(self, As, Bs, biases, Cs, stream=None) -> None:
+        """gemm_run_host_many: len(As) GEMMs from host buffers, copies pipelined
+        against the kernels; returns once every C is filled."""
+        n = len(As)
+        arr = ctypes.c_void_p * max(n, 1)
+        a, b, c = arr(*[_ptr(x) for x in As]), arr(*[_ptr(x) for x in Bs]), arr(*[_ptr(x) for x in Cs])
+        bb = None if biases is None else arr(*[_ptr(x) for x in biases])
+        _check(lib().gemm_run_host_many(self._h, n, a, b, bb, c, _stream_handle(stream)))
 
     def status(self) -> int:
         return lib().gemm_plan_status(self._h)

@@ -35,6 +35,7 @@ extern std::atomic<int32_t> g_debug_stall;
 extern std::atomic<int32_t> g_b_route;
 extern std::atomic<int32_t> g_split_route;
 extern std::atomic<int32_t> g_check;
+extern std::atomic<int64_t> g_share_poll;
 int query_params(gemm_device_params *d);
 int model_params_load(const char *path, gemm_device_params *out);
 int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out);
@@ -46,6 +47,8 @@ int run_plan_mx(gemm_plan_t p, const void *A, const void *SA, const void *B, con
                 const void *R, void *C, cudaStream_t stream);
 int mx_pack_scales(const void *scales, int64_t rows, int64_t K, int b_side, void *packed, cudaStream_t stream);
 int run_host(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream);
+int run_host_many(gemm_plan_t p, int n, const void *const *A, const void *const *B, const void *const *bias,
+                  void *const *C, cudaStream_t stream);
 int plan_status(gemm_plan_t p);
 int plan_config(gemm_plan_t p, gemm_config *out);
 int plan_launch_info(gemm_plan_t p, gemm_launch_info *out);
@@ -243,6 +246,13 @@ int gemm_run_host(gemm_plan_t plan, const void *A, const void *B, const void *bi
     return run_host(plan, A, B, bias, C, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int gemm_run_host_many(gemm_plan_t plan, int32_t n, const void *const *A, const void *const *B,
+                       const void *const *bias, void *const *C, gemm_stream_t stream)
+{
+    clear_error();
+    return run_host_many(plan, n, A, B, bias, C, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int gemm_plan_status(gemm_plan_t plan)
 {
     clear_error();
@@ -355,6 +365,11 @@ int gemm_debug_set(int32_t what, int64_t value)
     }
     if (what == 4) {
         g_check.store(value ? 1 : 0);
+        return GEMM_OK;
+    }
+    if (what == 5) {
+        if (value < 0) return set_error(GEMM_ERR_INVALID_ARG, "the share wait must be >= 0 cycles");
+        g_share_poll.store(value);
         return GEMM_OK;
     }
     return set_error(GEMM_ERR_INVALID_ARG, "unknown debug control %d", what);

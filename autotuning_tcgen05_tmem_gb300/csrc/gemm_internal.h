@@ -53,6 +53,15 @@ bool cluster_reduce_fits(const gemm_config &c, int dt);
 // Bytes of partials the busiest owner of a cluster split-K receives (16 KB slots).
 uint32_t cluster_recv_bytes(const gemm_config &c);
 
+// Launch record of configuration c for C = act(A·B + bias) on (M, N, K) in
+// dtype dt, with `act` the kernel's bias/activation code (0 none, 1 bias, 2
+// ReLU, 3 GELU) and B read from a K-major copy when `b_kmajor`: extents,
+// schedule, operand majorness, the tcgen05 instruction descriptor and the
+// shared-memory / TMEM layout, with alpha = 1.  Pointers, the split-K route
+// and the run's debug fields are left zero for the caller.
+KernelParams kernel_params_of(int64_t M, int64_t N, int64_t K, int dt, int act, const gemm_config &c,
+                              bool b_kmajor);
+
 // Host logic (planner.cpp)
 void params_default(gemm_device_params *d);
 void params_workshop(gemm_device_params *d);

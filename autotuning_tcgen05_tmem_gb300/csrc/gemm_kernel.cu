@@ -577,20 +577,21 @@ __device__ __noinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, con
     }
 }
 
-// Publishes this CTA's earlier global writes (ordered before this thread by a
-// CTA barrier) together with the increment; returns the count before it.
-__device__ __forceinline__ uint64_t atom_release_gpu_add_u64(uint64_t *ptr, uint64_t v)
-{
-    uint64_t old;
-    asm volatile("atom.release.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(ptr), "l"(v) : "memory");
-    return old;
-}
-
 // Adds with acquire-release semantics at GPU scope; returns the count before.
+// The release publishes this CTA's earlier global writes (ordered before this
+// thread by a CTA barrier) with the increment; the acquire makes the writes
+// published by earlier increments visible (passed on by the next CTA barrier).
 __device__ __forceinline__ int32_t atom_acq_rel_gpu_add(int32_t *ptr, int32_t v)
 {
     int32_t old;
     asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint64_t atom_acq_rel_gpu_add_u64(uint64_t *ptr, uint64_t v)
+{
+    uint64_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(ptr), "l"(v) : "memory");
     return old;
 }
 
@@ -601,24 +602,26 @@ __device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *ptr)
     return v;
 }
 
-// Waits until *ptr >= target (64-bit arrival counts that other CTAs of this
-// launch increment), with the same bound and abort protocol as the mbarrier waits.
-__device__ __noinline__ bool wait_epoch(const uint64_t *ptr, uint64_t target, const WaitCtl &c, int32_t site)
+// Split-K share counts: every launch adds exactly S arrivals to each share's
+// count (they only grow), so a count read before this slice's own arrival lies
+// in [base, base + S - 1] with base a multiple of S.  True once the other S - 1
+// slices have arrived (acquire: their partials are then visible), false when
+// `limit` SM cycles or the CTA's abort flag end the wait first.  Never an
+// error: the slices of a one-wave launch normally arrive within a microsecond
+// or two of each other, and a slice that is not resident (its SM held by
+// another kernel) only makes the owner hand its share over, to be finalised
+// by whichever slice arrives last.
+__device__ __noinline__ bool poll_share(const uint64_t *ptr, uint32_t S, const WaitCtl &c, long long limit)
 {
-    if (ld_acquire_gpu_u64(ptr) >= target) return true;
-    const long long limit_cycles = (long long)((double)c.timeout_ns * 2.2);
+    uint64_t v = ld_acquire_gpu_u64(ptr);
+    const uint64_t target = v - v % S + (S - 1);
+    if (v >= target) return true;
+    if (limit <= 0) return false;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         __nanosleep(32);
         if (ld_acquire_gpu_u64(ptr) >= target) return true;
-        if ((it & 15u) == 0) {
-            if (*c.abort) return false;
-            if (clock64() - t0 > limit_cycles) {
-                *c.abort = 1;
-                atomicCAS(c.status, 0, site);
-                return false;
-            }
-        }
+        if ((it & 15u) == 0 && (*c.abort || clock64() - t0 > limit)) return false;
     }
 }
 
@@ -1543,116 +1546,165 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             if (e_coop && !e_swap_ab) {
-                // Cooperative split-K (all slices resident, one unit per CTA).  The
-                // tile is cut into 32-row x 32-column blocks; block (row group rg,
-                // chunk c) belongs to slice (c/2 + max(1, chunks/2)*rg) mod S, which
-                // gives every epilogue warp an even share of every slice's blocks.
-                // A slice keeps its own blocks in TMEM and writes the others to the
+                // One-wave split-K (one unit per CTA), finalised share by share.
+                // The tile is cut into 32-row x 32-column blocks; block (row group
+                // rg, chunk c) belongs to share (c/2 + max(1, chunks/2)*rg) mod S,
+                // which gives every epilogue warp an even part of every share.
+                // Share j has its own arrival count (S per launch; the counts only
+                // grow).  Slice s writes the blocks of every other share to the
                 // workspace ([slice][block][4-column group][32 rows][4], 4 KB per
-                // block); after all S slices have arrived, each owner adds the S
-                // partials of its blocks in slice order and runs the epilogue.
+                // block) and arrives on those shares.  It then waits, for a bounded
+                // time, for the other S - 1 slices to arrive on its own share: if
+                // they do, it adds the S partials of its blocks in slice order
+                // (its own straight from TMEM) and runs the epilogue.  If they do
+                // not (a slice that is not resident, its SM held by another
+                // kernel), it writes its own blocks too and arrives; the slice
+                // whose arrival completes a share's count finalises that share
+                // from the workspace.  Nothing ever waits for a slice that may not
+                // run, and every route sums in slice order, so all give the same bits.
                 const int32_t S = e_split_k, me = w.split;
                 const int32_t half_chunks = chunks >= 2 ? chunks / 2 : 1;
                 const int32_t nblocks = (cta_rows / 32) * chunks;
                 // Per-warp fetch region in the ring: R blocks of 4 KB (R >= 1).
-                const int32_t fetch_r = max(1, min(S - 1, (int32_t)(p.off_staging / (kEpiWarps * 4096u))));
+                const int32_t fetch_r = max(1, min(S, (int32_t)(p.off_staging / (kEpiWarps * 4096u))));
                 const uint32_t fetch_base = base + (uint32_t)ew * (uint32_t)fetch_r * 4096u;
                 float4 *const xws = reinterpret_cast<float4 *>(e_workspace + (size_t)xtile * S * (size_t)tile_elems);
-                for (int32_t h = 0; h < halves; ++h) {
-                    const int32_t rg = h * 4 + q;
+                uint64_t *const counts = e_epochs + (size_t)xtile * S;
+                // This slice's partial of the blocks of share j (j < 0: of every
+                // share but its own) -> workspace.
+                auto write_blocks = [&](int32_t j) {
+                    for (int32_t h = 0; h < halves; ++h) {
+                        const int32_t rg = h * 4 + q;
 #pragma unroll 1
-                    for (int ci = 0; ci < 4; ++ci) {
-                        const int32_t c = cg + 2 * ci;
-                        if (c >= chunks) break;
-                        if ((c / 2 + half_chunks * rg) % S == me) continue;
-                        float v[32];
-                        if (nk > 0) tmem_load_chunk<32>(tacc + (uint32_t)(h * e_bn + c * 32), v);
-                        else {
+                        for (int ci = 0; ci < 4; ++ci) {
+                            const int32_t c = cg + 2 * ci;
+                            if (c >= chunks) break;
+                            const int32_t owner = (c / 2 + half_chunks * rg) % S;
+                            if (j < 0 ? owner == me : owner != j) continue;
+                            float v[32];
+                            if (nk > 0) tmem_load_chunk<32>(tacc + (uint32_t)(h * e_bn + c * 32), v);
+                            else {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                        }
-                        float4 *dst = xws + (size_t)(me * nblocks + rg * chunks + c) * 256 + lane;
-#pragma unroll
-                        for (int j4 = 0; j4 < 8; ++j4)
-                            dst[j4 * 32] = make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
-                    }
-                }
-                // Each launch adds exactly S arrivals per tile and the counts never
-                // reset: this slice's own arrival names its launch's base.
-                named_bar_sync(1, kEpiThreads);
-                bool cok = true;
-                if (ew == 0 && lane == 0) {
-                    const uint64_t before = atom_release_gpu_add_u64(e_epochs + xtile, 1);
-                    const uint64_t target = before - before % (uint64_t)S + (uint64_t)S;
-                    cok = wait_epoch(e_epochs + xtile, target, ctl, SITE_FIXUP);
-                }
-                if (named_bar_any(1, kEpiThreads, !cok)) break;
-                for (int32_t h = 0; h < halves; ++h) {
-                    const int32_t rg = h * 4 + q;
-#pragma unroll 1
-                    for (int ci = 0; ci < 4; ++ci) {
-                        const int32_t c = cg + 2 * ci;
-                        if (c >= chunks) break;
-                        if ((c / 2 + half_chunks * rg) % S != me) continue;
-                        const float4 *src = xws + (size_t)(rg * chunks + c) * 256 + lane;
-                        float v[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                        // The other slices' blocks are fetched R at a time with cp.async
-                        // into this warp's region of the (now idle) pipeline ring, each
-                        // thread reading back only its own 16-byte pieces; the sum runs
-                        // in slice order with this slice's partial read from TMEM.
-#pragma unroll 1
-                        for (int32_t s = 0; s < S;) {
-                            int32_t s_end = s, got = 0;
-                            while (s_end < S && (got < fetch_r || s_end == me)) {
-                                if (s_end != me) {
-                                    const uint32_t dst = fetch_base + (uint32_t)got * 4096u + (uint32_t)lane * 16u;
-                                    const float4 *g = src + (size_t)s_end * nblocks * 256;
-#pragma unroll
-                                    for (int j4 = 0; j4 < 8; ++j4) cp_async_16(dst + (uint32_t)j4 * 512u, g + j4 * 32);
-                                    ++got;
-                                }
-                                ++s_end;
+                                for (int t = 0; t < 32; ++t) v[t] = 0.0f;
                             }
-                            cp_async_commit_wait_all();
-                            int32_t slot = 0;
-                            for (; s < s_end; ++s) {
-                                if (s == me) {
-                                    if (nk > 0) {
+                            float4 *dst = xws + (size_t)(me * nblocks + rg * chunks + c) * 256 + lane;
 #pragma unroll
-                                        for (int hh = 0; hh < 2; ++hh) {
-                                            float o[16];
-                                            tmem_load_chunk<16>(tacc + (uint32_t)(h * e_bn + c * 32 + hh * 16), o);
+                            for (int j4 = 0; j4 < 8; ++j4)
+                                dst[j4 * 32] = make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+                        }
+                    }
+                };
+                // Sum of the S partials of share j's blocks in slice order, then
+                // the epilogue.  This slice's partial comes from TMEM when
+                // `own_tmem` (the accumulator is still held), else from the
+                // workspace like the others'.  The other blocks are fetched R at
+                // a time with cp.async into this warp's region of the (idle)
+                // pipeline ring, each thread reading back only its own pieces.
+                auto finalise_share = [&](int32_t j, bool own_tmem) {
+                    for (int32_t h = 0; h < halves; ++h) {
+                        const int32_t rg = h * 4 + q;
+#pragma unroll 1
+                        for (int ci = 0; ci < 4; ++ci) {
+                            const int32_t c = cg + 2 * ci;
+                            if (c >= chunks) break;
+                            if ((c / 2 + half_chunks * rg) % S != j) continue;
+                            const float4 *src = xws + (size_t)(rg * chunks + c) * 256 + lane;
+                            float v[32];
 #pragma unroll
-                                            for (int j = 0; j < 16; ++j) v[hh * 16 + j] += o[j];
+                            for (int t = 0; t < 32; ++t) v[t] = 0.0f;
+#pragma unroll 1
+                            for (int32_t s = 0; s < S;) {
+                                int32_t s_end = s, got = 0;
+                                while (s_end < S && (got < fetch_r || (s_end == me && own_tmem))) {
+                                    if (!(s_end == me && own_tmem)) {
+                                        const uint32_t dst = fetch_base + (uint32_t)got * 4096u + (uint32_t)lane * 16u;
+                                        const float4 *g = src + (size_t)s_end * nblocks * 256;
+#pragma unroll
+                                        for (int j4 = 0; j4 < 8; ++j4)
+                                            cp_async_16(dst + (uint32_t)j4 * 512u, g + j4 * 32);
+                                        ++got;
+                                    }
+                                    ++s_end;
+                                }
+                                cp_async_commit_wait_all();
+                                int32_t slot = 0;
+                                for (; s < s_end; ++s) {
+                                    if (s == me && own_tmem) {
+                                        if (nk > 0) {
+#pragma unroll
+                                            for (int hh = 0; hh < 2; ++hh) {
+                                                float o[16];
+                                                tmem_load_chunk<16>(tacc + (uint32_t)(h * e_bn + c * 32 + hh * 16),
+                                                                    o);
+#pragma unroll
+                                                for (int t = 0; t < 16; ++t) v[hh * 16 + t] += o[t];
+                                            }
                                         }
-                                    }
-                                } else {
-                                    const uint32_t from = fetch_base + (uint32_t)slot * 4096u + (uint32_t)lane * 16u;
+                                    } else {
+                                        const uint32_t from =
+                                            fetch_base + (uint32_t)slot * 4096u + (uint32_t)lane * 16u;
 #pragma unroll
-                                    for (int j4 = 0; j4 < 8; ++j4) {
-                                        const float4 t = ld_shared_v4(from + (uint32_t)j4 * 512u);
-                                        v[4 * j4] += t.x;
-                                        v[4 * j4 + 1] += t.y;
-                                        v[4 * j4 + 2] += t.z;
-                                        v[4 * j4 + 3] += t.w;
+                                        for (int j4 = 0; j4 < 8; ++j4) {
+                                            const float4 t = ld_shared_v4(from + (uint32_t)j4 * 512u);
+                                            v[4 * j4] += t.x;
+                                            v[4 * j4 + 1] += t.y;
+                                            v[4 * j4 + 2] += t.z;
+                                            v[4 * j4 + 3] += t.w;
+                                        }
+                                        ++slot;
                                     }
-                                    ++slot;
                                 }
                             }
+                            bias_act_rows(v, bcol[ci], e_epi, e_alpha);
+                            const int32_t n = c0 + c * 32, y = r0 + rg * 32;
+                            if (e_res) add_residual_rows<ODT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
+                            store_rows_chunk<ODT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                         }
-                        bias_act_rows(v, bcol[ci], e_epi, e_alpha);
-                        const int32_t n = c0 + c * 32, y = r0 + rg * 32;
-                        if (e_res) add_residual_rows<ODT>(v, e_resid, e_cols, y + lane, n, e_rows, e_cols);
-                        store_rows_chunk<ODT>(&tmC, ring, v, lane, n, y, n < e_cols && y < e_rows);
                     }
+                };
+                write_blocks(-1);
+                named_bar_sync(1, kEpiThreads);
+                // One warp arrives on the other shares (lane i on share me+1+i),
+                // learning which of them it completes, and waits on its own.
+                if (ew == 0) {
+                    bool last = false;
+                    if (lane < S - 1) {
+                        const int32_t j = (me + 1 + lane) % S;
+                        last = atom_acq_rel_gpu_add_u64(counts + j, 1) % (uint64_t)S == (uint64_t)(S - 1);
+                    }
+                    const uint32_t foreign = __ballot_sync(0xFFFFFFFFu, last);
+                    uint32_t own = 0;
+                    if (lane == 0) {
+                        own = poll_share(counts + me, (uint32_t)S, ctl, p.share_poll_cycles) ? 1u : 0u;
+                        if (own) atomicAdd(reinterpret_cast<unsigned long long *>(counts + me), 1ull);
+                    }
+                    own = __shfl_sync(0xFFFFFFFFu, own, 0);
+                    // bit i: share me+1+i to finalise; bit 31: own share ready
+                    if (lane == 0) *last_flag = (int32_t)(foreign | (own << 31));
+                }
+                named_bar_sync(1, kEpiThreads);
+                const uint32_t flags = (uint32_t)*last_flag;
+                named_bar_sync(1, kEpiThreads);   // the flag is rewritten below
+                if (flags >> 31) {
+                    finalise_share(me, true);
+                } else {
+                    // Hand the share over: publish this slice's own partial too.
+                    write_blocks(me);
+                    named_bar_sync(1, kEpiThreads);
+                    if (ew == 0 && lane == 0)
+                        *last_flag = atom_acq_rel_gpu_add_u64(counts + me, 1) % (uint64_t)S == (uint64_t)(S - 1);
+                    named_bar_sync(1, kEpiThreads);
+                    const bool mine = *last_flag != 0;
+                    named_bar_sync(1, kEpiThreads);
+                    if (mine) finalise_share(me, true);
                 }
                 release_acc(acc);
                 if (++acc == e_n_acc) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
+                for (int32_t i = 0; i < S - 1; ++i)
+                    if ((flags >> i) & 1u) finalise_share((me + 1 + i) % S, false);
                 continue;
             }
             float *ws = nullptr;
@@ -1716,41 +1768,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             if (e_split_k > 1) {
-                // Split-K fix-up.  Cooperative (one wave, cooperative launch):
-                // every K slice of the tile arrives, waits for the others, and
-                // finalises its share of the tile's 32-row blocks (block b goes to
-                // slice b mod S); the arrival counts only grow, and this slice's
-                // own arrival names its launch's base.  Otherwise the last slice
-                // to arrive finalises the whole tile and resets the count.  Either
-                // way the partials are summed in slice order.  One thread's
-                // release (after the CTA barrier that orders every epilogue
-                // thread's partial stores before it) publishes the CTA's partial;
-                // its acquire, passed on by the next CTA barrier, makes the other
-                // slices' partials visible to every epilogue thread.
+                // Split-K fix-up; every slice has written its whole partial.  One
+                // wave (swapped tiles here; unswapped ones take the path above):
+                // block b belongs to share b mod S, share j has its own arrival
+                // count, and each slice arrives on the other shares, then waits a
+                // bounded time on its own; the slice whose arrival completes a
+                // share's count finalises it, and an owner whose peers all
+                // arrived in time finalises its own.  Otherwise the last slice to
+                // arrive on the tile's counter finalises the whole tile and resets
+                // the count.  Either way the partials are summed in slice order.
+                // The releases (after the CTA barrier that orders every epilogue
+                // thread's partial stores before them) publish this CTA's
+                // partial; the acquires, passed on by the next CTA barrier, make
+                // the other slices' partials visible to every epilogue thread.
                 named_bar_sync(1, kEpiThreads);
-                if (ew == 0 && lane == 0) {
-                    int32_t mine;
+                if (ew == 0) {
+                    uint32_t shares = 0;   // bit j: finalise share j (last arriver: bit 0, the tile)
                     if (e_coop) {
-                        const uint64_t before = atom_release_gpu_add_u64(e_epochs + xtile, 1);
-                        const uint64_t target = before - before % (uint64_t)e_split_k + (uint64_t)e_split_k;
-                        mine = wait_epoch(e_epochs + xtile, target, ctl, SITE_FIXUP) ? 1 : 0;
-                    } else {
+                        const int32_t S = e_split_k, me = w.split;
+                        uint64_t *const counts = e_epochs + (size_t)xtile * S;
+                        bool last = false;
+                        if (lane < S - 1)
+                            last = atom_acq_rel_gpu_add_u64(counts + (me + 1 + lane) % S, 1) % (uint64_t)S ==
+                                   (uint64_t)(S - 1);
+                        const uint32_t foreign = __ballot_sync(0xFFFFFFFFu, last);
+                        uint32_t own = 0;
+                        if (lane == 0) {
+                            if (poll_share(counts + me, (uint32_t)S, ctl, p.share_poll_cycles)) {
+                                atomicAdd(reinterpret_cast<unsigned long long *>(counts + me), 1ull);
+                                own = 1;
+                            } else {
+                                own = atom_acq_rel_gpu_add_u64(counts + me, 1) % (uint64_t)S == (uint64_t)(S - 1);
+                            }
+                        }
+                        own = __shfl_sync(0xFFFFFFFFu, own, 0);
+                        for (int32_t i = 0; i < S - 1; ++i)
+                            if ((foreign >> i) & 1u) shares |= 1u << ((me + 1 + i) % S);
+                        if (own) shares |= 1u << me;
+                    } else if (lane == 0) {
                         const int32_t old = atom_acq_rel_gpu_add(e_counters + xtile, 1);
-                        mine = (old == e_split_k - 1) ? 1 : 0;
-                        if (mine) atomicExch(e_counters + xtile, 0);
+                        if (old == e_split_k - 1) {
+                            shares = 1;
+                            atomicExch(e_counters + xtile, 0);
+                        }
                     }
-                    *last_flag = mine;
+                    if (lane == 0) *last_flag = (int32_t)shares;
                 }
                 named_bar_sync(1, kEpiThreads);
-                const bool mine = *last_flag != 0;
+                const uint32_t shares = (uint32_t)*last_flag;
                 named_bar_sync(1, kEpiThreads);   // the flag is rewritten by the next unit
-                if (mine) {
-                    const float4 *tile_ws = reinterpret_cast<const float4 *>(
-                        e_workspace + (size_t)xtile * e_split_k * (size_t)tile_elems);
-                    const size_t slice4 = (size_t)tile_elems / 4;
-                    const int32_t rgroups = cta_rows / 32;
-                    const int32_t nblocks = rgroups * chunks;
-                    const int32_t first_b = e_coop ? w.split : 0, stride = e_coop ? e_split_k : 1;
+                const float4 *tile_ws =
+                    reinterpret_cast<const float4 *>(e_workspace + (size_t)xtile * e_split_k * (size_t)tile_elems);
+                const size_t slice4 = (size_t)tile_elems / 4;
+                const int32_t rgroups = cta_rows / 32;
+                const int32_t nblocks = rgroups * chunks;
+                const int32_t n_shares = e_coop ? e_split_k : 1;
+#pragma unroll 1
+                for (int32_t jsh = 0; jsh < n_shares; ++jsh) {
+                    if (!((shares >> jsh) & 1u)) continue;
+                    const int32_t first_b = jsh, stride = n_shares;
                     for (int32_t b = first_b + stride * ew; b < nblocks; b += stride * kEpiWarps) {
                         const int32_t rg = b % rgroups, c = b / rgroups;
                         const int32_t r = rg * 32 + lane;
@@ -2006,9 +2082,9 @@ cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, cons
                     const_cast<CUtensorMap *>(&c),  const_cast<CUtensorMap *>(sa ? sa : &none),
                     const_cast<CUtensorMap *>(sb ? sb : &none), const_cast<KernelParams *>(&p)};
     // Every launch allows programmatic overlap with the previous kernel on the
-    // stream (the kernel waits on griddepcontrol before touching memory); CTAs
-    // of a cooperative fix-up wait on each other, so those launches are also
-    // cooperative, which keeps all CTAs resident at once.
+    // stream (the kernel waits on griddepcontrol before touching memory).  No
+    // CTA waits without bound for another (the split-K share owners' waits
+    // fall back), so no launch needs to be cooperative.
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(grid);
@@ -2034,10 +2110,6 @@ cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, cons
         attr[1].val.clusterDim.x = 2;
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
-        cfg.numAttrs = 2;
-    } else if (p.coop_fixup) {
-        attr[1].id = cudaLaunchAttributeCooperative;
-        attr[1].val.cooperative = 1;
         cfg.numAttrs = 2;
     }
     return cudaLaunchKernelExC(&cfg, f, args);

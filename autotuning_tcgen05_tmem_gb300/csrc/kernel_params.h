@@ -38,7 +38,7 @@ struct KernelParams {
     float alpha;                       // C = act(alpha·(A·B) + bias): the product's scale
     float *workspace;                  // split-K partial tiles
     int32_t *counters;                 // split-K arrival counters, one per tile (last arriver)
-    uint64_t *epochs;                  // cooperative split-K: arrivals per tile, never reset
+    uint64_t *epochs;                  // one-wave split-K: arrivals per tile share ([tile][S]), never reset
     int32_t *status;                   // device status word (0 = ok)
     int64_t timeout_ns;                // bound of every mbarrier wait
     int32_t debug_stall;               // epilogue waits on a barrier nothing signals
@@ -46,8 +46,10 @@ struct KernelParams {
                                        // (bit 0 MMA-A, bit 1 MMA-B): the producer copies them
                                        // before the previous kernel has finished (epilogue
                                        // warps still wait for it)
-    int32_t coop_fixup;                // split-K slices finalise shares of their tile together
-                                       // (launched cooperatively: every unit has its own CTA)
+    int32_t coop_fixup;                // one-wave split-K: every unit has its own CTA, and the
+                                       // slices finalise their tile share by share
+    int64_t share_poll_cycles;         // how long a share's owner waits for the other slices
+                                       // (SM clock cycles) before handing its share over
     int32_t pair;                      // 1: cta_group::2, consecutive CTAs share 256-row tiles
     // Block-scaled FP8 (MX): the packed scale arrays (tensor maps tmSA, tmSB:
     // row atoms x sf_kt K atoms of 512 bytes), their per-stage shared-memory

@@ -39,6 +39,7 @@ namespace gemmgb {
 int query_params(gemm_device_params *d);      // runtime.cpp
 extern std::atomic<int64_t> g_timeout_ns;     // runtime.cpp
 extern std::atomic<int32_t> g_debug_stall;    // runtime.cpp
+extern std::atomic<int32_t> g_check;          // runtime.cpp
 
 namespace {
 
@@ -183,41 +184,10 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_epilogue e
     if (rc) return rc;
 
     const Layout L = layout_of(c, GEMM_BF16);
-    KernelParams k;
-    memset(&k, 0, sizeof(k));
-    k.rows = (int32_t)rows;
-    k.cols = (int32_t)cols;
-    k.K = (int32_t)K;
-    k.bm = c.bm;
-    k.bn = c.bn;
-    k.bk = c.bk;
-    k.stages = c.stages;
-    k.raster = c.raster;
-    k.group = c.group;
-    k.split_k = c.split_k;
-    k.tiles_m = (int32_t)tiles_m;
-    k.tiles_n = (int32_t)tiles_n;
-    k.num_kb = (int32_t)cdiv(K, c.bk);
-    k.num_units = (int32_t)(tiles * c.split_k);
-    k.swap_ab = c.swap_ab;
-    k.epi = epi;
-    k.alpha = 1.0f;                 // C = act(1·(A·B) + bias); residual stays null
-    k.a_mn_major = c.swap_ab ? 1 : 0;
-    k.b_mn_major = c.swap_ab ? 0 : 1;
-    k.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)k.a_mn_major << 15) | ((uint32_t)k.b_mn_major << 16) |
-              ((uint32_t)(c.bn >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-    k.a_stage_bytes = L.a_stage_bytes;
-    k.b_stage_bytes = L.b_stage_bytes;
-    k.tx_bytes = L.stage_bytes;
-    k.a_lbo = k.a_mn_major ? (uint32_t)(c.bk * 128) : 16u;
-    k.b_lbo = k.b_mn_major ? (uint32_t)(c.bk * 128) : 16u;
-    k.acc_cols = L.acc_cols;
-    k.n_acc = L.n_acc;
-    k.tmem_cols = L.tmem_cols;
-    k.off_b = L.off_b;
-    k.off_staging = L.off_staging;
-    k.off_bar = L.off_bar;
-    k.staging_buf_bytes = L.staging_buf_bytes;
+    // The same launch record as a plan of this configuration (B read MN-major
+    // in place); the split-K exchange goes through the last-arriver route,
+    // whose counters this call clears below.
+    KernelParams k = kernel_params_of(M, N, K, GEMM_BF16, epi, c, false);
     k.bias = epi != GEMM_EPI_NONE ? bias : nullptr;
     k.status = reinterpret_cast<int32_t *>(ds->scratch);
     k.counters = reinterpret_cast<int32_t *>(ds->scratch + 256);
@@ -234,5 +204,17 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_epilogue e
     const int smem = (int)std::min<int64_t>(ds->params.smem_per_block, std::max<int64_t>(L.smem_total, one_per_sm));
     e = launch_gemm(GEMM_BF16, ma, mb, mc, nullptr, nullptr, k, grid, smem, s);
     if (e != cudaSuccess) return set_error(GEMM_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+    if (g_check.load()) {
+        // Checked runs (GEMM_CHECK / gemm_debug_set(4, 1)): wait for the kernel
+        // and read the status word straight from the array, without allocating.
+        e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return set_error(GEMM_ERR_CUDA, "cudaStreamSynchronize (checked run): %s",
+                                               cudaGetErrorString(e));
+        int32_t st = 0;
+        e = cudaMemcpyFromSymbol(&st, g_noalloc_scratch, sizeof(st), 0, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return set_error(GEMM_ERR_CUDA, "reading the status word: %s", cudaGetErrorString(e));
+        if (st != 0)
+            return set_error(GEMM_ERR_TIMEOUT, "a device wait expired (site %d); the kernel returned early", st);
+    }
     return GEMM_OK;
 }

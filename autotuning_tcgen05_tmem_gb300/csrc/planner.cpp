@@ -106,6 +106,66 @@ Layout layout_of(const gemm_config &c, int dt)
     return L;
 }
 
+KernelParams kernel_params_of(int64_t M, int64_t N, int64_t K, int dt, int act, const gemm_config &c,
+                              bool b_kmajor)
+{
+    const Layout L = layout_of(c, dt);
+    KernelParams k;
+    memset(&k, 0, sizeof(k));
+    k.rows = (int32_t)(c.swap_ab ? N : M);
+    k.cols = (int32_t)(c.swap_ab ? M : N);
+    k.K = (int32_t)K;
+    k.bm = c.bm;
+    k.bn = c.bn;
+    k.bk = c.bk;
+    k.stages = c.stages;
+    k.raster = c.raster;
+    k.group = c.group;
+    k.split_k = c.split_k;
+    k.tiles_m = (int32_t)cdiv(k.rows, c.bm);
+    k.tiles_n = (int32_t)cdiv(k.cols, c.bn);
+    k.num_kb = (int32_t)cdiv(K, c.bk);
+    k.num_units = (int32_t)((int64_t)k.tiles_m * k.tiles_n * c.split_k);
+    k.swap_ab = c.swap_ab;
+    k.epi = act;
+    // User B is N-contiguous (MN-major) unless it is first transposed.  It is
+    // MMA-A when swapped and MMA-B otherwise; A is always K-major.
+    k.a_mn_major = (c.swap_ab && !b_kmajor) ? 1 : 0;
+    k.b_mn_major = (!c.swap_ab && !b_kmajor) ? 1 : 0;
+    // Operand formats: BF16 = 1 of kind::f16, TF32 = 2 of kind::tf32, E4M3 = 0 of kind::f8f6f4
+    // and of kind::mxf8f6f4.
+    const uint32_t fmt = dt == GEMM_BF16 ? 1u : dt == GEMM_FP32_TF32 ? 2u : 0u;
+    k.pair = c.cta_group == 2 ? 1 : 0;
+    k.alpha = 1.0f;
+    const uint32_t mma_m = k.pair ? 256u : 128u;  // a pair's MMA spans both CTAs' 128 rows
+    // Instruction descriptor: bits 4-5 the accumulator format (fp32 = 1), 7-9 and
+    // 10-12 A's and B's formats, 15 and 16 their majorness, 17-22 N/8, 24-28 M/16.
+    // The block-scaled kind has an fp32 accumulator implied and uses bits 4-5
+    // (and 29-30) for B's (A's) scale ID, set per MMA; bit 23 = 1 names the
+    // scales E8M0.
+    const bool mx = dt == GEMM_MXFP8_E4M3;
+    k.idesc = (mx ? (1u << 23) : (1u << 4)) | (fmt << 7) | (fmt << 10) | ((uint32_t)k.a_mn_major << 15) |
+              ((uint32_t)k.b_mn_major << 16) | ((uint32_t)(c.bn >> 3) << 17) | ((mma_m >> 4) << 24);
+    k.a_stage_bytes = L.a_stage_bytes;
+    k.b_stage_bytes = L.b_stage_bytes;
+    k.tx_bytes = L.stage_bytes + L.sf_stage_bytes;
+    k.sf_kt = mx ? (int32_t)mx_k_atoms(K) : 0;
+    k.sf_stage_bytes = L.sf_stage_bytes;
+    k.off_sf = L.off_sf;
+    k.sc_stage_cols = L.sc_stage_cols;
+    k.sc_col0 = L.sc_col0;
+    k.a_lbo = k.a_mn_major ? (uint32_t)(c.bk * 128) : 16u;
+    k.b_lbo = k.b_mn_major ? (uint32_t)(c.bk * 128) : 16u;
+    k.acc_cols = L.acc_cols;
+    k.n_acc = L.n_acc;
+    k.tmem_cols = L.tmem_cols;
+    k.off_b = L.off_b;
+    k.off_staging = L.off_staging;
+    k.off_bar = L.off_bar;
+    k.staging_buf_bytes = L.staging_buf_bytes;
+    return k;
+}
+
 // Whether split-K slices of a tile can reduce through distributed shared
 // memory: cluster of S in {2, 4, 8} CTAs, unswapped, and the partials an owner
 // receives (its blocks x (S - 1) x 16 KB) fit in its pipeline ring.  Blocks

@@ -42,6 +42,10 @@ std::atomic<int32_t> g_b_route{0};
 // memory when all units fit in one wave and the slices of a tile can form a
 // cluster, else global memory; 1 = always global memory.
 std::atomic<int32_t> g_split_route{0};
+// How long (SM clock cycles) the owner of a one-wave split-K share waits for
+// the other slices before it hands the share over: about 25 us at the top
+// clock.  0 makes every owner hand over at once (tests drive that path).
+std::atomic<int64_t> g_share_poll{50000};
 // Checked runs (GEMM_CHECK set to anything but 0 in the environment, or
 // gemm_debug_set(4, 1)): every run synchronises its stream and reports a
 // device-side timeout itself instead of leaving it to gemm_plan_status.
@@ -219,7 +223,7 @@ struct gemm_plan_s {
     float *workspace = nullptr;
     bool owns_workspace = false;
     int32_t *aux = nullptr;          // [0] status word, [1..n_counters] split-K counters
-    uint64_t *epochs = nullptr;      // cooperative split-K arrival counts (only ever grow)
+    uint64_t *epochs = nullptr;      // one-wave split-K: arrival counts per tile share (only ever grow)
     int64_t n_counters = 0;
     int64_t tiles = 0;
     std::vector<DescEntry> descs = std::vector<DescEntry>(16);
@@ -229,6 +233,11 @@ struct gemm_plan_s {
     int32_t independent = 0;         // GEMM_OPERAND_A | GEMM_OPERAND_B: operands that the work
                                      // queued before a launch never writes
     void *bt = nullptr;
+    // Host-buffer batches (run_host_many): a second plan of the same
+    // configuration (its own split-K workspace, counters and device buffers)
+    // and a second stream, so that one GEMM's copies overlap the other's kernel.
+    gemm_plan_s *twin = nullptr;
+    cudaStream_t side = nullptr;
 };
 
 namespace gemmgb {
@@ -302,66 +311,17 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     p->dev = dev;
     cudaGetDevice(&p->device);
     p->L = layout_of(cfg, dt);
-    KernelParams &k = p->kp;
-    memset(&k, 0, sizeof(k));
-    k.rows = (int32_t)(cfg.swap_ab ? N : M);
-    k.cols = (int32_t)(cfg.swap_ab ? M : N);
-    k.K = (int32_t)K;
-    k.bm = cfg.bm;
-    k.bn = cfg.bn;
-    k.bk = cfg.bk;
-    k.stages = cfg.stages;
-    k.raster = cfg.raster;
-    k.group = cfg.group;
-    k.split_k = cfg.split_k;
-    k.tiles_m = (int32_t)cdiv(k.rows, cfg.bm);
-    k.tiles_n = (int32_t)cdiv(k.cols, cfg.bn);
-    k.num_kb = (int32_t)cdiv(K, cfg.bk);
-    p->tiles = (int64_t)k.tiles_m * k.tiles_n;
-    k.num_units = (int32_t)(p->tiles * cfg.split_k);
-    k.swap_ab = cfg.swap_ab;
-    k.epi = act_code(epi);   // the kernel's bias/activation code; the residual is a run argument
     const int route = g_b_route.load();
     p->b_kmajor = route == 1 || (route == 0 && !b_in_place(dt, N));
-    // User B is N-contiguous (MN-major) unless it is first transposed.  It is
-    // MMA-A when swapped and MMA-B otherwise; A is always K-major.
-    k.a_mn_major = (cfg.swap_ab && !p->b_kmajor) ? 1 : 0;
-    k.b_mn_major = (!cfg.swap_ab && !p->b_kmajor) ? 1 : 0;
-    // Operand formats: BF16 = 1 of kind::f16, TF32 = 2 of kind::tf32, E4M3 = 0 of kind::f8f6f4
-    // and of kind::mxf8f6f4.
-    const uint32_t fmt = dt == GEMM_BF16 ? 1u : dt == GEMM_FP32_TF32 ? 2u : 0u;
-    k.pair = cfg.cta_group == 2 ? 1 : 0;
-    k.alpha = 1.0f;
-    const uint32_t mma_m = k.pair ? 256u : 128u;  // a pair's MMA spans both CTAs' 128 rows
-    // Instruction descriptor: bits 4-5 the accumulator format (fp32 = 1), 7-9 and
-    // 10-12 A's and B's formats, 15 and 16 their majorness, 17-22 N/8, 24-28 M/16.
-    // The block-scaled kind has an fp32 accumulator implied and uses bits 4-5
-    // (and 29-30) for B's (A's) scale ID, set per MMA; bit 23 = 1 names the
-    // scales E8M0.
-    const bool mx = dt == GEMM_MXFP8_E4M3;
-    k.idesc = (mx ? (1u << 23) : (1u << 4)) | (fmt << 7) | (fmt << 10) | ((uint32_t)k.a_mn_major << 15) |
-              ((uint32_t)k.b_mn_major << 16) | ((uint32_t)(cfg.bn >> 3) << 17) | ((mma_m >> 4) << 24);
-    k.a_stage_bytes = p->L.a_stage_bytes;
-    k.b_stage_bytes = p->L.b_stage_bytes;
-    k.tx_bytes = p->L.stage_bytes + p->L.sf_stage_bytes;
-    k.sf_kt = mx ? (int32_t)mx_k_atoms(K) : 0;
-    k.sf_stage_bytes = p->L.sf_stage_bytes;
-    k.off_sf = p->L.off_sf;
-    k.sc_stage_cols = p->L.sc_stage_cols;
-    k.sc_col0 = p->L.sc_col0;
-    k.a_lbo = k.a_mn_major ? (uint32_t)(cfg.bk * 128) : 16u;
-    k.b_lbo = k.b_mn_major ? (uint32_t)(cfg.bk * 128) : 16u;
-    k.acc_cols = p->L.acc_cols;
-    k.n_acc = p->L.n_acc;
-    k.tmem_cols = p->L.tmem_cols;
-    k.off_b = p->L.off_b;
-    k.off_staging = p->L.off_staging;
-    k.off_bar = p->L.off_bar;
-    k.staging_buf_bytes = p->L.staging_buf_bytes;
+    // The kernel's bias/activation code; the residual is a run argument.
+    p->kp = kernel_params_of(M, N, K, dt, act_code(epi), cfg, p->b_kmajor);
+    KernelParams &k = p->kp;
+    p->tiles = (int64_t)k.tiles_m * k.tiles_n;
     p->grid = (int)std::min<int64_t>(k.num_units, dev.sm_count);
-    // One wave of split-K units: the slices of a tile finalise it together.
-    // (The cooperative fix-up stages peer partials in the idle pipeline ring: it
-    // needs 8 warps x 4 KB of it.)
+    // One wave of split-K units: the slices of a tile finalise it share by
+    // share, each owner its own unless a peer is late (no slice ever waits for
+    // one that may not be resident).  The fix-up stages partials in the idle
+    // pipeline ring: it needs 8 warps x 4 KB of it.
     const bool ring_room = p->L.off_staging >= 8u * 4096u;
     k.coop_fixup = (cfg.split_k > 1 && k.num_units <= dev.sm_count && !k.pair && ring_room) ? 1 : 0;
     // Or the slices of a tile form a cluster and reduce through distributed
@@ -392,8 +352,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     k.counters = p->aux + 1;
     p->n_counters = n_counters;
     if (cfg.split_k > 1) {
-        e = cudaMalloc(&p->epochs, (size_t)n_counters * sizeof(uint64_t));
-        if (e == cudaSuccess) e = cudaMemset(p->epochs, 0, (size_t)n_counters * sizeof(uint64_t));
+        const size_t n_counts = (size_t)n_counters * (size_t)cfg.split_k;   // one per share of a tile
+        e = cudaMalloc(&p->epochs, n_counts * sizeof(uint64_t));
+        if (e == cudaSuccess) e = cudaMemset(p->epochs, 0, n_counts * sizeof(uint64_t));
         if (e != cudaSuccess) {
             cudaFree(p->epochs);
             cudaFree(p->aux);
@@ -431,10 +392,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
         return rc;
     }
     if (k.pair) {
-        // Pairs that fit at once: the persistent grid, and whether all split-K
-        // units are resident together (the slices then finalise cooperatively;
-        // the capacity check stands in for a cooperative launch, which does not
-        // combine with clusters).
+        // Pairs that fit at once: the persistent grid, and whether the split-K
+        // units make one wave (one unit per pair; the slices then finalise
+        // share by share, which needs no guarantee that they are resident
+        // together).
         int pairs = 0;
         e = max_active_clusters(dt, k.a_mn_major, k.b_mn_major, 2, 2, p->smem_request, &pairs);
         if (e != cudaSuccess || pairs < 1) {
@@ -495,6 +456,8 @@ void destroy_plan(gemm_plan_t p)
     cudaFree(p->hB);
     cudaFree(p->hBias);
     cudaFree(p->hC);
+    destroy_plan(p->twin);
+    if (p->side) cudaStreamDestroy(p->side);
     delete p;
 }
 
@@ -622,6 +585,7 @@ int run_plan_mx(gemm_plan_t p, const void *A, const void *SA, const void *B, con
     kp.residual = R;
     kp.timeout_ns = g_timeout_ns.load();
     kp.debug_stall = g_debug_stall.load();
+    kp.share_poll_cycles = g_share_poll.load();
     // Declared operands map to the kernel's MMA-A (bit 0) and MMA-B (bit 1);
     // swapped, MMA-A is B.  A K-major copy of B is written by the kernel just
     // before, so B then always waits.
@@ -721,9 +685,47 @@ static int read_status(gemm_plan_t p)
     if (st != 0) {
         // An early return may leave counts part-way: start them afresh.
         cudaMemset(p->aux, 0, (size_t)(1 + p->n_counters) * sizeof(int32_t));
-        if (p->epochs) cudaMemset(p->epochs, 0, (size_t)p->n_counters * sizeof(uint64_t));
+        if (p->epochs) cudaMemset(p->epochs, 0, (size_t)p->n_counters * p->cfg.split_k * sizeof(uint64_t));
         return set_error(GEMM_ERR_TIMEOUT, "a device wait expired (site %d); the kernel returned early", st);
     }
+    return GEMM_OK;
+}
+
+// Plan-owned device buffers for runs from host memory (allocated on first use).
+static int host_run_buffers(gemm_plan_t p)
+{
+    if (p->hC) return GEMM_OK;
+    const size_t e = (size_t)elt_bytes(p->dt), eo = (size_t)out_elt_bytes(p->dt);
+    const size_t nA = (size_t)p->M * p->K * e, nB = (size_t)p->K * p->N * e, nBias = (size_t)p->N * eo,
+                 nC = (size_t)p->M * p->N * eo;
+    cudaError_t err;
+    if ((nA && (err = cudaMalloc(&p->hA, nA)) != cudaSuccess) || (nB && (err = cudaMalloc(&p->hB, nB)) != cudaSuccess) ||
+        (err = cudaMalloc(&p->hBias, nBias)) != cudaSuccess || (err = cudaMalloc(&p->hC, nC)) != cudaSuccess)
+        return cuda_err(err, "cudaMalloc(host-run buffers)");
+    return GEMM_OK;
+}
+
+// Copies one GEMM's inputs in, runs it, and queues the copy of C back, all on `stream`.
+static int host_run_enqueue(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C,
+                            cudaStream_t stream)
+{
+    const size_t e = (size_t)elt_bytes(p->dt), eo = (size_t)out_elt_bytes(p->dt);
+    const size_t nA = (size_t)p->M * p->K * e, nB = (size_t)p->K * p->N * e, nBias = (size_t)p->N * eo,
+                 nC = (size_t)p->M * p->N * eo;
+    const bool has_bias = p->epi != GEMM_EPI_NONE;
+    if (has_bias && !bias) return set_error(GEMM_ERR_INVALID_ARG, "bias is required by the epilogue");
+    if (!C || (p->K > 0 && (!A || !B))) return set_error(GEMM_ERR_INVALID_ARG, "null A, B or C");
+    cudaError_t err;
+    if (nA && (err = cudaMemcpyAsync(p->hA, A, nA, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return cuda_err(err, "copy A to device");
+    if (nB && (err = cudaMemcpyAsync(p->hB, B, nB, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return cuda_err(err, "copy B to device");
+    if (has_bias && (err = cudaMemcpyAsync(p->hBias, bias, nBias, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return cuda_err(err, "copy bias to device");
+    int rc = run_plan(p, p->hA, p->hB, has_bias ? p->hBias : nullptr, p->hC, stream);
+    if (rc) return rc;
+    if ((err = cudaMemcpyAsync(C, p->hC, nC, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+        return cuda_err(err, "copy C to host");
     return GEMM_OK;
 }
 
@@ -731,32 +733,61 @@ int run_host(gemm_plan_t p, const void *A, const void *B, const void *bias, void
 {
     if (!p) return set_error(GEMM_ERR_INVALID_ARG, "null plan");
     if (p->M == 0 || p->N == 0) return GEMM_OK;
-    const size_t e = (size_t)elt_bytes(p->dt), eo = (size_t)out_elt_bytes(p->dt);
-    const size_t nA = (size_t)p->M * p->K * e, nB = (size_t)p->K * p->N * e, nBias = (size_t)p->N * eo,
-                 nC = (size_t)p->M * p->N * eo;
-    cudaError_t err;
-    if (!p->hC) {
-        if ((nA && (err = cudaMalloc(&p->hA, nA)) != cudaSuccess) ||
-            (nB && (err = cudaMalloc(&p->hB, nB)) != cudaSuccess) ||
-            (err = cudaMalloc(&p->hBias, nBias)) != cudaSuccess || (err = cudaMalloc(&p->hC, nC)) != cudaSuccess)
-            return cuda_err(err, "cudaMalloc(host-run buffers)");
-    }
-    if (nA && (err = cudaMemcpyAsync(p->hA, A, nA, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-        return cuda_err(err, "copy A to device");
-    if (nB && (err = cudaMemcpyAsync(p->hB, B, nB, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-        return cuda_err(err, "copy B to device");
-    const bool has_bias = p->epi != GEMM_EPI_NONE;
-    if (has_bias) {
-        if (!bias) return set_error(GEMM_ERR_INVALID_ARG, "bias is required by the epilogue");
-        if ((err = cudaMemcpyAsync(p->hBias, bias, nBias, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-            return cuda_err(err, "copy bias to device");
-    }
-    int rc = run_plan(p, p->hA, p->hB, has_bias ? p->hBias : nullptr, p->hC, stream);
+    int rc = host_run_buffers(p);
+    if (!rc) rc = host_run_enqueue(p, A, B, bias, C, stream);
     if (rc) return rc;
-    if ((err = cudaMemcpyAsync(C, p->hC, nC, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
-        return cuda_err(err, "copy C to host");
-    if ((err = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_err(err, "cudaStreamSynchronize");
+    cudaError_t err = cudaStreamSynchronize(stream);
+    if (err != cudaSuccess) return cuda_err(err, "cudaStreamSynchronize");
     return GEMM_OK;
+}
+
+// n GEMMs of the plan's shape from host buffers, pipelined: GEMM i runs on
+// `stream` when i is even and on the plan's second stream (with a second plan
+// of the same configuration, whose split-K state is its own) when i is odd, so
+// the copies of one GEMM overlap the kernel of the other.  Returns once every
+// C is in host memory, with both plans' device status words read.
+int run_host_many(gemm_plan_t p, int n, const void *const *A, const void *const *B, const void *const *bias,
+                  void *const *C, cudaStream_t stream)
+{
+    if (!p) return set_error(GEMM_ERR_INVALID_ARG, "null plan");
+    if (n < 0 || (n > 0 && (!A || !B || !C))) return set_error(GEMM_ERR_INVALID_ARG, "bad GEMM count or null arrays");
+    if (p->epi != GEMM_EPI_NONE && n > 0 && !bias) return set_error(GEMM_ERR_INVALID_ARG, "null bias array");
+    if (n == 0 || p->M == 0 || p->N == 0) return GEMM_OK;
+    int rc = host_run_buffers(p);
+    if (rc) return rc;
+    cudaError_t err;
+    if (n > 1 && !p->twin) {
+        rc = make_plan(p->M, p->N, p->K, p->dt, p->epi, p->cfg, p->dev, nullptr, &p->twin);
+        if (rc) return rc;
+        if ((rc = host_run_buffers(p->twin))) return rc;
+    }
+    if (n > 1 && !p->side && (err = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_err(err, "cudaStreamCreate");
+    if (p->twin) {
+        p->twin->kp.alpha = p->kp.alpha;
+        p->twin->independent = p->independent;
+    }
+    cudaEvent_t ev = nullptr;
+    if (n > 1) {
+        // the second stream starts after the work queued on the caller's stream
+        if ((err = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_err(err, "cudaEventCreate");
+        cudaEventRecord(ev, stream);
+        cudaStreamWaitEvent(p->side, ev, 0);
+    }
+    for (int i = 0; i < n && !rc; ++i) {
+        const bool odd = (i & 1) != 0;
+        rc = host_run_enqueue(odd ? p->twin : p, A[i], B[i], bias ? bias[i] : nullptr, C[i], odd ? p->side : stream);
+    }
+    cudaError_t e1 = cudaStreamSynchronize(stream);
+    cudaError_t e2 = p->side ? cudaStreamSynchronize(p->side) : cudaSuccess;
+    if (ev) cudaEventDestroy(ev);
+    if (rc) return rc;
+    if (e1 != cudaSuccess) return cuda_err(e1, "cudaStreamSynchronize");
+    if (e2 != cudaSuccess) return cuda_err(e2, "cudaStreamSynchronize (second stream)");
+    rc = read_status(p);
+    if (!rc && p->twin && n > 1) rc = read_status(p->twin);
+    return rc;
 }
 
 // ---------------------------------------------------------------------------

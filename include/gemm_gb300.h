@@ -341,9 +341,12 @@ int gemm_plan_config(gemm_plan_t plan, gemm_config *out);
 /* How a plan launches its GEMM kernel (library-specific; the pages have no
  * counterpart).  splitk_route: 0 = no split-K; 1 = partial tiles through
  * global memory, the last slice to arrive finalises the tile; 2 = partial
- * tiles through global memory, all slices finalise shares of the tile together
- * (cooperative launch, one wave); 3 = the slices of a tile form one
- * thread-block cluster and reduce through distributed shared memory. */
+ * tiles through global memory in one wave, each slice finalising its own share
+ * of the tile once the others have arrived (an owner whose peers are late, for
+ * instance not resident because another kernel holds their SMs, hands its
+ * share to whichever slice arrives last, so no slice waits for one that may
+ * not run); 3 = the slices of a tile form one thread-block cluster (resident
+ * together by construction) and reduce through distributed shared memory. */
 typedef struct {
     int32_t grid;          /* CTAs launched */
     int32_t block;         /* threads per CTA */
@@ -409,6 +412,24 @@ int gemm_mx_pack_scales(const void *scales, int64_t rows, int64_t K, int32_t b_s
  * Host buffers should be pinned for full copy bandwidth. */
 int gemm_run_host(gemm_plan_t plan, const void *A, const void *B, const void *bias, void *C,
                   gemm_stream_t stream);
+
+/* n independent GEMMs of the plan's shape from HOST buffers (A[i], B[i],
+ * bias[i] -> C[i]; bias may be NULL with GEMM_EPI_NONE; epilogues without
+ * residual), pipelined so that host<->device copies overlap the kernels: GEMM
+ * i runs on `stream` when i is even and on a second, plan-owned stream when i
+ * is odd, with a second plan of the same configuration (its own device
+ * buffers and split-K state, made on the first call with n > 1, so make that
+ * call before any stream capture).  The second stream starts after the work
+ * already queued on `stream`.  Returns after every C is in host memory and
+ * both plans' device status words have been read: GEMM_ERR_TIMEOUT if a device
+ * wait expired.  The copies overlap only when the host buffers are pinned
+ * (page-locked); pageable buffers give correct results without overlap.  Like
+ * gemm_run_host, this is the library's end-to-end entry point: the pages
+ * measure kernels, and this measures what a caller holding host data sees.
+ * "Tiling the hierarchy", double buffering (a copy overlaps compute only when
+ * it is asynchronous), applied one level up, to the host link. */
+int gemm_run_host_many(gemm_plan_t plan, int32_t n, const void *const *A, const void *const *B,
+                       const void *const *bias, void *const *C, gemm_stream_t stream);
 
 /* Synchronise and read the plan's device status word: GEMM_OK or
  * GEMM_ERR_TIMEOUT (a bounded wait expired; the status is cleared and the
@@ -491,8 +512,11 @@ int gemm_tune_batch(const int64_t *mnk, int32_t n, gemm_dtype dtype, gemm_epilog
  * wave and the slices of a tile can form a thread-block cluster, else through
  * global memory; 1 = always through global memory); what = 4: checked runs
  * (1 = every run synchronises and reports a device timeout, 0 = off; the
- * initial value comes from GEMM_CHECK).  Affects launches (what 0, 1, 4) or
- * plans (what 2, 3) made after the call, from any thread. */
+ * initial value comes from GEMM_CHECK); what = 5: how many SM clock cycles the
+ * owner of a one-wave split-K share (splitk_route 2) waits for the other
+ * slices before handing its share over (default 50000, about 25 us; 0 = hand
+ * over at once, which tests use to drive that path).  Affects launches (what
+ * 0, 1, 4, 5) or plans (what 2, 3) made after the call, from any thread. */
 int gemm_debug_set(int32_t what, int64_t value);
 
 /* ---------------------------------------------------------------------------
@@ -526,8 +550,11 @@ int gemm_debug_set(int32_t what, int64_t value);
  *     each call first clears, on `stream`, the status word and the counters it
  *     uses.  Calls whose work overlaps on the GPU (other streams, other host
  *     threads) race on the scratch and must be serialised by the caller.
- *   - A device wait that expires is recorded in the scratch's status word but is
- *     not reported by this call, which does not synchronise. */
+ *   - A device wait that expires is recorded in the scratch's status word.  In
+ *     checked-run mode (GEMM_CHECK, or gemm_debug_set(4, 1)) the call
+ *     synchronises `stream`, reads that word (without allocating) and returns
+ *     GEMM_ERR_TIMEOUT, like gemm_run; otherwise it is not reported, and the
+ *     next call clears it. */
 int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_epilogue epi, const gemm_config *cfg,
                      const void *A, const void *B, const void *bias, void *C, gemm_stream_t stream);
 

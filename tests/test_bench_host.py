@@ -76,3 +76,28 @@ def test_shipped_set_report_on_a_small_table():
     assert r["3"]["in_sample_mean"] == 1.0 and r["3"]["in_sample_worst"] == 1.0
     # c2 first (gain 2), then c0 (gain 1 on "a"); c1 then gains nothing, so the set stops at two
     assert [tuple(x) for x in r["3"]["configs"]] == [c[2], c[0]]
+
+
+def test_peak_choice_follows_the_sampled_clocks():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert not bench.power_capped({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []})
+    assert bench.power_capped({"sm_mhz": 1515.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]})
+    assert bench.power_capped({"sm_mhz": 1700.0, "sm_max_mhz": 2070.0, "reasons": []})
+    assert not bench.power_capped(None)
+
+
+def test_clock_samples_are_placed_by_their_own_timestamps():
+    sys.path.insert(0, ROOT)
+    import bench
+    import datetime
+    c = bench.ClockSampler(0)
+    c.proc = object()                       # as if nvidia-smi were running
+    base = datetime.datetime(2026, 1, 1, 12, 0, 0)
+    for i, mhz in enumerate((2070, 1500, 1500, 2070)):
+        t = base + datetime.timedelta(milliseconds=100 * i)
+        c.samples.append((t.timestamp(), [t.strftime("%Y/%m/%d %H:%M:%S.%f")[:-3], str(mhz), "2070", "900",
+                                          "0x0", "Not Active", "Not Active", "Not Active",
+                                          "Active" if mhz < 2000 else "Not Active"]))
+    s = c.summary_between(base.timestamp() + 0.05, base.timestamp() + 0.25)
+    assert s["samples_in_timed_region"] == 2 and s["sm_mhz"] == 1500 and s["reasons"] == ["sw_power_cap"]
