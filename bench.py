@@ -36,6 +36,10 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOP/s (or GB/s) per shape, % of roofline; tuned vs fixed-128x128 speedup"
 DEFAULT_WORKLOAD = "bf16_gelu_1000x1000x8192"
+# Timed beside the headline in the same run: the correctness-sized fp32 case,
+# the large square multiply and the 16-token decode (the targets are set on the
+# last two: >= 70% of the dense bf16 tensor peak and >= 80% of HBM bandwidth).
+PER_WORKLOAD = ["fp32_relu_256", "bf16_relu_8192", "bf16_decode_16x8192x28672"]
 
 
 def parse_args():
@@ -52,6 +56,8 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-fixed", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the per-workload block (the 256^3 fp32, 8192^3 and 16-token decode workloads)")
     ap.add_argument("--eager", action="store_true", help="launch from Python instead of a CUDA graph")
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload (the four headline shapes and the 30-shape sweep): one "
@@ -122,7 +128,10 @@ def set_bytes_of(w):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 100 ms.  Each sample is placed in time by
+    nvidia-smi's own timestamp (its output reaches the pipe in bursts, so the
+    time it is read says little), and `mark` brackets the timed region."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -147,8 +156,14 @@ class ClockSampler:
             time.sleep(0.02)
 
     def _reader(self):
+        import datetime
         for line in self.proc.stdout:
-            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+            f = [x.strip() for x in line.split(",")]
+            try:
+                t = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except (ValueError, IndexError):
+                t = time.time()
+            self.samples.append((t, f))
 
     def mark(self, which):
         setattr(self, which, time.time())
@@ -166,8 +181,13 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
-        inside = [s for t, s in self.samples if self.t0 is not None and self.t0 <= t <= self.t1]
-        near = inside or [s for _t, s in self.samples]
+        return self.summary_between(self.t0, self.t1)
+
+    def summary_between(self, t0, t1):
+        if self.proc is None or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        inside = [s for t, s in list(self.samples) if t0 is not None and t1 is not None and t0 <= t <= t1]
+        near = inside or [s for _t, s in list(self.samples)]
         def num(x):
             try:
                 return float(x)
@@ -187,7 +207,8 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None,
                 "reasons": sorted(reasons),
                 "samples_in_timed_region": len(inside),
-                "samples_total": len(self.samples)}
+                "samples_total": len(self.samples),
+                "window": "timed region" if inside else "whole run (no sample fell inside the timed region)"}
 
 
 # ---------------------------------------------------------------------------
@@ -396,9 +417,99 @@ def time_gemm(plan, sets, steps, warmup):
     return e0.elapsed_time(e1) / 1e3 / steps / len(sets)
 
 
+def power_capped(clocks_summary) -> bool:
+    """Whether the GPU ran under its power cap during a timed region: the
+    sustained tensor peak is then the fair denominator, else the burst one."""
+    if not clocks_summary:
+        return False
+    mhz, mx = clocks_summary.get("sm_mhz"), clocks_summary.get("sm_max_mhz")
+    return "sw_power_cap" in clocks_summary.get("reasons", []) or bool(mhz and mx and mhz < 0.95 * mx)
+
+
+def rotating_sets(w, l2_bytes, cap=512):
+    """How many input sets a step rotates over: enough that together they
+    exceed twice the L2 (so no timed GEMM is served from L2), at most `cap`."""
+    return int(min(cap, max(1, math.ceil(2 * l2_bytes / set_bytes_of(w)))))
+
+
+def measure_workload(w, devp, peaks, peak_src, operands="none", clocks=None, target_s=0.5,
+                     tune_report=False):
+    """The tuned plan of workload w and the fixed 128x128 tile, each timed over
+    rotating input sets (graph replay, CUDA events, about `target_s` seconds of
+    GEMMs); returns a dict with the value in the bound's unit, the roofline
+    share of the GEMM kernel, tuned vs fixed, the tuned configuration and the
+    SM clocks sampled during the tuned timing."""
+    import torch
+    import autotuning_tcgen05_tmem_gb300 as g
+    flops, cbytes, _elt = work_of(w)
+    nsets = rotating_sets(w, devp.l2_bytes)
+    sets = make_sets(w, nsets, torch.device("cuda", torch.cuda.current_device()))
+    t0 = time.perf_counter()
+    plan = g.plan(w.M, w.N, w.K, w.dtype, w.epi)
+    tune_s = time.perf_counter() - t0
+    try:
+        plan.set_independent_operands(declared(operands))
+        est = time_gemm(plan, sets, 2, 2)                     # calibrate the step count
+        steps = int(min(20000, max(3, target_s / max(est * nsets, 1e-7))))
+        if clocks is not None:
+            clocks.mark("t0")
+        t_tuned = time_gemm(plan, sets, steps, 5)
+        if clocks is not None:
+            clocks.mark("t1")
+        assert plan.status() == 0, g.last_error()
+        shape_clocks = clocks.summary() if clocks is not None else None
+        fixed = g.fixed_config(w.dtype, devp)
+        with g.plan_with_config(w.M, w.N, w.K, w.dtype, w.epi, fixed) as fp:
+            fp.set_independent_operands(declared(operands))
+            t_fixed = time_gemm(fp, sets, max(3, steps // 2), 5)
+            assert fp.status() == 0, g.last_error()
+        t_decl = {}
+        for decl in ("none", "B", "AB"):
+            if decl != operands:
+                plan.set_independent_operands(declared(decl))
+                t_decl[decl] = time_gemm(plan, sets, max(3, steps // 4), 5) * 1e6
+        plan.set_independent_operands(declared(operands))
+        cfg = list(plan.config.astuple())
+        info = plan.launch_info
+    finally:
+        plan.close()
+    # Under the power cap (seen in the clocks sampled during the timing) the
+    # sustained tensor peak is the denominator; otherwise the burst one.
+    region_s = t_tuned * steps * nsets
+    sustained = power_capped(shape_clocks) if shape_clocks is not None else region_s > 1.0
+    bf16_peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops", 1900.0)
+    tpeak = bf16_peak * peak_ratio(w.dtype)
+    bw = peaks.get("hbm_gbs", 6800.0)
+    tensor_bound = flops / (tpeak * 1e12) >= cbytes / (bw * 1e9)
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": flops / t_tuned / 1e12, "peak": tpeak, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": cbytes / t_tuned / 1e9, "peak": bw, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = (f"{peak_src} bf16 {'sustained' if sustained else 'burst'} x {peak_ratio(w.dtype)}"
+                           if tensor_bound else f"{peak_src} HBM")
+    out = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype, "epilogue": w.epi,
+           "value": roof["achieved"], "unit": roof["unit"],
+           "tflops": flops / t_tuned / 1e12, "gbs": cbytes / t_tuned / 1e9, "roofline": roof,
+           "tuned_config": cfg, "tuned_us": t_tuned * 1e6, "fixed_us": t_fixed * 1e6,
+           "tuned_vs_fixed": t_fixed / t_tuned, "operands": operands, "tuned_us_other_operands": t_decl,
+           "splitk_route": g.SPLITK_ROUTES.get(info.splitk_route, str(info.splitk_route)),
+           "plan_seconds": tune_s, "timed_region_s": region_s, "rotating_sets": nsets,
+           "l2": (f"{nsets} sets of {set_bytes_of(w) / 1e6:.1f} MB rotate ({nsets * set_bytes_of(w) / 1e6:.0f} MB "
+                  f"{'>' if nsets * set_bytes_of(w) > 2 * devp.l2_bytes else '<='} 2 x L2)"),
+           "clocks": shape_clocks}
+    if tune_report:
+        tr = g.tune(w.M, w.N, w.K, w.dtype, w.epi, topk=int(os.environ.get("GEMM_TUNE_TOPK", "24")))
+        st = tr.stats
+        out["tune"] = {"candidates": st.n_candidates, "measured": st.n_measured, "kendall_tau": st.kendall_tau,
+                       "top1_hit": st.top1_hit, "regret": st.regret, "search_seconds": st.tune_seconds}
+    del sets
+    torch.cuda.empty_cache()
+    return out
+
+
 def sweep(args):
     """One JSON line per workload: tuned vs fixed throughput and roofline share."""
-    import torch
     import autotuning_tcgen05_tmem_gb300 as g
     from autotuning_tcgen05_tmem_gb300 import _build, inputs
     _build.build()
@@ -416,59 +527,18 @@ def sweep(args):
     clocks.start()
     for name in names:
         w = inputs.WORKLOADS[name]
-        flops, cbytes, elt = work_of(w)
-        set_bytes = set_bytes_of(w)
-        nsets = int(min(8, max(1, math.ceil(2 * devp.l2_bytes / set_bytes))))
-        sets = make_sets(w, nsets, torch.device("cuda", 0))
         # Host side of the selection alone: enumerate and rank by the model
         # (microseconds; "Autotuning & cost models" §5 weighs it against the
-        # on-device search below).
+        # on-device search).
         t0 = time.perf_counter()
         cands = g.enumerate_configs(w.M, w.N, w.K, w.dtype, w.epi, devp)
         preds = [g.model_predict(w.M, w.N, w.K, w.dtype, w.epi, c_, devp).predicted_us for c_ in cands]
         host_rank_us = (time.perf_counter() - t0) * 1e6
-        t0 = time.perf_counter()
-        plan = g.plan(w.M, w.N, w.K, w.dtype, w.epi)
-        tune_s = time.perf_counter() - t0
-        plan.set_independent_operands(declared(args.operands))
-        steps = max(3, int(0.3 / max(1e-6, 1e-6 * 20 * nsets)))  # about 0.3 s at 20 us per GEMM
-        steps = min(steps, 2000)
-        clocks.mark("t0")
-        t_tuned = time_gemm(plan, sets, steps, 5)
-        clocks.mark("t1")
-        shape_clocks = clocks.summary()
-        with g.plan_with_config(w.M, w.N, w.K, w.dtype, w.epi, g.fixed_config(w.dtype, devp)) as fp:
-            fp.set_independent_operands(declared(args.operands))
-            t_fixed = time_gemm(fp, sets, steps, 5)
-        t_decl = {}
-        for decl in ("none", "B", "AB"):
-            if decl != args.operands:
-                plan.set_independent_operands(declared(decl))
-                t_decl[decl] = time_gemm(plan, sets, max(3, steps // 2), 5) * 1e6
-        plan.set_independent_operands(declared(args.operands))
-        # A timed region longer than a second runs under the power cap: the
-        # sustained tensor peak is the denominator there (as in the main line).
-        region_s = t_tuned * steps * nsets
-        sustained = region_s > 1.0
-        bf16_peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops", 1900.0)
-        tpeak = bf16_peak * peak_ratio(w.dtype)
-        bw = peaks.get("hbm_gbs", 6800.0)
-        roof_t = max(flops / (tpeak * 1e12), cbytes / (bw * 1e9))
-        line = {"workload": name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype, "epilogue": w.epi,
-                "tuned_config": list(plan.config.astuple()), "tuned_us": t_tuned * 1e6,
-                "tflops": flops / t_tuned / 1e12, "gbs": cbytes / t_tuned / 1e9,
-                "bound": "tensor" if flops / (tpeak * 1e12) >= cbytes / (bw * 1e9) else "hbm",
-                "roofline_frac": roof_t / t_tuned, "fixed_us": t_fixed * 1e6,
-                "tuned_vs_fixed": t_fixed / t_tuned, "operands": args.operands, "tuned_us_other_operands": t_decl,
-                "plan_seconds": tune_s, "timed_region_s": region_s,
-                "candidates": len(cands), "host_rank_us": host_rank_us,
-                "model_best_us": min(preds) if preds else None, "clocks": shape_clocks,
-                "peaks": f"{peak_src} bf16 {'sustained' if sustained else 'burst'} {bf16_peak} TFLOP/s, "
-                         f"HBM {bw} GB/s"}
+        line = measure_workload(w, devp, peaks, peak_src, args.operands, clocks, target_s=0.3)
+        line.update({"candidates": len(cands), "host_rank_us": host_rank_us,
+                     "model_best_us": min(preds) if preds else None,
+                     "bound": line["roofline"]["bound"], "roofline_frac": line["roofline"]["frac"]})
         print(json.dumps(line), flush=True)
-        plan.close()
-        del sets
-        torch.cuda.empty_cache()
     clocks.stop()
     return 0
 
@@ -573,7 +643,7 @@ def main():
     flops, cbytes, elt = work_of(w)
     devp = g.device_params_query()
     set_bytes = set_bytes_of(w)
-    nsets = int(min(8, max(1, math.ceil(2 * devp.l2_bytes / set_bytes))))
+    nsets = rotating_sets(w, devp.l2_bytes)
     sets = make_sets(w, nsets, dev)
 
     # --- plan: tune once (cost model + measurement), cached by shape ---------
@@ -616,7 +686,8 @@ def main():
     value = job_value(flops, nsets, args.steps, world, elapsed)
 
     # --- roofline of the GEMM kernel -----------------------------------------
-    sustained = elapsed > 1.0
+    clock_summary = clocks.summary()
+    sustained = power_capped(clock_summary)
     # another dtype's peak: the measured bf16 peak x the nominal dense ratio
     tpeak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops", 1900.0) * peak_ratio(w.dtype)
     bw = peaks.get("hbm_gbs", 6800.0)
@@ -654,7 +725,7 @@ def main():
                       "operands": OPERAND_NOTES[args.operands]},
            "roofline": roof,
            "gpu_launches": args.steps * nsets * launches_per_gemm,
-           "clocks": clocks.summary(),
+           "clocks": clock_summary,
            "plan_seconds": plan_s}
 
     # --- tuned vs fixed 128x128, and the tuner's own report -------------------
@@ -701,57 +772,55 @@ def main():
         hb = bias.cpu().pin_memory() if bias is not None else None
         h2d = (w.M * w.K + w.K * w.N) * elt + (w.N * elt_sizes(w.dtype)[1] if bias is not None else 0)
         d2h = w.M * w.N * elt_sizes(w.dtype)[1]
-        esteps = max(5, min(args.steps, 200))
-        # (1) Pipelined through the public device API: steps alternate over two
-        # streams, each with its own plan (a split-K plan runs on one stream at
-        # a time) and device buffers; a step copies its inputs in, runs, and
-        # reads its result back, and the copies of one step overlap the kernel
-        # of the other.
-        pl2 = [plan, g.plan_with_config(w.M, w.N, w.K, w.dtype, w.epi, cfg)]
-        st2 = [torch.cuda.Stream(), torch.cuda.Stream()]
-        dA = [torch.empty_like(A) for _ in range(2)]
-        dB = [torch.empty_like(B) for _ in range(2)]
-        db = [torch.empty_like(bias) if bias is not None else None for _ in range(2)]
-        dC = [torch.empty(w.M, w.N, dtype=inputs.out_torch_dtype(w.dtype), device=dev) for _ in range(2)]
-        hC2 = [torch.empty(w.M, w.N, dtype=inputs.out_torch_dtype(w.dtype)).pin_memory() for _ in range(2)]
-
-        def e2e_step(i):
-            s = i % 2
-            with torch.cuda.stream(st2[s]):
-                dA[s].copy_(hA, non_blocking=True)
-                dB[s].copy_(hB, non_blocking=True)
-                if hb is not None:
-                    db[s].copy_(hb, non_blocking=True)
-                pl2[s].run(dA[s], dB[s], db[s], dC[s], st2[s])
-                hC2[s].copy_(dC[s], non_blocking=True)
-
-        for i in range(4):
-            e2e_step(i)
+        esteps = max(6, min(args.steps, 200))
+        esteps += esteps % 2
+        hC = [torch.empty(w.M, w.N, dtype=inputs.out_torch_dtype(w.dtype)).pin_memory() for _ in range(2)]
+        hstream = torch.cuda.Stream()
+        # (1) gemm_run_host_many, the library's pipelined host-buffer entry
+        # point: every GEMM copies its inputs from pinned host memory and its
+        # result back, inside the timed region; the library alternates two
+        # streams (and two plans of the configuration) so one GEMM's copies
+        # overlap the other's kernel, and reads both plans' status words.
+        many = lambda n: plan.run_host_many([hA] * n, [hB] * n, None if hb is None else [hb] * n,
+                                             [hC[i % 2] for i in range(n)], hstream)
+        many(4)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for i in range(esteps):
-            e2e_step(i)
-        torch.cuda.synchronize()
+        many(esteps)
         dt = (time.perf_counter() - t0) / esteps
-        assert pl2[1].status() == 0, g.last_error()
-        pl2[1].close()
         out["e2e"] = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "steps": esteps,
-                      "path": "pinned host buffers -> two streams (copy in, gemm_run, copy out per step; one "
-                              "step's copies overlap the other's kernel)"}
+                      "path": "gemm_run_host_many (C ABI): pinned host buffers; per GEMM, copy A, B, bias in, "
+                              "run, copy C out; two streams inside the library overlap one GEMM's copies with "
+                              "the other's kernel; returns after every C is in host memory"}
         # (2) The synchronous host-buffer entry point, one call per step.
-        hC = torch.empty(w.M, w.N, dtype=inputs.out_torch_dtype(w.dtype)).pin_memory()
-        hstream = torch.cuda.Stream()
         for _ in range(3):
-            plan.run_host(hA, hB, hb, hC, hstream)
+            plan.run_host(hA, hB, hb, hC[0], hstream)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(esteps):
-            plan.run_host(hA, hB, hb, hC, hstream)
+            plan.run_host(hA, hB, hb, hC[0], hstream)
         dt = (time.perf_counter() - t0) / esteps
+        assert plan.status() == 0, g.last_error()
         out["e2e_sync"] = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                            "d2h_bytes_per_step": d2h, "steps": esteps,
-                           "path": "gemm_run_host (copies, one kernel, copy back, synchronise; per step)"}
+                           "path": "gemm_run_host (C ABI: copies, one kernel, copy back, synchronise; per step)"}
+
+    # --- the other workloads the targets are set on, timed in this run --------
+    if not args.no_per_workload and rank == 0 and world == 1:
+        pw_clocks = ClockSampler(local)
+        pw_clocks.start()
+        per = {}
+        for name in PER_WORKLOAD:
+            if name == w.name:
+                continue
+            r = measure_workload(inputs.WORKLOADS[name], devp, peaks, peak_src, args.operands, pw_clocks,
+                                 target_s=1.5 if name == "bf16_relu_8192" else 0.5)
+            per[name] = {k: r[k] for k in ("value", "unit", "roofline", "tuned_vs_fixed", "tuned_config",
+                                           "tuned_us", "fixed_us", "splitk_route", "timed_region_s", "l2",
+                                           "clocks")}
+        pw_clocks.stop()
+        out["per_workload"] = per
 
     # --- CPU oracle ------------------------------------------------------------
     if not args.no_cpu and rank == 0 and world == 1:
