@@ -49,7 +49,7 @@ EXPORTS = ["gemm_version", "gemm_last_error", "gemm_device_params_default",
            "gemm_cache_save", "gemm_cache_load", "gemm_plan_launch_info", "gemm_select_config_set",
            "gemm_plan_from_list", "gemm_tune_batch", "gemm_run_ex", "gemm_plan_set_scale",
            "gemm_run_mx", "gemm_mx_scales_bytes", "gemm_mx_pack_scales", "gemm_model_params_load",
-           "gemm_plan_set_independent_operands", "gemm_run_host_many"]
+           "gemm_plan_set_independent_operands", "gemm_run_host_many", "gemm_plan_tuned_on", "gemm_tune_on"]
 
 
 class GemmError(RuntimeError):
@@ -190,6 +190,10 @@ def _load_library(path: str):
         "gemm_debug_set": (ctypes.c_int, [i32, i64]),
         "gemm_run_noalloc": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, P(Config), vp, vp, vp, vp, vp]),
         "gemm_run_host_many": (ctypes.c_int, [vp, i32, P(vp), P(vp), P(vp), P(vp), vp]),
+        "gemm_plan_tuned_on": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp,
+                                              P(vp)]),
+        "gemm_tune_on": (ctypes.c_int, [i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, i32,
+                                        P(TuneRow), i32, P(i32), P(RankStats)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -416,6 +420,15 @@ def plan(M, N, K, dtype="bf16", epi="none") -> Plan:
     return Plan(h.value, M, N, K, _dt(dtype), _ep(epi))
 
 
+def plan_tuned_on(M, N, K, dtype, epi, A, B, bias=None, SA=None, SB=None) -> Plan:
+    """gemm_plan_tuned_on: like plan(), timing the candidates on copies of the
+    given device operands on a cache miss."""
+    h = ctypes.c_void_p()
+    _check(lib().gemm_plan_tuned_on(M, N, K, _dt(dtype), _ep(epi), _ptr(A), _ptr(SA), _ptr(B), _ptr(SB), _ptr(bias),
+                                    ctypes.byref(h)))
+    return Plan(h.value, M, N, K, _dt(dtype), _ep(epi))
+
+
 def plan_with_config(M, N, K, dtype, epi, cfg: Config) -> Plan:
     h = ctypes.c_void_p()
     _check(lib().gemm_plan_with_config(M, N, K, _dt(dtype), _ep(epi), ctypes.byref(cfg), ctypes.byref(h)))
@@ -439,6 +452,16 @@ def tune(M, N, K, dtype="bf16", epi="none", topk=0, cap=4096) -> TuneResult:
     n = ctypes.c_int32(0)
     s = RankStats()
     _check(lib().gemm_tune(M, N, K, _dt(dtype), _ep(epi), topk, rows, cap, ctypes.byref(n), ctypes.byref(s)))
+    return TuneResult([rows[i] for i in range(n.value)], s)
+
+
+def tune_on(M, N, K, dtype, epi, A, B, bias=None, SA=None, SB=None, topk=0, cap=4096) -> TuneResult:
+    """gemm_tune_on: the ranked table, timed on copies of the given operands."""
+    rows = (TuneRow * cap)()
+    n = ctypes.c_int32(0)
+    s = RankStats()
+    _check(lib().gemm_tune_on(M, N, K, _dt(dtype), _ep(epi), _ptr(A), _ptr(SA), _ptr(B), _ptr(SB), _ptr(bias), topk,
+                              rows, cap, ctypes.byref(n), ctypes.byref(s)))
     return TuneResult([rows[i] for i in range(n.value)], s)
 
 

@@ -36,9 +36,10 @@ extern std::atomic<int32_t> g_b_route;
 extern std::atomic<int32_t> g_split_route;
 extern std::atomic<int32_t> g_check;
 extern std::atomic<int64_t> g_share_poll;
+extern std::atomic<int32_t> g_tune_fill;
 int query_params(gemm_device_params *d);
 int model_params_load(const char *path, gemm_device_params *out);
-int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out);
+int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out, const TuneInputs *user);
 int plan_explicit(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &cfg, gemm_plan_t *out);
 int run_plan(gemm_plan_t p, const void *A, const void *B, const void *bias, void *C, cudaStream_t stream);
 int run_plan_ex(gemm_plan_t p, const void *A, const void *B, const void *bias, const void *R, void *C,
@@ -57,7 +58,7 @@ int plan_set_independent_operands(gemm_plan_t p, int32_t mask);
 void destroy_plan(gemm_plan_t p);
 int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, uint64_t seed,
          std::vector<gemm_tune_row> &rows, gemm_rank_stats &stats, gemm_config *winner,
-         const gemm_config *list, int nlist);
+         const gemm_config *list, int nlist, const TuneInputs *user);
 int plan_from_list(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config *list, int nlist,
                    gemm_plan_t *out);
 int tune_batch(const int64_t *mnk, int n, int dt, int epi, const char *path, int32_t *n_tuned);
@@ -168,7 +169,16 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue e
 {
     clear_error();
     if (!out) return set_error(GEMM_ERR_INVALID_ARG, "null output");
-    return plan_tuned(M, N, K, dtype, epi, out);
+    return plan_tuned(M, N, K, dtype, epi, out, nullptr);
+}
+
+int gemm_plan_tuned_on(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, const void *A,
+                       const void *SA, const void *B, const void *SB, const void *bias, gemm_plan_t *out)
+{
+    clear_error();
+    if (!out) return set_error(GEMM_ERR_INVALID_ARG, "null output");
+    const TuneInputs in{A, B, bias, SA, SB};
+    return plan_tuned(M, N, K, dtype, epi, out, &in);
 }
 
 int gemm_plan_with_config(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
@@ -262,12 +272,13 @@ int gemm_plan_status(gemm_plan_t plan)
 void gemm_plan_destroy(gemm_plan_t plan) { destroy_plan(plan); }
 
 static int tune_into(int64_t M, int64_t N, int64_t K, int dtype, int epi, int mode, int32_t k, uint64_t seed,
-                     gemm_tune_row *rows, int32_t cap, int32_t *n_rows, gemm_rank_stats *stats)
+                     gemm_tune_row *rows, int32_t cap, int32_t *n_rows, gemm_rank_stats *stats,
+                     const TuneInputs *user = nullptr)
 {
     if (!n_rows || cap < 0 || (cap > 0 && !rows)) return set_error(GEMM_ERR_INVALID_ARG, "gemm_tune: bad argument");
     std::vector<gemm_tune_row> v;
     gemm_rank_stats s;
-    const int rc = tune(M, N, K, dtype, epi, mode, k, seed, v, s, nullptr, nullptr, 0);
+    const int rc = tune(M, N, K, dtype, epi, mode, k, seed, v, s, nullptr, nullptr, 0, user);
     if (rc) return rc;
     int32_t i = 0;
     for (; i < cap && i < (int32_t)v.size(); ++i) rows[i] = v[i];
@@ -282,6 +293,16 @@ int gemm_tune(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue e
     clear_error();
     return tune_into(M, N, K, dtype, epi, topk > 0 ? GEMM_SEARCH_MODEL_TOPK : GEMM_SEARCH_EXHAUSTIVE, topk, 0, rows,
                      cap, n_rows, stats);
+}
+
+int gemm_tune_on(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, const void *A, const void *SA,
+                 const void *B, const void *SB, const void *bias, int32_t topk, gemm_tune_row *rows, int32_t cap,
+                 int32_t *n_rows, gemm_rank_stats *stats)
+{
+    clear_error();
+    const TuneInputs in{A, B, bias, SA, SB};
+    return tune_into(M, N, K, dtype, epi, topk > 0 ? GEMM_SEARCH_MODEL_TOPK : GEMM_SEARCH_EXHAUSTIVE, topk, 0, rows,
+                     cap, n_rows, stats, &in);
 }
 
 int gemm_tune_search(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, gemm_search mode,
@@ -370,6 +391,11 @@ int gemm_debug_set(int32_t what, int64_t value)
     if (what == 5) {
         if (value < 0) return set_error(GEMM_ERR_INVALID_ARG, "the share wait must be >= 0 cycles");
         g_share_poll.store(value);
+        return GEMM_OK;
+    }
+    if (what == 6) {
+        if (value < 0 || value > 1) return set_error(GEMM_ERR_INVALID_ARG, "tuning fill must be 0 or 1");
+        g_tune_fill.store((int32_t)value);
         return GEMM_OK;
     }
     return set_error(GEMM_ERR_INVALID_ARG, "unknown debug control %d", what);

@@ -62,6 +62,13 @@ uint32_t cluster_recv_bytes(const gemm_config &c);
 KernelParams kernel_params_of(int64_t M, int64_t N, int64_t K, int dt, int act, const gemm_config &c,
                               bool b_kmajor);
 
+// Operands a caller lends the tuner (device pointers in the layouts gemm_run and
+// gemm_run_mx take; SA and SB packed MX scales, block-scaled plans only): the
+// candidates are timed on copies of them instead of on synthetic fills.
+struct TuneInputs {
+    const void *A, *B, *bias, *SA, *SB;
+};
+
 // Host logic (planner.cpp)
 void params_default(gemm_device_params *d);
 void params_workshop(gemm_device_params *d);
@@ -89,8 +96,8 @@ cudaError_t launch_gemm(int dt, const CUtensorMap &a, const CUtensorMap &b, cons
                         const CUtensorMap *sa, const CUtensorMap *sb, const KernelParams &p, int grid, int smem_bytes,
                         cudaStream_t stream);
 cudaError_t launch_transpose(const void *src, void *dst, int64_t rows, int64_t cols, int elt, cudaStream_t stream);
-cudaError_t launch_fill_uniform(void *dst, int64_t n, int dt, float scale, uint32_t seed,
-                                cudaStream_t stream);
+cudaError_t launch_fill_random(void *dst, int64_t n, int dt, float scale, uint32_t seed, int dist,
+                               cudaStream_t stream);
 cudaError_t launch_mx_pack(const uint8_t *src, int64_t rows, int64_t K, int b_side, uint8_t *dst,
                            cudaStream_t stream);
 

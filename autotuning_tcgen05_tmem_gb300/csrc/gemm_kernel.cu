@@ -1902,18 +1902,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Fills a buffer with a counter-based pseudo-random uniform in [-scale, scale]
-// (tuning inputs: same value distribution as real operands, never user data).
-__global__ void fill_uniform_kernel(void *dst, int64_t n, int dt, float scale, uint32_t seed)
+// Counter-based 32-bit hash of element i (a finaliser of the splitmix family).
+__device__ __forceinline__ uint32_t hash_u32(uint32_t x)
+{
+    x ^= x >> 16;
+    x *= 0x7FEB352Du;
+    x ^= x >> 15;
+    x *= 0x846CA68Bu;
+    x ^= x >> 16;
+    return x;
+}
+
+// Fills a buffer with counter-based pseudo-random values: dist 0 uniform in
+// [-scale, scale], dist 1 normal with standard deviation `scale` (Box-Muller
+// on two hashed uniforms).  Tuning inputs only, never user data.
+__global__ void fill_random_kernel(void *dst, int64_t n, int dt, float scale, uint32_t seed, int dist)
 {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        uint32_t x = (uint32_t)i * 0x9E3779B9u ^ seed;
-        x ^= x >> 16;
-        x *= 0x7FEB352Du;
-        x ^= x >> 15;
-        x *= 0x846CA68Bu;
-        x ^= x >> 16;
-        const float f = ((float)(x >> 8) * (1.0f / 16777216.0f) * 2.0f - 1.0f) * scale;
+        const uint32_t x = hash_u32((uint32_t)i * 0x9E3779B9u ^ seed);
+        float f;
+        if (dist == 0) {
+            f = ((float)(x >> 8) * (1.0f / 16777216.0f) * 2.0f - 1.0f) * scale;
+        } else {
+            const uint32_t y = hash_u32(x ^ 0x68E31DA4u ^ (uint32_t)(i >> 32));
+            const float u1 = ((float)(x >> 8) + 1.0f) * (1.0f / 16777216.0f);   // (0, 1]
+            const float u2 = (float)(y >> 8) * (1.0f / 16777216.0f);
+            f = sqrtf(-2.0f * logf(u1)) * cospif(2.0f * u2) * scale;
+        }
         if (dt == 0) reinterpret_cast<__nv_bfloat16 *>(dst)[i] = __float2bfloat16_rn(f);
         else if (dt == 2 || dt == 3) reinterpret_cast<__nv_fp8_storage_t *>(dst)[i] = __nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3);
         else reinterpret_cast<float *>(dst)[i] = f;
@@ -2192,12 +2207,13 @@ cudaError_t launch_mx_pack(const uint8_t *src, int64_t rows, int64_t K, int b_si
     return cudaGetLastError();
 }
 
-cudaError_t launch_fill_uniform(void *dst, int64_t n, int dt, float scale, uint32_t seed, cudaStream_t stream)
+cudaError_t launch_fill_random(void *dst, int64_t n, int dt, float scale, uint32_t seed, int dist,
+                               cudaStream_t stream)
 {
     if (n <= 0) return cudaSuccess;
     int64_t blocks = (n + 255) / 256;
     if (blocks > 4096) blocks = 4096;
-    fill_uniform_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dst, n, dt, scale, seed);
+    fill_random_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dst, n, dt, scale, seed, dist);
     return cudaGetLastError();
 }
 

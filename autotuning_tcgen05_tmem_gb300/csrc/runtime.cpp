@@ -46,6 +46,10 @@ std::atomic<int32_t> g_split_route{0};
 // the other slices before it hands the share over: about 25 us at the top
 // clock.  0 makes every owner hand over at once (tests drive that path).
 std::atomic<int64_t> g_share_poll{50000};
+// Value distribution of the tuner's synthetic operands: 1 = normal with
+// standard deviation 1/sqrt(K) (the default: the workloads' N(0,1)/sqrt(K)
+// family), 0 = uniform of the same standard deviation.
+std::atomic<int32_t> g_tune_fill{1};
 // Checked runs (GEMM_CHECK set to anything but 0 in the environment, or
 // gemm_debug_set(4, 1)): every run synchronises its stream and reports a
 // device-side timeout itself instead of leaving it to gemm_plan_status.
@@ -822,7 +826,7 @@ static int env_int(const char *name, int dflt)
 
 int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, uint64_t seed,
          std::vector<gemm_tune_row> &rows, gemm_rank_stats &stats, gemm_config *winner,
-         const gemm_config *list, int nlist)
+         const gemm_config *list, int nlist, const TuneInputs *user)
 {
     const auto t_start = std::chrono::steady_clock::now();
     memset(&stats, 0, sizeof(stats));
@@ -924,7 +928,22 @@ int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, u
         cudaStream_t s;
         ~StreamGuard() { cudaStreamDestroy(s); }
     } sg{stream};
-    const float scale_ab = (float)sqrt(3.0 / (double)std::max<int64_t>(K, 1));
+    // Synthetic operands with the workloads' spread (standard deviation
+    // 1/sqrt(K), "Tile Selection", "Measurement, and what it must control":
+    // tuning inputs must resemble the real ones in distribution), or copies of
+    // the caller's own operands.
+    const int fill = g_tune_fill.load();
+    const float sd = (float)(1.0 / sqrt((double)std::max<int64_t>(K, 1)));
+    const float scale_ab = fill == 0 ? sd * (float)sqrt(3.0) : sd;
+    if (user) {
+        // the caller's operands are read on this private stream: finish what
+        // the device has queued first (their producers may be on any stream)
+        if ((err = cudaDeviceSynchronize()) != cudaSuccess) return cuda_err(err, "cudaDeviceSynchronize");
+        const bool need_b = K > 0 && N > 0, need_a = K > 0 && M > 0;
+        if ((need_a && !user->A) || (need_b && !user->B) || (epi != GEMM_EPI_NONE && !user->bias) ||
+            (mx && K > 0 && (!user->SA || !user->SB)))
+            return set_error(GEMM_ERR_INVALID_ARG, "tuning on given operands: A, B, bias (and MX scales) are needed");
+    }
     for (int s = 0; s < nsets; ++s) {
         void *a = nullptr, *b = nullptr, *bb = nullptr, *c = nullptr;
         if ((err = cudaMalloc(&a, bytes_a)) != cudaSuccess) return cuda_err(err, "cudaMalloc(tuning A)");
@@ -935,18 +954,33 @@ int tune(int64_t M, int64_t N, int64_t K, int dt, int epi, int mode, int topk, u
         buf.bias.push_back(bb);
         if ((err = cudaMalloc(&c, bytes_c)) != cudaSuccess) return cuda_err(err, "cudaMalloc(tuning C)");
         buf.C.push_back(c);
-        launch_fill_uniform(a, (int64_t)(bytes_a / e), dt, scale_ab, 0x1234u + 17u * s, stream);
-        launch_fill_uniform(b, (int64_t)(bytes_b / e), dt, scale_ab, 0x5678u + 17u * s, stream);
-        launch_fill_uniform(bb, (int64_t)(bytes_bias / eo), odt, 0.1f, 0x9ABCu + 17u * s, stream);
+        if (user) {
+            // Every set a copy of the caller's operands (distinct addresses, so
+            // the rotation still keeps the timed GEMMs out of L2).
+            if (M * K > 0) cudaMemcpyAsync(a, user->A, (size_t)(M * K) * e, cudaMemcpyDeviceToDevice, stream);
+            if (K * N > 0) cudaMemcpyAsync(b, user->B, (size_t)(K * N) * e, cudaMemcpyDeviceToDevice, stream);
+            if (epi != GEMM_EPI_NONE) cudaMemcpyAsync(bb, user->bias, (size_t)N * eo, cudaMemcpyDeviceToDevice, stream);
+        } else {
+            launch_fill_random(a, (int64_t)(bytes_a / e), dt, scale_ab, 0x1234u + 17u * s, fill, stream);
+            launch_fill_random(b, (int64_t)(bytes_b / e), dt, scale_ab, 0x5678u + 17u * s, fill, stream);
+            launch_fill_random(bb, (int64_t)(bytes_bias / eo), odt, 0.1f, 0x9ABCu + 17u * s, fill, stream);
+        }
         if (mx) {
-            // Packed scales of 2^0 (E8M0 127): the timing does not depend on their values.
+            // Packed scales: the caller's, or 2^0 (E8M0 127) for synthetic operands.
             void *sa = nullptr, *sb = nullptr;
             if ((err = cudaMalloc(&sa, bytes_sa)) != cudaSuccess) return cuda_err(err, "cudaMalloc(tuning SA)");
             buf.SA.push_back(sa);
             if ((err = cudaMalloc(&sb, bytes_sb)) != cudaSuccess) return cuda_err(err, "cudaMalloc(tuning SB)");
             buf.SB.push_back(sb);
-            cudaMemsetAsync(sa, 127, bytes_sa, stream);
-            cudaMemsetAsync(sb, 127, bytes_sb, stream);
+            if (user && K > 0) {
+                cudaMemcpyAsync(sa, user->SA, (size_t)(mx_row_atoms(M) * mx_k_atoms(K) * kMxAtomBytes),
+                                cudaMemcpyDeviceToDevice, stream);
+                cudaMemcpyAsync(sb, user->SB, (size_t)(mx_row_atoms(N) * mx_k_atoms(K) * kMxAtomBytes),
+                                cudaMemcpyDeviceToDevice, stream);
+            } else {
+                cudaMemsetAsync(sa, 127, bytes_sa, stream);
+                cudaMemsetAsync(sb, 127, bytes_sb, stream);
+            }
         }
     }
     size_t ws_bytes = 0;
@@ -1168,7 +1202,7 @@ static std::string cache_key(int64_t M, int64_t N, int64_t K, int dt, int epi, c
     return buf;
 }
 
-int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out)
+int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out, const TuneInputs *user)
 {
     *out = nullptr;
     int rc = check_extents(M, N, K);
@@ -1209,7 +1243,7 @@ int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *ou
     std::vector<gemm_tune_row> rows;
     gemm_rank_stats stats;
     rc = tune(M, N, K, dt, epi, exhaustive ? GEMM_SEARCH_EXHAUSTIVE : GEMM_SEARCH_MODEL_TOPK, topk, 0, rows, stats,
-              &cfg, nullptr, 0);
+              &cfg, nullptr, 0, user);
     if (rc) return rc;
     {
         std::lock_guard<std::mutex> lk(g_cache_mu);
@@ -1244,7 +1278,7 @@ int plan_from_list(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_
                 return make_plan(M, N, K, dt, epi, list[i], dev, nullptr, out);
         return set_error(GEMM_ERR_UNSUPPORTED, "no configuration of the list runs this shape");
     }
-    rc = tune(M, N, K, dt, epi, GEMM_SEARCH_EXHAUSTIVE, 0, 0, rows, stats, &cfg, list, nlist);
+    rc = tune(M, N, K, dt, epi, GEMM_SEARCH_EXHAUSTIVE, 0, 0, rows, stats, &cfg, list, nlist, nullptr);
     if (rc) return rc;
     return make_plan(M, N, K, dt, epi, cfg, dev, nullptr, out);
 }
@@ -1258,7 +1292,7 @@ int tune_batch(const int64_t *mnk, int n, int dt, int epi, const char *path, int
     cache_stats(&before, nullptr, nullptr);
     for (int i = 0; i < n; ++i) {
         gemm_plan_t p = nullptr;
-        const int rc = plan_tuned(mnk[3 * i], mnk[3 * i + 1], mnk[3 * i + 2], dt, epi, &p);
+        const int rc = plan_tuned(mnk[3 * i], mnk[3 * i + 1], mnk[3 * i + 2], dt, epi, &p, nullptr);
         if (rc) return rc;
         destroy_plan(p);
     }

@@ -298,9 +298,29 @@ int gemm_model_params_load(const char *path, gemm_device_params *dev);
  * the fixed config without timing; GEMM_TUNE_MODE=exhaustive|topk (default
  * topk); GEMM_TUNE_TOPK=k (default 24).  Synchronises; never touches user
  * memory.  The returned handle is owned by the caller (gemm_plan_destroy) and
- * may be used on one stream at a time. */
+ * may be used on one stream at a time.  The synthetic operands the candidates
+ * are timed on are normally distributed with standard deviation 1/sqrt(K), the
+ * spread of the workloads' N(0,1)/sqrt(K) operands ("Tile Selection",
+ * "Measurement, and what it must control": tuning inputs must resemble the real
+ * ones in distribution, not merely in shape; gemm_debug_set(6, 0) selects a
+ * uniform fill of the same spread); gemm_plan_tuned_on times them on the
+ * caller's own operands instead. */
 int gemm_plan(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi,
               gemm_plan_t *out);
+
+/* gemm_plan, but on a cache miss the candidates are timed on copies of the
+ * caller's operands (device pointers in the layouts gemm_run / gemm_run_mx
+ * take: A [M, K], B [K, N], bias [N] unless GEMM_EPI_NONE, and for block-scaled
+ * FP8 the packed scales SA and SB; SA and SB are NULL otherwise) instead of on
+ * synthetic ones, so that the values, and the power they draw under the power
+ * cap, are the real ones ("Tile Selection", "Measurement, and what it must
+ * control").  The operands are only read: the call first synchronises the
+ * device (their producers may be on any stream), then copies them into
+ * library-owned buffers; it never writes caller memory.  The winner is cached
+ * under the same key as gemm_plan's.  GEMM_ERR_INVALID_ARG when an operand the
+ * shape needs is NULL. */
+int gemm_plan_tuned_on(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, const void *A,
+                       const void *SA, const void *B, const void *SB, const void *bias, gemm_plan_t *out);
 
 /* Plan with an explicit configuration (no tuning, no cache).  Returns
  * GEMM_ERR_INFEASIBLE, with the reason in gemm_last_error, if it breaks a rule. */
@@ -445,6 +465,12 @@ int gemm_tune(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue e
               int32_t topk, gemm_tune_row *rows, int32_t cap, int32_t *n_rows,
               gemm_rank_stats *stats);
 
+/* gemm_tune on copies of the caller's operands (as gemm_plan_tuned_on takes
+ * them) instead of synthetic ones; never touches the cache. */
+int gemm_tune_on(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, const void *A, const void *SA,
+                 const void *B, const void *SB, const void *bias, int32_t topk, gemm_tune_row *rows, int32_t cap,
+                 int32_t *n_rows, gemm_rank_stats *stats);
+
 /* Search strategies at a given measurement budget ("Autotuning & cost models"
  * §6): time every candidate; the cost model's top k (plus the fixed tile, so
  * tuning never loses to it — "CuTile Autotuning"); or k candidates drawn
@@ -515,8 +541,10 @@ int gemm_tune_batch(const int64_t *mnk, int32_t n, gemm_dtype dtype, gemm_epilog
  * initial value comes from GEMM_CHECK); what = 5: how many SM clock cycles the
  * owner of a one-wave split-K share (splitk_route 2) waits for the other
  * slices before handing its share over (default 50000, about 25 us; 0 = hand
- * over at once, which tests use to drive that path).  Affects launches (what
- * 0, 1, 4, 5) or plans (what 2, 3) made after the call, from any thread. */
+ * over at once, which tests use to drive that path); what = 6: the value
+ * distribution of the tuner's synthetic operands (1 = normal, the default; 0 =
+ * uniform of the same standard deviation).  Affects launches (what 0, 1, 4, 5),
+ * plans (what 2, 3) or tunings (what 6) made after the call, from any thread. */
 int gemm_debug_set(int32_t what, int64_t value);
 
 /* ---------------------------------------------------------------------------

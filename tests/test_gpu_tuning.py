@@ -1,6 +1,7 @@
 """The selection layer on the GPU: tune-once cache, the fixed-tile switch,
 selection exactness (the chosen configuration is the measured fastest within
 3%), the tune report, and the bounded-wait timeout path."""
+import ctypes
 import os
 
 import numpy as np
@@ -239,3 +240,44 @@ def test_checked_runs_report_a_device_timeout_from_the_run_itself():
         assert p.status() == 0
     from gpu_util import device_bits, oracle_rounded_bits
     assert np.array_equal(device_bits(C.cpu()), oracle_rounded_bits(A, B, bias, "relu", g.BF16))
+
+
+def test_tuning_on_the_callers_operands():
+    """gemm_tune_on / gemm_plan_tuned_on time the candidates on copies of the
+    caller's operands: the caller's buffers are left as they were, the plan
+    runs correctly, and the winner is cached under gemm_plan's key."""
+    M, N, K = 256, 384, 1024
+    A, B, bias = operands(M, N, K, "bf16", "int", seed=31)
+    Ad, Bd, bd = A.cuda(), B.cuda(), bias.cuda()
+    before = [t.clone() for t in (Ad, Bd, bd)]
+    r = g.tune_on(M, N, K, "bf16", "relu", Ad, Bd, bd, topk=6)
+    assert r.stats.n_measured >= 6 and all(row.status == 0 for row in r.rows if row.measured_us > 0)
+    g.cache_clear()
+    with g.plan_tuned_on(M, N, K, "bf16", "relu", Ad, Bd, bd) as p:
+        Cd, _ = alloc_out(M, N, g.BF16)
+        p.run(Ad, Bd, bd, Cd)
+        assert p.status() == 0
+        cfg = p.config.astuple()
+    for t, b in zip((Ad, Bd, bd), before):
+        assert torch.equal(t, b)
+    from gpu_util import device_bits, oracle_rounded_bits
+    assert np.array_equal(device_bits(Cd.cpu()), oracle_rounded_bits(A, B, bias, "relu", g.BF16))
+    st = g.cache_stats()
+    with g.plan(M, N, K, "bf16", "relu") as p2:          # served from the cache
+        assert p2.config.astuple() == cfg
+    assert g.cache_stats()["hits"] == st["hits"] + 1
+    # a missing operand is an argument error
+    rc = g.lib().gemm_tune_on(M, N, K, g.BF16, 2, None, None, g._ptr(Bd), None, g._ptr(bd), 4, None, 0,
+                              ctypes.byref(ctypes.c_int32(0)), None)
+    assert rc == g.ERR_INVALID_ARG
+
+
+def test_uniform_and_normal_tuning_fills_both_run():
+    M, N, K = 256, 256, 512
+    try:
+        g.debug_set(6, 0)
+        a = g.tune(M, N, K, "bf16", "gelu", topk=4)
+    finally:
+        g.debug_set(6, 1)
+    b = g.tune(M, N, K, "bf16", "gelu", topk=4)
+    assert a.stats.n_measured >= 4 and b.stats.n_measured >= 4
