@@ -27,6 +27,14 @@ _LIB_PATH = os.path.join(_HERE, "_build", "liboracle_gemm.so")
 EPI_NONE, EPI_BIAS, EPI_BIAS_RELU, EPI_BIAS_GELU = 0, 1, 2, 3
 # Residual variants: the epilogue above, then + R ([M, N], the residual connection).
 EPI_BIAS_RESIDUAL, EPI_BIAS_RELU_RESIDUAL, EPI_BIAS_GELU_RESIDUAL = 4, 5, 6
+# Gated (GLU-style dual-output) epilogues over a fused gate+up weight:
+# C = act(A·B_gate + b_gate) ⊙ (A·B_up + b_up) with act ReLU, GELU or SiLU.
+EPI_BIAS_REGLU, EPI_BIAS_GEGLU, EPI_BIAS_SWIGLU = 7, 8, 9
+GLU_EPILOGUES = (EPI_BIAS_REGLU, EPI_BIAS_GEGLU, EPI_BIAS_SWIGLU)
+# Fused weight layout: B is [K, N] with N a multiple of 64; its columns come in
+# blocks of 32, gate and up alternating, so that output column o (of N/2) is
+# gate column 64·(o // 32) + o % 32 and up column 32 more.
+GLU_BLOCK = 32
 
 _lib = None
 
@@ -94,11 +102,51 @@ def default_threads() -> int:
         return os.cpu_count() or 1
 
 
+def glu_columns(N: int):
+    """(gate columns, up columns) of a fused [K, N] weight, in output-column order."""
+    if N % (2 * GLU_BLOCK):
+        raise ValueError("the fused gate+up width must be a multiple of 64")
+    o = np.arange(N // 2)
+    gate = 2 * GLU_BLOCK * (o // GLU_BLOCK) + o % GLU_BLOCK
+    return gate, gate + GLU_BLOCK
+
+
+def glu_act(x, epi: int):
+    """The gate's activation in fp64: ReLU, GELU (erf form) or SiLU x·σ(x)."""
+    x = np.asarray(x, dtype=np.float64)
+    if epi == EPI_BIAS_REGLU:
+        return np.maximum(x, 0.0)
+    if epi == EPI_BIAS_GEGLU:
+        from scipy.special import erf
+        return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))
+    if epi == EPI_BIAS_SWIGLU:
+        from scipy.special import expit
+        return x * expit(x)
+    raise ValueError("not a gated epilogue")
+
+
+def glu(A, B, bias, epi: int, threads: int | None = None, alpha: float = 1.0) -> np.ndarray:
+    """fp64 C [M, N/2] = act(alpha·A·B_gate + b_gate) ⊙ (alpha·A·B_up + b_up) for
+    the fused weight B [K, N] and bias [N] ("Tiling the hierarchy", fusion: the
+    elementwise chain after the product is fused onto it; "CuTile Autotuning":
+    dual-GEMM kernels such as Linear + GLU activation).  The two products come
+    from the plain oracle on the de-interleaved columns."""
+    Bf = _as_f32_input(B)
+    gate, up = glu_columns(Bf.shape[1])
+    bf = _as_f32_input(bias).reshape(-1)
+    g = gemm(A, Bf[:, gate], bf[gate], EPI_BIAS, threads, alpha=alpha)
+    u = gemm(A, Bf[:, up], bf[up], EPI_BIAS, threads, alpha=alpha)
+    return glu_act(g, epi) * u
+
+
 def gemm(A, B, bias=None, epi: int = EPI_NONE, threads: int | None = None, residual=None,
          alpha: float = 1.0) -> np.ndarray:
     """fp64 C = act(alpha·A·B + bias) for A [M,K], B [K,N], bias [N] (or None);
     for the residual epilogues (4, 5, 6) C = act(alpha·A·B + bias) + R with R
-    [M, N] (its values exactly, in fp64)."""
+    [M, N] (its values exactly, in fp64); for the gated epilogues (7, 8, 9) the
+    GLU-style product of glu() ([M, N/2])."""
+    if epi in GLU_EPILOGUES:
+        return glu(A, B, bias, epi, threads, alpha)
     if epi >= EPI_BIAS_RESIDUAL:
         if residual is None:
             raise ValueError("the residual epilogue needs R")
@@ -133,7 +181,15 @@ def gemm(A, B, bias=None, epi: int = EPI_NONE, threads: int | None = None, resid
 
 def gemm_entries(A, B, bias, epi: int, rows, cols, residual=None, alpha: float = 1.0) -> np.ndarray:
     """fp64 values of C at the listed (row, col) positions, one dot product each
-    (plus R at those positions for the residual epilogues)."""
+    (plus R at those positions for the residual epilogues; the gated
+    epilogues take output columns, of N/2)."""
+    if epi in GLU_EPILOGUES:
+        Bf = _as_f32_input(B)
+        gate, up = glu_columns(Bf.shape[1])
+        c = np.asarray(cols)
+        g = gemm_entries(A, Bf, bias, EPI_BIAS, rows, gate[c], alpha=alpha)
+        u = gemm_entries(A, Bf, bias, EPI_BIAS, rows, up[c], alpha=alpha)
+        return glu_act(g, epi) * u
     if epi >= EPI_BIAS_RESIDUAL:
         if residual is None:
             raise ValueError("the residual epilogue needs R")

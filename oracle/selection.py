@@ -226,6 +226,11 @@ def workshop_sweep(M, N, K, dev: WorkshopDevice = WorkshopDevice()):
 DT_BF16, DT_FP32, DT_FP8, DT_MXFP8 = 0, 1, 2, 3
 EPI_NONE, EPI_BIAS, EPI_RELU, EPI_GELU = 0, 1, 2, 3
 EPI_BIAS_RES, EPI_RELU_RES, EPI_GELU_RES = 4, 5, 6   # the same plus a residual R
+EPI_REGLU, EPI_GEGLU, EPI_SWIGLU = 7, 8, 9          # gated: act(gate) ⊙ up over a fused [K, N] weight, C [M, N/2]
+
+
+def is_glu(epi):
+    return epi in (EPI_REGLU, EPI_GEGLU, EPI_SWIGLU)
 
 R_OK, R_CTA_GROUP, R_UMMA_M, R_UMMA_N, R_LAYOUT, R_BK, R_STAGES, R_SCHEDULE, \
     R_SPLIT_K, R_ALIGN, R_TMEM, R_SMEM, R_REGS = range(13)
@@ -391,6 +396,10 @@ def gb300_check(M, N, K, dtype, epi, cfg: Config, dev: Device):
     if dtype == DT_MXFP8 and cfg.swap_ab == 0 and cfg.bn not in (128, 256):
         return R_LAYOUT
     if dtype == DT_MXFP8 and cfg.swap_ab == 1 and cfg.bn % 128 != 0 and M > cfg.bn:
+        return R_LAYOUT
+    # Gated epilogues: a tile holds whole 64-column gate+up block pairs of the
+    # fused weight and drains them in one pass (unswapped, no split-K).
+    if is_glu(epi) and (cfg.swap_ab != 0 or cfg.split_k != 1 or cfg.bn % 64 != 0 or N % 64 != 0):
         return R_LAYOUT
     if cfg.bk % span != 0 or not (1 <= cfg.bk // span <= 4):
         return R_BK
@@ -573,14 +582,16 @@ def gb300_model(M, N, K, dtype, epi, cfg: Config, dev: Device):
     panel = (tiles / wave_tiles) * K * (rows_w * cfg.bm + cols_w * cfg.bn) * per_k
     operand = in_bytes if in_bytes <= dev.l2_bytes / 2 else max(in_bytes, panel)
     eo = out_elt_bytes(dtype)
-    hbm = (operand + M * N * eo + (N * eo if epi != EPI_NONE else 0)
-           + (M * N * eo if epi >= EPI_BIAS_RES else 0))      # C, bias, residual R
+    c_cols = N // 2 if is_glu(epi) else N                     # a gated C is half the fused width
+    hbm = (operand + M * c_cols * eo + (N * eo if epi != EPI_NONE else 0)
+           + (M * N * eo if epi in (EPI_BIAS_RES, EPI_RELU_RES, EPI_GELU_RES) else 0))   # C, bias, residual R
     hbm_s = hbm / (dev.hbm_gbs * 1e9)
 
     latency_s = per_cta_units * slice_kb * dev.mem_latency_us * 1e-6 / cfg.stages
     main = max(mma_s, l2_s, hbm_s, latency_s)
 
-    per_clock = dev.epi_gelu_elems_per_clk if epi in (EPI_GELU, EPI_GELU_RES) else dev.epi_elems_per_clk
+    per_clock = dev.epi_gelu_elems_per_clk if epi in (EPI_GELU, EPI_GELU_RES, EPI_GEGLU, EPI_SWIGLU) \
+        else dev.epi_elems_per_clk
     rate = per_clock * clock
     elems = rows_cta * cfg.bn          # one CTA's share of a tile
     partial = elems * 4

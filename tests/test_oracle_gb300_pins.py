@@ -49,6 +49,7 @@ SHAPES = [
     (1000, 1000, 8192, sel.DT_FP8, sel.EPI_GELU),
     (2048, 1024, 4096, sel.DT_MXFP8, sel.EPI_BIAS),
     (300, 320, 1032, sel.DT_BF16, sel.EPI_BIAS),
+    (512, 28672, 4096, sel.DT_BF16, sel.EPI_GEGLU),      # gated: fused gate+up weight, C of half its width
 ]
 
 
@@ -174,11 +175,12 @@ def test_panel_law_catches_slices_counted_once(monkeypatch):
 
 def _compulsory_bytes(M, N, K, dt, epi):
     e, eo = ELT[dt], OUT[dt]
-    b = (M * K + K * N) * e + M * N * eo
+    gated = epi in (sel.EPI_REGLU, sel.EPI_GEGLU, sel.EPI_SWIGLU)
+    b = (M * K + K * N) * e + M * (N // 2 if gated else N) * eo      # A, B, C (a gated C: N/2 wide)
     if epi != sel.EPI_NONE:
-        b += N * eo
-    if epi >= sel.EPI_BIAS_RES:
-        b += M * N * eo
+        b += N * eo                                                  # bias (fused, N wide when gated)
+    if epi in (sel.EPI_BIAS_RES, sel.EPI_RELU_RES, sel.EPI_GELU_RES):
+        b += M * N * eo                                              # R
     return b
 
 
@@ -248,9 +250,17 @@ def test_hbm_pin_catches_a_dropped_output_term(monkeypatch):
 
 
 def test_hbm_pin_catches_a_dropped_c_term(monkeypatch):
-    _plant(monkeypatch, "gb300_model", "hbm = (operand + M * N * eo +", "hbm = (operand +")
+    _plant(monkeypatch, "gb300_model", "hbm = (operand + M * c_cols * eo +", "hbm = (operand +")
     with pytest.raises(AssertionError):
         test_hbm_bytes_are_compulsory_when_operands_fit_in_half_of_l2()
+
+
+def test_gated_shapes_only_generate_unswapped_unsplit_tiles_of_whole_block_pairs():
+    dev = sel.Device()
+    cands = sel.gb300_candidates(512, 28672, 4096, sel.DT_BF16, sel.EPI_GEGLU, dev)
+    assert cands and all(c.swap_ab == 0 and c.split_k == 1 and c.bn % 64 == 0 for c in cands)
+    assert sel.gb300_check(512, 28672 + 32, 4096, sel.DT_BF16, sel.EPI_GEGLU, sel.Config(128, 128, 64, 4),
+                           dev) == sel.R_LAYOUT
 
 
 def test_hbm_pin_catches_a_wrong_output_size(monkeypatch):
@@ -343,6 +353,7 @@ GEN_SHAPES = [
     (1000, 1000, 8192, sel.DT_FP8, sel.EPI_GELU),
     (16, 8192, 8192, sel.DT_MXFP8, sel.EPI_NONE),
     (300, 320, 1032, sel.DT_BF16, sel.EPI_BIAS),
+    (512, 28672, 4096, sel.DT_BF16, sel.EPI_SWIGLU),
 ]
 
 
