@@ -22,9 +22,11 @@ BF16, FP32_TF32, FP8_E4M3, MXFP8_E4M3 = 0, 1, 2, 3
 OPERAND_A, OPERAND_B = 1, 2            # gemm_plan_set_independent_operands
 EPI_NONE, EPI_BIAS, EPI_BIAS_RELU, EPI_BIAS_GELU = 0, 1, 2, 3
 EPI_BIAS_RESIDUAL, EPI_BIAS_RELU_RESIDUAL, EPI_BIAS_GELU_RESIDUAL = 4, 5, 6
+EPI_BIAS_REGLU, EPI_BIAS_GEGLU, EPI_BIAS_SWIGLU = 7, 8, 9
 EPILOGUES = {"none": EPI_NONE, "bias": EPI_BIAS, "relu": EPI_BIAS_RELU, "gelu": EPI_BIAS_GELU,
              "bias_residual": EPI_BIAS_RESIDUAL, "relu_residual": EPI_BIAS_RELU_RESIDUAL,
-             "gelu_residual": EPI_BIAS_GELU_RESIDUAL}
+             "gelu_residual": EPI_BIAS_GELU_RESIDUAL,
+             "reglu": EPI_BIAS_REGLU, "geglu": EPI_BIAS_GEGLU, "swiglu": EPI_BIAS_SWIGLU}
 DTYPES = {"bf16": BF16, "fp32": FP32_TF32, "tf32": FP32_TF32, "fp8": FP8_E4M3, "e4m3": FP8_E4M3,
           "mxfp8": MXFP8_E4M3}
 

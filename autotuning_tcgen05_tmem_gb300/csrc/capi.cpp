@@ -90,7 +90,7 @@ void gemm_device_params_workshop(gemm_device_params *out)
 
 static bool enums_ok(int dt, int epi)
 {
-    return dt >= GEMM_BF16 && dt <= GEMM_MXFP8_E4M3 && epi >= GEMM_EPI_NONE && epi <= GEMM_EPI_BIAS_GELU_RESIDUAL;
+    return dt >= GEMM_BF16 && dt <= GEMM_MXFP8_E4M3 && epi >= GEMM_EPI_NONE && epi <= GEMM_EPI_BIAS_SWIGLU;
 }
 
 int gemm_check_config(int64_t M, int64_t N, int64_t K, gemm_dtype dtype, gemm_epilogue epi, const gemm_config *cfg,

@@ -20,6 +20,10 @@ constexpr int kAuxSmem = 2048;     // barriers and flags (1 KB) + 1 KB of base-a
 constexpr int kMaxStages = 16;
 constexpr int kMaxSplitK = 16;
 
+// Gated epilogues: C [M, N/2] = act(gate) ⊙ up over a fused [K, N] weight.
+inline bool is_glu(int epi) { return epi >= GEMM_EPI_BIAS_REGLU && epi <= GEMM_EPI_BIAS_SWIGLU; }
+inline bool is_residual(int epi) { return epi >= GEMM_EPI_BIAS_RESIDUAL && epi <= GEMM_EPI_BIAS_GELU_RESIDUAL; }
+
 // FP8 operands, plain (one tensor scale) or block-scaled (MX).
 inline bool is_fp8(int dt) { return dt == GEMM_FP8_E4M3 || dt == GEMM_MXFP8_E4M3; }
 // Operand element size, and the size of C, bias and R (FP8 operands give bf16).

@@ -692,6 +692,27 @@ __device__ __forceinline__ void bias_act_rows(float (&v)[32], float lane_bias, i
     }
 }
 
+// Gated (GLU-style) epilogue of a 32-column output chunk: g holds the gate
+// chunk, u the up chunk of the fused accumulator (one row per lane); lane j
+// holds column j's biases.  g becomes act(alpha·g + b_gate) · (alpha·u + b_up),
+// act ReLU (epi 7), GELU (8) or SiLU x / (1 + e^-x) (9).
+__device__ __forceinline__ void glu_rows(float (&g)[32], const float (&u)[32], float gate_bias, float up_bias, int epi,
+                                         float alpha)
+{
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        float x = g[j], y = u[j];
+        if (alpha != 1.0f) {
+            x *= alpha;
+            y *= alpha;
+        }
+        x += __shfl_sync(0xFFFFFFFFu, gate_bias, j);
+        y += __shfl_sync(0xFFFFFFFFu, up_bias, j);
+        const float a = epi == 7 ? fmaxf(x, 0.0f) : epi == 8 ? gelu_erf(x) : __fdividef(x, 1.0f + __expf(-x));
+        g[j] = a * y;
+    }
+}
+
 __device__ __forceinline__ void bias_act_cols(float (&v)[16], float row_bias, int epi, float alpha)
 {
     if (alpha != 1.0f) {
@@ -1712,7 +1733,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             for (int32_t h = 0; h < halves; ++h) {
                 const int32_t r = h * 128 + q * 32 + lane;
-                if (!e_swap_ab) {
+                if (e_epi >= 7) {
+                    // Gated epilogue (unswapped, one slice, the planner's rule):
+                    // accumulator chunks 2p (gate) and 2p + 1 (up) of the fused
+                    // tile give output chunk p, columns c0/2 + 32p of C [M, N/2].
+#pragma unroll 1
+                    for (int pi = 0; pi < 2; ++pi) {
+                        const int32_t pp = cg + 2 * pi;
+                        if (2 * pp >= chunks) break;
+                        float g[32], u[32];
+                        if (nk > 0) {
+                            tmem_load_chunk<32>(tacc + (uint32_t)(h * e_bn + 2 * pp * 32), g);
+                            tmem_load_chunk<32>(tacc + (uint32_t)(h * e_bn + 2 * pp * 32 + 32), u);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) g[j] = u[j] = 0.0f;
+                        }
+                        const float gb = load_bias1<ODT>(e_bias, c0 + 64 * pp + lane, e_cols);
+                        const float ub = load_bias1<ODT>(e_bias, c0 + 64 * pp + 32 + lane, e_cols);
+                        glu_rows(g, u, gb, ub, e_epi, e_alpha);
+                        const int32_t n = (c0 >> 1) + pp * 32, y = r0 + h * 128 + q * 32;
+                        store_rows_chunk<ODT>(&tmC, ring, g, lane, n, y, n < (e_cols >> 1) && y < e_rows);
+                    }
+                } else if (!e_swap_ab) {
 #pragma unroll
                     for (int ci = 0; ci < 4; ++ci) {
                         const int32_t c = cg + 2 * ci;

@@ -214,7 +214,8 @@ const char *reason_text(int r)
     case GEMM_REASON_UMMA_N: return "bn must be a multiple of 16 in [16, 256]";
     case GEMM_REASON_LAYOUT:
         return "bn must be a multiple of 32 and of the 128-byte span when B is MN-major (a CTA pair: bn/2 a "
-               "multiple of the span; block-scaled FP8: bn 128 or 256, or swapped a multiple of 128 or >= M)";
+               "multiple of the span; block-scaled FP8: bn 128 or 256, or swapped a multiple of 128 or >= M; "
+               "gated epilogues: unswapped, split_k 1, bn and N multiples of 64)";
     case GEMM_REASON_BK: return "bk must be 1..4 spans of 128 bytes (block-scaled FP8: 128 or 256)";
     case GEMM_REASON_STAGES: return "stages must be in 2..16";
     case GEMM_REASON_SCHEDULE: return "raster must be 0/1 and group one of 1,2,4,8,16";
@@ -230,7 +231,6 @@ const char *reason_text(int r)
 int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_config &c,
                  const gemm_device_params &d)
 {
-    (void)epi;
     const int e = elt_bytes(dt);
     const int span = span_elems(dt);
     if (c.cta_group != 1 && c.cta_group != 2) return GEMM_REASON_CTA_GROUP;
@@ -248,6 +248,10 @@ int check_config(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_co
     // starts every tile on an atom: bn a multiple of 128, or all of M in one tile.
     if (dt == GEMM_MXFP8_E4M3 && c.swap_ab == 0 && c.bn != 128 && c.bn != 256) return GEMM_REASON_LAYOUT;
     if (dt == GEMM_MXFP8_E4M3 && c.swap_ab == 1 && c.bn % 128 != 0 && M > c.bn) return GEMM_REASON_LAYOUT;
+    // Gated epilogues: a tile holds whole 64-column gate+up block pairs of the
+    // fused weight and drains them in one pass (unswapped, no split-K).
+    if (is_glu(epi) && (c.swap_ab != 0 || c.split_k != 1 || c.bn % 64 != 0 || N % 64 != 0))
+        return GEMM_REASON_LAYOUT;
     if (c.bk % span != 0 || c.bk / span < 1 || c.bk / span > 4) return GEMM_REASON_BK;
     if (dt == GEMM_MXFP8_E4M3 && c.bk != 128 && c.bk != 256) return GEMM_REASON_BK;
     if (c.stages < 2 || c.stages > kMaxStages) return GEMM_REASON_STAGES;
@@ -438,10 +442,12 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
     const double panel = ((double)tiles / (double)wave_tiles) * (double)K *
                          ((double)rows_w * c.bm + (double)cols_w * c.bn) * (e + sf_per_k);
     const double operand = (in_bytes <= (double)d.l2_bytes / 2.0) ? in_bytes : std::max(in_bytes, panel);
-    // C, bias, and the residual R of the "+ R" epilogues.
+    // C (half the fused width for the gated epilogues), bias, and the residual
+    // R of the "+ R" epilogues.
     const double eo = out_elt_bytes(dt);
-    const double hbm = operand + (double)M * N * eo + (epi != GEMM_EPI_NONE ? (double)N * eo : 0.0) +
-                       (epi >= GEMM_EPI_BIAS_RESIDUAL ? (double)M * N * eo : 0.0);
+    const double c_cols = is_glu(epi) ? (double)(N / 2) : (double)N;
+    const double hbm = operand + (double)M * c_cols * eo + (epi != GEMM_EPI_NONE ? (double)N * eo : 0.0) +
+                       (is_residual(epi) ? (double)M * N * eo : 0.0);
     const double t_hbm = hbm / (d.hbm_gbs * 1e9);
 
     // Bytes in flight ("Tiling the hierarchy", double buffering): the ring
@@ -450,7 +456,8 @@ gemm_model_terms predict(int64_t M, int64_t N, int64_t K, int dt, int epi, const
     const double t_main = std::max(std::max(t_mma, t_l2), std::max(t_hbm, t_lat));
 
     // Epilogue and split-K exchange.
-    const bool gelu = epi == GEMM_EPI_BIAS_GELU || epi == GEMM_EPI_BIAS_GELU_RESIDUAL;
+    const bool gelu = epi == GEMM_EPI_BIAS_GELU || epi == GEMM_EPI_BIAS_GELU_RESIDUAL ||
+                      epi == GEMM_EPI_BIAS_GEGLU || epi == GEMM_EPI_BIAS_SWIGLU;
     const double rate = (gelu ? d.epi_gelu_elems_per_clk : d.epi_elems_per_clk) * clk;
     const double elems = (double)rows_cta * c.bn;   // one CTA's share of a tile
     const double part = elems * 4.0;

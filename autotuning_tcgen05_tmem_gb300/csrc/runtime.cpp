@@ -264,11 +264,13 @@ static int configure_smem_limit(int dt, int64_t bytes)
 
 static bool valid_enums(int dt, int epi)
 {
-    return dt >= GEMM_BF16 && dt <= GEMM_MXFP8_E4M3 && epi >= GEMM_EPI_NONE && epi <= GEMM_EPI_BIAS_GELU_RESIDUAL;
+    return dt >= GEMM_BF16 && dt <= GEMM_MXFP8_E4M3 && epi >= GEMM_EPI_NONE && epi <= GEMM_EPI_BIAS_SWIGLU;
 }
 
 // Residual epilogues are the bias / ReLU / GELU ones followed by "+ R".
-static bool has_residual(int epi) { return epi >= GEMM_EPI_BIAS_RESIDUAL; }
+static bool has_residual(int epi) { return is_residual(epi); }
+// The kernel's epilogue code: 0 none, 1 bias, 2 ReLU, 3 GELU, and the gated
+// 7 ReGLU, 8 GeGLU, 9 SwiGLU; the residual is a run argument.
 static int act_code(int epi) { return has_residual(epi) ? epi - 3 : epi; }
 
 static int check_extents(int64_t M, int64_t N, int64_t K)
@@ -524,8 +526,10 @@ static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const
     }
     if (!rc) {
         const int odt = is_fp8(dt) ? GEMM_BF16 : dt;   // C's type
+        // A gated epilogue writes C of half the fused width.
+        const uint64_t c_cols = is_glu(p->epi) ? (uint64_t)p->N / 2 : (uint64_t)p->N;
         if (!c.swap_ab)
-            rc = encode_2d(&d.mc, odt, C, p->N, p->M, 32, 32,
+            rc = encode_2d(&d.mc, odt, C, c_cols, p->M, 32, 32,
                            odt == GEMM_BF16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE);
         else
@@ -701,7 +705,7 @@ static int host_run_buffers(gemm_plan_t p)
     if (p->hC) return GEMM_OK;
     const size_t e = (size_t)elt_bytes(p->dt), eo = (size_t)out_elt_bytes(p->dt);
     const size_t nA = (size_t)p->M * p->K * e, nB = (size_t)p->K * p->N * e, nBias = (size_t)p->N * eo,
-                 nC = (size_t)p->M * p->N * eo;
+                 nC = (size_t)p->M * (is_glu(p->epi) ? p->N / 2 : p->N) * eo;
     cudaError_t err;
     if ((nA && (err = cudaMalloc(&p->hA, nA)) != cudaSuccess) || (nB && (err = cudaMalloc(&p->hB, nB)) != cudaSuccess) ||
         (err = cudaMalloc(&p->hBias, nBias)) != cudaSuccess || (err = cudaMalloc(&p->hC, nC)) != cudaSuccess)
@@ -715,7 +719,7 @@ static int host_run_enqueue(gemm_plan_t p, const void *A, const void *B, const v
 {
     const size_t e = (size_t)elt_bytes(p->dt), eo = (size_t)out_elt_bytes(p->dt);
     const size_t nA = (size_t)p->M * p->K * e, nB = (size_t)p->K * p->N * e, nBias = (size_t)p->N * eo,
-                 nC = (size_t)p->M * p->N * eo;
+                 nC = (size_t)p->M * (is_glu(p->epi) ? p->N / 2 : p->N) * eo;
     const bool has_bias = p->epi != GEMM_EPI_NONE;
     if (has_bias && !bias) return set_error(GEMM_ERR_INVALID_ARG, "bias is required by the epilogue");
     if (!C || (p->K > 0 && (!A || !B))) return set_error(GEMM_ERR_INVALID_ARG, "null A, B or C");

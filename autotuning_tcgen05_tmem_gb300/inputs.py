@@ -62,6 +62,19 @@ for _t in TOKENS:
 
 SWEEP = [WORKLOADS[f"bf16_gelu_{p}_t{t}"] for t in TOKENS for (p, _k, _n) in PROJECTIONS]
 
+# Gated projections over a fused gate+up weight (4096 -> 2 x 14336, C of
+# 14336 columns): GeGLU and SwiGLU at 512 and 2048 tokens.
+for _t in (512, 2048):
+    for _act in ("geglu", "swiglu"):
+        _name = f"bf16_{_act}_gate_up_t{_t}"
+        WORKLOADS[_name] = Workload(_name, _t, 28672, 4096, BF16, _act, "scaled_normal")
+GATED = ("reglu", "geglu", "swiglu")
+
+
+def out_cols(w) -> int:
+    """Columns of C: half the fused width for the gated epilogues."""
+    return w.N // 2 if w.epi in GATED else w.N
+
 # FP8 E4M3 operands (bf16 C) on the square, under-filled and decode shapes.
 WORKLOADS["fp8_relu_8192"] = Workload("fp8_relu_8192", 8192, 8192, 8192, FP8, "relu", "scaled_normal")
 WORKLOADS["fp8_gelu_1000x1000x8192"] = Workload("fp8_gelu_1000x1000x8192", 1000, 1000, 8192, FP8, "gelu",

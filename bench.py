@@ -111,16 +111,19 @@ def scale_bytes_of(w):
 
 
 def work_of(w):
+    """FLOPs and compulsory bytes of one GEMM (a gated C is half the fused width)."""
+    from autotuning_tcgen05_tmem_gb300 import inputs
     elt, eo = elt_sizes(w.dtype)
     flops = 2.0 * w.M * w.N * w.K
     bytes_ = (w.M * w.K + w.K * w.N) * elt + scale_bytes_of(w) + (w.N * eo if w.epi != "none" else 0) + \
-        w.M * w.N * eo
+        w.M * inputs.out_cols(w) * eo
     return flops, bytes_, elt
 
 
 def set_bytes_of(w):
+    from autotuning_tcgen05_tmem_gb300 import inputs
     elt, eo = elt_sizes(w.dtype)
-    return (w.M * w.K + w.K * w.N) * elt + scale_bytes_of(w) + (w.N + w.M * w.N) * eo
+    return (w.M * w.K + w.K * w.N) * elt + scale_bytes_of(w) + (w.N + w.M * inputs.out_cols(w)) * eo
 
 
 # ---------------------------------------------------------------------------
@@ -302,7 +305,7 @@ def make_sets(w, nsets, device):
     from autotuning_tcgen05_tmem_gb300 import inputs
     sets = []
     for s in range(nsets):
-        C = torch.empty(w.M, w.N, dtype=inputs.out_torch_dtype(w.dtype), device=device)
+        C = torch.empty(w.M, inputs.out_cols(w), dtype=inputs.out_torch_dtype(w.dtype), device=device)
         if w.dtype == "mxfp8":
             A, SA, B, SB, bias = inputs.make_mx_workload(w, seed=100 + 10 * s, device=device)
             sets.append((A, g.mx_pack_scales(SA, w.M, w.K, False), B, g.mx_pack_scales(SB, w.N, w.K, True),
@@ -520,7 +523,8 @@ def sweep(args):
     names = ["fp32_relu_256", "bf16_gelu_1000x1000x8192", "bf16_relu_8192", "bf16_decode_16x8192x28672"] + \
         [w.name for w in inputs.SWEEP] + ["fp8_gelu_1000x1000x8192", "fp8_relu_8192", "fp8_decode_16x8192x28672",
                                           "mxfp8_gelu_1000x1000x8192", "mxfp8_relu_8192",
-                                          "mxfp8_decode_16x8192x28672"]
+                                          "mxfp8_decode_16x8192x28672"] + \
+        [n for n in inputs.WORKLOADS if "_gate_up_t" in n and n.split("_")[1] in inputs.GATED]
     if args.workloads:
         names = [n for n in args.workloads.split(",")]
     clocks = ClockSampler(0)      # sampled through the sweep; each line summarises its tuned timing

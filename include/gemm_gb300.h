@@ -97,7 +97,20 @@ typedef enum {
      * connection's. */
     GEMM_EPI_BIAS_RESIDUAL = 4,       /* C = A·B + bias + R          */
     GEMM_EPI_BIAS_RELU_RESIDUAL = 5,  /* C = max(A·B + bias, 0) + R  */
-    GEMM_EPI_BIAS_GELU_RESIDUAL = 6   /* C = gelu(A·B + bias) + R    */
+    GEMM_EPI_BIAS_GELU_RESIDUAL = 6,  /* C = gelu(A·B + bias) + R    */
+    /* Gated (GLU-style dual output) variants over a fused gate+up weight: B is
+     * [K, N] with N a multiple of 64 whose columns come in blocks of 32, gate
+     * and up alternating, and bias [N] likewise; C is [M, N/2] with
+     *   C[m, o] = act(G[m, o]) · U[m, o],  G = A·B[:, gate(o)] + bias[gate(o)],
+     *   U = A·B[:, up(o)] + bias[up(o)],  gate(o) = 64·(o/32) + o%32,  up(o) = gate(o) + 32.
+     * One pass over the fused weight, the activation and the product fused
+     * into the epilogue ("Tiling the hierarchy", fusion: an elementwise chain
+     * fused onto the product that feeds it; "CuTile Autotuning": fused
+     * dual-GEMM kernels, Linear + GLU activation).  Unswapped, single-slice
+     * configurations only (swap_ab 0, split_k 1), bn a multiple of 64. */
+    GEMM_EPI_BIAS_REGLU = 7,          /* act = ReLU                  */
+    GEMM_EPI_BIAS_GEGLU = 8,          /* act = GELU (erf form)       */
+    GEMM_EPI_BIAS_SWIGLU = 9          /* act = SiLU, x / (1 + e^-x)  */
 } gemm_epilogue;
 
 /*

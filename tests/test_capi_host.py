@@ -39,7 +39,10 @@ SHAPES = [(256, 256, 256, 1, 2), (1000, 1000, 8192, 0, 3), (8192, 8192, 8192, 0,
           (512, 1024, 4096, 2, 6), (100, 104, 48, 2, 1),
           # block-scaled FP8 (MX): no swap, no pairs, bn 128/256, bk 128/256, scale slots in TMEM
           (1000, 1000, 8192, 3, 3), (8192, 8192, 8192, 3, 2), (16, 28672, 8192, 3, 0), (300, 200, 128, 3, 2),
-          (512, 1024, 4096, 3, 6), (100, 104, 48, 3, 1)]
+          (512, 1024, 4096, 3, 6), (100, 104, 48, 3, 1),
+          # gated epilogues (ReGLU, GeGLU, SwiGLU) over a fused gate+up weight
+          (512, 28672, 4096, 0, 8), (16, 28672, 4096, 0, 9), (1000, 1024, 8192, 2, 7), (256, 256, 256, 1, 8),
+          (300, 192, 72, 0, 7)]
 
 
 def test_library_exports_every_declared_symbol():
@@ -92,7 +95,9 @@ def test_check_config_equals_oracle_on_a_grid():
                           (100, 104, 48, 3)]:
         for t in sample:
             c = g.make_config(*t)
-            assert g.check_config(M, N, K, dt, 2, c, d) == sel.gb300_check(M, N, K, dt, 2, sel.Config(*t), od), (M, N, K, dt, t)
+            for epi in (2, 8):
+                assert g.check_config(M, N, K, dt, epi, c, d) == sel.gb300_check(M, N, K, dt, epi, sel.Config(*t), od), \
+                    (M, N, K, dt, epi, t)
 
 
 def test_check_config_register_rule():
