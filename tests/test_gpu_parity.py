@@ -236,10 +236,12 @@ def test_run_host_many_matches_run(cfg):
 
 def test_gelu_epilogue_pointwise_accuracy():
     """C = gelu(x·1 + 0) over a sweep of x.  The device's erf (Abramowitz &
-    Stegun 7.1.26) has absolute error <= 1.5e-7, so |GELU_dev - GELU| <=
-    0.5·|x|·1.5e-7 before the bf16 rounding; the bf16 result may therefore
-    differ from the exactly rounded one by at most one rounding step plus that
-    bound (which is what matters far in the negative tail, where GELU ~ 0)."""
+    Stegun 7.1.28) has absolute error <= 3e-7, and its fp32 evaluation (a
+    sixteenth power) adds at most about 1.2e-5 of erfc <= 1, so |GELU_dev - GELU|
+    <= 0.5·|x|·(3e-7 + 1.2e-5) before the bf16 rounding; the bf16 result may
+    therefore differ from the exactly rounded one by at most one rounding step
+    plus that bound (which is what matters far in the negative tail, where
+    GELU ~ 0)."""
     M, N, K = 512, 64, 64
     xs = torch.linspace(-8, 8, M, dtype=torch.float64)
     A = torch.zeros(M, K, dtype=torch.float32)
@@ -255,7 +257,7 @@ def test_gelu_epilogue_pointwise_accuracy():
     got = out.double().numpy()
     x = A.double().numpy()[:, :1]
     step = np.abs(exact) * 2.0 ** -8 + 1e-38           # one bf16 rounding step
-    allowed = step + 0.5 * np.abs(x) * 1.5e-7 * 1.01
+    allowed = step + 0.5 * np.abs(x) * (3e-7 + 1.2e-5) * 1.01
     assert np.all(np.abs(got - exact) <= allowed), np.argwhere(np.abs(got - exact) > allowed)[:5]
     want = oracle_rounded_bits(A, B, bias, "gelu", g.BF16)
     core = (x[:, 0] >= -1.0)                         # 1 + erf >= 0.31: the bound is relative here
