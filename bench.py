@@ -420,6 +420,21 @@ def time_gemm(plan, sets, steps, warmup):
     return e0.elapsed_time(e1) / 1e3 / steps / len(sets)
 
 
+def captured_traffic(name, cfg):
+    """DRAM bytes of one launch of this workload's kernel in this configuration,
+    from the committed ncu summaries (profiles/traffic.json), or None when no
+    capture of the current build exists for it."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        ents = json.load(f).get(name) or []
+    for ent in ents if isinstance(ents, list) else [ents]:
+        if ent.get("source_digest") == _build._sources_digest() and ent.get("config") == list(cfg):
+            return ent.get("dram_bytes_per_launch")
+    return None
+
+
 def power_capped(clocks_summary) -> bool:
     """Whether the GPU ran under its power cap during a timed region: the
     sustained tensor peak is then the fair denominator, else the burst one."""
@@ -489,6 +504,7 @@ def measure_workload(w, devp, peaks, peak_src, operands="none", clocks=None, tar
     else:
         roof = {"bound": "hbm", "achieved": cbytes / t_tuned / 1e9, "peak": bw, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = captured_traffic(w.name, cfg)
     roof["peak_source"] = (f"{peak_src} bf16 {'sustained' if sustained else 'burst'} x {peak_ratio(w.dtype)}"
                            if tensor_bound else f"{peak_src} HBM")
     out = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype, "epilogue": w.epi,
@@ -697,15 +713,7 @@ def main():
     bw = peaks.get("hbm_gbs", 6800.0)
     t_compute = flops / (tpeak * 1e12)
     t_memory = cbytes / (bw * 1e9)
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        with open(tr_path) as f:
-            tr = json.load(f)
-        ents = tr.get(w.name) or []
-        for ent in ents if isinstance(ents, list) else [ents]:
-            if ent.get("source_digest") == _build._sources_digest() and ent.get("config") == list(cfg.astuple()):
-                traffic = ent.get("dram_bytes_per_launch")
+    traffic = captured_traffic(w.name, cfg.astuple())
     if t_compute >= t_memory:
         roof = {"bound": "tensor", "achieved": flops / gemm_s / 1e12, "peak": tpeak, "unit": "TFLOP/s"}
     else:
@@ -721,6 +729,8 @@ def main():
            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "epilogue": w.epi,
                       "dtype": w.dtype, "tile_config": cfg.asdict(),
+                      "splitk_route": g.SPLITK_ROUTES.get(plan.launch_info.splitk_route,
+                                                          str(plan.launch_info.splitk_route)),
                       "step": f"{nsets} GEMMs, one per rotating input set",
                       "l2": f"inputs rotate over {nsets} sets ({nsets * set_bytes / 1e6:.0f} MB > 2 x L2 "
                             f"{devp.l2_bytes / 1e6:.0f} MB)" if nsets * set_bytes > 2 * devp.l2_bytes
