@@ -424,6 +424,7 @@ def captured_traffic(name, cfg):
     """DRAM bytes of one launch of this workload's kernel in this configuration,
     from the committed ncu summaries (profiles/traffic.json), or None when no
     capture of the current build exists for it."""
+    from autotuning_tcgen05_tmem_gb300 import _build
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None

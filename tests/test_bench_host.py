@@ -101,3 +101,22 @@ def test_clock_samples_are_placed_by_their_own_timestamps():
                                           "Active" if mhz < 2000 else "Not Active"]))
     s = c.summary_between(base.timestamp() + 0.05, base.timestamp() + 0.25)
     assert s["samples_in_timed_region"] == 2 and s["sm_mhz"] == 1500 and s["reasons"] == ["sw_power_cap"]
+
+
+def test_captured_traffic_matches_workload_config_and_build():
+    """The roofline's traffic comes from the committed ncu summaries only for the
+    same workload, configuration and source digest; anything else reads None."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from autotuning_tcgen05_tmem_gb300 import _build
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        table = json.load(f)
+    name, ents = next(iter(table.items()))
+    ent = ents[0] if isinstance(ents, list) else ents
+    got = bench.captured_traffic(name, ent["config"])
+    if ent["source_digest"] == _build._sources_digest():
+        assert got == ent["dram_bytes_per_launch"]
+    else:
+        assert got is None
+    assert bench.captured_traffic(name, [1] * 9) is None
+    assert bench.captured_traffic("no_such_workload", ent["config"]) is None
