@@ -109,7 +109,8 @@ class TuneRow(ctypes.Structure):
 
 class LaunchInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("grid", "block", "smem_bytes", "cluster", "splitk_route", "b_transposed", "units", "tiles")]
+                ("grid", "block", "smem_bytes", "cluster", "splitk_route", "b_transposed", "units", "tiles",
+                 "span_copies")]
 
     def asdict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -37,6 +37,7 @@ extern std::atomic<int32_t> g_split_route;
 extern std::atomic<int32_t> g_check;
 extern std::atomic<int64_t> g_share_poll;
 extern std::atomic<int32_t> g_tune_fill;
+extern std::atomic<int32_t> g_span3d;
 int query_params(gemm_device_params *d);
 int model_params_load(const char *path, gemm_device_params *out);
 int plan_tuned(int64_t M, int64_t N, int64_t K, int dt, int epi, gemm_plan_t *out, const TuneInputs *user);
@@ -396,6 +397,11 @@ int gemm_debug_set(int32_t what, int64_t value)
     if (what == 6) {
         if (value < 0 || value > 1) return set_error(GEMM_ERR_INVALID_ARG, "tuning fill must be 0 or 1");
         g_tune_fill.store((int32_t)value);
+        return GEMM_OK;
+    }
+    if (what == 7) {
+        if (value < 0 || value > 1) return set_error(GEMM_ERR_INVALID_ARG, "span copies must be 0 or 1");
+        g_span3d.store((int32_t)value);
         return GEMM_OK;
     }
     return set_error(GEMM_ERR_INVALID_ARG, "unknown debug control %d", what);

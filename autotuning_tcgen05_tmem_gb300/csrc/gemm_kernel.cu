@@ -215,6 +215,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *m, uint32_t cluster_bar,
+                                                 int32_t x, int32_t y, int32_t z)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(cluster_bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 // Load into this CTA's shared memory, completing bytes on the barrier of the
 // pair's leader (a shared::cluster address): the second CTA of a CTA pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *m, uint32_t cluster_bar,
@@ -1086,6 +1106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sb0 = base + p.off_b;
         const int32_t a_loads = A_MN ? cta_rows / SPAN : bk / SPAN;
         const int32_t b_loads = B_MN ? cta_bcols / SPAN : bk / SPAN;
+        const bool a3d = p.a_span3d != 0, b3d = p.b_span3d != 0;
         // One stage's copies, split by operand: bit 0 of `what` issues MMA-A's
         // panel (with its MX scale atoms), bit 1 MMA-B's; `arm` first posts the
         // stage's full byte count on its barrier.
@@ -1100,37 +1121,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (arm) mbar_arrive_expect_tx(fb, tx);
                 // K-major operand: boxes of [rows x one span of K], one per span;
                 // MN-major operand: boxes of [bk x one span of MN], one per span.
-                if (what & 1u)
-                    for (int32_t j = 0; j < a_loads; ++j) {
-                        if constexpr (A_MN) tma_load_2d(sa + (uint32_t)(j * bk * 128), &tmA, fb, ra + j * SPAN, k0);
-                        else tma_load_2d(sa + (uint32_t)(j * cta_rows * 128), &tmA, fb, k0 + j * SPAN, ra);
+                // A 3-D view takes all of the stage's spans in one copy; the
+                // boxes land span after span, as the per-span copies would.
+                if (what & 1u) {
+                    if (a3d) {
+                        if constexpr (A_MN) tma_load_3d(sa, &tmA, fb, 0, k0, ra / SPAN);
+                        else tma_load_3d(sa, &tmA, fb, 0, ra, k0 / SPAN);
+                    } else {
+                        for (int32_t j = 0; j < a_loads; ++j) {
+                            if constexpr (A_MN) tma_load_2d(sa + (uint32_t)(j * bk * 128), &tmA, fb, ra + j * SPAN, k0);
+                            else tma_load_2d(sa + (uint32_t)(j * cta_rows * 128), &tmA, fb, k0 + j * SPAN, ra);
+                        }
                     }
-                if (what & 2u)
-                    for (int32_t j = 0; j < b_loads; ++j) {
-                        if constexpr (B_MN) tma_load_2d(sb + (uint32_t)(j * bk * 128), &tmB, fb, rb + j * SPAN, k0);
-                        else tma_load_2d(sb + (uint32_t)(j * cta_bcols * 128), &tmB, fb, k0 + j * SPAN, rb);
+                }
+                if (what & 2u) {
+                    if (b3d) {
+                        if constexpr (B_MN) tma_load_3d(sb, &tmB, fb, 0, k0, rb / SPAN);
+                        else tma_load_3d(sb, &tmB, fb, 0, rb, k0 / SPAN);
+                    } else {
+                        for (int32_t j = 0; j < b_loads; ++j) {
+                            if constexpr (B_MN) tma_load_2d(sb + (uint32_t)(j * bk * 128), &tmB, fb, rb + j * SPAN, k0);
+                            else tma_load_2d(sb + (uint32_t)(j * cta_bcols * 128), &tmB, fb, k0 + j * SPAN, rb);
+                        }
                     }
+                }
                 if constexpr (DT == 3) {
-                    // The stage's scale atoms: for each 128 rows of MMA-A,
-                    // then each 128 columns of MMA-B (one atom when bn < 128:
-                    // such a tile starts on an atom), its bk/128 consecutive
-                    // K atoms, one tensor copy each (the packed array seen as
-                    // rows of one 512-byte atom, 128 words wide).  Swapped,
+                    // The stage's scale atoms, one tensor copy per operand (the
+                    // packed array seen as [row atoms][K atoms][128 words]):
+                    // for the tile's 128-row groups of MMA-A, then its 128-column
+                    // groups of MMA-B (one atom when bn < 128: such a tile
+                    // starts on an atom), their bk/128 consecutive K atoms,
+                    // landing as [group][K atom] atoms of 512 bytes.  Swapped,
                     // MMA-A is B (rows along N) and MMA-B is A.
                     const uint32_t ka = (uint32_t)bk / 128u, run = ka * 512u;
                     const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
                     const int32_t k_atom = kb * (int32_t)ka;
                     const CUtensorMap *sm_a = A_MN || p.swap_ab ? &tmSB : &tmSA;
                     const CUtensorMap *sm_b = A_MN || p.swap_ab ? &tmSA : &tmSB;
-                    const int32_t na = pair ? 1 : bm / 128, nb = max(1, bn / 128);
-                    if (what & 1u)
-                        for (int32_t h = 0; h < na; ++h)
-                            tma_load_2d(sf + (uint32_t)h * run, sm_a, fb, 0,
-                                        (w.tile_m * (bm / 128) + h) * p.sf_kt + k_atom);
-                    if (what & 2u)
-                        for (int32_t j = 0; j < nb; ++j)
-                            tma_load_2d(sf + (uint32_t)(na + j) * run, sm_b, fb, 0,
-                                        (w.tile_n * bn / 128 + j) * p.sf_kt + k_atom);
+                    const int32_t na = pair ? 1 : bm / 128;
+                    if (what & 1u) tma_load_3d(sf, sm_a, fb, 0, k_atom, w.tile_m * (bm / 128));
+                    if (what & 2u) tma_load_3d(sf + (uint32_t)na * run, sm_b, fb, 0, k_atom, w.tile_n * bn / 128);
                 }
             } else if (leader) {
                 if constexpr (pair) {
@@ -1138,32 +1168,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // memory and complete on the leader's barrier, where the MMAs wait.
                     const uint32_t fbr = mapa_u32(fb, lead_rank);
                     if (arm) mbar_arrive_expect_tx_remote(fbr, tx);
-                    if (what & 1u)
-                        for (int32_t j = 0; j < a_loads; ++j) {
-                            if constexpr (A_MN)
-                                tma_load_2d_pair(sa + (uint32_t)(j * bk * 128), &tmA, fbr, ra + j * SPAN, k0);
-                            else
-                                tma_load_2d_pair(sa + (uint32_t)(j * cta_rows * 128), &tmA, fbr, k0 + j * SPAN, ra);
+                    if (what & 1u) {
+                        if (a3d) {
+                            if constexpr (A_MN) tma_load_3d_pair(sa, &tmA, fbr, 0, k0, ra / SPAN);
+                            else tma_load_3d_pair(sa, &tmA, fbr, 0, ra, k0 / SPAN);
+                        } else {
+                            for (int32_t j = 0; j < a_loads; ++j) {
+                                if constexpr (A_MN)
+                                    tma_load_2d_pair(sa + (uint32_t)(j * bk * 128), &tmA, fbr, ra + j * SPAN, k0);
+                                else
+                                    tma_load_2d_pair(sa + (uint32_t)(j * cta_rows * 128), &tmA, fbr, k0 + j * SPAN,
+                                                     ra);
+                            }
                         }
-                    if (what & 2u)
-                        for (int32_t j = 0; j < b_loads; ++j) {
-                            if constexpr (B_MN)
-                                tma_load_2d_pair(sb + (uint32_t)(j * bk * 128), &tmB, fbr, rb + j * SPAN, k0);
-                            else
-                                tma_load_2d_pair(sb + (uint32_t)(j * cta_bcols * 128), &tmB, fbr, k0 + j * SPAN,
-                                                 rb);
+                    }
+                    if (what & 2u) {
+                        if (b3d) {
+                            if constexpr (B_MN) tma_load_3d_pair(sb, &tmB, fbr, 0, k0, rb / SPAN);
+                            else tma_load_3d_pair(sb, &tmB, fbr, 0, rb, k0 / SPAN);
+                        } else {
+                            for (int32_t j = 0; j < b_loads; ++j) {
+                                if constexpr (B_MN)
+                                    tma_load_2d_pair(sb + (uint32_t)(j * bk * 128), &tmB, fbr, rb + j * SPAN, k0);
+                                else
+                                    tma_load_2d_pair(sb + (uint32_t)(j * cta_bcols * 128), &tmB, fbr,
+                                                     k0 + j * SPAN, rb);
+                            }
                         }
+                    }
                     if constexpr (DT == 3) {
                         // MX: this CTA's 128 rows of A scales and all of the
                         // tile's B scales (the pair MMA reads each CTA's own).
                         const uint32_t ka = (uint32_t)bk / 128u, run = ka * 512u;
                         const uint32_t sf = base + p.off_sf + stage * p.sf_stage_bytes;
                         const int32_t k_atom = kb * (int32_t)ka;
-                        if (what & 1u) tma_load_2d_pair(sf, &tmSA, fbr, 0, (w.tile_m * 2 + 1) * p.sf_kt + k_atom);
-                        if (what & 2u)
-                            for (int32_t j = 0; j < bn / 128; ++j)
-                                tma_load_2d_pair(sf + (uint32_t)(1 + j) * run, &tmSB, fbr, 0,
-                                                 (w.tile_n * bn / 128 + j) * p.sf_kt + k_atom);
+                        if (what & 1u) tma_load_3d_pair(sf, &tmSA, fbr, 0, k_atom, w.tile_m * 2 + 1);
+                        if (what & 2u) tma_load_3d_pair(sf + run, &tmSB, fbr, 0, k_atom, w.tile_n * bn / 128);
                     }
                 }
             }

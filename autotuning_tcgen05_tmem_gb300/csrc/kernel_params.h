@@ -28,6 +28,9 @@ struct KernelParams {
     int32_t tiles_m, tiles_n, num_kb, num_units;
     int32_t swap_ab, epi;
     int32_t a_mn_major, b_mn_major;   // operand majorness in shared memory
+    int32_t a_span3d, b_span3d;       // MMA-A / MMA-B: the tensor map views the operand as
+                                       // [spans][rows][one 128-byte span], and one copy takes
+                                       // all of a stage's spans (0: one copy per span)
     uint32_t idesc;                    // tcgen05 instruction descriptor
     uint32_t a_stage_bytes, b_stage_bytes, tx_bytes;
     uint32_t a_lbo, b_lbo;             // leading-byte offsets of MN-major operands

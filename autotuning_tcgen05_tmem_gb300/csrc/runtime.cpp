@@ -50,6 +50,9 @@ std::atomic<int64_t> g_share_poll{50000};
 // standard deviation 1/sqrt(K) (the default: the workloads' N(0,1)/sqrt(K)
 // family), 0 = uniform of the same standard deviation.
 std::atomic<int32_t> g_tune_fill{1};
+// Operands read with one tensor copy per stage where the layout allows (1), or
+// one copy per 128-byte span (0), in plans made from now on.
+std::atomic<int32_t> g_span3d{1};
 // Checked runs (GEMM_CHECK set to anything but 0 in the environment, or
 // gemm_debug_set(4, 1)): every run synchronises its stream and reports a
 // device-side timeout itself instead of leaving it to gemm_plan_status.
@@ -97,6 +100,31 @@ static int encode_2d(CUtensorMap *m, int dt, const void *ptr, uint64_t inner, ui
     if (r != CUDA_SUCCESS)
         return set_error(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] box [%u x %u]", (int)r,
                          (unsigned long long)outer, (unsigned long long)inner, box_outer, box_inner);
+    return GEMM_OK;
+}
+
+// The same [outer][inner] matrix seen in 3-D as [inner / span][outer][span]
+// (inner a whole number of spans): a box of [n_spans][box_outer][span] takes a
+// stage's consecutive spans in one copy and lands them span after span, as
+// n_spans two-dimensional copies of [box_outer][span] would.
+static int encode_spans(CUtensorMap *m, int dt, const void *ptr, uint64_t inner, uint64_t outer, uint32_t span,
+                        uint32_t box_outer, uint32_t n_spans)
+{
+    if (!encoder_ready()) return set_error(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const uint64_t e = (uint64_t)elt_bytes(dt);
+    const cuuint64_t dims[3] = {span, outer, inner / span};
+    const cuuint64_t strides[2] = {inner * e, span * e};
+    const cuuint32_t box[3] = {span, box_outer, n_spans};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType t = dt == GEMM_BF16       ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                  : is_fp8(dt)          ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUresult r = g_encode(m, t, 3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] in spans, box [%u x %u x %u]",
+                         (int)r, (unsigned long long)outer, (unsigned long long)inner, n_spans, box_outer, span);
     return GEMM_OK;
 }
 
@@ -322,6 +350,19 @@ int make_plan(int64_t M, int64_t N, int64_t K, int dt, int epi, const gemm_confi
     // The kernel's bias/activation code; the residual is a run argument.
     p->kp = kernel_params_of(M, N, K, dt, act_code(epi), cfg, p->b_kmajor);
     KernelParams &k = p->kp;
+    // One tensor copy per operand and stage where a stage spans several
+    // 128-byte spans of an operand whose contiguous extent is a whole number of
+    // spans (so that the 3-D view stays inside the matrix): the TMA unit takes
+    // about as long over a copy whatever its size.  MMA-A's contiguous extent is
+    // K (K-major) or N (B in place, swapped); MMA-B's K or N likewise.
+    if (g_span3d.load()) {
+        const int span = span_elems(dt);
+        const int cta_rows = k.pair ? 128 : cfg.bm, cta_bcols = k.pair ? cfg.bn / 2 : cfg.bn;
+        const int a_loads = k.a_mn_major ? cta_rows / span : cfg.bk / span;
+        const int b_loads = k.b_mn_major ? cta_bcols / span : cfg.bk / span;
+        k.a_span3d = a_loads > 1 && (k.a_mn_major ? N : K) % span == 0 ? 1 : 0;
+        k.b_span3d = b_loads > 1 && (k.b_mn_major ? N : K) % span == 0 ? 1 : 0;
+    }
     p->tiles = (int64_t)k.tiles_m * k.tiles_n;
     p->grid = (int)std::min<int64_t>(k.num_units, dev.sm_count);
     // One wave of split-K units: the slices of a tile finalise it share by
@@ -467,21 +508,25 @@ void destroy_plan(gemm_plan_t p)
     delete p;
 }
 
-// A packed MX scale array as a tensor of 32-bit words: one row per 512-byte
-// atom (row atoms x K atoms rows, 128 words each), box [bk/128 atoms x 128].
-static int encode_scales(CUtensorMap *m, const void *ptr, int64_t rows, uint32_t box_rows)
+// A packed MX scale array as a 3-D tensor of 32-bit words: [row atoms][K atoms]
+// [128 words] (one 512-byte atom per 128 words).  The box takes a stage's whole
+// run for one operand in a single copy: bk/128 K atoms of each of the tile's
+// `box_atoms` row atoms (each copy costs the TMA unit about as much as a data
+// stage's, whatever its size, so one copy per operand and stage, not per atom).
+static int encode_scales(CUtensorMap *m, const void *ptr, int64_t row_atoms, int64_t k_atoms, uint32_t ka,
+                         uint32_t box_atoms)
 {
     if (!encoder_ready()) return set_error(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-    const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {512};
-    const cuuint32_t box[2] = {128, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+    const cuuint64_t dims[3] = {128, (cuuint64_t)k_atoms, (cuuint64_t)row_atoms};
+    const cuuint64_t strides[2] = {512, (cuuint64_t)k_atoms * 512};
+    const cuuint32_t box[3] = {128, ka, box_atoms};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
-        return set_error(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for the MX scales [%lld atoms]", (int)r,
-                         (long long)rows);
+        return set_error(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for the MX scales [%lld x %lld atoms]",
+                         (int)r, (long long)row_atoms, (long long)k_atoms);
     return GEMM_OK;
 }
 
@@ -513,12 +558,24 @@ static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const
         const uint32_t b_rows = c.swap_ab ? c.bm : (pair ? (uint32_t)c.bn / 2 : (uint32_t)c.bn);
         CUtensorMap *am = c.swap_ab ? &d.mb : &d.ma;
         CUtensorMap *bm = c.swap_ab ? &d.ma : &d.mb;
-        rc = encode_2d(am, dt, A, p->K, p->M, span, a_rows, CU_TENSOR_MAP_SWIZZLE_128B,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        // Whether each matrix is read in spans (one copy per stage): A is
+        // MMA-A unless swapped, B the other one.
+        const bool a_spans = (c.swap_ab ? p->kp.b_span3d : p->kp.a_span3d) != 0;
+        const bool b_spans = (c.swap_ab ? p->kp.a_span3d : p->kp.b_span3d) != 0;
+        const uint32_t k_spans = (uint32_t)c.bk / (uint32_t)span;
+        if (a_spans)
+            rc = encode_spans(am, dt, A, p->K, p->M, span, a_rows, k_spans);
+        else
+            rc = encode_2d(am, dt, A, p->K, p->M, span, a_rows, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
         if (!rc) {
-            if (p->b_kmajor)
+            if (p->b_kmajor && b_spans)
+                rc = encode_spans(bm, dt, p->bt, p->K, p->N, span, b_rows, k_spans);
+            else if (p->b_kmajor)
                 rc = encode_2d(bm, dt, p->bt, p->K, p->N, span, b_rows, CU_TENSOR_MAP_SWIZZLE_128B,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+            else if (b_spans)
+                rc = encode_spans(bm, dt, B, p->N, p->K, span, c.bk, b_rows / (uint32_t)span);
             else
                 rc = encode_2d(bm, dt, B, p->N, p->K, span, c.bk, CU_TENSOR_MAP_SWIZZLE_128B,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
@@ -539,9 +596,14 @@ static int get_descs(gemm_plan_t p, const void *A, const void *B, void *C, const
     memset(&d.msa, 0, sizeof(d.msa));
     memset(&d.msb, 0, sizeof(d.msb));
     if (!rc && dt == GEMM_MXFP8_E4M3 && p->K > 0) {
+        // Row atoms per copy: the MMA-A side of a tile (one per CTA of a pair,
+        // else bm/128) and the MMA-B side (bn/128, at least one); swapped, B's
+        // scales feed MMA-A and A's MMA-B.
         const uint32_t ka = (uint32_t)c.bk / 128u;
-        rc = encode_scales(&d.msa, SA, mx_row_atoms(p->M) * mx_k_atoms(p->K), ka);
-        if (!rc) rc = encode_scales(&d.msb, SB, mx_row_atoms(p->N) * mx_k_atoms(p->K), ka);
+        const uint32_t na = c.cta_group == 2 ? 1u : (uint32_t)c.bm / 128u;
+        const uint32_t nb = (uint32_t)std::max(1, c.bn / 128);
+        rc = encode_scales(&d.msa, SA, mx_row_atoms(p->M), mx_k_atoms(p->K), ka, c.swap_ab ? nb : na);
+        if (!rc) rc = encode_scales(&d.msb, SB, mx_row_atoms(p->N), mx_k_atoms(p->K), ka, c.swap_ab ? na : nb);
     }
     if (rc) return rc;
     d.a = A;
@@ -665,6 +727,7 @@ int plan_launch_info(gemm_plan_t p, gemm_launch_info *out)
     out->b_transposed = p->b_kmajor ? 1 : 0;
     out->units = k.num_units;
     out->tiles = (int32_t)p->tiles;
+    out->span_copies = (k.a_span3d ? 1 : 0) | (k.b_span3d ? 2 : 0);
     return GEMM_OK;
 }
 

@@ -389,6 +389,8 @@ typedef struct {
     int32_t b_transposed;  /* 1: B is first copied to a K-major layout (one extra kernel) */
     int32_t units;         /* work units: tiles x split_k */
     int32_t tiles;         /* output tiles */
+    int32_t span_copies;   /* bit 0: MMA-A, bit 1: MMA-B is copied with one tensor copy per
+                              stage over all its 128-byte spans (see gemm_debug_set, what = 7) */
 } gemm_launch_info;
 
 int gemm_plan_launch_info(gemm_plan_t plan, gemm_launch_info *out);
@@ -556,8 +558,12 @@ int gemm_tune_batch(const int64_t *mnk, int32_t n, gemm_dtype dtype, gemm_epilog
  * slices before handing its share over (default 50000, about 25 us; 0 = hand
  * over at once, which tests use to drive that path); what = 6: the value
  * distribution of the tuner's synthetic operands (1 = normal, the default; 0 =
- * uniform of the same standard deviation).  Affects launches (what 0, 1, 4, 5),
- * plans (what 2, 3) or tunings (what 6) made after the call, from any thread. */
+ * uniform of the same standard deviation); what = 7: how the producer copies
+ * an operand's stage (1 = the default: one tensor copy for all of the stage's
+ * 128-byte spans where the operand's contiguous extent is a whole number of
+ * spans; 0 = one copy per span; the results are the same bits either way).
+ * Affects launches (what 0, 1, 4, 5), plans (what 2, 3, 7) or tunings (what 6)
+ * made after the call, from any thread. */
 int gemm_debug_set(int32_t what, int64_t value);
 
 /* ---------------------------------------------------------------------------

@@ -194,7 +194,9 @@ def test_argument_errors_are_status_codes():
     with pytest.raises(g.GemmError):
         g.debug_set(0, 0)
     with pytest.raises(g.GemmError):
-        g.debug_set(7, 1)
+        g.debug_set(7, 2)
+    with pytest.raises(g.GemmError):
+        g.debug_set(8, 1)
 
 
 def test_device_calls_without_a_gpu_fail_loudly():
